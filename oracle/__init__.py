@@ -1,0 +1,147 @@
+"""fp64 CPU oracle for the paged KV-cache decode path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this package; the product path never does.  It shares
+no code with the CUDA library under ``paged_kv_cache_272_gb300/``.
+
+The arithmetic lives in ``oracle.c`` (plain loops, fp64); this module only compiles
+it with gcc and marshals numpy arrays through ctypes.  ``block_manager.py`` holds the
+plain-Python reference of the host block manager.
+
+Every bf16 tensor crosses this boundary as its raw uint16 bit pattern, so the oracle
+reads exactly the bytes the GPU reads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
+    """Compile ``oracle.c`` into a shared library with gcc (OpenMP for the
+    multi-threaded CPU baseline).  Returns the library path."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", *extra_flags, src,
+           "-o", out + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and return the ctypes handle."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_abi_version.restype = I
+    lib.oracle_kv_write.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    lib.oracle_kv_write.restype = I
+    lib.oracle_block_copy.argtypes = [P, P, P, I, I, I, I, I]
+    lib.oracle_block_copy.restype = I
+    lib.oracle_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+                                     P, I, I]
+    lib.oracle_attention.restype = I
+    lib.oracle_kv_bytes_per_token.argtypes = [I, I, I, I]
+    lib.oracle_kv_bytes_per_token.restype = ctypes.c_int64
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _u16(a) -> np.ndarray:
+    """Raw bf16 bit patterns as a contiguous uint16 array (numpy or torch input)."""
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().cpu().contiguous()
+        assert a.dtype == torch.bfloat16, a.dtype
+        return a.view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what} failed with code {rc}")
+
+
+def kv_write(k_cache: np.ndarray, v_cache: np.ndarray, k_new, v_new, slot_mapping,
+             lib=None) -> None:
+    """In place: K/V cache[slot // bs][h][slot % bs][:] = new[t][h][:] (uint16 arrays)."""
+    lib = lib or load()
+    NB, Hkv, bs, D = k_cache.shape
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = slots.shape[0]
+    assert k_new.shape == (T, Hkv, D) and v_new.shape == (T, Hkv, D)
+    _check(lib.oracle_kv_write(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                               _ptr(slots), T, NB, Hkv, D, bs), "oracle_kv_write")
+
+
+def block_copy(k_cache: np.ndarray, v_cache: np.ndarray, pairs, lib=None) -> None:
+    """In place: K/V cache[dst] = K/V cache[src] for each (src, dst) row of ``pairs``."""
+    lib = lib or load()
+    NB, Hkv, bs, D = k_cache.shape
+    pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    _check(lib.oracle_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0],
+                                 NB, Hkv, D, bs), "oracle_block_copy")
+
+
+def attention(q, k_cache, v_cache, block_tables, context_lens, scale: float, sel=None,
+              nthreads: int = 1, lib=None) -> np.ndarray:
+    """fp64 decode attention.  Returns out[S][Hq][D], or out[len(sel)][D] when ``sel``
+    lists (sequence, query head) pairs."""
+    lib = lib or load()
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    assert bt.ndim == 2 and bt.shape[0] == S and ctx.shape == (S,)
+    MB = bt.shape[1]
+    if sel is None:
+        out = np.empty((S, Hq, D), dtype=np.float64)
+        sel_p, nsel = None, 0
+    else:
+        sel_a = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((sel_a.shape[0], D), dtype=np.float64)
+        sel_p, nsel = _ptr(sel_a), sel_a.shape[0]
+    _check(lib.oracle_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
+                                _ptr(ctx), S, MB, Hq, Hkv, D, bs, NB, float(scale), sel_p, nsel,
+                                int(nthreads)), "oracle_attention")
+    return out
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, bytes_per_elem: int,
+                       lib=None) -> int:
+    """2 x layers x kv_heads x head_dim x bytes ("Inference optimization", KV cache)."""
+    lib = lib or load()
+    return int(lib.oracle_kv_bytes_per_token(layers, kv_heads, head_dim, bytes_per_elem))

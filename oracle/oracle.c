@@ -1,0 +1,203 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the paged KV-cache decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark may load this library.  It shares no code, header, table or
+ * helper with the CUDA library; it reads the same input bytes and nothing else.
+ *
+ * What it computes, and where the pages state it:
+ *
+ *  - oracle_kv_write: the new token's K/V is computed once and appended to the cache
+ *    ("Inference optimization", section "KV cache": only the N-th token's K/V is
+ *    computed and concatenated with tokens 1..N-1; section "Step 1: KV cache", the
+ *    KVCache.update method).  With a paged cache the append lands in the physical
+ *    block the block table names ("Continuous batching and PagedAttention", section 3
+ *    PagedAttention: per-request block table, logical block -> physical block).
+ *    Slot = physical_block * block_size + offset.  A negative slot is skipped.
+ *
+ *  - oracle_block_copy: copy-on-write makes a private copy of a shared block when a
+ *    request diverges ("Continuous batching and PagedAttention", section 3, the
+ *    copy-on-write sharing paragraph).  Byte copy of every KV head of the block.
+ *
+ *  - oracle_attention: Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V
+ *    ("System-level optimization: batching, PagedAttention and FlashAttention",
+ *    section 3.1, the attention equation; section 3.3 passes scale = head_dim**-0.5).
+ *    Each sequence's blocks are first gathered into a contiguous K/V (the contiguous
+ *    KVCache view of "Inference optimization", Step 1), then the textbook softmax
+ *    is taken in fp64 with the maximum subtracted.  No partitioning, no tiling.
+ *    Query head h reads KV head h / (Hq/Hkv) (grouped-query attention: 64 query
+ *    heads share 8 KV heads, "Inference optimization", exercise 3).
+ *
+ * Layouts (all row-major, element type bf16 stored as uint16 bit patterns):
+ *   q[S][Hq][D], k_cache/v_cache[NB][Hkv][block_size][D],
+ *   block_tables[S][MB] int32, context_lens[S] int32, out[S][Hq][D] fp64.
+ *
+ * Return codes: 0 ok, -1 bad sizes, -2 index out of range (nothing is read or written
+ * outside the buffers; the whole call is abandoned at the first bad index).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> fp64 is exact: the bf16 bits are the top half of an fp32. */
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_abi_version(void) { return 1; }
+
+int oracle_kv_write(uint16_t *k_cache, uint16_t *v_cache,
+                    const uint16_t *k_new, const uint16_t *v_new,
+                    const int64_t *slot_mapping, int num_tokens,
+                    int num_blocks, int num_kv_heads, int head_dim, int block_size) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return -1;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return -2;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t dst = (((size_t)block * num_kv_heads + h) * block_size + offset) * head_dim;
+            size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                k_cache[dst + d] = k_new[src + d];
+                v_cache[dst + d] = v_new[src + d];
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *pairs, int num_pairs,
+                      int num_blocks, int num_kv_heads, int head_dim, int block_size) {
+    if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return -1;
+    const size_t block_elems = (size_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < num_pairs; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return -2;
+        for (size_t e = 0; e < block_elems; ++e) {
+            k_cache[(size_t)dst * block_elems + e] = k_cache[(size_t)src * block_elems + e];
+            v_cache[(size_t)dst * block_elems + e] = v_cache[(size_t)src * block_elems + e];
+        }
+    }
+    return 0;
+}
+
+/* One (sequence, query head) output.  kc/vc are caller scratch of ctx*head_dim doubles. */
+static int attend_one(double *out, const uint16_t *q, const uint16_t *k_cache,
+                      const uint16_t *v_cache, const int32_t *block_table, int ctx,
+                      int max_blocks, int head, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, double scale,
+                      double *kc, double *vc, double *x) {
+    const int group = num_q_heads / num_kv_heads;
+    const int kv_head = head / group;
+    if (ctx > max_blocks * block_size) return -2;
+    /* Gather the logical token sequence into a contiguous K/V. */
+    for (int t = 0; t < ctx; ++t) {
+        int32_t block = block_table[t / block_size];
+        if (block < 0 || block >= num_blocks) return -2;
+        int offset = t % block_size;
+        size_t row = (((size_t)block * num_kv_heads + kv_head) * block_size + offset) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+            kc[(size_t)t * head_dim + d] = bf16_to_f64(k_cache[row + d]);
+            vc[(size_t)t * head_dim + d] = bf16_to_f64(v_cache[row + d]);
+        }
+    }
+    if (ctx == 0) {
+        for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+        return 0;
+    }
+    /* Scores x_t = scale * q . k_t */
+    double m = -INFINITY;
+    for (int t = 0; t < ctx; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < head_dim; ++d) acc += bf16_to_f64(q[d]) * kc[(size_t)t * head_dim + d];
+        x[t] = scale * acc;
+        if (x[t] > m) m = x[t];
+    }
+    /* Softmax weights and the weighted sum of V. */
+    double denom = 0.0;
+    for (int t = 0; t < ctx; ++t) {
+        x[t] = exp(x[t] - m);
+        denom += x[t];
+    }
+    for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t < ctx; ++t) acc += x[t] * vc[(size_t)t * head_dim + d];
+        out[d] = acc / denom;
+    }
+    return 0;
+}
+
+/*
+ * out[S][Hq][D] in fp64.  If `sel` is non-NULL only the `nsel` (sequence, head) pairs
+ * sel[2i], sel[2i+1] are computed, and out is then [nsel][D].  nthreads <= 0 means
+ * one thread.  Returns 0, -1 (bad sizes) or -2 (index out of range).
+ */
+int oracle_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                     const uint16_t *v_cache, const int32_t *block_tables,
+                     const int32_t *context_lens, int num_seqs, int max_blocks,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, double scale, const int32_t *sel, int nsel, int nthreads) {
+    if (num_seqs < 0 || max_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    const int npairs = sel ? nsel : num_seqs * num_q_heads;
+    int max_ctx = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (context_lens[s] < 0) return -1;
+        if (context_lens[s] > max_ctx) max_ctx = context_lens[s];
+    }
+    if (nthreads <= 0) nthreads = 1;
+    int status = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        size_t n = (size_t)(max_ctx > 0 ? max_ctx : 1);
+        double *kc = (double *)malloc(n * head_dim * sizeof(double));
+        double *vc = (double *)malloc(n * head_dim * sizeof(double));
+        double *x = (double *)malloc(n * sizeof(double));
+        int local = (kc && vc && x) ? 0 : -3;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < npairs; ++i) {
+            if (local) continue;
+            int s = sel ? sel[2 * i] : i / num_q_heads;
+            int h = sel ? sel[2 * i + 1] : i % num_q_heads;
+            if (s < 0 || s >= num_seqs || h < 0 || h >= num_q_heads) { local = -2; continue; }
+            int rc = attend_one(out + (size_t)i * head_dim,
+                                q + ((size_t)s * num_q_heads + h) * head_dim, k_cache, v_cache,
+                                block_tables + (size_t)s * max_blocks, context_lens[s], max_blocks,
+                                h, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                scale, kc, vc, x);
+            if (rc) local = rc;
+        }
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+        if (local && !status) status = local;
+        free(kc);
+        free(vc);
+        free(x);
+    }
+    return status;
+}
+
+/* KV bytes one token occupies: 2 (K and V) x layers x KV heads x head_dim x bytes per
+ * element ("Inference optimization", section "KV cache", the memory formula). */
+int64_t oracle_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int bytes_per_elem) {
+    return (int64_t)2 * layers * kv_heads * head_dim * bytes_per_elem;
+}

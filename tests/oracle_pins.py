@@ -1,0 +1,395 @@
+"""Pins of the fp64 oracle to facts outside itself.
+
+Each ``pin_*`` takes a loaded oracle library and raises AssertionError when the oracle
+disagrees with a value the pages print, a closed form, a library routine, an
+invariant of the method, or brute force on a tiny input.  ``test_oracle_pins.py`` runs
+them on the real oracle; ``test_oracle_mutants.py`` plants plausible mistakes in the
+oracle's C source and checks that every mistake trips at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from oracle.block_manager import BlockManager
+from paged_kv_cache_272_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+BS = 16
+
+
+def _rows(path):
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            data, cite = line.split("|", 1)
+            yield data.split(), cite.strip()
+
+
+def bf16(a) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def host_caches(w):
+    """uint16 copies of the workload's caches (the oracle's working state)."""
+    k = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    v = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    return k, v
+
+
+def run_step(w, lib):
+    """Oracle decode step: copy-on-write, write the new token, attend.  fp64 out."""
+    k, v = host_caches(w)
+    if w.cow_pairs.size:
+        oracle.block_copy(k, v, w.cow_pairs, lib=lib)
+    if w.slot_mapping.size:
+        oracle.kv_write(k, v, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    return oracle.attention(w.q, k, v, w.block_tables, w.context_lens, w.scale, lib=lib), k, v
+
+
+def gather(k, table, ctx, kv_head):
+    """Contiguous [ctx][D] rows of one KV head (fp64), read through the block table."""
+    rows = []
+    for t in range(ctx):
+        rows.append(k[table[t // BS], kv_head, t % BS])
+    u = np.stack(rows).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().double().numpy()
+
+
+# -------------------------------------------------------------------------------------
+# Values printed on the pages
+# -------------------------------------------------------------------------------------
+def pin_kv_bytes_golden(lib):
+    n = 0
+    for (L, H, D, B, T, expect), cite in _rows(os.path.join(GOLDEN, "kv_bytes.txt")):
+        got = oracle.kv_bytes_per_token(int(L), int(H), int(D), int(B), lib=lib) * int(T)
+        assert got == int(expect), (got, expect, cite)
+        n += 1
+    for (L, H, D, B, T, div, printed, tol), cite in _rows(
+            os.path.join(GOLDEN, "kv_bytes_rounded.txt")):
+        got = oracle.kv_bytes_per_token(int(L), int(H), int(D), int(B), lib=lib) * int(T)
+        assert abs(got / float(div) - float(printed)) <= float(tol), (got, printed, cite)
+        n += 1
+    assert n >= 6
+
+
+def pin_gqa_reduction(lib):
+    # Inference optimization, exercise 3: 64 query heads over 8 KV heads -> 8x less KV.
+    mha = oracle.kv_bytes_per_token(80, 64, 128, 2, lib=lib)
+    gqa = oracle.kv_bytes_per_token(80, 8, 128, 2, lib=lib)
+    assert mha == 8 * gqa
+
+
+def pin_block_counts():
+    for (tokens, blocks), cite in _rows(os.path.join(GOLDEN, "block_counts.txt")):
+        bm = BlockManager(64, BS)
+        bm.add_seq(0)
+        bm.append_tokens(0, int(tokens))
+        assert len(bm.block_table(0)) == int(blocks), cite
+        assert 0 <= bm.internal_waste(0) < BS
+
+
+# -------------------------------------------------------------------------------------
+# Closed forms and special cases
+# -------------------------------------------------------------------------------------
+def pin_ctx1_returns_v(lib):
+    """One token: its softmax weight is exp(0)/exp(0) = 1, so the output is V exactly."""
+    w = workloads.build("ctx1", [1, 1, 1], 4, 2, 64, seed=11)
+    out, k, v = run_step(w, lib)
+    for s in range(3):
+        for h in range(4):
+            want = to_f64(w.v_new[s, h // 2])
+            assert np.array_equal(out[s, h], want), (s, h)
+
+
+def pin_uniform_scores_mean(lib):
+    """q = 0 makes every score equal, so the output is the plain mean of V."""
+    w = workloads.build("uniform", [5, 16, 33, 70], 4, 2, 64, seed=12)
+    w.q.zero_()
+    out, k, v = run_step(w, lib)
+    for s in range(w.num_seqs):
+        for h in range(4):
+            vc = gather(v, w.block_tables[s], int(w.context_lens[s]), h // 2)
+            np.testing.assert_allclose(out[s, h], vc.mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def pin_equal_keys_mean(lib):
+    """All keys of a sequence equal: scores equal again, output = mean of V."""
+    w = workloads.build("eqk", [9, 40], 2, 1, 64, seed=13)
+    k, v = host_caches(w)
+    oracle.kv_write(k, v, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    for s in range(2):
+        n = int(w.context_lens[s])
+        row = k[w.block_tables[s][0], 0, 0].copy()
+        for t in range(n):
+            k[w.block_tables[s][t // BS], 0, t % BS] = row
+        out = oracle.attention(w.q, k, v, w.block_tables, w.context_lens, w.scale, lib=lib)
+        vc = gather(v, w.block_tables[s], n, 0)
+        for h in range(2):
+            np.testing.assert_allclose(out[s, h], vc.mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def pin_two_token_closed_form(lib):
+    """Two tokens with scores a*scale and 0: weights are the logistic function of a*scale.
+
+    Two KV heads with different keys and four query heads pin the consecutive
+    query-head grouping (head h reads KV head h // 2)."""
+    D, Hq, Hkv = 64, 4, 2
+    w = workloads.build("closed", [2], Hq, Hkv, D, seed=14, poison=False)
+    k, v = host_caches(w)
+    oracle.kv_write(k, v, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    b = w.block_tables[0][0]
+    e = np.zeros(D, np.float32)
+    one = bf16(e).view(torch.int16).numpy().view(np.uint16)  # zeros
+    k[b, :, 0:2] = one
+    # KV head 0: k_0 = e_3, KV head 1: k_0 = e_7; k_1 = 0 for both
+    for g, axis in ((0, 3), (1, 7)):
+        e = np.zeros(D, np.float32)
+        e[axis] = 1.0
+        k[b, g, 0] = bf16(e).view(torch.int16).numpy().view(np.uint16)
+    a = np.array([2.0, -3.0, 5.0, 0.5], np.float32)
+    qv = np.zeros((1, Hq, D), np.float32)
+    for h in range(Hq):
+        qv[0, h, 3] = a[h]          # only KV head 0's key sees this
+        qv[0, h, 7] = -a[h] / 2     # only KV head 1's key sees this
+    q = bf16(qv)
+    out = oracle.attention(q, k, v, w.block_tables, w.context_lens, w.scale, lib=lib)
+    for h in range(Hq):
+        g = h // 2
+        x0 = (a[h] if g == 0 else -a[h] / 2) * w.scale
+        w0 = 1.0 / (1.0 + math.exp(-x0))
+        v0 = gather(v, w.block_tables[0], 2, g)
+        want = w0 * v0[0] + (1.0 - w0) * v0[1]
+        np.testing.assert_allclose(out[0, h], want, rtol=1e-13, atol=1e-15)
+
+
+def pin_ctx_zero(lib):
+    w = workloads.build("zero", [3, 3], 2, 1, 64, seed=15)
+    k, v = host_caches(w)
+    oracle.kv_write(k, v, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    ctx = w.context_lens.copy()
+    ctx[1] = 0
+    out = oracle.attention(w.q, k, v, w.block_tables, ctx, w.scale, lib=lib)
+    assert np.all(out[1] == 0.0)
+    assert np.all(np.isfinite(out[0]))
+
+
+# -------------------------------------------------------------------------------------
+# Library routine and brute force
+# -------------------------------------------------------------------------------------
+class ContiguousKVCache:
+    """The contiguous cache of "Inference optimization", Step 1: per layer and head a
+    [max_seq][D] array; update() appends new rows along the sequence axis."""
+
+    def __init__(self, num_layers, num_heads, head_dim, max_seq_len):
+        self.k = np.zeros((num_layers, num_heads, max_seq_len, head_dim), np.float64)
+        self.v = np.zeros_like(self.k)
+        self.seq_len = 0
+
+    def update(self, layer, new_k, new_v):
+        n = new_k.shape[1]
+        end = self.seq_len + n
+        self.k[layer, :, self.seq_len:end] = new_k
+        self.v[layer, :, self.seq_len:end] = new_v
+        self.seq_len = end
+        return self.k[layer, :, :end], self.v[layer, :, :end]
+
+
+def contiguous_from_paged(k, v, table, ctx, Hkv, D, chunk=7):
+    """Feed a sequence's tokens, in logical order and in chunks, through the
+    contiguous cache."""
+    cache = ContiguousKVCache(1, Hkv, D, ctx)
+    kk = vv = None
+    for t0 in range(0, ctx, chunk):
+        t1 = min(ctx, t0 + chunk)
+        nk = np.stack([gather(k, table, t1, g)[t0:t1] for g in range(Hkv)])
+        nv = np.stack([gather(v, table, t1, g)[t0:t1] for g in range(Hkv)])
+        kk, vv = cache.update(0, nk, nv)
+    return kk, vv
+
+
+def pin_sdpa_contiguous(lib, cfg=1, ctx_override=None, Hq=None, Hkv=None, seed=16):
+    """Paged oracle == torch's fp64 scaled_dot_product_attention over the contiguous
+    cache (the library routine of "System-level optimization", section 3.3)."""
+    if ctx_override is None:
+        w = workloads.make_config(cfg)
+    else:
+        w = workloads.build("sdpa", ctx_override, Hq, Hkv, 64, seed=seed)
+    out, k, v = run_step(w, lib)
+    G = w.num_q_heads // w.num_kv_heads
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        kk, vv = contiguous_from_paged(k, v, w.block_tables[s], n, w.num_kv_heads,
+                                       w.head_dim)
+        qt = torch.from_numpy(to_f64(w.q[s])).view(1, w.num_q_heads, 1, w.head_dim)
+        kt = torch.from_numpy(kk).repeat_interleave(G, dim=0).unsqueeze(0)
+        vt = torch.from_numpy(vv).repeat_interleave(G, dim=0).unsqueeze(0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=w.scale)
+        np.testing.assert_allclose(out[s], ref[0, :, 0].numpy(), rtol=1e-11, atol=1e-12)
+
+
+def pin_brute_force_tiny(lib):
+    """Configuration 1 recomputed with explicit Python loops and math.exp."""
+    w = workloads.make_config(1)
+    out, k, v = run_step(w, lib)
+    q = to_f64(w.q)
+    G = w.num_q_heads // w.num_kv_heads
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        for h in range(w.num_q_heads):
+            kc = gather(k, w.block_tables[s], n, h // G)
+            vc = gather(v, w.block_tables[s], n, h // G)
+            xs = [w.scale * sum(q[s, h, d] * kc[t, d] for d in range(w.head_dim))
+                  for t in range(n)]
+            mx = max(xs)
+            ws = [math.exp(x - mx) for x in xs]
+            tot = sum(ws)
+            for d in range(w.head_dim):
+                want = sum(ws[t] * vc[t, d] for t in range(n)) / tot
+                assert abs(out[s, h, d] - want) <= 1e-12 * (1 + abs(want)), (s, h, d)
+
+
+def pin_large_magnitude(lib):
+    """q scaled by 30: scores reach hundreds; the result stays finite and equals the
+    library routine."""
+    w = workloads.build("big", [17, 64, 200], 4, 2, 64, seed=17)
+    w.q.mul_(30)
+    out, k, v = run_step(w, lib)
+    assert np.all(np.isfinite(out))
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        for h in range(4):
+            kc = gather(k, w.block_tables[s], n, h // 2)
+            vc = gather(v, w.block_tables[s], n, h // 2)
+            x = torch.from_numpy(to_f64(w.q[s, h]) @ kc.T * w.scale)
+            want = torch.softmax(x, 0).numpy() @ vc
+            np.testing.assert_allclose(out[s, h], want, rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------------------------------------
+# Invariants of the paged layout
+# -------------------------------------------------------------------------------------
+def pin_permutation_invariance(lib):
+    """Relabelling the physical blocks (and the tables with them) changes nothing:
+    the table alone decides which bytes a sequence sees."""
+    w = workloads.build("perm", [3, 16, 17, 50, 90], 4, 2, 64, seed=18)
+    out, k, v = run_step(w, lib)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(w.num_blocks)
+    k2 = np.empty_like(k)
+    v2 = np.empty_like(v)
+    k2[perm] = k
+    v2[perm] = v
+    bt = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    out2 = oracle.attention(w.q, k2, v2, bt, w.context_lens, w.scale, lib=lib)
+    assert np.array_equal(out, out2)
+
+
+def pin_gqa_equals_mha(lib):
+    """GQA equals MHA whose KV heads are the GQA heads repeated G times (consecutive
+    grouping)."""
+    G = 4
+    w = workloads.build("gqa", [5, 31, 47], 8, 2, 64, seed=19)
+    out, k, v = run_step(w, lib)
+    km = np.ascontiguousarray(np.repeat(k, G, axis=1))
+    vm = np.ascontiguousarray(np.repeat(v, G, axis=1))
+    out2 = oracle.attention(w.q, km, vm, w.block_tables, w.context_lens, w.scale, lib=lib)
+    assert np.array_equal(out, out2)
+
+
+def pin_shared_prefix_equals_private(lib):
+    """Sequences that share prefix blocks give the same result as if each had a
+    private copy of those blocks."""
+    w = workloads.build("prefix", [40, 33, 50, 65], 4, 2, 64, seed=20,
+                        shared_prefix_tokens=32, cow_last_block=True, free_fraction=3.0)
+    out, k, v = run_step(w, lib)
+    free = sorted(set(range(w.num_blocks)) - set(w.block_tables[w.block_tables >= 0].tolist())
+                  - set(w.cow_pairs[:, 0].tolist()))
+    bt = w.block_tables.copy()
+    it = iter(free)
+    for s in range(1, w.num_seqs):
+        for j in range(2):
+            nb = next(it)
+            k[nb] = k[bt[s, j]]
+            v[nb] = v[bt[s, j]]
+            bt[s, j] = nb
+    assert len(set(bt[:, 0].tolist())) == w.num_seqs
+    out2 = oracle.attention(w.q, k, v, bt, w.context_lens, w.scale, lib=lib)
+    assert np.array_equal(out, out2)
+
+
+def pin_write_matches_kvcache_update(lib):
+    """Appending tokens one by one through slots reproduces the contiguous cache's
+    update() sequence when read back through the block table."""
+    Hkv, D, n = 2, 64, 37
+    bm = BlockManager(12, BS, free_order=np.random.default_rng(3).permutation(12))
+    bm.add_seq(0)
+    k = np.full((12, Hkv, BS, D), workloads.NAN_BF16, np.uint16)
+    v = k.copy()
+    gen = torch.Generator().manual_seed(4)
+    newk = torch.randn(n, Hkv, D, generator=gen).to(torch.bfloat16)
+    newv = torch.randn(n, Hkv, D, generator=gen).to(torch.bfloat16)
+    cache = ContiguousKVCache(1, Hkv, D, n)
+    for t in range(n):
+        slot, cow = bm.append_slot(0)
+        assert cow is None
+        oracle.kv_write(k, v, newk[t:t + 1], newv[t:t + 1], [slot], lib=lib)
+        kk, vv = cache.update(0, to_f64(newk[t:t + 1]).transpose(1, 0, 2),
+                              to_f64(newv[t:t + 1]).transpose(1, 0, 2))
+    table = bm.block_table(0)
+    for g in range(Hkv):
+        assert np.array_equal(gather(k, table, n, g), kk[g])
+        assert np.array_equal(gather(v, table, n, g), vv[g])
+
+
+def pin_write_bytes(lib):
+    """Only the addressed rows change; a negative slot is skipped."""
+    NB, Hkv, D = 6, 2, 64
+    rng = np.random.default_rng(21)
+    k = rng.integers(0, 2 ** 16, size=(NB, Hkv, BS, D), dtype=np.uint16)
+    v = rng.integers(0, 2 ** 16, size=(NB, Hkv, BS, D), dtype=np.uint16)
+    k0, v0 = k.copy(), v.copy()
+    newk = rng.integers(0, 2 ** 16, size=(3, Hkv, D), dtype=np.uint16)
+    newv = rng.integers(0, 2 ** 16, size=(3, Hkv, D), dtype=np.uint16)
+    slots = [5 * BS + 15, -1, 0 * BS + 3]
+    oracle.kv_write(k, v, newk, newv, slots, lib=lib)
+    k0[5, :, 15] = newk[0]
+    v0[5, :, 15] = newv[0]
+    k0[0, :, 3] = newk[2]
+    v0[0, :, 3] = newv[2]
+    assert np.array_equal(k, k0) and np.array_equal(v, v0)
+
+
+def pin_copy_bytes(lib):
+    """Copy-on-write: the destination block equals the source in every KV head, for K
+    and V; nothing else changes."""
+    NB, Hkv, D = 8, 3, 64
+    rng = np.random.default_rng(22)
+    k = rng.integers(0, 2 ** 16, size=(NB, Hkv, BS, D), dtype=np.uint16)
+    v = rng.integers(0, 2 ** 16, size=(NB, Hkv, BS, D), dtype=np.uint16)
+    k0, v0 = k.copy(), v.copy()
+    pairs = [(1, 6), (4, 2), (7, 0)]
+    oracle.block_copy(k, v, pairs, lib=lib)
+    for s, d in pairs:
+        k0[d] = k0[s]
+        v0[d] = v0[s]
+    assert np.array_equal(k, k0) and np.array_equal(v, v0)
+
+
+ALL_PINS = [
+    pin_kv_bytes_golden, pin_gqa_reduction, pin_ctx1_returns_v, pin_uniform_scores_mean,
+    pin_equal_keys_mean, pin_two_token_closed_form, pin_ctx_zero, pin_sdpa_contiguous,
+    pin_brute_force_tiny, pin_large_magnitude, pin_permutation_invariance, pin_gqa_equals_mha,
+    pin_shared_prefix_equals_private, pin_write_matches_kvcache_update, pin_write_bytes,
+    pin_copy_bytes,
+]
