@@ -1,0 +1,409 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = copy-on-write block copy (when the workload has pairs) + paged KV write of
+the step's new tokens + paged decode attention (plan, split-K partitions, LSE merge),
+all through the C ABI of libpagedkv.so on one stream.
+
+Prints ONE JSON line.  ``value`` is KV-read GB/s of the whole step (algorithmic bytes:
+every context token's K and V row of every KV head, read once) with inputs resident in
+HBM; ``e2e`` is the same metric with the step's inputs copied from pinned host memory
+and the output copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+                    [--variant auto|fma|mma] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_272_gb300 import workloads  # noqa: E402
+
+DEFAULT_CONFIG = 2
+METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); seq-steps/sec/layer"
+L2_BYTES = 129 * 1024 * 1024
+ATTN_SOURCES = ["paged_kv_cache_272_gb300/csrc/attention.cu",
+                "paged_kv_cache_272_gb300/csrc/attention_mma.cu",
+                "paged_kv_cache_272_gb300/csrc/attention.cuh",
+                "paged_kv_cache_272_gb300/csrc/pkv_common.cuh"]
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def recorded_traffic(workload: str, variant: str):
+    """DRAM bytes per attention call from the committed ncu summary, only if it was
+    taken on the current attention sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(f"{workload}/{variant}")
+    if not e or e.get("source_hash") != attn_source_hash():
+        return None
+    return e.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def setup_dist(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------------------------------
+# CPU oracle baseline (a bounded sample of the same workload)
+# -------------------------------------------------------------------------------------
+def oracle_sample_step(w, n_seqs: int, nthreads: int, k_host, v_host):
+    import oracle
+    sub_bt = np.ascontiguousarray(w.block_tables[:n_seqs])
+    sub_ctx = np.ascontiguousarray(w.context_lens[:n_seqs])
+    q = w.q[:n_seqs].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.attention(q, k_host, v_host, sub_bt, sub_ctx, w.scale, nthreads=nthreads)
+    return time.perf_counter() - t0, int(sub_ctx.astype(np.int64).sum())
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """Time the oracle, as it stands, on all host cores over the first sequences of the
+    workload, growing the sample until it takes about budget_s / 3, then once more."""
+    nthreads = os.cpu_count() or 1
+    k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    v_host = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    n = min(w.num_seqs, 2)
+    while True:
+        dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
+        if dt > budget_s / 3 or n >= w.num_seqs:
+            break
+        n = min(w.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 3) / max(dt, 1e-3)))))
+    dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
+    kv_bytes = tok * 2 * w.num_kv_heads * w.head_dim * 2
+    return {"value": kv_bytes / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"first {n} of {w.num_seqs} sequences, all {w.num_q_heads} query heads, "
+                      f"{tok} context tokens; fp64 C oracle, OpenMP over (sequence, head)",
+            "seconds": dt, "seq_steps_per_s_per_layer": n / dt}
+
+
+# -------------------------------------------------------------------------------------
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workloads.make_config(args.config, device="cpu" if args.config == 1 else "cuda"
+                              if torch.cuda.is_available() else "cpu")
+    nthreads = os.cpu_count() or 1
+    k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    v_host = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    # size one step to about 2 s of oracle work
+    n = min(w.num_seqs, 2)
+    while True:
+        dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
+        if dt > 0.7 or n >= w.num_seqs:
+            break
+        n = min(w.num_seqs, max(n + 1, int(n * min(8.0, 0.7 / max(dt, 1e-3)))))
+    for _ in range(args.warmup):
+        oracle_sample_step(w, n, nthreads, k_host, v_host)
+    tot_t, tot_tok = 0.0, 0
+    for _ in range(args.steps):
+        dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
+        tot_t += dt
+        tot_tok += tok
+    kv = tot_tok * 2 * w.num_kv_heads * w.head_dim * 2
+    value = kv / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_seqs": n, "num_seqs": w.num_seqs},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"first {n} of {w.num_seqs} sequences per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "world_size": world,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    from paged_kv_cache_272_gb300 import ops
+    world, rank, local = setup_dist(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    variant = {"auto": ops.PKV_ATTN_AUTO, "fma": ops.PKV_ATTN_FMA,
+               "mma": ops.PKV_ATTN_MMA}[args.variant]
+    ops.set_attention_variant(variant)
+
+    w = workloads.make_config(args.config, device="cuda")
+    S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    k = w.k_cache.to(dev).contiguous()
+    v = w.v_cache.to(dev).contiguous()
+    q = w.q.to(dev).contiguous()
+    k_new, v_new = w.k_new.to(dev).contiguous(), w.v_new.to(dev).contiguous()
+    slots = torch.as_tensor(w.slot_mapping, dtype=torch.int64, device=dev)
+    pairs = torch.as_tensor(w.cow_pairs.reshape(-1, 2), dtype=torch.int32, device=dev)
+    bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev)
+    ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev)
+    out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device=dev)
+    P = w.partition_size
+    mcl = w.max_context_len
+    ws = ops.alloc_workspace(S, Hq, D, mcl, P, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes = workloads.kv_read_bytes(w)
+    max_parts = (mcl + P - 1) // P
+    launches_per_step = (1 if pairs.numel() else 0) + 1 + 2 + (1 if max_parts > 1 else 0)
+    working_set = kv_bytes + q.numel() * 2 * 2
+    flush = working_set < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def step():
+        if pairs.numel():
+            ops.paged_block_copy(k, v, pairs, err_flag=err, stream=stream)
+        ops.paged_kv_write(k_new, v_new, slots, k, v, err_flag=err, stream=stream)
+        ops.paged_attention_decode(out, q, k, v, bt, ctx, w.scale, mcl, ws, P, err_flag=err,
+                                   stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()} during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t_end = time.perf_counter() + 0.8          # bring clocks to their loaded state
+        while time.perf_counter() < t_end:
+            step()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            if flush:
+                scratch.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            if pairs.numel():
+                ops.paged_block_copy(k, v, pairs, err_flag=err, stream=stream)
+            ops.paged_kv_write(k_new, v_new, slots, k, v, err_flag=err, stream=stream)
+            e1.record(stream)
+            ops.paged_attention_decode(out, q, k, v, bt, ctx, w.scale, mcl, ws, P, err_flag=err,
+                                       stream=stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        t_end = time.perf_counter() + 0.4
+        while time.perf_counter() < t_end:
+            step()
+            torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    attn_avg_ms = max_over_ranks(sum(attn_ms) / len(attn_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # ---- end to end through the public API, host buffers ------------------------------
+    h = {name: t.cpu().pin_memory() for name, t in
+         (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("pairs", pairs),
+          ("bt", bt), ("ctx", ctx))}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dkn, dvn = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    dsl, dpr = torch.empty_like(slots), torch.empty_like(pairs)
+    dbt, dctx = torch.empty_like(bt), torch.empty_like(ctx)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        dq.copy_(h["q"], non_blocking=True)
+        dkn.copy_(h["k_new"], non_blocking=True)
+        dvn.copy_(h["v_new"], non_blocking=True)
+        dsl.copy_(h["slots"], non_blocking=True)
+        dbt.copy_(h["bt"], non_blocking=True)
+        dctx.copy_(h["ctx"], non_blocking=True)
+        if dpr.numel():
+            dpr.copy_(h["pairs"], non_blocking=True)
+            ops.paged_block_copy(k, v, dpr, err_flag=err, stream=stream)
+        ops.paged_kv_write(dkn, dvn, dsl, k, v, err_flag=err, stream=stream)
+        ops.paged_attention_decode(out, dq, k, v, dbt, dctx, w.scale, mcl, ws, P, err_flag=err,
+                                   stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        if flush:
+            scratch.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()  # the host has the step's output
+        e2e_ms += a.elapsed_time(b)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_value = world * kv_bytes * args.steps / (e2e_ms / 1e3) / 1e9
+
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()}")
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = kv_bytes / (attn_avg_ms / 1e3) / 1e9
+    vname = {0: "auto", 1: "fma", 2: "mma"}[variant]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "head_dim": D, "block_size": w.block_size, "partition_size": P,
+            "num_blocks": w.num_blocks, "mean_context": float(w.context_lens.mean()),
+            "max_context": mcl, "kv_bytes_per_step": kv_bytes,
+            "cow_pairs_per_step": int(w.cow_pairs.shape[0]),
+            "new_tokens_per_step": int(w.slot_mapping.shape[0]),
+            "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
+                   "inputs larger than L2 (KV read per step >> 129 MB)"),
+            "attention_variant": vname, "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_hbm_peak": 100.0 * value / peak,
+        "seq_steps_per_s_per_layer": world * S / (ms_per_step / 1e3),
+        "attention_ms": attn_avg_ms,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(w.name, vname),
+                     "kernel": "paged_attention_decode (plan + partition + merge kernels)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

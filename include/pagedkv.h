@@ -1,0 +1,187 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the paged KV-cache decode path on one GB300.
+ *
+ * The operations follow the statement of the problem on the pages:
+ *  - the KV cache is cut into fixed-size blocks of 16 tokens handed out from one pool,
+ *    and each request's block table maps its logical block i to a physical block
+ *    ("Continuous batching and PagedAttention", section 3 PagedAttention;
+ *    "System-level optimization: batching, PagedAttention and FlashAttention",
+ *    section 2.3 PagedAttention solution);
+ *  - each decode step computes only the new token's K/V and appends it to the cache
+ *    ("Inference optimization", section "KV cache");
+ *  - shared blocks are copied when a request diverges (copy-on-write, "Continuous
+ *    batching and PagedAttention", section 3, copy-on-write sharing);
+ *  - attention is softmax(q K^T * scale) V with scale = head_dim^-1/2
+ *    ("System-level optimization", sections 3.1 and 3.3).
+ *
+ * Conventions shared by every call
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major:
+ *      q, out              [num_seqs][num_q_heads][head_dim]
+ *      k_cache, v_cache    [num_blocks][num_kv_heads][block_size][head_dim]
+ *      k_new, v_new        [num_tokens][num_kv_heads][head_dim]
+ *    int32 block_tables [num_seqs][max_blocks_per_seq], int32 context_lens [num_seqs],
+ *    int64 slot_mapping [num_tokens], int32 block_pairs [num_pairs][2] = (src, dst).
+ *  - Every pointer argument of the GPU calls is a device pointer owned by the caller.
+ *    The library never allocates, frees or synchronises on these calls; work is
+ *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - context_lens counts every token attended, the one written this step included.
+ *  - Token t of sequence s lives in block block_tables[s][t / 16] at offset t % 16;
+ *    slot = physical_block * 16 + offset.
+ *  - Return value: PKV_OK, or a negative PKV_ERR_* code for arguments rejected on the
+ *    host (nothing is enqueued then), or PKV_ERR_CUDA if a launch failed.
+ *  - err_flag (device int32, caller-owned, may be NULL): a kernel that meets a bad
+ *    index (block id outside [0, num_blocks), slot outside the pool, context longer
+ *    than the block table or than max_context_len) ORs a PKV_DEV_* bit into it and
+ *    skips that access.  No kernel traps or waits without a bound.
+ *  - head_dim must be 64 or 128; block_size must be 16; q, out, the caches and the
+ *    new K/V must be 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_ERR_NULL (-1)        /* a required pointer is NULL                        */
+#define PKV_ERR_SHAPE (-2)       /* a size is out of range or head_dim unsupported    */
+#define PKV_ERR_BLOCK_SIZE (-3)  /* block_size is not 16                              */
+#define PKV_ERR_ALIGN (-4)       /* a bf16 buffer is not 16-byte aligned              */
+#define PKV_ERR_WORKSPACE (-5)   /* workspace smaller than the size query returns     */
+#define PKV_ERR_CUDA (-6)        /* a CUDA runtime call or kernel launch failed       */
+#define PKV_ERR_OOM (-10)        /* block pool: no free block                         */
+#define PKV_ERR_UNKNOWN_SEQ (-11)/* block pool: no such sequence                      */
+#define PKV_ERR_DUP_SEQ (-12)    /* block pool: sequence id already in use            */
+#define PKV_ERR_REFCOUNT (-13)   /* block pool: refcount underflow (corrupt state)    */
+#define PKV_ERR_ARG (-14)        /* block pool: bad argument                          */
+
+#define PKV_DEV_BAD_BLOCK 1      /* block table entry or copy pair outside the pool   */
+#define PKV_DEV_BAD_SLOT 2       /* slot_mapping entry >= num_blocks * 16             */
+#define PKV_DEV_BAD_CONTEXT 4    /* context_len < 0 or beyond table / max_context_len */
+#define PKV_DEV_TIMEOUT 8        /* a bounded wait inside a kernel gave up            */
+
+/* Library ABI version (incremented on any signature change). */
+int paged_kv_version(void);
+
+/* Human-readable text of a PKV_ERR_* code. Never NULL; static storage. */
+const char *paged_kv_strerror(int code);
+
+/*
+ * paged_kv_write -- append this step's new tokens to the paged cache.
+ * For t < num_tokens and every KV head h:
+ *   k_cache[slot/16][h][slot%16][:] = k_new[t][h][:]   (same for v), slot = slot_mapping[t].
+ * A negative slot is skipped (padding).  Bit-exact byte movement.  Two tokens with the
+ * same slot in one call race (the caller must not do that).
+ * Source: "Inference optimization", section "KV cache" (only the new token's K/V is
+ * computed and appended) and section "Step 1: KV cache" (the update method).
+ */
+int paged_kv_write(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
+                   int num_tokens, uint16_t *k_cache, uint16_t *v_cache, int num_blocks,
+                   int num_kv_heads, int head_dim, int block_size, int32_t *err_flag,
+                   void *stream);
+
+/*
+ * paged_block_copy -- copy-on-write of whole blocks.
+ * For every pair i: k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], all KV
+ * heads, bit-exact.  The dsts of one call must be distinct and no dst may be the src of
+ * another pair in the same call (the copies run concurrently).
+ * Source: "Continuous batching and PagedAttention", section 3 PagedAttention, the
+ * copy-on-write paragraph (a shared block is copied only when a request diverges).
+ */
+int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_pairs,
+                     int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                     int block_size, int32_t *err_flag, void *stream);
+
+/*
+ * Bytes of device workspace paged_attention_decode needs for these sizes.
+ * partition_size <= 0 selects the default (512 tokens).
+ */
+size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                      int max_context_len, int partition_size);
+
+/*
+ * paged_attention_decode -- one query token per sequence attends over its paged cache.
+ * For every sequence s and query head h, with n = context_lens[s], g = h / (Hq/Hkv):
+ *   x_t = scale * q[s][h] . K_s[t][g],   t < n, where K_s[t] is read through block_tables
+ *   out[s][h] = sum_t exp(x_t - max x) V_s[t][g] / sum_t exp(x_t - max x)
+ * computed in fp32 from bf16 inputs and rounded to bf16.  n == 0 gives zeros.
+ * Long contexts are split into partitions of partition_size tokens (a multiple of 16;
+ * <= 0 selects 512) whose partial results are merged with a log-sum-exp reduction.
+ * max_context_len is a host-side upper bound of context_lens (it sizes the workspace);
+ * a context above it sets PKV_DEV_BAD_CONTEXT and that sequence's output is zeros.
+ * workspace (device, >= paged_attention_workspace_size bytes, 256-byte aligned) is
+ * scratch owned by the caller; its contents need no initialisation and are
+ * overwritten.  Calls that share a workspace must be ordered on one stream.
+ * Source: "System-level optimization", section 3.1 (attention equation) and 3.3
+ * (scale); "Continuous batching and PagedAttention", section 3 (block tables).
+ */
+int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int partition_size, int max_context_len,
+                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                           void *stream);
+
+/*
+ * Attention kernel selection, process-wide (for measurement; the default is AUTO).
+ * Returns the previous value, or PKV_ERR_ARG for an unknown value.
+ */
+#define PKV_ATTN_AUTO 0
+#define PKV_ATTN_FMA 1   /* CUDA-core dot products and accumulation */
+#define PKV_ATTN_MMA 2   /* tensor-core tiles for the query-group contraction */
+int paged_attention_set_variant(int variant);
+
+/* ------------------------------------------------------------------------------------
+ * Host block manager ("Continuous batching and PagedAttention", section 3; "System-level
+ * optimization", section 2.3): one pool of fixed-size blocks, a block table per
+ * sequence, reference counts, fork for shared prefixes / parallel sampling, and
+ * copy-on-write when a sequence appends into a block it shares.
+ * Allocation order: the free pool is a stack that starts as free_order (first element
+ * handed out first; NULL = 0, 1, 2, ...); a freed block goes on top.  pkv_seq_free
+ * releases a sequence's blocks from its last logical block to its first.
+ * Every failing call leaves the pool unchanged.  Not thread-safe: one pool per thread.
+ * ------------------------------------------------------------------------------------ */
+typedef struct pkv_pool pkv_pool;
+
+int pkv_pool_create(int num_blocks, int block_size, const int32_t *free_order, pkv_pool **out);
+void pkv_pool_destroy(pkv_pool *pool);
+int pkv_pool_num_free(const pkv_pool *pool);
+int pkv_block_refcount(const pkv_pool *pool, int block);  /* <0 on a bad block id */
+
+int pkv_seq_add(pkv_pool *pool, int64_t seq);
+int pkv_seq_fork(pkv_pool *pool, int64_t parent, int64_t child);
+int pkv_seq_free(pkv_pool *pool, int64_t seq);
+int pkv_seq_num_tokens(const pkv_pool *pool, int64_t seq, int *num_tokens);
+int pkv_seq_num_blocks(const pkv_pool *pool, int64_t seq, int *num_blocks);
+
+/* Reserve the slot of the sequence's next token.  *cow_src/*cow_dst = -1 unless the
+ * token falls in a shared block, in which case the block was replaced by a fresh one
+ * and the caller must copy cow_src -> cow_dst (paged_block_copy) before writing. */
+int pkv_seq_append_slot(pkv_pool *pool, int64_t seq, int64_t *slot, int32_t *cow_src,
+                        int32_t *cow_dst);
+
+/* `count` append_slot calls, all or nothing.  slots[count] and cow_pairs[2*count] may
+ * be NULL; *num_cow (may be NULL) receives the number of pairs written. */
+int pkv_seq_append_tokens(pkv_pool *pool, int64_t seq, int count, int64_t *slots,
+                          int32_t *cow_pairs, int *num_cow);
+
+/* One decode step: one append_slot per listed sequence, in order, all or nothing.
+ * slot_mapping[n]; cow_pairs[2*n] receives the copies to make; *num_cow their count. */
+int pkv_pool_step(pkv_pool *pool, const int64_t *seqs, int n, int64_t *slot_mapping,
+                  int32_t *cow_pairs, int *num_cow);
+
+/* Block tables [n][max_blocks] (unused entries = pad) and context lengths of `seqs`. */
+int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_blocks,
+                    int32_t pad, int32_t *block_tables, int32_t *context_lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

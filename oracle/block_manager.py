@@ -121,6 +121,22 @@ class BlockManager:
             raise
         return slots, pairs
 
+    def step(self, seqs):
+        """One decode step: append_slot for each listed sequence in order, all or
+        nothing.  Returns (slot_mapping, cow_pairs)."""
+        snapshot = self._snapshot()
+        slots, pairs = [], []
+        try:
+            for s in seqs:
+                slot, cow = self.append_slot(s)
+                slots.append(slot)
+                if cow is not None:
+                    pairs.append(cow)
+        except BlockManagerError:
+            self._restore(snapshot)
+            raise
+        return slots, pairs
+
     def fork(self, parent: int, child: int) -> None:
         """The child shares every block of the parent (refcount + 1 each)."""
         table = self._need(parent)

@@ -1,0 +1,486 @@
+// Paged decode attention: plan, split-K partition kernel (CUDA-core variant), LSE merge,
+// and the C entry points.
+//
+// What is computed ("System-level optimization: batching, PagedAttention and
+// FlashAttention", section 3.1, the attention equation, and section 3.3, scale =
+// head_dim^-1/2): for each sequence s and query head h,
+//   out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s
+// over the context_lens[s] tokens that block_tables[s] reaches ("Continuous batching
+// and PagedAttention", section 3: logical block i -> physical block; 16-token blocks).
+//
+// How: the context is split into partitions of part_tokens tokens.  One work item is
+// (sequence, partition, KV head, query sub-group); it streams the partition's K/V
+// blocks once and serves every query head of the group from them, keeping a running
+// maximum, a running sum and an unnormalised output (online softmax, fp32).  A
+// sequence with one partition is written straight to `out`; otherwise each partition
+// leaves (o_p / l_p, m_p + log2 l_p) and a second kernel merges them:
+//   M = max_p lse_p,  out = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M).
+// Scores are kept in the base-2 domain (q is pre-scaled by scale * log2 e).
+#include <math.h>
+
+#include <atomic>
+
+#include "attention.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ------------------------------------------------------------------------------------
+// Plan: partitions per sequence, exclusive scan, the work-item list; zero the output of
+// sequences with no tokens (or an invalid length; the bad length is flagged).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int head_dim) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
+  for (int base = 0; base < a.num_seqs; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int n = 0;
+    if (s < a.num_seqs) {
+      int c = a.context_lens[s];
+      if (c < 0 || c > cap) {
+        flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+        c = 0;
+      }
+      n = (c + a.part_tokens - 1) / a.part_tokens;
+      a.nparts[s] = n;
+      if (n == 0) {  // no partition will write this sequence's output
+        uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * head_dim);
+        for (int i = 0; i < a.num_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    int v = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, t, o);
+        if (lane >= o) t += y;
+      }
+      warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int off = carry + v - n + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int p = 0; p < n; ++p) a.items[off + p] = s * a.max_parts + p;
+    const int chunk_total = warp_tot[31];
+    __syncthreads();
+    if (threadIdx.x == 0) carry += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *a.num_items = carry;
+}
+
+// ------------------------------------------------------------------------------------
+// Partition kernel, CUDA-core variant.
+// Block = 4 warps.  Each warp takes every 4th 16-token block of the partition; a lane
+// loads 16-byte chunks of the block's K and V rows (LPT lanes per row), forms partial
+// dot products against the GM query heads, sums them over the row's lanes with
+// shuffles, and keeps its own online-softmax state.  The 4 warp states are merged in
+// shared memory at the end of the item.
+// ------------------------------------------------------------------------------------
+template <int D, int GM>
+__global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
+  constexpr int LPT = D / 8;             // lanes per token row (one 16-byte chunk each)
+  constexpr int TPI = 32 / LPT;          // rows one warp-wide load covers
+  constexpr int NI = kBlockSize / TPI;   // loads per block per lane
+  constexpr int NW = 4;
+  __shared__ __align__(16) float q_s[GM][D];
+  __shared__ float red_m[NW][GM], red_l[NW][GM];
+  __shared__ __align__(16) float red_o[NW][GM][D];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tg = lane / LPT;
+  const int dc = lane % LPT;
+  const int per_pair = a.num_kv_heads * a.sub_groups;
+  const int total = *a.num_items * per_pair;
+
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    const int pair = w / per_pair;
+    const int rem = w - pair * per_pair;
+    const int g = rem / a.sub_groups;
+    const int sub = rem - g * a.sub_groups;
+    const int packed = a.items[pair];
+    const int s = packed / a.max_parts;
+    const int p = packed - s * a.max_parts;
+    const int ctx = a.context_lens[s];
+    const int t0 = p * a.part_tokens;
+    const int t1 = min(ctx, t0 + a.part_tokens);
+    const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
+    const int h0 = g * a.group + sub * GM;
+    const int gcnt = min(GM, a.group - sub * GM);
+    const bool single = a.nparts[s] == 1;
+
+    for (int i = threadIdx.x; i < GM * D; i += blockDim.x) {
+      const int j = i / D, d = i - j * D;
+      q_s[j][d] = j < gcnt
+                      ? bf16_to_f32(a.q[((size_t)s * a.num_q_heads + h0 + j) * D + d]) * a.scale_log2
+                      : 0.f;
+    }
+    __syncthreads();
+
+    float m[GM], l[GM], acc[GM][8];
+#pragma unroll
+    for (int j = 0; j < GM; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+    }
+
+    const int32_t *bt = a.block_tables + (size_t)s * a.max_blocks + t0 / kBlockSize;
+    for (int jb = warp; jb < nblk; jb += NW) {
+      const int blk = bt[jb];
+      if ((unsigned)blk >= (unsigned)a.num_blocks) {
+        if (lane == 0) flag_error(a.err, PKV_DEV_BAD_BLOCK);
+        continue;
+      }
+      const size_t base = ((size_t)blk * a.num_kv_heads + g) * (size_t)(kBlockSize * D);
+      const uint4 *kp = reinterpret_cast<const uint4 *>(a.k_cache + base);
+      const uint4 *vp = reinterpret_cast<const uint4 *>(a.v_cache + base);
+      uint4 kr[NI], vr[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) kr[i] = ld_stream_v4(kp + i * 32 + lane);
+#pragma unroll
+      for (int i = 0; i < NI; ++i) vr[i] = ld_stream_v4(vp + i * 32 + lane);
+      const int tb = t0 + jb * kBlockSize + tg;  // token of load i: tb + i * TPI
+
+      float sc[NI][GM];
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const float4 qa = *reinterpret_cast<const float4 *>(&q_s[j][dc * 8]);
+        const float4 qb = *reinterpret_cast<const float4 *>(&q_s[j][dc * 8 + 4]);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          float x = qa.x * bf16_lo(kr[i].x);
+          x = fmaf(qa.y, bf16_hi(kr[i].x), x);
+          x = fmaf(qa.z, bf16_lo(kr[i].y), x);
+          x = fmaf(qa.w, bf16_hi(kr[i].y), x);
+          x = fmaf(qb.x, bf16_lo(kr[i].z), x);
+          x = fmaf(qb.y, bf16_hi(kr[i].z), x);
+          x = fmaf(qb.z, bf16_lo(kr[i].w), x);
+          x = fmaf(qb.w, bf16_hi(kr[i].w), x);
+          sc[i][j] = x;
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+#pragma unroll
+          for (int j = 0; j < GM; ++j) sc[i][j] += __shfl_xor_sync(kFull, sc[i][j], off);
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (tb + i * TPI >= t1)
+#pragma unroll
+          for (int j = 0; j < GM; ++j) sc[i][j] = -INFINITY;
+
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        float bmax = sc[0][j];
+#pragma unroll
+        for (int i = 1; i < NI; ++i) bmax = fmaxf(bmax, sc[i][j]);
+#pragma unroll
+        for (int off = LPT; off < 32; off <<= 1)
+          bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, off));
+        const float mn = fmaxf(m[j], bmax);
+        const float alpha = exp2f(m[j] - mn);
+        m[j] = mn;
+        l[j] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] *= alpha;
+      }
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const bool valid = tb + i * TPI < t1;
+        float vf[8];
+        vf[0] = bf16_lo(vr[i].x); vf[1] = bf16_hi(vr[i].x);
+        vf[2] = bf16_lo(vr[i].y); vf[3] = bf16_hi(vr[i].y);
+        vf[4] = bf16_lo(vr[i].z); vf[5] = bf16_hi(vr[i].z);
+        vf[6] = bf16_lo(vr[i].w); vf[7] = bf16_hi(vr[i].w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vf[e] = valid ? vf[e] : 0.f;  // rows past the end may hold anything
+#pragma unroll
+        for (int j = 0; j < GM; ++j) {
+          const float pr = exp2f(sc[i][j] - m[j]);
+          l[j] += pr;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(pr, vf[e], acc[j][e]);
+        }
+      }
+    }
+
+    // Sum over the warp's token groups (lanes that share a head_dim chunk).
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1)
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        l[j] += __shfl_xor_sync(kFull, l[j], off);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] += __shfl_xor_sync(kFull, acc[j][e], off);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        red_m[warp][j] = m[j];
+        red_l[warp][j] = l[j];
+      }
+    if (tg == 0)
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        *reinterpret_cast<float4 *>(&red_o[warp][j][dc * 8]) =
+            make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+        *reinterpret_cast<float4 *>(&red_o[warp][j][dc * 8 + 4]) =
+            make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+      }
+    __syncthreads();
+
+    for (int i = threadIdx.x; i < GM * D; i += blockDim.x) {
+      const int j = i / D, d = i - j * D;
+      if (j >= gcnt) continue;
+      float M = red_m[0][j];
+#pragma unroll
+      for (int ww = 1; ww < NW; ++ww) M = fmaxf(M, red_m[ww][j]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) {
+        const float c = exp2f(red_m[ww][j] - M);
+        L = fmaf(red_l[ww][j], c, L);
+        O = fmaf(red_o[ww][j][d], c, O);
+      }
+      const int h = h0 + j;
+      if (single) {
+        a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(O / L);
+      } else {
+        const size_t idx = ((size_t)s * a.max_parts + p) * a.num_q_heads + h;
+        a.part_o[idx * D + d] = O / L;
+        if (d == 0) a.part_lse[idx] = M + log2f(L);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Merge of the partitions: one warp per (sequence, query head).
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) attn_reduce_kernel(const AttnArgs a) {
+  constexpr int PER = D / 32;
+  const int s = blockIdx.x;
+  const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (h >= a.num_q_heads) return;
+  const int np = a.nparts[s];
+  if (np <= 1) return;  // written directly by the partition kernel, or zeroed by the plan
+  const size_t row0 = (size_t)s * a.max_parts * a.num_q_heads + h;  // + p * Hq
+  float M = -INFINITY;
+  for (int p = lane; p < np; p += 32) M = fmaxf(M, a.part_lse[row0 + (size_t)p * a.num_q_heads]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  float L = 0.f, acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int p = 0; p < np; ++p) {
+    const size_t row = row0 + (size_t)p * a.num_q_heads;
+    const float c = exp2f(a.part_lse[row] - M);
+    L += c;
+    const float *po = a.part_o + row * D + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(po);
+      acc[0] = fmaf(c, v.x, acc[0]);
+      acc[1] = fmaf(c, v.y, acc[1]);
+      acc[2] = fmaf(c, v.z, acc[2]);
+      acc[3] = fmaf(c, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2 *>(po);
+      acc[0] = fmaf(c, v.x, acc[0]);
+      acc[1] = fmaf(c, v.y, acc[1]);
+    }
+  }
+  const float inv = 1.f / L;
+  uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
+}
+
+template <typename K>
+int blocks_per_sm(K kernel, int threads) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
+    n = 1;
+  return n;
+}
+
+template <int D, int GM>
+int launch_fma_t(const AttnArgs &a, cudaStream_t st) {
+  static int occ = 0;
+  if (!occ) occ = blocks_per_sm(attn_fma_kernel<D, GM>, 128);
+  const int64_t upper = (int64_t)a.num_seqs * a.max_parts * a.num_kv_heads * a.sub_groups;
+  int64_t grid = (int64_t)device_sm_count() * occ;
+  if (grid > upper) grid = upper;
+  if (grid < 1) grid = 1;
+  attn_fma_kernel<D, GM><<<(int)grid, 128, 0, st>>>(a);
+  return (int)cudaGetLastError();
+}
+
+std::atomic<int> g_variant{PKV_ATTN_AUTO};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+  AttnWorkspace w;
+  size_t off = 0;
+  const size_t S = (size_t)num_seqs, P = (size_t)max_parts, H = (size_t)num_q_heads;
+  w.nparts_off = off;
+  off = align256(off + S * sizeof(int32_t));
+  w.num_items_off = off;
+  off = align256(off + sizeof(int32_t));
+  w.items_off = off;
+  off = align256(off + S * P * sizeof(int32_t));
+  w.lse_off = off;
+  off = align256(off + S * P * H * sizeof(float));
+  w.o_off = off;
+  off = align256(off + S * P * H * (size_t)head_dim * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+int launch_attn_fma(const AttnArgs &a, int head_dim, int width, cudaStream_t st) {
+  if (head_dim == 128) {
+    switch (width) {
+      case 1: return launch_fma_t<128, 1>(a, st);
+      case 2: return launch_fma_t<128, 2>(a, st);
+      case 4: return launch_fma_t<128, 4>(a, st);
+      default: return launch_fma_t<128, 8>(a, st);
+    }
+  }
+  switch (width) {
+    case 1: return launch_fma_t<64, 1>(a, st);
+    case 2: return launch_fma_t<64, 2>(a, st);
+    case 4: return launch_fma_t<64, 4>(a, st);
+    default: return launch_fma_t<64, 8>(a, st);
+  }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+namespace {
+constexpr int kDefaultPartition = 512;
+
+int max_parts_for(int max_context_len, int part) {
+  const int mp = (max_context_len + part - 1) / part;
+  return mp > 0 ? mp : 1;
+}
+}  // namespace
+
+extern "C" {
+
+size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                      int max_context_len, int partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+  return attn_workspace_layout(num_seqs, num_q_heads, head_dim,
+                               max_parts_for(max_context_len, part))
+      .total;
+}
+
+int paged_attention_set_variant(int variant) {
+  if (variant != PKV_ATTN_AUTO && variant != PKV_ATTN_FMA && variant != PKV_ATTN_MMA)
+    return PKV_ERR_ARG;
+  return g_variant.exchange(variant);
+}
+
+int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int partition_size, int max_context_len,
+                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                           void *stream) {
+  if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_blocks <= 0 || max_context_len < 0 || num_q_heads % num_kv_heads != 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return PKV_ERR_SHAPE;
+  const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+  if (part % kBlockSize != 0) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PKV_ERR_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ALIGN;
+  const int max_parts = max_parts_for(max_context_len, part);
+  if ((int64_t)num_seqs * max_parts >= (int64_t)1 << 31) return PKV_ERR_SHAPE;
+  const AttnWorkspace ws = attn_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  if (workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_ALIGN;
+
+  char *wb = static_cast<char *>(workspace);
+  AttnArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.part_tokens = part;
+  a.max_parts = max_parts;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
+  a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
+  a.items = reinterpret_cast<int32_t *>(wb + ws.items_off);
+  a.part_lse = reinterpret_cast<float *>(wb + ws.lse_off);
+  a.part_o = reinterpret_cast<float *>(wb + ws.o_off);
+  a.err = err_flag;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  attn_plan_kernel<<<1, 1024, 0, st>>>(a, head_dim);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+
+  const int variant = g_variant.load();
+  const int gwidth = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
+  int width = gwidth;
+  if (a.group > 8) width = 8;
+  a.sub_groups = (a.group + width - 1) / width;
+  int rc;
+  if (variant == PKV_ATTN_MMA) {
+    a.sub_groups = (a.group + 7) / 8;
+    rc = launch_attn_mma(a, head_dim, st);
+  } else {
+    rc = launch_attn_fma(a, head_dim, width, st);
+  }
+  if (rc != 0) return PKV_ERR_CUDA;
+  if (max_parts > 1) {
+    dim3 grid(num_seqs, (num_q_heads + 7) / 8);
+    if (head_dim == 128)
+      attn_reduce_kernel<128><<<grid, 256, 0, st>>>(a);
+    else
+      attn_reduce_kernel<64><<<grid, 256, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// Internal interface between the decode-attention translation units.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// One work item is (sequence s, partition p) x (KV head g, query sub-group);
+// items[] holds s * max_parts + p for every non-empty partition, in order.
+struct AttnArgs {
+  uint16_t *out;                 // [S][Hq][D] bf16
+  const uint16_t *q;             // [S][Hq][D] bf16
+  const uint16_t *k_cache;       // [NB][Hkv][16][D] bf16
+  const uint16_t *v_cache;
+  const int32_t *block_tables;   // [S][MB]
+  const int32_t *context_lens;   // [S]
+  int num_seqs, max_blocks, num_q_heads, num_kv_heads, group, num_blocks;
+  int part_tokens;               // partition size in tokens (multiple of 16)
+  int max_parts;                 // partitions per sequence the workspace holds
+  int sub_groups;                // query sub-groups per KV head (group > kernel width)
+  float scale_log2;              // scale * log2(e): scores live in the base-2 domain
+  // workspace
+  int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
+  int32_t *num_items;            // [1]
+  int32_t *items;                // [S * max_parts]
+  float *part_lse;               // [S][max_parts][Hq]   log2-sum-exp2 of the partition
+  float *part_o;                 // [S][max_parts][Hq][D] normalised partial output
+  int32_t *err;
+};
+
+// Workspace carving (256-byte aligned sections).
+struct AttnWorkspace {
+  size_t nparts_off, num_items_off, items_off, lse_off, o_off, total;
+};
+AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
+
+// Launchers (return a cudaError_t value).
+int launch_attn_fma(const AttnArgs &a, int head_dim, int width, cudaStream_t st);
+int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st);
+
+}  // namespace pkv

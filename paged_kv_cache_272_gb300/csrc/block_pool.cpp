@@ -1,0 +1,266 @@
+// Host block manager: one pool of fixed-size KV blocks, a block table per sequence,
+// reference counts, fork (shared prefixes, parallel sampling) and copy-on-write.
+//
+// The pages' rules ("Continuous batching and PagedAttention", section 3 PagedAttention;
+// "System-level optimization", section 2.3 PagedAttention solution): blocks of one
+// size come from a single pool on demand, a request's blocks need not be contiguous,
+// released blocks are reused at once, shared blocks are read-only and a private copy
+// is made only when a request writes into a shared block.
+//
+// Allocation policy (the pages leave it open): the free pool is a stack seeded with
+// free_order (first element handed out first); a freed block goes on top.  Every
+// failing call leaves the pool unchanged: the block demand of a call is counted before
+// anything is modified.
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pagedkv.h"
+
+struct pkv_pool {
+  int num_blocks = 0;
+  int block_size = 16;
+  std::vector<int32_t> free_stack;  // back() is handed out next
+  std::vector<int32_t> refcount;
+  struct Seq {
+    std::vector<int32_t> table;
+    int64_t num_tokens = 0;
+  };
+  std::unordered_map<int64_t, Seq> seqs;
+
+  int32_t alloc() {
+    int32_t b = free_stack.back();
+    free_stack.pop_back();
+    refcount[b] = 1;
+    return b;
+  }
+
+  // Blocks one append at token position n needs, given pending refcount changes.
+  int demand(const Seq &sq, int64_t n, std::unordered_map<int32_t, int> &delta) const {
+    if (n % block_size == 0) return 1;
+    int32_t last = sq.table[n / block_size];
+    int rc = refcount[last] + delta[last];
+    if (rc > 1) {
+      delta[last] -= 1;
+      return 1;
+    }
+    return 0;
+  }
+
+  // One append (demand already checked).  Returns the slot; fills the COW pair.
+  int64_t append(Seq &sq, int32_t *src, int32_t *dst) {
+    const int64_t n = sq.num_tokens;
+    *src = -1;
+    *dst = -1;
+    if (n % block_size == 0) {
+      sq.table.push_back(alloc());
+    } else {
+      int32_t &last = sq.table[n / block_size];
+      if (refcount[last] > 1) {
+        int32_t fresh = alloc();
+        refcount[last] -= 1;
+        *src = last;
+        *dst = fresh;
+        last = fresh;
+      }
+    }
+    sq.num_tokens = n + 1;
+    return (int64_t)sq.table[n / block_size] * block_size + n % block_size;
+  }
+};
+
+extern "C" {
+
+int pkv_pool_create(int num_blocks, int block_size, const int32_t *free_order, pkv_pool **out) {
+  if (!out) return PKV_ERR_NULL;
+  *out = nullptr;
+  if (num_blocks <= 0 || block_size <= 0) return PKV_ERR_ARG;
+  pkv_pool *p = new (std::nothrow) pkv_pool();
+  if (!p) return PKV_ERR_OOM;
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->refcount.assign(num_blocks, 0);
+  p->free_stack.resize(num_blocks);
+  std::vector<char> seen(num_blocks, 0);
+  for (int i = 0; i < num_blocks; ++i) {
+    int32_t b = free_order ? free_order[i] : i;
+    if (b < 0 || b >= num_blocks || seen[b]) {
+      delete p;
+      return PKV_ERR_ARG;
+    }
+    seen[b] = 1;
+    p->free_stack[num_blocks - 1 - i] = b;
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+void pkv_pool_destroy(pkv_pool *pool) { delete pool; }
+
+int pkv_pool_num_free(const pkv_pool *pool) {
+  return pool ? (int)pool->free_stack.size() : PKV_ERR_NULL;
+}
+
+int pkv_block_refcount(const pkv_pool *pool, int block) {
+  if (!pool) return PKV_ERR_NULL;
+  if (block < 0 || block >= pool->num_blocks) return PKV_ERR_ARG;
+  return pool->refcount[block];
+}
+
+int pkv_seq_add(pkv_pool *pool, int64_t seq) {
+  if (!pool) return PKV_ERR_NULL;
+  if (pool->seqs.count(seq)) return PKV_ERR_DUP_SEQ;
+  pool->seqs.emplace(seq, pkv_pool::Seq());
+  return PKV_OK;
+}
+
+int pkv_seq_fork(pkv_pool *pool, int64_t parent, int64_t child) {
+  if (!pool) return PKV_ERR_NULL;
+  auto it = pool->seqs.find(parent);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  if (pool->seqs.count(child)) return PKV_ERR_DUP_SEQ;
+  pkv_pool::Seq copy = it->second;
+  for (int32_t b : copy.table) pool->refcount[b] += 1;
+  pool->seqs.emplace(child, std::move(copy));
+  return PKV_OK;
+}
+
+int pkv_seq_free(pkv_pool *pool, int64_t seq) {
+  if (!pool) return PKV_ERR_NULL;
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  const auto &table = it->second.table;
+  for (int32_t b : table)
+    if (pool->refcount[b] <= 0) return PKV_ERR_REFCOUNT;
+  for (auto r = table.rbegin(); r != table.rend(); ++r) {
+    if (--pool->refcount[*r] == 0) pool->free_stack.push_back(*r);
+  }
+  pool->seqs.erase(it);
+  return PKV_OK;
+}
+
+int pkv_seq_num_tokens(const pkv_pool *pool, int64_t seq, int *num_tokens) {
+  if (!pool || !num_tokens) return PKV_ERR_NULL;
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  *num_tokens = (int)it->second.num_tokens;
+  return PKV_OK;
+}
+
+int pkv_seq_num_blocks(const pkv_pool *pool, int64_t seq, int *num_blocks) {
+  if (!pool || !num_blocks) return PKV_ERR_NULL;
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  *num_blocks = (int)it->second.table.size();
+  return PKV_OK;
+}
+
+int pkv_seq_append_slot(pkv_pool *pool, int64_t seq, int64_t *slot, int32_t *cow_src,
+                        int32_t *cow_dst) {
+  if (!pool || !slot || !cow_src || !cow_dst) return PKV_ERR_NULL;
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  std::unordered_map<int32_t, int> delta;
+  if (pool->demand(it->second, it->second.num_tokens, delta) > (int)pool->free_stack.size())
+    return PKV_ERR_OOM;
+  *slot = pool->append(it->second, cow_src, cow_dst);
+  return PKV_OK;
+}
+
+int pkv_seq_append_tokens(pkv_pool *pool, int64_t seq, int count, int64_t *slots,
+                          int32_t *cow_pairs, int *num_cow) {
+  if (!pool) return PKV_ERR_NULL;
+  if (count < 0) return PKV_ERR_ARG;
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+  auto &sq = it->second;
+  // Demand: a copy only for the first token (afterwards the block is private), plus
+  // one block per block boundary crossed.
+  std::unordered_map<int32_t, int> delta;
+  int64_t need = 0;
+  if (count > 0) {
+    const int64_t n = sq.num_tokens, bs = pool->block_size;
+    const int64_t have = (n + bs - 1) / bs, want = (n + count + bs - 1) / bs;
+    need = want - have;
+    if (n % bs != 0) need += pool->demand(sq, n, delta);
+  }
+  if (need > (int64_t)pool->free_stack.size()) return PKV_ERR_OOM;
+  int ncow = 0;
+  for (int i = 0; i < count; ++i) {
+    int32_t src, dst;
+    int64_t s = pool->append(sq, &src, &dst);
+    if (slots) slots[i] = s;
+    if (src >= 0) {
+      if (cow_pairs) {
+        cow_pairs[2 * ncow] = src;
+        cow_pairs[2 * ncow + 1] = dst;
+      }
+      ++ncow;
+    }
+  }
+  if (num_cow) *num_cow = ncow;
+  return PKV_OK;
+}
+
+int pkv_pool_step(pkv_pool *pool, const int64_t *seqs, int n, int64_t *slot_mapping,
+                  int32_t *cow_pairs, int *num_cow) {
+  if (!pool || (n > 0 && (!seqs || !slot_mapping))) return PKV_ERR_NULL;
+  if (n < 0) return PKV_ERR_ARG;
+  // Count the demand of the whole step first (a sequence may appear more than once).
+  std::unordered_map<int32_t, int> delta;
+  std::unordered_map<int64_t, int64_t> extra_tokens;
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    auto it = pool->seqs.find(seqs[i]);
+    if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+    // Only a sequence's first append of the step can land in a shared block; later
+    // ones land in the block that append made private or allocated.
+    const int64_t k = extra_tokens[seqs[i]]++;
+    const int64_t pos = it->second.num_tokens + k;
+    if (pos % pool->block_size == 0) {
+      need += 1;
+    } else if (k == 0) {
+      need += pool->demand(it->second, pos, delta);
+    }
+  }
+  if (need > (int64_t)pool->free_stack.size()) return PKV_ERR_OOM;
+  int ncow = 0;
+  for (int i = 0; i < n; ++i) {
+    auto &sq = pool->seqs.find(seqs[i])->second;
+    int32_t src, dst;
+    slot_mapping[i] = pool->append(sq, &src, &dst);
+    if (src >= 0) {
+      if (cow_pairs) {
+        cow_pairs[2 * ncow] = src;
+        cow_pairs[2 * ncow + 1] = dst;
+      }
+      ++ncow;
+    }
+  }
+  if (num_cow) *num_cow = ncow;
+  return PKV_OK;
+}
+
+int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_blocks,
+                    int32_t pad, int32_t *block_tables, int32_t *context_lens) {
+  if (!pool || (n > 0 && (!seqs || !block_tables || !context_lens))) return PKV_ERR_NULL;
+  if (n < 0 || max_blocks <= 0) return PKV_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    auto it = pool->seqs.find(seqs[i]);
+    if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
+    if ((int)it->second.table.size() > max_blocks) return PKV_ERR_ARG;
+  }
+  for (int i = 0; i < n; ++i) {
+    const auto &sq = pool->seqs.find(seqs[i])->second;
+    int32_t *row = block_tables + (size_t)i * max_blocks;
+    size_t nb = sq.table.size();
+    if (nb) std::memcpy(row, sq.table.data(), nb * sizeof(int32_t));
+    for (int j = (int)nb; j < max_blocks; ++j) row[j] = pad;
+    context_lens[i] = (int32_t)sq.num_tokens;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+"""Thin Python binding of libpagedkv.so (argument marshalling only).
+
+Every function here takes torch tensors on the GPU, checks dtypes and shapes, and
+passes raw pointers, sizes and the current CUDA stream to the C entry point of the
+same name declared in ``include/pagedkv.h``.  All work runs in the library's CUDA
+kernels.  If the library is missing the import raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
+DEFAULT_PARTITION = 512
+
+# Every entry point the header declares: name -> (restype, argtypes).
+_P, _I, _F, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                         ctypes.c_int64)
+SIGNATURES = {
+    "paged_kv_version": (_I, []),
+    "paged_kv_strerror": (ctypes.c_char_p, [_I]),
+    "paged_kv_write": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "paged_block_copy": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                    _I, _P, _SZ, _P, _P]),
+    "paged_attention_set_variant": (_I, [_I]),
+    "pkv_pool_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
+    "pkv_pool_destroy": (None, [_P]),
+    "pkv_pool_num_free": (_I, [_P]),
+    "pkv_block_refcount": (_I, [_P, _I]),
+    "pkv_seq_add": (_I, [_P, _I64]),
+    "pkv_seq_fork": (_I, [_P, _I64, _I64]),
+    "pkv_seq_free": (_I, [_P, _I64]),
+    "pkv_seq_num_tokens": (_I, [_P, _I64, _P]),
+    "pkv_seq_num_blocks": (_I, [_P, _I64, _P]),
+    "pkv_seq_append_slot": (_I, [_P, _I64, _P, _P, _P]),
+    "pkv_seq_append_tokens": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "pkv_pool_step": (_I, [_P, _P, _I, _P, _P, _P]),
+    "pkv_pool_export": (_I, [_P, _P, _I, _I, ctypes.c_int32, _P, _P]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with __graft_entry__.build() or "
+            "python -m paged_kv_cache_272_gb300.build (there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = lib.paged_kv_strerror(code).decode()
+        super().__init__(f"{what}: {msg} (code {code})")
+        self.code = code
+
+
+def check(code: int, what: str) -> None:
+    if code != 0:
+        raise PagedKVError(code, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bf16_cuda(name, t):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous bf16 CUDA tensor")
+
+
+def _i32(name, t):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def paged_kv_write(k_new, v_new, slot_mapping, k_cache, v_cache, err_flag=None, stream=None):
+    """Scatter k_new/v_new [T][Hkv][D] into the caches [NB][Hkv][16][D] at slot_mapping."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16_cuda(n, t)
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda:
+        raise TypeError("slot_mapping must be an int64 CUDA tensor")
+    NB, Hkv, bs, D = k_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, D) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    check(lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping.contiguous()), T,
+                             _ptr(k_cache), _ptr(v_cache), NB, Hkv, D, bs, _ptr(err_flag),
+                             _stream(stream)), "paged_kv_write")
+
+
+def paged_block_copy(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
+    """Copy whole blocks src -> dst for each row of block_pairs [P][2] (int32)."""
+    _bf16_cuda("k_cache", k_cache)
+    _bf16_cuda("v_cache", v_cache)
+    _i32("block_pairs", block_pairs)
+    NB, Hkv, bs, D = k_cache.shape
+    P = block_pairs.numel() // 2
+    check(lib.paged_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, NB, Hkv, D,
+                               bs, _ptr(err_flag), _stream(stream)), "paged_block_copy")
+
+
+def paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                   partition_size=DEFAULT_PARTITION) -> int:
+    return int(lib.paged_attention_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                  max_context_len, partition_size))
+
+
+def alloc_workspace(num_seqs, num_q_heads, head_dim, max_context_len,
+                    partition_size=DEFAULT_PARTITION, device="cuda"):
+    n = paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                       partition_size)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           max_context_len, workspace, partition_size=DEFAULT_PARTITION,
+                           err_flag=None, stream=None):
+    """out[S][Hq][D] = softmax(scale q K^T) V over each sequence's paged context."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16_cuda(n, t)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S][max_blocks] and context_lens [S]")
+    check(lib.paged_attention_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
+        int(partition_size), int(max_context_len), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)), "paged_attention_decode")
+
+
+def set_attention_variant(variant: int) -> int:
+    prev = lib.paged_attention_set_variant(int(variant))
+    if prev < 0:
+        raise PagedKVError(prev, "paged_attention_set_variant")
+    return prev

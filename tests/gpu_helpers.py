@@ -1,0 +1,104 @@
+"""Helpers shared by the GPU parity tests: run one decode step through the C ABI and
+compare it with the oracle."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_272_gb300 import workloads
+
+ATOL, RTOL, MEAN_TOL = 1e-2, 1e-2, 2e-3
+NTHREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def ops():
+    from paged_kv_cache_272_gb300 import ops as _ops
+    return _ops
+
+
+def to_cuda(w: workloads.Workload):
+    """Device copies of everything one step reads."""
+    dev = "cuda"
+    return dict(
+        k=w.k_cache.to(dev).contiguous().clone(), v=w.v_cache.to(dev).contiguous().clone(),
+        q=w.q.to(dev).contiguous(), k_new=w.k_new.to(dev).contiguous(),
+        v_new=w.v_new.to(dev).contiguous(),
+        slots=torch.as_tensor(w.slot_mapping, dtype=torch.int64, device=dev),
+        pairs=torch.as_tensor(w.cow_pairs.reshape(-1, 2), dtype=torch.int32, device=dev),
+        bt=torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev),
+        ctx=torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev))
+
+
+def gpu_step(w: workloads.Workload, variant=None, partition_size=None, max_context_len=None,
+             d=None, block_tables=None, context_lens=None):
+    """copy-on-write -> write -> attention through the C ABI.  Returns (out, k, v, err)."""
+    o = ops()
+    d = d or to_cuda(w)
+    if variant is not None:
+        o.set_attention_variant(variant)
+    P = partition_size or w.partition_size
+    mcl = w.max_context_len if max_context_len is None else max_context_len
+    bt = d["bt"] if block_tables is None else block_tables
+    ctx = d["ctx"] if context_lens is None else context_lens
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if d["pairs"].numel():
+        o.paged_block_copy(d["k"], d["v"], d["pairs"], err_flag=err)
+    if d["slots"].numel():
+        o.paged_kv_write(d["k_new"], d["v_new"], d["slots"], d["k"], d["v"], err_flag=err)
+    S, Hq, D = d["q"].shape
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = o.alloc_workspace(S, Hq, D, mcl, P)
+    ws.fill_(0xFF)  # stale workspace content must not matter
+    o.paged_attention_decode(out, d["q"], d["k"], d["v"], bt, ctx, w.scale, mcl, ws, P,
+                             err_flag=err)
+    torch.cuda.synchronize()
+    if variant is not None:
+        o.set_attention_variant(o.PKV_ATTN_AUTO)
+    return out, d["k"], d["v"], int(err.item())
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_caches(w: workloads.Workload):
+    k, v = u16(w.k_cache).copy(), u16(w.v_cache).copy()
+    if w.cow_pairs.size:
+        oracle.block_copy(k, v, w.cow_pairs)
+    if w.slot_mapping.size:
+        oracle.kv_write(k, v, u16(w.k_new), u16(w.v_new), w.slot_mapping)
+    return k, v
+
+
+def oracle_out(w, k, v, sel=None, context_lens=None, block_tables=None):
+    ctx = w.context_lens if context_lens is None else context_lens
+    bt = w.block_tables if block_tables is None else block_tables
+    return oracle.attention(u16(w.q), k, v, bt, ctx, w.scale, sel=sel, nthreads=NTHREADS)
+
+
+def assert_attention_close(gpu_out: torch.Tensor, ref: np.ndarray, what=""):
+    g = gpu_out.detach().float().cpu().double().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} elements out of tolerance, max err "
+                           f"{err.max():.3g} at {np.unravel_index(err.argmax(), err.shape)}")
+    assert err.mean() <= MEAN_TOL, f"{what}: mean |err| {err.mean():.3g} > {MEAN_TOL}"
+    return float(err.max()), float(err.mean())
+
+
+def sample_pairs(w, n_short=64, seed=0):
+    """(sequence, head) pairs: every sequence of the longest context with one head per
+    KV head, plus random others."""
+    rng = np.random.default_rng(seed)
+    G = w.num_q_heads // w.num_kv_heads
+    longest = np.flatnonzero(w.context_lens == w.context_lens.max())
+    pairs = [(int(s), int(g * G + rng.integers(G))) for s in longest
+             for g in range(w.num_kv_heads)]
+    for _ in range(n_short):
+        pairs.append((int(rng.integers(w.num_seqs)), int(rng.integers(w.num_q_heads))))
+    return np.array(pairs, dtype=np.int32)

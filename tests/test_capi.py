@@ -1,0 +1,79 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_lists_the_path():
+    names = declared_functions()
+    for want in ("paged_kv_write", "paged_attention_decode", "paged_block_copy",
+                 "paged_attention_workspace_size", "paged_kv_strerror", "pkv_pool_create",
+                 "pkv_pool_step", "pkv_seq_append_slot"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    from paged_kv_cache_272_gb300 import ops
+    lib = ctypes.CDLL(ops.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) <= set(ops.SIGNATURES)
+
+
+def test_host_side_validation():
+    from paged_kv_cache_272_gb300.ops import lib
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    # block size other than 16
+    assert lib.paged_kv_write(fake, fake, fake, 4, fake, fake, 8, 1, 64, 8, None, None) == -3
+    # head_dim not a multiple of 8
+    assert lib.paged_kv_write(fake, fake, fake, 4, fake, fake, 8, 1, 60, 16, None, None) == -2
+    # NULL pointer
+    assert lib.paged_kv_write(None, fake, fake, 4, fake, fake, 8, 1, 64, 16, None, None) == -1
+    # misaligned
+    assert lib.paged_kv_write(fake + 2, fake, fake, 4, fake, fake, 8, 1, 64, 16, None, None) == -4
+    # nothing to do is fine and touches nothing
+    assert lib.paged_kv_write(None, None, None, 0, None, None, 8, 1, 64, 16, None, None) == 0
+    assert lib.paged_block_copy(fake, fake, fake, 2, 8, 1, 64, 12, None, None) == -3
+    assert lib.paged_block_copy(None, None, None, 0, 8, 1, 64, 16, None, None) == 0
+    ws = lib.paged_attention_workspace_size(4, 8, 128, 1000, 512)
+    assert ws > 0 and ws % 256 == 0
+    args = lambda **kw: [kw.get("out", fake), fake, fake, fake, fake, fake, kw.get("S", 4), 8,
+                         kw.get("Hq", 8), kw.get("Hkv", 2), kw.get("D", 128), kw.get("bs", 16),
+                         16, ctypes.c_float(0.1), kw.get("part", 512), 1000, fake,
+                         kw.get("ws", ws), None, None]
+    assert lib.paged_attention_decode(*args(bs=32)) == -3
+    assert lib.paged_attention_decode(*args(D=96)) == -2
+    assert lib.paged_attention_decode(*args(Hq=6, Hkv=4)) == -2
+    assert lib.paged_attention_decode(*args(part=100)) == -2
+    assert lib.paged_attention_decode(*args(out=None)) == -1
+    assert lib.paged_attention_decode(*args(ws=ws - 1)) == -5
+    assert lib.paged_attention_decode(*args(S=0)) == 0
+    assert lib.paged_attention_set_variant(7) == -14
+
+
+def test_strerror():
+    from paged_kv_cache_272_gb300.ops import lib
+    for code in (0, -1, -2, -3, -4, -5, -6, -10, -11, -12, -13, -14, -99):
+        assert lib.paged_kv_strerror(code)
+
+
+def test_workspace_size_formula():
+    from paged_kv_cache_272_gb300.ops import paged_attention_workspace_size as wsz
+    # Partials: S * max_parts * Hq * (D + 1) floats dominate.
+    S, Hq, D = 128, 64, 128
+    n = wsz(S, Hq, D, 131072, 512)
+    assert n >= S * 256 * Hq * (D + 1) * 4
+    assert n < S * 256 * Hq * (D + 1) * 4 + S * 256 * 4 + 4096

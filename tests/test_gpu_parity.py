@@ -1,0 +1,197 @@
+"""GPU parity through the C ABI: the paged write and block copy are bit-exact against
+the oracle; attention matches the fp64 oracle within |err| <= 1e-2 + 1e-2 |ref| per
+element and mean |err| <= 2e-3, on the five workloads and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+from paged_kv_cache_272_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+FMA, MMA = 1, 2
+VARIANTS = [FMA]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _make(cfg):
+    # the tiny workload is drawn on the host; the others on the device (then copied
+    # to the host for the oracle)
+    return workloads.make_config(cfg, device="cpu" if cfg == 1 else "cuda")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_config_parity_full(cfg, variant):
+    w = _make(cfg)
+    out, k, v, err = H.gpu_step(w, variant)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    assert np.array_equal(H.u16(k), ko), "paged write / block copy not bit-exact (K)"
+    assert np.array_equal(H.u16(v), vo), "paged write / block copy not bit-exact (V)"
+    ref = H.oracle_out(w, ko, vo)
+    H.assert_attention_close(out, ref, f"config {cfg}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_config5_long_context_sampled(variant):
+    """8 x 131072 + 120 short contexts at full size; the oracle computes a sample of
+    (sequence, head) outputs one by one.  Write and copy are checked in full."""
+    w = _make(5)
+    out, k, v, err = H.gpu_step(w, variant)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    assert np.array_equal(H.u16(k), ko)
+    assert np.array_equal(H.u16(v), vo)
+    sel = H.sample_pairs(w, n_short=48)
+    ref = H.oracle_out(w, ko, vo, sel=sel)
+    got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+              torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+    H.assert_attention_close(got, ref, "config 5 sample")
+    # every output finite, and the full output is a convex combination per element
+    # bound: |o| <= max |v| over the context
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 64, 8), (64, 2, 1), (128, 32, 32), (64, 12, 4)])
+def test_boundary_contexts(D, Hq, Hkv, variant):
+    ctx = [1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025, 1536, 2000]
+    w = workloads.build("edges", ctx, Hq, Hkv, D, seed=77, device="cuda")
+    out, k, v, err = H.gpu_step(w, variant)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    H.assert_attention_close(out, H.oracle_out(w, ko, vo), f"edges D{D} G{Hq // Hkv}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 8, 16])
+def test_group_sizes(G, variant):
+    w = workloads.build("groups", [7, 100, 530, 1100], 2 * G, 2, 128, seed=80 + G,
+                        device="cuda")
+    out, k, v, err = H.gpu_step(w, variant)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    H.assert_attention_close(out, H.oracle_out(w, ko, vo), f"G={G}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_partition_size_invariance(variant):
+    """Split-K merge: partitions of 16, 64, 512 and 8192 tokens all match the oracle and
+    each other."""
+    ctx = np.random.default_rng(3).integers(1, 3000, size=24)
+    w = workloads.build("parts", ctx, 16, 2, 128, seed=90, device="cuda")
+    ko, vo = H.oracle_caches(w)
+    ref = H.oracle_out(w, ko, vo)
+    outs = []
+    for P in (16, 64, 512, 8192):
+        out, k, v, err = H.gpu_step(w, variant, partition_size=P)
+        assert err == 0
+        H.assert_attention_close(out, ref, f"partition {P}")
+        outs.append(out.float())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_large_magnitude_scores(variant):
+    w = workloads.build("big", [40, 600, 1500], 16, 2, 128, seed=95, device="cuda")
+    w.q.mul_(30)
+    out, k, v, err = H.gpu_step(w, variant)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    H.assert_attention_close(out, H.oracle_out(w, ko, vo), "q x 30")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_context_one_returns_v(variant):
+    w = workloads.build("one", [1] * 8, 16, 2, 128, seed=96, device="cuda")
+    out, k, v, err = H.gpu_step(w, variant)
+    G = 8
+    want = w.v_new.repeat_interleave(G, dim=1)  # [S][Hq][D]
+    assert torch.equal(out, want.to(out.device)), "ctx 1 must return V exactly"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_zero_context_and_bad_context(variant):
+    w = workloads.build("zero", [5, 40, 700, 33], 8, 2, 128, seed=97, device="cuda")
+    ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device="cuda").clone()
+    ctx[1] = 0
+    ctx[2] = 5000  # beyond the block table and max_context_len
+    out, k, v, err = H.gpu_step(w, variant, context_lens=ctx, max_context_len=1000)
+    assert err & 4  # PKV_DEV_BAD_CONTEXT
+    assert torch.all(out[1] == 0) and torch.all(out[2] == 0)
+    ko, vo = H.oracle_caches(w)
+    ref = H.oracle_out(w, ko, vo)
+    H.assert_attention_close(out[[0, 3]], ref[[0, 3]], "valid neighbours")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_bad_block_id_is_flagged_not_read(variant):
+    w = workloads.build("badblk", [40, 70], 8, 2, 128, seed=98, device="cuda")
+    bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device="cuda").clone()
+    bt[1, 2] = w.num_blocks + 1000
+    out, k, v, err = H.gpu_step(w, variant, block_tables=bt)
+    assert err & 1  # PKV_DEV_BAD_BLOCK
+    ko, vo = H.oracle_caches(w)
+    ref = H.oracle_out(w, ko, vo)
+    H.assert_attention_close(out[:1], ref[:1], "untouched sequence")
+
+
+def test_write_and_copy_bit_exact_on_arbitrary_bytes():
+    """All 65536 bf16 bit patterns (NaNs, infinities, subnormals) survive the write and
+    the copy unchanged; skipped (-1) slots write nothing; a bad slot is flagged."""
+    o = H.ops()
+    NB, Hkv, D = 64, 4, 128
+    g = torch.Generator(device="cpu").manual_seed(5)
+    kc = torch.randint(-32768, 32768, (NB, Hkv, 16, D), generator=g, dtype=torch.int16)
+    vc = torch.randint(-32768, 32768, (NB, Hkv, 16, D), generator=g, dtype=torch.int16)
+    T = 300
+    kn = torch.arange(T * Hkv * D, dtype=torch.int32).remainder(65536).sub(32768).to(
+        torch.int16).view(T, Hkv, D)
+    vn = kn.flip(0).contiguous()
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
+    slots[::17] = -1
+    bad = slots.clone()
+    bad[5] = NB * 16 + 3
+    pairs = torch.tensor([[3, 60], [10, 61], [0, 62], [33, 63]], dtype=torch.int32)
+    k0, v0 = kc.numpy().view(np.uint16).copy(), vc.numpy().view(np.uint16).copy()
+    import oracle
+    oracle.kv_write(k0, v0, kn.numpy().view(np.uint16), vn.numpy().view(np.uint16),
+                    slots.numpy())
+    oracle.block_copy(k0, v0, pairs.numpy())
+    kd, vd = kc.view(torch.bfloat16).cuda(), vc.view(torch.bfloat16).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o.paged_kv_write(kn.view(torch.bfloat16).cuda(), vn.view(torch.bfloat16).cuda(),
+                     slots.cuda(), kd, vd, err_flag=err)
+    o.paged_block_copy(kd, vd, pairs.cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(H.u16(kd), k0) and np.array_equal(H.u16(vd), v0)
+    # a slot beyond the pool is flagged and skipped
+    kd2, vd2 = kc.view(torch.bfloat16).cuda(), vc.view(torch.bfloat16).cuda()
+    o.paged_kv_write(kn.view(torch.bfloat16).cuda(), vn.view(torch.bfloat16).cuda(),
+                     bad.cuda(), kd2, vd2, err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() & 2
+
+
+def test_empty_calls_are_noops():
+    o = H.ops()
+    kc = torch.zeros(4, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    e = torch.zeros(0, 1, 64, dtype=torch.bfloat16, device="cuda")
+    o.paged_kv_write(e, e, torch.zeros(0, dtype=torch.int64, device="cuda"), kc, vc)
+    o.paged_block_copy(kc, vc, torch.zeros(0, 2, dtype=torch.int32, device="cuda"))
+    q = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    ws = o.alloc_workspace(0, 2, 64, 16)
+    o.paged_attention_decode(q.clone(), q, kc, vc,
+                             torch.zeros(0, 1, dtype=torch.int32, device="cuda"),
+                             torch.zeros(0, dtype=torch.int32, device="cuda"), 0.125, 16, ws)
+    torch.cuda.synchronize()
