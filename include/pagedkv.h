@@ -129,6 +129,31 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
                            void *stream);
 
 /*
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that cannot
+ * allocate device memory (no cudaMalloc on their thread, memory owned by another
+ * runtime's pool, or a stream being captured by someone else).  The pages have no
+ * counterpart; it is a deployment convenience.
+ * Same arguments and result as paged_attention_decode, minus the workspace: the
+ * split-K scratch is a fixed device array of PKV_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps until the process exits.
+ * Sizes whose paged_attention_workspace_size exceeds it return PKV_ERR_WORKSPACE and
+ * enqueue nothing.  The call allocates nothing (no cudaMalloc/cudaFree or allocating
+ * library routine).  Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture.  All calls on one device share the array: calls whose kernels
+ * overlap on the GPU (other streams, other threads) race, so order them on one
+ * stream.  The array keeps the last call's contents; nothing in it needs clearing.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int paged_attention_decode_noalloc(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs,
+                                   int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks, float scale,
+                                   int partition_size, int max_context_len, int32_t *err_flag,
+                                   void *stream);
+
+/*
  * Attention kernel selection, process-wide (for measurement; the default is AUTO).
  * Returns the previous value, or PKV_ERR_ARG for an unknown value.
  */

@@ -484,3 +484,58 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// Allocation-free decode attention.
+//
+// Some callers cannot call cudaMalloc at all: code that runs while a CUDA graph is
+// being recorded by someone else, an embedding runtime whose memory is owned by its
+// own pool, a real-time service that forbids allocation on the serving thread.  For
+// them the split-K workspace lives in this fixed device array instead of a buffer
+// the caller passes.  Every GPU that loads the library holds the array until the
+// process exits.  All calls on a device share it and it keeps the last call's
+// contents; the attention path overwrites every part of it it reads, so nothing needs
+// clearing between calls.  Calls whose kernels overlap on the GPU race on it.
+// ------------------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];
+
+// Device address of the array on the current device, looked up once per device.  In
+// host code the array's name is only a host-side stand-in, never a device address.
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PKV_ERR_CUDA;
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_attention_decode_noalloc(
+    uint16_t *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+    int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, float scale, int partition_size, int max_context_len, int32_t *err_flag,
+    void *stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0)
+    return PKV_ERR_SHAPE;
+  const size_t need = paged_attention_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                     max_context_len, partition_size);
+  if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != PKV_OK) return rc;
+  return paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                                block_size, num_blocks, scale, partition_size, max_context_len,
+                                scratch, (size_t)PKV_NOALLOC_SCRATCH_BYTES, err_flag, stream);
+}

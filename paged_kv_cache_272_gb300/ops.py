@@ -31,6 +31,8 @@ SIGNATURES = {
     "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _I, _P, _SZ, _P, _P]),
     "paged_attention_set_variant": (_I, [_I]),
+    "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                            _F, _I, _I, _P, _P]),
     "pkv_pool_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_pool_destroy": (None, [_P]),
     "pkv_pool_num_free": (_I, [_P]),
