@@ -28,58 +28,57 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------------------------------
-// Plan: partitions per sequence, exclusive scan, the work-item list; zero the output of
-// sequences with no tokens (or an invalid length; the bad length is flagged).
+// Plan (one CTA): validate context lengths, count partitions, zero the output of
+// sequences with no tokens (a bad length is flagged and treated as empty), and list
+// the partitions as records ordered by block count, largest first (a counting sort
+// over 1..32 blocks; order within one size is arbitrary and does not affect results).
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int head_dim) {
-  __shared__ int warp_tot[32];
-  __shared__ int carry;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) carry = 0;
+  constexpr int kBins = 33;
+  __shared__ int hist[kBins];
+  __shared__ int cursor[kBins];
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
-  for (int base = 0; base < a.num_seqs; base += blockDim.x) {
-    const int s = base + threadIdx.x;
-    int n = 0;
-    if (s < a.num_seqs) {
-      int c = a.context_lens[s];
-      if (c < 0 || c > cap) {
-        flag_error(a.err, PKV_DEV_BAD_CONTEXT);
-        c = 0;
-      }
-      n = (c + a.part_tokens - 1) / a.part_tokens;
-      a.nparts[s] = n;
-      if (n == 0) {  // no partition will write this sequence's output
-        uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * head_dim);
-        for (int i = 0; i < a.num_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-      }
+  const int P = a.part_tokens;
+  for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
+    int c = a.context_lens[s];
+    if (c < 0 || c > cap) {
+      flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+      c = 0;
     }
-    int v = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, v, o);
-      if (lane >= o) v += y;
+    const int n = (c + P - 1) / P;
+    a.nparts[s] = n;
+    if (n == 0) {  // no partition will write this sequence's output
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * head_dim);
+      for (int i = 0; i < a.num_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
     }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      int t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, t, o);
-        if (lane >= o) t += y;
-      }
-      warp_tot[lane] = t;
+    for (int p = 0; p < n; ++p) {
+      const int nb = (min(c, (p + 1) * P) - p * P + kBlockSize - 1) / kBlockSize;
+      atomicAdd(&hist[min(nb, 32)], 1);
     }
-    __syncthreads();
-    const int off = carry + v - n + (warp > 0 ? warp_tot[warp - 1] : 0);
-    for (int p = 0; p < n; ++p) a.items[off + p] = s * a.max_parts + p;
-    const int chunk_total = warp_tot[31];
-    __syncthreads();
-    if (threadIdx.x == 0) carry += chunk_total;
-    __syncthreads();
   }
-  if (threadIdx.x == 0) *a.num_items = carry;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int b = 32; b >= 1; --b) {
+      cursor[b] = run;
+      run += hist[b];
+    }
+    *a.num_items = run;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
+    const int n = a.nparts[s];
+    if (n == 0) continue;
+    const int c = a.context_lens[s];  // validated above (n > 0)
+    for (int p = 0; p < n; ++p) {
+      const int t0 = p * P, t1 = min(c, t0 + P);
+      const int nb = (t1 - t0 + kBlockSize - 1) / kBlockSize;
+      const int pos = atomicAdd(&cursor[min(nb, 32)], 1);
+      a.items[pos] = make_int4(s, t0, t1, n == 1);
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -111,16 +110,13 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
     const int rem = w - pair * per_pair;
     const int g = rem / a.sub_groups;
     const int sub = rem - g * a.sub_groups;
-    const int packed = a.items[pair];
-    const int s = packed / a.max_parts;
-    const int p = packed - s * a.max_parts;
-    const int ctx = a.context_lens[s];
-    const int t0 = p * a.part_tokens;
-    const int t1 = min(ctx, t0 + a.part_tokens);
+    const int4 rec = a.items[pair];
+    const int s = rec.x, t0 = rec.y, t1 = rec.z;
+    const bool single = rec.w != 0;
+    const int p = t0 / a.part_tokens;
     const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
     const int h0 = g * a.group + sub * GM;
     const int gcnt = min(GM, a.group - sub * GM);
-    const bool single = a.nparts[s] == 1;
 
     for (int i = threadIdx.x; i < GM * D; i += blockDim.x) {
       const int j = i / D, d = i - j * D;
@@ -350,7 +346,7 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
   w.num_items_off = off;
   off = align256(off + sizeof(int32_t));
   w.items_off = off;
-  off = align256(off + S * P * sizeof(int32_t));
+  off = align256(off + S * P * sizeof(int4));
   w.lse_off = off;
   off = align256(off + S * P * H * sizeof(float));
   w.o_off = off;
@@ -450,7 +446,7 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
-  a.items = reinterpret_cast<int32_t *>(wb + ws.items_off);
+  a.items = reinterpret_cast<int4 *>(wb + ws.items_off);
   a.part_lse = reinterpret_cast<float *>(wb + ws.lse_off);
   a.part_o = reinterpret_cast<float *>(wb + ws.o_off);
   a.err = err_flag;
@@ -464,8 +460,15 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   int width = gwidth;
   if (a.group > 8) width = 8;
   a.sub_groups = (a.group + width - 1) / width;
+  // AUTO: the tensor-core variant once a KV head serves 4 or more query heads (the
+  // CUDA-core dot products then cost more issue slots than the bytes they consume);
+  // the CUDA-core variant for MHA and small groups, where it already streams at the
+  // HBM roofline.  The TMA tensor map indexes rows with 32-bit coordinates.
+  const bool tma_ok = (int64_t)num_blocks * num_kv_heads * kBlockSize < ((int64_t)1 << 31);
+  const bool use_mma =
+      tma_ok && (variant == PKV_ATTN_MMA || (variant == PKV_ATTN_AUTO && a.group >= 4));
   int rc;
-  if (variant == PKV_ATTN_MMA) {
+  if (use_mma) {
     a.sub_groups = (a.group + 7) / 8;
     rc = launch_attn_mma(a, head_dim, st);
   } else {

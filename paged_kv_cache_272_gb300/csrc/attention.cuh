@@ -5,8 +5,10 @@
 
 namespace pkv {
 
-// One work item is (sequence s, partition p) x (KV head g, query sub-group);
-// items[] holds s * max_parts + p for every non-empty partition, in order.
+// One work item is (sequence s, partition p) x (KV head g, query sub-group).  The plan
+// kernel lists every non-empty partition as an int4 record {s, t0, t1, single} (tokens
+// [t0, t1) of sequence s; single = the sequence has one partition), ordered by block
+// count, largest first, so that round-robin dealing of records to CTAs balances load.
 struct AttnArgs {
   uint16_t *out;                 // [S][Hq][D] bf16
   const uint16_t *q;             // [S][Hq][D] bf16
@@ -22,7 +24,7 @@ struct AttnArgs {
   // workspace
   int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]
-  int32_t *items;                // [S * max_parts]
+  int4 *items;                   // [S * max_parts] records {s, t0, t1, single}
   float *part_lse;               // [S][max_parts][Hq]   log2-sum-exp2 of the partition
   float *part_o;                 // [S][max_parts][Hq][D] normalised partial output
   int32_t *err;

@@ -1,6 +1,524 @@
-// Tensor-core variant of the partition kernel (placeholder until written).
+// Partition kernel, tensor-core variant: the query-group contraction on mma.sync tiles,
+// K/V tiles staged by TMA into per-warp shared-memory rings.
+//
+// Same arithmetic as the CUDA-core variant (softmax(scale q K^T) V per query head with
+// an online max and sum in fp32, "System-level optimization: batching, PagedAttention
+// and FlashAttention", sections 3.1 and 3.3), arranged for GB300:
+//
+//  * One CTA = one producer warp + NW consumer warps, one CTA per SM, persistent over
+//    the plan's records (dealt round-robin).  Block jb of an item goes to consumer
+//    warp jb % NW.
+//  * The producer reads each block id from the block table ("Continuous batching and
+//    PagedAttention", section 3: logical block -> physical block) and issues TMA tiled
+//    copies (cp.async.bulk.tensor.2d, 128-byte swizzle) of the block's K and V head
+//    tiles (16 rows x head_dim bf16) into the target warp's ring slot; completion is
+//    signalled on the slot's "full" mbarrier with the byte count.  The consumer frees
+//    the slot through its "empty" mbarrier.  Every wait is bounded.
+//  * A consumer computes S^T[16 tokens x 8 heads] = K Q^T with mma.m16n8k16 (tokens are
+//    the M dimension, the query group is N, head_dim is K), so a GQA-8 group fills the
+//    tile exactly; Q^T fragments live in registers for the whole item.  The softmax
+//    weights P (rounded to bf16) go from the accumulator layout to the B-operand layout
+//    with movmatrix (an 8x8 transpose in registers), and O^T[head_dim x 8] += V^T P^T is
+//    a second set of mma tiles whose A operand ldmatrix.trans reads straight from the
+//    staged V tile.  The sum of the weights uses the same rounded values.
+//  * At the end of an item the NW warp states (max, sum, O) are merged in shared
+//    memory, and the item's result goes to `out` (one partition) or to the split-K
+//    partials (merged later by the LSE kernel).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
 #include "attention.cuh"
 
 namespace pkv {
-int launch_attn_mma(const AttnArgs &, int, cudaStream_t) { return (int)cudaErrorNotSupported; }
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr long long kWaitCycles = 2000000000LL;  // about one second at GB300 clocks
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on one phase.  Gives up (returning false) after about a second, or at
+// once when another warp of the CTA has already given up; the first to give up raises
+// the CTA's abort flag and the device error bit.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      flag_error(err, PKV_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies in flight).
+__device__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// c += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Byte offset of element (row, col) inside a staged [16][D] tile: TMA writes each
+// 64-column half as a [16][128 B] box with the 128-byte swizzle (16-byte chunk index
+// XOR row % 8), halves 2 KB apart.
+__device__ __forceinline__ uint32_t tile_off(int row, int col) {
+  const int half = col >> 6, chunk = (col & 63) >> 3;
+  return (uint32_t)(half * 2048 + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+template <int D, int NW, int NS>
+struct MmaLayout {
+  static constexpr int kTile = kBlockSize * D * 2;   // bytes of one K (or V) head tile
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kRow = D + 4;                 // padded merge row (floats)
+  static constexpr int kStagesBytes = NW * NS * kStage;
+  static constexpr int kMergeBytes = NW * 8 * kRow * 4 + 2 * NW * 8 * 4;
+  static constexpr int kBarBytes = 2 * NW * NS * 8 + NW * NS * 4 + 16;
+  static constexpr int kSmem = 1024 + kStagesBytes + kMergeBytes + kBarBytes;
+};
+
+template <int D, int NW, int NS>
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
+    attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv) {
+  using L = MmaLayout<D, NW, NS>;
+  constexpr int KSTEPS = D / 16;
+  constexpr int HALVES = D / 64;
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte aligned stage area (the swizzle pattern repeats every 1024 bytes).
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  unsigned char *base = smem_raw + (base_u32 - raw_u32);
+  float *red_o = reinterpret_cast<float *>(base + L::kStagesBytes);         // [NW][8][kRow]
+  float *red_m = red_o + NW * 8 * L::kRow;                                   // [NW][8]
+  float *red_l = red_m + NW * 8;                                             // [NW][8]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(red_l + NW * 8);             // full, empty
+  int *valid = reinterpret_cast<int *>(bars + 2 * NW * NS);                  // [NW][NS]
+  volatile int *abort_flag = valid + NW * NS;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + NW * NS * 8;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int per_pair = a.num_kv_heads * a.sub_groups;
+  const int total = *a.num_items * per_pair;
+
+  if (warp == NW) {
+    // ------------------------------- producer -------------------------------------
+    int cnt = 0;  // lane w < NW: blocks handed to consumer warp w so far
+    bool stop = false;
+    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+      const int pair = item / per_pair;
+      const int g = (item - pair * per_pair) / a.sub_groups;
+      const int4 rec = a.items[pair];
+      const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
+      const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
+      for (int c = 0; c < nblk && !stop; c += 32) {
+        const int j = c + lane;
+        const int blk = j < nblk ? bt[j] : 0;
+        const bool bad = j < nblk && (unsigned)blk >= (unsigned)a.num_blocks;
+        if (bad) flag_error(a.err, PKV_DEV_BAD_BLOCK);
+        const int n = min(32, nblk - c);
+        for (int jj = 0; jj < n; ++jj) {
+          const int w = (c + jj) % NW;
+          const int b = __shfl_sync(kFull, blk, jj);
+          const int isbad = __shfl_sync(kFull, (int)bad, jj);
+          const int cw = __shfl_sync(kFull, cnt, w);
+          const int slot = cw % NS;
+          const uint32_t par = ((cw / NS) & 1) ^ 1;
+          int ok = 1;
+          if (lane == 0) {
+            const uint32_t fb = full0 + 8 * (w * NS + slot);
+            ok = mbar_wait(empty0 + 8 * (w * NS + slot), par, abort_flag, a.err);
+            if (ok) {
+              if (isbad) {
+                valid[w * NS + slot] = 0;
+                mbar_arrive(fb);
+              } else {
+                valid[w * NS + slot] = 1;
+                mbar_arrive_expect_tx(fb, L::kStage);
+                const uint32_t dst = base_u32 + (uint32_t)((w * NS + slot) * L::kStage);
+                const int y = (b * a.num_kv_heads + g) * kBlockSize;
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                  tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
+                  tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                }
+              }
+            }
+          }
+          ok = __shfl_sync(kFull, ok, 0);
+          if (!ok) {
+            stop = true;
+            break;
+          }
+          if (lane == w) ++cnt;
+        }
+      }
+    }
+    // Wait for every copy still in flight before the CTA may exit.
+    if (lane < NW) {
+      for (int i = max(0, cnt - NS); i < cnt; ++i)
+        mbar_drain(full0 + 8 * (lane * NS + i % NS), (i / NS) & 1);
+    }
+    return;
+  }
+
+  // --------------------------------- consumers --------------------------------------
+  const int gid = lane >> 2, tig = lane & 3;
+  int cnt = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const int pair = item / per_pair;
+    const int rem = item - pair * per_pair;
+    const int g = rem / a.sub_groups;
+    const int sub = rem - g * a.sub_groups;
+    const int4 rec = a.items[pair];
+    const int s = rec.x, t0 = rec.y, t1 = rec.z;
+    const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
+    const int h0 = g * a.group + sub * 8;
+    const int gcnt = min(8, a.group - sub * 8);
+
+    // Q^T as the B operand: thread (gid, tig) holds q[h0 + gid][16kk + 2tig (+8) .. +1].
+    uint32_t qb[KSTEPS][2];
+    {
+      const uint32_t *qrow =
+          reinterpret_cast<const uint32_t *>(a.q + ((size_t)s * a.num_q_heads + h0 + gid) * D);
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        qb[kk][0] = gid < gcnt ? qrow[(16 * kk + 2 * tig) >> 1] : 0u;
+        qb[kk][1] = gid < gcnt ? qrow[(16 * kk + 8 + 2 * tig) >> 1] : 0u;
+      }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[KSTEPS][4];
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+    for (int jb = warp; jb < nblk; jb += NW) {
+      const int slot = cnt % NS;
+      const uint32_t par = (cnt / NS) & 1;
+      ++cnt;
+      const uint32_t fb = full0 + 8 * (warp * NS + slot);
+      int ok = mbar_wait(fb, par, abort_flag, a.err);
+      ok = __all_sync(kFull, ok);
+      if (!ok) continue;  // aborted: keep the item/barrier sequence, skip the work
+      const int nvalid = min(kBlockSize, t1 - (t0 + jb * kBlockSize));
+      const uint32_t kst = base_u32 + (uint32_t)((warp * NS + slot) * L::kStage);
+      const uint32_t vst = kst + L::kTile;
+      if (valid[warp * NS + slot]) {
+        if (nvalid < kBlockSize) {
+          // Rows past the end of the context may hold anything (even NaN): zero them in
+          // V so that their zero weights contribute exactly nothing.
+          unsigned char *vrow = base + (vst - base_u32);
+          const int nz = (kBlockSize - nvalid) * (D / 8);
+          for (int i = lane; i < nz; i += 32) {
+            const int row = nvalid + i / (D / 8), ch = i % (D / 8);
+            *reinterpret_cast<uint4 *>(vrow + (ch >> 3) * 2048 + row * 128 + (ch & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // S^T = K Q^T  (rows: tokens gid, gid + 8; columns: heads 2 tig, 2 tig + 1)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kst + tile_off(row, 16 * kk + (lane >> 4) * 8), a0, a1, a2, a3);
+            mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          }
+        }
+        float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
+        float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+        if (gid >= nvalid) x0 = x1 = -INFINITY;
+        if (gid + 8 >= nvalid) x2 = x3 = -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        const uint32_t p01 = pack_bf16(exp2f(x0 - m0), exp2f(x1 - m1));
+        const uint32_t p23 = pack_bf16(exp2f(x2 - m0), exp2f(x3 - m1));
+        l0 = fmaf(l0, al0, bf16_lo(p01) + bf16_lo(p23));
+        l1 = fmaf(l1, al1, bf16_hi(p01) + bf16_hi(p23));
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          acc[mt][0] *= al0;
+          acc[mt][1] *= al1;
+          acc[mt][2] *= al0;
+          acc[mt][3] *= al1;
+        }
+        // P^T as the B operand of O^T += V^T P^T.
+        const uint32_t b0 = movmatrix_t(p01), b1 = movmatrix_t(p23);
+        {
+          const int j4 = lane >> 3;
+          const int tok = (lane & 7) + ((j4 >> 1) << 3);
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vst + tile_off(tok, 16 * mt + ((j4 & 1) << 3)), a0, a1, a2, a3);
+            mma16816(acc[mt], a0, a1, a2, a3, b0, b1);
+          }
+        }
+        if (nvalid < kBlockSize)  // generic writes above, async-proxy (TMA) writes next
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * (warp * NS + slot));
+    }
+
+    // ---- merge the NW warp states of this item ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    if (gid == 0) {
+      red_m[warp * 8 + 2 * tig] = m0;
+      red_m[warp * 8 + 2 * tig + 1] = m1;
+      red_l[warp * 8 + 2 * tig] = l0;
+      red_l[warp * 8 + 2 * tig + 1] = l1;
+    }
+    {
+      float *ro = red_o + warp * 8 * L::kRow;
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        ro[(2 * tig) * L::kRow + 16 * mt + gid] = acc[mt][0];
+        ro[(2 * tig + 1) * L::kRow + 16 * mt + gid] = acc[mt][1];
+        ro[(2 * tig) * L::kRow + 16 * mt + gid + 8] = acc[mt][2];
+        ro[(2 * tig + 1) * L::kRow + 16 * mt + gid + 8] = acc[mt][3];
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    const bool single = rec.w != 0;
+    const int p = t0 / a.part_tokens;
+    for (int i = threadIdx.x; i < gcnt * D; i += NW * 32) {
+      const int j = i / D, d = i - j * D;
+      float M = red_m[j];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) M = fmaxf(M, red_m[w * 8 + j]);
+      float Lsum = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float c = exp2f(red_m[w * 8 + j] - M);
+        Lsum = fmaf(red_l[w * 8 + j], c, Lsum);
+        O = fmaf(red_o[(w * 8 + j) * L::kRow + d], c, O);
+      }
+      const int h = h0 + j;
+      if (single) {
+        a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(O / Lsum);
+      } else {
+        const size_t idx = ((size_t)s * a.max_parts + p) * a.num_q_heads + h;
+        a.part_o[idx * D + d] = O / Lsum;
+        if (d == 0) a.part_lse[idx] = M + log2f(Lsum);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Host side: tensor maps (cached) and launch.
+// ------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The cache viewed as a 2-D tensor [num_blocks * Hkv * 16 rows][head_dim], boxes of
+// 16 rows x 64 columns (128 bytes) with the 128-byte swizzle.
+bool encode_kv_map(CUtensorMap *m, const void *base, uint64_t rows, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct MapCache {
+  struct Entry {
+    const void *base;
+    uint64_t rows;
+    int D;
+    CUtensorMap map;
+  };
+  std::mutex mu;
+  Entry e[8];
+  int n = 0, next = 0;
+  bool get(const void *base, uint64_t rows, int D, CUtensorMap *out) {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < n; ++i)
+      if (e[i].base == base && e[i].rows == rows && e[i].D == D) {
+        *out = e[i].map;
+        return true;
+      }
+    CUtensorMap m;
+    if (!encode_kv_map(&m, base, rows, D)) return false;
+    Entry &slot = e[next];
+    next = (next + 1) % 8;
+    if (n < 8) ++n;
+    slot.base = base;
+    slot.rows = rows;
+    slot.D = D;
+    slot.map = m;
+    *out = m;
+    return true;
+  }
+};
+MapCache g_maps;
+
+template <int D, int NW, int NS>
+int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                 cudaStream_t st) {
+  using L = MmaLayout<D, NW, NS>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        attn_mma_kernel<D, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  const int64_t upper = (int64_t)a.num_seqs * a.max_parts * a.num_kv_heads * a.sub_groups;
+  int64_t grid = device_sm_count();
+  if (grid > upper) grid = upper;
+  if (grid < 1) grid = 1;
+  attn_mma_kernel<D, NW, NS><<<(int)grid, (NW + 1) * 32, L::kSmem, st>>>(a, tk, tv);
+  return (int)cudaGetLastError();
+}
+
+// Ring shape (consumer warps x stages per warp), overridable for tuning through the
+// PKV_MMA_RING environment variable ("8x2", "4x4", "8x3").
+int ring_choice() {
+  static int choice = -1;
+  if (choice < 0) {
+    const char *v = std::getenv("PKV_MMA_RING");
+    choice = 0;
+    if (v && std::strcmp(v, "4x4") == 0) choice = 1;
+    if (v && std::strcmp(v, "8x3") == 0) choice = 2;
+  }
+  return choice;
+}
+
+}  // namespace
+
+int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
+  const uint64_t rows = (uint64_t)a.num_blocks * a.num_kv_heads * kBlockSize;
+  if (rows >= (1ull << 31)) return (int)cudaErrorInvalidValue;
+  CUtensorMap tk, tv;
+  if (!g_maps.get(a.k_cache, rows, head_dim, &tk) || !g_maps.get(a.v_cache, rows, head_dim, &tv))
+    return (int)cudaErrorInvalidValue;
+  if (head_dim == 64) return launch_mma_t<64, 8, 4>(a, tk, tv, st);
+  switch (ring_choice()) {
+    case 1: return launch_mma_t<128, 4, 4>(a, tk, tv, st);
+    case 2: return launch_mma_t<128, 8, 3>(a, tk, tv, st);
+    default: return launch_mma_t<128, 8, 2>(a, tk, tv, st);
+  }
+}
+
 }  // namespace pkv

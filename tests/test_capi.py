@@ -76,4 +76,4 @@ def test_workspace_size_formula():
     S, Hq, D = 128, 64, 128
     n = wsz(S, Hq, D, 131072, 512)
     assert n >= S * 256 * Hq * (D + 1) * 4
-    assert n < S * 256 * Hq * (D + 1) * 4 + S * 256 * 4 + 4096
+    assert n < S * 256 * Hq * (D + 1) * 4 + S * 256 * 16 + 4096

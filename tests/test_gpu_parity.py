@@ -11,7 +11,7 @@ from paged_kv_cache_272_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 FMA, MMA = 1, 2
-VARIANTS = [FMA]
+VARIANTS = [FMA, MMA]
 
 
 @pytest.fixture(scope="module", autouse=True)
