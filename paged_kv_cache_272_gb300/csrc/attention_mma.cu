@@ -5,8 +5,8 @@
 // an online max and sum in fp32, "System-level optimization: batching, PagedAttention
 // and FlashAttention", sections 3.1 and 3.3), arranged for GB300:
 //
-//  * One CTA = one producer warp + NW consumer warps, one CTA per SM, persistent over
-//    the plan's records (dealt round-robin).  Block jb of an item goes to consumer
+//  * One CTA = one producer warp + NW consumer warps, several CTAs per SM, persistent
+//    over the plan's records (dealt round-robin).  Block jb of an item goes to consumer
 //    warp jb % NW.
 //  * The producer reads each block id from the block table ("Continuous batching and
 //    PagedAttention", section 3: logical block -> physical block) and issues TMA tiled
@@ -157,7 +157,7 @@ struct MmaLayout {
 };
 
 template <int D, int NW, int NS>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+__global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (NW <= 4 ? 2 : 1)))
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
   using L = MmaLayout<D, NW, NS>;
@@ -192,39 +192,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
   if (warp == NW) {
     // ------------------------------- producer -------------------------------------
-    int cnt = 0;  // lane w < NW: blocks handed to consumer warp w so far
+    // Lane w < NW feeds consumer warp w: block jb of an item goes to lane jb % NW, so
+    // the lanes issue their copies side by side.  Lane w counts the blocks it handed
+    // to warp w (ring slot = count % NS, phase = count / NS).
+    int cnt = 0;
     bool stop = false;
-    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
-      const int pair = item / per_pair;
-      const int g = (item - pair * per_pair) / a.sub_groups;
-      const int4 rec = a.items[pair];
+    int item = blockIdx.x;
+    int4 rec = item < total ? a.items[item / per_pair] : make_int4(0, 0, 0, 0);
+    while (item < total && !stop) {
+      const int g = (item % per_pair) / a.sub_groups;
+      const int next = item + gridDim.x;
+      const int4 rec_next = next < total ? a.items[next / per_pair] : rec;  // prefetch
       const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
       const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
       for (int c = 0; c < nblk && !stop; c += 32) {
-        const int j = c + lane;
-        const int blk = j < nblk ? bt[j] : 0;
-        const bool bad = j < nblk && (unsigned)blk >= (unsigned)a.num_blocks;
-        if (bad) flag_error(a.err, PKV_DEV_BAD_BLOCK);
+        const int blk_lane = c + lane < nblk ? bt[c + lane] : 0;  // 32 table entries
         const int n = min(32, nblk - c);
-        for (int jj = 0; jj < n; ++jj) {
-          const int w = (c + jj) % NW;
-          const int b = __shfl_sync(kFull, blk, jj);
-          const int isbad = __shfl_sync(kFull, (int)bad, jj);
-          const int cw = __shfl_sync(kFull, cnt, w);
-          const int slot = cw % NS;
-          const uint32_t par = ((cw / NS) & 1) ^ 1;
+        for (int r = 0; r < n; r += NW) {
+          const int b = __shfl_sync(kFull, blk_lane, (r + lane) & 31);
           int ok = 1;
-          if (lane == 0) {
-            const uint32_t fb = full0 + 8 * (w * NS + slot);
-            ok = mbar_wait(empty0 + 8 * (w * NS + slot), par, abort_flag, a.err);
+          if (lane < NW && r + lane < n) {
+            const int slot = cnt % NS;
+            const uint32_t fb = full0 + 8 * (lane * NS + slot);
+            ok = mbar_wait(empty0 + 8 * (lane * NS + slot), ((cnt / NS) & 1) ^ 1, abort_flag,
+                           a.err);
             if (ok) {
-              if (isbad) {
-                valid[w * NS + slot] = 0;
+              if ((unsigned)b >= (unsigned)a.num_blocks) {
+                flag_error(a.err, PKV_DEV_BAD_BLOCK);
+                valid[lane * NS + slot] = 0;
                 mbar_arrive(fb);
               } else {
-                valid[w * NS + slot] = 1;
+                valid[lane * NS + slot] = 1;
                 mbar_arrive_expect_tx(fb, L::kStage);
-                const uint32_t dst = base_u32 + (uint32_t)((w * NS + slot) * L::kStage);
+                const uint32_t dst = base_u32 + (uint32_t)((lane * NS + slot) * L::kStage);
                 const int y = (b * a.num_kv_heads + g) * kBlockSize;
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
@@ -232,16 +232,17 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                   tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
                 }
               }
+              ++cnt;
             }
           }
-          ok = __shfl_sync(kFull, ok, 0);
-          if (!ok) {
+          if (!__all_sync(kFull, ok)) {
             stop = true;
             break;
           }
-          if (lane == w) ++cnt;
         }
       }
+      item = next;
+      rec = rec_next;
     }
     // Wait for every copy still in flight before the CTA may exit.
     if (lane < NW) {
@@ -484,8 +485,15 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
+  static int occ = 0;
+  if (!occ) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_mma_kernel<D, NW, NS>,
+                                                      (NW + 1) * 32, L::kSmem) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+  }
   const int64_t upper = (int64_t)a.num_seqs * a.max_parts * a.num_kv_heads * a.sub_groups;
-  int64_t grid = device_sm_count();
+  int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
   attn_mma_kernel<D, NW, NS><<<(int)grid, (NW + 1) * 32, L::kSmem, st>>>(a, tk, tv);
@@ -493,14 +501,15 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 }
 
 // Ring shape (consumer warps x stages per warp), overridable for tuning through the
-// PKV_MMA_RING environment variable ("8x2", "4x4", "8x3").
+// PKV_MMA_RING environment variable.
 int ring_choice() {
   static int choice = -1;
   if (choice < 0) {
+    static const char *names[] = {"4x2", "8x2", "8x3", "4x3", "2x2", "2x3", "3x2", "2x4", "3x3"};
     const char *v = std::getenv("PKV_MMA_RING");
     choice = 0;
-    if (v && std::strcmp(v, "4x4") == 0) choice = 1;
-    if (v && std::strcmp(v, "8x3") == 0) choice = 2;
+    for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
+      if (std::strcmp(v, names[i]) == 0) choice = i;
   }
   return choice;
 }
@@ -513,11 +522,17 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
   CUtensorMap tk, tv;
   if (!g_maps.get(a.k_cache, rows, head_dim, &tk) || !g_maps.get(a.v_cache, rows, head_dim, &tv))
     return (int)cudaErrorInvalidValue;
-  if (head_dim == 64) return launch_mma_t<64, 8, 4>(a, tk, tv, st);
+  if (head_dim == 64) return launch_mma_t<64, 4, 4>(a, tk, tv, st);
   switch (ring_choice()) {
-    case 1: return launch_mma_t<128, 4, 4>(a, tk, tv, st);
+    case 1: return launch_mma_t<128, 8, 2>(a, tk, tv, st);
     case 2: return launch_mma_t<128, 8, 3>(a, tk, tv, st);
-    default: return launch_mma_t<128, 8, 2>(a, tk, tv, st);
+    case 3: return launch_mma_t<128, 4, 3>(a, tk, tv, st);
+    case 4: return launch_mma_t<128, 2, 2>(a, tk, tv, st);
+    case 5: return launch_mma_t<128, 2, 3>(a, tk, tv, st);
+    case 6: return launch_mma_t<128, 3, 2>(a, tk, tv, st);
+    case 7: return launch_mma_t<128, 2, 4>(a, tk, tv, st);
+    case 8: return launch_mma_t<128, 3, 3>(a, tk, tv, st);
+    default: return launch_mma_t<128, 4, 2>(a, tk, tv, st);
   }
 }
 
