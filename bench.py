@@ -243,7 +243,7 @@ def run_ours(args):
     bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev)
     ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev)
     out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device=dev)
-    P = w.partition_size
+    P = args.partition or w.partition_size
     mcl = w.max_context_len
     ws = ops.alloc_workspace(S, Hq, D, mcl, P, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -397,6 +397,8 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partition", type=int, default=0,
+                    help="split-K partition size in tokens (default: the workload's, 512)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -30,17 +30,23 @@ constexpr unsigned kFull = 0xffffffffu;
 // ------------------------------------------------------------------------------------
 // Plan (one CTA): validate context lengths, count partitions, zero the output of
 // sequences with no tokens (a bad length is flagged and treated as empty), and list
-// the partitions as records ordered by block count, largest first (a counting sort
-// over 1..32 blocks; order within one size is arbitrary and does not affect results).
+//  * the partitions as records ordered by block count, largest first (a counting sort
+//    over 1..32 blocks; order within one size is arbitrary and does not affect
+//    results), and
+//  * the merge units of sequences with several partitions: (sequence, group of 8
+//    query heads, chunk of kChunk partitions), units of multi-chunk sequences first.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int head_dim) {
   constexpr int kBins = 33;
   __shared__ int hist[kBins];
   __shared__ int cursor[kBins];
+  __shared__ int ucount[2], ucursor[2];  // merge units: [0] multi-chunk, [1] one chunk
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x < 2) ucount[threadIdx.x] = 0;
   __syncthreads();
   const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
   const int P = a.part_tokens;
+  const int G8 = (a.num_q_heads + 7) / 8;
   for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
     int c = a.context_lens[s];
     if (c < 0 || c > cap) {
@@ -53,10 +59,16 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
       uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * head_dim);
       for (int i = 0; i < a.num_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
     }
-    for (int p = 0; p < n; ++p) {
-      const int nb = (min(c, (p + 1) * P) - p * P + kBlockSize - 1) / kBlockSize;
-      atomicAdd(&hist[min(nb, 32)], 1);
+    if (n > 1) {
+      const int nch = (n + kChunk - 1) / kChunk;
+      atomicAdd(&ucount[nch > 1 ? 0 : 1], nch * G8);
+      if (nch > 1)  // arrival counters of the second merge level
+        for (int g = 0; g < G8; ++g) a.cnt_seq[(size_t)s * G8 + g] = 0;
     }
+    // n - 1 (or n) partitions of P tokens and at most one shorter tail.
+    const int nfull = c / P, tail = c - nfull * P;
+    if (nfull) atomicAdd(&hist[min(P / kBlockSize, 32)], nfull);
+    if (tail) atomicAdd(&hist[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -66,17 +78,29 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
       run += hist[b];
     }
     *a.num_items = run;
+    ucursor[0] = 0;
+    ucursor[1] = ucount[0];
+    *a.num_units = ucount[0] + ucount[1];
   }
   __syncthreads();
   for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
     const int n = a.nparts[s];
     if (n == 0) continue;
     const int c = a.context_lens[s];  // validated above (n > 0)
-    for (int p = 0; p < n; ++p) {
-      const int t0 = p * P, t1 = min(c, t0 + P);
-      const int nb = (t1 - t0 + kBlockSize - 1) / kBlockSize;
-      const int pos = atomicAdd(&cursor[min(nb, 32)], 1);
-      a.items[pos] = make_int4(s, t0, t1, n == 1);
+    const int nfull = c / P, tail = c - nfull * P;
+    if (nfull) {
+      int pos = atomicAdd(&cursor[min(P / kBlockSize, 32)], nfull);
+      for (int p = 0; p < nfull; ++p) a.items[pos++] = make_int4(s, p * P, (p + 1) * P, n);
+    }
+    if (tail) {
+      const int pos = atomicAdd(&cursor[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
+      a.items[pos] = make_int4(s, nfull * P, c, n);
+    }
+    if (n > 1) {
+      const int nch = (n + kChunk - 1) / kChunk;
+      int pos = atomicAdd(&ucursor[nch > 1 ? 0 : 1], nch * G8);
+      for (int ch = 0; ch < nch; ++ch)
+        for (int g = 0; g < G8; ++g) a.units[pos++] = make_int4(s, g, ch, n);
     }
   }
 }
@@ -112,7 +136,7 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
     const int sub = rem - g * a.sub_groups;
     const int4 rec = a.items[pair];
     const int s = rec.x, t0 = rec.y, t1 = rec.z;
-    const bool single = rec.w != 0;
+    const bool single = rec.w == 1;
     const int p = t0 / a.part_tokens;
     const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
     const int h0 = g * a.group + sub * GM;
@@ -269,46 +293,115 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
 }
 
 // ------------------------------------------------------------------------------------
-// Merge of the partitions: one warp per (sequence, query head).
+// Merge of the partitions (log-sum-exp weights):
+//   M = max_k lse_k,  o = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M).
+// A warp merges n entries of one query head: their lse values are read 32 at a time
+// (one per lane), their outputs eight at a time with all loads issued before use, and
+// the running sum is rescaled when the maximum grows.  Reads bypass L1 (the second
+// level reads results other CTAs of the same launch wrote).
 // ------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) attn_reduce_kernel(const AttnArgs a) {
+__device__ __forceinline__ void warp_merge(const float *lse, const float *o, size_t stride, int n,
+                                           int lane, float &m, float &L, float (&acc)[D / 32]) {
   constexpr int PER = D / 32;
-  const int s = blockIdx.x;
-  const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (h >= a.num_q_heads) return;
-  const int np = a.nparts[s];
-  if (np <= 1) return;  // written directly by the partition kernel, or zeroed by the plan
-  const size_t row0 = (size_t)s * a.max_parts * a.num_q_heads + h;  // + p * Hq
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) M = fmaxf(M, a.part_lse[row0 + (size_t)p * a.num_q_heads]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  float L = 0.f, acc[PER];
+  m = -INFINITY;
+  L = 0.f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int p = 0; p < np; ++p) {
-    const size_t row = row0 + (size_t)p * a.num_q_heads;
-    const float c = exp2f(a.part_lse[row] - M);
-    L += c;
-    const float *po = a.part_o + row * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4 *>(po);
-      acc[0] = fmaf(c, v.x, acc[0]);
-      acc[1] = fmaf(c, v.y, acc[1]);
-      acc[2] = fmaf(c, v.z, acc[2]);
-      acc[3] = fmaf(c, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2 *>(po);
-      acc[0] = fmaf(c, v.x, acc[0]);
-      acc[1] = fmaf(c, v.y, acc[1]);
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    const int cnt = min(32, n - k0);
+    const float x = lane < cnt ? __ldcg(lse + (size_t)(k0 + lane) * stride) : -INFINITY;
+    float mb = x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+    const float mn = fmaxf(m, mb);
+    const float sc = exp2f(m - mn);
+    m = mn;
+    const float w = exp2f(x - mn);  // this lane's entry weight (0 past the end)
+    float ws = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(kFull, ws, off);
+    L = fmaf(L, sc, ws);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= sc;
+    for (int k = 0; k < cnt; k += 8) {
+      float c[8], v[8][PER];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        c[u] = __shfl_sync(kFull, w, (k + u) & 31);
+        if (k + u < cnt) {
+          const float *src = o + (size_t)(k0 + k + u) * stride * D + lane * PER;
+          if constexpr (PER == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+            v[u][0] = t.x, v[u][1] = t.y, v[u][2] = t.z, v[u][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+            v[u][0] = t.x, v[u][1] = t.y;
+          }
+        } else {
+          c[u] = 0.f;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(c[u], v[u][e], acc[e]);
     }
   }
-  const float inv = 1.f / L;
-  uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+}
+
+// Persistent over the plan's merge units; warp w of a unit serves query head 8 g + w.
+// A sequence with one chunk is finished by its units; one with several leaves a result
+// per chunk, and the unit that completes its last chunk merges them.
+template <int D>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
+  constexpr int PER = D / 32;
+  __shared__ int last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G8 = (a.num_q_heads + 7) / 8;
+  const int nu = *a.num_units;
+  for (int u = blockIdx.x; u < nu; u += gridDim.x) {
+    const int4 un = a.units[u];
+    const int s = un.x, g8 = un.y, ch = un.z, np = un.w;
+    const int nch = (np + kChunk - 1) / kChunk;
+    const int h = g8 * 8 + warp;
+    const int p0 = ch * kChunk, n = min(kChunk, np - p0);
+    float m, L, acc[PER];
+    if (h < a.num_q_heads) {
+      const size_t row = ((size_t)s * a.max_parts + p0) * a.num_q_heads + h;
+      warp_merge<D>(a.part_lse + row, a.part_o + row * D, a.num_q_heads, n, lane, m, L, acc);
+      const float inv = 1.f / L;
+      if (nch == 1) {
+        uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
+        for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
+      } else {
+        const size_t crow = ((size_t)s * a.max_chunks + ch) * a.num_q_heads + h;
+        float *o = a.chunk_o + crow * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = acc[e] * inv;
+        if (lane == 0) a.chunk_lse[crow] = m + log2f(L);
+      }
+    }
+    if (nch > 1) {  // uniform over the CTA
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) last = atomicAdd(&a.cnt_seq[(size_t)s * G8 + g8], 1) == nch - 1;
+      __syncthreads();
+      if (last && h < a.num_q_heads) {
+        __threadfence();
+        const size_t row = (size_t)s * a.max_chunks * a.num_q_heads + h;
+        warp_merge<D>(a.chunk_lse + row, a.chunk_o + row * D, a.num_q_heads, nch, lane, m, L, acc);
+        const float inv = 1.f / L;
+        uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
+      }
+      __syncthreads();  // `last` is rewritten by the next unit
+    }
+  }
 }
 
 template <typename K>
@@ -328,6 +421,22 @@ int launch_fma_t(const AttnArgs &a, cudaStream_t st) {
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
   attn_fma_kernel<D, GM><<<(int)grid, 128, 0, st>>>(a);
+  return (int)cudaGetLastError();
+}
+
+int launch_merge(const AttnArgs &a, int head_dim, int64_t max_units, cudaStream_t st) {
+  static int occ[2] = {0, 0};
+  const int k = head_dim == 128 ? 1 : 0;
+  if (!occ[k])
+    occ[k] = head_dim == 128 ? blocks_per_sm(attn_merge_kernel<128>, 256)
+                             : blocks_per_sm(attn_merge_kernel<64>, 256);
+  int64_t grid = (int64_t)device_sm_count() * occ[k];
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+  if (head_dim == 128)
+    attn_merge_kernel<128><<<(int)grid, 256, 0, st>>>(a);
+  else
+    attn_merge_kernel<64><<<(int)grid, 256, 0, st>>>(a);
   return (int)cudaGetLastError();
 }
 
@@ -351,6 +460,17 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
   off = align256(off + S * P * H * sizeof(float));
   w.o_off = off;
   off = align256(off + S * P * H * (size_t)head_dim * sizeof(float));
+  const size_t C = (P + kChunk - 1) / kChunk, G8 = (H + 7) / 8;
+  w.units_off = off;
+  off = align256(off + S * G8 * C * sizeof(int4));
+  w.num_units_off = off;
+  off = align256(off + sizeof(int32_t));
+  w.cnt_seq_off = off;
+  off = align256(off + S * G8 * sizeof(int32_t));
+  w.chunk_lse_off = off;
+  off = align256(off + S * C * H * sizeof(float));
+  w.chunk_o_off = off;
+  off = align256(off + S * C * H * (size_t)head_dim * sizeof(float));
   w.total = off;
   return w;
 }
@@ -449,17 +569,16 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   a.items = reinterpret_cast<int4 *>(wb + ws.items_off);
   a.part_lse = reinterpret_cast<float *>(wb + ws.lse_off);
   a.part_o = reinterpret_cast<float *>(wb + ws.o_off);
+  a.max_chunks = (max_parts + kChunk - 1) / kChunk;
+  a.units = reinterpret_cast<int4 *>(wb + ws.units_off);
+  a.num_units = reinterpret_cast<int32_t *>(wb + ws.num_units_off);
+  a.cnt_seq = reinterpret_cast<int32_t *>(wb + ws.cnt_seq_off);
+  a.chunk_lse = reinterpret_cast<float *>(wb + ws.chunk_lse_off);
+  a.chunk_o = reinterpret_cast<float *>(wb + ws.chunk_o_off);
   a.err = err_flag;
 
   cudaStream_t st = (cudaStream_t)stream;
-  attn_plan_kernel<<<1, 1024, 0, st>>>(a, head_dim);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-
   const int variant = g_variant.load();
-  const int gwidth = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
-  int width = gwidth;
-  if (a.group > 8) width = 8;
-  a.sub_groups = (a.group + width - 1) / width;
   // AUTO: the tensor-core variant once a KV head serves 4 or more query heads (the
   // CUDA-core dot products then cost more issue slots than the bytes they consume);
   // the CUDA-core variant for MHA and small groups, where it already streams at the
@@ -467,21 +586,16 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   const bool tma_ok = (int64_t)num_blocks * num_kv_heads * kBlockSize < ((int64_t)1 << 31);
   const bool use_mma =
       tma_ok && (variant == PKV_ATTN_MMA || (variant == PKV_ATTN_AUTO && a.group >= 4));
-  int rc;
-  if (use_mma) {
-    a.sub_groups = (a.group + 7) / 8;
-    rc = launch_attn_mma(a, head_dim, st);
-  } else {
-    rc = launch_attn_fma(a, head_dim, width, st);
-  }
+  const int width = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
+  a.sub_groups = use_mma ? (a.group + 7) / 8 : (a.group + width - 1) / width;
+
+  attn_plan_kernel<<<1, 1024, 0, st>>>(a, head_dim);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  const int rc = use_mma ? launch_attn_mma(a, head_dim, st) : launch_attn_fma(a, head_dim, width, st);
   if (rc != 0) return PKV_ERR_CUDA;
   if (max_parts > 1) {
-    dim3 grid(num_seqs, (num_q_heads + 7) / 8);
-    if (head_dim == 128)
-      attn_reduce_kernel<128><<<grid, 256, 0, st>>>(a);
-    else
-      attn_reduce_kernel<64><<<grid, 256, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    const int64_t units = (int64_t)num_seqs * ((num_q_heads + 7) / 8) * a.max_chunks;
+    if (launch_merge(a, head_dim, units, st) != 0) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

@@ -5,10 +5,17 @@
 
 namespace pkv {
 
+constexpr int kChunk = 32;  // partitions one merge unit combines
+
 // One work item is (sequence s, partition p) x (KV head g, query sub-group).  The plan
-// kernel lists every non-empty partition as an int4 record {s, t0, t1, single} (tokens
-// [t0, t1) of sequence s; single = the sequence has one partition), ordered by block
-// count, largest first, so that round-robin dealing of records to CTAs balances load.
+// kernel lists every non-empty partition as an int4 record {s, t0, t1, np} (tokens
+// [t0, t1) of sequence s, which has np partitions), ordered by block count, largest
+// first, so that round-robin dealing of records to CTAs balances load.
+//
+// The merge kernel works on units (sequence, group of 8 query heads, chunk of up to
+// kChunk partitions), also listed by the plan; a sequence with several chunks leaves
+// one result per chunk, and the unit that completes the sequence's last chunk (an
+// arrival counter) merges those.
 struct AttnArgs {
   uint16_t *out;                 // [S][Hq][D] bf16
   const uint16_t *q;             // [S][Hq][D] bf16
@@ -20,19 +27,26 @@ struct AttnArgs {
   int part_tokens;               // partition size in tokens (multiple of 16)
   int max_parts;                 // partitions per sequence the workspace holds
   int sub_groups;                // query sub-groups per KV head (group > kernel width)
+  int max_chunks;                // ceil(max_parts / kChunk)
   float scale_log2;              // scale * log2(e): scores live in the base-2 domain
   // workspace
   int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]
-  int4 *items;                   // [S * max_parts] records {s, t0, t1, single}
+  int4 *items;                   // [S * max_parts] records {s, t0, t1, np}
   float *part_lse;               // [S][max_parts][Hq]   log2-sum-exp2 of the partition
   float *part_o;                 // [S][max_parts][Hq][D] normalised partial output
+  int4 *units;                   // [S * head groups * max_chunks] {s, head group, chunk, np}
+  int32_t *num_units;            // [1]
+  int32_t *cnt_seq;              // [S][head groups] chunks merged (multi-chunk sequences)
+  float *chunk_lse;              // [S][max_chunks][Hq]
+  float *chunk_o;                // [S][max_chunks][Hq][D]
   int32_t *err;
 };
 
 // Workspace carving (256-byte aligned sections).
 struct AttnWorkspace {
-  size_t nparts_off, num_items_off, items_off, lse_off, o_off, total;
+  size_t nparts_off, num_items_off, items_off, lse_off, o_off, units_off, num_units_off,
+      cnt_seq_off, chunk_lse_off, chunk_o_off, total;
 };
 AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
 

@@ -23,7 +23,7 @@
 //    staged V tile.  The sum of the weights uses the same rounded values.
 //  * At the end of an item the NW warp states (max, sum, O) are merged in shared
 //    memory, and the item's result goes to `out` (one partition) or to the split-K
-//    partials (merged later by the LSE kernel).
+//    partials (merged by the LSE merge kernel).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -145,6 +145,26 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col) {
   return (uint32_t)(half * 2048 + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
+// Q^T as the B operand of S^T = K Q^T for one item: thread (gid, tig) holds
+// q[h0 + gid][16 kk + 2 tig (+8) .. +1] as bf16 pairs (zero for heads past the group).
+template <int D>
+__device__ __forceinline__ void load_q_frag(uint32_t (&qb)[D / 16][2], const AttnArgs &a,
+                                            int item, int per_pair, int4 rec, int gid, int tig,
+                                            bool live) {
+  const int rem = item % per_pair;
+  const int g = rem / a.sub_groups;
+  const int sub = rem - g * a.sub_groups;
+  const int h0 = g * a.group + sub * 8;
+  const bool on = live && gid < min(8, a.group - sub * 8);
+  const uint32_t *qrow =
+      reinterpret_cast<const uint32_t *>(a.q + ((size_t)rec.x * a.num_q_heads + h0 + gid) * D);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    qb[kk][0] = on ? qrow[(16 * kk + 2 * tig) >> 1] : 0u;
+    qb[kk][1] = on ? qrow[(16 * kk + 8 + 2 * tig) >> 1] : 0u;
+  }
+}
+
 template <int D, int NW, int NS>
 struct MmaLayout {
   static constexpr int kTile = kBlockSize * D * 2;   // bytes of one K (or V) head tile
@@ -199,14 +219,23 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     bool stop = false;
     int item = blockIdx.x;
     int4 rec = item < total ? a.items[item / per_pair] : make_int4(0, 0, 0, 0);
+    int4 rec_next = item + (int)gridDim.x < total ? a.items[(item + gridDim.x) / per_pair] : rec;
+    // The first 32 block-table entries of an item, one per lane, fetched an item ahead.
+    auto first_chunk = [&](int it, int4 r) -> int {
+      if (it >= total) return 0;
+      const int nb = (r.z - r.y + kBlockSize - 1) / kBlockSize;
+      return lane < nb ? a.block_tables[(size_t)r.x * a.max_blocks + r.y / kBlockSize + lane] : 0;
+    };
+    int chunk0 = first_chunk(item, rec);
     while (item < total && !stop) {
       const int g = (item % per_pair) / a.sub_groups;
-      const int next = item + gridDim.x;
-      const int4 rec_next = next < total ? a.items[next / per_pair] : rec;  // prefetch
+      const int next = item + gridDim.x, nn = next + gridDim.x;
+      const int4 rec_nn = nn < total ? a.items[nn / per_pair] : rec_next;
+      const int chunk0_next = first_chunk(next, rec_next);
       const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
       const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
       for (int c = 0; c < nblk && !stop; c += 32) {
-        const int blk_lane = c + lane < nblk ? bt[c + lane] : 0;  // 32 table entries
+        const int blk_lane = c == 0 ? chunk0 : (c + lane < nblk ? bt[c + lane] : 0);
         const int n = min(32, nblk - c);
         for (int r = 0; r < n; r += NW) {
           const int b = __shfl_sync(kFull, blk_lane, (r + lane) & 31);
@@ -243,6 +272,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       }
       item = next;
       rec = rec_next;
+      rec_next = rec_nn;
+      chunk0 = chunk0_next;
     }
     // Wait for every copy still in flight before the CTA may exit.
     if (lane < NW) {
@@ -255,28 +286,26 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
   // --------------------------------- consumers --------------------------------------
   const int gid = lane >> 2, tig = lane & 3;
   int cnt = 0;
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    const int pair = item / per_pair;
-    const int rem = item - pair * per_pair;
+  // Records and Q^T fragments are fetched one item ahead, so that an item boundary
+  // costs only the merge below.
+  int item = blockIdx.x;
+  int4 rec = item < total ? a.items[item / per_pair] : make_int4(0, 0, 0, 0);
+  int4 rec_next = item + (int)gridDim.x < total ? a.items[(item + gridDim.x) / per_pair] : rec;
+  uint32_t qb[KSTEPS][2];
+  load_q_frag<D>(qb, a, item < total ? item : 0, per_pair, rec, gid, tig, item < total);
+  for (; item < total; item += gridDim.x) {
+    const int nxt = item + gridDim.x, nn = nxt + gridDim.x;
+    const int4 rec_nn = nn < total ? a.items[nn / per_pair] : rec_next;
+    uint32_t qn[KSTEPS][2];
+    load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_next, gid, tig, nxt < total);
+    const int rem = item % per_pair;
     const int g = rem / a.sub_groups;
     const int sub = rem - g * a.sub_groups;
-    const int4 rec = a.items[pair];
     const int s = rec.x, t0 = rec.y, t1 = rec.z;
     const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
     const int h0 = g * a.group + sub * 8;
     const int gcnt = min(8, a.group - sub * 8);
 
-    // Q^T as the B operand: thread (gid, tig) holds q[h0 + gid][16kk + 2tig (+8) .. +1].
-    uint32_t qb[KSTEPS][2];
-    {
-      const uint32_t *qrow =
-          reinterpret_cast<const uint32_t *>(a.q + ((size_t)s * a.num_q_heads + h0 + gid) * D);
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        qb[kk][0] = gid < gcnt ? qrow[(16 * kk + 2 * tig) >> 1] : 0u;
-        qb[kk][1] = gid < gcnt ? qrow[(16 * kk + 8 + 2 * tig) >> 1] : 0u;
-      }
-    }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc[KSTEPS][4];
 #pragma unroll
@@ -384,7 +413,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
-    const bool single = rec.w != 0;
+    const bool single = rec.w == 1;
     const int p = t0 / a.part_tokens;
     for (int i = threadIdx.x; i < gcnt * D; i += NW * 32) {
       const int j = i / D, d = i - j * D;
@@ -408,6 +437,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    rec = rec_next;
+    rec_next = rec_nn;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      qb[kk][0] = qn[kk][0];
+      qb[kk][1] = qn[kk][1];
+    }
   }
 }
 

@@ -72,8 +72,12 @@ def test_strerror():
 
 def test_workspace_size_formula():
     from paged_kv_cache_272_gb300.ops import paged_attention_workspace_size as wsz
-    # Partials: S * max_parts * Hq * (D + 1) floats dominate.
-    S, Hq, D = 128, 64, 128
+    # Partials dominate: S * max_parts * Hq * (D + 1) floats, plus one chunk result
+    # (same shape) per 32 partitions, the work records, merge units and counters.
+    S, Hq, D, P = 128, 64, 128, 256
+    C, G8 = P // 32, Hq // 8
     n = wsz(S, Hq, D, 131072, 512)
-    assert n >= S * 256 * Hq * (D + 1) * 4
-    assert n < S * 256 * Hq * (D + 1) * 4 + S * 256 * 16 + 4096
+    part = S * P * Hq * (D + 1) * 4
+    chunk = S * C * Hq * (D + 1) * 4
+    assert n >= part + chunk
+    assert n < part + chunk + S * P * 16 + S * G8 * C * 16 + S * G8 * 4 + S * 4 + 16 * 256
