@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
       run += hist[b];
     }
     *a.num_items = run;
+    *a.work_next = 0;
     ucursor[0] = 0;
     ucursor[1] = ucount[0];
     *a.num_units = ucount[0] + ucount[1];
@@ -454,6 +455,8 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
   off = align256(off + S * sizeof(int32_t));
   w.num_items_off = off;
   off = align256(off + sizeof(int32_t));
+  w.work_next_off = off;
+  off = align256(off + sizeof(int32_t));
   w.items_off = off;
   off = align256(off + S * P * sizeof(int4));
   w.lse_off = off;
@@ -566,6 +569,7 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
+  a.work_next = reinterpret_cast<int32_t *>(wb + ws.work_next_off);
   a.items = reinterpret_cast<int4 *>(wb + ws.items_off);
   a.part_lse = reinterpret_cast<float *>(wb + ws.lse_off);
   a.part_o = reinterpret_cast<float *>(wb + ws.o_off);

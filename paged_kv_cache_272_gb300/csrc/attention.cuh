@@ -32,6 +32,7 @@ struct AttnArgs {
   // workspace
   int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]
+  int32_t *work_next;            // [1] next record to claim (tensor-core kernel)
   int4 *items;                   // [S * max_parts] records {s, t0, t1, np}
   float *part_lse;               // [S][max_parts][Hq]   log2-sum-exp2 of the partition
   float *part_o;                 // [S][max_parts][Hq][D] normalised partial output
@@ -45,7 +46,7 @@ struct AttnArgs {
 
 // Workspace carving (256-byte aligned sections).
 struct AttnWorkspace {
-  size_t nparts_off, num_items_off, items_off, lse_off, o_off, units_off, num_units_off,
+  size_t nparts_off, num_items_off, work_next_off, items_off, lse_off, o_off, units_off, num_units_off,
       cnt_seq_off, chunk_lse_off, chunk_o_off, total;
 };
 AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);

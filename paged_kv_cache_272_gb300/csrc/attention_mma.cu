@@ -5,8 +5,10 @@
 // an online max and sum in fp32, "System-level optimization: batching, PagedAttention
 // and FlashAttention", sections 3.1 and 3.3), arranged for GB300:
 //
-//  * One CTA = one producer warp + NW consumer warps, several CTAs per SM, persistent
-//    over the plan's records (dealt round-robin).  Block jb of an item goes to consumer
+//  * One CTA = one producer warp + NW consumer warps, several CTAs per SM, persistent:
+//    the producer claims the plan's records (largest first) from a global counter and
+//    announces them to the consumers through a small shared-memory ring, so CTAs that
+//    drew lighter records take more of them.  Block jb of an item goes to consumer
 //    warp jb % NW.
 //  * The producer reads each block id from the block table ("Continuous batching and
 //    PagedAttention", section 3: logical block -> physical block) and issues TMA tiled
@@ -170,10 +172,13 @@ struct MmaLayout {
   static constexpr int kTile = kBlockSize * D * 2;   // bytes of one K (or V) head tile
   static constexpr int kStage = 2 * kTile;
   static constexpr int kRow = D + 4;                 // padded merge row (floats)
+  static constexpr int kRing = 4;                    // item slots producer -> consumers
   static constexpr int kStagesBytes = NW * NS * kStage;
   static constexpr int kMergeBytes = NW * 8 * kRow * 4 + 2 * NW * 8 * 4;
-  static constexpr int kBarBytes = 2 * NW * NS * 8 + NW * NS * 4 + 16;
-  static constexpr int kSmem = 1024 + kStagesBytes + kMergeBytes + kBarBytes;
+  // mbarriers (block full/empty, item full/empty), item records, then ints
+  static constexpr int kCtlBytes =
+      (2 * NW * NS + 2 * kRing) * 8 + (kRing + 1) * 16 + (kRing + 2 + NW * NS) * 4 + 16;
+  static constexpr int kSmem = 1024 + kStagesBytes + kMergeBytes + kCtlBytes;
 };
 
 template <int D, int NW, int NS>
@@ -191,16 +196,25 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
   float *red_o = reinterpret_cast<float *>(base + L::kStagesBytes);         // [NW][8][kRow]
   float *red_m = red_o + NW * 8 * L::kRow;                                   // [NW][8]
   float *red_l = red_m + NW * 8;                                             // [NW][8]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(red_l + NW * 8);             // full, empty
-  int *valid = reinterpret_cast<int *>(bars + 2 * NW * NS);                  // [NW][NS]
-  volatile int *abort_flag = valid + NW * NS;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(red_l + NW * 8);
+  int4 *ring_rec = reinterpret_cast<int4 *>(bars + 2 * NW * NS + 2 * L::kRing);  // [kRing]
+  volatile int4 *cons_rec = ring_rec + L::kRing;
+  int *ring_item = reinterpret_cast<int *>(ring_rec + L::kRing + 1);         // [kRing]
+  volatile int *cons_item = ring_item + L::kRing;
+  volatile int *abort_flag = cons_item + 1;
+  int *valid = const_cast<int *>(abort_flag) + 1;                            // [NW][NS]
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + NW * NS * 8;
+  const uint32_t ifull0 = empty0 + NW * NS * 8, iempty0 = ifull0 + L::kRing * 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW * NS; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < L::kRing; ++i) {
+      mbar_init(ifull0 + 8 * i, 1);
+      mbar_init(iempty0 + 8 * i, 1);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -212,26 +226,44 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
 
   if (warp == NW) {
     // ------------------------------- producer -------------------------------------
-    // Lane w < NW feeds consumer warp w: block jb of an item goes to lane jb % NW, so
-    // the lanes issue their copies side by side.  Lane w counts the blocks it handed
-    // to warp w (ring slot = count % NS, phase = count / NS).
+    // Items are claimed from the plan's list (largest first) through a global counter,
+    // one item ahead, and announced to the consumers through a small ring of item
+    // slots.  Lane w < NW feeds consumer warp w: block jb of an item goes to lane
+    // jb % NW, so the lanes issue their copies side by side.  Lane w counts the blocks
+    // it handed to warp w (ring slot = count % NS, phase = count / NS).
     int cnt = 0;
     bool stop = false;
-    int item = blockIdx.x;
-    int4 rec = item < total ? a.items[item / per_pair] : make_int4(0, 0, 0, 0);
-    int4 rec_next = item + (int)gridDim.x < total ? a.items[(item + gridDim.x) / per_pair] : rec;
-    // The first 32 block-table entries of an item, one per lane, fetched an item ahead.
-    auto first_chunk = [&](int it, int4 r) -> int {
+    auto claim = [&]() -> int {
+      int it = 0;
+      if (lane == 0) it = atomicAdd(a.work_next, 1);
+      return __shfl_sync(kFull, it, 0);
+    };
+    auto first_chunk = [&](int it, int4 r) -> int {  // 32 block-table entries, one per lane
       if (it >= total) return 0;
       const int nb = (r.z - r.y + kBlockSize - 1) / kBlockSize;
       return lane < nb ? a.block_tables[(size_t)r.x * a.max_blocks + r.y / kBlockSize + lane] : 0;
     };
-    int chunk0 = first_chunk(item, rec);
-    while (item < total && !stop) {
-      const int g = (item % per_pair) / a.sub_groups;
-      const int next = item + gridDim.x, nn = next + gridDim.x;
-      const int4 rec_nn = nn < total ? a.items[nn / per_pair] : rec_next;
-      const int chunk0_next = first_chunk(next, rec_next);
+    auto publish = [&](int k, int it, int4 r) -> bool {
+      int ok = 1;
+      if (lane == 0) {
+        const int slot = k % L::kRing;
+        ok = mbar_wait(iempty0 + 8 * slot, ((k / L::kRing) & 1) ^ 1, abort_flag, a.err);
+        if (ok) {
+          ring_item[slot] = it;
+          ring_rec[slot] = r;
+          mbar_arrive(ifull0 + 8 * slot);
+        }
+      }
+      return __shfl_sync(kFull, ok, 0) != 0;
+    };
+    int cur = claim();
+    int4 rec = cur < total ? a.items[cur / per_pair] : make_int4(0, 0, 0, 0);
+    int chunk0 = first_chunk(cur, rec);
+    stop = !publish(0, cur, rec);
+    for (int k = 0; cur < total && !stop; ++k) {
+      const int nxt = claim();
+      const int4 rec_n = nxt < total ? a.items[nxt / per_pair] : rec;
+      const int g = (cur % per_pair) / a.sub_groups;
       const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
       const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
       for (int c = 0; c < nblk && !stop; c += 32) {
@@ -270,10 +302,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
           }
         }
       }
-      item = next;
-      rec = rec_next;
-      rec_next = rec_nn;
-      chunk0 = chunk0_next;
+      const int chunk0_n = first_chunk(nxt, rec_n);
+      if (!stop) stop = !publish(k + 1, nxt, rec_n);
+      cur = nxt;
+      rec = rec_n;
+      chunk0 = chunk0_n;
     }
     // Wait for every copy still in flight before the CTA may exit.
     if (lane < NW) {
@@ -284,21 +317,35 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
   }
 
   // --------------------------------- consumers --------------------------------------
+  // Thread 0 takes item k from the ring and leaves it in cons_item / cons_rec; a
+  // consumer-wide barrier then hands it to every consumer thread, so all consumer
+  // warps follow the same item sequence (and the same barriers) even after a timeout.
+  auto fetch = [&](int k) {
+    const int slot = k % L::kRing;
+    if (mbar_wait(ifull0 + 8 * slot, (k / L::kRing) & 1, abort_flag, a.err)) {
+      *cons_item = ring_item[slot];
+      const int4 r = ring_rec[slot];
+      cons_rec->x = r.x;
+      cons_rec->y = r.y;
+      cons_rec->z = r.z;
+      cons_rec->w = r.w;
+      mbar_arrive(iempty0 + 8 * slot);
+    } else {
+      *cons_item = total;  // give up: behave as if the list had ended
+    }
+  };
   const int gid = lane >> 2, tig = lane & 3;
   int cnt = 0;
-  // Records and Q^T fragments are fetched one item ahead, so that an item boundary
-  // costs only the merge below.
-  int item = blockIdx.x;
-  int4 rec = item < total ? a.items[item / per_pair] : make_int4(0, 0, 0, 0);
-  int4 rec_next = item + (int)gridDim.x < total ? a.items[(item + gridDim.x) / per_pair] : rec;
+  if (threadIdx.x == 0) fetch(0);
+  __syncwarp();
+  asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+  int cur = *cons_item;
+  int4 rec = make_int4(cons_rec->x, cons_rec->y, cons_rec->z, cons_rec->w);
   uint32_t qb[KSTEPS][2];
-  load_q_frag<D>(qb, a, item < total ? item : 0, per_pair, rec, gid, tig, item < total);
-  for (; item < total; item += gridDim.x) {
-    const int nxt = item + gridDim.x, nn = nxt + gridDim.x;
-    const int4 rec_nn = nn < total ? a.items[nn / per_pair] : rec_next;
-    uint32_t qn[KSTEPS][2];
-    load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_next, gid, tig, nxt < total);
-    const int rem = item % per_pair;
+  load_q_frag<D>(qb, a, cur < total ? cur : 0, per_pair, rec, gid, tig, cur < total);
+  asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // cons_* read by all
+  for (int k = 0; cur < total; ++k) {
+    const int rem = cur % per_pair;
     const int g = rem / a.sub_groups;
     const int sub = rem - g * a.sub_groups;
     const int s = rec.x, t0 = rec.y, t1 = rec.z;
@@ -390,7 +437,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       if (lane == 0) mbar_arrive(empty0 + 8 * (warp * NS + slot));
     }
 
-    // ---- merge the NW warp states of this item ----
+    // ---- merge the NW warp states of this item; take the next item meanwhile ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, off);
@@ -412,7 +459,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         ro[(2 * tig + 1) * L::kRow + 16 * mt + gid + 8] = acc[mt][3];
       }
     }
+    if (threadIdx.x == 0) fetch(k + 1);
+    __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    const int nxt = *cons_item;
+    const int4 rec_n = make_int4(cons_rec->x, cons_rec->y, cons_rec->z, cons_rec->w);
+    uint32_t qn[KSTEPS][2];
+    load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
     const bool single = rec.w == 1;
     const int p = t0 / a.part_tokens;
     for (int i = threadIdx.x; i < gcnt * D; i += NW * 32) {
@@ -437,8 +490,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
-    rec = rec_next;
-    rec_next = rec_nn;
+    cur = nxt;
+    rec = rec_n;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       qb[kk][0] = qn[kk][0];
@@ -541,7 +594,7 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 int ring_choice() {
   static int choice = -1;
   if (choice < 0) {
-    static const char *names[] = {"4x2", "8x2", "8x3", "4x3", "2x2", "2x3", "3x2", "2x4", "3x3"};
+    static const char *names[] = {"3x2", "8x2", "8x3", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3"};
     const char *v = std::getenv("PKV_MMA_RING");
     choice = 0;
     for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
@@ -565,10 +618,10 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
     case 3: return launch_mma_t<128, 4, 3>(a, tk, tv, st);
     case 4: return launch_mma_t<128, 2, 2>(a, tk, tv, st);
     case 5: return launch_mma_t<128, 2, 3>(a, tk, tv, st);
-    case 6: return launch_mma_t<128, 3, 2>(a, tk, tv, st);
+    case 6: return launch_mma_t<128, 4, 2>(a, tk, tv, st);
     case 7: return launch_mma_t<128, 2, 4>(a, tk, tv, st);
     case 8: return launch_mma_t<128, 3, 3>(a, tk, tv, st);
-    default: return launch_mma_t<128, 4, 2>(a, tk, tv, st);
+    default: return launch_mma_t<128, 3, 2>(a, tk, tv, st);
   }
 }
 
