@@ -351,7 +351,9 @@ def run_ours(args):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
     achieved = kv_bytes / (attn_avg_ms / 1e3) / 1e9
-    vname = {0: "auto", 1: "fma", 2: "mma"}[variant]
+    G = Hq // Hkv
+    # the kernel AUTO picks: tensor-core tiles once a KV head serves 4+ query heads
+    vname = {1: "fma", 2: "mma"}.get(variant, "mma" if G >= 4 else "fma")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -366,7 +368,8 @@ def run_ours(args):
             "new_tokens_per_step": int(w.slot_mapping.shape[0]),
             "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
                    "inputs larger than L2 (KV read per step >> 129 MB)"),
-            "attention_variant": vname, "parallelism": "replicas" if world > 1 else "single"},
+            "attention_variant": args.variant, "attention_kernel": vname,
+            "parallelism": "replicas" if world > 1 else "single"},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "seq_steps_per_s_per_layer": world * S / (ms_per_step / 1e3),
         "attention_ms": attn_avg_ms,
@@ -376,7 +379,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(w.name, vname),
-                     "kernel": "paged_attention_decode (plan + partition + merge kernels)",
+                     "kernel": "paged_attention_decode: plan + partition (%s) + merge kernels"
+                               % vname,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clk.summary(),
     }
