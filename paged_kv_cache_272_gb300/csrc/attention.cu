@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
   __shared__ int hist[kBins];
   __shared__ int cursor[kBins];
   __shared__ int ucount[2], ucursor[2];  // merge units: [0] multi-chunk, [1] one chunk
+  pdl_trigger();
+  pdl_wait();
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x < 2) ucount[threadIdx.x] = 0;
   __syncthreads();
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tg = lane / LPT;
   const int dc = lane % LPT;
+  pdl_trigger();
+  pdl_wait();
   const int per_pair = a.num_kv_heads * a.sub_groups;
   const int total = *a.num_items * per_pair;
 
@@ -362,6 +366,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   __shared__ int last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G8 = (a.num_q_heads + 7) / 8;
+  pdl_trigger();
+  pdl_wait();
   const int nu = *a.num_units;
   for (int u = blockIdx.x; u < nu; u += gridDim.x) {
     const int4 un = a.units[u];
@@ -421,8 +427,7 @@ int launch_fma_t(const AttnArgs &a, cudaStream_t st) {
   int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  attn_fma_kernel<D, GM><<<(int)grid, 128, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_fma_kernel<D, GM>, dim3((int)grid), dim3(128), 0, st, a);
 }
 
 int launch_merge(const AttnArgs &a, int head_dim, int64_t max_units, cudaStream_t st) {
@@ -434,11 +439,9 @@ int launch_merge(const AttnArgs &a, int head_dim, int64_t max_units, cudaStream_
   int64_t grid = (int64_t)device_sm_count() * occ[k];
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  if (head_dim == 128)
-    attn_merge_kernel<128><<<(int)grid, 256, 0, st>>>(a);
-  else
-    attn_merge_kernel<64><<<(int)grid, 256, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  return (int)(head_dim == 128
+                   ? launch_pdl(attn_merge_kernel<128>, dim3((int)grid), dim3(256), 0, st, a)
+                   : launch_pdl(attn_merge_kernel<64>, dim3((int)grid), dim3(256), 0, st, a));
 }
 
 std::atomic<int> g_variant{PKV_ATTN_AUTO};
@@ -593,8 +596,8 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   const int width = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
   a.sub_groups = use_mma ? (a.group + 7) / 8 : (a.group + width - 1) / width;
 
-  attn_plan_kernel<<<1, 1024, 0, st>>>(a, head_dim);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, a, head_dim) != cudaSuccess)
+    return PKV_ERR_CUDA;
   const int rc = use_mma ? launch_attn_mma(a, head_dim, st) : launch_attn_fma(a, head_dim, width, st);
   if (rc != 0) return PKV_ERR_CUDA;
   if (max_parts > 1) {

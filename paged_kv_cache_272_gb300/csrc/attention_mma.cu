@@ -220,6 +220,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the plan's records (and the step's cache writes) are complete
 
   const int per_pair = a.num_kv_heads * a.sub_groups;
   const int total = *a.num_items * per_pair;
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       if (lane == 0) it = atomicAdd(a.work_next, 1);
       return __shfl_sync(kFull, it, 0);
     };
-    auto first_chunk = [&](int it, int4 r) -> int {  // 32 block-table entries, one per lane
+    auto first_chunk = [&](int it, int4 r) -> int {  // first block-table entries, one per lane
       if (it >= total) return 0;
       const int nb = (r.z - r.y + kBlockSize - 1) / kBlockSize;
       return lane < nb ? a.block_tables[(size_t)r.x * a.max_blocks + r.y / kBlockSize + lane] : 0;
@@ -266,9 +268,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       const int g = (cur % per_pair) / a.sub_groups;
       const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
       const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
-      for (int c = 0; c < nblk && !stop; c += 32) {
+      // Block ids come 32 lanes at a time, in chunks of CH (a multiple of NW) so that
+      // block jb = c + r + lane always lands on warp jb % NW.
+      constexpr int CH = (32 / NW) * NW;
+      for (int c = 0; c < nblk && !stop; c += CH) {
         const int blk_lane = c == 0 ? chunk0 : (c + lane < nblk ? bt[c + lane] : 0);
-        const int n = min(32, nblk - c);
+        const int n = min(CH, nblk - c);
         for (int r = 0; r < n; r += NW) {
           const int b = __shfl_sync(kFull, blk_lane, (r + lane) & 31);
           int ok = 1;
@@ -585,8 +590,8 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
   int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  attn_mma_kernel<D, NW, NS><<<(int)grid, (NW + 1) * 32, L::kSmem, st>>>(a, tk, tv);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_mma_kernel<D, NW, NS>, dim3((int)grid), dim3((NW + 1) * 32),
+                         (size_t)L::kSmem, st, a, tk, tv);
 }
 
 // Ring shape (consumer warps x stages per warp), overridable for tuning through the
@@ -594,7 +599,7 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 int ring_choice() {
   static int choice = -1;
   if (choice < 0) {
-    static const char *names[] = {"3x2", "8x2", "8x3", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3"};
+    static const char *names[] = {"3x2", "8x2", "4x4", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3"};
     const char *v = std::getenv("PKV_MMA_RING");
     choice = 0;
     for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
@@ -614,7 +619,7 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
   if (head_dim == 64) return launch_mma_t<64, 4, 4>(a, tk, tv, st);
   switch (ring_choice()) {
     case 1: return launch_mma_t<128, 8, 2>(a, tk, tv, st);
-    case 2: return launch_mma_t<128, 8, 3>(a, tk, tv, st);
+    case 2: return launch_mma_t<128, 4, 4>(a, tk, tv, st);
     case 3: return launch_mma_t<128, 4, 3>(a, tk, tv, st);
     case 4: return launch_mma_t<128, 2, 2>(a, tk, tv, st);
     case 5: return launch_mma_t<128, 2, 3>(a, tk, tv, st);

@@ -19,6 +19,8 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__
                                 const int64_t *__restrict__ slots, int64_t total, int row_vecs,
                                 int heads, int64_t num_slots, uint4 *__restrict__ k_cache,
                                 uint4 *__restrict__ v_cache, int32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t row = i / row_vecs;  // t * heads + h
@@ -43,6 +45,8 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__
 __global__ void block_copy_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                                   const int32_t *__restrict__ pairs, int64_t total,
                                   int64_t block_vecs, int num_blocks, int32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t p = i / block_vecs;
@@ -120,11 +124,12 @@ int paged_kv_write(const uint16_t *k_new, const uint16_t *v_new, const int64_t *
   const int row_vecs = head_dim / 8;
   const int64_t total = (int64_t)num_tokens * num_kv_heads * row_vecs;
   const int threads = 256;
-  kv_write_kernel<<<grid_for(total, threads), threads, 0, (cudaStream_t)stream>>>(
+  const cudaError_t e = launch_pdl(
+      kv_write_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
       reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
       slot_mapping, total, row_vecs, num_kv_heads, (int64_t)num_blocks * kBlockSize,
       reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), err_flag);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_pairs,
@@ -140,10 +145,11 @@ int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_
   const int64_t block_vecs = (int64_t)num_kv_heads * kBlockSize * head_dim / 8;
   const int64_t total = (int64_t)num_pairs * block_vecs;
   const int threads = 256;
-  block_copy_kernel<<<grid_for(total, threads), threads, 0, (cudaStream_t)stream>>>(
+  const cudaError_t e = launch_pdl(
+      block_copy_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
       reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), block_pairs, total,
       block_vecs, num_blocks, err_flag);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // extern "C"
