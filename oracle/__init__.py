@@ -63,6 +63,17 @@ def _declare(lib):
     lib.oracle_attention.restype = I
     lib.oracle_kv_bytes_per_token.argtypes = [I, I, I, I]
     lib.oracle_kv_bytes_per_token.restype = ctypes.c_int64
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_kv_write_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, ctypes.c_float]
+    lib.oracle_kv_write_fp8.restype = I
+    lib.oracle_block_copy_fp8.argtypes = [P, P, P, I, I, I, I, I]
+    lib.oracle_block_copy_fp8.restype = I
+    lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+                                         ctypes.c_double, ctypes.c_double, P, I, I]
+    lib.oracle_attention_fp8.restype = I
     return lib
 
 
@@ -145,3 +156,62 @@ def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, bytes_per_elem
     """2 x layers x kv_heads x head_dim x bytes ("Inference optimization", KV cache)."""
     lib = lib or load()
     return int(lib.oracle_kv_bytes_per_token(layers, kv_heads, head_dim, bytes_per_elem))
+
+
+# ---- FP8 (E4M3) cache -------------------------------------------------------------
+def e4m3_decode(code: int, lib=None) -> float:
+    return float((lib or load()).oracle_e4m3_decode(int(code)))
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    return int((lib or load()).oracle_e4m3_encode(float(x)))
+
+
+def kv_write_fp8(k_cache: np.ndarray, v_cache: np.ndarray, k_new, v_new, slot_mapping,
+                 k_scale: float, v_scale: float, lib=None) -> None:
+    """In place on uint8 caches: code = E4M3(bf16 / scale) at each slot."""
+    lib = lib or load()
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    NB, Hkv, bs, D = k_cache.shape
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = slots.shape[0]
+    _check(lib.oracle_kv_write_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                   _ptr(slots), T, NB, Hkv, D, bs, float(k_scale),
+                                   float(v_scale)), "oracle_kv_write_fp8")
+
+
+def block_copy_fp8(k_cache: np.ndarray, v_cache: np.ndarray, pairs, lib=None) -> None:
+    lib = lib or load()
+    NB, Hkv, bs, D = k_cache.shape
+    pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    _check(lib.oracle_block_copy_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0],
+                                     NB, Hkv, D, bs), "oracle_block_copy_fp8")
+
+
+def attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                  k_scale: float, v_scale: float, sel=None, nthreads: int = 1,
+                  lib=None) -> np.ndarray:
+    """fp64 decode attention over an E4M3 cache (element = decode(code) * scale)."""
+    lib = lib or load()
+    q = _u16(q)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    MB = bt.shape[1]
+    if sel is None:
+        out = np.empty((S, Hq, D), dtype=np.float64)
+        sel_p, nsel = None, 0
+    else:
+        sel_a = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((sel_a.shape[0], D), dtype=np.float64)
+        sel_p, nsel = _ptr(sel_a), sel_a.shape[0]
+    _check(lib.oracle_attention_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
+                                    _ptr(ctx), S, MB, Hq, Hkv, D, bs, NB, float(scale),
+                                    float(k_scale), float(v_scale), sel_p, nsel, int(nthreads)),
+           "oracle_attention_fp8")
+    return out

@@ -201,3 +201,171 @@ int oracle_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
 int64_t oracle_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int bytes_per_elem) {
     return (int64_t)2 * layers * kv_heads * head_dim * bytes_per_elem;
 }
+
+/* ------------------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache.  "Continuous batching and PagedAttention", section 4 (vLLM's
+ * kv_cache_dtype="fp8" option) and "Inference optimization", exercise 1 (quantised KV
+ * caches hold more concurrent requests).  The pages name the format only; the codec
+ * below follows the OCP 8-bit floating point E4M3 definition: 1 sign bit, 4 exponent
+ * bits (bias 7), 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite
+ * value 448.  Rounding is to nearest, ties to even; a finite value beyond 448 saturates
+ * to +-448 (the "satfinite" convention).  A cache element holds
+ * code = E4M3(bf16_value / scale), the division taken in fp32, and stands for
+ * decode(code) * scale.
+ * ------------------------------------------------------------------------------------ */
+double oracle_e4m3_decode(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);            /* a = f * 2^e2, f in [0.5, 1): a = 1.xxx * 2^(e2 - 1) */
+    int E = e2 - 1;
+    if (E < -6) E = -6;       /* subnormal range shares the spacing of 2^-6 */
+    const double spacing = ldexp(1.0, E - 3);
+    const double r = rint(a / spacing); /* default rounding mode: nearest, ties to even */
+    const double v = r * spacing;
+    if (v >= 448.0) return sign | 0x7E;
+    if (v == 0.0) return sign;
+    if (v < ldexp(1.0, -6)) return sign | (uint8_t)(v / ldexp(1.0, -9));
+    int ev;
+    frexp(v, &ev);
+    const int Ev = ev - 1;
+    const int mant = (int)((v / ldexp(1.0, Ev) - 1.0) * 8.0);
+    return sign | (uint8_t)(((Ev + 7) << 3) | mant);
+}
+
+int oracle_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
+                        const uint16_t *v_new, const int64_t *slot_mapping, int num_tokens,
+                        int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                        float k_scale, float v_scale) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return -1;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return -2;
+        int64_t block = slot / block_size, offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t dst = (((size_t)block * num_kv_heads + h) * block_size + offset) * head_dim;
+            size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                float kx = (float)bf16_to_f64(k_new[src + d]);
+                float vx = (float)bf16_to_f64(v_new[src + d]);
+                k_cache[dst + d] = oracle_e4m3_encode(kx / k_scale);
+                v_cache[dst + d] = oracle_e4m3_encode(vx / v_scale);
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pairs, int num_pairs,
+                          int num_blocks, int num_kv_heads, int head_dim, int block_size) {
+    if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return -1;
+    const size_t block_elems = (size_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < num_pairs; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return -2;
+        memcpy(k_cache + (size_t)dst * block_elems, k_cache + (size_t)src * block_elems, block_elems);
+        memcpy(v_cache + (size_t)dst * block_elems, v_cache + (size_t)src * block_elems, block_elems);
+    }
+    return 0;
+}
+
+/* Decode attention over an E4M3 cache: every element is decode(code) * scale in fp64;
+ * the rest is the same textbook softmax as oracle_attention. */
+int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
+                         const uint8_t *v_cache, const int32_t *block_tables,
+                         const int32_t *context_lens, int num_seqs, int max_blocks,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, double scale, double k_scale, double v_scale,
+                         const int32_t *sel, int nsel, int nthreads) {
+    if (num_seqs < 0 || max_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    const int npairs = sel ? nsel : num_seqs * num_q_heads;
+    const int group = num_q_heads / num_kv_heads;
+    int max_ctx = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (context_lens[s] < 0) return -1;
+        if (context_lens[s] > max_ctx) max_ctx = context_lens[s];
+    }
+    if (nthreads <= 0) nthreads = 1;
+    int status = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        size_t n = (size_t)(max_ctx > 0 ? max_ctx : 1);
+        double *kc = (double *)malloc(n * head_dim * sizeof(double));
+        double *vc = (double *)malloc(n * head_dim * sizeof(double));
+        double *x = (double *)malloc(n * sizeof(double));
+        int local = (kc && vc && x) ? 0 : -3;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < npairs; ++i) {
+            if (local) continue;
+            int s = sel ? sel[2 * i] : i / num_q_heads;
+            int h = sel ? sel[2 * i + 1] : i % num_q_heads;
+            if (s < 0 || s >= num_seqs || h < 0 || h >= num_q_heads) { local = -2; continue; }
+            const int ctx = context_lens[s], kv_head = h / group;
+            const int32_t *table = block_tables + (size_t)s * max_blocks;
+            double *o = out + (size_t)i * head_dim;
+            const uint16_t *qh = q + ((size_t)s * num_q_heads + h) * head_dim;
+            if (ctx > max_blocks * block_size) { local = -2; continue; }
+            int bad = 0;
+            for (int t = 0; t < ctx && !bad; ++t) {
+                int32_t block = table[t / block_size];
+                if (block < 0 || block >= num_blocks) { bad = 1; break; }
+                size_t row = (((size_t)block * num_kv_heads + kv_head) * block_size +
+                              t % block_size) * head_dim;
+                for (int d = 0; d < head_dim; ++d) {
+                    kc[(size_t)t * head_dim + d] = oracle_e4m3_decode(k_cache[row + d]) * k_scale;
+                    vc[(size_t)t * head_dim + d] = oracle_e4m3_decode(v_cache[row + d]) * v_scale;
+                }
+            }
+            if (bad) { local = -2; continue; }
+            if (ctx == 0) {
+                for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int t = 0; t < ctx; ++t) {
+                double acc = 0.0;
+                for (int d = 0; d < head_dim; ++d) acc += bf16_to_f64(qh[d]) * kc[(size_t)t * head_dim + d];
+                x[t] = scale * acc;
+                if (x[t] > m) m = x[t];
+            }
+            double denom = 0.0;
+            for (int t = 0; t < ctx; ++t) {
+                x[t] = exp(x[t] - m);
+                denom += x[t];
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int t = 0; t < ctx; ++t) acc += x[t] * vc[(size_t)t * head_dim + d];
+                o[d] = acc / denom;
+            }
+        }
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+        if (local && !status) status = local;
+        free(kc);
+        free(vc);
+        free(x);
+    }
+    return status;
+}

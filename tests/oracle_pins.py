@@ -393,3 +393,149 @@ ALL_PINS = [
     pin_shared_prefix_equals_private, pin_write_matches_kvcache_update, pin_write_bytes,
     pin_copy_bytes,
 ]
+
+
+# -------------------------------------------------------------------------------------
+# FP8 (E4M3) cache
+# -------------------------------------------------------------------------------------
+def pin_quant_capacity(lib):
+    """The byte formula is linear in the element width: at the same memory an fp8 cache
+    holds 2x the tokens of a 16-bit one and an int4 cache about 4x (the pages' figures).
+    The width argument is given in bits here, so the ratio is width-independent."""
+    for (fmt, bits, gain), cite in _rows(os.path.join(GOLDEN, "kv_quant_capacity.txt")):
+        b16 = oracle.kv_bytes_per_token(80, 8, 128, 16, lib=lib)
+        bq = oracle.kv_bytes_per_token(80, 8, 128, int(bits), lib=lib)
+        assert b16 / bq == float(gain), (fmt, cite)
+
+
+def pin_e4m3_table(lib):
+    for (code, value), what in _rows(os.path.join(GOLDEN, "e4m3_codes.txt")):
+        got = oracle.e4m3_decode(int(code, 16), lib=lib)
+        if value == "nan":
+            assert math.isnan(got), what
+        else:
+            assert got == float(value) and math.copysign(1, got) == math.copysign(1, float(value)), \
+                (code, got, what)
+
+
+def _grid():
+    vals = []
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        v = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        vals.append((s * v, c))
+    return vals
+
+
+def pin_e4m3_nearest(lib):
+    """Every code decodes to its grid value and encodes back; random floats encode to
+    the nearest grid value (ties to the even mantissa); beyond 448 saturates.  The grid
+    here is enumerated independently of the oracle's codec."""
+    grid = _grid()
+    for v, c in grid:
+        assert oracle.e4m3_decode(c, lib=lib) == v
+        if v != 0 or c in (0x00, 0x80):
+            assert oracle.e4m3_encode(v, lib=lib) == c, (v, c)
+    finite = sorted({v for v, c in grid})
+    rng = np.random.default_rng(23)
+    xs = np.concatenate([rng.uniform(-500, 500, 4000), rng.uniform(-0.05, 0.05, 4000),
+                         rng.standard_normal(4000) * 3]).astype(np.float32)
+    # exact midpoints between neighbours, to exercise ties
+    mids = [(a + b) / 2 for a, b in zip(finite[:-1], finite[1:])]
+    xs = np.concatenate([xs, np.asarray(mids, np.float32)])
+    for x in xs:
+        x = float(x)
+        code = oracle.e4m3_encode(x, lib=lib)
+        got = oracle.e4m3_decode(code, lib=lib)
+        if abs(x) > 448:
+            assert got == math.copysign(448.0, x), x
+            continue
+        best = min(abs(x - v) for v in finite)
+        cands = [c for v, c in grid if abs(x - v) == best]
+        if len(cands) > 1:  # a tie: the even mantissa wins (signed zeros aside)
+            cands = [c for c in cands if (c & 1) == 0 and (c & 0x7F) != 0 or
+                     (c & 0x7F) == 0 and math.copysign(1, x) == (-1 if c & 0x80 else 1)]
+        assert abs(got - x) == best and code in cands, (x, code, got, cands)
+
+
+def _fp8_workload(seed, ctx, Hq=8, Hkv=2, D=128, **kw):
+    w = workloads.build("fp8", ctx, Hq, Hkv, D, seed=seed, **kw)
+    return w
+
+
+def pin_fp8_write(lib):
+    """The written byte is E4M3(bf16 / scale) (division in fp32), slots skipped when
+    negative, everything else untouched; the stored value is within half a grid step."""
+    NB, Hkv, D = 6, 2, 128
+    rng = np.random.default_rng(29)
+    k = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    v = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    k0, v0 = k.copy(), v.copy()
+    gen = torch.Generator().manual_seed(31)
+    newk = (torch.randn(3, Hkv, D, generator=gen) * 40).to(torch.bfloat16)
+    newv = (torch.randn(3, Hkv, D, generator=gen) * 0.01).to(torch.bfloat16)
+    ks, vs = 0.37, 0.0021
+    slots = [4 * BS + 9, -1, 1 * BS + 0]
+    oracle.kv_write_fp8(k, v, newk, newv, slots, ks, vs, lib=lib)
+    for t, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        b, o = slot // BS, slot % BS
+        for h in range(Hkv):
+            for d in range(D):
+                xk = float(np.float32(float(newk[t, h, d])) / np.float32(ks))
+                xv = float(np.float32(float(newv[t, h, d])) / np.float32(vs))
+                k0[b, h, o, d] = oracle.e4m3_encode(xk, lib=lib)
+                v0[b, h, o, d] = oracle.e4m3_encode(xv, lib=lib)
+                dk = oracle.e4m3_decode(int(k0[b, h, o, d]), lib=lib)
+                if abs(xk) <= 448:
+                    assert abs(dk - xk) <= max(abs(xk) / 16, 2.0 ** -10)
+    assert np.array_equal(k, k0) and np.array_equal(v, v0)
+
+
+def pin_fp8_attention_equals_bf16(lib):
+    """With power-of-two scales every decoded element is a bf16 value, so attention over
+    the E4M3 cache equals the pinned bf16 oracle over those values, bit for bit."""
+    w = _fp8_workload(37, [1, 5, 16, 33, 70], poison=False)
+    out16, k16, v16 = run_step(w, lib)
+    kq = np.zeros(k16.shape, np.uint8)
+    vq = np.zeros(v16.shape, np.uint8)
+    ks, vs = 0.25, 2.0
+    oracle.kv_write_fp8(kq, vq, _all_rows(k16), _all_rows(v16), np.arange(k16.shape[0] * BS),
+                        ks, vs, lib=lib)
+    dec = np.vectorize(lambda c: oracle.e4m3_decode(int(c), lib=lib))
+    kd = torch.from_numpy(dec(kq) * ks).to(torch.bfloat16)
+    vd = torch.from_numpy(dec(vq) * vs).to(torch.bfloat16)
+    assert torch.equal(kd.double(), torch.from_numpy(dec(kq) * ks))  # exact in bf16
+    ref = oracle.attention(w.q, kd, vd, w.block_tables, w.context_lens, w.scale, lib=lib)
+    got = oracle.attention_fp8(w.q, kq, vq, w.block_tables, w.context_lens, w.scale, ks, vs,
+                               lib=lib)
+    assert np.array_equal(ref, got)
+
+
+def _all_rows(cache_u16):
+    """[NB][Hkv][16][D] uint16 -> [NB*16][Hkv][D] rows in slot order (for a full write)."""
+    NB, Hkv, bs, D = cache_u16.shape
+    return np.ascontiguousarray(cache_u16.transpose(0, 2, 1, 3).reshape(NB * bs, Hkv, D))
+
+
+def pin_fp8_copy(lib):
+    NB, Hkv, D = 8, 2, 128
+    rng = np.random.default_rng(41)
+    k = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    v = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
+    k0, v0 = k.copy(), v.copy()
+    pairs = [(1, 6), (4, 2)]
+    oracle.block_copy_fp8(k, v, pairs, lib=lib)
+    for s, d in pairs:
+        k0[d] = k0[s]
+        v0[d] = v0[s]
+    assert np.array_equal(k, k0) and np.array_equal(v, v0)
+
+
+FP8_PINS = [pin_quant_capacity, pin_e4m3_table, pin_e4m3_nearest, pin_fp8_write,
+            pin_fp8_attention_equals_bf16, pin_fp8_copy]
+ALL_PINS = ALL_PINS + FP8_PINS
