@@ -159,22 +159,44 @@ def job_throughput(bytes_per_rank_step: int, steps: int, rank_ms: float, world: 
 # -------------------------------------------------------------------------------------
 # CPU oracle baseline (a bounded sample of the same workload)
 # -------------------------------------------------------------------------------------
+FP8_K_SCALE, FP8_V_SCALE = 0.02, 0.015  # N(0,1) data stays well inside E4M3's +-448
+
+
 def oracle_sample_step(w, n_seqs: int, nthreads: int, k_host, v_host):
     import oracle
     sub_bt = np.ascontiguousarray(w.block_tables[:n_seqs])
     sub_ctx = np.ascontiguousarray(w.context_lens[:n_seqs])
     q = w.q[:n_seqs].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
-    oracle.attention(q, k_host, v_host, sub_bt, sub_ctx, w.scale, nthreads=nthreads)
+    if k_host.dtype == np.uint8:
+        oracle.attention_fp8(q, k_host, v_host, sub_bt, sub_ctx, w.scale, FP8_K_SCALE,
+                             FP8_V_SCALE, nthreads=nthreads)
+    else:
+        oracle.attention(q, k_host, v_host, sub_bt, sub_ctx, w.scale, nthreads=nthreads)
     return time.perf_counter() - t0, int(sub_ctx.astype(np.int64).sum())
 
 
-def cpu_baseline(w, budget_s: float = 12.0):
+def host_caches(w, fp8: bool):
+    """The oracle's copy of the pre-step cache (E4M3 codes quantised by the oracle)."""
+    import oracle
+    k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    v_host = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    if not fp8:
+        return k_host, v_host
+    NB, Hkv, bs, D = k_host.shape
+    rows = lambda c: np.ascontiguousarray(c.transpose(0, 2, 1, 3).reshape(NB * bs, Hkv, D))
+    kq = np.zeros((NB, Hkv, bs, D), np.uint8)
+    vq = np.zeros_like(kq)
+    oracle.kv_write_fp8(kq, vq, rows(k_host), rows(v_host), np.arange(NB * bs), FP8_K_SCALE,
+                        FP8_V_SCALE)
+    return kq, vq
+
+
+def cpu_baseline(w, budget_s: float = 12.0, fp8: bool = False):
     """Time the oracle, as it stands, on all host cores over the first sequences of the
     workload, growing the sample until it takes about budget_s / 3, then once more."""
     nthreads = os.cpu_count() or 1
-    k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    v_host = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    k_host, v_host = host_caches(w, fp8)
     n = min(w.num_seqs, 2)
     while True:
         dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
@@ -185,7 +207,7 @@ def cpu_baseline(w, budget_s: float = 12.0):
     while reps == 0 or dt < budget_s / 3:  # repeat short samples for a stable time
         d, t = oracle_sample_step(w, n, nthreads, k_host, v_host)
         reps, dt, tok = reps + 1, dt + d, tok + t
-    kv_bytes = tok * 2 * w.num_kv_heads * w.head_dim * 2
+    kv_bytes = tok * 2 * w.num_kv_heads * w.head_dim * (1 if fp8 else 2)
     return {"value": kv_bytes / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"first {n} of {w.num_seqs} sequences, all {w.num_q_heads} query heads, "
                       f"{tok // reps} context tokens, {reps} repetitions; fp64 C oracle, "
@@ -246,8 +268,20 @@ def run_ours(args):
 
     w = workloads.make_config(args.config, device="cuda")
     S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
-    k = w.k_cache.to(dev).contiguous()
-    v = w.v_cache.to(dev).contiguous()
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        # Quantise the whole pre-step cache once (untimed) with the library's own write.
+        NB = w.num_blocks
+        k = torch.empty(NB, Hkv, 16, D, dtype=torch.uint8, device=dev)
+        v = torch.empty_like(k)
+        rows = lambda c: c.permute(0, 2, 1, 3).reshape(NB * 16, Hkv, D).contiguous()
+        ops.paged_kv_write_fp8(rows(w.k_cache), rows(w.v_cache),
+                               torch.arange(NB * 16, dtype=torch.int64, device=dev), k, v,
+                               FP8_K_SCALE, FP8_V_SCALE)
+        torch.cuda.synchronize()
+    else:
+        k = w.k_cache.to(dev).contiguous()
+        v = w.v_cache.to(dev).contiguous()
     q = w.q.to(dev).contiguous()
     k_new, v_new = w.k_new.to(dev).contiguous(), w.v_new.to(dev).contiguous()
     slots = torch.as_tensor(w.slot_mapping, dtype=torch.int64, device=dev)
@@ -260,19 +294,37 @@ def run_ours(args):
     ws = ops.alloc_workspace(S, Hq, D, mcl, P, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    kv_bytes = workloads.kv_read_bytes(w)
+    kv_bytes = workloads.kv_read_bytes(w) // (2 if fp8 else 1)
     max_parts = (mcl + P - 1) // P
     launches_per_step = (1 if pairs.numel() else 0) + 1 + 2 + (1 if max_parts > 1 else 0)
     working_set = kv_bytes + q.numel() * 2 * 2
     flush = working_set < 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
+    def do_copy(pr):
+        (ops.paged_block_copy_fp8 if fp8 else ops.paged_block_copy)(k, v, pr, err_flag=err,
+                                                                     stream=stream)
+
+    def do_write(kn, vn, sl):
+        if fp8:
+            ops.paged_kv_write_fp8(kn, vn, sl, k, v, FP8_K_SCALE, FP8_V_SCALE, err_flag=err,
+                                   stream=stream)
+        else:
+            ops.paged_kv_write(kn, vn, sl, k, v, err_flag=err, stream=stream)
+
+    def do_attn(qq, btt, cx):
+        if fp8:
+            ops.paged_attention_decode_fp8(out, qq, k, v, btt, cx, w.scale, FP8_K_SCALE,
+                                           FP8_V_SCALE, mcl, ws, P, err_flag=err, stream=stream)
+        else:
+            ops.paged_attention_decode(out, qq, k, v, btt, cx, w.scale, mcl, ws, P, err_flag=err,
+                                       stream=stream)
+
     def step():
         if pairs.numel():
-            ops.paged_block_copy(k, v, pairs, err_flag=err, stream=stream)
-        ops.paged_kv_write(k_new, v_new, slots, k, v, err_flag=err, stream=stream)
-        ops.paged_attention_decode(out, q, k, v, bt, ctx, w.scale, mcl, ws, P, err_flag=err,
-                                   stream=stream)
+            do_copy(pairs)
+        do_write(k_new, v_new, slots)
+        do_attn(q, bt, ctx)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -295,11 +347,10 @@ def run_ours(args):
             e0, e1, e2 = ev[i]
             e0.record(stream)
             if pairs.numel():
-                ops.paged_block_copy(k, v, pairs, err_flag=err, stream=stream)
-            ops.paged_kv_write(k_new, v_new, slots, k, v, err_flag=err, stream=stream)
+                do_copy(pairs)
+            do_write(k_new, v_new, slots)
             e1.record(stream)
-            ops.paged_attention_decode(out, q, k, v, bt, ctx, w.scale, mcl, ws, P, err_flag=err,
-                                       stream=stream)
+            do_attn(q, bt, ctx)
             e2.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -333,10 +384,9 @@ def run_ours(args):
         dctx.copy_(h["ctx"], non_blocking=True)
         if dpr.numel():
             dpr.copy_(h["pairs"], non_blocking=True)
-            ops.paged_block_copy(k, v, dpr, err_flag=err, stream=stream)
-        ops.paged_kv_write(dkn, dvn, dsl, k, v, err_flag=err, stream=stream)
-        ops.paged_attention_decode(out, dq, k, v, dbt, dctx, w.scale, mcl, ws, P, err_flag=err,
-                                   stream=stream)
+            do_copy(dpr)
+        do_write(dkn, dvn, dsl)
+        do_attn(dq, dbt, dctx)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -364,13 +414,16 @@ def run_ours(args):
     G = Hq // Hkv
     # the kernel AUTO picks: tensor-core tiles once a KV head serves 4+ query heads
     vname = {1: "fma", 2: "mma"}.get(variant, "mma" if G >= 4 else "fma")
+    if fp8:
+        vname = "mma-fp8"  # the E4M3 cache always runs the tensor-core kernel
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV / f16 tiles" if fp8 else "bf16",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "workload": w.name, "kv_dtype": args.kv_dtype, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
             "head_dim": D, "block_size": w.block_size, "partition_size": P,
             "num_blocks": w.num_blocks, "mean_context": float(w.context_lens.mean()),
             "max_context": mcl, "kv_bytes_per_step": kv_bytes,
@@ -395,7 +448,7 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, fp8=fp8)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -413,6 +466,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition size in tokens (default: the workload's, 512)")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

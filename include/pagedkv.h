@@ -128,6 +128,44 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
                            void *workspace, size_t workspace_bytes, int32_t *err_flag,
                            void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * E4M3 (FP8) KV cache.  "Continuous batching and PagedAttention", section 4: the
+ * kv_cache_dtype="fp8" option doubles the batch a GPU holds; "Inference optimization",
+ * exercise 1: quantised KV caches hold proportionally more concurrent requests.
+ * Format: OCP E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * largest finite 448).  A cache element is one byte, code = E4M3(x / scale) with the
+ * division rounded to nearest in fp32 and the conversion rounded to nearest even with
+ * finite saturation; it stands for decode(code) * scale.  One scale per cache (k_scale,
+ * v_scale, > 0).  Layout as for bf16 with 1-byte elements.
+ * ------------------------------------------------------------------------------------ */
+
+/* Quantise and scatter the step's bf16 K/V into E4M3 caches (otherwise as
+ * paged_kv_write).  head_dim a multiple of 16. */
+int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
+                       int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
+                       int num_kv_heads, int head_dim, int block_size, float k_scale,
+                       float v_scale, int32_t *err_flag, void *stream);
+
+/* Copy-on-write of whole blocks of E4M3 caches (as paged_block_copy, bit-exact). */
+int paged_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *block_pairs,
+                         int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, int32_t *err_flag, void *stream);
+
+/* Decode attention over E4M3 caches: as paged_attention_decode with every K element
+ * decode(code) * k_scale and every V element decode(code) * v_scale.  The scores are
+ * formed on tensor cores in f16 (E4M3 codes convert to f16 exactly; q is rounded
+ * bf16 -> f16, exact for 2^-14 <= |q| <= 65504) with fp32 accumulation; the softmax
+ * weights enter the P.V tile as f16.  head_dim must be 128.  The workspace is the one
+ * paged_attention_workspace_size gives. */
+int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs,
+                               int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, float scale,
+                               float k_scale, float v_scale, int partition_size,
+                               int max_context_len, void *workspace, size_t workspace_bytes,
+                               int32_t *err_flag, void *stream);
+
 /*
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that cannot
  * allocate device memory (no cudaMalloc on their thread, memory owned by another

@@ -250,10 +250,15 @@ int oracle_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_ne
     if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
         return -1;
     const int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int t = 0; t < num_tokens; ++t)
+        if (slot_mapping[t] >= num_slots) return -2;
+    /* tokens are independent (distinct slots), so the loop may run on several threads */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
         if (slot < 0) continue;
-        if (slot >= num_slots) return -2;
         int64_t block = slot / block_size, offset = slot % block_size;
         for (int h = 0; h < num_kv_heads; ++h) {
             size_t dst = (((size_t)block * num_kv_heads + h) * block_size + offset) * head_dim;

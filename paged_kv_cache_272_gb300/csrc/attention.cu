@@ -172,8 +172,8 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
         continue;
       }
       const size_t base = ((size_t)blk * a.num_kv_heads + g) * (size_t)(kBlockSize * D);
-      const uint4 *kp = reinterpret_cast<const uint4 *>(a.k_cache + base);
-      const uint4 *vp = reinterpret_cast<const uint4 *>(a.v_cache + base);
+      const uint4 *kp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.k_cache) + base);
+      const uint4 *vp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.v_cache) + base);
       uint4 kr[NI], vr[NI];
 #pragma unroll
       for (int i = 0; i < NI; ++i) kr[i] = ld_stream_v4(kp + i * 32 + lane);
@@ -511,30 +511,13 @@ int max_parts_for(int max_context_len, int part) {
 }
 }  // namespace
 
-extern "C" {
-
-size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_dim,
-                                      int max_context_len, int partition_size) {
-  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
-  const int part = partition_size > 0 ? partition_size : kDefaultPartition;
-  return attn_workspace_layout(num_seqs, num_q_heads, head_dim,
-                               max_parts_for(max_context_len, part))
-      .total;
-}
-
-int paged_attention_set_variant(int variant) {
-  if (variant != PKV_ATTN_AUTO && variant != PKV_ATTN_FMA && variant != PKV_ATTN_MMA)
-    return PKV_ERR_ARG;
-  return g_variant.exchange(variant);
-}
-
-int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
-                           const uint16_t *v_cache, const int32_t *block_tables,
-                           const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
-                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                           int num_blocks, float scale, int partition_size, int max_context_len,
-                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
-                           void *stream) {
+static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
+                       const void *v_cache, const int32_t *block_tables,
+                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, float scale, int partition_size, int max_context_len,
+                       void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
+                       bool kv8, float k_scale, float v_scale) {
   if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_context_len < 0 || num_q_heads % num_kv_heads != 0 ||
@@ -569,7 +552,9 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   a.num_blocks = num_blocks;
   a.part_tokens = part;
   a.max_parts = max_parts;
-  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.scale_log2 = (float)((double)scale * (kv8 ? (double)k_scale : 1.0) * 1.4426950408889634);
+  a.v_scale = kv8 ? v_scale : 1.0f;
+  a.kv8 = kv8 ? 1 : 0;
   a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
   a.work_next = reinterpret_cast<int32_t *>(wb + ws.work_next_off);
@@ -591,8 +576,9 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
   // the CUDA-core variant for MHA and small groups, where it already streams at the
   // HBM roofline.  The TMA tensor map indexes rows with 32-bit coordinates.
   const bool tma_ok = (int64_t)num_blocks * num_kv_heads * kBlockSize < ((int64_t)1 << 31);
-  const bool use_mma =
-      tma_ok && (variant == PKV_ATTN_MMA || (variant == PKV_ATTN_AUTO && a.group >= 4));
+  const bool use_mma = kv8 || (tma_ok && (variant == PKV_ATTN_MMA ||
+                                          (variant == PKV_ATTN_AUTO && a.group >= 4)));
+  if (kv8 && !tma_ok) return PKV_ERR_SHAPE;
   const int width = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
   a.sub_groups = use_mma ? (a.group + 7) / 8 : (a.group + width - 1) / width;
 
@@ -605,6 +591,53 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
     if (launch_merge(a, head_dim, units, st) != 0) return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+extern "C" {
+
+size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                      int max_context_len, int partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+  return attn_workspace_layout(num_seqs, num_q_heads, head_dim,
+                               max_parts_for(max_context_len, part))
+      .total;
+}
+
+int paged_attention_set_variant(int variant) {
+  if (variant != PKV_ATTN_AUTO && variant != PKV_ATTN_FMA && variant != PKV_ATTN_MMA)
+    return PKV_ERR_ARG;
+  return g_variant.exchange(variant);
+}
+
+
+int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int partition_size, int max_context_len,
+                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                           void *stream) {
+  return decode_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, partition_size, max_context_len, workspace,
+                     workspace_bytes, err_flag, stream, false, 1.0f, 1.0f);
+}
+
+int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs,
+                               int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, float scale,
+                               float k_scale, float v_scale, int partition_size,
+                               int max_context_len, void *workspace, size_t workspace_bytes,
+                               int32_t *err_flag, void *stream) {
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PKV_ERR_SHAPE;
+  return decode_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, partition_size, max_context_len, workspace,
+                     workspace_bytes, err_flag, stream, true, k_scale, v_scale);
 }
 
 }  // extern "C"

@@ -19,8 +19,8 @@ constexpr int kChunk = 32;  // partitions one merge unit combines
 struct AttnArgs {
   uint16_t *out;                 // [S][Hq][D] bf16
   const uint16_t *q;             // [S][Hq][D] bf16
-  const uint16_t *k_cache;       // [NB][Hkv][16][D] bf16
-  const uint16_t *v_cache;
+  const void *k_cache;           // [NB][Hkv][16][D] bf16 (or E4M3 codes when kv8)
+  const void *v_cache;
   const int32_t *block_tables;   // [S][MB]
   const int32_t *context_lens;   // [S]
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, group, num_blocks;
@@ -28,7 +28,9 @@ struct AttnArgs {
   int max_parts;                 // partitions per sequence the workspace holds
   int sub_groups;                // query sub-groups per KV head (group > kernel width)
   int max_chunks;                // ceil(max_parts / kChunk)
-  float scale_log2;              // scale * log2(e): scores live in the base-2 domain
+  float scale_log2;              // scale * log2(e) (* k_scale for an E4M3 cache)
+  float v_scale;                 // multiplies every output (1 for a bf16 cache)
+  int kv8;                       // the caches hold E4M3 codes instead of bf16
   // workspace
   int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]

@@ -27,6 +27,8 @@
 //    memory, and the item's result goes to `out` (one partition) or to the split-K
 //    partials (merged by the LSE merge kernel).
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -134,6 +136,46 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
+// c += A(16x16, row) * B(16x8, col), f16 inputs, fp32 accumulate (E4M3 cache path).
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], uint32_t a0, uint32_t a1,
+                                             uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2, exactly (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+// Byte offset of byte column c of row r in a staged E4M3 tile: [16][128 B] written by TMA
+// with the 128-byte swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t tile8_off(int r, int c) {
+  return (uint32_t)(r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -149,6 +191,31 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col) {
 
 // Q^T as the B operand of S^T = K Q^T for one item: thread (gid, tig) holds
 // q[h0 + gid][16 kk + 2 tig (+8) .. +1] as bf16 pairs (zero for heads past the group).
+// For the E4M3 cache the head_dim index inside each 16-wide k-step is permuted so that a
+// thread's four K elements are four consecutive bytes: logical k = 2 tig + j reads
+// column 16 kk + 4 tig + j and k = 2 tig + 8 + j reads 16 kk + 4 tig + 2 + j.  Q uses
+// the same permutation (a dot product does not depend on the order of its terms), in
+// f16 (bf16 -> f16 is exact for |q| in [2^-14, 65504]; smaller magnitudes keep f16's
+// subnormal precision).
+template <int D>
+__device__ __forceinline__ void load_q_frag_f16perm(uint32_t (&qb)[D / 16][2], const AttnArgs &a,
+                                                    int item, int per_pair, int4 rec, int gid,
+                                                    int tig, bool live) {
+  const int rem = item % per_pair;
+  const int g = rem / a.sub_groups;
+  const int sub = rem - g * a.sub_groups;
+  const int h0 = g * a.group + sub * 8;
+  const bool on = live && gid < min(8, a.group - sub * 8);
+  const uint2 *qrow =
+      reinterpret_cast<const uint2 *>(a.q + ((size_t)rec.x * a.num_q_heads + h0 + gid) * D);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint2 w = on ? qrow[(16 * kk + 4 * tig) >> 2] : make_uint2(0u, 0u);
+    qb[kk][0] = pack_f16(bf16_lo(w.x), bf16_hi(w.x));
+    qb[kk][1] = pack_f16(bf16_lo(w.y), bf16_hi(w.y));
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void load_q_frag(uint32_t (&qb)[D / 16][2], const AttnArgs &a,
                                             int item, int per_pair, int4 rec, int gid, int tig,
@@ -167,9 +234,9 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qb)[D / 16][2], const Att
   }
 }
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool KV8 = false>
 struct MmaLayout {
-  static constexpr int kTile = kBlockSize * D * 2;   // bytes of one K (or V) head tile
+  static constexpr int kTile = kBlockSize * D * (KV8 ? 1 : 2);  // one K (or V) head tile
   static constexpr int kStage = 2 * kTile;
   static constexpr int kRow = D + 4;                 // padded merge row (floats)
   static constexpr int kRing = 4;                    // item slots producer -> consumers
@@ -181,11 +248,11 @@ struct MmaLayout {
   static constexpr int kSmem = 1024 + kStagesBytes + kMergeBytes + kCtlBytes;
 };
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool KV8>
 __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (NW <= 4 ? 2 : 1)))
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
-  using L = MmaLayout<D, NW, NS>;
+  using L = MmaLayout<D, NW, NS, KV8>;
   constexpr int KSTEPS = D / 16;
   constexpr int HALVES = D / 64;
   extern __shared__ unsigned char smem_raw[];
@@ -292,10 +359,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
                 mbar_arrive_expect_tx(fb, L::kStage);
                 const uint32_t dst = base_u32 + (uint32_t)((lane * NS + slot) * L::kStage);
                 const int y = (b * a.num_kv_heads + g) * kBlockSize;
+                if constexpr (KV8) {  // one [16][128 B] box per tile
+                  tma_load_2d(dst, &tk, 0, y, fb);
+                  tma_load_2d(dst + L::kTile, &tv, 0, y, fb);
+                } else {
 #pragma unroll
-                for (int h = 0; h < HALVES; ++h) {
-                  tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
-                  tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                  for (int h = 0; h < HALVES; ++h) {
+                    tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
+                    tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                  }
                 }
               }
               ++cnt;
@@ -347,7 +419,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
   int cur = *cons_item;
   int4 rec = make_int4(cons_rec->x, cons_rec->y, cons_rec->z, cons_rec->w);
   uint32_t qb[KSTEPS][2];
-  load_q_frag<D>(qb, a, cur < total ? cur : 0, per_pair, rec, gid, tig, cur < total);
+  if constexpr (KV8)
+    load_q_frag_f16perm<D>(qb, a, cur < total ? cur : 0, per_pair, rec, gid, tig, cur < total);
+  else
+    load_q_frag<D>(qb, a, cur < total ? cur : 0, per_pair, rec, gid, tig, cur < total);
   asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // cons_* read by all
   for (int k = 0; cur < total; ++k) {
     const int rem = cur % per_pair;
@@ -379,17 +454,32 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
           // Rows past the end of the context may hold anything (even NaN): zero them in
           // V so that their zero weights contribute exactly nothing.
           unsigned char *vrow = base + (vst - base_u32);
-          const int nz = (kBlockSize - nvalid) * (D / 8);
-          for (int i = lane; i < nz; i += 32) {
-            const int row = nvalid + i / (D / 8), ch = i % (D / 8);
-            *reinterpret_cast<uint4 *>(vrow + (ch >> 3) * 2048 + row * 128 + (ch & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
+          if constexpr (KV8) {  // rows of 128 bytes
+            for (int i = lane; i < (kBlockSize - nvalid) * 8; i += 32)
+              *reinterpret_cast<uint4 *>(vrow + (nvalid + i / 8) * 128 + (i % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          } else {
+            const int nz = (kBlockSize - nvalid) * (D / 8);
+            for (int i = lane; i < nz; i += 32) {
+              const int row = nvalid + i / (D / 8), ch = i % (D / 8);
+              *reinterpret_cast<uint4 *>(vrow + (ch >> 3) * 2048 + row * 128 + (ch & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
           }
           __syncwarp();
         }
         // S^T = K Q^T  (rows: tokens gid, gid + 8; columns: heads 2 tig, 2 tig + 1)
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        {
+        if constexpr (KV8) {
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t w0 = lds32(kst + tile8_off(gid, 16 * kk + 4 * tig));
+            const uint32_t w1 = lds32(kst + tile8_off(gid + 8, 16 * kk + 4 * tig));
+            mma16816_f16(sc, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
+                         e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), qb[kk][0],
+                         qb[kk][1]);
+          }
+        } else {
           const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -412,10 +502,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
         m0 = n0;
         m1 = n1;
-        const uint32_t p01 = pack_bf16(exp2f(x0 - m0), exp2f(x1 - m1));
-        const uint32_t p23 = pack_bf16(exp2f(x2 - m0), exp2f(x3 - m1));
-        l0 = fmaf(l0, al0, bf16_lo(p01) + bf16_lo(p23));
-        l1 = fmaf(l1, al1, bf16_hi(p01) + bf16_hi(p23));
+        uint32_t p01, p23;
+        if constexpr (KV8) {
+          p01 = pack_f16(exp2f(x0 - m0), exp2f(x1 - m1));
+          p23 = pack_f16(exp2f(x2 - m0), exp2f(x3 - m1));
+          l0 = fmaf(l0, al0, f16_lo(p01) + f16_lo(p23));
+          l1 = fmaf(l1, al1, f16_hi(p01) + f16_hi(p23));
+        } else {
+          p01 = pack_bf16(exp2f(x0 - m0), exp2f(x1 - m1));
+          p23 = pack_bf16(exp2f(x2 - m0), exp2f(x3 - m1));
+          l0 = fmaf(l0, al0, bf16_lo(p01) + bf16_lo(p23));
+          l1 = fmaf(l1, al1, bf16_hi(p01) + bf16_hi(p23));
+        }
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) {
           acc[mt][0] *= al0;
@@ -425,7 +523,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         }
         // P^T as the B operand of O^T += V^T P^T.
         const uint32_t b0 = movmatrix_t(p01), b1 = movmatrix_t(p23);
-        {
+        if constexpr (KV8) {
+          // V^T fragments: 4 consecutive bytes of token rows gid and gid + 8 (columns
+          // 16 mt + 4 tig ..), converted to f16 and transposed 8x8 by movmatrix.  Output
+          // row L of the m-tile is head_dim column 16 mt + 4 (L & 7) / 2 ... (see merge).
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            const uint32_t w0 = lds32(vst + tile8_off(gid, 16 * mt + 4 * tig));
+            const uint32_t w1 = lds32(vst + tile8_off(gid + 8, 16 * mt + 4 * tig));
+            const uint32_t a0 = movmatrix_t(e4m3x2_to_f16x2(w0 & 0xffffu));
+            const uint32_t a1 = movmatrix_t(e4m3x2_to_f16x2(w0 >> 16));
+            const uint32_t a2 = movmatrix_t(e4m3x2_to_f16x2(w1 & 0xffffu));
+            const uint32_t a3 = movmatrix_t(e4m3x2_to_f16x2(w1 >> 16));
+            mma16816_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+          }
+        } else {
           const int j4 = lane >> 3;
           const int tok = (lane & 7) + ((j4 >> 1) << 3);
 #pragma unroll
@@ -456,12 +568,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     }
     {
       float *ro = red_o + warp * 8 * L::kRow;
+      // Accumulator rows gid and gid + 8 of m-tile mt are head_dim columns d0 and d1.
+      const int d0 = KV8 ? 4 * (gid >> 1) + (gid & 1) : gid;
+      const int d1 = KV8 ? d0 + 2 : gid + 8;
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
-        ro[(2 * tig) * L::kRow + 16 * mt + gid] = acc[mt][0];
-        ro[(2 * tig + 1) * L::kRow + 16 * mt + gid] = acc[mt][1];
-        ro[(2 * tig) * L::kRow + 16 * mt + gid + 8] = acc[mt][2];
-        ro[(2 * tig + 1) * L::kRow + 16 * mt + gid + 8] = acc[mt][3];
+        ro[(2 * tig) * L::kRow + 16 * mt + d0] = acc[mt][0];
+        ro[(2 * tig + 1) * L::kRow + 16 * mt + d0] = acc[mt][1];
+        ro[(2 * tig) * L::kRow + 16 * mt + d1] = acc[mt][2];
+        ro[(2 * tig + 1) * L::kRow + 16 * mt + d1] = acc[mt][3];
       }
     }
     if (threadIdx.x == 0) fetch(k + 1);
@@ -470,7 +585,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     const int nxt = *cons_item;
     const int4 rec_n = make_int4(cons_rec->x, cons_rec->y, cons_rec->z, cons_rec->w);
     uint32_t qn[KSTEPS][2];
-    load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
+    if constexpr (KV8)
+      load_q_frag_f16perm<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
+    else
+      load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
     const bool single = rec.w == 1;
     const int p = t0 / a.part_tokens;
     for (int i = threadIdx.x; i < gcnt * D; i += NW * 32) {
@@ -486,11 +604,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         O = fmaf(red_o[(w * 8 + j) * L::kRow + d], c, O);
       }
       const int h = h0 + j;
+      const float o = O / Lsum * a.v_scale;  // v_scale is 1 for a bf16 cache
       if (single) {
-        a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(O / Lsum);
+        a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(o);
       } else {
         const size_t idx = ((size_t)s * a.max_parts + p) * a.num_q_heads + h;
-        a.part_o[idx * D + d] = O / Lsum;
+        a.part_o[idx * D + d] = o;
         if (d == 0) a.part_lse[idx] = M + log2f(Lsum);
       }
     }
@@ -524,14 +643,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // The cache viewed as a 2-D tensor [num_blocks * Hkv * 16 rows][head_dim], boxes of
 // 16 rows x 64 columns (128 bytes) with the 128-byte swizzle.
-bool encode_kv_map(CUtensorMap *m, const void *base, uint64_t rows, int D) {
+// elem = 2 (bf16) or 1 (E4M3 codes): boxes of 16 rows x 128 bytes either way.
+bool encode_kv_map(CUtensorMap *m, const void *base, uint64_t rows, int D, int elem) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  cuuint64_t strides[1] = {(cuuint64_t)D * elem};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)kBlockSize};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+  return fn(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -540,27 +661,28 @@ struct MapCache {
   struct Entry {
     const void *base;
     uint64_t rows;
-    int D;
+    int D, elem;
     CUtensorMap map;
   };
   std::mutex mu;
   Entry e[8];
   int n = 0, next = 0;
-  bool get(const void *base, uint64_t rows, int D, CUtensorMap *out) {
+  bool get(const void *base, uint64_t rows, int D, int elem, CUtensorMap *out) {
     std::lock_guard<std::mutex> g(mu);
     for (int i = 0; i < n; ++i)
-      if (e[i].base == base && e[i].rows == rows && e[i].D == D) {
+      if (e[i].base == base && e[i].rows == rows && e[i].D == D && e[i].elem == elem) {
         *out = e[i].map;
         return true;
       }
     CUtensorMap m;
-    if (!encode_kv_map(&m, base, rows, D)) return false;
+    if (!encode_kv_map(&m, base, rows, D, elem)) return false;
     Entry &slot = e[next];
     next = (next + 1) % 8;
     if (n < 8) ++n;
     slot.base = base;
     slot.rows = rows;
     slot.D = D;
+    slot.elem = elem;
     slot.map = m;
     *out = m;
     return true;
@@ -568,20 +690,20 @@ struct MapCache {
 };
 MapCache g_maps;
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool KV8 = false>
 int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                  cudaStream_t st) {
-  using L = MmaLayout<D, NW, NS>;
+  using L = MmaLayout<D, NW, NS, KV8>;
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(
-        attn_mma_kernel<D, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        attn_mma_kernel<D, NW, NS, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
   static int occ = 0;
   if (!occ) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_mma_kernel<D, NW, NS>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_mma_kernel<D, NW, NS, KV8>,
                                                       (NW + 1) * 32, L::kSmem) != cudaSuccess ||
         occ < 1)
       occ = 1;
@@ -590,7 +712,7 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
   int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  return (int)launch_pdl(attn_mma_kernel<D, NW, NS>, dim3((int)grid), dim3((NW + 1) * 32),
+  return (int)launch_pdl(attn_mma_kernel<D, NW, NS, KV8>, dim3((int)grid), dim3((NW + 1) * 32),
                          (size_t)L::kSmem, st, a, tk, tv);
 }
 
@@ -613,9 +735,15 @@ int ring_choice() {
 int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
   const uint64_t rows = (uint64_t)a.num_blocks * a.num_kv_heads * kBlockSize;
   if (rows >= (1ull << 31)) return (int)cudaErrorInvalidValue;
+  const int elem = a.kv8 ? 1 : 2;
   CUtensorMap tk, tv;
-  if (!g_maps.get(a.k_cache, rows, head_dim, &tk) || !g_maps.get(a.v_cache, rows, head_dim, &tv))
+  if (!g_maps.get(a.k_cache, rows, head_dim, elem, &tk) ||
+      !g_maps.get(a.v_cache, rows, head_dim, elem, &tv))
     return (int)cudaErrorInvalidValue;
+  if (a.kv8) {
+    if (head_dim != 128) return (int)cudaErrorInvalidValue;
+    return launch_mma_t<128, 3, 2, true>(a, tk, tv, st);
+  }
   if (head_dim == 64) return launch_mma_t<64, 4, 4>(a, tk, tv, st);
   switch (ring_choice()) {
     case 1: return launch_mma_t<128, 8, 2>(a, tk, tv, st);

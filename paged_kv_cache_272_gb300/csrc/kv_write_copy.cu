@@ -4,6 +4,8 @@
 // bit-exact by construction.  Sources: "Inference optimization", section "KV cache"
 // (append only the new token's K/V) and "Continuous batching and PagedAttention",
 // section 3 (copy-on-write of a shared block when a request diverges).
+#include <cuda_fp8.h>
+
 #include <cstring>
 
 #include "pkv_common.cuh"
@@ -37,6 +39,44 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__
     const int64_t dst = ((block * heads + h) * kBlockSize + offset) * row_vecs + e;
     k_cache[dst] = k_new[i];
     v_cache[dst] = v_new[i];
+  }
+}
+
+// E4M3 write: thread i handles 8 consecutive elements of one (token, KV head) row:
+// code = E4M3(x / scale) with the division rounded to nearest in fp32, then the
+// hardware conversion (round to nearest even, finite saturation).
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float scale) {
+  const float2 lo = make_float2(__fdiv_rn(bf16_lo(w0), scale), __fdiv_rn(bf16_hi(w0), scale));
+  const float2 hi = make_float2(__fdiv_rn(bf16_lo(w1), scale), __fdiv_rn(bf16_hi(w1), scale));
+  const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+  return (a & 0xffffu) | (b << 16);
+}
+
+__global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
+                                    const uint4 *__restrict__ v_new,
+                                    const int64_t *__restrict__ slots, int64_t total, int row_vecs,
+                                    int heads, int64_t num_slots, uint2 *__restrict__ k_cache,
+                                    uint2 *__restrict__ v_cache, float k_scale, float v_scale,
+                                    int32_t *err) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t row = i / row_vecs;  // t * heads + h
+    const int e = (int)(i - row * row_vecs);
+    const int64_t t = row / heads;
+    const int h = (int)(row - t * heads);
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      flag_error(err, PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t dst = (((slot >> 4) * heads + h) * kBlockSize + (slot & 15)) * row_vecs + e;
+    const uint4 kv = k_new[i], vv = v_new[i];
+    k_cache[dst] = make_uint2(quant4(kv.x, kv.y, k_scale), quant4(kv.z, kv.w, k_scale));
+    v_cache[dst] = make_uint2(quant4(vv.x, vv.y, v_scale), quant4(vv.z, vv.w, v_scale));
   }
 }
 
@@ -143,6 +183,54 @@ int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_
   if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_NULL;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
   const int64_t block_vecs = (int64_t)num_kv_heads * kBlockSize * head_dim / 8;
+  const int64_t total = (int64_t)num_pairs * block_vecs;
+  const int threads = 256;
+  const cudaError_t e = launch_pdl(
+      block_copy_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
+      reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), block_pairs, total,
+      block_vecs, num_blocks, err_flag);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
+                       int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
+                       int num_kv_heads, int head_dim, int block_size, float k_scale,
+                       float v_scale, int32_t *err_flag, void *stream) {
+  if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 16 != 0 || !(k_scale > 0.f) || !(v_scale > 0.f))
+    return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ALIGN;
+  const int row_vecs = head_dim / 8;
+  const int64_t total = (int64_t)num_tokens * num_kv_heads * row_vecs;
+  const int threads = 256;
+  const cudaError_t e = launch_pdl(
+      kv_write_fp8_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
+      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
+      slot_mapping, total, row_vecs, num_kv_heads, (int64_t)num_blocks * kBlockSize,
+      reinterpret_cast<uint2 *>(k_cache), reinterpret_cast<uint2 *>(v_cache), k_scale, v_scale,
+      err_flag);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int paged_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *block_pairs,
+                         int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, int32_t *err_flag, void *stream) {
+  if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
+  if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 16 != 0)
+    return PKV_ERR_SHAPE;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_NULL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+  const int64_t block_vecs = (int64_t)num_kv_heads * kBlockSize * head_dim / 16;
   const int64_t total = (int64_t)num_pairs * block_vecs;
   const int threads = 256;
   const cudaError_t e = launch_pdl(

@@ -33,6 +33,10 @@ SIGNATURES = {
     "paged_attention_set_variant": (_I, [_I]),
     "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                             _F, _I, _I, _P, _P]),
+    "paged_kv_write_fp8": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
+    "paged_block_copy_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                        _F, _F, _I, _I, _P, _SZ, _P, _P]),
     "pkv_pool_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_pool_destroy": (None, [_P]),
     "pkv_pool_num_free": (_I, [_P]),
@@ -162,3 +166,57 @@ def set_attention_variant(variant: int) -> int:
     if prev < 0:
         raise PagedKVError(prev, "paged_attention_set_variant")
     return prev
+
+
+# ---- E4M3 (FP8) cache ----------------------------------------------------------------
+def _u8_cuda(name, t):
+    if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous uint8 CUDA tensor (E4M3 codes)")
+
+
+def paged_kv_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                       err_flag=None, stream=None):
+    """Quantise bf16 k_new/v_new [T][Hkv][D] to E4M3 and scatter into uint8 caches."""
+    _bf16_cuda("k_new", k_new)
+    _bf16_cuda("v_new", v_new)
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    NB, Hkv, bs, D = k_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, D) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    check(lib.paged_kv_write_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping.contiguous()), T,
+                                 _ptr(k_cache), _ptr(v_cache), NB, Hkv, D, bs, float(k_scale),
+                                 float(v_scale), _ptr(err_flag), _stream(stream)),
+          "paged_kv_write_fp8")
+
+
+def paged_block_copy_fp8(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    _i32("block_pairs", block_pairs)
+    NB, Hkv, bs, D = k_cache.shape
+    check(lib.paged_block_copy_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
+                                   block_pairs.numel() // 2, NB, Hkv, D, bs, _ptr(err_flag),
+                                   _stream(stream)), "paged_block_copy_fp8")
+
+
+def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                               k_scale, v_scale, max_context_len, workspace,
+                               partition_size=DEFAULT_PARTITION, err_flag=None, stream=None):
+    _bf16_cuda("out", out)
+    _bf16_cuda("q", q)
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    check(lib.paged_attention_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
+        float(k_scale), float(v_scale), int(partition_size), int(max_context_len),
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream)),
+        "paged_attention_decode_fp8")
