@@ -136,7 +136,9 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
  * largest finite 448).  A cache element is one byte, code = E4M3(x / scale) with the
  * division rounded to nearest in fp32 and the conversion rounded to nearest even with
  * finite saturation; it stands for decode(code) * scale.  One scale per cache (k_scale,
- * v_scale, > 0).  Layout as for bf16 with 1-byte elements.
+ * v_scale, > 0).  Layouts: k_cache [num_blocks][num_kv_heads][16][head_dim] like the
+ * bf16 cache; v_cache transposed within each block, [num_blocks][num_kv_heads][head_dim][16]
+ * (so the P.V tile reads consecutive tokens).  Both 16-byte aligned.
  * ------------------------------------------------------------------------------------ */
 
 /* Quantise and scatter the step's bf16 K/V into E4M3 caches (otherwise as

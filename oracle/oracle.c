@@ -212,6 +212,8 @@ int64_t oracle_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int by
  * to +-448 (the "satfinite" convention).  A cache element holds
  * code = E4M3(bf16_value / scale), the division taken in fp32, and stands for
  * decode(code) * scale.
+ * Layouts: K codes [NB][Hkv][block_size][D] like the bf16 cache; V codes transposed
+ * within each block, [NB][Hkv][D][block_size] (an interface choice of the E4M3 cache).
  * ------------------------------------------------------------------------------------ */
 double oracle_e4m3_decode(uint8_t c) {
     const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
@@ -262,12 +264,13 @@ int oracle_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_ne
         int64_t block = slot / block_size, offset = slot % block_size;
         for (int h = 0; h < num_kv_heads; ++h) {
             size_t dst = (((size_t)block * num_kv_heads + h) * block_size + offset) * head_dim;
+            size_t vbase = ((size_t)block * num_kv_heads + h) * head_dim * block_size + offset;
             size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
             for (int d = 0; d < head_dim; ++d) {
                 float kx = (float)bf16_to_f64(k_new[src + d]);
                 float vx = (float)bf16_to_f64(v_new[src + d]);
                 k_cache[dst + d] = oracle_e4m3_encode(kx / k_scale);
-                v_cache[dst + d] = oracle_e4m3_encode(vx / v_scale);
+                v_cache[vbase + (size_t)d * block_size] = oracle_e4m3_encode(vx / v_scale);
             }
         }
     }
@@ -336,9 +339,12 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                 if (block < 0 || block >= num_blocks) { bad = 1; break; }
                 size_t row = (((size_t)block * num_kv_heads + kv_head) * block_size +
                               t % block_size) * head_dim;
+                size_t vcol = ((size_t)block * num_kv_heads + kv_head) * head_dim * block_size +
+                              t % block_size;
                 for (int d = 0; d < head_dim; ++d) {
                     kc[(size_t)t * head_dim + d] = oracle_e4m3_decode(k_cache[row + d]) * k_scale;
-                    vc[(size_t)t * head_dim + d] = oracle_e4m3_decode(v_cache[row + d]) * v_scale;
+                    vc[(size_t)t * head_dim + d] =
+                        oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size]) * v_scale;
                 }
             }
             if (bad) { local = -2; continue; }

@@ -16,6 +16,8 @@
 //    tiles (16 rows x head_dim bf16) into the target warp's ring slot; completion is
 //    signalled on the slot's "full" mbarrier with the byte count.  The consumer frees
 //    the slot through its "empty" mbarrier.  Every wait is bounded.
+//  * (E4M3 cache: K tiles by TMA as above, V tiles -- stored transposed, [d][16] -- by a
+//    plain bulk copy; codes convert to f16 in registers, see the KV8 branches.)
 //  * A consumer computes S^T[16 tokens x 8 heads] = K Q^T with mma.m16n8k16 (tokens are
 //    the M dimension, the query group is N, head_dim is K), so a GQA-8 group fills the
 //    tile exactly; Q^T fragments live in registers for the whole item.  The softmax
@@ -103,6 +105,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both ends 16-byte aligned).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -359,9 +370,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
                 mbar_arrive_expect_tx(fb, L::kStage);
                 const uint32_t dst = base_u32 + (uint32_t)((lane * NS + slot) * L::kStage);
                 const int y = (b * a.num_kv_heads + g) * kBlockSize;
-                if constexpr (KV8) {  // one [16][128 B] box per tile
+                if constexpr (KV8) {
+                  // K: one [16][128 B] swizzled box; V (stored [d][16]): 2 KB contiguous
                   tma_load_2d(dst, &tk, 0, y, fb);
-                  tma_load_2d(dst + L::kTile, &tv, 0, y, fb);
+                  bulk_load(dst + L::kTile,
+                            static_cast<const uint8_t *>(a.v_cache) + (size_t)y * D, L::kTile,
+                            fb);
                 } else {
 #pragma unroll
                   for (int h = 0; h < HALVES; ++h) {
@@ -450,15 +464,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
       const uint32_t kst = base_u32 + (uint32_t)((warp * NS + slot) * L::kStage);
       const uint32_t vst = kst + L::kTile;
       if (valid[warp * NS + slot]) {
-        if (nvalid < kBlockSize) {
+        if (!KV8 && nvalid < kBlockSize) {
           // Rows past the end of the context may hold anything (even NaN): zero them in
-          // V so that their zero weights contribute exactly nothing.
+          // V so that their zero weights contribute exactly nothing.  (The E4M3 path masks
+          // those codes in registers instead.)
           unsigned char *vrow = base + (vst - base_u32);
-          if constexpr (KV8) {  // rows of 128 bytes
-            for (int i = lane; i < (kBlockSize - nvalid) * 8; i += 32)
-              *reinterpret_cast<uint4 *>(vrow + (nvalid + i / 8) * 128 + (i % 8) * 16) =
-                  make_uint4(0, 0, 0, 0);
-          } else {
+          {
             const int nz = (kBlockSize - nvalid) * (D / 8);
             for (int i = lane; i < nz; i += 32) {
               const int row = nvalid + i / (D / 8), ch = i % (D / 8);
@@ -470,11 +481,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         }
         // S^T = K Q^T  (rows: tokens gid, gid + 8; columns: heads 2 tig, 2 tig + 1)
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // E4M3 path: tile row m of S^T holds token tokA (m = gid) / tokB (m = gid + 8), a
+        // token order in which the P.V operand's four k-slots of a thread are four
+        // consecutive tokens (the transposed V codes of one head_dim row).
+        const int tokA = KV8 ? 4 * (gid >> 1) + (gid & 1) : gid;
+        const int tokB = KV8 ? tokA + 2 : gid + 8;
         if constexpr (KV8) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
-            const uint32_t w0 = lds32(kst + tile8_off(gid, 16 * kk + 4 * tig));
-            const uint32_t w1 = lds32(kst + tile8_off(gid + 8, 16 * kk + 4 * tig));
+            const uint32_t w0 = lds32(kst + tile8_off(tokA, 16 * kk + 4 * tig));
+            const uint32_t w1 = lds32(kst + tile8_off(tokB, 16 * kk + 4 * tig));
             mma16816_f16(sc, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
                          e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), qb[kk][0],
                          qb[kk][1]);
@@ -490,8 +506,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         }
         float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
         float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
-        if (gid >= nvalid) x0 = x1 = -INFINITY;
-        if (gid + 8 >= nvalid) x2 = x3 = -INFINITY;
+        if (tokA >= nvalid) x0 = x1 = -INFINITY;
+        if (tokB >= nvalid) x2 = x3 = -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -524,18 +540,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         // P^T as the B operand of O^T += V^T P^T.
         const uint32_t b0 = movmatrix_t(p01), b1 = movmatrix_t(p23);
         if constexpr (KV8) {
-          // V^T fragments: 4 consecutive bytes of token rows gid and gid + 8 (columns
-          // 16 mt + 4 tig ..), converted to f16 and transposed 8x8 by movmatrix.  Output
-          // row L of the m-tile is head_dim column 16 mt + 4 (L & 7) / 2 ... (see merge).
+          // V^T[d][token] fragments straight from the transposed codes: head_dim rows
+          // 16 mt + gid (+8), tokens 4 tig .. 4 tig + 3 = k-slots 2 tig, +1, 2 tig + 8, +9.
+          // Codes of tokens past the end of the context are masked to +0.
+          uint32_t vmask = 0xffffffffu;
+          if (nvalid < kBlockSize) {
+            vmask = 0u;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              if (4 * tig + b < nvalid) vmask |= 0xffu << (8 * b);
+          }
 #pragma unroll
           for (int mt = 0; mt < KSTEPS; ++mt) {
-            const uint32_t w0 = lds32(vst + tile8_off(gid, 16 * mt + 4 * tig));
-            const uint32_t w1 = lds32(vst + tile8_off(gid + 8, 16 * mt + 4 * tig));
-            const uint32_t a0 = movmatrix_t(e4m3x2_to_f16x2(w0 & 0xffffu));
-            const uint32_t a1 = movmatrix_t(e4m3x2_to_f16x2(w0 >> 16));
-            const uint32_t a2 = movmatrix_t(e4m3x2_to_f16x2(w1 & 0xffffu));
-            const uint32_t a3 = movmatrix_t(e4m3x2_to_f16x2(w1 >> 16));
-            mma16816_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+            const uint32_t w0 = lds32(vst + (16 * mt + gid) * 16 + 4 * tig) & vmask;
+            const uint32_t w1 = lds32(vst + (16 * mt + gid + 8) * 16 + 4 * tig) & vmask;
+            mma16816_f16(acc[mt], e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
+                         e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), b0, b1);
           }
         } else {
           const int j4 = lane >> 3;
@@ -547,7 +567,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
             mma16816(acc[mt], a0, a1, a2, a3, b0, b1);
           }
         }
-        if (nvalid < kBlockSize)  // generic writes above, async-proxy (TMA) writes next
+        if (!KV8 && nvalid < kBlockSize)  // generic writes above, async-proxy writes next
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       __syncwarp();
@@ -569,8 +589,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     {
       float *ro = red_o + warp * 8 * L::kRow;
       // Accumulator rows gid and gid + 8 of m-tile mt are head_dim columns d0 and d1.
-      const int d0 = KV8 ? 4 * (gid >> 1) + (gid & 1) : gid;
-      const int d1 = KV8 ? d0 + 2 : gid + 8;
+      const int d0 = gid, d1 = gid + 8;
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         ro[(2 * tig) * L::kRow + 16 * mt + d0] = acc[mt][0];

@@ -53,11 +53,13 @@ __device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float scale
   return (a & 0xffffu) | (b << 16);
 }
 
+// V codes are stored transposed within a block, [block][head][d][offset], so each of the
+// row's 8 V codes is a separate byte store.
 __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
                                     const uint4 *__restrict__ v_new,
                                     const int64_t *__restrict__ slots, int64_t total, int row_vecs,
                                     int heads, int64_t num_slots, uint2 *__restrict__ k_cache,
-                                    uint2 *__restrict__ v_cache, float k_scale, float v_scale,
+                                    uint8_t *__restrict__ v_cache, float k_scale, float v_scale,
                                     int32_t *err) {
   pdl_trigger();
   pdl_wait();
@@ -76,7 +78,14 @@ __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
     const int64_t dst = (((slot >> 4) * heads + h) * kBlockSize + (slot & 15)) * row_vecs + e;
     const uint4 kv = k_new[i], vv = v_new[i];
     k_cache[dst] = make_uint2(quant4(kv.x, kv.y, k_scale), quant4(kv.z, kv.w, k_scale));
-    v_cache[dst] = make_uint2(quant4(vv.x, vv.y, v_scale), quant4(vv.z, vv.w, v_scale));
+    const uint32_t v0 = quant4(vv.x, vv.y, v_scale), v1 = quant4(vv.z, vv.w, v_scale);
+    const int D = row_vecs * 8;
+    uint8_t *vcol = v_cache + (((slot >> 4) * heads + h) * D + e * 8) * kBlockSize + (slot & 15);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      vcol[j * kBlockSize] = (uint8_t)(v0 >> (8 * j));
+      vcol[(4 + j) * kBlockSize] = (uint8_t)(v1 >> (8 * j));
+    }
   }
 }
 
@@ -215,8 +224,7 @@ int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64
       kv_write_fp8_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
       reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
       slot_mapping, total, row_vecs, num_kv_heads, (int64_t)num_blocks * kBlockSize,
-      reinterpret_cast<uint2 *>(k_cache), reinterpret_cast<uint2 *>(v_cache), k_scale, v_scale,
-      err_flag);
+      reinterpret_cast<uint2 *>(k_cache), v_cache, k_scale, v_scale, err_flag);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

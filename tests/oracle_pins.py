@@ -468,7 +468,8 @@ def _fp8_workload(seed, ctx, Hq=8, Hkv=2, D=128, **kw):
 
 def pin_fp8_write(lib):
     """The written byte is E4M3(bf16 / scale) (division in fp32), slots skipped when
-    negative, everything else untouched; the stored value is within half a grid step."""
+    negative, everything else untouched; the stored value is within half a grid step.
+    K codes sit at [block][head][offset][d], V codes at [block][head][d][offset]."""
     NB, Hkv, D = 6, 2, 128
     rng = np.random.default_rng(29)
     k = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
@@ -489,7 +490,7 @@ def pin_fp8_write(lib):
                 xk = float(np.float32(float(newk[t, h, d])) / np.float32(ks))
                 xv = float(np.float32(float(newv[t, h, d])) / np.float32(vs))
                 k0[b, h, o, d] = oracle.e4m3_encode(xk, lib=lib)
-                v0[b, h, o, d] = oracle.e4m3_encode(xv, lib=lib)
+                v0.reshape(NB, Hkv, D, BS)[b, h, d, o] = oracle.e4m3_encode(xv, lib=lib)
                 dk = oracle.e4m3_decode(int(k0[b, h, o, d]), lib=lib)
                 if abs(xk) <= 448:
                     assert abs(dk - xk) <= max(abs(xk) / 16, 2.0 ** -10)
@@ -507,8 +508,11 @@ def pin_fp8_attention_equals_bf16(lib):
     oracle.kv_write_fp8(kq, vq, _all_rows(k16), _all_rows(v16), np.arange(k16.shape[0] * BS),
                         ks, vs, lib=lib)
     dec = np.vectorize(lambda c: oracle.e4m3_decode(int(c), lib=lib))
+    NB, Hkv, bs, D = kq.shape
     kd = torch.from_numpy(dec(kq) * ks).to(torch.bfloat16)
-    vd = torch.from_numpy(dec(vq) * vs).to(torch.bfloat16)
+    # V codes are stored [block][head][d][offset]
+    vt = np.ascontiguousarray(vq.reshape(NB, Hkv, D, bs).transpose(0, 1, 3, 2))
+    vd = torch.from_numpy(dec(vt) * vs).to(torch.bfloat16)
     assert torch.equal(kd.double(), torch.from_numpy(dec(kq) * ks))  # exact in bf16
     ref = oracle.attention(w.q, kd, vd, w.block_tables, w.context_lens, w.scale, lib=lib)
     got = oracle.attention_fp8(w.q, kq, vq, w.block_tables, w.context_lens, w.scale, ks, vs,

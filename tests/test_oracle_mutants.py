@@ -46,9 +46,12 @@ MUTANTS = [
     ("e4m3-no-saturate", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
     ("fp8-write-no-scale", "k_cache[dst + d] = oracle_e4m3_encode(kx / k_scale);",
      "k_cache[dst + d] = oracle_e4m3_encode(kx);"),
-    ("fp8-attn-v-scale",
-     "vc[(size_t)t * head_dim + d] = oracle_e4m3_decode(v_cache[row + d]) * v_scale;",
-     "vc[(size_t)t * head_dim + d] = oracle_e4m3_decode(v_cache[row + d]) * k_scale;"),
+    ("fp8-attn-v-scale", "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size]) * v_scale;",
+     "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size]) * k_scale;"),
+    ("fp8-v-untransposed", "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size])",
+     "oracle_e4m3_decode(v_cache[row + d])"),
+    ("fp8-write-v-untransposed", "v_cache[vbase + (size_t)d * block_size] =",
+     "v_cache[dst + d] ="),
     ("fp8-copy-k-only",
      "memcpy(v_cache + (size_t)dst * block_elems, v_cache + (size_t)src * block_elems, block_elems);",
      ""),
