@@ -260,7 +260,8 @@ struct MmaLayout {
 };
 
 template <int D, int NW, int NS, bool KV8>
-__global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (NW <= 4 ? 2 : 1)))
+__global__ void __launch_bounds__((NW + 1) * 32,
+                                  NW == 1 ? 8 : (NW <= 2 ? 4 : (NW <= 3 ? 3 : (NW <= 4 ? 2 : 1))))
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
   using L = MmaLayout<D, NW, NS, KV8>;
@@ -311,7 +312,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     // slots.  Lane w < NW feeds consumer warp w: block jb of an item goes to lane
     // jb % NW, so the lanes issue their copies side by side.  Lane w counts the blocks
     // it handed to warp w (ring slot = count % NS, phase = count / NS).
-    int cnt = 0;
+    int cnt = 0;               // blocks handed to warp `lane` so far
+    int pslot = 0, pphase = 0;  // = cnt % NS, (cnt / NS) & 1, kept incrementally
     bool stop = false;
     auto claim = [&]() -> int {
       int it = 0;
@@ -356,10 +358,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
           const int b = __shfl_sync(kFull, blk_lane, (r + lane) & 31);
           int ok = 1;
           if (lane < NW && r + lane < n) {
-            const int slot = cnt % NS;
+            const int slot = pslot;
             const uint32_t fb = full0 + 8 * (lane * NS + slot);
-            ok = mbar_wait(empty0 + 8 * (lane * NS + slot), ((cnt / NS) & 1) ^ 1, abort_flag,
-                           a.err);
+            ok = mbar_wait(empty0 + 8 * (lane * NS + slot), pphase ^ 1, abort_flag, a.err);
             if (ok) {
               if ((unsigned)b >= (unsigned)a.num_blocks) {
                 flag_error(a.err, PKV_DEV_BAD_BLOCK);
@@ -385,6 +386,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
                 }
               }
               ++cnt;
+              if (++pslot == NS) {
+                pslot = 0;
+                pphase ^= 1;
+              }
             }
           }
           if (!__all_sync(kFull, ok)) {
@@ -426,7 +431,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     }
   };
   const int gid = lane >> 2, tig = lane & 3;
-  int cnt = 0;
+  int cslot = 0, cphase = 0;  // ring slot and phase of this warp's next block
+  // Per-thread shared-memory offsets inside a stage (the swizzle folded in once; a k-step
+  // then only flips the 16-byte chunk bits 4..6, which a stage base never sets).
+  const int tokA8 = 4 * (gid >> 1) + (gid & 1), tokB8 = tokA8 + 2;  // E4M3 token order
+  const uint32_t koffA = KV8 ? (uint32_t)(tokA8 * 128 + ((tokA8 & 7) << 4) + 4 * tig) : 0u;
+  const uint32_t koffB = KV8 ? (uint32_t)(tokB8 * 128 + ((tokB8 & 7) << 4) + 4 * tig) : 0u;
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row (bf16 K tile)
+  const uint32_t koff16 = (uint32_t)(lrow * 128 + ((((lane >> 4) & 1) ^ (lrow & 7)) << 4));
   if (threadIdx.x == 0) fetch(0);
   __syncwarp();
   asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
@@ -453,9 +465,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
     for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
     for (int jb = warp; jb < nblk; jb += NW) {
-      const int slot = cnt % NS;
-      const uint32_t par = (cnt / NS) & 1;
-      ++cnt;
+      const int slot = cslot;
+      const uint32_t par = cphase;
+      if (++cslot == NS) {
+        cslot = 0;
+        cphase ^= 1;
+      }
       const uint32_t fb = full0 + 8 * (warp * NS + slot);
       int ok = mbar_wait(fb, par, abort_flag, a.err);
       ok = __all_sync(kFull, ok);
@@ -484,23 +499,24 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW <= 2 ? 4 : (NW <= 3 ? 3 : (N
         // E4M3 path: tile row m of S^T holds token tokA (m = gid) / tokB (m = gid + 8), a
         // token order in which the P.V operand's four k-slots of a thread are four
         // consecutive tokens (the transposed V codes of one head_dim row).
-        const int tokA = KV8 ? 4 * (gid >> 1) + (gid & 1) : gid;
-        const int tokB = KV8 ? tokA + 2 : gid + 8;
+        const int tokA = KV8 ? tokA8 : gid;
+        const int tokB = KV8 ? tokB8 : gid + 8;
         if constexpr (KV8) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
-            const uint32_t w0 = lds32(kst + tile8_off(tokA, 16 * kk + 4 * tig));
-            const uint32_t w1 = lds32(kst + tile8_off(tokB, 16 * kk + 4 * tig));
+            const uint32_t w0 = lds32(kst + (koffA ^ (uint32_t)(kk << 4)));
+            const uint32_t w1 = lds32(kst + (koffB ^ (uint32_t)(kk << 4)));
             mma16816_f16(sc, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
                          e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), qb[kk][0],
                          qb[kk][1]);
           }
         } else {
-          const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
+            // column 16 kk + 8 (lane >> 4): half kk / 4, chunk (2 kk + (lane >> 4)) & 7
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(kst + tile_off(row, 16 * kk + (lane >> 4) * 8), a0, a1, a2, a3);
+            ldsm_x4(kst + (uint32_t)((kk >> 2) * 2048) + (koff16 ^ (uint32_t)(((2 * kk) & 7) << 4)),
+                    a0, a1, a2, a3);
             mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
           }
         }
@@ -740,7 +756,8 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 int ring_choice() {
   static int choice = -1;
   if (choice < 0) {
-    static const char *names[] = {"3x2", "8x2", "4x4", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3"};
+    static const char *names[] = {"3x2", "8x2", "4x4", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3",
+                                  "1x4", "1x6"};
     const char *v = std::getenv("PKV_MMA_RING");
     choice = 0;
     for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
@@ -761,7 +778,19 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
     return (int)cudaErrorInvalidValue;
   if (a.kv8) {
     if (head_dim != 128) return (int)cudaErrorInvalidValue;
-    return launch_mma_t<128, 3, 2, true>(a, tk, tv, st);
+    switch (ring_choice()) {
+      case 1: return launch_mma_t<128, 8, 2, true>(a, tk, tv, st);
+      case 2: return launch_mma_t<128, 4, 4, true>(a, tk, tv, st);
+      case 3: return launch_mma_t<128, 4, 3, true>(a, tk, tv, st);
+      case 4: return launch_mma_t<128, 2, 2, true>(a, tk, tv, st);
+      case 5: return launch_mma_t<128, 2, 3, true>(a, tk, tv, st);
+      case 6: return launch_mma_t<128, 4, 2, true>(a, tk, tv, st);
+      case 7: return launch_mma_t<128, 2, 4, true>(a, tk, tv, st);
+      case 8: return launch_mma_t<128, 3, 3, true>(a, tk, tv, st);
+      case 9: return launch_mma_t<128, 1, 4, true>(a, tk, tv, st);
+      case 10: return launch_mma_t<128, 1, 6, true>(a, tk, tv, st);
+      default: return launch_mma_t<128, 3, 2, true>(a, tk, tv, st);
+    }
   }
   if (head_dim == 64) return launch_mma_t<64, 4, 4>(a, tk, tv, st);
   switch (ring_choice()) {
@@ -773,6 +802,8 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
     case 6: return launch_mma_t<128, 4, 2>(a, tk, tv, st);
     case 7: return launch_mma_t<128, 2, 4>(a, tk, tv, st);
     case 8: return launch_mma_t<128, 3, 3>(a, tk, tv, st);
+    case 9: return launch_mma_t<128, 1, 4>(a, tk, tv, st);
+    case 10: return launch_mma_t<128, 1, 6>(a, tk, tv, st);
     default: return launch_mma_t<128, 3, 2>(a, tk, tv, st);
   }
 }
