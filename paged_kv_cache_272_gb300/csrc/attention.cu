@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
     if (n > 1) {
       const int nch = (n + kChunk - 1) / kChunk;
       atomicAdd(&ucount[nch > 1 ? 0 : 1], nch * G8);
-      if (nch > 1)  // arrival counters of the second merge level
-        for (int g = 0; g < G8; ++g) a.cnt_seq[(size_t)s * G8 + g] = 0;
+      if (nch > 1)  // arrival counters of the second merge level, one per head
+        for (int h = 0; h < a.num_q_heads; ++h) a.cnt_seq[(size_t)s * a.num_q_heads + h] = 0;
     }
     // n - 1 (or n) partitions of P tokens and at most one shorter tail.
     const int nfull = c / P, tail = c - nfull * P;
@@ -357,57 +357,53 @@ __device__ __forceinline__ void warp_merge(const float *lse, const float *o, siz
   }
 }
 
-// Persistent over the plan's merge units; warp w of a unit serves query head 8 g + w.
-// A sequence with one chunk is finished by its units; one with several leaves a result
-// per chunk, and the unit that completes its last chunk merges them.
+// Persistent and warp-granular: a work item is (merge unit, one of its 8 query heads), so
+// the warps of a CTA never wait for one another.  A sequence with one chunk is finished
+// by its items; one with several leaves a result per chunk and head, and the warp that
+// completes the last chunk of a head (an arrival counter per sequence and head) merges
+// that head's chunk results.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   constexpr int PER = D / 32;
-  __shared__ int last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G8 = (a.num_q_heads + 7) / 8;
+  const int lane = threadIdx.x & 31;
+  const int warps = (int)(gridDim.x * (blockDim.x >> 5));
   pdl_trigger();
   pdl_wait();
-  const int nu = *a.num_units;
-  for (int u = blockIdx.x; u < nu; u += gridDim.x) {
-    const int4 un = a.units[u];
+  const int nitems = *a.num_units * 8;
+  for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nitems; it += warps) {
+    const int4 un = a.units[it >> 3];
     const int s = un.x, g8 = un.y, ch = un.z, np = un.w;
+    const int h = g8 * 8 + (it & 7);
+    if (h >= a.num_q_heads) continue;
     const int nch = (np + kChunk - 1) / kChunk;
-    const int h = g8 * 8 + warp;
     const int p0 = ch * kChunk, n = min(kChunk, np - p0);
     float m, L, acc[PER];
-    if (h < a.num_q_heads) {
-      const size_t row = ((size_t)s * a.max_parts + p0) * a.num_q_heads + h;
-      warp_merge<D>(a.part_lse + row, a.part_o + row * D, a.num_q_heads, n, lane, m, L, acc);
-      const float inv = 1.f / L;
-      if (nch == 1) {
-        uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+    const size_t row = ((size_t)s * a.max_parts + p0) * a.num_q_heads + h;
+    warp_merge<D>(a.part_lse + row, a.part_o + row * D, a.num_q_heads, n, lane, m, L, acc);
+    float inv = 1.f / L;
+    if (nch == 1) {
+      uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
-      } else {
-        const size_t crow = ((size_t)s * a.max_chunks + ch) * a.num_q_heads + h;
-        float *o = a.chunk_o + crow * D + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = acc[e] * inv;
-        if (lane == 0) a.chunk_lse[crow] = m + log2f(L);
-      }
+      for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
+      continue;
     }
-    if (nch > 1) {  // uniform over the CTA
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) last = atomicAdd(&a.cnt_seq[(size_t)s * G8 + g8], 1) == nch - 1;
-      __syncthreads();
-      if (last && h < a.num_q_heads) {
-        __threadfence();
-        const size_t row = (size_t)s * a.max_chunks * a.num_q_heads + h;
-        warp_merge<D>(a.chunk_lse + row, a.chunk_o + row * D, a.num_q_heads, nch, lane, m, L, acc);
-        const float inv = 1.f / L;
-        uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+    const size_t crow = ((size_t)s * a.max_chunks + ch) * a.num_q_heads + h;
+    float *co = a.chunk_o + crow * D + lane * PER;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
-      }
-      __syncthreads();  // `last` is rewritten by the next unit
-    }
+    for (int e = 0; e < PER; ++e) co[e] = acc[e] * inv;
+    if (lane == 0) a.chunk_lse[crow] = m + log2f(L);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&a.cnt_seq[(size_t)s * a.num_q_heads + h], 1) == nch - 1;
+    if (!__shfl_sync(kFull, last, 0)) continue;
+    __threadfence();
+    const size_t row2 = (size_t)s * a.max_chunks * a.num_q_heads + h;
+    warp_merge<D>(a.chunk_lse + row2, a.chunk_o + row2 * D, a.num_q_heads, nch, lane, m, L, acc);
+    inv = 1.f / L;
+    uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
   }
 }
 
@@ -472,7 +468,7 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
   w.num_units_off = off;
   off = align256(off + sizeof(int32_t));
   w.cnt_seq_off = off;
-  off = align256(off + S * G8 * sizeof(int32_t));
+  off = align256(off + S * H * sizeof(int32_t));
   w.chunk_lse_off = off;
   off = align256(off + S * C * H * sizeof(float));
   w.chunk_o_off = off;

@@ -14,8 +14,8 @@ constexpr int kChunk = 32;  // partitions one merge unit combines
 //
 // The merge kernel works on units (sequence, group of 8 query heads, chunk of up to
 // kChunk partitions), also listed by the plan; a sequence with several chunks leaves
-// one result per chunk, and the unit that completes the sequence's last chunk (an
-// arrival counter) merges those.
+// one result per chunk and head, and the warp that completes a head's last chunk (an
+// arrival counter per sequence and head) merges those.
 struct AttnArgs {
   uint16_t *out;                 // [S][Hq][D] bf16
   const uint16_t *q;             // [S][Hq][D] bf16
@@ -40,7 +40,7 @@ struct AttnArgs {
   float *part_o;                 // [S][max_parts][Hq][D] normalised partial output
   int4 *units;                   // [S * head groups * max_chunks] {s, head group, chunk, np}
   int32_t *num_units;            // [1]
-  int32_t *cnt_seq;              // [S][head groups] chunks merged (multi-chunk sequences)
+  int32_t *cnt_seq;              // [S][Hq] chunks merged per head (multi-chunk sequences)
   float *chunk_lse;              // [S][max_chunks][Hq]
   float *chunk_o;                // [S][max_chunks][Hq][D]
   int32_t *err;

@@ -80,4 +80,4 @@ def test_workspace_size_formula():
     part = S * P * Hq * (D + 1) * 4
     chunk = S * C * Hq * (D + 1) * 4
     assert n >= part + chunk
-    assert n < part + chunk + S * P * 16 + S * G8 * C * 16 + S * G8 * 4 + S * 4 + 16 * 256
+    assert n < part + chunk + S * P * 16 + S * G8 * C * 16 + S * Hq * 4 + S * 4 + 16 * 256
