@@ -74,6 +74,9 @@ def _declare(lib):
     lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
                                          ctypes.c_double, ctypes.c_double, P, I, I]
     lib.oracle_attention_fp8.restype = I
+    lib.oracle_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                             ctypes.c_double, P, I, I]
+    lib.oracle_attention_prefill.restype = I
     return lib
 
 
@@ -214,4 +217,34 @@ def attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                     _ptr(ctx), S, MB, Hq, Hkv, D, bs, NB, float(scale),
                                     float(k_scale), float(v_scale), sel_p, nsel, int(nthreads)),
            "oracle_attention_fp8")
+    return out
+
+
+# ---- chunked prefill ----------------------------------------------------------------
+def attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                      scale: float, sel=None, nthreads: int = 1, lib=None) -> np.ndarray:
+    """fp64 causal attention of each sequence's last L = query_start[s+1] - query_start[s]
+    tokens over its paged cache.  q is [T][Hq][D]; returns out[T][Hq][D], or
+    out[len(sel)][D] for the (token, head) pairs in ``sel``."""
+    lib = lib or load()
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    S = ctx.shape[0]
+    assert bt.ndim == 2 and bt.shape[0] == S and qs.shape == (S + 1,)
+    if sel is None:
+        out = np.empty((T, Hq, D), dtype=np.float64)
+        sel_p, nsel = None, 0
+    else:
+        sel_a = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((sel_a.shape[0], D), dtype=np.float64)
+        sel_p, nsel = _ptr(sel_a), sel_a.shape[0]
+    _check(lib.oracle_attention_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(bt), _ptr(ctx), _ptr(qs), S, T, bt.shape[1], Hq,
+                                        Hkv, D, bs, NB, float(scale), sel_p, nsel,
+                                        int(nthreads)), "oracle_attention_prefill")
     return out

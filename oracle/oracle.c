@@ -28,6 +28,10 @@
  *    Query head h reads KV head h / (Hq/Hkv) (grouped-query attention: 64 query
  *    heads share 8 KV heads, "Inference optimization", exercise 3).
  *
+ *  - oracle_attention_prefill: the same softmax for several new tokens per sequence
+ *    (chunked prefill), each seeing the tokens up to its own position (causal); see
+ *    the comment above the function.
+ *
  * Layouts (all row-major, element type bf16 stored as uint16 bit patterns):
  *   q[S][Hq][D], k_cache/v_cache[NB][Hkv][block_size][D],
  *   block_tables[S][MB] int32, context_lens[S] int32, out[S][Hq][D] fp64.
@@ -369,6 +373,82 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                 for (int t = 0; t < ctx; ++t) acc += x[t] * vc[(size_t)t * head_dim + d];
                 o[d] = acc / denom;
             }
+        }
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+        if (local && !status) status = local;
+        free(kc);
+        free(vc);
+        free(x);
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Chunked prefill: several new query tokens per sequence.  "Continuous batching and
+ * PagedAttention", section 2 (continuous batching): a long prefill inserted into a
+ * decode batch stalls every decoding request, and the first remedy is to cut the
+ * prefill into chunks spread over several iterations.  A chunk's tokens attend
+ * causally ("System-level optimization", section 3.3 calls the library routine with
+ * is_causal=True): a query token at position p sees the cached tokens 0..p, itself
+ * included, and nothing after it.
+ *
+ * Sequence s contributes L = query_start[s+1] - query_start[s] query tokens, rows
+ * query_start[s] .. query_start[s+1]-1 of q and out ([num_tokens][Hq][D]); they are
+ * the last L of its context_lens[s] tokens, already in the cache, so query token i
+ * (0 <= i < L) sits at position p = context_lens[s] - L + i.  Each (token, head) row is
+ * the textbook softmax over the first p + 1 tokens, exactly as oracle_attention computes
+ * a decode row with context p + 1.  sel, if given, lists nsel (token, head) pairs and
+ * out is then [nsel][D].
+ * ------------------------------------------------------------------------------------ */
+int oracle_attention_prefill(double *out, const uint16_t *q, const uint16_t *k_cache,
+                             const uint16_t *v_cache, const int32_t *block_tables,
+                             const int32_t *context_lens, const int32_t *query_start,
+                             int num_seqs, int num_tokens, int max_blocks, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                             double scale, const int32_t *sel, int nsel, int nthreads) {
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks <= 0 || num_q_heads <= 0 ||
+        num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return -1;
+    if (query_start[0] != 0 || query_start[num_seqs] != num_tokens) return -1;
+    int max_ctx = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int L = query_start[s + 1] - query_start[s];
+        if (L < 0 || context_lens[s] < L) return -1;
+        if (context_lens[s] > max_ctx) max_ctx = context_lens[s];
+    }
+    const int npairs = sel ? nsel : num_tokens * num_q_heads;
+    if (nthreads <= 0) nthreads = 1;
+    int status = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        size_t n = (size_t)(max_ctx > 0 ? max_ctx : 1);
+        double *kc = (double *)malloc(n * head_dim * sizeof(double));
+        double *vc = (double *)malloc(n * head_dim * sizeof(double));
+        double *x = (double *)malloc(n * sizeof(double));
+        int local = (kc && vc && x) ? 0 : -3;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < npairs; ++i) {
+            if (local) continue;
+            const int tok = sel ? sel[2 * i] : i / num_q_heads;
+            const int h = sel ? sel[2 * i + 1] : i % num_q_heads;
+            if (tok < 0 || tok >= num_tokens || h < 0 || h >= num_q_heads) { local = -2; continue; }
+            int s = 0; /* the sequence whose rows hold token tok */
+            while (query_start[s + 1] <= tok) ++s;
+            const int L = query_start[s + 1] - query_start[s];
+            const int pos = context_lens[s] - L + (tok - query_start[s]);
+            int rc = attend_one(out + (size_t)i * head_dim,
+                                q + ((size_t)tok * num_q_heads + h) * head_dim, k_cache, v_cache,
+                                block_tables + (size_t)s * max_blocks, pos + 1, max_blocks, h,
+                                num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                scale, kc, vc, x);
+            if (rc) local = rc;
         }
 #ifdef _OPENMP
 #pragma omp critical

@@ -214,3 +214,162 @@ def kv_read_bytes(w: Workload) -> int:
     """Algorithmic KV bytes one decode step reads: every context token's K and V row
     for every KV head, once."""
     return int(w.context_lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+
+
+# -------------------------------------------------------------------------------------
+# Chunked prefill: several new tokens per sequence
+# -------------------------------------------------------------------------------------
+@dataclass
+class PrefillWorkload:
+    """One chunked-prefill step.  Sequence s ends the step with context_lens[s] tokens,
+    the last L_s = query_start[s+1] - query_start[s] of them new: their K/V are written
+    at slots slot_mapping[query_start[s]:query_start[s+1]] (positions ctx - L .. ctx - 1)
+    and their queries are rows query_start[s] .. query_start[s+1] - 1 of q."""
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    num_blocks: int
+    context_lens: np.ndarray        # int32 [S]
+    query_start: np.ndarray         # int32 [S+1]
+    block_tables: np.ndarray        # int32 [S][MB]
+    slot_mapping: np.ndarray        # int64 [T]
+    q: torch.Tensor                 # bf16 [T][Hq][D]
+    k_new: torch.Tensor             # bf16 [T][Hkv][D]
+    v_new: torch.Tensor
+    k_cache: torch.Tensor           # bf16 [NB][Hkv][16][D], state before the step
+    v_cache: torch.Tensor
+    scale: float
+    block_size: int = BLOCK_SIZE
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start[-1])
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        return np.diff(self.query_start)
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.query_lens.max()) if self.num_seqs else 0
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_tables.shape[1])
+
+
+def build_prefill(name: str, context_lens, query_lens, num_q_heads: int, num_kv_heads: int,
+                  head_dim: int, seed: int, device="cpu", num_blocks: int | None = None,
+                  free_fraction: float = 0.10, poison: bool = True,
+                  max_blocks: int | None = None) -> PrefillWorkload:
+    """Draw one chunked-prefill step: tables from a seeded permutation of the pool,
+    N(0,1) bf16 values; blocks no table reaches and the slots of the step's new tokens
+    hold NaN before the step."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    L = np.asarray(query_lens, dtype=np.int64)
+    S = ctx.shape[0]
+    assert L.shape == (S,) and (L >= 0).all() and (L <= ctx).all()
+    bs = BLOCK_SIZE
+    nblk = (ctx + bs - 1) // bs
+    needed = int(nblk.sum())
+    if num_blocks is None:
+        num_blocks = max(1, int(np.ceil(needed * (1.0 + free_fraction))))
+    assert num_blocks >= needed
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    MB = max(1, int(nblk.max()) if S else 1) if max_blocks is None else max_blocks
+    tables = np.full((S, MB), -1, dtype=np.int32)
+    cursor = 0
+    for s in range(S):
+        tables[s, :nblk[s]] = perm[cursor:cursor + nblk[s]]
+        cursor += nblk[s]
+    qs = np.zeros(S + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(L)
+    T = int(qs[-1])
+    slots = np.zeros(T, dtype=np.int64)
+    for s in range(S):
+        pos = np.arange(ctx[s] - L[s], ctx[s])
+        slots[qs[s]:qs[s + 1]] = tables[s, pos // bs].astype(np.int64) * bs + pos % bs
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    D, Hkv, Hq = head_dim, num_kv_heads, num_q_heads
+    q = _values((T, Hq, D), gen, device)
+    k_cache = _values((num_blocks, Hkv, bs, D), gen, device)
+    v_cache = _values((num_blocks, Hkv, bs, D), gen, device)
+    k_new = _values((T, Hkv, D), gen, device)
+    v_new = _values((T, Hkv, D), gen, device)
+    if poison:
+        used = np.zeros(num_blocks, dtype=bool)
+        for s in range(S):
+            used[tables[s, :nblk[s]]] = True
+        nan = torch.tensor(NAN_BF16, dtype=torch.int16).view(torch.bfloat16).item()
+        unused = torch.as_tensor(np.nonzero(~used)[0].astype(np.int64), device=device)
+        if unused.numel():
+            k_cache[unused] = nan
+            v_cache[unused] = nan
+        if T:
+            b = torch.as_tensor((slots // bs).astype(np.int64), device=device)
+            o = torch.as_tensor((slots % bs).astype(np.int64), device=device)
+            k_cache[b, :, o] = nan
+            v_cache[b, :, o] = nan
+    return PrefillWorkload(name=name, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                           num_blocks=num_blocks, context_lens=ctx.astype(np.int32),
+                           query_start=qs, block_tables=tables, slot_mapping=slots, q=q,
+                           k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                           scale=D ** -0.5)
+
+
+PREFILL_CONFIG_NAMES = {
+    1: "prefill-tiny-gqa2-d64",
+    2: "chunked-prefill-llama3-70b-gqa8",
+    3: "chunked-prefill-llama2-7b-mha",
+}
+
+
+def make_prefill_config(n: int, device="cpu", seed: int | None = None, **kw) -> PrefillWorkload:
+    """Chunked-prefill workloads, seed 2000 + n unless given.
+
+    1: five sequences of mixed shape (decode row, whole prompt, chunk after a cached
+       prefix, ragged lengths), GQA-2, head_dim 64 -- small enough for the oracle.
+    2: Llama-3-70B attention shapes (64 query heads, 8 KV heads, head_dim 128): 16
+       sequences, each prefilling a 512-token chunk after a cached prefix of
+       U{0..3584} tokens (a scheduler's per-step token budget of 8192).
+    3: Llama-2-7B shapes (32 heads, MHA, head_dim 128): 8 sequences, 512-token chunks
+       after U{0..3584} cached tokens.
+    """
+    seed = 2000 + n if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    name = PREFILL_CONFIG_NAMES[n]
+    if n == 1:
+        ctx, L = [1, 5, 40, 70, 100], [1, 5, 17, 2, 64]
+        return build_prefill(name, ctx, L, 4, 2, 64, seed, device, **kw)
+    if n in (2, 3):
+        S = 16 if n == 2 else 8
+        prior = rng.integers(0, 3584, size=S, endpoint=True)
+        L = np.full(S, 512)
+        Hq, Hkv = (64, 8) if n == 2 else (32, 32)
+        return build_prefill(name, prior + L, L, Hq, Hkv, 128, seed, device, **kw)
+    raise ValueError(n)
+
+
+def prefill_flops(w: PrefillWorkload) -> int:
+    """Algorithmic flops of the step's attention: each (query token, head) row at
+    position p multiplies its q with p + 1 keys and sums p + 1 value rows, 2 D flops
+    each (4 D per visible key)."""
+    total = 0
+    for s in range(w.num_seqs):
+        L = int(w.query_start[s + 1] - w.query_start[s])
+        c = int(w.context_lens[s])
+        # sum over i < L of (c - L + i + 1)
+        total += L * (c - L) + L * (L + 1) // 2
+    return total * 4 * w.head_dim * w.num_q_heads

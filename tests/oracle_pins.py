@@ -543,3 +543,91 @@ def pin_fp8_copy(lib):
 FP8_PINS = [pin_quant_capacity, pin_e4m3_table, pin_e4m3_nearest, pin_fp8_write,
             pin_fp8_attention_equals_bf16, pin_fp8_copy]
 ALL_PINS = ALL_PINS + FP8_PINS
+
+
+# -------------------------------------------------------------------------------------
+# Chunked prefill (causal attention of several new tokens per sequence)
+# -------------------------------------------------------------------------------------
+def run_prefill(w, lib, sel=None):
+    """Oracle chunked-prefill step: write the step's new tokens, attend.  fp64 out."""
+    k, v = host_caches(w)
+    if w.slot_mapping.size:
+        oracle.kv_write(k, v, w.k_new, w.v_new, w.slot_mapping, lib=lib)
+    out = oracle.attention_prefill(w.q, k, v, w.block_tables, w.context_lens, w.query_start,
+                                   w.scale, sel=sel, lib=lib)
+    return out, k, v
+
+
+def pin_prefill_sdpa_causal(lib):
+    """Whole prompts (L == context) equal torch's fp64 scaled_dot_product_attention
+    with is_causal=True over the contiguous cache ("System-level optimization",
+    section 3.3 calls the routine that way); GQA by repeating each KV head."""
+    ctx = [1, 2, 15, 16, 17, 40]
+    w = workloads.build_prefill("sdpa-causal", ctx, ctx, 6, 2, 64, seed=81)
+    out, k, v = run_prefill(w, lib)
+    G = 3
+    for s in range(w.num_seqs):
+        n, t0 = int(w.context_lens[s]), int(w.query_start[s])
+        kk, vv = contiguous_from_paged(k, v, w.block_tables[s], n, 2, 64)
+        qt = torch.from_numpy(to_f64(w.q[t0:t0 + n])).permute(1, 0, 2).unsqueeze(0)
+        kt = torch.from_numpy(kk).repeat_interleave(G, dim=0).unsqueeze(0)
+        vt = torch.from_numpy(vv).repeat_interleave(G, dim=0).unsqueeze(0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True,
+                                                                scale=w.scale)
+        np.testing.assert_allclose(out[t0:t0 + n], ref[0].permute(1, 0, 2).numpy(),
+                                   rtol=1e-11, atol=1e-12)
+
+
+def pin_prefill_chunks_equal_whole(lib):
+    """Cutting a prompt into chunks changes nothing: causality makes a token's output
+    depend only on the tokens up to it, so the chunk that ends at position c, attended
+    with context c, reproduces those rows of the whole-prompt prefill exactly."""
+    N, cuts = 90, [0, 23, 24, 57, 90]
+    w = workloads.build_prefill("whole", [N], [N], 4, 2, 64, seed=82)
+    whole, k, v = run_prefill(w, lib)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        part = oracle.attention_prefill(w.q[a:b], k, v, w.block_tables, [b], [0, b - a],
+                                        w.scale, lib=lib)
+        assert np.array_equal(part, whole[a:b]), (a, b)
+
+
+def pin_prefill_last_row_is_decode(lib):
+    """The last new token of each sequence attends over the whole context, as a decode
+    step's query does."""
+    ctx, L = [3, 40, 70, 33], [3, 17, 5, 1]
+    w = workloads.build_prefill("lastrow", ctx, L, 4, 1, 64, seed=83)
+    out, k, v = run_prefill(w, lib)
+    last = w.query_start[1:] - 1
+    dec = oracle.attention(w.q[torch.as_tensor(last.astype(np.int64))], k, v, w.block_tables,
+                           w.context_lens, w.scale, lib=lib)
+    assert np.array_equal(out[last], dec)
+
+
+def pin_prefill_brute_force(lib):
+    """A chunk after a cached prefix recomputed with explicit Python loops: row i of
+    the chunk sees tokens 0 .. ctx - L + i."""
+    ctx, L = [21, 9], [6, 9]
+    w = workloads.build_prefill("brute", ctx, L, 2, 1, 64, seed=84)
+    out, k, v = run_prefill(w, lib)
+    q = to_f64(w.q)
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        kc = gather(k, w.block_tables[s], n, 0)
+        vc = gather(v, w.block_tables[s], n, 0)
+        for i in range(L[s]):
+            tok = int(w.query_start[s]) + i
+            vis = n - L[s] + i + 1
+            for h in range(2):
+                xs = [w.scale * sum(q[tok, h, d] * kc[t, d] for d in range(64))
+                      for t in range(vis)]
+                mx = max(xs)
+                ws = [math.exp(x - mx) for x in xs]
+                tot = sum(ws)
+                for d in range(0, 64, 7):
+                    want = sum(ws[t] * vc[t, d] for t in range(vis)) / tot
+                    assert abs(out[tok, h, d] - want) <= 1e-12 * (1 + abs(want)), (s, i, h, d)
+
+
+PREFILL_PINS = [pin_prefill_sdpa_causal, pin_prefill_chunks_equal_whole,
+                pin_prefill_last_row_is_decode, pin_prefill_brute_force]
+ALL_PINS = ALL_PINS + PREFILL_PINS

@@ -55,6 +55,13 @@ MUTANTS = [
     ("fp8-copy-k-only",
      "memcpy(v_cache + (size_t)dst * block_elems, v_cache + (size_t)src * block_elems, block_elems);",
      ""),
+    ("prefill-position-from-chunk",
+     "const int pos = context_lens[s] - L + (tok - query_start[s]);",
+     "const int pos = tok - query_start[s];"),
+    ("prefill-excludes-self", "pos + 1, max_blocks, h,", "pos, max_blocks, h,"),
+    ("prefill-not-causal", "pos + 1, max_blocks, h,", "context_lens[s], max_blocks, h,"),
+    ("prefill-q-row-of-sequence", "q + ((size_t)tok * num_q_heads + h) * head_dim",
+     "q + ((size_t)s * num_q_heads + h) * head_dim"),
 ]
 
 

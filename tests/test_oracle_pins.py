@@ -45,3 +45,16 @@ def test_index_errors(lib):
     ctx[0] = bt.shape[1] * 16 + 1  # beyond the table
     with pytest.raises(oracle.OracleError):
         oracle.attention(w.q, k, v, w.block_tables, ctx, w.scale, lib=lib)
+
+
+def test_prefill_rejects_bad_query_start(lib):
+    import numpy as np
+    from paged_kv_cache_272_gb300 import workloads
+    w = workloads.build_prefill("err", [20, 8], [4, 8], 2, 1, 64, seed=41)
+    k, v = P.host_caches(w)
+    for ctx, qs in (([3, 8], [0, 4, 12]),      # chunk longer than its context
+                    ([20, 8], [0, 4, 11]),     # last entry is not the token count
+                    ([20, 8], [1, 4, 12])):    # does not start at 0
+        with pytest.raises(oracle.OracleError):
+            oracle.attention_prefill(w.q, k, v, w.block_tables, np.array(ctx, np.int32),
+                                     np.array(qs, np.int32), w.scale, lib=lib)
