@@ -194,6 +194,37 @@ int paged_attention_decode_noalloc(uint16_t *out, const uint16_t *q, const uint1
                                    void *stream);
 
 /*
+ * paged_attention_prefill -- chunked prefill: several new query tokens per sequence,
+ * each attending causally over the sequence's paged cache.
+ * Sequence s owns the L = query_start[s+1] - query_start[s] rows query_start[s] ..
+ * query_start[s+1]-1 of q and out ([num_tokens][num_q_heads][head_dim] bf16); they are
+ * its last L tokens, so row i (0 <= i < L) is the token at position
+ * p = context_lens[s] - L + i, and its K/V must already be in the cache (paged_kv_write
+ * of the chunk's slots before this call).  For every such row and query head h, with
+ * g = h / (Hq/Hkv):
+ *   out[row][h] = sum_{t<=p} exp(x_t - max x) V_s[t][g] / sum_{t<=p} exp(x_t - max x),
+ *   x_t = scale * q[row][h] . K_s[t][g]
+ * computed on tensor cores (bf16 products, fp32 accumulation and softmax; the weights
+ * enter the P.V product rounded to bf16) and rounded to bf16.  L == 1 is a decode row.
+ * query_start: int32 [num_seqs + 1], device, non-decreasing, query_start[num_seqs] <=
+ * num_tokens.  max_query_len: host upper bound of every L (it sizes the launch).
+ * A sequence with L > max_query_len, L > context_lens[s], a context longer than its
+ * block table or a query_start outside [0, num_tokens] sets PKV_DEV_BAD_CONTEXT and
+ * its rows are left unwritten; a bad block id sets PKV_DEV_BAD_BLOCK.  No workspace.
+ * head_dim 64 or 128.
+ * Sources: "Continuous batching and PagedAttention", section 2 (chunked prefill) and
+ * section 3 (block tables); "System-level optimization", section 3.3 (is_causal=True,
+ * scale = head_dim^-1/2).
+ */
+int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables,
+                            const int32_t *context_lens, const int32_t *query_start,
+                            int num_seqs, int num_tokens, int max_blocks_per_seq,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, float scale, int max_query_len, int32_t *err_flag,
+                            void *stream);
+
+/*
  * Attention kernel selection, process-wide (for measurement; the default is AUTO).
  * Returns the previous value, or PKV_ERR_ARG for an unknown value.
  */

@@ -37,6 +37,8 @@ SIGNATURES = {
     "paged_block_copy_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _F, _I, _I, _P, _SZ, _P, _P]),
+    "paged_attention_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     _F, _I, _P, _P]),
     "pkv_pool_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_pool_destroy": (None, [_P]),
     "pkv_pool_num_free": (_I, [_P]),
@@ -159,6 +161,29 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
         int(partition_size), int(max_context_len), _ptr(workspace), workspace.numel(),
         _ptr(err_flag), _stream(stream)), "paged_attention_decode")
+
+
+def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                            scale, max_query_len, err_flag=None, stream=None):
+    """Chunked prefill: rows query_start[s] .. query_start[s+1]-1 of q [T][Hq][D] are the
+    last tokens of sequence s and attend causally over its paged context; out [T][Hq][D]."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16_cuda(n, t)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    _i32("query_start", query_start)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if D2 != D or tuple(out.shape) != (T, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("block_tables must be [S][max_blocks] and query_start [S+1]")
+    check(lib.paged_attention_prefill(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), _ptr(query_start), S, T, block_tables.shape[1], Hq, Hkv, D, bs, NB,
+        float(scale), int(max_query_len), _ptr(err_flag), _stream(stream)),
+        "paged_attention_prefill")
 
 
 def set_attention_variant(variant: int) -> int:

@@ -62,6 +62,19 @@ def test_host_side_validation():
     assert lib.paged_attention_decode(*args(ws=ws - 1)) == -5
     assert lib.paged_attention_decode(*args(S=0)) == 0
     assert lib.paged_attention_set_variant(7) == -14
+    pre = lambda **kw: [kw.get("out", fake), kw.get("q", fake), fake, fake, fake, fake, fake,
+                        kw.get("S", 4), kw.get("T", 64), 8, kw.get("Hq", 8), kw.get("Hkv", 2),
+                        kw.get("D", 128), kw.get("bs", 16), 16, ctypes.c_float(0.1),
+                        kw.get("maxq", 16), None, None]
+    assert lib.paged_attention_prefill(*pre(bs=8)) == -3
+    assert lib.paged_attention_prefill(*pre(D=80)) == -2
+    assert lib.paged_attention_prefill(*pre(Hq=6, Hkv=4)) == -2
+    assert lib.paged_attention_prefill(*pre(maxq=-1)) == -2
+    assert lib.paged_attention_prefill(*pre(S=70000)) == -2
+    assert lib.paged_attention_prefill(*pre(q=None)) == -1
+    assert lib.paged_attention_prefill(*pre(out=fake + 4)) == -4
+    assert lib.paged_attention_prefill(*pre(S=0)) == 0
+    assert lib.paged_attention_prefill(*pre(T=0)) == 0
 
 
 def test_strerror():
