@@ -1,4 +1,4 @@
-"""Benchmark of the paged decode step on GB300.
+"""Benchmark of the paged decode step (default) and of the chunked-prefill step on GB300.
 
 One step = copy-on-write block copy (when the workload has pairs) + paged KV write of
 the step's new tokens + paged decode attention (plan, split-K partitions, LSE merge),
@@ -11,6 +11,11 @@ and the output copied back inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
                     [--variant auto|fma|mma] [--impl ours|reference]
+    python bench.py --path prefill [--config 1..3]
+
+With ``--path prefill`` one step = paged KV write of every sequence's new chunk +
+chunked-prefill attention (causal, tensor cores); ``value`` is attention TFLOP/s of the
+whole step (algorithmic flops: 4 head_dim per visible (query row, key) pair).
 """
 from __future__ import annotations
 
@@ -37,12 +42,17 @@ L2_BYTES = 129 * 1024 * 1024
 ATTN_SOURCES = ["paged_kv_cache_272_gb300/csrc/attention.cu",
                 "paged_kv_cache_272_gb300/csrc/attention_mma.cu",
                 "paged_kv_cache_272_gb300/csrc/attention.cuh",
+                "paged_kv_cache_272_gb300/csrc/tc_common.cuh",
                 "paged_kv_cache_272_gb300/csrc/pkv_common.cuh"]
+PREFILL_SOURCES = ["paged_kv_cache_272_gb300/csrc/prefill.cu",
+                   "paged_kv_cache_272_gb300/csrc/tc_common.cuh",
+                   "paged_kv_cache_272_gb300/csrc/pkv_common.cuh"]
+PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s (% of GB300 bf16 tensor peak)"
 
 
-def attn_source_hash() -> str:
+def attn_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in ATTN_SOURCES:
+    for p in sources or ATTN_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -56,7 +66,7 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def recorded_traffic(workload: str, variant: str):
+def recorded_traffic(workload: str, variant: str, sources=None):
     """DRAM bytes per attention call from the committed ncu summary, only if it was
     taken on the current attention sources."""
     try:
@@ -65,7 +75,7 @@ def recorded_traffic(workload: str, variant: str):
     except (OSError, ValueError):
         return None
     e = rec.get(f"{workload}/{variant}")
-    if not e or e.get("source_hash") != attn_source_hash():
+    if not e or e.get("source_hash") != attn_source_hash(sources):
         return None
     return e.get("dram_bytes_per_call")
 
@@ -456,12 +466,238 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# -------------------------------------------------------------------------------------
+# Chunked prefill
+# -------------------------------------------------------------------------------------
+def prefill_oracle_sample(w, sel, nthreads, k_host, v_host):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attention_prefill(w.q.cpu(), k_host, v_host, w.block_tables, w.context_lens,
+                             w.query_start, w.scale, sel=sel, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    # flops of the sampled rows: 4 D per visible key
+    seq = np.searchsorted(w.query_start, sel[:, 0], side="right") - 1
+    L = w.query_start[seq + 1] - w.query_start[seq]
+    pos = w.context_lens[seq] - L + (sel[:, 0] - w.query_start[seq])
+    return dt, int((pos.astype(np.int64) + 1).sum()) * 4 * w.head_dim
+
+
+def prefill_host_caches(w):
+    """The oracle's copy of the cache after the step's write."""
+    import oracle
+    k = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    v = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    oracle.kv_write(k, v, w.k_new.cpu(), w.v_new.cpu(), w.slot_mapping)
+    return k, v
+
+
+def prefill_sample_rows(w, budget_s, nthreads, k_host, v_host, seed=0):
+    """Random (token, head) rows, grown until the oracle takes about budget_s."""
+    rng = np.random.default_rng(seed)
+    n = 64
+    while True:
+        sel = np.stack([rng.integers(0, w.num_tokens, n), rng.integers(0, w.num_q_heads, n)],
+                       axis=1).astype(np.int32)
+        dt, fl = prefill_oracle_sample(w, sel, nthreads, k_host, v_host)
+        if dt > budget_s or n >= 1 << 20:
+            return sel, dt, fl
+        n = int(n * min(8.0, max(1.5, budget_s / max(dt, 1e-3))))
+
+
+def prefill_cpu_baseline(w, budget_s: float = 12.0):
+    nthreads = os.cpu_count() or 1
+    k_host, v_host = prefill_host_caches(w)
+    sel, dt, fl = prefill_sample_rows(w, budget_s / 3, nthreads, k_host, v_host)
+    reps, tot_t, tot_f = 0, 0.0, 0
+    while reps == 0 or tot_t < budget_s / 3:
+        d, f = prefill_oracle_sample(w, sel, nthreads, k_host, v_host)
+        reps, tot_t, tot_f = reps + 1, tot_t + d, tot_f + f
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{sel.shape[0]} random (token, head) rows of {w.num_tokens} x "
+                      f"{w.num_q_heads}, {reps} repetitions; fp64 C oracle, OpenMP over rows",
+            "seconds": tot_t}
+
+
+def run_prefill_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workloads.make_prefill_config(args.config, device="cpu")
+    nthreads = os.cpu_count() or 1
+    k_host, v_host = prefill_host_caches(w)
+    sel, _, _ = prefill_sample_rows(w, 0.7, nthreads, k_host, v_host)
+    for _ in range(args.warmup):
+        prefill_oracle_sample(w, sel, nthreads, k_host, v_host)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        d, f = prefill_oracle_sample(w, sel, nthreads, k_host, v_host)
+        tot_t, tot_f = tot_t + d, tot_f + f
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_rows": int(sel.shape[0])},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": f"{sel.shape[0]} random (token, head) rows per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill(args):
+    from paged_kv_cache_272_gb300 import ops
+    world, rank, local = setup_dist(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make_prefill_config(args.config, device="cuda")
+    T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    k = w.k_cache.to(dev).contiguous()
+    v = w.v_cache.to(dev).contiguous()
+    q = w.q.to(dev).contiguous()
+    k_new, v_new = w.k_new.to(dev).contiguous(), w.v_new.to(dev).contiguous()
+    slots = torch.as_tensor(w.slot_mapping, dtype=torch.int64, device=dev)
+    bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev)
+    ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev)
+    qs = torch.as_tensor(w.query_start, dtype=torch.int32, device=dev)
+    out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = workloads.prefill_flops(w)
+    kv_bytes = int(w.context_lens.astype(np.int64).sum()) * 2 * Hkv * D * 2
+    working_set = kv_bytes + 2 * q.numel() * 2
+    flush = working_set < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def do_write(kn, vn, sl):
+        ops.paged_kv_write(kn, vn, sl, k, v, err_flag=err, stream=stream)
+
+    def do_attn(qq, btt, cx, qss):
+        ops.paged_attention_prefill(out, qq, k, v, btt, cx, qss, w.scale, w.max_query_len,
+                                    err_flag=err, stream=stream)
+
+    def step():
+        do_write(k_new, v_new, slots)
+        do_attn(q, bt, ctx, qs)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()} during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t_end = time.perf_counter() + 0.8
+        while time.perf_counter() < t_end:
+            step()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            if flush:
+                scratch.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            do_write(k_new, v_new, slots)
+            e1.record(stream)
+            do_attn(q, bt, ctx, qs)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        t_end = time.perf_counter() + 0.4
+        while time.perf_counter() < t_end:
+            step()
+            torch.cuda.synchronize()
+    step_ms = max_over_ranks(sum(a.elapsed_time(c) for a, b, c in ev), world)
+    attn_ms = max_over_ranks(sum(b.elapsed_time(c) for a, b, c in ev) / args.steps, world)
+    value = world * flops * args.steps / (step_ms / 1e3) / 1e12
+
+    h = {name: t.cpu().pin_memory() for name, t in
+         (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("bt", bt),
+          ("ctx", ctx), ("qs", qs))}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dd = {n: torch.empty_like(t, device=dev) for n, t in h.items()}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        for n in h:
+            dd[n].copy_(h[n], non_blocking=True)
+        do_write(dd["k_new"], dd["v_new"], dd["slots"])
+        do_attn(dd["q"], dd["bt"], dd["ctx"], dd["qs"])
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        if flush:
+            scratch.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms += a.elapsed_time(b)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()}")
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (attn_ms / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": w.name, "num_seqs": w.num_seqs, "new_tokens_per_step": T,
+            "max_query_len": w.max_query_len, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "head_dim": D, "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "mean_context": float(w.context_lens.mean()), "max_context": w.max_context_len,
+            "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
+            "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
+                   "working set (KV + q + out) larger than twice L2"),
+            "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_bf16_peak": 100.0 * value / peak,
+        "attention_ms": attn_ms,
+        "e2e": {"value": world * flops * args.steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(w.name, "prefill", PREFILL_SOURCES),
+                     "kernel": "paged_attention_prefill (prefill_kernel, mma.sync bf16)",
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--path", default="decode", choices=["decode", "prefill"],
+                    help="decode step (default) or chunked-prefill step")
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="workload number (decode 1..5, default 2; prefill 1..3, default 2)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition", type=int, default=0,
@@ -470,7 +706,13 @@ def main():
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.config is None:
+        args.config = DEFAULT_CONFIG
+    if args.path == "prefill":
+        if args.config not in workloads.PREFILL_CONFIG_NAMES:
+            ap.error("--path prefill takes --config 1..3")
+        (run_prefill_reference if args.impl == "reference" else run_prefill)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
