@@ -276,6 +276,114 @@ int pkv_pool_step(pkv_pool *pool, const int64_t *seqs, int n, int64_t *slot_mapp
 int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_blocks,
                     int32_t pad, int32_t *block_tables, int32_t *context_lens);
 
+/* ------------------------------------------------------------------------------------
+ * Block pool: sharing primitives used by the prefix cache.
+ * ------------------------------------------------------------------------------------ */
+/* A new sequence whose table starts with `num_blocks` allocated blocks (each refcount
+ * + 1), holding num_blocks * block_size tokens already. */
+int pkv_seq_add_shared(pkv_pool *pool, int64_t seq, const int32_t *blocks, int num_blocks);
+/* One more / one fewer holder of an allocated block (a block returns to the pool when
+ * its last holder releases it). */
+int pkv_block_retain(pkv_pool *pool, int block);
+int pkv_block_release(pkv_pool *pool, int block);
+
+/* ------------------------------------------------------------------------------------
+ * Prefix cache: a trie of full prompt blocks with LRU eviction ("Inference
+ * optimization", Step 3 prefix cache and exercise 4; "Continuous batching and
+ * PagedAttention", section 3, shared read-only blocks).  An entry is one full
+ * block_size-token block of a prompt, reached from the root by the prompt's blocks
+ * before it; the cache holds one reference on each cached block.  A lookup matches at
+ * most (num_tokens - 1) / block_size blocks (the last prompt token is always
+ * computed).  Entries carry last-use stamps; only leaves are evicted, least recently
+ * used first; an insertion evicts down to max_entries.  Host memory only.
+ * ------------------------------------------------------------------------------------ */
+typedef struct pkv_prefix_cache pkv_prefix_cache;
+int pkv_pcache_create(pkv_pool *pool, int max_entries, pkv_prefix_cache **out);
+/* Releases the cache's references; the pool must outlive the cache. */
+void pkv_pcache_destroy(pkv_prefix_cache *cache);
+/* Blocks of the longest cached prefix of tokens[num_tokens] into blocks[max_blocks];
+ * returns how many (>= 0) or an error.  No side effect. */
+int pkv_pcache_lookup(const pkv_prefix_cache *cache, const int32_t *tokens, int num_tokens,
+                      int32_t *blocks, int max_blocks);
+/* Record that a request uses the first num_matched matched blocks: touches them and
+ * counts the lookup in the statistics. */
+int pkv_pcache_use(pkv_prefix_cache *cache, const int32_t *tokens, int num_tokens,
+                   int num_matched);
+/* Cache the full blocks of a computed prompt (table: its block table, at least
+ * num_tokens / block_size entries, all allocated), touching each, then evict down to
+ * max_entries. */
+int pkv_pcache_insert(pkv_prefix_cache *cache, const int32_t *tokens, int num_tokens,
+                      const int32_t *table, int table_len);
+/* Evict the least recently used leaf whose block only the cache holds: 1 if one was
+ * evicted (one pool block freed), 0 if none. */
+int pkv_pcache_evict_free_one(pkv_prefix_cache *cache);
+/* out[6] = lookups, lookups with a hit, tokens looked up, tokens matched, entries,
+ * evictions. */
+int pkv_pcache_stats(const pkv_prefix_cache *cache, int64_t *out);
+
+/* ------------------------------------------------------------------------------------
+ * Continuous-batching scheduler with chunked prefill ("Continuous batching and
+ * PagedAttention", section 2: iteration-level scheduling, chunked prefill with a
+ * per-step token budget; "Inference optimization", continuous batching and exercise 2).
+ * Each step: (1) retire requests that produced all their output tokens (free their
+ * blocks); (2) one decode token for every running request whose prompt is complete,
+ * in admission order; (3) the next prefill chunk of requests still prefilling, while
+ * the step's token budget lasts; (4) admit waiting requests first come first served
+ * while fewer than max_num_seqs run and budget is left (static_batching != 0: only into
+ * an empty batch).  Admission starts a request's table with its prefix-cache match.
+ * Out of blocks: evict an unused cached block, else preempt the most recently admitted
+ * request (its blocks are freed; it is recomputed from the start when readmitted).
+ * A request's KV holds its prompt and all output tokens but the last; the step that
+ * completes a prompt samples the first output token and caches the prompt's full
+ * blocks.  Sequence ids in the pool are the request ids.
+ * ------------------------------------------------------------------------------------ */
+typedef struct pkv_sched pkv_sched;
+
+/* One step's work, in host memory owned by the scheduler (valid until the next step).
+ * Entries: decode entries (query_len 1) first, then prefill chunks. */
+typedef struct {
+  int num_seqs;                 /* scheduled sequences                              */
+  int num_decode;               /* of which decode entries (the first num_decode)   */
+  int num_tokens;               /* new tokens = sum of query_lens                   */
+  int max_blocks;               /* row length of block_tables                       */
+  int num_cow;                  /* copy-on-write pairs to apply before the writes   */
+  int finished;                 /* requests retired at the start of this step       */
+  int preempted;                /* requests preempted during this step              */
+  int running;                  /* running requests after the step                  */
+  int waiting;                  /* waiting requests after the step                  */
+  const int64_t *seq_ids;       /* [num_seqs]                                       */
+  const int32_t *query_lens;    /* [num_seqs] new tokens per sequence               */
+  const int32_t *context_lens;  /* [num_seqs] tokens after the step's writes        */
+  const int32_t *query_start;   /* [num_seqs + 1] offsets of each sequence's tokens */
+  const int64_t *slot_mapping;  /* [num_tokens] slots of the new tokens, in order   */
+  const int32_t *block_tables;  /* [num_seqs][max_blocks], unused entries -1        */
+  const int32_t *cow_pairs;     /* [num_cow][2] (src, dst)                          */
+} pkv_step_plan;
+
+typedef struct {
+  int64_t steps, finished, preemptions, decode_tokens, prefill_tokens, busy_steps;
+  double fill_sum;              /* sum over steps of running / max_num_seqs         */
+  double busy_fill_sum;         /* the same over steps that end with requests waiting */
+  int64_t slots_held;           /* sum over steps and running requests of token slots */
+  int64_t slots_unused;         /* ... of which not holding a token (internal waste)  */
+} pkv_sched_stats;
+
+/* cache may be NULL (no prefix caching); it must use the same pool.
+ * max_batched_tokens >= max_num_seqs. */
+int pkv_sched_create(pkv_pool *pool, pkv_prefix_cache *cache, int max_num_seqs,
+                     int max_batched_tokens, int static_batching, pkv_sched **out);
+/* Frees the blocks of requests still running. */
+void pkv_sched_destroy(pkv_sched *sched);
+/* Queue a request (prompt_tokens may be NULL: the request then bypasses the cache). */
+int pkv_sched_add_request(pkv_sched *sched, int64_t id, int prompt_len,
+                          const int32_t *prompt_tokens, int output_len);
+/* Run one step; fills *plan.  Returns the number of scheduled sequences (0 when
+ * nothing is left to do), or PKV_ERR_OOM when requests remain but none can progress
+ * (the pool is too small for the request at the head of the queue). */
+int pkv_sched_step(pkv_sched *sched, pkv_step_plan *plan);
+int pkv_sched_done(const pkv_sched *sched);  /* 1 when no request is waiting or running */
+int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
+
 #ifdef __cplusplus
 }
 #endif

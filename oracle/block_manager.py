@@ -137,6 +137,31 @@ class BlockManager:
             raise
         return slots, pairs
 
+    def add_seq_shared(self, seq: int, blocks) -> None:
+        """A new sequence whose table starts with the given full blocks, already holding
+        their tokens (a prefix shared with a cache or another request)."""
+        if seq in self.tables:
+            raise BlockManagerError(f"sequence {seq} already exists")
+        for b in blocks:
+            if not 0 <= b < self.num_blocks or self.refcount[b] <= 0:
+                raise BlockManagerError(f"block {b} is not allocated")
+        for b in blocks:
+            self.refcount[b] += 1
+        self.tables[seq] = list(blocks)
+        self.num_tokens[seq] = len(blocks) * self.block_size
+
+    def retain(self, b: int) -> None:
+        """One more holder of an allocated block."""
+        if not 0 <= b < self.num_blocks or self.refcount[b] <= 0:
+            raise BlockManagerError(f"block {b} is not allocated")
+        self.refcount[b] += 1
+
+    def release(self, b: int) -> None:
+        """One holder fewer; the block returns to the pool when none is left."""
+        if not 0 <= b < self.num_blocks:
+            raise BlockManagerError(f"bad block {b}")
+        self._release(b)
+
     def fork(self, parent: int, child: int) -> None:
         """The child shares every block of the parent (refcount + 1 each)."""
         table = self._need(parent)

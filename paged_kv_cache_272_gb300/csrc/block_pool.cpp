@@ -17,59 +17,7 @@
 #include <unordered_map>
 #include <vector>
 
-#include "pagedkv.h"
-
-struct pkv_pool {
-  int num_blocks = 0;
-  int block_size = 16;
-  std::vector<int32_t> free_stack;  // back() is handed out next
-  std::vector<int32_t> refcount;
-  struct Seq {
-    std::vector<int32_t> table;
-    int64_t num_tokens = 0;
-  };
-  std::unordered_map<int64_t, Seq> seqs;
-
-  int32_t alloc() {
-    int32_t b = free_stack.back();
-    free_stack.pop_back();
-    refcount[b] = 1;
-    return b;
-  }
-
-  // Blocks one append at token position n needs, given pending refcount changes.
-  int demand(const Seq &sq, int64_t n, std::unordered_map<int32_t, int> &delta) const {
-    if (n % block_size == 0) return 1;
-    int32_t last = sq.table[n / block_size];
-    int rc = refcount[last] + delta[last];
-    if (rc > 1) {
-      delta[last] -= 1;
-      return 1;
-    }
-    return 0;
-  }
-
-  // One append (demand already checked).  Returns the slot; fills the COW pair.
-  int64_t append(Seq &sq, int32_t *src, int32_t *dst) {
-    const int64_t n = sq.num_tokens;
-    *src = -1;
-    *dst = -1;
-    if (n % block_size == 0) {
-      sq.table.push_back(alloc());
-    } else {
-      int32_t &last = sq.table[n / block_size];
-      if (refcount[last] > 1) {
-        int32_t fresh = alloc();
-        refcount[last] -= 1;
-        *src = last;
-        *dst = fresh;
-        last = fresh;
-      }
-    }
-    sq.num_tokens = n + 1;
-    return (int64_t)sq.table[n / block_size] * block_size + n % block_size;
-  }
-};
+#include "block_pool.hpp"
 
 extern "C" {
 
@@ -116,6 +64,36 @@ int pkv_seq_add(pkv_pool *pool, int64_t seq) {
   return PKV_OK;
 }
 
+int pkv_seq_add_shared(pkv_pool *pool, int64_t seq, const int32_t *blocks, int num_blocks) {
+  if (!pool || (num_blocks > 0 && !blocks)) return PKV_ERR_NULL;
+  if (num_blocks < 0) return PKV_ERR_ARG;
+  if (pool->seqs.count(seq)) return PKV_ERR_DUP_SEQ;
+  for (int i = 0; i < num_blocks; ++i)
+    if (blocks[i] < 0 || blocks[i] >= pool->num_blocks || pool->refcount[blocks[i]] <= 0)
+      return PKV_ERR_ARG;
+  pkv_pool::Seq sq;
+  sq.table.assign(blocks, blocks + num_blocks);
+  sq.num_tokens = (int64_t)num_blocks * pool->block_size;
+  for (int32_t b : sq.table) pool->refcount[b] += 1;
+  pool->seqs.emplace(seq, std::move(sq));
+  return PKV_OK;
+}
+
+int pkv_block_retain(pkv_pool *pool, int block) {
+  if (!pool) return PKV_ERR_NULL;
+  if (block < 0 || block >= pool->num_blocks || pool->refcount[block] <= 0) return PKV_ERR_ARG;
+  pool->refcount[block] += 1;
+  return PKV_OK;
+}
+
+int pkv_block_release(pkv_pool *pool, int block) {
+  if (!pool) return PKV_ERR_NULL;
+  if (block < 0 || block >= pool->num_blocks) return PKV_ERR_ARG;
+  if (pool->refcount[block] <= 0) return PKV_ERR_REFCOUNT;
+  pool->release(block);
+  return PKV_OK;
+}
+
 int pkv_seq_fork(pkv_pool *pool, int64_t parent, int64_t child) {
   if (!pool) return PKV_ERR_NULL;
   auto it = pool->seqs.find(parent);
@@ -134,9 +112,7 @@ int pkv_seq_free(pkv_pool *pool, int64_t seq) {
   const auto &table = it->second.table;
   for (int32_t b : table)
     if (pool->refcount[b] <= 0) return PKV_ERR_REFCOUNT;
-  for (auto r = table.rbegin(); r != table.rend(); ++r) {
-    if (--pool->refcount[*r] == 0) pool->free_stack.push_back(*r);
-  }
+  for (auto r = table.rbegin(); r != table.rend(); ++r) pool->release(*r);
   pool->seqs.erase(it);
   return PKV_OK;
 }

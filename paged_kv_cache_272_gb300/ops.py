@@ -52,6 +52,22 @@ SIGNATURES = {
     "pkv_seq_append_tokens": (_I, [_P, _I64, _I, _P, _P, _P]),
     "pkv_pool_step": (_I, [_P, _P, _I, _P, _P, _P]),
     "pkv_pool_export": (_I, [_P, _P, _I, _I, ctypes.c_int32, _P, _P]),
+    "pkv_seq_add_shared": (_I, [_P, _I64, _P, _I]),
+    "pkv_block_retain": (_I, [_P, _I]),
+    "pkv_block_release": (_I, [_P, _I]),
+    "pkv_pcache_create": (_I, [_P, _I, ctypes.POINTER(_P)]),
+    "pkv_pcache_destroy": (None, [_P]),
+    "pkv_pcache_lookup": (_I, [_P, _P, _I, _P, _I]),
+    "pkv_pcache_use": (_I, [_P, _P, _I, _I]),
+    "pkv_pcache_insert": (_I, [_P, _P, _I, _P, _I]),
+    "pkv_pcache_evict_free_one": (_I, [_P]),
+    "pkv_pcache_stats": (_I, [_P, _P]),
+    "pkv_sched_create": (_I, [_P, _P, _I, _I, _I, ctypes.POINTER(_P)]),
+    "pkv_sched_destroy": (None, [_P]),
+    "pkv_sched_add_request": (_I, [_P, _I64, _I, _P, _I]),
+    "pkv_sched_step": (_I, [_P, _P]),
+    "pkv_sched_done": (_I, [_P]),
+    "pkv_sched_get_stats": (_I, [_P, _P]),
 }
 
 

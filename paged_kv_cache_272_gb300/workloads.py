@@ -373,3 +373,55 @@ def prefill_flops(w: PrefillWorkload) -> int:
         # sum over i < L of (c - L + i + 1)
         total += L * (c - L) + L * (L + 1) // 2
     return total * 4 * w.head_dim * w.num_q_heads
+
+
+# -------------------------------------------------------------------------------------
+# Request streams for the continuous-batching scheduler and the prefix cache
+# -------------------------------------------------------------------------------------
+@dataclass
+class Request:
+    rid: int
+    prompt: np.ndarray      # int32 token ids
+    output_len: int
+
+
+def pareto_output_lens(rng, n, xm=16, alpha=1.5, cap=2048) -> np.ndarray:
+    """Output lengths floor(xm * U^(-1/alpha)) clipped to cap (a Pareto law: most
+    requests short, a few hundreds of times longer)."""
+    u = 1.0 - rng.random(n)
+    return np.minimum(cap, np.floor(xm * u ** (-1.0 / alpha))).astype(np.int64)
+
+
+def make_requests(kind: str, seed: int = 0, n: int | None = None) -> list[Request]:
+    """Seeded request streams.
+
+    ``pareto``: n (default 50) requests, prompts U{16..256} random tokens, Pareto output
+    lengths (xm 16, shape 1.5, at most 2048).
+    ``shared-prefix``: n (default 1000) requests; 60% start with one of 5 common prefixes
+    (U{64..256} tokens each) followed by a private U{8..64}-token suffix, the rest are
+    private prompts of U{32..256} tokens; Pareto output lengths capped at 256.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed + 4242))
+    reqs = []
+    if kind == "pareto":
+        n = 50 if n is None else n
+        outs = pareto_output_lens(rng, n)
+        for i in range(n):
+            P = int(rng.integers(16, 256, endpoint=True))
+            reqs.append(Request(i, rng.integers(0, 32000, P).astype(np.int32), int(outs[i])))
+        return reqs
+    if kind == "shared-prefix":
+        n = 1000 if n is None else n
+        prefixes = [rng.integers(0, 32000, int(rng.integers(64, 256, endpoint=True)))
+                    .astype(np.int32) for _ in range(5)]
+        outs = pareto_output_lens(rng, n, cap=256)
+        for i in range(n):
+            if rng.random() < 0.6:
+                pre = prefixes[int(rng.integers(5))]
+                suf = rng.integers(0, 32000, int(rng.integers(8, 64, endpoint=True)))
+                prompt = np.concatenate([pre, suf.astype(np.int32)])
+            else:
+                prompt = rng.integers(0, 32000, int(rng.integers(32, 256, endpoint=True)))
+            reqs.append(Request(i, prompt.astype(np.int32), int(outs[i])))
+        return reqs
+    raise ValueError(kind)

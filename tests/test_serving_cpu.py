@@ -1,0 +1,268 @@
+"""Continuous-batching scheduler and prefix cache (host code, CPU only).
+
+* The plain-Python references (``oracle/scheduler.py``, ``oracle/prefix_trie.py``)
+  against what the pages state: slot fill above 80% under continuous batching with
+  Pareto output lengths ("Inference optimization", exercise 2), prefix-cache hit rate
+  above 55% for 1000 requests of which 60% share 5 prefixes with at most 500 LRU
+  entries (exercise 4), near-zero KV waste with paging ("Inference optimization",
+  PagedAttention), continuous batching ahead of static batching ("Continuous batching
+  and PagedAttention", section 2) -- plus conservation invariants and brute force.
+* The C++ scheduler and cache against those references, step by step.
+"""
+import numpy as np
+import pytest
+
+from oracle.block_manager import BlockManager
+from oracle.prefix_trie import PrefixTrie
+from oracle.scheduler import Scheduler as RefScheduler
+from paged_kv_cache_272_gb300 import workloads
+
+BS = 16
+
+
+def ref_run(reqs, num_blocks, max_seqs, budget, static=False, cache_entries=None,
+            free_order=None, max_steps=200000):
+    bm = BlockManager(num_blocks, BS, free_order=free_order)
+    cache = PrefixTrie(bm, cache_entries) if cache_entries is not None else None
+    s = RefScheduler(bm, max_seqs, budget, static=static, cache=cache)
+    for r in reqs:
+        s.add_request(r.rid, r.prompt.tolist(), r.output_len)
+    plans = []
+    while not s.done():
+        plans.append(s.step())
+        assert len(plans) < max_steps
+    return s, bm, cache, plans
+
+
+# -------------------------------------------------------------------------------------
+# Pins of the references
+# -------------------------------------------------------------------------------------
+def test_exercise2_continuous_fill_above_80_percent():
+    reqs = workloads.make_requests("pareto", seed=1)
+    cont, bm, _, _ = ref_run(reqs, 4000, 8, 512)
+    stat, _, _, _ = ref_run(reqs, 4000, 8, 512, static=True)
+    assert cont.finished == stat.finished == len(reqs)
+    assert cont.busy_fill_sum / cont.busy_steps > 0.80
+    assert cont.fill_sum / cont.steps > stat.fill_sum / stat.steps
+    assert cont.steps < stat.steps                     # more tokens per step
+    assert bm.num_free() == bm.num_blocks              # nothing leaked
+
+
+def test_outputs_and_prompts_are_conserved():
+    """Without preemption or caching every request computes its prompt once and writes
+    the K/V of all its outputs but the last."""
+    reqs = workloads.make_requests("pareto", seed=2, n=40)
+    s, _, _, plans = ref_run(reqs, 4000, 6, 300)
+    assert s.preemptions == 0
+    assert s.prefill_tokens == sum(len(r.prompt) for r in reqs)
+    assert s.decode_tokens == sum(r.output_len - 1 for r in reqs)
+    # a request's tokens appear at consecutive positions, each position once
+    seen = {}
+    for p in plans:
+        for rid, q, c in zip(p.seqs, p.query_lens, p.context_lens):
+            seen.setdefault(rid, []).append((c - q, c))
+    for r in reqs:
+        spans = seen[r.rid]
+        assert spans[0][0] == 0 and all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+        assert spans[-1][1] == len(r.prompt) + r.output_len - 1
+
+
+def test_waste_is_below_one_block_per_request():
+    reqs = workloads.make_requests("pareto", seed=3)
+    s, _, _, _ = ref_run(reqs, 4000, 8, 512)
+    frac = s.slots_unused / s.slots_held
+    assert frac < 0.05  # the pages quote about 4% with paging
+    # each running request wastes at most block_size - 1 slots per step
+    assert s.slots_unused <= (BS - 1) * s.fill_sum * 8 + 1e-9
+
+
+def test_budget_and_slots_are_respected():
+    reqs = workloads.make_requests("pareto", seed=4, n=60)
+    s, _, _, plans = ref_run(reqs, 4000, 5, 64)
+    for p in plans:
+        assert sum(p.query_lens) <= 64
+        assert len(p.seqs) <= 5
+        assert all(q == 1 for q in p.query_lens[:p.num_decode])
+
+
+def test_preemption_under_block_pressure_completes_everything():
+    reqs = workloads.make_requests("pareto", seed=5, n=30)
+    s, bm, _, plans = ref_run(reqs, 40, 8, 128)
+    assert s.preemptions > 0
+    assert s.finished == len(reqs)
+    assert bm.num_free() == bm.num_blocks
+
+
+def test_pool_too_small_is_reported():
+    from oracle.block_manager import BlockManagerError
+    reqs = [workloads.Request(0, np.arange(100, dtype=np.int32), 5)]
+    with pytest.raises(BlockManagerError):
+        ref_run(reqs, 4, 2, 256)
+
+
+def test_exercise4_prefix_hit_rate_above_55_percent():
+    reqs = workloads.make_requests("shared-prefix", seed=6)
+    s, bm, cache, _ = ref_run(reqs, 8000, 32, 2048, cache_entries=500)
+    assert cache.lookups == len(reqs)
+    assert cache.hits / cache.lookups > 0.55
+    assert len(cache.entries) <= 500
+    # prefill work saved = matched tokens
+    assert s.prefill_tokens == sum(len(r.prompt) for r in reqs) - cache.matched_tokens
+
+
+def test_trie_lookup_equals_brute_force_longest_prefix():
+    rng = np.random.default_rng(7)
+    bm = BlockManager(400)
+    trie = PrefixTrie(bm, 10 ** 6)
+    base = rng.integers(0, 5, 160).tolist()       # few symbols: many shared prefixes
+    prompts = []
+    for i in range(40):
+        cut = int(rng.integers(0, 160))
+        p = base[:cut] + rng.integers(0, 5, int(rng.integers(1, 80))).tolist()
+        bm.add_seq(i)
+        bm.append_tokens(i, len(p))
+        trie.insert(p, bm.block_table(i))
+        prompts.append(p)
+    for q in prompts + [base, base[:33], [9] * 40]:
+        want = 0
+        for p in prompts:          # longest common full-block prefix with any inserted
+            k = 0
+            while (k + 1) * BS <= min(len(p), len(q)) and p[:(k + 1) * BS] == q[:(k + 1) * BS]:
+                k += 1
+            want = max(want, k)
+        assert len(trie.lookup(q)) == min(want, (len(q) - 1) // BS)
+
+
+def test_trie_lru_evicts_least_recent_leaf_first():
+    bm = BlockManager(64)
+    trie = PrefixTrie(bm, 3)
+    a = list(range(48))             # three full blocks: a chain of three entries
+    bm.add_seq(0)
+    bm.append_tokens(0, 48)
+    trie.insert(a, bm.block_table(0))
+    b = list(range(100, 132))       # two more entries: over the limit of 3
+    bm.add_seq(1)
+    bm.append_tokens(1, 32)
+    trie.insert(b, bm.block_table(1))
+    # the leaves were a's third block (older) and b's second block; the older goes
+    # first, then a's second block (now a leaf), leaving a[0], b[0], b[1]
+    assert set(len(k) for k in trie.entries) == {16, 32}
+    assert tuple(a[:16]) in trie.entries and tuple(b[:32]) in trie.entries
+    assert tuple(a[:32]) not in trie.entries
+
+
+# -------------------------------------------------------------------------------------
+# The C++ scheduler and cache against the references
+# -------------------------------------------------------------------------------------
+def native_run(reqs, num_blocks, max_seqs, budget, static=False, cache_entries=None,
+               free_order=None):
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
+    pool = BlockPool(num_blocks, BS, free_order=free_order)
+    cache = PrefixCache(pool, cache_entries) if cache_entries is not None else None
+    s = Scheduler(pool, max_seqs, budget, static=static, cache=cache)
+    for r in reqs:
+        s.add_request(r.rid, r.prompt, r.output_len)
+    plans = []
+    while not s.done():
+        plans.append(s.step())
+    return s, pool, cache, plans
+
+
+CASES = {
+    "continuous": dict(kind="pareto", n=50, blocks=4000, seqs=8, budget=512),
+    "static": dict(kind="pareto", n=50, blocks=4000, seqs=8, budget=512, static=True),
+    "small-budget": dict(kind="pareto", n=40, blocks=4000, seqs=6, budget=40),
+    "preemption": dict(kind="pareto", n=30, blocks=40, seqs=8, budget=128),
+    "prefix-cache": dict(kind="shared-prefix", n=300, blocks=3000, seqs=16, budget=1024,
+                         cache=100),
+    "prefix-cache-pressure": dict(kind="shared-prefix", n=200, blocks=120, seqs=8,
+                                  budget=512, cache=60),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_native_scheduler_matches_reference(name):
+    c = CASES[name]
+    reqs = workloads.make_requests(c["kind"], seed=11, n=c["n"])
+    order = np.random.default_rng(12).permutation(c["blocks"])
+    ref, bm, rcache, rplans = ref_run(reqs, c["blocks"], c["seqs"], c["budget"],
+                                      c.get("static", False), c.get("cache"), order)
+    nat, pool, ncache, nplans = native_run(reqs, c["blocks"], c["seqs"], c["budget"],
+                                           c.get("static", False), c.get("cache"), order)
+    assert len(nplans) == len(rplans)
+    for i, (a, b) in enumerate(zip(nplans, rplans)):
+        assert a.seq_ids.tolist() == b.seqs, i
+        assert a.num_decode == b.num_decode, i
+        assert a.query_lens.tolist() == b.query_lens, i
+        assert a.context_lens.tolist() == b.context_lens, i
+        assert a.slot_mapping.tolist() == b.slots, i
+        assert a.query_start.tolist() == [0] + np.cumsum(b.query_lens).tolist(), i
+        assert [tuple(x) for x in a.cow_pairs.tolist()] == [tuple(x) for x in b.cow_pairs], i
+        assert (a.finished, a.preempted) == (b.finished, b.preempted), i
+        for row, rid in zip(a.block_tables, a.seq_ids):
+            t = bm.tables.get(int(rid))
+            if t is not None and b is rplans[-1]:
+                assert row[:len(t)].tolist() == t
+    st = nat.stats()
+    assert st["steps"] == ref.steps and st["finished"] == ref.finished
+    assert st["preemptions"] == ref.preemptions
+    assert st["decode_tokens"] == ref.decode_tokens
+    assert st["prefill_tokens"] == ref.prefill_tokens
+    assert st["slots_held"] == ref.slots_held and st["slots_unused"] == ref.slots_unused
+    assert st["busy_steps"] == ref.busy_steps
+    assert abs(st["fill_sum"] - ref.fill_sum) < 1e-9
+    if rcache is not None:
+        cs = ncache.stats()
+        assert (cs["lookups"], cs["hits"], cs["matched_tokens"], cs["evictions"]) == (
+            rcache.lookups, rcache.hits, rcache.matched_tokens, rcache.evictions)
+        assert cs["entries"] == len(rcache.entries)
+    assert pool.num_free() + (ncache.stats()["entries"] if ncache else 0) >= 0
+
+
+def test_native_block_tables_match_reference_each_step():
+    """The exported tables of every step equal the reference pool's tables then."""
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
+    reqs = workloads.make_requests("shared-prefix", seed=13, n=120)
+    bm = BlockManager(400)
+    rs = RefScheduler(bm, 8, 256, cache=PrefixTrie(bm, 50))
+    pool = BlockPool(400)
+    ns = Scheduler(pool, 8, 256, cache=PrefixCache(pool, 50))
+    for r in reqs:
+        rs.add_request(r.rid, r.prompt.tolist(), r.output_len)
+        ns.add_request(r.rid, r.prompt, r.output_len)
+    while not rs.done():
+        b = rs.step()
+        a = ns.step()
+        for row, rid in zip(a.block_tables, a.seq_ids):
+            t = bm.tables[int(rid)]
+            assert row[:len(t)].tolist() == t and (row[len(t):] == -1).all()
+    assert ns.done()
+
+
+def test_native_cache_api_matches_reference():
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import PrefixCache
+    rng = np.random.default_rng(14)
+    bm, pool = BlockManager(200), BlockPool(200)
+    trie, cache = PrefixTrie(bm, 12), PrefixCache(pool, 12)
+    base = rng.integers(0, 3, 128).tolist()
+    for i in range(30):
+        p = base[:int(rng.integers(0, 128))] + rng.integers(0, 3, int(rng.integers(1, 60))).tolist()
+        assert cache.lookup(p) == trie.lookup(p)
+        m = trie.lookup(p)
+        trie.use(p, len(m))
+        cache.use(p, len(m))
+        bm.add_seq(i)
+        bm.append_tokens(i, len(p))
+        pool.add_seq(i)
+        pool.append_tokens(i, len(p))
+        trie.insert(p, bm.block_table(i))
+        cache.insert(p, pool.block_table(i))
+        if i % 3 == 2:
+            bm.free_seq(i - 1)
+            pool.free_seq(i - 1)
+            assert cache.evict_free_one() == trie.evict_free_one()
+        assert pool.num_free() == bm.num_free()
+        assert cache.stats()["entries"] == len(trie.entries)
