@@ -689,13 +689,244 @@ def run_prefill(args):
         dist.destroy_process_group()
 
 
+# -------------------------------------------------------------------------------------
+# Continuous-batching serving run (scheduler + prefix cache + all kernels)
+# -------------------------------------------------------------------------------------
+SERVE_METRIC = "continuous-batching serving throughput, output tokens/s (paged KV, Llama-3-70B attention shapes)"
+SERVE_CONFIGS = {
+    1: dict(name="serve-pareto-1024req-gqa8", kind="pareto", n=1024, cache=None),
+    2: dict(name="serve-shared-prefix-1000req-gqa8", kind="shared-prefix", n=1000, cache=4096),
+}
+SERVE_SHAPE = dict(Hq=64, Hkv=8, D=128, max_num_seqs=128, budget=2048)
+
+
+def serve_setup(cfg, static=False, n=None, device="cuda"):
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.driver import ServingDriver
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
+    reqs = workloads.make_requests(cfg["kind"], seed=3000, n=cfg["n"] if n is None else n)
+    sh = SERVE_SHAPE
+    max_ctx = max(len(r.prompt) + r.output_len for r in reqs)
+    blocks = sh["max_num_seqs"] * ((max_ctx + 15) // 16) + (cfg["cache"] or 0)
+    pool = BlockPool(blocks)
+    cache = PrefixCache(pool, cfg["cache"]) if cfg["cache"] else None
+    sched = Scheduler(pool, sh["max_num_seqs"], sh["budget"], static=static, cache=cache)
+    drv = ServingDriver(sched, blocks, sh["Hq"], sh["Hkv"], sh["D"], max_ctx, seed=7,
+                        device=device)
+    for r in reqs:
+        drv.add_request(r.rid, r.prompt, r.output_len)
+    return reqs, pool, cache, sched, drv
+
+
+def serve_run(drv, stream, decode_bytes_per_token):
+    """Run the stream to completion, one synchronised step at a time (the sampled
+    tokens would go back to the host).  Returns timing and counts."""
+    dev_ms, dec_ms, dec_bytes, steps, outs = 0.0, 0.0, 0, 0, 0
+    evs = []
+    dec_ev = []
+    drv.on_decode = lambda k: dec_ev[-1][k].record(stream)
+    t0 = time.perf_counter()
+    while not drv.done():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dec_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+        drv.on_start = lambda: a.record(stream)
+        x, dec, pre = drv.step()
+        if x.token_ids.shape[0] == 0:
+            continue
+        nd = x.num_decode
+        # what a sampler reads: every decode row, the last row of each prefill chunk
+        last = [pre[int(e) - 1] for e in x.prefill_query_start[1:]] if pre is not None else []
+        drv.fetch(dec, *last)
+        b.record(stream)
+        stream.synchronize()
+        steps += 1
+        p = x.plan
+        outs += nd + int(sum(1 for i in range(nd, p.seq_ids.shape[0])
+                             if p.context_lens[i] == len(drv.prompts[int(p.seq_ids[i])])))
+        dev_ms += a.elapsed_time(b)
+        if nd:
+            dec_ms += dec_ev[-1][0].elapsed_time(dec_ev[-1][1])
+            dec_bytes += int(p.context_lens[:nd].astype(np.int64).sum()) * decode_bytes_per_token
+    wall = time.perf_counter() - t0
+    drv.on_decode = None
+    drv.on_start = None
+    return dict(wall_s=wall, device_ms=dev_ms, decode_ms=dec_ms, decode_bytes=dec_bytes,
+                steps=steps, output_tokens=outs)
+
+
+def serve_cpu_baseline(cfg, budget_s=12.0):
+    """The oracle (plain-Python scheduler on the reference block manager and prefix
+    trie, fp64 C attention) on the host cores over the first steps of the same stream."""
+    import oracle
+    from oracle.block_manager import BlockManager
+    from oracle.prefix_trie import PrefixTrie
+    from oracle.scheduler import Scheduler as RefScheduler
+    from paged_kv_cache_272_gb300 import driver as drvmod
+    sh = SERVE_SHAPE
+    reqs = workloads.make_requests(cfg["kind"], seed=3000, n=cfg["n"])
+    max_ctx = max(len(r.prompt) + r.output_len for r in reqs)
+    blocks = sh["max_num_seqs"] * ((max_ctx + 15) // 16) + (cfg["cache"] or 0)
+    bm = BlockManager(blocks)
+    cache = PrefixTrie(bm, cfg["cache"]) if cfg["cache"] else None
+    sch = RefScheduler(bm, sh["max_num_seqs"], sh["budget"], cache=cache)
+    prompts = {}
+    for r in reqs:
+        prompts[r.rid] = r.prompt
+        sch.add_request(r.rid, r.prompt.tolist(), r.output_len)
+    g = torch.Generator().manual_seed(7)
+    bf = lambda *s_: torch.randn(*s_, generator=g).to(torch.bfloat16)
+    rows = 4096
+    k_tab, v_tab, q_tab = bf(rows, sh["Hkv"], sh["D"]), bf(rows, sh["Hkv"], sh["D"]), bf(rows, sh["Hq"], sh["D"])
+    u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kh = np.zeros((blocks, sh["Hkv"], 16, sh["D"]), np.uint16)
+    vh = np.zeros_like(kh)
+    nthreads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    steps = outs = 0
+    while not sch.done() and time.perf_counter() - t0 < budget_s:
+        pl = sch.step()
+        if not pl.seqs:
+            continue
+        n = len(pl.seqs)
+        MB = max(len(bm.tables[r]) for r in pl.seqs)
+        tables, _ = bm.export(pl.seqs, MB)
+        qst = np.concatenate([[0], np.cumsum(pl.query_lens)]).astype(np.int32)
+        from paged_kv_cache_272_gb300.serving import Plan
+        plan = Plan(seq_ids=np.array(pl.seqs, np.int64), num_decode=pl.num_decode,
+                    query_lens=np.array(pl.query_lens, np.int32),
+                    context_lens=np.array(pl.context_lens, np.int32), query_start=qst,
+                    slot_mapping=np.array(pl.slots, np.int64),
+                    block_tables=np.array(tables, np.int32),
+                    cow_pairs=np.array(pl.cow_pairs, np.int32).reshape(-1, 2),
+                    finished=pl.finished, preempted=pl.preempted, running=0, waiting=0)
+        x = drvmod.prepare(plan, prompts, rows, rows)
+        if plan.cow_pairs.size:
+            oracle.block_copy(kh, vh, plan.cow_pairs)
+        idx = torch.from_numpy(x.kv_rows)
+        oracle.kv_write(kh, vh, u16(k_tab[idx]), u16(v_tab[idx]), plan.slot_mapping)
+        q = u16(q_tab[torch.from_numpy(x.q_rows)])
+        nd = plan.num_decode
+        if nd:
+            oracle.attention(q[:nd], kh, vh, plan.block_tables[:nd], plan.context_lens[:nd],
+                             sh["D"] ** -0.5, nthreads=nthreads)
+        if n > nd:
+            oracle.attention_prefill(q[nd:], kh, vh, plan.block_tables[nd:],
+                                     plan.context_lens[nd:], x.prefill_query_start,
+                                     sh["D"] ** -0.5, nthreads=nthreads)
+        steps += 1
+        outs += nd + sum(1 for i in range(nd, n)
+                         if plan.context_lens[i] == len(prompts[int(plan.seq_ids[i])]))
+    dt = time.perf_counter() - t0
+    return {"value": outs / dt, "unit": "output tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"first {steps} scheduler steps of the stream ({outs} output tokens); "
+                      "plain-Python scheduler, fp64 C attention with OpenMP",
+            "seconds": dt, "steps": steps}
+
+
+def run_serve_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    cfg = SERVE_CONFIGS[args.config]
+    r = serve_cpu_baseline(cfg, budget_s=max(3.0, 1.0 * (args.steps + args.warmup)))
+    line = {"impl": "reference", "metric": SERVE_METRIC, "value": r["value"],
+            "unit": "output tokens/s", "n_gpus": args.gpus, "steps": r["steps"],
+            "warmup": 0, "ms_per_step": r["seconds"] / max(1, r["steps"]) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg["name"]},
+            "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": r["value"], "unit": "output tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_serve(args):
+    world, rank, local = setup_dist(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = SERVE_CONFIGS[args.config]
+    sh = SERVE_SHAPE
+    stream = torch.cuda.current_stream(dev)
+    per_tok = 2 * sh["Hkv"] * sh["D"] * 2
+    # warm-up: the first requests of the stream, run to completion
+    for _ in range(max(1, args.warmup)):
+        _, _, _, _, drv = serve_setup(cfg, n=64, device=dev)
+        serve_run(drv, stream, per_tok)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        reqs, pool, cache, sched, drv = serve_setup(cfg, device=dev)
+        res = serve_run(drv, stream, per_tok)
+        barrier(world)
+    if int(drv.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(drv.err.item())}")
+    st = sched.stats()
+    cs = cache.stats() if cache is not None else None
+    _, _, _, ssched, sdrv = serve_setup(cfg, static=True, device=dev)
+    sres = serve_run(sdrv, stream, per_tok)
+    dev_s = max_over_ranks(res["device_ms"], world) / 1e3
+    wall = max_over_ranks(res["wall_s"], world)
+    outs = res["output_tokens"]
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = res["decode_bytes"] / (res["decode_ms"] / 1e3) / 1e9 if res["decode_ms"] else 0.0
+    line = {
+        "metric": SERVE_METRIC, "value": world * outs / dev_s, "unit": "output tokens/s",
+        "n_gpus": world, "steps": res["steps"], "warmup": args.warmup,
+        "ms_per_step": res["device_ms"] / res["steps"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg["name"], "requests": len(reqs),
+                   "max_num_seqs": sh["max_num_seqs"], "max_batched_tokens": sh["budget"],
+                   "num_q_heads": sh["Hq"], "num_kv_heads": sh["Hkv"], "head_dim": sh["D"],
+                   "num_blocks": pool.num_blocks,
+                   "prefix_cache_entries": cfg["cache"],
+                   "output_tokens": outs,
+                   "l2": "per-step working sets are the live KV of the batch; no flush (a "
+                         "serving loop runs back to back)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "e2e": {"value": world * outs / wall, "unit": "output tokens/s",
+                "h2d_bytes_per_step": drv.h2d_bytes / res["steps"],
+                "d2h_bytes_per_step": drv.d2h_bytes / res["steps"],
+                "wall_s": wall, "note": "whole loop: host scheduler, pinned copies in and "
+                                        "out, kernels, one synchronisation per step"},
+        "gpu_launches": drv.launches,
+        "value_note": "value: output tokens over the device time of the steps (copies in, "
+                      "kernels, copies out); e2e: over the wall time of the whole loop",
+        "utilisation": {"fill_all_steps": st["fill_sum"] / st["steps"],
+                        "fill_while_queued": (st["busy_fill_sum"] / st["busy_steps"]
+                                              if st["busy_steps"] else None),
+                        "kv_waste": st["slots_unused"] / max(1, st["slots_held"]),
+                        "preemptions": st["preemptions"]},
+        "static_batching": {"e2e_output_tokens_per_s": sres["output_tokens"] / sres["wall_s"],
+                            "device_output_tokens_per_s": sres["output_tokens"] / (sres["device_ms"] / 1e3),
+                            "steps": sres["steps"],
+                            "fill_all_steps": ssched.stats()["fill_sum"] / ssched.stats()["steps"]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "paged_attention_decode inside the serving loop (algorithmic KV "
+                               "bytes of the decode entries / decode attention time)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "clocks": clk.summary(),
+    }
+    if cs is not None:
+        line["prefix_cache"] = {"request_hit_rate": cs["hits"] / max(1, cs["lookups"]),
+                                "token_hit_rate": cs["matched_tokens"] / max(1, cs["query_tokens"]),
+                                **cs}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = serve_cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--path", default="decode", choices=["decode", "prefill"],
-                    help="decode step (default) or chunked-prefill step")
+    ap.add_argument("--path", default="decode", choices=["decode", "prefill", "serve"],
+                    help="decode step (default), chunked-prefill step, or a whole "
+                         "continuous-batching serving run")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
                     help="workload number (decode 1..5, default 2; prefill 1..3, default 2)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
@@ -708,7 +939,11 @@ def main():
     args = ap.parse_args()
     if args.config is None:
         args.config = DEFAULT_CONFIG
-    if args.path == "prefill":
+    if args.path == "serve":
+        if args.config not in SERVE_CONFIGS:
+            ap.error("--path serve takes --config 1..2")
+        (run_serve_reference if args.impl == "reference" else run_serve)(args)
+    elif args.path == "prefill":
         if args.config not in workloads.PREFILL_CONFIG_NAMES:
             ap.error("--path prefill takes --config 1..3")
         (run_prefill_reference if args.impl == "reference" else run_prefill)(args)

@@ -1,0 +1,213 @@
+"""Continuous-batching step driver: runs the native scheduler's steps on the GPU.
+
+Each step the C++ scheduler (``serving.Scheduler``) decides which requests run and
+reserves their slots; the driver copies the step's arrays and the new tokens' q/K/V to
+the device and launches the library's kernels on one stream:
+
+    paged_block_copy        copy-on-write pairs (if any)
+    paged_kv_write          K/V of every new token (decode tokens and prefill chunks)
+    paged_attention_decode  the decode entries (one query token each)
+    paged_attention_prefill the prefill chunks (causal, tensor cores)
+
+There is no model: the new tokens' K/V rows and query rows are taken from fixed seeded
+tables.  A token's K/V depend only on its token id and position, so two requests with
+the same prompt prefix hold the same K/V there and a cached prefix block is valid for
+both; a query row depends on the request and position.  Output tokens get synthetic ids
+from (request, position).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import ops
+from .serving import Plan, Scheduler
+
+BS = 16
+
+
+def kv_row(token_ids: np.ndarray, positions: np.ndarray, rows: int) -> np.ndarray:
+    """Row of the K/V tables for (token id, position)."""
+    return (token_ids.astype(np.int64) * 1000003 + positions.astype(np.int64) * 7919) % rows
+
+
+def q_row(rids: np.ndarray, positions: np.ndarray, rows: int) -> np.ndarray:
+    return (rids.astype(np.int64) * 2654435761 + positions.astype(np.int64) * 40503) % rows
+
+
+def output_token(rids: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    """Synthetic id of the output token at a position (>= prompt length)."""
+    return ((rids.astype(np.int64) * 7777 + positions.astype(np.int64) * 131) % 32000).astype(
+        np.int32)
+
+
+@dataclass
+class StepInputs:
+    """Host arrays of one step (everything the kernels read besides the caches)."""
+    plan: Plan
+    token_ids: np.ndarray      # int32 [T] ids of the new tokens, in slot order
+    positions: np.ndarray      # int32 [T]
+    kv_rows: np.ndarray        # int64 [T] rows of the K/V tables
+    q_rows: np.ndarray         # int64 [T] rows of the query table
+    num_decode: int
+    decode_ctx_max: int
+    prefill_query_start: np.ndarray  # int32 [n_prefill + 1], offsets within the prefill rows
+    prefill_max_query: int
+
+
+def prepare(plan: Plan, prompts: dict, kv_rows_n: int, q_rows_n: int) -> StepInputs:
+    """Token ids, positions and table rows of a step's new tokens (host only)."""
+    ids, pos, rid_of = [], [], []
+    for i, rid in enumerate(plan.seq_ids.tolist()):
+        L, c = int(plan.query_lens[i]), int(plan.context_lens[i])
+        p = np.arange(c - L, c, dtype=np.int64)
+        prompt = prompts[rid]
+        t = np.where(p < len(prompt), prompt[np.minimum(p, len(prompt) - 1)],
+                     output_token(np.full_like(p, rid), p))
+        ids.append(t.astype(np.int32))
+        pos.append(p.astype(np.int32))
+        rid_of.append(np.full(L, rid, np.int64))
+    cat = lambda xs, dt: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)
+    ids, pos, rid_of = cat(ids, np.int32), cat(pos, np.int32), cat(rid_of, np.int64)
+    nd = plan.num_decode
+    pq = plan.query_start[nd:] - plan.query_start[nd]
+    return StepInputs(plan=plan, token_ids=ids, positions=pos,
+                      kv_rows=kv_row(ids, pos, kv_rows_n), q_rows=q_row(rid_of, pos, q_rows_n),
+                      num_decode=nd,
+                      decode_ctx_max=int(plan.context_lens[:nd].max()) if nd else 0,
+                      prefill_query_start=pq.astype(np.int32),
+                      prefill_max_query=int(plan.query_lens[nd:].max()) if len(pq) > 1 else 0)
+
+
+class ServingDriver:
+    def __init__(self, sched: Scheduler, num_blocks: int, num_q_heads: int, num_kv_heads: int,
+                 head_dim: int, max_context: int, seed: int = 0, table_rows: int = 4096,
+                 device="cuda", partition_size: int = 512):
+        self.sched = sched
+        self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
+        self.dev = torch.device(device)
+        self.scale = head_dim ** -0.5
+        g = torch.Generator().manual_seed(seed)
+        bf = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+        # host tables (the "model"): K/V rows by (token, position), q rows by (request, pos)
+        self.k_tab, self.v_tab = bf(table_rows, num_kv_heads, head_dim), bf(table_rows, num_kv_heads, head_dim)
+        self.q_tab = bf(table_rows, num_q_heads, head_dim)
+        self.rows = table_rows
+        self.k_cache = torch.zeros(num_blocks, num_kv_heads, BS, head_dim, dtype=torch.bfloat16,
+                                   device=self.dev)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.prompts: dict[int, np.ndarray] = {}
+        self.max_context = max_context
+        self.P = partition_size
+        self.ws = ops.alloc_workspace(sched.max_num_seqs, num_q_heads, head_dim, max_context,
+                                      partition_size, device=self.dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.launches = 0
+        self._bufs = {}
+        self._host = {}
+        self.h2d_bytes = 0
+        self.d2h_bytes = 0
+        self.on_decode = None  # optional hook(0 before / 1 after) around decode attention
+        self.on_start = None   # optional hook called before the step's first copy
+
+    def add_request(self, rid: int, prompt, output_len: int) -> None:
+        self.prompts[rid] = np.ascontiguousarray(prompt, dtype=np.int32)
+        self.sched.add_request(rid, self.prompts[rid], output_len)
+
+    def done(self) -> bool:
+        return self.sched.done()
+
+    def _stage(self, name, shape, dtype):
+        """A pinned host buffer and its device twin, grown on demand; returns views of
+        the requested shape."""
+        n = int(np.prod(shape)) if len(shape) else 1
+        buf = self._bufs.get(name)
+        if buf is None or buf[0].numel() < n:
+            cap = max(n, 1) * 2
+            buf = (torch.empty(cap, dtype=dtype).pin_memory(),
+                   torch.empty(cap, dtype=dtype, device=self.dev))
+            self._bufs[name] = buf
+        return buf[0][:n].view(shape), buf[1][:n].view(shape)
+
+    def _h2d(self, name, arr, dtype):
+        h, d = self._stage(name, tuple(arr.shape), dtype)
+        h.copy_(torch.from_numpy(np.ascontiguousarray(arr)))
+        d.copy_(h, non_blocking=True)
+        self.h2d_bytes += h.numel() * h.element_size()
+        return d
+
+    def _rows(self, name, table, rows):
+        idx = torch.from_numpy(rows)
+        h, d = self._stage(name, (rows.shape[0],) + tuple(table.shape[1:]), table.dtype)
+        torch.index_select(table, 0, idx, out=h)
+        d.copy_(h, non_blocking=True)
+        self.h2d_bytes += h.numel() * h.element_size()
+        return d
+
+    def fetch(self, *outs):
+        """Copy a step's outputs to pinned host memory (what a sampler would read)."""
+        res = []
+        for i, t in enumerate(outs):
+            if t is None:
+                res.append(None)
+                continue
+            n = t.numel()
+            h = self._host.get(i)
+            if h is None or h.numel() < n:
+                h = torch.empty(max(n, 1) * 2, dtype=t.dtype).pin_memory()
+                self._host[i] = h
+            v = h[:n].view(t.shape)
+            v.copy_(t, non_blocking=True)
+            self.d2h_bytes += n * t.element_size()
+            res.append(v)
+        return res
+
+    def step(self):
+        """One scheduler step and its kernels.  Returns (inputs, decode_out, prefill_out)
+        (device tensors; decode_out is [num_decode][Hq][D], prefill_out [tokens][Hq][D]).
+        The step's host arrays go through pinned staging buffers; the caller synchronises
+        (or reads the outputs) before the next step reuses them."""
+        plan = self.sched.step()
+        x = prepare(plan, self.prompts, self.rows, self.rows)
+        T = x.token_ids.shape[0]
+        if T == 0:
+            return x, None, None
+        if self.on_start is not None:
+            self.on_start()
+        k_new = self._rows("k", self.k_tab, x.kv_rows)
+        v_new = self._rows("v", self.v_tab, x.kv_rows)
+        q = self._rows("q", self.q_tab, x.q_rows)
+        slots = self._h2d("slots", plan.slot_mapping, torch.int64)
+        tables = self._h2d("tables", plan.block_tables, torch.int32)
+        ctx = self._h2d("ctx", plan.context_lens, torch.int32)
+        if plan.cow_pairs.size:
+            pairs = self._h2d("pairs", plan.cow_pairs, torch.int32)
+            ops.paged_block_copy(self.k_cache, self.v_cache, pairs, err_flag=self.err,
+                                 stream=self.stream)
+            self.launches += 1
+        ops.paged_kv_write(k_new, v_new, slots, self.k_cache, self.v_cache, err_flag=self.err,
+                           stream=self.stream)
+        self.launches += 1
+        nd = x.num_decode
+        dec_out = pre_out = None
+        if nd:
+            dec_out = self._stage("dec_out", (nd, self.Hq, self.D), torch.bfloat16)[1]
+            if self.on_decode is not None:
+                self.on_decode(0)
+            ops.paged_attention_decode(dec_out, q[:nd], self.k_cache, self.v_cache, tables[:nd],
+                                       ctx[:nd], self.scale, x.decode_ctx_max, self.ws, self.P,
+                                       err_flag=self.err, stream=self.stream)
+            if self.on_decode is not None:
+                self.on_decode(1)
+            self.launches += 3 if x.decode_ctx_max > self.P else 2
+        if plan.seq_ids.shape[0] > nd:
+            pq = self._h2d("pq", x.prefill_query_start, torch.int32)
+            pre_out = self._stage("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)[1]
+            ops.paged_attention_prefill(pre_out, q[nd:], self.k_cache, self.v_cache, tables[nd:],
+                                        ctx[nd:], pq, self.scale, x.prefill_max_query,
+                                        err_flag=self.err, stream=self.stream)
+            self.launches += 1
+        return x, dec_out, pre_out

@@ -266,3 +266,35 @@ def test_native_cache_api_matches_reference():
             assert cache.evict_free_one() == trie.evict_free_one()
         assert pool.num_free() == bm.num_free()
         assert cache.stats()["entries"] == len(trie.entries)
+
+
+def test_driver_step_inputs_follow_the_plan():
+    """The driver's host preparation: prompt tokens for prefill chunks, synthetic output
+    tokens for decode entries, K/V rows that depend only on (token, position)."""
+    from paged_kv_cache_272_gb300 import driver
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import Scheduler
+    reqs = workloads.make_requests("pareto", seed=15, n=10)
+    pool = BlockPool(2000)
+    s = Scheduler(pool, 4, 64)
+    prompts = {}
+    for r in reqs:
+        prompts[r.rid] = r.prompt
+        s.add_request(r.rid, r.prompt, r.output_len)
+    while not s.done():
+        plan = s.step()
+        x = driver.prepare(plan, prompts, 4096, 4096)
+        assert x.token_ids.shape[0] == plan.slot_mapping.shape[0]
+        for i, rid in enumerate(plan.seq_ids.tolist()):
+            a, b = int(plan.query_start[i]), int(plan.query_start[i + 1])
+            c, L = int(plan.context_lens[i]), int(plan.query_lens[i])
+            assert x.positions[a:b].tolist() == list(range(c - L, c))
+            P = len(prompts[rid])
+            if i < plan.num_decode:
+                assert L == 1 and c - 1 >= P
+                assert x.token_ids[a] == driver.output_token(np.array([rid]), np.array([c - 1]))[0]
+            else:
+                assert x.token_ids[a:b].tolist() == prompts[rid][c - L:c].tolist()
+        nd = plan.num_decode
+        assert x.prefill_query_start.tolist() == (plan.query_start[nd:] - plan.query_start[nd]).tolist()
+        assert (x.kv_rows == driver.kv_row(x.token_ids, x.positions, 4096)).all()
