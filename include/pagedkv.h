@@ -225,6 +225,16 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
                             void *stream);
 
 /*
+ * Chunked-prefill kernel selection, process-wide (for measurement; default AUTO = the
+ * tcgen05 kernel for head_dim 128, the mma.sync kernel for head_dim 64).  Returns the
+ * previous value, or PKV_ERR_ARG for an unknown value.
+ */
+#define PKV_PREFILL_AUTO 0
+#define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
+#define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
+int paged_attention_prefill_set_variant(int variant);
+
+/*
  * Attention kernel selection, process-wide (for measurement; the default is AUTO).
  * Returns the previous value, or PKV_ERR_ARG for an unknown value.
  */

@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <atomic>
 #include <climits>
 
 #include "tc_common.cuh"
@@ -339,6 +340,444 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
                          dim3(kWarps * 32), (size_t)Lay::kSmem, st, a, tk, tv);
 }
 
+
+// ------------------------------------------------------------------------------------
+// tcgen05 variant (head_dim 128): the same arithmetic on the 5th-generation tensor
+// cores.  One CTA = 128 (token, head) rows of one (sequence, KV head), six warps:
+//  * warps 0-3 ("softmax"): thread t owns row t -- TMEM lane t of the S and O
+//    accumulators and row t of the Q and P tiles in shared memory.  They stage Q,
+//    read each S tile from TMEM (tcgen05.ld), scale, mask, keep the running max and
+//    sum, write the bf16 weights P to shared memory, rescale O in TMEM when the
+//    running max grows by more than 2^8 (the sum and O always share one reference, so
+//    a stale reference only needs to keep exp2 below 2^8), and finally normalise O.
+//  * warp 4 ("mma", one elected lane): S_j = Q K_j^T (M 128, N 64, K 128) into one of
+//    two TMEM S buffers, then O += P_{j-1} V_{j-1} (M 128, N 128, K 64) into the TMEM O
+//    accumulator, by tcgen05.mma from shared-memory descriptors; tcgen05.commit signals
+//    the mbarriers (S ready, O ready, K/V stage free).  Issuing S_j before P_{j-1} V_{j-1}
+//    overlaps the next scores with the current softmax.
+//  * warp 5 ("tma", lanes 0-3): K/V tiles of 64 keys into a 3-stage ring as in the
+//    mma.sync variant.
+// Shared-memory tiles use the 128-byte swizzle that TMA writes: Q [2 halves of
+// head_dim][128 rows][128 B], P [128 rows][64 keys x 2 B], K and V of a stage
+// [2 halves][64 keys][128 B].  Q, K (both K-major) and P (K-major) enter as
+// canonical SW128 operands (8-row groups 1024 B apart); V enters as the MN-major
+// operand of O += P V (64-column chunks 8192 B apart, 8-key groups 1024 B apart).
+// TMEM: S buffers at columns 0 and 64, O at columns 128..255 (256 allocated).
+
+constexpr int kTcRows = 128;
+constexpr int kTcWarps = 6;
+constexpr uint32_t kTmemCols = 256;
+
+template <int NST>
+struct TcLayout {
+  static constexpr int kQ = 0;                       // 32 KB
+  static constexpr int kP = 32768;                   // 16 KB
+  static constexpr int kStage0 = 49152;              // NST x 32 KB (K 16 KB, V 16 KB)
+  static constexpr int kStage = 32768;
+  static constexpr int kGuard = 16384;               // slack after the last stage
+  static constexpr int kBars = kStage0 + NST * kStage + kGuard;
+  static constexpr int kNumBars = 2 * NST + 7;       // kv full/empty, S full x2/free x2,
+                                                     // P full, O done, final
+  static constexpr int kSmem = 1024 + kBars + kNumBars * 8 + 16;
+};
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+template <int NST>
+__global__ void __launch_bounds__(kTcWarps * 32, 1)
+    prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv) {
+  constexpr int D = 128;
+  using Lay = TcLayout<NST>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char *gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + Lay::kQ, sP = base + Lay::kP, sSt = base + Lay::kStage0;
+  const uint32_t kv_full = base + Lay::kBars, kv_empty = kv_full + 8 * NST;
+  const uint32_t s_full = kv_empty + 8 * NST, s_free = s_full + 16, p_full = s_free + 16;
+  const uint32_t o_done = p_full + 8, fin = o_done + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Lay::kBars + Lay::kNumBars * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int tile = a.row_tiles - 1 - (int)blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(kv_full + 8 * i, kTileBlocks);
+      mbar_init(kv_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(s_free + 8 * i, 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+  const int ctx = a.context_lens[s];
+  const int L = q1 - q0;
+  if (q0 < 0 || L < 0 || q1 > a.num_tokens || L > a.max_query_len || L > ctx ||
+      ctx > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+    return;
+  }
+  const int G = a.group;
+  const int rows = L * G;
+  const int r0 = tile * kTcRows;
+  if (r0 >= rows) return;
+  const int first_pos = ctx - L;
+  const int r_last = min(r0 + kTcRows, rows) - 1;
+  const int kv_end = first_pos + r_last / G + 1;
+  const int nkt = (kv_end + kKeys - 1) / kKeys;
+
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  if (warp < 4) {
+    // ---------------- softmax warps: thread t owns row t ----------------
+    const int t = threadIdx.x;
+    const int r = r0 + t;
+    const bool valid = r < rows;
+    const int pos = first_pos + (valid ? r : r_last) / G;
+    const int warp_pos_lo = first_pos + min(r0 + warp * 32, r_last) / G;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint16_t *orow = a.out + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D;
+    {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          a.q + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = valid ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(sQ + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4), v.x, v.y, v.z,
+                     v.w);
+      }
+    }
+    fence_proxy_async();
+    named_bar_sync(1, 160);
+
+    float m = -INFINITY, l = 0.f;
+    int o_seen = -1;  // last P V product whose completion this thread has observed
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int sb = j & 1;
+      const int t0 = j * kKeys;
+      if (!mbar_wait(s_full + 8 * sb, (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[64];
+      {
+        uint32_t (&x0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[0]);
+        uint32_t (&x1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[32]);
+        tmem_ld32(tS + 64 * sb + lane_base, x0);
+        tmem_ld32(tS + 64 * sb + 32 + lane_base, x1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free + 8 * sb);
+
+      const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float v = __uint_as_float(x[c]) * a.scale_log2;
+        if (need_mask && t0 + c > pos) v = -INFINITY;
+        x[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      if (j == 0) {
+        m = mx;  // key 0 is visible to every row
+      } else {
+        const bool need = mx > m + 8.f;
+        if (__any_sync(kAll, need)) {
+          if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          o_seen = j - 1;
+          tc_fence_after();
+          const float mn = need ? mx : m;
+          const float corr = exp2f(m - mn);
+          m = mn;
+          l *= corr;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * cc + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(tO + 32 * cc + lane_base, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      uint32_t pk[32];
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        pk[c] = pack_bf16(exp2f(__uint_as_float(x[2 * c]) - m),
+                          exp2f(__uint_as_float(x[2 * c + 1]) - m));
+        ps += bf16_lo(pk[c]) + bf16_hi(pk[c]);
+      }
+      l += ps;
+      // The P tile is free once the previous P V product has completed.
+      if (j >= 1 && o_seen < j - 1) {
+        if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        o_seen = j - 1;
+      }
+      if (t0 + kKeys > kv_end) {
+        // Last tile: V rows at or past kv_end (tail of the last block, blocks not staged)
+        // are set to zero so that their zero weights contribute exactly nothing.
+        const int st = j % NST;
+        if (!mbar_wait(kv_full + 8 * st, (uint32_t)(j / NST) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vst = sSt + st * Lay::kStage + 16384;
+        const int z0 = kv_end - t0;
+        for (int i = t; i < (kKeys - z0) * 16; i += 128) {
+          const int row = z0 + (i >> 4), rem = i & 15;
+          st_shared_v4(vst + (rem >> 3) * 8192 + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
+        }
+      }
+      const uint32_t prow = sP + t * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(prow + ((c ^ (t & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                     pk[4 * c + 3]);
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && o_seen < nkt - 1 &&
+        !mbar_wait(o_done, (uint32_t)(nkt - 1) & 1u, abort_flag, a.err))
+      ok = false;
+    if (ok && !*abort_flag) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc + lane_base, o);
+        tmem_wait_ld();
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(
+                pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (warp == 4) {
+    // ---------------- mma warp: lane 0 issues ----------------
+    named_bar_sync(1, 160);
+    tc_fence_after();
+    constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
+    constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
+    auto issue_pv = [&](int i) -> bool {
+      if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, a.err)) return false;
+      tc_fence_after();
+      const uint32_t vst = sSt + (i % NST) * Lay::kStage + 16384;
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k)
+          tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024), sw128_desc(vst + 2048 * k, 8192, 1024),
+                 idO, (i > 0 || k > 0) ? 1u : 0u);
+        tc_commit(o_done);
+        tc_commit(kv_empty + 8 * (i % NST));
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int st = j % NST, sb = j & 1;
+      if (!mbar_wait(kv_full + 8 * st, (uint32_t)(j / NST) & 1u, abort_flag, a.err) ||
+          (j >= 2 && !mbar_wait(s_free + 8 * sb, (uint32_t)((j - 2) >> 1) & 1u, abort_flag, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t kst = sSt + st * Lay::kStage;
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(s_full + 8 * sb);
+      }
+      __syncwarp();
+      if (j >= 1 && !issue_pv(j - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok) issue_pv(nkt - 1);
+    // Every MMA this thread issued has completed once `fin` fires (they complete in order).
+    if (lane == 0) tc_commit(fin);
+    __syncwarp();
+    mbar_drain(fin, 0);
+    tc_fence_before();
+  } else {
+    // ---------------- tma warp: lane b stages block b of each key tile ----------------
+    const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
+    int issued = 0;
+    if (lane < kTileBlocks) {
+      for (int j = 0; j < nkt; ++j) {
+        const int st = j % NST;
+        if (j >= NST &&
+            !mbar_wait(kv_empty + 8 * st, (uint32_t)((j - NST) / NST) & 1u, abort_flag, a.err))
+          break;
+        const int tok = j * kKeys + lane * kBlockSize;
+        int blk = -1;
+        if (tok < kv_end) {
+          blk = table[tok / kBlockSize];
+          if (blk < 0 || blk >= a.num_blocks) {
+            flag_error(a.err, PKV_DEV_BAD_BLOCK);
+            blk = -1;
+          }
+        }
+        const uint32_t bar = kv_full + 8 * st;
+        mbar_arrive_expect_tx(bar, blk >= 0 ? 2u * 4096u : 0u);  // K and V head tiles
+        if (blk >= 0) {
+          const int row = (blk * a.num_kv_heads + g) * kBlockSize;
+          const uint32_t dk = sSt + st * Lay::kStage + lane * 2048;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d(dk + h * 8192, &tk, h * 64, row, bar);
+            tma_load_2d(dk + 16384 + h * 8192, &tv, h * 64, row, bar);
+          }
+        }
+        issued = j + 1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && *abort_flag)
+      for (int j = max(0, issued - NST); j < issued; ++j)
+        mbar_drain(kv_full + 8 * (j % NST), (uint32_t)(j / NST) & 1u);
+  }
+
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+template <int NST>
+int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                      cudaStream_t st) {
+  using Lay = TcLayout<NST>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        prefill_tc_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  return (int)launch_pdl(prefill_tc_kernel<NST>,
+                         dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
+                              (unsigned)a.num_seqs),
+                         dim3(kTcWarps * 32), (size_t)Lay::kSmem, st, a, tk, tv);
+}
+
+std::atomic<int> g_prefill_variant{PKV_PREFILL_AUTO};
+
 }  // namespace
 }  // namespace pkv
 
@@ -362,7 +801,10 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ALIGN;
   const int group = num_q_heads / num_kv_heads;
-  const int64_t tiles = ((int64_t)max_query_len * group + kRows - 1) / kRows;
+  const int variant = g_prefill_variant.load();
+  const bool tc = head_dim == 128 && variant != PKV_PREFILL_MMA;
+  const int rows_per_cta = tc ? kTcRows : kRows;
+  const int64_t tiles = ((int64_t)max_query_len * group + rows_per_cta - 1) / rows_per_cta;
   const uint64_t cache_rows = (uint64_t)num_blocks * num_kv_heads * kBlockSize;
   if (tiles > INT_MAX || cache_rows >= (1ull << 31)) return PKV_ERR_SHAPE;
   if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
@@ -390,7 +832,14 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
-                                 : launch_prefill_t<64, 4>(a, tk, tv, st);
+  const int rc = tc ? launch_prefill_tc<3>(a, tk, tv, st)
+                    : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
+                                      : launch_prefill_t<64, 4>(a, tk, tv, st);
   return rc == 0 ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int paged_attention_prefill_set_variant(int variant) {
+  if (variant != PKV_PREFILL_AUTO && variant != PKV_PREFILL_MMA && variant != PKV_PREFILL_TC)
+    return PKV_ERR_ARG;
+  return g_prefill_variant.exchange(variant);
 }

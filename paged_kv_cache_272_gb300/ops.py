@@ -16,6 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
+PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
 DEFAULT_PARTITION = 512
 
@@ -31,6 +32,7 @@ SIGNATURES = {
     "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _I, _P, _SZ, _P, _P]),
     "paged_attention_set_variant": (_I, [_I]),
+    "paged_attention_prefill_set_variant": (_I, [_I]),
     "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                             _F, _I, _I, _P, _P]),
     "paged_kv_write_fp8": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
@@ -200,6 +202,15 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
         _ptr(context_lens), _ptr(query_start), S, T, block_tables.shape[1], Hq, Hkv, D, bs, NB,
         float(scale), int(max_query_len), _ptr(err_flag), _stream(stream)),
         "paged_attention_prefill")
+
+
+def set_prefill_variant(variant: int) -> int:
+    """Select the chunked-prefill kernel (PKV_PREFILL_AUTO / _MMA / _TC); returns the
+    previous selection."""
+    prev = lib.paged_attention_prefill_set_variant(int(variant))
+    if prev < 0:
+        raise PagedKVError(prev, "paged_attention_prefill_set_variant")
+    return prev
 
 
 def set_attention_variant(variant: int) -> int:

@@ -18,6 +18,16 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
+@pytest.fixture(params=["tc", "mma"])
+def variant(request):
+    """Run a test with the tcgen05 kernel and with the mma.sync kernel (head_dim 64 always
+    takes the mma.sync kernel)."""
+    o = H.ops()
+    prev = o.set_prefill_variant(o.PKV_PREFILL_TC if request.param == "tc" else o.PKV_PREFILL_MMA)
+    yield request.param
+    o.set_prefill_variant(prev)
+
+
 def dev(w):
     d = "cuda"
     return dict(k=w.k_cache.to(d).contiguous().clone(), v=w.v_cache.to(d).contiguous().clone(),
@@ -80,7 +90,7 @@ def test_prefill_tiny_config():
 
 
 @pytest.mark.parametrize("cfg", [2, 3])
-def test_prefill_full_size_sampled(cfg):
+def test_prefill_full_size_sampled(cfg, variant):
     w = workloads.make_prefill_config(cfg, device="cuda")
     out, err = gpu_prefill(w)
     assert err == 0
@@ -93,7 +103,7 @@ def test_prefill_full_size_sampled(cfg):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 3, 8, 16])
-def test_prefill_shapes(G, D):
+def test_prefill_shapes(G, D, variant):
     """Ragged chunk and context lengths around the 64-row and 64-key tile edges, a
     decode row (L = 1), a whole prompt (L = ctx), contexts not a multiple of 16."""
     ctx = [1, 16, 17, 64, 65, 130, 200, 300, 77]
@@ -105,7 +115,7 @@ def test_prefill_shapes(G, D):
     H.assert_attention_close(out, oracle_prefill(w), f"prefill G={G} D={D}")
 
 
-def test_prefill_empty_chunks_and_bound():
+def test_prefill_empty_chunks_and_bound(variant):
     """Sequences with no new token produce nothing; max_query_len above every chunk only
     adds CTAs that exit; rows outside every chunk stay untouched."""
     ctx, L = [40, 10, 90, 5], [0, 10, 0, 3]
@@ -115,7 +125,7 @@ def test_prefill_empty_chunks_and_bound():
     H.assert_attention_close(out, oracle_prefill(w), "prefill with empty chunks")
 
 
-def test_prefill_chunks_match_whole_prompt():
+def test_prefill_chunks_match_whole_prompt(variant):
     """A prompt prefilled in three chunks (three calls, growing context) gives the rows
     of the single whole-prompt call."""
     N, cuts = 300, [0, 100, 228, 300]
@@ -134,7 +144,7 @@ def test_prefill_chunks_match_whole_prompt():
         assert torch.equal(part, whole[a:b]), (a, b)
 
 
-def test_prefill_decode_rows_match_decode_kernel():
+def test_prefill_decode_rows_match_decode_kernel(variant):
     """L = 1 everywhere is a decode step: the prefill kernel and the decode path agree
     with the oracle (and so within twice the tolerance with each other)."""
     ctx = [5, 100, 700, 1500]
@@ -154,11 +164,11 @@ def test_prefill_decode_rows_match_decode_kernel():
     H.assert_attention_close(dec, ref, "decode of the same rows")
 
 
-def test_prefill_flags_bad_inputs():
+def test_prefill_flags_bad_inputs(variant):
     """A chunk longer than its context and a block id outside the pool are reported in
     the error flag (the kernel skips them; nothing faults)."""
     ctx, L = [40, 30], [8, 8]
-    w = workloads.build_prefill("prefill-bad", ctx, L, 4, 2, 64, seed=98, device="cuda")
+    w = workloads.build_prefill("prefill-bad", ctx, L, 4, 2, 128, seed=98, device="cuda")
     d = dev(w)
     bad_ctx = torch.tensor([5, 30], dtype=torch.int32, device="cuda")
     _, err = gpu_prefill(w, d, context_lens=bad_ctx)
@@ -169,3 +179,23 @@ def test_prefill_flags_bad_inputs():
     assert err & H.ops().DEV_BAD_BLOCK
     _, err = gpu_prefill(w, dev(w), max_query_len=4)  # chunks longer than the bound
     assert err & H.ops().DEV_BAD_CONTEXT
+
+
+def test_prefill_long_context_rows():
+    """A short chunk after a long cached context (many key tiles, lazy rescaling of the
+    output as the running maximum grows) and a chunk spanning several 128-row tiles."""
+    o = H.ops()
+    ctx, L = [9000, 3000, 700], [40, 300, 129]
+    w = workloads.build_prefill("prefill-long", ctx, L, 16, 2, 128, seed=99, device="cuda")
+    w.q.mul_(4)  # sharper softmax: the running maximum moves more
+    for v in (o.PKV_PREFILL_TC, o.PKV_PREFILL_MMA):
+        prev = o.set_prefill_variant(v)
+        try:
+            out, err = gpu_prefill(w)
+        finally:
+            o.set_prefill_variant(prev)
+        assert err == 0
+        sel = sample_rows(w, n=256, seed=5)
+        got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+                  torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+        H.assert_attention_close(got, oracle_prefill(w, sel=sel), f"prefill long variant {v}")
