@@ -64,6 +64,7 @@ extern "C" {
 #define PKV_DEV_BAD_SLOT 2       /* slot_mapping entry >= num_blocks * 16             */
 #define PKV_DEV_BAD_CONTEXT 4    /* context_len < 0 or beyond table / max_context_len */
 #define PKV_DEV_TIMEOUT 8        /* a bounded wait inside a kernel gave up            */
+#define PKV_DEV_LAYOUT 16        /* shared-memory window misaligned (kernel skipped)  */
 
 /* Library ABI version (incremented on any signature change). */
 int paged_kv_version(void);

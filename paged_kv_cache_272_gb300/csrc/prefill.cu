@@ -346,10 +346,11 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 // cores.  One CTA = 128 (token, head) rows of one (sequence, KV head), six warps:
 //  * warps 0-3 ("softmax"): thread t owns row t -- TMEM lane t of the S and O
 //    accumulators and row t of the Q and P tiles in shared memory.  They stage Q,
-//    read each S tile from TMEM (tcgen05.ld), scale, mask, keep the running max and
-//    sum, write the bf16 weights P to shared memory, rescale O in TMEM when the
-//    running max grows by more than 2^8 (the sum and O always share one reference, so
-//    a stale reference only needs to keep exp2 below 2^8), and finally normalise O.
+//    read each S tile from TMEM (tcgen05.ld), mask, keep the running max and sum
+//    (the sum in fp32 from the unrounded weights), write the bf16 weights P to shared
+//    memory, rescale O in TMEM when the running max grows by more than 8 in the log2
+//    domain (the sum and O always share one reference, so a stale reference only needs
+//    to keep the weights below 2^8), and finally normalise O.
 //  * warp 4 ("mma", one elected lane): S_j = Q K_j^T (M 128, N 64, K 128) into one of
 //    two TMEM S buffers, then O += P_{j-1} V_{j-1} (M 128, N 128, K 64) into the TMEM O
 //    accumulator, by tcgen05.mma from shared-memory descriptors; tcgen05.commit signals
@@ -368,17 +369,19 @@ constexpr int kTcRows = 128;
 constexpr int kTcWarps = 6;
 constexpr uint32_t kTmemCols = 256;
 
+// Shared memory is requested 1024-byte aligned and sized exactly, so that two CTAs fit
+// on one SM with NST = 2 (2 x 112 KB); a CTA whose window is not aligned reports an
+// error and exits without touching it.
 template <int NST>
 struct TcLayout {
   static constexpr int kQ = 0;                       // 32 KB
   static constexpr int kP = 32768;                   // 16 KB
   static constexpr int kStage0 = 49152;              // NST x 32 KB (K 16 KB, V 16 KB)
   static constexpr int kStage = 32768;
-  static constexpr int kGuard = 16384;               // slack after the last stage
-  static constexpr int kBars = kStage0 + NST * kStage + kGuard;
+  static constexpr int kBars = kStage0 + NST * kStage;
   static constexpr int kNumBars = 2 * NST + 7;       // kv full/empty, S full x2/free x2,
                                                      // P full, O done, final
-  static constexpr int kSmem = 1024 + kBars + kNumBars * 8 + 16;
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16;
 };
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -422,6 +425,14 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// 2^x by the MUFU ex2 instruction (subnormal results flush to zero: such weights are
+// below 2^-126 of the row maximum's).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -445,15 +456,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 template <int NST>
-__global__ void __launch_bounds__(kTcWarps * 32, 1)
+__global__ void __launch_bounds__(kTcWarps * 32, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
   constexpr int D = 128;
   using Lay = TcLayout<NST>;
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  unsigned char *gbase = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) unsigned char smem_tc[];
+  const uint32_t base = smem_u32(smem_tc);
+  if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
+    if (threadIdx.x == 0) flag_error(a.err, PKV_DEV_LAYOUT);
+    return;
+  }
+  unsigned char *gbase = smem_tc;
   const uint32_t sQ = base + Lay::kQ, sP = base + Lay::kP, sSt = base + Lay::kStage0;
   const uint32_t kv_full = base + Lay::kBars, kv_empty = kv_full + 8 * NST;
   const uint32_t s_full = kv_empty + 8 * NST, s_free = s_full + 16, p_full = s_free + 16;
@@ -558,15 +572,19 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free + 8 * sb);
 
+      // Raw scores; keys past the row's position become -inf (diagonal tiles only).  The
+      // max is taken on raw scores (scale > 0), the weights are 2^(scale s - m) by one
+      // FFMA and one ex2 each.
       const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        float v = __uint_as_float(x[c]) * a.scale_log2;
+        float v = __uint_as_float(x[c]);
         if (need_mask && t0 + c > pos) v = -INFINITY;
         x[c] = __float_as_uint(v);
         mx = fmaxf(mx, v);
       }
+      mx *= a.scale_log2;
       if (j == 0) {
         m = mx;  // key 0 is visible to every row
       } else {
@@ -579,7 +597,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
           o_seen = j - 1;
           tc_fence_after();
           const float mn = need ? mx : m;
-          const float corr = exp2f(m - mn);
+          const float corr = fast_exp2(m - mn);
           m = mn;
           l *= corr;
 #pragma unroll 1
@@ -595,14 +613,17 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         }
       }
       uint32_t pk[32];
-      float ps = 0.f;
+      float ps0 = 0.f, ps1 = 0.f;
+      const float sl = a.scale_log2, nm = -m;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        pk[c] = pack_bf16(exp2f(__uint_as_float(x[2 * c]) - m),
-                          exp2f(__uint_as_float(x[2 * c + 1]) - m));
-        ps += bf16_lo(pk[c]) + bf16_hi(pk[c]);
+        const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), sl, nm));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), sl, nm));
+        ps0 += p0;
+        ps1 += p1;
+        pk[c] = pack_bf16(p0, p1);
       }
-      l += ps;
+      l += ps0 + ps1;
       // The P tile is free once the previous P V product has completed.
       if (j >= 1 && o_seen < j - 1) {
         if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
@@ -765,8 +786,12 @@ int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtenso
   using Lay = TcLayout<NST>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
+    cudaError_t e = cudaFuncSetAttribute(
         prefill_tc_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_tc_kernel<NST>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
@@ -832,7 +857,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = tc ? launch_prefill_tc<3>(a, tk, tv, st)
+  const int rc = tc ? launch_prefill_tc<2>(a, tk, tv, st)
                     : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
                                       : launch_prefill_t<64, 4>(a, tk, tv, st);
   return rc == 0 ? PKV_OK : PKV_ERR_CUDA;
