@@ -356,11 +356,12 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 //    accumulator, by tcgen05.mma from shared-memory descriptors; tcgen05.commit signals
 //    the mbarriers (S ready, O ready, K/V stage free).  Issuing S_j before P_{j-1} V_{j-1}
 //    overlaps the next scores with the current softmax.
-//  * warp 5 ("tma", lanes 0-3): K/V tiles of 64 keys into a 3-stage ring as in the
-//    mma.sync variant.
+//  * warp 5 ("tma"): lanes 0-3 load the four K blocks of each 64-key tile, lanes 4-7
+//    the four V blocks, each into its own two-slot ring (TMA tiled copies as in the
+//    mma.sync variant).
 // Shared-memory tiles use the 128-byte swizzle that TMA writes: Q [2 halves of
-// head_dim][128 rows][128 B], P [128 rows][64 keys x 2 B], K and V of a stage
-// [2 halves][64 keys][128 B].  Q, K (both K-major) and P (K-major) enter as
+// head_dim][128 rows][128 B], P [128 rows][64 keys x 2 B], K and V tiles
+// [2 halves][64 keys][128 B] per ring slot.  Q, K (both K-major) and P (K-major) enter as
 // canonical SW128 operands (8-row groups 1024 B apart); V enters as the MN-major
 // operand of O += P V (64-column chunks 8192 B apart, 8-key groups 1024 B apart).
 // TMEM: S buffers at columns 0 and 64, O at columns 128..255 (256 allocated).
@@ -370,17 +371,19 @@ constexpr int kTcWarps = 6;
 constexpr uint32_t kTmemCols = 256;
 
 // Shared memory is requested 1024-byte aligned and sized exactly, so that two CTAs fit
-// on one SM with NST = 2 (2 x 112 KB); a CTA whose window is not aligned reports an
-// error and exits without touching it.
-template <int NST>
+// on one SM (2 x 112 KB); a CTA whose window is not aligned reports an error and exits
+// without touching it.  K and V tiles live in separate two-slot rings: a K slot is
+// released as soon as its scores are computed, a V slot once its P V product is done,
+// so the next K tiles load while the current softmax runs.
 struct TcLayout {
   static constexpr int kQ = 0;                       // 32 KB
   static constexpr int kP = 32768;                   // 16 KB
-  static constexpr int kStage0 = 49152;              // NST x 32 KB (K 16 KB, V 16 KB)
-  static constexpr int kStage = 32768;
-  static constexpr int kBars = kStage0 + NST * kStage;
-  static constexpr int kNumBars = 2 * NST + 7;       // kv full/empty, S full x2/free x2,
-                                                     // P full, O done, final
+  static constexpr int kK = 49152;                   // 2 x 16 KB
+  static constexpr int kV = 81920;                   // 2 x 16 KB
+  static constexpr int kSlot = 16384;
+  static constexpr int kBars = 114688;
+  static constexpr int kNumBars = 15;                // K full/empty x2, V full/empty x2,
+                                                     // S full/free x2, P full, O done, final
   static constexpr int kSmem = kBars + kNumBars * 8 + 16;
 };
 
@@ -455,12 +458,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                : "memory");
 }
 
-template <int NST>
 __global__ void __launch_bounds__(kTcWarps * 32, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
   constexpr int D = 128;
-  using Lay = TcLayout<NST>;
+  using Lay = TcLayout;
   extern __shared__ __align__(1024) unsigned char smem_tc[];
   const uint32_t base = smem_u32(smem_tc);
   if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
@@ -468,9 +470,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     return;
   }
   unsigned char *gbase = smem_tc;
-  const uint32_t sQ = base + Lay::kQ, sP = base + Lay::kP, sSt = base + Lay::kStage0;
-  const uint32_t kv_full = base + Lay::kBars, kv_empty = kv_full + 8 * NST;
-  const uint32_t s_full = kv_empty + 8 * NST, s_free = s_full + 16, p_full = s_free + 16;
+  const uint32_t sQ = base + Lay::kQ, sP = base + Lay::kP;
+  const uint32_t sK = base + Lay::kK, sV = base + Lay::kV;
+  const uint32_t k_full = base + Lay::kBars, k_empty = k_full + 16;
+  const uint32_t v_full = k_empty + 16, v_empty = v_full + 16;
+  const uint32_t s_full = v_empty + 16, s_free = s_full + 16, p_full = s_free + 16;
   const uint32_t o_done = p_full + 8, fin = o_done + 8;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Lay::kBars + Lay::kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -480,11 +484,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   const int tile = a.row_tiles - 1 - (int)blockIdx.x;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(kv_full + 8 * i, kTileBlocks);
-      mbar_init(kv_empty + 8 * i, 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(k_full + 8 * i, kTileBlocks);
+      mbar_init(k_empty + 8 * i, 1);
+      mbar_init(v_full + 8 * i, kTileBlocks);
+      mbar_init(v_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
       mbar_init(s_free + 8 * i, 4);
     }
@@ -635,12 +639,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       if (t0 + kKeys > kv_end) {
         // Last tile: V rows at or past kv_end (tail of the last block, blocks not staged)
         // are set to zero so that their zero weights contribute exactly nothing.
-        const int st = j % NST;
-        if (!mbar_wait(kv_full + 8 * st, (uint32_t)(j / NST) & 1u, abort_flag, a.err)) {
+        if (!mbar_wait(v_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) {
           ok = false;
           break;
         }
-        const uint32_t vst = sSt + st * Lay::kStage + 16384;
+        const uint32_t vst = sV + (j & 1) * Lay::kSlot;
         const int z0 = kv_end - t0;
         for (int i = t; i < (kKeys - z0) * 16; i += 128) {
           const int row = z0 + (i >> 4), rem = i & 15;
@@ -688,30 +691,32 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
     constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
     auto issue_pv = [&](int i) -> bool {
-      if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, a.err)) return false;
+      if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, a.err) ||
+          !mbar_wait(v_full + 8 * (i & 1), (uint32_t)(i >> 1) & 1u, abort_flag, a.err))
+        return false;
       tc_fence_after();
-      const uint32_t vst = sSt + (i % NST) * Lay::kStage + 16384;
+      const uint32_t vst = sV + (i & 1) * Lay::kSlot;
       if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kKeys / 16; ++k)
           tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024), sw128_desc(vst + 2048 * k, 8192, 1024),
                  idO, (i > 0 || k > 0) ? 1u : 0u);
         tc_commit(o_done);
-        tc_commit(kv_empty + 8 * (i % NST));
+        tc_commit(v_empty + 8 * (i & 1));
       }
       __syncwarp();
       return true;
     };
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      const int st = j % NST, sb = j & 1;
-      if (!mbar_wait(kv_full + 8 * st, (uint32_t)(j / NST) & 1u, abort_flag, a.err) ||
+      const int sb = j & 1;
+      if (!mbar_wait(k_full + 8 * sb, (uint32_t)(j >> 1) & 1u, abort_flag, a.err) ||
           (j >= 2 && !mbar_wait(s_free + 8 * sb, (uint32_t)((j - 2) >> 1) & 1u, abort_flag, a.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t kst = sSt + st * Lay::kStage;
+      const uint32_t kst = sK + sb * Lay::kSlot;
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -719,6 +724,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
                  sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
                  kk > 0 ? 1u : 0u);
         tc_commit(s_full + 8 * sb);
+        tc_commit(k_empty + 8 * sb);
       }
       __syncwarp();
       if (j >= 1 && !issue_pv(j - 1)) {
@@ -733,16 +739,21 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     mbar_drain(fin, 0);
     tc_fence_before();
   } else {
-    // ---------------- tma warp: lane b stages block b of each key tile ----------------
+    // ---------------- tma warp: lanes 0-3 stage K blocks, lanes 4-7 V blocks ----------------
     const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
+    const bool is_v = lane >= kTileBlocks;
+    const int b = lane & (kTileBlocks - 1);
+    const uint32_t full = is_v ? v_full : k_full, empty = is_v ? v_empty : k_empty;
+    const uint32_t ring = is_v ? sV : sK;
+    const CUtensorMap *map = is_v ? &tv : &tk;
     int issued = 0;
-    if (lane < kTileBlocks) {
+    if (lane < 2 * kTileBlocks) {
       for (int j = 0; j < nkt; ++j) {
-        const int st = j % NST;
-        if (j >= NST &&
-            !mbar_wait(kv_empty + 8 * st, (uint32_t)((j - NST) / NST) & 1u, abort_flag, a.err))
+        const int slot = j & 1;
+        if (j >= 2 &&
+            !mbar_wait(empty + 8 * slot, (uint32_t)((j - 2) >> 1) & 1u, abort_flag, a.err))
           break;
-        const int tok = j * kKeys + lane * kBlockSize;
+        const int tok = j * kKeys + b * kBlockSize;
         int blk = -1;
         if (tok < kv_end) {
           blk = table[tok / kBlockSize];
@@ -751,24 +762,22 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
             blk = -1;
           }
         }
-        const uint32_t bar = kv_full + 8 * st;
-        mbar_arrive_expect_tx(bar, blk >= 0 ? 2u * 4096u : 0u);  // K and V head tiles
+        const uint32_t bar = full + 8 * slot;
+        mbar_arrive_expect_tx(bar, blk >= 0 ? 4096u : 0u);  // one head tile, two halves
         if (blk >= 0) {
           const int row = (blk * a.num_kv_heads + g) * kBlockSize;
-          const uint32_t dk = sSt + st * Lay::kStage + lane * 2048;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_2d(dk + h * 8192, &tk, h * 64, row, bar);
-            tma_load_2d(dk + 16384 + h * 8192, &tv, h * 64, row, bar);
-          }
+          const uint32_t dst = ring + slot * Lay::kSlot + b * 2048;
+          tma_load_2d(dst, map, 0, row, bar);
+          tma_load_2d(dst + 8192, map, 64, row, bar);
         }
         issued = j + 1;
       }
     }
     __syncwarp();
-    if (lane == 0 && *abort_flag)
-      for (int j = max(0, issued - NST); j < issued; ++j)
-        mbar_drain(kv_full + 8 * (j % NST), (uint32_t)(j / NST) & 1u);
+    // If a wait gave up, let the copies still in flight land before the CTA exits.
+    if ((lane == 0 || lane == kTileBlocks) && *abort_flag)
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_drain(full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
   }
 
   __syncthreads();
@@ -780,22 +789,21 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   }
 }
 
-template <int NST>
 int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                       cudaStream_t st) {
-  using Lay = TcLayout<NST>;
+  using Lay = TcLayout;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
-        prefill_tc_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+        prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_tc_kernel<NST>,
+      e = cudaFuncSetAttribute(prefill_tc_kernel,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  return (int)launch_pdl(prefill_tc_kernel<NST>,
+  return (int)launch_pdl(prefill_tc_kernel,
                          dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
                               (unsigned)a.num_seqs),
                          dim3(kTcWarps * 32), (size_t)Lay::kSmem, st, a, tk, tv);
@@ -857,7 +865,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = tc ? launch_prefill_tc<2>(a, tk, tv, st)
+  const int rc = tc ? launch_prefill_tc(a, tk, tv, st)
                     : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
                                       : launch_prefill_t<64, 4>(a, tk, tv, st);
   return rc == 0 ? PKV_OK : PKV_ERR_CUDA;
