@@ -352,13 +352,13 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 //    domain (the sum and O always share one reference, so a stale reference only needs
 //    to keep the weights below 2^8), and finally normalise O.
 //  * warp 4 ("mma", one elected lane): S_j = Q K_j^T (M 128, N 64, K 128) into one of
-//    two TMEM S buffers, then O += P_{j-1} V_{j-1} (M 128, N 128, K 64) into the TMEM O
+//    two TMEM S buffers, and O += P_j V_j (M 128, N 128, K 64) into the TMEM O
 //    accumulator, by tcgen05.mma from shared-memory descriptors; tcgen05.commit signals
-//    the mbarriers (S ready, O ready, K/V stage free).  Issuing S_j before P_{j-1} V_{j-1}
-//    overlaps the next scores with the current softmax.
-//  * warp 5 ("tma"): lanes 0-3 load the four K blocks of each 64-key tile, lanes 4-7
-//    the four V blocks, each into its own two-slot ring (TMA tiled copies as in the
-//    mma.sync variant).
+//    the mbarriers (S ready, O ready, K/V slot free).  S runs up to one tile ahead of
+//    P V, so the next scores are ready when the softmax of a tile ends.
+//  * warps 5 and 6 ("tma"): lanes 0-3 load the four K (warp 5) or V (warp 6) blocks of
+//    each 64-key tile into their own two-slot ring (TMA tiled copies as in the mma.sync
+//    variant), reading the block ids one tile ahead.
 // Shared-memory tiles use the 128-byte swizzle that TMA writes: Q [2 halves of
 // head_dim][128 rows][128 B], P [128 rows][64 keys x 2 B], K and V tiles
 // [2 halves][64 keys][128 B] per ring slot.  Q, K (both K-major) and P (K-major) enter as
@@ -367,7 +367,7 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 // TMEM: S buffers at columns 0 and 64, O at columns 128..255 (256 allocated).
 
 constexpr int kTcRows = 128;
-constexpr int kTcWarps = 6;
+constexpr int kTcWarps = 7;
 constexpr uint32_t kTmemCols = 256;
 
 // Shared memory is requested 1024-byte aligned and sized exactly, so that two CTAs fit
@@ -686,87 +686,110 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     tc_fence_before();
   } else if (warp == 4) {
     // ---------------- mma warp: lane 0 issues ----------------
+    // A polling loop issues whichever product is ready, P V first (the softmax of the
+    // next tile waits for it), and lets S run at most one tile ahead of P V (two S
+    // buffers).  Lane 0 tests the barriers without blocking and broadcasts the result.
     named_bar_sync(1, 160);
     tc_fence_after();
     constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
     constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
-    auto issue_pv = [&](int i) -> bool {
-      if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, a.err) ||
-          !mbar_wait(v_full + 8 * (i & 1), (uint32_t)(i >> 1) & 1u, abort_flag, a.err))
-        return false;
-      tc_fence_after();
-      const uint32_t vst = sV + (i & 1) * Lay::kSlot;
-      if (lane == 0) {
+    int js = 0, jp = 0;
+    long long idle_since = -1;
+    while (jp < nkt) {
+      bool progressed = false;
+      if (jp < js) {
+        int ready = 0;
+        if (lane == 0)
+          ready = mbar_test_wait(p_full, (uint32_t)jp & 1u) &&
+                  mbar_test_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u);
+        if (__shfl_sync(kAll, ready, 0)) {
+          tc_fence_after();
+          const uint32_t vst = sV + (jp & 1) * Lay::kSlot;
+          if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < kKeys / 16; ++k)
-          tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024), sw128_desc(vst + 2048 * k, 8192, 1024),
-                 idO, (i > 0 || k > 0) ? 1u : 0u);
-        tc_commit(o_done);
-        tc_commit(v_empty + 8 * (i & 1));
+            for (int k = 0; k < kKeys / 16; ++k)
+              tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
+                     sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
+            tc_commit(o_done);
+            tc_commit(v_empty + 8 * (jp & 1));
+          }
+          __syncwarp();
+          ++jp;
+          progressed = true;
+        }
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(k_full + 8 * sb, (uint32_t)(j >> 1) & 1u, abort_flag, a.err) ||
-          (j >= 2 && !mbar_wait(s_free + 8 * sb, (uint32_t)((j - 2) >> 1) & 1u, abort_flag, a.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t kst = sK + sb * Lay::kSlot;
-      if (lane == 0) {
+      if (js < nkt && js <= jp + 1) {
+        const int sb = js & 1;
+        int ready = 0;
+        if (lane == 0)
+          ready = mbar_test_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u) &&
+                  (js < 2 || mbar_test_wait(s_free + 8 * sb, (uint32_t)((js - 2) >> 1) & 1u));
+        if (__shfl_sync(kAll, ready, 0)) {
+          tc_fence_after();
+          const uint32_t kst = sK + sb * Lay::kSlot;
+          if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(s_full + 8 * sb);
-        tc_commit(k_empty + 8 * sb);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(s_full + 8 * sb);
+            tc_commit(k_empty + 8 * sb);
+          }
+          __syncwarp();
+          ++js;
+          progressed = true;
+        }
       }
-      __syncwarp();
-      if (j >= 1 && !issue_pv(j - 1)) {
-        ok = false;
-        break;
+      if (progressed) {
+        idle_since = -1;
+      } else {
+        if (*abort_flag) break;
+        const long long now = clock64();
+        if (idle_since < 0) {
+          idle_since = now;
+        } else if (now - idle_since > kWaitCycles) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            flag_error(a.err, PKV_DEV_TIMEOUT);
+          }
+          break;
+        }
       }
     }
-    if (ok) issue_pv(nkt - 1);
     // Every MMA this thread issued has completed once `fin` fires (they complete in order).
     if (lane == 0) tc_commit(fin);
     __syncwarp();
     mbar_drain(fin, 0);
     tc_fence_before();
   } else {
-    // ---------------- tma warp: lanes 0-3 stage K blocks, lanes 4-7 V blocks ----------------
+    // ---------------- producer warps: warp 5 stages K, warp 6 V; lane b block b ----------------
     const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
-    const bool is_v = lane >= kTileBlocks;
-    const int b = lane & (kTileBlocks - 1);
+    const bool is_v = warp == 6;
     const uint32_t full = is_v ? v_full : k_full, empty = is_v ? v_empty : k_empty;
     const uint32_t ring = is_v ? sV : sK;
     const CUtensorMap *map = is_v ? &tv : &tk;
     int issued = 0;
-    if (lane < 2 * kTileBlocks) {
+    if (lane < kTileBlocks) {
+      // block ids are read one tile ahead, so their latency overlaps the slot waits
+      int next = lane * kBlockSize < kv_end ? table[lane] : INT_MIN;
       for (int j = 0; j < nkt; ++j) {
         const int slot = j & 1;
+        int blk = next;
+        const int tok_n = (j + 1) * kKeys + lane * kBlockSize;
+        next = (j + 1 < nkt && tok_n < kv_end) ? table[tok_n / kBlockSize] : INT_MIN;
         if (j >= 2 &&
             !mbar_wait(empty + 8 * slot, (uint32_t)((j - 2) >> 1) & 1u, abort_flag, a.err))
           break;
-        const int tok = j * kKeys + b * kBlockSize;
-        int blk = -1;
-        if (tok < kv_end) {
-          blk = table[tok / kBlockSize];
-          if (blk < 0 || blk >= a.num_blocks) {
-            flag_error(a.err, PKV_DEV_BAD_BLOCK);
-            blk = -1;
-          }
+        if (blk != INT_MIN && (blk < 0 || blk >= a.num_blocks)) {
+          flag_error(a.err, PKV_DEV_BAD_BLOCK);
+          blk = INT_MIN;
         }
         const uint32_t bar = full + 8 * slot;
-        mbar_arrive_expect_tx(bar, blk >= 0 ? 4096u : 0u);  // one head tile, two halves
-        if (blk >= 0) {
+        mbar_arrive_expect_tx(bar, blk != INT_MIN ? 4096u : 0u);  // one head tile, two halves
+        if (blk != INT_MIN) {
           const int row = (blk * a.num_kv_heads + g) * kBlockSize;
-          const uint32_t dst = ring + slot * Lay::kSlot + b * 2048;
+          const uint32_t dst = ring + slot * Lay::kSlot + lane * 2048;
           tma_load_2d(dst, map, 0, row, bar);
           tma_load_2d(dst + 8192, map, 64, row, bar);
         }
@@ -775,7 +798,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     }
     __syncwarp();
     // If a wait gave up, let the copies still in flight land before the CTA exits.
-    if ((lane == 0 || lane == kTileBlocks) && *abort_flag)
+    if (lane == 0 && *abort_flag)
       for (int j = max(0, issued - 2); j < issued; ++j)
         mbar_drain(full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
   }
