@@ -660,9 +660,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && o_seen < nkt - 1 &&
-        !mbar_wait(o_done, (uint32_t)(nkt - 1) & 1u, abort_flag, a.err))
-      ok = false;
+    // Every product has completed once the MMA warp's final commit fires.
+    if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
     if (ok && !*abort_flag) {
       tc_fence_after();
       const float inv = 1.f / l;
