@@ -554,6 +554,9 @@ def run_prefill(args):
     world, rank, local = setup_dist(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
+          "tc": ops.PKV_PREFILL_TC}[args.prefill_kernel]
+    ops.set_prefill_variant(pk)
     w = workloads.make_prefill_config(args.config, device="cuda")
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
     k = w.k_cache.to(dev).contiguous()
@@ -653,6 +656,9 @@ def run_prefill(args):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (attn_ms / 1e3) / 1e12
+    # AUTO runs the tcgen05 kernel for head_dim 128 and the mma.sync kernel for 64
+    tc = pk == ops.PKV_PREFILL_TC or (pk == ops.PKV_PREFILL_AUTO and D == 128)
+    kname = "prefill-tc" if tc else "prefill-mma"
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
@@ -664,6 +670,7 @@ def run_prefill(args):
             "head_dim": D, "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(w.context_lens.mean()), "max_context": w.max_context_len,
             "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
+            "prefill_kernel": kname,
             "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
                    "working set (KV + q + out) larger than twice L2"),
             "parallelism": "replicas" if world > 1 else "single"},
@@ -675,8 +682,10 @@ def run_prefill(args):
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.name, "prefill", PREFILL_SOURCES),
-                     "kernel": "paged_attention_prefill (prefill_kernel, mma.sync bf16)",
+                     "traffic": recorded_traffic(w.name, kname, PREFILL_SOURCES),
+                     "kernel": ("paged_attention_prefill: prefill_tc_kernel (tcgen05.mma, "
+                                "TMEM accumulators)" if tc else
+                                "paged_attention_prefill: prefill_kernel (mma.sync)"),
                      "peak_source": f"{peak_kind} bf16_tflops (burst)"},
         "clocks": clk.summary(),
     }
@@ -935,6 +944,9 @@ def main():
                     help="split-K partition size in tokens (default: the workload's, 512)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc"],
+                    help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc "
+                         "for head_dim 128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.config is None:
