@@ -33,6 +33,8 @@
 
 #include <atomic>
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 
 #include "tc_common.cuh"
 
@@ -382,8 +384,9 @@ struct TcLayout {
   static constexpr int kV = 81920;                   // 2 x 16 KB
   static constexpr int kSlot = 16384;
   static constexpr int kBars = 114688;
-  static constexpr int kNumBars = 15;                // K full/empty x2, V full/empty x2,
-                                                     // S full/free x2, P full, O done, final
+  static constexpr int kNumBars = 18;                // K full/empty x2, V full/empty x2,
+                                                     // S full/free x2, P full x2, O done,
+                                                     // final, P V done x2
   static constexpr int kSmem = kBars + kNumBars * 8 + 16;
 };
 
@@ -404,6 +407,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same with the A operand (M x K: one row per TMEM lane, two 16-bit elements per
+// 32-bit column, the lower k in the low half) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -458,6 +472,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                : "memory");
 }
 
+template <bool PT>
 __global__ void __launch_bounds__(kTcWarps * 32, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
@@ -475,7 +490,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   const uint32_t k_full = base + Lay::kBars, k_empty = k_full + 16;
   const uint32_t v_full = k_empty + 16, v_empty = v_full + 16;
   const uint32_t s_full = v_empty + 16, s_free = s_full + 16, p_full = s_free + 16;
-  const uint32_t o_done = p_full + 8, fin = o_done + 8;
+  const uint32_t o_done = p_full + 16, fin = o_done + 8, pv_done = fin + 8;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + Lay::kBars + Lay::kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -491,8 +506,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       mbar_init(v_empty + 8 * i, 1);
       mbar_init(s_full + 8 * i, 1);
       mbar_init(s_free + 8 * i, 4);
+      mbar_init(p_full + 8 * i, 4);
+      mbar_init(pv_done + 8 * i, 1);
     }
-    mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(fin, 1);
     *abort_flag = 0;
@@ -572,22 +588,29 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         tmem_ld32(tS + 64 * sb + 32 + lane_base, x1);
         tmem_wait_ld();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free + 8 * sb);
+      if (!PT) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free + 8 * sb);
+      }
 
       // Raw scores; keys past the row's position become -inf (diagonal tiles only).  The
       // max is taken on raw scores (scale > 0), the weights are 2^(scale s - m) by one
       // FFMA and one ex2 each.
+      // (Eight independent max chains and four sum chains keep the reductions short.)
       const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
-      float mx = -INFINITY;
+      float mxv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mxv[c] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         float v = __uint_as_float(x[c]);
         if (need_mask && t0 + c > pos) v = -INFINITY;
         x[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        mxv[c & 7] = fmaxf(mxv[c & 7], v);
       }
+      float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                       fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
       mx *= a.scale_log2;
       if (j == 0) {
         m = mx;  // key 0 is visible to every row
@@ -617,19 +640,18 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         }
       }
       uint32_t pk[32];
-      float ps0 = 0.f, ps1 = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
       const float sl = a.scale_log2, nm = -m;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), sl, nm));
         const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), sl, nm));
-        ps0 += p0;
-        ps1 += p1;
+        ps[c & 3] += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      l += ps0 + ps1;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       // The P tile is free once the previous P V product has completed.
-      if (j >= 1 && o_seen < j - 1) {
+      if (!PT && j >= 1 && o_seen < j - 1) {
         if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
           ok = false;
           break;
@@ -650,15 +672,24 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
           st_shared_v4(vst + (rem >> 3) * 8192 + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
         }
       }
-      const uint32_t prow = sP + t * 128;
+      if (PT) {
+        // P overwrites the first 32 columns of this tile's S buffer (already read).
+        if (t0 + kKeys > kv_end) fence_proxy_async();  // the zeroed V rows
+        tmem_st32(tS + 64 * sb + lane_base, pk);
+        tmem_wait_st();
+      } else {
+        const uint32_t prow = sP + t * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(prow + ((c ^ (t & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                     pk[4 * c + 3]);
-      fence_proxy_async();
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(prow + ((c ^ (t & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                       pk[4 * c + 3]);
+        fence_proxy_async();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      // Two P barriers (by tile parity): without the P-tile wait above (P in tensor
+      // memory) the softmax may finish tile j + 1 before the MMA warp has seen tile j.
+      if (lane == 0) mbar_arrive(p_full + 8 * sb);
     }
     // Every product has completed once the MMA warp's final commit fires.
     if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
@@ -699,18 +730,24 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       if (jp < js) {
         int ready = 0;
         if (lane == 0)
-          ready = mbar_test_wait(p_full, (uint32_t)jp & 1u) &&
+          ready = mbar_test_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u) &&
                   mbar_test_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u);
         if (__shfl_sync(kAll, ready, 0)) {
           tc_fence_after();
           const uint32_t vst = sV + (jp & 1) * Lay::kSlot;
           if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k)
-              tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
-                     sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kKeys / 16; ++k) {
+              if (PT)
+                tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k, sw128_desc(vst + 2048 * k, 8192, 1024),
+                          idO, (jp > 0 || k > 0) ? 1u : 0u);
+              else
+                tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
+                       sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
+            }
             tc_commit(o_done);
             tc_commit(v_empty + 8 * (jp & 1));
+            if (PT) tc_commit(pv_done + 8 * (jp & 1));
           }
           __syncwarp();
           ++jp;
@@ -721,8 +758,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         const int sb = js & 1;
         int ready = 0;
         if (lane == 0)
+          // S buffer sb is free once tile js - 2's scores were read (and, with P in
+          // tensor memory, its P V product -- which reads P from that buffer -- is done).
           ready = mbar_test_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u) &&
-                  (js < 2 || mbar_test_wait(s_free + 8 * sb, (uint32_t)((js - 2) >> 1) & 1u));
+                  (js < 2 || mbar_test_wait((PT ? pv_done : s_free) + 8 * sb,
+                                            (uint32_t)((js - 2) >> 1) & 1u));
         if (__shfl_sync(kAll, ready, 0)) {
           tc_fence_after();
           const uint32_t kst = sK + sb * Lay::kSlot;
@@ -811,24 +851,38 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   }
 }
 
-int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                      cudaStream_t st) {
+template <bool PT>
+int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                        cudaStream_t st) {
   using Lay = TcLayout;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
-        prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+        prefill_tc_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_tc_kernel,
+      e = cudaFuncSetAttribute(prefill_tc_kernel<PT>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  return (int)launch_pdl(prefill_tc_kernel,
+  return (int)launch_pdl(prefill_tc_kernel<PT>,
                          dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
                               (unsigned)a.num_seqs),
                          dim3(kTcWarps * 32), (size_t)Lay::kSmem, st, a, tk, tv);
+}
+
+// P staged in shared memory by default; PKV_PREFILL_P=tmem selects the variant that keeps
+// P in tensor memory (the A operand of P V read from TMEM), which measures the same.
+int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                      cudaStream_t st) {
+  static int p_in_tmem = -1;
+  if (p_in_tmem < 0) {
+    const char *v = std::getenv("PKV_PREFILL_P");
+    p_in_tmem = (v && std::strcmp(v, "tmem") == 0) ? 1 : 0;
+  }
+  return p_in_tmem ? launch_prefill_tc_t<true>(a, tk, tv, st)
+                   : launch_prefill_tc_t<false>(a, tk, tv, st);
 }
 
 std::atomic<int> g_prefill_variant{PKV_PREFILL_AUTO};
