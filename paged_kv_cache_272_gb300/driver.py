@@ -132,20 +132,17 @@ class ServingDriver:
             self._bufs[name] = buf
         return buf[0][:n].view(shape), buf[1][:n].view(shape)
 
-    def _h2d(self, name, arr, dtype):
+    def _put(self, name, arr, dtype):
+        """Stage a host array in its pinned buffer; returns (pinned view, device view)."""
         h, d = self._stage(name, tuple(arr.shape), dtype)
         h.copy_(torch.from_numpy(np.ascontiguousarray(arr)))
-        d.copy_(h, non_blocking=True)
-        self.h2d_bytes += h.numel() * h.element_size()
-        return d
+        return h, d
 
-    def _rows(self, name, table, rows):
-        idx = torch.from_numpy(rows)
+    def _put_rows(self, name, table, rows):
+        """Stage rows of a host table (the synthetic model's output) in a pinned buffer."""
         h, d = self._stage(name, (rows.shape[0],) + tuple(table.shape[1:]), table.dtype)
-        torch.index_select(table, 0, idx, out=h)
-        d.copy_(h, non_blocking=True)
-        self.h2d_bytes += h.numel() * h.element_size()
-        return d
+        torch.index_select(table, 0, torch.from_numpy(rows), out=h)
+        return h, d
 
     def fetch(self, *outs):
         """Copy a step's outputs to pinned host memory (what a sampler would read)."""
@@ -175,17 +172,29 @@ class ServingDriver:
         T = x.token_ids.shape[0]
         if T == 0:
             return x, None, None
+        # Host side first (the synthetic model's rows and the plan's arrays into pinned
+        # buffers), then the copies and kernels back to back on the stream.
+        staged = {"k": self._put_rows("k", self.k_tab, x.kv_rows),
+                  "v": self._put_rows("v", self.v_tab, x.kv_rows),
+                  "q": self._put_rows("q", self.q_tab, x.q_rows),
+                  "slots": self._put("slots", plan.slot_mapping, torch.int64),
+                  "tables": self._put("tables", plan.block_tables, torch.int32),
+                  "ctx": self._put("ctx", plan.context_lens, torch.int32)}
+        if plan.cow_pairs.size:
+            staged["pairs"] = self._put("pairs", plan.cow_pairs, torch.int32)
+        if plan.seq_ids.shape[0] > x.num_decode:
+            staged["pq"] = self._put("pq", x.prefill_query_start, torch.int32)
         if self.on_start is not None:
             self.on_start()
-        k_new = self._rows("k", self.k_tab, x.kv_rows)
-        v_new = self._rows("v", self.v_tab, x.kv_rows)
-        q = self._rows("q", self.q_tab, x.q_rows)
-        slots = self._h2d("slots", plan.slot_mapping, torch.int64)
-        tables = self._h2d("tables", plan.block_tables, torch.int32)
-        ctx = self._h2d("ctx", plan.context_lens, torch.int32)
+        dv = {}
+        for name, (h, d) in staged.items():
+            d.copy_(h, non_blocking=True)
+            self.h2d_bytes += h.numel() * h.element_size()
+            dv[name] = d
+        k_new, v_new, q = dv["k"], dv["v"], dv["q"]
+        slots, tables, ctx = dv["slots"], dv["tables"], dv["ctx"]
         if plan.cow_pairs.size:
-            pairs = self._h2d("pairs", plan.cow_pairs, torch.int32)
-            ops.paged_block_copy(self.k_cache, self.v_cache, pairs, err_flag=self.err,
+            ops.paged_block_copy(self.k_cache, self.v_cache, dv["pairs"], err_flag=self.err,
                                  stream=self.stream)
             self.launches += 1
         ops.paged_kv_write(k_new, v_new, slots, self.k_cache, self.v_cache, err_flag=self.err,
@@ -204,7 +213,7 @@ class ServingDriver:
                 self.on_decode(1)
             self.launches += 3 if x.decode_ctx_max > self.P else 2
         if plan.seq_ids.shape[0] > nd:
-            pq = self._h2d("pq", x.prefill_query_start, torch.int32)
+            pq = dv["pq"]
             pre_out = self._stage("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)[1]
             ops.paged_attention_prefill(pre_out, q[nd:], self.k_cache, self.v_cache, tables[nd:],
                                         ctx[nd:], pq, self.scale, x.prefill_max_query,
