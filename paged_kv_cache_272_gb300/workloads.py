@@ -210,6 +210,18 @@ def make_config(n: int, device="cpu", seed: int | None = None, **kw) -> Workload
     raise ValueError(n)
 
 
+def unique_kv_read_bytes(w: Workload) -> int:
+    """KV bytes of the distinct (physical block, token offset) slots a step reads: a
+    shared prefix block counts once however many tables point at it."""
+    depth = {}  # physical block -> tokens read from it (the deepest use if shared)
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        for b in range((n + w.block_size - 1) // w.block_size):
+            blk = int(w.block_tables[s, b])
+            depth[blk] = max(depth.get(blk, 0), min(w.block_size, n - b * w.block_size))
+    return sum(depth.values()) * 2 * w.num_kv_heads * w.head_dim * 2
+
+
 def kv_read_bytes(w: Workload) -> int:
     """Algorithmic KV bytes one decode step reads: every context token's K and V row
     for every KV head, once."""
