@@ -298,3 +298,35 @@ def test_driver_step_inputs_follow_the_plan():
         nd = plan.num_decode
         assert x.prefill_query_start.tolist() == (plan.query_start[nd:] - plan.query_start[nd]).tolist()
         assert (x.kv_rows == driver.kv_row(x.token_ids, x.positions, 4096)).all()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_native_scheduler_fuzz(seed):
+    """Random pools, slot counts, budgets, cache sizes and request mixes (including pools
+    small enough to force preemption and cache eviction): the native scheduler takes
+    the reference's decisions at every step."""
+    rng = np.random.default_rng(100 + seed)
+    kind = "shared-prefix" if seed % 2 else "pareto"
+    reqs = workloads.make_requests(kind, seed=200 + seed, n=int(rng.integers(10, 60)))
+    for r in reqs:
+        r.output_len = int(min(r.output_len, rng.integers(1, 200)))
+    seqs = int(rng.integers(1, 12))
+    budget = int(rng.integers(seqs, 600))
+    need = max((len(r.prompt) + r.output_len + 15) // 16 for r in reqs)
+    blocks = int(rng.integers(need + 1, need * 6))
+    cache = int(rng.integers(0, 200)) if kind == "shared-prefix" else None
+    static = bool(seed % 3 == 0)
+    order = rng.permutation(blocks)
+    ref, bm, rcache, rplans = ref_run(reqs, blocks, seqs, budget, static, cache, order)
+    nat, pool, ncache, nplans = native_run(reqs, blocks, seqs, budget, static, cache, order)
+    assert len(nplans) == len(rplans)
+    for a, b in zip(nplans, rplans):
+        assert a.seq_ids.tolist() == b.seqs
+        assert a.slot_mapping.tolist() == b.slots
+        assert a.context_lens.tolist() == b.context_lens
+        assert (a.finished, a.preempted) == (b.finished, b.preempted)
+    st = nat.stats()
+    assert (st["preemptions"], st["finished"]) == (ref.preemptions, ref.finished)
+    assert ref.finished == len(reqs)
+    if rcache is not None:
+        assert ncache.stats()["evictions"] == rcache.evictions
