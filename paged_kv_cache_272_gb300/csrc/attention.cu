@@ -313,9 +313,32 @@ __device__ __forceinline__ void warp_merge(const float *lse, const float *o, siz
   L = 0.f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  // Eight outputs at a time, every load of a batch issued before any use.
+  auto load8 = [&](int first, int cnt, float (&v)[8][PER]) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (first + u < cnt) {
+        const float *src = o + (size_t)(first + u) * stride * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+          v[u][0] = t.x, v[u][1] = t.y, v[u][2] = t.z, v[u][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+          v[u][0] = t.x, v[u][1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+      }
+    }
+  };
   for (int k0 = 0; k0 < n; k0 += 32) {
     const int cnt = min(32, n - k0);
     const float x = lane < cnt ? __ldcg(lse + (size_t)(k0 + lane) * stride) : -INFINITY;
+    // The first eight outputs do not depend on the weights: load them together with the
+    // lse values (one round trip for sequences with at most eight partitions).
+    float v[8][PER];
+    load8(k0, k0 + cnt, v);
     float mb = x;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
@@ -330,29 +353,13 @@ __device__ __forceinline__ void warp_merge(const float *lse, const float *o, siz
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] *= sc;
     for (int k = 0; k < cnt; k += 8) {
-      float c[8], v[8][PER];
+      if (k > 0) load8(k0 + k, k0 + cnt, v);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        c[u] = __shfl_sync(kFull, w, (k + u) & 31);
-        if (k + u < cnt) {
-          const float *src = o + (size_t)(k0 + k + u) * stride * D + lane * PER;
-          if constexpr (PER == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-            v[u][0] = t.x, v[u][1] = t.y, v[u][2] = t.z, v[u][3] = t.w;
-          } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-            v[u][0] = t.x, v[u][1] = t.y;
-          }
-        } else {
-          c[u] = 0.f;
+        const float c = k + u < cnt ? __shfl_sync(kFull, w, (k + u) & 31) : 0.f;
 #pragma unroll
-          for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
-        }
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(c, v[u][e], acc[e]);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = fmaf(c[u], v[u][e], acc[e]);
     }
   }
 }
