@@ -330,3 +330,44 @@ def test_native_scheduler_fuzz(seed):
     assert ref.finished == len(reqs)
     if rcache is not None:
         assert ncache.stats()["evictions"] == rcache.evictions
+
+
+def test_native_serving_api_rejects_bad_arguments():
+    import ctypes
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.ops import lib
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
+    ERR_NULL, ERR_ARG, ERR_DUP = -1, -14, -12
+    h = ctypes.c_void_p()
+    assert lib.pkv_pcache_create(None, 4, ctypes.byref(h)) == ERR_NULL
+    pool = BlockPool(8)
+    assert lib.pkv_pcache_create(pool._h, -1, ctypes.byref(h)) == ERR_ARG
+    assert lib.pkv_sched_create(pool._h, None, 0, 16, 0, ctypes.byref(h)) == ERR_ARG
+    assert lib.pkv_sched_create(pool._h, None, 8, 4, 0, ctypes.byref(h)) == ERR_ARG  # budget < slots
+    other = BlockPool(8)
+    c_other = PrefixCache(other, 4)
+    assert lib.pkv_sched_create(pool._h, c_other._h, 2, 16, 0, ctypes.byref(h)) == ERR_ARG
+    s = Scheduler(pool, 2, 16)
+    assert lib.pkv_sched_add_request(s._h, 1, 0, None, 3) == ERR_ARG      # empty prompt
+    assert lib.pkv_sched_add_request(s._h, 1, 4, None, 0) == ERR_ARG      # no output token
+    assert lib.pkv_sched_add_request(s._h, 1, 4, None, 3) == 0
+    assert lib.pkv_sched_add_request(s._h, 1, 4, None, 3) == ERR_DUP
+    # a cached block must be allocated; a table too short for the prompt is refused
+    cache = PrefixCache(pool, 4)
+    toks = np.arange(32, dtype=np.int32)
+    table = np.array([0], dtype=np.int32)
+    assert lib.pkv_pcache_insert(cache._h, toks.ctypes.data, 32, table.ctypes.data, 1) == ERR_ARG
+    assert lib.pkv_block_retain(pool._h, 3) == ERR_ARG   # free block
+    assert lib.pkv_block_release(pool._h, 99) == ERR_ARG
+    assert lib.pkv_seq_add_shared(pool._h, 5, table.ctypes.data, 1) == ERR_ARG  # block 0 free
+
+
+def test_pool_too_small_native():
+    from paged_kv_cache_272_gb300.block_pool import BlockPool, OutOfBlocks
+    from paged_kv_cache_272_gb300.serving import Scheduler
+    pool = BlockPool(4)
+    s = Scheduler(pool, 2, 256)
+    s.add_request(0, np.arange(100, dtype=np.int32), 5)
+    with pytest.raises(OutOfBlocks):
+        while not s.done():
+            s.step()
