@@ -30,6 +30,7 @@ import time
 
 import numpy as np
 import torch
+from torch.cuda import nvtx
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -363,17 +364,23 @@ def run_ours(args):
             torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
+        nvtx.range_push("timed decode steps")
         for i in range(args.steps):
             if flush:
                 scratch.zero_()
             e0, e1, e2 = ev[i]
+            nvtx.range_push(f"step {i}")
             e0.record(stream)
             if pairs.numel():
                 do_copy(pairs)
             do_write(k_new, v_new, slots)
             e1.record(stream)
+            nvtx.range_push("paged_attention_decode")
             do_attn(q, bt, ctx)
+            nvtx.range_pop()
             e2.record(stream)
+            nvtx.range_pop()
+        nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
         t_end = time.perf_counter() + 0.4
@@ -614,15 +621,21 @@ def run_prefill(args):
             torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
+        nvtx.range_push("timed prefill steps")
         for i in range(args.steps):
             if flush:
                 scratch.zero_()
             e0, e1, e2 = ev[i]
+            nvtx.range_push(f"step {i}")
             e0.record(stream)
             do_write(k_new, v_new, slots)
             e1.record(stream)
+            nvtx.range_push("paged_attention_prefill")
             do_attn(q, bt, ctx, qs)
+            nvtx.range_pop()
             e2.record(stream)
+            nvtx.range_pop()
+        nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
         t_end = time.perf_counter() + 0.4
@@ -752,7 +765,9 @@ def serve_run(drv, stream, decode_bytes_per_token):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dec_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
         drv.on_start = lambda: a.record(stream)
+        nvtx.range_push(f"serving step {steps}")
         x, dec, pre = drv.step()
+        nvtx.range_pop()
         if x.token_ids.shape[0] == 0:
             continue
         nd = x.num_decode

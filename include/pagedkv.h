@@ -87,6 +87,15 @@ int paged_kv_write(const uint16_t *k_new, const uint16_t *v_new, const int64_t *
                    void *stream);
 
 /*
+ * paged_kv_check_slots -- host-side validation of a slot mapping (HOST memory) before it
+ * is used by paged_kv_write: PKV_OK, or PKV_ERR_ARG if a slot is >= num_blocks *
+ * block_size or two tokens share a slot (the writes would race).  Negative slots are
+ * padding and ignored.  O(n log n); a debugging aid, not part of the step.
+ */
+int paged_kv_check_slots(const int64_t *slot_mapping, int num_tokens, int num_blocks,
+                         int block_size);
+
+/*
  * paged_block_copy -- copy-on-write of whole blocks.
  * For every pair i: k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], all KV
  * heads, bit-exact.  The dsts of one call must be distinct and no dst may be the src of

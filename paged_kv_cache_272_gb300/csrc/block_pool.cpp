@@ -11,6 +11,7 @@
 // free_order (first element handed out first); a freed block goes on top.  Every
 // failing call leaves the pool unchanged: the block demand of a call is counted before
 // anything is modified.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -237,6 +238,23 @@ int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_bl
     context_lens[i] = (int32_t)sq.num_tokens;
   }
   return PKV_OK;
+}
+
+int paged_kv_check_slots(const int64_t *slot_mapping, int num_tokens, int num_blocks,
+                         int block_size) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0) return PKV_ERR_ARG;
+  if (num_tokens > 0 && !slot_mapping) return PKV_ERR_NULL;
+  const int64_t limit = (int64_t)num_blocks * block_size;
+  std::vector<int64_t> live;
+  live.reserve((size_t)num_tokens);
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;  // padding
+    if (s >= limit) return PKV_ERR_ARG;
+    live.push_back(s);
+  }
+  std::sort(live.begin(), live.end());
+  return std::adjacent_find(live.begin(), live.end()) == live.end() ? PKV_OK : PKV_ERR_ARG;
 }
 
 }  // extern "C"

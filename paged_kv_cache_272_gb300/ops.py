@@ -28,6 +28,7 @@ SIGNATURES = {
     "paged_kv_strerror": (ctypes.c_char_p, [_I]),
     "paged_kv_write": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
     "paged_block_copy": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "paged_kv_check_slots": (_I, [_P, _I, _I, _I]),
     "paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _I, _P, _SZ, _P, _P]),
@@ -134,6 +135,14 @@ def paged_kv_write(k_new, v_new, slot_mapping, k_cache, v_cache, err_flag=None, 
     check(lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping.contiguous()), T,
                              _ptr(k_cache), _ptr(v_cache), NB, Hkv, D, bs, _ptr(err_flag),
                              _stream(stream)), "paged_kv_write")
+
+
+def paged_kv_check_slots(slot_mapping, num_blocks, block_size=16) -> None:
+    """Raise if a host slot mapping has an out-of-range or repeated slot."""
+    import numpy as np
+    a = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    check(lib.paged_kv_check_slots(a.ctypes.data if a.size else None, a.shape[0], num_blocks,
+                                   block_size), "paged_kv_check_slots")
 
 
 def paged_block_copy(k_cache, v_cache, block_pairs, err_flag=None, stream=None):

@@ -94,3 +94,14 @@ def test_workspace_size_formula():
     chunk = S * C * Hq * (D + 1) * 4
     assert n >= part + chunk
     assert n < part + chunk + S * P * 16 + S * G8 * C * 16 + S * Hq * 4 + S * 4 + 16 * 256
+
+
+def test_slot_mapping_check():
+    import numpy as np
+    from paged_kv_cache_272_gb300 import ops
+    ops.paged_kv_check_slots(np.array([0, 5, 17, -1, -1, 63]), 4)
+    ops.paged_kv_check_slots(np.zeros(0, np.int64), 4)
+    with pytest.raises(ops.PagedKVError):
+        ops.paged_kv_check_slots(np.array([3, 9, 3]), 4)       # two tokens, one slot
+    with pytest.raises(ops.PagedKVError):
+        ops.paged_kv_check_slots(np.array([64]), 4)             # past the pool

@@ -371,3 +371,12 @@ def test_pool_too_small_native():
     with pytest.raises(OutOfBlocks):
         while not s.done():
             s.step()
+
+
+def test_scheduler_plans_pass_the_slot_check():
+    """Every step's slot mapping from the native scheduler is in range and race free."""
+    from paged_kv_cache_272_gb300 import ops
+    reqs = workloads.make_requests("shared-prefix", seed=31, n=80)
+    nat, pool, cache, plans = native_run(reqs, 300, 8, 256, cache_entries=40)
+    for p in plans:
+        ops.paged_kv_check_slots(p.slot_mapping, 300)
