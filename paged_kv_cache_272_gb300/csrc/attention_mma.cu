@@ -68,10 +68,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-// Two E4M3 codes (low byte first) -> f16x2, exactly (every E4M3 value is an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes (lowest byte first) -> two f16x2 words (codes 0-1, codes 2-3), exactly:
+// the 32-bit word is split into its two 16-bit halves in registers and each half
+// converted by one cvt.rn.f16x2.e4m3x2.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -392,9 +396,10 @@ __global__ void __launch_bounds__((NW + 1) * 32,
           for (int kk = 0; kk < KSTEPS; ++kk) {
             const uint32_t w0 = lds32(kst + (koffA ^ (uint32_t)(kk << 4)));
             const uint32_t w1 = lds32(kst + (koffB ^ (uint32_t)(kk << 4)));
-            mma16816_f16(sc, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
-                         e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), qb[kk][0],
-                         qb[kk][1]);
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(w0, a0, a2);
+            e4m3x4_to_f16x2x2(w1, a1, a3);
+            mma16816_f16(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
           }
         } else {
 #pragma unroll
@@ -445,19 +450,25 @@ __global__ void __launch_bounds__((NW + 1) * 32,
           // V^T[d][token] fragments straight from the transposed codes: head_dim rows
           // 16 mt + gid (+8), tokens 4 tig .. 4 tig + 3 = k-slots 2 tig, +1, 2 tig + 8, +9.
           // Codes of tokens past the end of the context are masked to +0.
-          uint32_t vmask = 0xffffffffu;
-          if (nvalid < kBlockSize) {
-            vmask = 0u;
+          auto pv8 = [&](uint32_t vmask) {
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              const uint32_t w0 = lds32(vst + (16 * mt + gid) * 16 + 4 * tig) & vmask;
+              const uint32_t w1 = lds32(vst + (16 * mt + gid + 8) * 16 + 4 * tig) & vmask;
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma16816_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+            }
+          };
+          if (nvalid == kBlockSize) {
+            pv8(0xffffffffu);  // a full block: no mask (the AND folds away)
+          } else {
+            uint32_t vmask = 0u;
 #pragma unroll
             for (int b = 0; b < 4; ++b)
               if (4 * tig + b < nvalid) vmask |= 0xffu << (8 * b);
-          }
-#pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            const uint32_t w0 = lds32(vst + (16 * mt + gid) * 16 + 4 * tig) & vmask;
-            const uint32_t w1 = lds32(vst + (16 * mt + gid + 8) * 16 + 4 * tig) & vmask;
-            mma16816_f16(acc[mt], e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
-                         e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16), b0, b1);
+            pv8(vmask);
           }
         } else {
           const int j4 = lane >> 3;
