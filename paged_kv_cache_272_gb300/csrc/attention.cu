@@ -49,12 +49,14 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
   const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
   const int P = a.part_tokens;
   const int G8 = (a.num_q_heads + 7) / 8;
+  int first_c = 0;  // this thread's first sequence's (validated) length, kept for pass 2
   for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
     int c = a.context_lens[s];
     if (c < 0 || c > cap) {
       flag_error(a.err, PKV_DEV_BAD_CONTEXT);
       c = 0;
     }
+    if (s == threadIdx.x) first_c = c;
     const int n = (c + P - 1) / P;
     a.nparts[s] = n;
     if (n == 0) {  // no partition will write this sequence's output
@@ -87,9 +89,10 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int h
   }
   __syncthreads();
   for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
-    const int n = a.nparts[s];
+    // validated in pass 1 (a length is re-read only past the first 1024 sequences)
+    const int c = s == threadIdx.x ? first_c : (a.nparts[s] ? a.context_lens[s] : 0);
+    const int n = (c + P - 1) / P;
     if (n == 0) continue;
-    const int c = a.context_lens[s];  // validated above (n > 0)
     const int nfull = c / P, tail = c - nfull * P;
     if (nfull) {
       int pos = atomicAdd(&cursor[min(P / kBlockSize, 32)], nfull);
