@@ -17,7 +17,9 @@
 //    signalled on the slot's "full" mbarrier with the byte count.  The consumer frees
 //    the slot through its "empty" mbarrier.  Every wait is bounded.
 //  * (E4M3 cache: K tiles by TMA as above, V tiles -- stored transposed, [d][16] -- by a
-//    plain bulk copy; codes convert to f16 in registers, see the KV8 branches.)
+//    plain bulk copy; a ring stage holds two blocks, so a stage carries the bytes of one
+//    bf16 block and one softmax update covers 32 tokens; codes convert to f16 in
+//    registers, see the KV8 branches.)
 //  * A consumer computes S^T[16 tokens x 8 heads] = K Q^T with mma.m16n8k16 (tokens are
 //    the M dimension, the query group is N, head_dim is K), so a GQA-8 group fills the
 //    tile exactly; Q^T fragments live in registers for the whole item.  The softmax
@@ -25,9 +27,11 @@
 //    with movmatrix (an 8x8 transpose in registers), and O^T[head_dim x 8] += V^T P^T is
 //    a second set of mma tiles whose A operand ldmatrix.trans reads straight from the
 //    staged V tile.  The sum of the weights uses the same rounded values.
-//  * At the end of an item the NW warp states (max, sum, O) are merged in shared
-//    memory, and the item's result goes to `out` (one partition) or to the split-K
-//    partials (merged by the LSE merge kernel).
+//  * At the end of an item each consumer warp writes its state (max, sum, O tiles) into
+//    the last ring stage it consumed, which it keeps until the merge is done (no merge
+//    buffer: the shared memory goes to more CTAs per SM); each warp then merges a slice
+//    of head_dim across the NW states, and the item's result goes to `out` (one
+//    partition) or to the split-K partials (merged by the LSE merge kernel).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -66,6 +70,19 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, float &a, float &b, float &c, float &d) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+               : "r"(addr)
+               : "memory");
 }
 
 // Four E4M3 codes (lowest byte first) -> two f16x2 words (codes 0-1, codes 2-3), exactly:
@@ -138,20 +155,24 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qb)[D / 16][2], const Att
 template <int D, int NW, int NS, bool KV8 = false>
 struct MmaLayout {
   static constexpr int kTile = kBlockSize * D * (KV8 ? 1 : 2);  // one K (or V) head tile
-  static constexpr int kStage = 2 * kTile;
-  static constexpr int kRow = D + 4;                 // padded merge row (floats)
+  // Blocks per ring stage: two for the E4M3 cache, so that a stage carries as many bytes
+  // (and a consumer step as many tokens per softmax update) as one bf16 block.
+  static constexpr int kBps = KV8 ? 2 : 1;
+  static constexpr int kStage = 2 * kTile * kBps;  // [K0 V0 (K1 V1)]
   static constexpr int kRing = 4;                    // item slots producer -> consumers
   static constexpr int kStagesBytes = NW * NS * kStage;
-  static constexpr int kMergeBytes = NW * 8 * kRow * 4 + 2 * NW * 8 * 4;
+  // Item-end merge: each consumer warp leaves its state (float4 chunks [KSTEPS + 1][32
+  // lanes]) in the last stage it consumed, so the merge needs no buffer of its own.
+  static_assert((D / 16 + 1) * 32 * 16 <= kStage, "warp state must fit in one stage");
   // mbarriers (block full/empty, item full/empty), item records, then ints
   static constexpr int kCtlBytes =
-      (2 * NW * NS + 2 * kRing) * 8 + (kRing + 1) * 16 + (kRing + 2 + NW * NS) * 4 + 16;
-  static constexpr int kSmem = 1024 + kStagesBytes + kMergeBytes + kCtlBytes;
+      (2 * NW * NS + 2 * kRing) * 8 + (kRing + 1) * 16 + (kRing + 2 + NW * NS + NW) * 4 + 16;
+  static constexpr int kSmem = 1024 + kStagesBytes + kCtlBytes;
 };
 
 template <int D, int NW, int NS, bool KV8>
 __global__ void __launch_bounds__((NW + 1) * 32,
-                                  NW == 1 ? 8 : (NW <= 2 ? 4 : (NW <= 3 ? 3 : (NW <= 4 ? 2 : 1))))
+                                  NW == 1 ? 8 : (NW <= 2 ? 5 : (NW <= 3 ? 4 : (NW <= 4 ? 2 : 1))))
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
   using L = MmaLayout<D, NW, NS, KV8>;
@@ -162,16 +183,14 @@ __global__ void __launch_bounds__((NW + 1) * 32,
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   unsigned char *base = smem_raw + (base_u32 - raw_u32);
-  float *red_o = reinterpret_cast<float *>(base + L::kStagesBytes);         // [NW][8][kRow]
-  float *red_m = red_o + NW * 8 * L::kRow;                                   // [NW][8]
-  float *red_l = red_m + NW * 8;                                             // [NW][8]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(red_l + NW * 8);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base + L::kStagesBytes);
   int4 *ring_rec = reinterpret_cast<int4 *>(bars + 2 * NW * NS + 2 * L::kRing);  // [kRing]
   volatile int4 *cons_rec = ring_rec + L::kRing;
   int *ring_item = reinterpret_cast<int *>(ring_rec + L::kRing + 1);         // [kRing]
   volatile int *cons_item = ring_item + L::kRing;
   volatile int *abort_flag = cons_item + 1;
   int *valid = const_cast<int *>(abort_flag) + 1;                            // [NW][NS]
+  volatile uint32_t *state_at = reinterpret_cast<volatile uint32_t *>(valid + NW * NS);  // [NW]
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + NW * NS * 8;
   const uint32_t ifull0 = empty0 + NW * NS * 8, iempty0 = ifull0 + L::kRing * 8;
 
@@ -199,10 +218,12 @@ __global__ void __launch_bounds__((NW + 1) * 32,
     // ------------------------------- producer -------------------------------------
     // Items are claimed from the plan's list (largest first) through a global counter,
     // one item ahead, and announced to the consumers through a small ring of item
-    // slots.  Lane w < NW feeds consumer warp w: block jb of an item goes to lane
-    // jb % NW, so the lanes issue their copies side by side.  Lane w counts the blocks
-    // it handed to warp w (ring slot = count % NS, phase = count / NS).
-    int cnt = 0;               // blocks handed to warp `lane` so far
+    // slots.  Lane w < NW feeds consumer warp w: stage js of an item (blocks
+    // kBps js .. kBps js + kBps - 1) goes to lane js % NW, so the lanes issue their
+    // copies side by side.  Lane w counts the stages it handed to warp w (ring slot =
+    // count % NS, phase = count / NS).
+    constexpr int BPS = L::kBps;
+    int cnt = 0;               // stages handed to warp `lane` so far
     int pslot = 0, pphase = 0;  // = cnt % NS, (cnt / NS) & 1, kept incrementally
     bool stop = false;
     auto claim = [&]() -> int {
@@ -238,40 +259,56 @@ __global__ void __launch_bounds__((NW + 1) * 32,
       const int g = (cur % per_pair) / a.sub_groups;
       const int nblk = (rec.z - rec.y + kBlockSize - 1) / kBlockSize;
       const int32_t *bt = a.block_tables + (size_t)rec.x * a.max_blocks + rec.y / kBlockSize;
-      // Block ids come 32 lanes at a time, in chunks of CH (a multiple of NW) so that
-      // block jb = c + r + lane always lands on warp jb % NW.
-      constexpr int CH = (32 / NW) * NW;
+      // Block ids come 32 lanes at a time, in chunks of CH (a multiple of NW * BPS) so
+      // that the blocks of stage js = (c + r) / BPS + lane always land on warp js % NW.
+      constexpr int CH = (32 / (NW * BPS)) * NW * BPS;
       for (int c = 0; c < nblk && !stop; c += CH) {
         const int blk_lane = c == 0 ? chunk0 : (c + lane < nblk ? bt[c + lane] : 0);
         const int n = min(CH, nblk - c);
-        for (int r = 0; r < n; r += NW) {
-          const int b = __shfl_sync(kFull, blk_lane, (r + lane) & 31);
+        for (int r = 0; r < n; r += NW * BPS) {
+          int bj[BPS];
+#pragma unroll
+          for (int j = 0; j < BPS; ++j)
+            bj[j] = __shfl_sync(kFull, blk_lane, (r + BPS * lane + j) & 31);
           int ok = 1;
-          if (lane < NW && r + lane < n) {
+          if (lane < NW && r + BPS * lane < n) {
             const int slot = pslot;
             const uint32_t fb = full0 + 8 * (lane * NS + slot);
             ok = mbar_wait(empty0 + 8 * (lane * NS + slot), pphase ^ 1, abort_flag, a.err);
             if (ok) {
-              if ((unsigned)b >= (unsigned)a.num_blocks) {
-                flag_error(a.err, PKV_DEV_BAD_BLOCK);
-                valid[lane * NS + slot] = 0;
+              // bit j: block j of the stage exists and its id is inside the pool
+              int vbits = 0;
+#pragma unroll
+              for (int j = 0; j < BPS; ++j) {
+                if (r + BPS * lane + j >= n) continue;
+                if ((unsigned)bj[j] >= (unsigned)a.num_blocks)
+                  flag_error(a.err, PKV_DEV_BAD_BLOCK);
+                else
+                  vbits |= 1 << j;
+              }
+              valid[lane * NS + slot] = vbits;
+              if (vbits == 0) {
                 mbar_arrive(fb);
               } else {
-                valid[lane * NS + slot] = 1;
-                mbar_arrive_expect_tx(fb, L::kStage);
-                const uint32_t dst = base_u32 + (uint32_t)((lane * NS + slot) * L::kStage);
-                const int y = (b * a.num_kv_heads + g) * kBlockSize;
-                if constexpr (KV8) {
-                  // K: one [16][128 B] swizzled box; V (stored [d][16]): 2 KB contiguous
-                  tma_load_2d(dst, &tk, 0, y, fb);
-                  bulk_load(dst + L::kTile,
-                            static_cast<const uint8_t *>(a.v_cache) + (size_t)y * D, L::kTile,
-                            fb);
-                } else {
+                mbar_arrive_expect_tx(fb, __popc(vbits) * 2 * L::kTile);
 #pragma unroll
-                  for (int h = 0; h < HALVES; ++h) {
-                    tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
-                    tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                for (int j = 0; j < BPS; ++j) {
+                  if (!((vbits >> j) & 1)) continue;
+                  const uint32_t dst =
+                      base_u32 + (uint32_t)((lane * NS + slot) * L::kStage + j * 2 * L::kTile);
+                  const int y = (bj[j] * a.num_kv_heads + g) * kBlockSize;
+                  if constexpr (KV8) {
+                    // K: one [16][128 B] swizzled box; V (stored [d][16]): 2 KB contiguous
+                    tma_load_2d(dst, &tk, 0, y, fb);
+                    bulk_load(dst + L::kTile,
+                              static_cast<const uint8_t *>(a.v_cache) + (size_t)y * D, L::kTile,
+                              fb);
+                  } else {
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h) {
+                      tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
+                      tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                    }
                   }
                 }
               }
@@ -354,7 +391,9 @@ __global__ void __launch_bounds__((NW + 1) * 32,
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-    for (int jb = warp; jb < nblk; jb += NW) {
+    const int nstage = (nblk + L::kBps - 1) / L::kBps;
+    int held = -1;  // ring slot this warp keeps until the item's merge is done
+    for (int jb = warp; jb < nstage; jb += NW) {
       const int slot = cslot;
       const uint32_t par = cphase;
       if (++cslot == NS) {
@@ -364,93 +403,78 @@ __global__ void __launch_bounds__((NW + 1) * 32,
       const uint32_t fb = full0 + 8 * (warp * NS + slot);
       int ok = mbar_wait(fb, par, abort_flag, a.err);
       ok = __all_sync(kFull, ok);
-      if (!ok) continue;  // aborted: keep the item/barrier sequence, skip the work
-      const int nvalid = min(kBlockSize, t1 - (t0 + jb * kBlockSize));
+      if (!ok) continue;  // aborted: keep the item/barrier sequence, skip the work (the
+                          // slot is not released: the producer has stopped)
       const uint32_t kst = base_u32 + (uint32_t)((warp * NS + slot) * L::kStage);
-      const uint32_t vst = kst + L::kTile;
-      if (valid[warp * NS + slot]) {
-        if (!KV8 && nvalid < kBlockSize) {
-          // Rows past the end of the context may hold anything (even NaN): zero them in
-          // V so that their zero weights contribute exactly nothing.  (The E4M3 path masks
-          // those codes in registers instead.)
-          unsigned char *vrow = base + (vst - base_u32);
-          {
-            const int nz = (kBlockSize - nvalid) * (D / 8);
-            for (int i = lane; i < nz; i += 32) {
-              const int row = nvalid + i / (D / 8), ch = i % (D / 8);
-              *reinterpret_cast<uint4 *>(vrow + (ch >> 3) * 2048 + row * 128 + (ch & 7) * 16) =
-                  make_uint4(0, 0, 0, 0);
+      if constexpr (KV8) {
+        // Two blocks per stage (2 jb, 2 jb + 1); a block that is absent (past the end of
+        // the item) or whose id was rejected counts as having no valid token.
+        const int vb = valid[warp * NS + slot];
+        int nv[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          nv[j] = ((vb >> j) & 1) ? max(0, min(kBlockSize, t1 - (t0 + (2 * jb + j) * kBlockSize)))
+                                  : 0;
+        if (nv[0] | nv[1]) {
+          // S^T = K Q^T per block (rows: tokens tokA8, tokB8; columns: heads 2 tig, +1).
+          // Tile row m of S^T holds token tokA8 (m = gid) / tokB8 (m = gid + 8), a token
+          // order in which the P.V operand's four k-slots of a thread are four
+          // consecutive tokens (the transposed V codes of one head_dim row).
+          float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (nv[j] == 0) continue;
+            const uint32_t kj = kst + (uint32_t)(j * 2 * L::kTile);
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+              const uint32_t w0 = lds32(kj + (koffA ^ (uint32_t)(kk << 4)));
+              const uint32_t w1 = lds32(kj + (koffB ^ (uint32_t)(kk << 4)));
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma16816_f16(sc[j], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
           }
-          __syncwarp();
-        }
-        // S^T = K Q^T  (rows: tokens gid, gid + 8; columns: heads 2 tig, 2 tig + 1)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        // E4M3 path: tile row m of S^T holds token tokA (m = gid) / tokB (m = gid + 8), a
-        // token order in which the P.V operand's four k-slots of a thread are four
-        // consecutive tokens (the transposed V codes of one head_dim row).
-        const int tokA = KV8 ? tokA8 : gid;
-        const int tokB = KV8 ? tokB8 : gid + 8;
-        if constexpr (KV8) {
+          float x[2][4];
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            const uint32_t w0 = lds32(kst + (koffA ^ (uint32_t)(kk << 4)));
-            const uint32_t w1 = lds32(kst + (koffB ^ (uint32_t)(kk << 4)));
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(w0, a0, a2);
-            e4m3x4_to_f16x2x2(w1, a1, a3);
-            mma16816_f16(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[j][i] = sc[j][i] * a.scale_log2;
+            if (tokA8 >= nv[j]) x[j][0] = x[j][1] = -INFINITY;
+            if (tokB8 >= nv[j]) x[j][2] = x[j][3] = -INFINITY;
           }
-        } else {
+          float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+          float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            // column 16 kk + 8 (lane >> 4): half kk / 4, chunk (2 kk + (lane >> 4)) & 7
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kst + (uint32_t)((kk >> 2) * 2048) + (koff16 ^ (uint32_t)(((2 * kk) & 7) << 4)),
-                    a0, a1, a2, a3);
-            mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
           }
-        }
-        float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
-        float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
-        if (tokA >= nvalid) x0 = x1 = -INFINITY;
-        if (tokB >= nvalid) x2 = x3 = -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+          const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+          const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+          m0 = n0;
+          m1 = n1;
+          uint32_t p01[2], p23[2];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-        }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        uint32_t p01, p23;
-        if constexpr (KV8) {
-          p01 = pack_f16(exp2f(x0 - m0), exp2f(x1 - m1));
-          p23 = pack_f16(exp2f(x2 - m0), exp2f(x3 - m1));
-          l0 = fmaf(l0, al0, f16_lo(p01) + f16_lo(p23));
-          l1 = fmaf(l1, al1, f16_hi(p01) + f16_hi(p23));
-        } else {
-          p01 = pack_bf16(exp2f(x0 - m0), exp2f(x1 - m1));
-          p23 = pack_bf16(exp2f(x2 - m0), exp2f(x3 - m1));
-          l0 = fmaf(l0, al0, bf16_lo(p01) + bf16_lo(p23));
-          l1 = fmaf(l1, al1, bf16_hi(p01) + bf16_hi(p23));
-        }
+          for (int j = 0; j < 2; ++j) {
+            p01[j] = pack_f16(exp2f(x[j][0] - m0), exp2f(x[j][1] - m1));
+            p23[j] = pack_f16(exp2f(x[j][2] - m0), exp2f(x[j][3] - m1));
+          }
+          // the sum of the weights uses the rounded (f16) values that multiply V
+          l0 = fmaf(l0, al0, (f16_lo(p01[0]) + f16_lo(p23[0])) + (f16_lo(p01[1]) + f16_lo(p23[1])));
+          l1 = fmaf(l1, al1, (f16_hi(p01[0]) + f16_hi(p23[0])) + (f16_hi(p01[1]) + f16_hi(p23[1])));
 #pragma unroll
-        for (int mt = 0; mt < KSTEPS; ++mt) {
-          acc[mt][0] *= al0;
-          acc[mt][1] *= al1;
-          acc[mt][2] *= al0;
-          acc[mt][3] *= al1;
-        }
-        // P^T as the B operand of O^T += V^T P^T.
-        const uint32_t b0 = movmatrix_t(p01), b1 = movmatrix_t(p23);
-        if constexpr (KV8) {
-          // V^T[d][token] fragments straight from the transposed codes: head_dim rows
-          // 16 mt + gid (+8), tokens 4 tig .. 4 tig + 3 = k-slots 2 tig, +1, 2 tig + 8, +9.
-          // Codes of tokens past the end of the context are masked to +0.
-          auto pv8 = [&](uint32_t vmask) {
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+          // O^T += V^T P^T per block, P^T as the B operand (movmatrix), V^T[d][token]
+          // fragments straight from the transposed codes: head_dim rows 16 mt + gid (+8),
+          // tokens 4 tig .. 4 tig + 3 = k-slots 2 tig, +1, 2 tig + 8, +9.  Codes of tokens
+          // past the end of the context are masked to +0.
+          auto pv8 = [&](uint32_t vst, uint32_t b0, uint32_t b1, uint32_t vmask) {
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) {
               const uint32_t w0 = lds32(vst + (16 * mt + gid) * 16 + 4 * tig) & vmask;
@@ -461,16 +485,77 @@ __global__ void __launch_bounds__((NW + 1) * 32,
               mma16816_f16(acc[mt], a0, a1, a2, a3, b0, b1);
             }
           };
-          if (nvalid == kBlockSize) {
-            pv8(0xffffffffu);  // a full block: no mask (the AND folds away)
-          } else {
-            uint32_t vmask = 0u;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              if (4 * tig + b < nvalid) vmask |= 0xffu << (8 * b);
-            pv8(vmask);
+          for (int j = 0; j < 2; ++j) {
+            if (nv[j] == 0) continue;
+            const uint32_t b0 = movmatrix_t(p01[j]), b1 = movmatrix_t(p23[j]);
+            const uint32_t vst = kst + (uint32_t)(j * 2 * L::kTile + L::kTile);
+            if (nv[j] == kBlockSize) {
+              pv8(vst, b0, b1, 0xffffffffu);  // a full block: no mask (the AND folds away)
+            } else {
+              uint32_t vmask = 0u;
+#pragma unroll
+              for (int b = 0; b < 4; ++b)
+                if (4 * tig + b < nv[j]) vmask |= 0xffu << (8 * b);
+              pv8(vst, b0, b1, vmask);
+            }
           }
-        } else {
+        }
+      } else {
+        const int nvalid = min(kBlockSize, t1 - (t0 + jb * kBlockSize));
+        const uint32_t vst = kst + L::kTile;
+        if (valid[warp * NS + slot]) {
+          if (nvalid < kBlockSize) {
+            // Rows past the end of the context may hold anything (even NaN): zero them in
+            // V so that their zero weights contribute exactly nothing.
+            unsigned char *vrow = base + (vst - base_u32);
+            {
+              const int nz = (kBlockSize - nvalid) * (D / 8);
+              for (int i = lane; i < nz; i += 32) {
+                const int row = nvalid + i / (D / 8), ch = i % (D / 8);
+                *reinterpret_cast<uint4 *>(vrow + (ch >> 3) * 2048 + row * 128 + (ch & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+            }
+            __syncwarp();
+          }
+          // S^T = K Q^T  (rows: tokens gid, gid + 8; columns: heads 2 tig, 2 tig + 1)
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            // column 16 kk + 8 (lane >> 4): half kk / 4, chunk (2 kk + (lane >> 4)) & 7
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kst + (uint32_t)((kk >> 2) * 2048) + (koff16 ^ (uint32_t)(((2 * kk) & 7) << 4)),
+                    a0, a1, a2, a3);
+            mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          }
+          float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
+          float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+          if (gid >= nvalid) x0 = x1 = -INFINITY;
+          if (gid + 8 >= nvalid) x2 = x3 = -INFINITY;
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+          }
+          const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+          const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+          m0 = n0;
+          m1 = n1;
+          const uint32_t p01 = pack_bf16(exp2f(x0 - m0), exp2f(x1 - m1));
+          const uint32_t p23 = pack_bf16(exp2f(x2 - m0), exp2f(x3 - m1));
+          l0 = fmaf(l0, al0, bf16_lo(p01) + bf16_lo(p23));
+          l1 = fmaf(l1, al1, bf16_hi(p01) + bf16_hi(p23));
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][2] *= al0;
+            acc[mt][3] *= al1;
+          }
+          // P^T as the B operand of O^T += V^T P^T.
+          const uint32_t b0 = movmatrix_t(p01), b1 = movmatrix_t(p23);
           const int j4 = lane >> 3;
           const int tok = (lane & 7) + ((j4 >> 1) << 3);
 #pragma unroll
@@ -479,38 +564,40 @@ __global__ void __launch_bounds__((NW + 1) * 32,
             ldsm_x4_t(vst + tile_off(tok, 16 * mt + ((j4 & 1) << 3)), a0, a1, a2, a3);
             mma16816(acc[mt], a0, a1, a2, a3, b0, b1);
           }
+          if (nvalid < kBlockSize)  // generic writes above, async-proxy writes next
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        if (!KV8 && nvalid < kBlockSize)  // generic writes above, async-proxy writes next
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * (warp * NS + slot));
+      if (jb + NW < nstage) {
+        if (lane == 0) mbar_arrive(empty0 + 8 * (warp * NS + slot));
+      } else {
+        held = (int)slot;  // the warp's last stage of the item: kept for its merge state
+      }
     }
 
     // ---- merge the NW warp states of this item; take the next item meanwhile ----
+    // Each warp that consumed a stage of the item keeps its last stage and writes its
+    // state there -- per lane the accumulator tile acc[mt][0..3] as float4 chunk mt and
+    // (m0, m1, l0, l1) as chunk KSTEPS, chunk-major (chunk c of lane i at 512 c + 16 i),
+    // so a warp's 16-byte accesses hit distinct banks -- and publishes the stage address.
+    // Warp w then merges m-tiles w, w + NW, ... of every warp's state and writes that
+    // slice of the item's output; the held stages are released after a second barrier.
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, off);
       l1 += __shfl_xor_sync(kFull, l1, off);
     }
-    if (gid == 0) {
-      red_m[warp * 8 + 2 * tig] = m0;
-      red_m[warp * 8 + 2 * tig + 1] = m1;
-      red_l[warp * 8 + 2 * tig] = l0;
-      red_l[warp * 8 + 2 * tig + 1] = l1;
-    }
-    {
-      float *ro = red_o + warp * 8 * L::kRow;
-      // Accumulator rows gid and gid + 8 of m-tile mt are head_dim columns d0 and d1.
-      const int d0 = gid, d1 = gid + 8;
+    const uint32_t held_at =
+        held >= 0 ? base_u32 + (uint32_t)((warp * NS + held) * L::kStage) : ~0u;
+    if (held >= 0) {
+      const uint32_t at = held_at + (uint32_t)lane * 16u;
 #pragma unroll
-      for (int mt = 0; mt < KSTEPS; ++mt) {
-        ro[(2 * tig) * L::kRow + 16 * mt + d0] = acc[mt][0];
-        ro[(2 * tig + 1) * L::kRow + 16 * mt + d0] = acc[mt][1];
-        ro[(2 * tig) * L::kRow + 16 * mt + d1] = acc[mt][2];
-        ro[(2 * tig + 1) * L::kRow + 16 * mt + d1] = acc[mt][3];
-      }
+      for (int mt = 0; mt < KSTEPS; ++mt)
+        sts128(at + (uint32_t)(mt * 512), acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+      sts128(at + (uint32_t)(KSTEPS * 512), m0, m1, l0, l1);
     }
+    if (lane == 0) state_at[warp] = held_at;
     if (threadIdx.x == 0) fetch(k + 1);
     __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
@@ -521,31 +608,85 @@ __global__ void __launch_bounds__((NW + 1) * 32,
       load_q_frag_f16perm<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
     else
       load_q_frag<D>(qn, a, nxt < total ? nxt : 0, per_pair, rec_n, gid, tig, nxt < total);
-    const bool single = rec.w == 1;
-    const int p = t0 / a.part_tokens;
-    for (int i = threadIdx.x; i < gcnt * D; i += NW * 32) {
-      const int j = i / D, d = i - j * D;
-      float M = red_m[j];
-#pragma unroll
-      for (int w = 1; w < NW; ++w) M = fmaxf(M, red_m[w * 8 + j]);
-      float Lsum = 0.f, O = 0.f;
+    if (warp < KSTEPS) {
+      // Weights of the warp states for this lane's two heads (2 tig, 2 tig + 1).
+      uint32_t src[NW];
+      float wm0[NW], wm1[NW], wl0[NW], wl1[NW];
+      float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float c = exp2f(red_m[w * 8 + j] - M);
-        Lsum = fmaf(red_l[w * 8 + j], c, Lsum);
-        O = fmaf(red_o[(w * 8 + j) * L::kRow + d], c, O);
+        src[w] = state_at[w];
+        wm0[w] = wm1[w] = -INFINITY;
+        wl0[w] = wl1[w] = 0.f;
+        if (src[w] != ~0u) {
+          src[w] += (uint32_t)lane * 16u;
+          lds128(src[w] + (uint32_t)(KSTEPS * 512), wm0[w], wm1[w], wl0[w], wl1[w]);
+          M0 = fmaxf(M0, wm0[w]);
+          M1 = fmaxf(M1, wm1[w]);
+        }
       }
-      const int h = h0 + j;
-      const float o = O / Lsum * a.v_scale;  // v_scale is 1 for a bf16 cache
-      if (single) {
-        a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(o);
-      } else {
-        const size_t idx = ((size_t)s * a.max_parts + p) * a.num_q_heads + h;
-        a.part_o[idx * D + d] = o;
-        if (d == 0) a.part_lse[idx] = M + log2f(Lsum);
+      float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        wm0[w] = src[w] != ~0u ? exp2f(wm0[w] - M0) : 0.f;  // now the weights
+        wm1[w] = src[w] != ~0u ? exp2f(wm1[w] - M1) : 0.f;
+        L0 = fmaf(wl0[w], wm0[w], L0);
+        L1 = fmaf(wl1[w], wm1[w], L1);
+      }
+      const float f0 = a.v_scale / L0, f1 = a.v_scale / L1;  // v_scale is 1 for bf16
+      const bool single = rec.w == 1;
+      const int p = t0 / a.part_tokens;
+      const int hA = 2 * tig, hB = 2 * tig + 1;  // heads of this lane, within the item
+      const size_t rowA = single ? ((size_t)s * a.num_q_heads + h0 + hA)
+                                 : (((size_t)s * a.max_parts + p) * a.num_q_heads + h0 + hA);
+      for (int mt = warp; mt < KSTEPS; mt += NW) {
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          if (src[w] == ~0u) continue;
+          float v0, v1, v2, v3;
+          lds128(src[w] + (uint32_t)(mt * 512), v0, v1, v2, v3);
+          o[0] = fmaf(v0, wm0[w], o[0]);
+          o[1] = fmaf(v1, wm1[w], o[1]);
+          o[2] = fmaf(v2, wm0[w], o[2]);
+          o[3] = fmaf(v3, wm1[w], o[3]);
+        }
+        // o[0]: (head hA, d0), o[1]: (hB, d0), o[2]: (hA, d0 + 8), o[3]: (hB, d0 + 8)
+        const int d0 = 16 * mt + gid;
+        if (single) {
+          uint16_t *oa = a.out + rowA * D + d0;
+          if (hA < gcnt) {
+            oa[0] = f32_to_bf16(o[0] * f0);
+            oa[8] = f32_to_bf16(o[2] * f0);
+          }
+          if (hB < gcnt) {
+            oa[D] = f32_to_bf16(o[1] * f1);
+            oa[D + 8] = f32_to_bf16(o[3] * f1);
+          }
+        } else {
+          float *oa = a.part_o + rowA * D + d0;
+          if (hA < gcnt) {
+            oa[0] = o[0] * f0;
+            oa[8] = o[2] * f0;
+          }
+          if (hB < gcnt) {
+            oa[D] = o[1] * f1;
+            oa[D + 8] = o[3] * f1;
+          }
+        }
+      }
+      if (!single && warp == 0 && gid == 0) {
+        if (hA < gcnt) a.part_lse[rowA] = M0 + log2f(L0);
+        if (hB < gcnt) a.part_lse[rowA + 1] = M1 + log2f(L1);
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+    if (held >= 0) {
+      // generic writes into the stage above, async-proxy writes into it next
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * (warp * NS + held));
+    }
     cur = nxt;
     rec = rec_n;
 #pragma unroll
@@ -649,18 +790,40 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 }
 
 // Ring shape (consumer warps x stages per warp), overridable for tuning through the
-// PKV_MMA_RING environment variable.
+// PKV_MMA_RING environment variable; -1 = the path's default.
 int ring_choice() {
-  static int choice = -1;
-  if (choice < 0) {
+  static int choice = -2;
+  if (choice == -2) {
     static const char *names[] = {"3x2", "8x2", "4x4", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3",
                                   "1x4", "1x6"};
     const char *v = std::getenv("PKV_MMA_RING");
-    choice = 0;
+    choice = -1;
     for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
       if (std::strcmp(v, names[i]) == 0) choice = i;
   }
   return choice;
+}
+
+template <bool KV8>
+int launch_mma_ring(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                    cudaStream_t st) {
+  // Defaults measured on GB300: bf16 (one 8 KB block per stage) 3 consumer warps x 2
+  // stages, 3 CTAs per SM; E4M3 (two blocks, 8 KB, per stage) 2 x 2, 5 CTAs per SM.
+  int c = ring_choice();
+  if (c < 0) c = KV8 ? 4 : 0;
+  switch (c) {
+    case 1: return launch_mma_t<128, 8, 2, KV8>(a, tk, tv, st);
+    case 2: return launch_mma_t<128, 4, 4, KV8>(a, tk, tv, st);
+    case 3: return launch_mma_t<128, 4, 3, KV8>(a, tk, tv, st);
+    case 4: return launch_mma_t<128, 2, 2, KV8>(a, tk, tv, st);
+    case 5: return launch_mma_t<128, 2, 3, KV8>(a, tk, tv, st);
+    case 6: return launch_mma_t<128, 4, 2, KV8>(a, tk, tv, st);
+    case 7: return launch_mma_t<128, 2, 4, KV8>(a, tk, tv, st);
+    case 8: return launch_mma_t<128, 3, 3, KV8>(a, tk, tv, st);
+    case 9: return launch_mma_t<128, 1, 4, KV8>(a, tk, tv, st);
+    case 10: return launch_mma_t<128, 1, 6, KV8>(a, tk, tv, st);
+    default: return launch_mma_t<128, 3, 2, KV8>(a, tk, tv, st);
+  }
 }
 
 }  // namespace
@@ -679,34 +842,10 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
     return (int)cudaErrorInvalidValue;
   if (a.kv8) {
     if (head_dim != 128) return (int)cudaErrorInvalidValue;
-    switch (ring_choice()) {
-      case 1: return launch_mma_t<128, 8, 2, true>(a, tk, tv, st);
-      case 2: return launch_mma_t<128, 4, 4, true>(a, tk, tv, st);
-      case 3: return launch_mma_t<128, 4, 3, true>(a, tk, tv, st);
-      case 4: return launch_mma_t<128, 2, 2, true>(a, tk, tv, st);
-      case 5: return launch_mma_t<128, 2, 3, true>(a, tk, tv, st);
-      case 6: return launch_mma_t<128, 4, 2, true>(a, tk, tv, st);
-      case 7: return launch_mma_t<128, 2, 4, true>(a, tk, tv, st);
-      case 8: return launch_mma_t<128, 3, 3, true>(a, tk, tv, st);
-      case 9: return launch_mma_t<128, 1, 4, true>(a, tk, tv, st);
-      case 10: return launch_mma_t<128, 1, 6, true>(a, tk, tv, st);
-      default: return launch_mma_t<128, 3, 2, true>(a, tk, tv, st);
-    }
+    return launch_mma_ring<true>(a, tk, tv, st);
   }
   if (head_dim == 64) return launch_mma_t<64, 4, 4>(a, tk, tv, st);
-  switch (ring_choice()) {
-    case 1: return launch_mma_t<128, 8, 2>(a, tk, tv, st);
-    case 2: return launch_mma_t<128, 4, 4>(a, tk, tv, st);
-    case 3: return launch_mma_t<128, 4, 3>(a, tk, tv, st);
-    case 4: return launch_mma_t<128, 2, 2>(a, tk, tv, st);
-    case 5: return launch_mma_t<128, 2, 3>(a, tk, tv, st);
-    case 6: return launch_mma_t<128, 4, 2>(a, tk, tv, st);
-    case 7: return launch_mma_t<128, 2, 4>(a, tk, tv, st);
-    case 8: return launch_mma_t<128, 3, 3>(a, tk, tv, st);
-    case 9: return launch_mma_t<128, 1, 4>(a, tk, tv, st);
-    case 10: return launch_mma_t<128, 1, 6>(a, tk, tv, st);
-    default: return launch_mma_t<128, 3, 2>(a, tk, tv, st);
-  }
+  return launch_mma_ring<false>(a, tk, tv, st);
 }
 
 }  // namespace pkv

@@ -11,6 +11,7 @@ import oracle
 from paged_kv_cache_272_gb300 import workloads
 
 ATOL, RTOL, MEAN_TOL = 1e-2, 1e-2, 2e-3
+K_SCALE, V_SCALE = 0.02, 0.015  # E4M3 cache scales of the FP8 tests
 NTHREADS = max(1, min(32, os.cpu_count() or 1))
 
 
@@ -102,3 +103,51 @@ def sample_pairs(w, n_short=64, seed=0):
     for _ in range(n_short):
         pairs.append((int(rng.integers(w.num_seqs)), int(rng.integers(w.num_q_heads))))
     return np.array(pairs, dtype=np.int32)
+
+
+def rows_of(cache: torch.Tensor) -> torch.Tensor:
+    """[NB][Hkv][16][D] -> [NB*16][Hkv][D] in slot order (to quantise a whole cache)."""
+    NB, Hkv, bs, D = cache.shape
+    return cache.permute(0, 2, 1, 3).reshape(NB * bs, Hkv, D).contiguous()
+
+
+def fp8_step(w, ks=K_SCALE, vs=V_SCALE, partition_size=None, block_tables=None):
+    """Quantise the pre-step cache, then COW copy + new-token write + attention, on the
+    GPU and in the oracle.  Returns (gpu_out, gpu k/v codes, oracle k/v codes, err)."""
+    o = ops()
+    dev = "cuda"
+    NB, Hkv, bs, D = w.k_cache.shape
+    kq = torch.zeros(NB, Hkv, bs, D, dtype=torch.uint8, device=dev)
+    vq = torch.zeros_like(kq)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    slots_all = torch.arange(NB * bs, dtype=torch.int64, device=dev)
+    o.paged_kv_write_fp8(rows_of(w.k_cache.to(dev)), rows_of(w.v_cache.to(dev)), slots_all, kq, vq,
+                         ks, vs, err_flag=err)
+    d = to_cuda(w)
+    if d["pairs"].numel():
+        o.paged_block_copy_fp8(kq, vq, d["pairs"], err_flag=err)
+    if d["slots"].numel():
+        o.paged_kv_write_fp8(d["k_new"], d["v_new"], d["slots"], kq, vq, ks, vs, err_flag=err)
+    S, Hq, _ = d["q"].shape
+    P = partition_size or w.partition_size
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, P)
+    bt = d["bt"] if block_tables is None else block_tables
+    o.paged_attention_decode_fp8(out, d["q"], kq, vq, bt, d["ctx"], w.scale, ks, vs,
+                                 w.max_context_len, ws, P, err_flag=err)
+    torch.cuda.synchronize()
+    # oracle
+    ko = np.zeros((NB, Hkv, bs, D), np.uint8)
+    vo = np.zeros_like(ko)
+    oracle.kv_write_fp8(ko, vo, u16(rows_of(w.k_cache.cpu())), u16(rows_of(w.v_cache.cpu())),
+                        np.arange(NB * bs), ks, vs)
+    if w.cow_pairs.size:
+        oracle.block_copy_fp8(ko, vo, w.cow_pairs)
+    if w.slot_mapping.size:
+        oracle.kv_write_fp8(ko, vo, u16(w.k_new), u16(w.v_new), w.slot_mapping, ks, vs)
+    return out, kq.cpu().numpy(), vq.cpu().numpy(), ko, vo, int(err.item())
+
+
+def fp8_ref(w, ko, vo, ks=K_SCALE, vs=V_SCALE, sel=None):
+    return oracle.attention_fp8(u16(w.q), ko, vo, w.block_tables, w.context_lens, w.scale, ks,
+                                vs, sel=sel, nthreads=NTHREADS)

@@ -11,7 +11,7 @@ from paged_kv_cache_272_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 BS = 16
-K_SCALE, V_SCALE = 0.02, 0.015
+K_SCALE, V_SCALE = H.K_SCALE, H.V_SCALE
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -27,51 +27,7 @@ def same_codes(a: np.ndarray, b: np.ndarray) -> bool:
     return bool(np.all((a == b) | nan))
 
 
-def rows_of(cache: torch.Tensor) -> torch.Tensor:
-    """[NB][Hkv][16][D] -> [NB*16][Hkv][D] in slot order (to quantise a whole cache)."""
-    NB, Hkv, bs, D = cache.shape
-    return cache.permute(0, 2, 1, 3).reshape(NB * bs, Hkv, D).contiguous()
-
-
-def fp8_step(w, ks=K_SCALE, vs=V_SCALE, partition_size=None):
-    """Quantise the pre-step cache, then COW copy + new-token write + attention, on the
-    GPU and in the oracle.  Returns (gpu_out, gpu k/v codes, oracle k/v codes, err)."""
-    o = H.ops()
-    dev = "cuda"
-    NB, Hkv, bs, D = w.k_cache.shape
-    kq = torch.zeros(NB, Hkv, bs, D, dtype=torch.uint8, device=dev)
-    vq = torch.zeros_like(kq)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    slots_all = torch.arange(NB * bs, dtype=torch.int64, device=dev)
-    o.paged_kv_write_fp8(rows_of(w.k_cache.to(dev)), rows_of(w.v_cache.to(dev)), slots_all, kq, vq,
-                         ks, vs, err_flag=err)
-    d = H.to_cuda(w)
-    if d["pairs"].numel():
-        o.paged_block_copy_fp8(kq, vq, d["pairs"], err_flag=err)
-    if d["slots"].numel():
-        o.paged_kv_write_fp8(d["k_new"], d["v_new"], d["slots"], kq, vq, ks, vs, err_flag=err)
-    S, Hq, _ = d["q"].shape
-    P = partition_size or w.partition_size
-    out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
-    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, P)
-    o.paged_attention_decode_fp8(out, d["q"], kq, vq, d["bt"], d["ctx"], w.scale, ks, vs,
-                                 w.max_context_len, ws, P, err_flag=err)
-    torch.cuda.synchronize()
-    # oracle
-    ko = np.zeros((NB, Hkv, bs, D), np.uint8)
-    vo = np.zeros_like(ko)
-    oracle.kv_write_fp8(ko, vo, H.u16(rows_of(w.k_cache.cpu())), H.u16(rows_of(w.v_cache.cpu())),
-                        np.arange(NB * bs), ks, vs)
-    if w.cow_pairs.size:
-        oracle.block_copy_fp8(ko, vo, w.cow_pairs)
-    if w.slot_mapping.size:
-        oracle.kv_write_fp8(ko, vo, H.u16(w.k_new), H.u16(w.v_new), w.slot_mapping, ks, vs)
-    return out, kq.cpu().numpy(), vq.cpu().numpy(), ko, vo, int(err.item())
-
-
-def fp8_ref(w, ko, vo, ks=K_SCALE, vs=V_SCALE, sel=None):
-    return oracle.attention_fp8(H.u16(w.q), ko, vo, w.block_tables, w.context_lens, w.scale, ks,
-                                vs, sel=sel, nthreads=H.NTHREADS)
+rows_of, fp8_step, fp8_ref = H.rows_of, H.fp8_step, H.fp8_ref
 
 
 def test_write_fp8_all_bf16_patterns():
@@ -141,6 +97,20 @@ def test_fp8_scales_and_magnitude():
         out, kq, vq, ko, vo, err = fp8_step(w, ks, vs)
         assert err == 0
         H.assert_attention_close(out, fp8_ref(w, ko, vo, ks, vs), f"fp8 scales {ks} {vs}")
+
+
+def test_fp8_bad_block_id_is_flagged_not_read():
+    """A block id outside the pool (in the first or the second block of a two-block
+    stage) is flagged and skipped; the other sequences are unaffected."""
+    w = workloads.build("fp8-badblk", [40, 70, 100, 333], 8, 2, 128, seed=98, device="cuda")
+    for pos in (2, 3):
+        bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device="cuda").clone()
+        bt[1, pos] = w.num_blocks + 1000
+        out, kq, vq, ko, vo, err = fp8_step(w, block_tables=bt)
+        assert err & H.ops().DEV_BAD_BLOCK
+        ref = fp8_ref(w, ko, vo)
+        keep = [0, 2, 3]
+        H.assert_attention_close(out[keep], ref[keep], f"untouched sequences (block {pos})")
 
 
 def test_fp8_rejects_other_head_dims():

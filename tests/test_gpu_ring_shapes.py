@@ -1,6 +1,6 @@
 """Every ring shape of the tensor-core kernel (consumer warps x stages, chosen once per
-process through PKV_MMA_RING) on partitions shorter and longer than 32 blocks, checked
-against the oracle in a fresh process each."""
+process through PKV_MMA_RING) on partitions shorter and longer than 32 blocks, with the
+bf16 and the E4M3 cache, checked against the oracle in a fresh process each."""
 import os
 import subprocess
 import sys
@@ -25,6 +25,10 @@ for P in (64, 512, 1024, 8192):
     out, k, v, err = H.gpu_step(w, 2, partition_size=P)
     assert err == 0, (P, err)
     H.assert_attention_close(out, ref, "ring {ring} partition %d" % P)
+for P in (64, 512, 8192):
+    out, kq, vq, ko8, vo8, err = H.fp8_step(w, partition_size=P)
+    assert err == 0, (P, err)
+    H.assert_attention_close(out, H.fp8_ref(w, ko8, vo8), "ring {ring} E4M3 partition %d" % P)
 print("ok")
 """
 
