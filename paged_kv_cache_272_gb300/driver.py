@@ -1,8 +1,8 @@
 """Continuous-batching step driver: runs the native scheduler's steps on the GPU.
 
 Each step the C++ scheduler (``serving.Scheduler``) decides which requests run and
-reserves their slots; the driver copies the step's arrays and the new tokens' q/K/V to
-the device and launches the library's kernels on one stream:
+reserves their slots; the driver copies the step's arrays to the device, forms the new
+tokens' q/K/V there and launches the library's kernels on one stream:
 
     paged_block_copy        copy-on-write pairs (if any)
     paged_kv_write          K/V of every new token (decode tokens and prefill chunks)
@@ -10,10 +10,12 @@ the device and launches the library's kernels on one stream:
     paged_attention_prefill the prefill chunks (causal, tensor cores)
 
 There is no model: the new tokens' K/V rows and query rows are taken from fixed seeded
-tables.  A token's K/V depend only on its token id and position, so two requests with
-the same prompt prefix hold the same K/V there and a cached prefix block is valid for
-both; a query row depends on the request and position.  Output tokens get synthetic ids
-from (request, position).
+tables kept on the device (standing in for the layers that would produce them there);
+a step copies only the row indices and gathers the rows on the device.  A token's K/V
+depend only on its token id and position, so two requests with the same prompt prefix
+hold the same K/V there and a cached prefix block is valid for both; a query row
+depends on the request and position.  Output tokens get synthetic ids from (request,
+position).
 """
 from __future__ import annotations
 
@@ -58,22 +60,24 @@ class StepInputs:
 
 
 def prepare(plan: Plan, prompts: dict, kv_rows_n: int, q_rows_n: int) -> StepInputs:
-    """Token ids, positions and table rows of a step's new tokens (host only)."""
-    ids, pos, rid_of = [], [], []
-    for i, rid in enumerate(plan.seq_ids.tolist()):
-        L, c = int(plan.query_lens[i]), int(plan.context_lens[i])
-        p = np.arange(c - L, c, dtype=np.int64)
-        prompt = prompts[rid]
-        t = np.where(p < len(prompt), prompt[np.minimum(p, len(prompt) - 1)],
-                     output_token(np.full_like(p, rid), p))
-        ids.append(t.astype(np.int32))
-        pos.append(p.astype(np.int32))
-        rid_of.append(np.full(L, rid, np.int64))
-    cat = lambda xs, dt: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)
-    ids, pos, rid_of = cat(ids, np.int32), cat(pos, np.int32), cat(rid_of, np.int64)
+    """Token ids, positions and table rows of a step's new tokens (host only).  Entry i
+    covers positions context_lens[i] - query_lens[i] .. context_lens[i] - 1; a position
+    inside the request's prompt takes the prompt's token, any later one a generated id."""
+    seq = plan.seq_ids.astype(np.int64)
+    L = plan.query_lens.astype(np.int64)
+    c = plan.context_lens.astype(np.int64)
+    T = int(L.sum())
+    starts = np.cumsum(L) - L
+    rid_of = np.repeat(seq, L)
+    pos = np.repeat(c - L, L) + (np.arange(T, dtype=np.int64) - np.repeat(starts, L))
+    ids = output_token(rid_of, pos)
+    plen = np.fromiter((len(prompts[r]) for r in seq.tolist()), dtype=np.int64, count=len(seq))
+    for i in np.flatnonzero(c - L < plen).tolist():  # entries that reach into their prompt
+        lo, hi = int(c[i] - L[i]), int(min(c[i], plen[i]))
+        ids[starts[i]:starts[i] + hi - lo] = prompts[int(seq[i])][lo:hi]
     nd = plan.num_decode
     pq = plan.query_start[nd:] - plan.query_start[nd]
-    return StepInputs(plan=plan, token_ids=ids, positions=pos,
+    return StepInputs(plan=plan, token_ids=ids.astype(np.int32), positions=pos.astype(np.int32),
                       kv_rows=kv_row(ids, pos, kv_rows_n), q_rows=q_row(rid_of, pos, q_rows_n),
                       num_decode=nd,
                       decode_ctx_max=int(plan.context_lens[:nd].max()) if nd else 0,
@@ -91,9 +95,12 @@ class ServingDriver:
         self.scale = head_dim ** -0.5
         g = torch.Generator().manual_seed(seed)
         bf = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
-        # host tables (the "model"): K/V rows by (token, position), q rows by (request, pos)
+        # tables (the "model"): K/V rows by (token, position), q rows by (request, pos);
+        # host copies for checking, device copies for the steps
         self.k_tab, self.v_tab = bf(table_rows, num_kv_heads, head_dim), bf(table_rows, num_kv_heads, head_dim)
         self.q_tab = bf(table_rows, num_q_heads, head_dim)
+        self.k_tab_d, self.v_tab_d, self.q_tab_d = (t.to(self.dev) for t in
+                                                     (self.k_tab, self.v_tab, self.q_tab))
         self.rows = table_rows
         self.k_cache = torch.zeros(num_blocks, num_kv_heads, BS, head_dim, dtype=torch.bfloat16,
                                    device=self.dev)
@@ -107,6 +114,7 @@ class ServingDriver:
         self.stream = torch.cuda.current_stream(self.dev)
         self.launches = 0
         self._bufs = {}
+        self._dbufs = {}
         self._host = {}
         self.h2d_bytes = 0
         self.d2h_bytes = 0
@@ -138,11 +146,14 @@ class ServingDriver:
         h.copy_(torch.from_numpy(np.ascontiguousarray(arr)))
         return h, d
 
-    def _put_rows(self, name, table, rows):
-        """Stage rows of a host table (the synthetic model's output) in a pinned buffer."""
-        h, d = self._stage(name, (rows.shape[0],) + tuple(table.shape[1:]), table.dtype)
-        torch.index_select(table, 0, torch.from_numpy(rows), out=h)
-        return h, d
+    def _dev(self, name, shape, dtype):
+        """A device buffer, grown on demand; returns a view of the requested shape."""
+        n = int(np.prod(shape)) if len(shape) else 1
+        buf = self._dbufs.get(name)
+        if buf is None or buf.numel() < n:
+            buf = torch.empty(max(n, 1) * 2, dtype=dtype, device=self.dev)
+            self._dbufs[name] = buf
+        return buf[:n].view(shape)
 
     def fetch(self, *outs):
         """Copy a step's outputs to pinned host memory (what a sampler would read)."""
@@ -172,11 +183,11 @@ class ServingDriver:
         T = x.token_ids.shape[0]
         if T == 0:
             return x, None, None
-        # Host side first (the synthetic model's rows and the plan's arrays into pinned
-        # buffers), then the copies and kernels back to back on the stream.
-        staged = {"k": self._put_rows("k", self.k_tab, x.kv_rows),
-                  "v": self._put_rows("v", self.v_tab, x.kv_rows),
-                  "q": self._put_rows("q", self.q_tab, x.q_rows),
+        # Host side first (the rows of the synthetic model and the plan's arrays into
+        # pinned buffers), then the copies, the row gathers and the kernels back to back
+        # on the stream.
+        staged = {"kvr": self._put("kvr", x.kv_rows, torch.int64),
+                  "qr": self._put("qr", x.q_rows, torch.int64),
                   "slots": self._put("slots", plan.slot_mapping, torch.int64),
                   "tables": self._put("tables", plan.block_tables, torch.int32),
                   "ctx": self._put("ctx", plan.context_lens, torch.int32)}
@@ -191,7 +202,12 @@ class ServingDriver:
             d.copy_(h, non_blocking=True)
             self.h2d_bytes += h.numel() * h.element_size()
             dv[name] = d
-        k_new, v_new, q = dv["k"], dv["v"], dv["q"]
+        k_new = self._dev("k", (T, self.Hkv, self.D), torch.bfloat16)
+        v_new = self._dev("v", (T, self.Hkv, self.D), torch.bfloat16)
+        q = self._dev("q", (T, self.Hq, self.D), torch.bfloat16)
+        torch.index_select(self.k_tab_d, 0, dv["kvr"], out=k_new)
+        torch.index_select(self.v_tab_d, 0, dv["kvr"], out=v_new)
+        torch.index_select(self.q_tab_d, 0, dv["qr"], out=q)
         slots, tables, ctx = dv["slots"], dv["tables"], dv["ctx"]
         if plan.cow_pairs.size:
             ops.paged_block_copy(self.k_cache, self.v_cache, dv["pairs"], err_flag=self.err,
@@ -203,7 +219,7 @@ class ServingDriver:
         nd = x.num_decode
         dec_out = pre_out = None
         if nd:
-            dec_out = self._stage("dec_out", (nd, self.Hq, self.D), torch.bfloat16)[1]
+            dec_out = self._dev("dec_out", (nd, self.Hq, self.D), torch.bfloat16)
             if self.on_decode is not None:
                 self.on_decode(0)
             ops.paged_attention_decode(dec_out, q[:nd], self.k_cache, self.v_cache, tables[:nd],
@@ -214,7 +230,7 @@ class ServingDriver:
             self.launches += 3 if x.decode_ctx_max > self.P else 2
         if plan.seq_ids.shape[0] > nd:
             pq = dv["pq"]
-            pre_out = self._stage("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)[1]
+            pre_out = self._dev("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)
             ops.paged_attention_prefill(pre_out, q[nd:], self.k_cache, self.v_cache, tables[nd:],
                                         ctx[nd:], pq, self.scale, x.prefill_max_query,
                                         err_flag=self.err, stream=self.stream)

@@ -268,14 +268,16 @@ def test_native_cache_api_matches_reference():
         assert cache.stats()["entries"] == len(trie.entries)
 
 
-def test_driver_step_inputs_follow_the_plan():
+@pytest.mark.parametrize("num_blocks", [2000, 40])
+def test_driver_step_inputs_follow_the_plan(num_blocks):
     """The driver's host preparation: prompt tokens for prefill chunks, synthetic output
-    tokens for decode entries, K/V rows that depend only on (token, position)."""
+    tokens for decode entries, K/V rows that depend only on (token, position); with a
+    small pool requests are preempted and prefilled again from the start."""
     from paged_kv_cache_272_gb300 import driver
     from paged_kv_cache_272_gb300.block_pool import BlockPool
     from paged_kv_cache_272_gb300.serving import Scheduler
     reqs = workloads.make_requests("pareto", seed=15, n=10)
-    pool = BlockPool(2000)
+    pool = BlockPool(num_blocks)
     s = Scheduler(pool, 4, 64)
     prompts = {}
     for r in reqs:
@@ -294,10 +296,15 @@ def test_driver_step_inputs_follow_the_plan():
                 assert L == 1 and c - 1 >= P
                 assert x.token_ids[a] == driver.output_token(np.array([rid]), np.array([c - 1]))[0]
             else:
-                assert x.token_ids[a:b].tolist() == prompts[rid][c - L:c].tolist()
+                pos = np.arange(c - L, c)
+                want = [int(prompts[rid][p]) if p < P else
+                        int(driver.output_token(np.array([rid]), np.array([p]))[0]) for p in pos]
+                assert x.token_ids[a:b].tolist() == want
         nd = plan.num_decode
         assert x.prefill_query_start.tolist() == (plan.query_start[nd:] - plan.query_start[nd]).tolist()
         assert (x.kv_rows == driver.kv_row(x.token_ids, x.positions, 4096)).all()
+    if num_blocks == 40:
+        assert s.stats()["preemptions"] > 0
 
 
 @pytest.mark.parametrize("seed", range(12))
