@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
   pdl_wait();
   const int per_pair = a.num_kv_heads * a.sub_groups;
   const int total = *a.num_items * per_pair;
+  // K/V rows are read once: evict them first, so partials and queries stay in L2
+  const uint64_t pol = l2_evict_first_policy();
 
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const int pair = w / per_pair;
@@ -179,9 +181,9 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
       const uint4 *vp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.v_cache) + base);
       uint4 kr[NI], vr[NI];
 #pragma unroll
-      for (int i = 0; i < NI; ++i) kr[i] = ld_stream_v4(kp + i * 32 + lane);
+      for (int i = 0; i < NI; ++i) kr[i] = ld_stream_v4_hint(kp + i * 32 + lane, pol);
 #pragma unroll
-      for (int i = 0; i < NI; ++i) vr[i] = ld_stream_v4(vp + i * 32 + lane);
+      for (int i = 0; i < NI; ++i) vr[i] = ld_stream_v4_hint(vp + i * 32 + lane, pol);
       const int tb = t0 + jb * kBlockSize + tg;  // token of load i: tb + i * TPI
 
       float sc[NI][GM];

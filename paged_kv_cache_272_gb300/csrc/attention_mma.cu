@@ -223,6 +223,8 @@ __global__ void __launch_bounds__((NW + 1) * 32,
     // copies side by side.  Lane w counts the stages it handed to warp w (ring slot =
     // count % NS, phase = count / NS).
     constexpr int BPS = L::kBps;
+    // K/V tiles are read once: evict them first, so partials and queries stay in L2
+    const uint64_t pol = l2_evict_first_policy();
     int cnt = 0;               // stages handed to warp `lane` so far
     int pslot = 0, pphase = 0;  // = cnt % NS, (cnt / NS) & 1, kept incrementally
     bool stop = false;
@@ -299,15 +301,15 @@ __global__ void __launch_bounds__((NW + 1) * 32,
                   const int y = (bj[j] * a.num_kv_heads + g) * kBlockSize;
                   if constexpr (KV8) {
                     // K: one [16][128 B] swizzled box; V (stored [d][16]): 2 KB contiguous
-                    tma_load_2d(dst, &tk, 0, y, fb);
-                    bulk_load(dst + L::kTile,
-                              static_cast<const uint8_t *>(a.v_cache) + (size_t)y * D, L::kTile,
-                              fb);
+                    tma_load_2d_hint(dst, &tk, 0, y, fb, pol);
+                    bulk_load_hint(dst + L::kTile,
+                                   static_cast<const uint8_t *>(a.v_cache) + (size_t)y * D,
+                                   L::kTile, fb, pol);
                   } else {
 #pragma unroll
                     for (int h = 0; h < HALVES; ++h) {
-                      tma_load_2d(dst + h * 2048, &tk, h * 64, y, fb);
-                      tma_load_2d(dst + L::kTile + h * 2048, &tv, h * 64, y, fb);
+                      tma_load_2d_hint(dst + h * 2048, &tk, h * 64, y, fb, pol);
+                      tma_load_2d_hint(dst + L::kTile + h * 2048, &tv, h * 64, y, fb, pol);
                     }
                   }
                 }

@@ -18,11 +18,28 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit) {
 
 // 16-byte read-only load of streamed data: bypass L1 allocation; the KV cache is read
 // once per step so L1 reuse is nil.
+// L2 policy for data read once (streamed KV tiles): its lines are the first replaced, so
+// the lines other data keeps (partial results, queries) survive the stream.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
+  return r;
+}
+
+// The same with an L2 cache policy (see l2_evict_first_policy).
+__device__ __forceinline__ uint4 ld_stream_v4_hint(const void *p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
   return r;
 }
 
