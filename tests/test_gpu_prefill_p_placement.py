@@ -1,7 +1,7 @@
-"""The tcgen05 chunked-prefill kernel with P kept in tensor memory (chosen once per
-process through PKV_PREFILL_P=tmem): the prefill parity tests of the tcgen05 variant,
-then repeated calls on the full-size workload with the device error flag checked (the
-P-ready barriers must never run a phase ahead)."""
+"""Both placements of the tcgen05 chunked-prefill kernel's P tile (chosen once per
+process through PKV_PREFILL_P: "tmem", the default, or "smem"): the prefill parity
+tests of the tcgen05 variant, then repeated calls on the full-size workload with the
+device error flag checked (the P-ready barriers must never run a phase ahead)."""
 import os
 import subprocess
 import sys
@@ -36,22 +36,24 @@ print("ok")
 """
 
 
-def _run(args, script=None):
-    env = dict(os.environ, PKV_PREFILL_P="tmem")
+def _run(args, placement, script=None):
+    env = dict(os.environ, PKV_PREFILL_P=placement)
     cmd = [sys.executable] + (["-c", script] if script else args)
     return subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900, cwd=ROOT)
 
 
-def test_prefill_parity_with_p_in_tmem():
+@pytest.mark.parametrize("placement", ["smem", "tmem"])
+def test_prefill_parity_per_p_placement(placement):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     r = _run(["-m", "pytest", os.path.join(HERE, "test_gpu_prefill.py"), "-q", "-x", "-m", "gpu",
-              "-k", "tc or long or tiny", "-p", "no:cacheprovider"])
+              "-k", "tc or long or tiny", "-p", "no:cacheprovider"], placement)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
-def test_repeated_calls_with_p_in_tmem():
+@pytest.mark.parametrize("placement", ["smem", "tmem"])
+def test_repeated_calls_per_p_placement(placement):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    r = _run(None, REPEAT.format(root=ROOT))
+    r = _run(None, placement, REPEAT.format(root=ROOT))
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
