@@ -95,6 +95,14 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, u
       : "r"(four));
 }
 
+// 2^x by the MUFU ex2 instruction (relative error below 2^-22; subnormal results flush to
+// zero: such weights are below 2^-126 of the running maximum's).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -453,24 +461,26 @@ __global__ void __launch_bounds__((NW + 1) * 32,
             mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
           }
           const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-          const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+          const float al0 = ex2_ftz(m0 - n0), al1 = ex2_ftz(m1 - n1);
           m0 = n0;
           m1 = n1;
           uint32_t p01[2], p23[2];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            p01[j] = pack_f16(exp2f(x[j][0] - m0), exp2f(x[j][1] - m1));
-            p23[j] = pack_f16(exp2f(x[j][2] - m0), exp2f(x[j][3] - m1));
+            p01[j] = pack_f16(ex2_ftz(x[j][0] - m0), ex2_ftz(x[j][1] - m1));
+            p23[j] = pack_f16(ex2_ftz(x[j][2] - m0), ex2_ftz(x[j][3] - m1));
           }
           // the sum of the weights uses the rounded (f16) values that multiply V
           l0 = fmaf(l0, al0, (f16_lo(p01[0]) + f16_lo(p23[0])) + (f16_lo(p01[1]) + f16_lo(p23[1])));
           l1 = fmaf(l1, al1, (f16_hi(p01[0]) + f16_hi(p23[0])) + (f16_hi(p01[1]) + f16_hi(p23[1])));
+          {
+            // acc[mt][0, 1] and acc[mt][2, 3] are (head 2 tig, head 2 tig + 1) pairs
+            const uint64_t al = f32x2(al0, al1);
 #pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            acc[mt][0] *= al0;
-            acc[mt][1] *= al1;
-            acc[mt][2] *= al0;
-            acc[mt][3] *= al1;
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              f32x2_split(mul_f32x2(f32x2(acc[mt][0], acc[mt][1]), al), acc[mt][0], acc[mt][1]);
+              f32x2_split(mul_f32x2(f32x2(acc[mt][2], acc[mt][3]), al), acc[mt][2], acc[mt][3]);
+            }
           }
           // O^T += V^T P^T per block, P^T as the B operand (movmatrix), V^T[d][token]
           // fragments straight from the transposed codes: head_dim rows 16 mt + gid (+8),
