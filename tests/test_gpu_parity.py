@@ -195,3 +195,28 @@ def test_empty_calls_are_noops():
                              torch.zeros(0, 1, dtype=torch.int32, device="cuda"),
                              torch.zeros(0, dtype=torch.int32, device="cuda"), 0.125, 16, ws)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_more_sequences_than_plan_threads(variant):
+    """2600 sequences: more than one round of the plan kernel's 1024 threads (the second
+    round re-reads its lengths), thousands of records and merge units; one invalid and
+    one empty length among them.  Sampled rows against the oracle; the invalid and empty
+    sequences' outputs are zero."""
+    rng = np.random.default_rng(123)
+    ctx = rng.integers(1, 1400, size=2600)
+    w = workloads.build("many-seqs", ctx, 8, 2, 128, seed=124, device="cuda")
+    bad = torch.as_tensor(w.context_lens, dtype=torch.int32, device="cuda").clone()
+    bad[1500] = 0
+    bad[2100] = 1 << 20  # beyond every table and max_context_len
+    out, k, v, err = H.gpu_step(w, variant, context_lens=bad)
+    assert err & H.ops().DEV_BAD_CONTEXT
+    assert torch.all(out[1500] == 0) and torch.all(out[2100] == 0)
+    pairs = [(s, h) for s in (0, 1023, 1024, 1025, 2047, 2048, 2599) for h in (0, 5)]
+    pairs += [(int(rng.integers(2600)), int(rng.integers(8))) for _ in range(64)]
+    sel = np.array([p for p in pairs if p[0] not in (1500, 2100)], dtype=np.int32)
+    ko, vo = H.oracle_caches(w)
+    ref = H.oracle_out(w, ko, vo, sel=sel)
+    got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+              torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+    H.assert_attention_close(got, ref, "2600 sequences")
