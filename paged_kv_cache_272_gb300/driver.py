@@ -128,23 +128,30 @@ class ServingDriver:
     def done(self) -> bool:
         return self.sched.done()
 
-    def _stage(self, name, shape, dtype):
-        """A pinned host buffer and its device twin, grown on demand; returns views of
-        the requested shape."""
-        n = int(np.prod(shape)) if len(shape) else 1
-        buf = self._bufs.get(name)
-        if buf is None or buf[0].numel() < n:
-            cap = max(n, 1) * 2
-            buf = (torch.empty(cap, dtype=dtype).pin_memory(),
-                   torch.empty(cap, dtype=dtype, device=self.dev))
-            self._bufs[name] = buf
-        return buf[0][:n].view(shape), buf[1][:n].view(shape)
-
-    def _put(self, name, arr, dtype):
-        """Stage a host array in its pinned buffer; returns (pinned view, device view)."""
-        h, d = self._stage(name, tuple(arr.shape), dtype)
-        h.copy_(torch.from_numpy(np.ascontiguousarray(arr)))
-        return h, d
+    def _pack(self, arrays, slot):
+        """Stage host arrays [(name, numpy array, torch dtype)] in one pinned buffer of
+        `slot`, each at a 256-byte aligned offset, so a step needs one host-to-device
+        copy.  Returns (pinned bytes, device bytes, {name: (offset, shape, dtype)})."""
+        layout, off = {}, 0
+        for name, arr, dt in arrays:
+            nb = arr.size * torch.empty(0, dtype=dt).element_size()
+            layout[name] = (off, tuple(arr.shape), dt, nb)
+            off += (nb + 255) & ~255
+        total = max(off, 256)
+        h = self._bufs.get(slot)
+        if h is None or h.numel() < total:
+            h = torch.empty(total * 2, dtype=torch.uint8).pin_memory()
+            self._bufs[slot] = h
+        d = self._dbufs.get("in")
+        if d is None or d.numel() < total:
+            d = torch.empty(total * 2, dtype=torch.uint8, device=self.dev)
+            self._dbufs["in"] = d
+        hn = h.numpy()
+        for name, arr, dt in arrays:
+            o, shape, _, nb = layout[name]
+            np_dt = {torch.int64: np.int64, torch.int32: np.int32}[dt]
+            hn[o:o + nb].view(np_dt)[:] = np.ascontiguousarray(arr, dtype=np_dt).ravel()
+        return h[:total], d[:total], layout
 
     def _dev(self, name, shape, dtype):
         """A device buffer, grown on demand; returns a view of the requested shape."""
@@ -155,53 +162,62 @@ class ServingDriver:
             self._dbufs[name] = buf
         return buf[:n].view(shape)
 
-    def fetch(self, *outs):
-        """Copy a step's outputs to pinned host memory (what a sampler would read)."""
+    def fetch(self, *outs, slot=0):
+        """Copy a step's outputs to pinned host memory (what a sampler would read), into
+        the buffers of `slot` (so a step's outputs stay readable while the next step,
+        using the other slot, runs)."""
         res = []
         for i, t in enumerate(outs):
             if t is None:
                 res.append(None)
                 continue
             n = t.numel()
-            h = self._host.get(i)
+            h = self._host.get((i, slot))
             if h is None or h.numel() < n:
                 h = torch.empty(max(n, 1) * 2, dtype=t.dtype).pin_memory()
-                self._host[i] = h
+                self._host[(i, slot)] = h
             v = h[:n].view(t.shape)
             v.copy_(t, non_blocking=True)
             self.d2h_bytes += n * t.element_size()
             res.append(v)
         return res
 
-    def step(self):
-        """One scheduler step and its kernels.  Returns (inputs, decode_out, prefill_out)
-        (device tensors; decode_out is [num_decode][Hq][D], prefill_out [tokens][Hq][D]).
-        The step's host arrays go through pinned staging buffers; the caller synchronises
-        (or reads the outputs) before the next step reuses them."""
+    def plan_step(self, slot=0):
+        """Host part of one step: the scheduler's plan, the new tokens' ids, positions and
+        table rows, and the step's arrays in pinned staging buffers of `slot`.  Touches
+        no device memory, so it may run while the previous step's kernels execute (use
+        another slot than a step whose copies may still be pending).  Returns the staged
+        step, or its inputs alone when the plan has no new token."""
         plan = self.sched.step()
         x = prepare(plan, self.prompts, self.rows, self.rows)
-        T = x.token_ids.shape[0]
-        if T == 0:
-            return x, None, None
-        # Host side first (the rows of the synthetic model and the plan's arrays into
-        # pinned buffers), then the copies, the row gathers and the kernels back to back
-        # on the stream.
-        staged = {"kvr": self._put("kvr", x.kv_rows, torch.int64),
-                  "qr": self._put("qr", x.q_rows, torch.int64),
-                  "slots": self._put("slots", plan.slot_mapping, torch.int64),
-                  "tables": self._put("tables", plan.block_tables, torch.int32),
-                  "ctx": self._put("ctx", plan.context_lens, torch.int32)}
+        if x.token_ids.shape[0] == 0:
+            return x, None
+        arrays = [("kvr", x.kv_rows, torch.int64), ("qr", x.q_rows, torch.int64),
+                  ("slots", plan.slot_mapping, torch.int64),
+                  ("tables", plan.block_tables, torch.int32),
+                  ("ctx", plan.context_lens, torch.int32)]
         if plan.cow_pairs.size:
-            staged["pairs"] = self._put("pairs", plan.cow_pairs, torch.int32)
+            arrays.append(("pairs", plan.cow_pairs, torch.int32))
         if plan.seq_ids.shape[0] > x.num_decode:
-            staged["pq"] = self._put("pq", x.prefill_query_start, torch.int32)
+            arrays.append(("pq", x.prefill_query_start, torch.int32))
+        staged = self._pack(arrays, slot)
+        return x, staged
+
+    def launch_step(self, x, staged):
+        """Device part of one step, queued on the stream: the copies of the staged arrays,
+        the row gathers and the library's kernels.  Returns (decode_out, prefill_out)
+        (device tensors; decode_out is [num_decode][Hq][D], prefill_out [tokens][Hq][D])."""
+        if staged is None:
+            return None, None
+        plan = x.plan
+        T = x.token_ids.shape[0]
         if self.on_start is not None:
             self.on_start()
-        dv = {}
-        for name, (h, d) in staged.items():
-            d.copy_(h, non_blocking=True)
-            self.h2d_bytes += h.numel() * h.element_size()
-            dv[name] = d
+        hbuf, dbuf, layout = staged
+        dbuf.copy_(hbuf, non_blocking=True)
+        self.h2d_bytes += hbuf.numel()
+        dv = {name: dbuf[o:o + nb].view(dt).view(shape)
+              for name, (o, shape, dt, nb) in layout.items()}
         k_new = self._dev("k", (T, self.Hkv, self.D), torch.bfloat16)
         v_new = self._dev("v", (T, self.Hkv, self.D), torch.bfloat16)
         q = self._dev("q", (T, self.Hq, self.D), torch.bfloat16)
@@ -209,7 +225,7 @@ class ServingDriver:
         torch.index_select(self.v_tab_d, 0, dv["kvr"], out=v_new)
         torch.index_select(self.q_tab_d, 0, dv["qr"], out=q)
         slots, tables, ctx = dv["slots"], dv["tables"], dv["ctx"]
-        if plan.cow_pairs.size:
+        if "pairs" in dv:
             ops.paged_block_copy(self.k_cache, self.v_cache, dv["pairs"], err_flag=self.err,
                                  stream=self.stream)
             self.launches += 1
@@ -229,10 +245,17 @@ class ServingDriver:
                 self.on_decode(1)
             self.launches += 3 if x.decode_ctx_max > self.P else 2
         if plan.seq_ids.shape[0] > nd:
-            pq = dv["pq"]
             pre_out = self._dev("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)
             ops.paged_attention_prefill(pre_out, q[nd:], self.k_cache, self.v_cache, tables[nd:],
-                                        ctx[nd:], pq, self.scale, x.prefill_max_query,
+                                        ctx[nd:], dv["pq"], self.scale, x.prefill_max_query,
                                         err_flag=self.err, stream=self.stream)
             self.launches += 1
-        return x, dec_out, pre_out
+        return dec_out, pre_out
+
+    def step(self):
+        """One scheduler step and its kernels: plan_step then launch_step.  Returns
+        (inputs, decode_out, prefill_out).  The caller synchronises (or reads the
+        outputs) before the next step reuses the staging buffers."""
+        x, staged = self.plan_step()
+        dec, pre = self.launch_step(x, staged)
+        return x, dec, pre

@@ -22,8 +22,40 @@ def u16(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def _steps(drv, overlap):
+    """(inputs, decode_out, prefill_out) of every step, in order.  Without overlap the
+    host waits for each step before the next; with overlap it keeps two steps in flight
+    as the serving benchmark does (step k + 1 planned and queued before step k's outputs,
+    read back into the other slot's pinned buffers, are waited for)."""
+    if not overlap:
+        while not drv.done():
+            x, dec, pre = drv.step()
+            torch.cuda.synchronize()
+            yield x, dec, pre
+        return
+    slot, pending = 0, []
+    while not drv.done():
+        x, staged = drv.plan_step(slot)
+        if staged is None:
+            continue
+        dec, pre = drv.launch_step(x, staged)
+        hd, hp = drv.fetch(dec, pre, slot=slot)
+        ev = torch.cuda.Event()
+        ev.record()
+        pending.append((x, hd, hp, ev))
+        slot ^= 1
+        if len(pending) == 2:
+            x0, hd0, hp0, ev0 = pending.pop(0)
+            ev0.synchronize()
+            yield x0, hd0, hp0
+    for x0, hd0, hp0, ev0 in pending:
+        ev0.synchronize()
+        yield x0, hd0, hp0
+
+
+@pytest.mark.parametrize("overlap", [False, True])
 @pytest.mark.parametrize("cache_entries,blocks", [(None, 400), (40, 400), (30, 60)])
-def test_driver_steps_match_oracle(cache_entries, blocks):
+def test_driver_steps_match_oracle(cache_entries, blocks, overlap):
     from paged_kv_cache_272_gb300.block_pool import BlockPool
     from paged_kv_cache_272_gb300.driver import ServingDriver
     from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
@@ -41,9 +73,7 @@ def test_driver_steps_match_oracle(cache_entries, blocks):
     kh = np.zeros((blocks, Hkv, 16, D), np.uint16)
     vh = np.zeros_like(kh)
     steps = 0
-    while not drv.done():
-        x, dec, pre = drv.step()
-        torch.cuda.synchronize()
+    for x, dec, pre in _steps(drv, overlap):
         steps += 1
         p = x.plan
         if x.token_ids.shape[0] == 0:
