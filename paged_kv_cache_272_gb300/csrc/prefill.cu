@@ -345,19 +345,23 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 
 // ------------------------------------------------------------------------------------
 // tcgen05 variant (head_dim 128): the same arithmetic on the 5th-generation tensor
-// cores.  One CTA = 128 (token, head) rows of one (sequence, KV head), six warps:
+// cores.  One CTA = 128 (token, head) rows of one (sequence, KV head), eight warps:
 //  * warps 0-3 ("softmax"): thread t owns row t -- TMEM lane t of the S and O
-//    accumulators and row t of the Q and P tiles in shared memory.  They stage Q,
-//    read each S tile from TMEM (tcgen05.ld), mask, keep the running max and sum
-//    (the sum in fp32 from the unrounded weights), write the bf16 weights P to shared
-//    memory, rescale O in TMEM when the running max grows by more than 8 in the log2
-//    domain (the sum and O always share one reference, so a stale reference only needs
-//    to keep the weights below 2^8), and finally normalise O.
-//  * warp 4 ("mma", one elected lane): S_j = Q K_j^T (M 128, N 64, K 128) into one of
-//    two TMEM S buffers, and O += P_j V_j (M 128, N 128, K 64) into the TMEM O
-//    accumulator, by tcgen05.mma from shared-memory descriptors; tcgen05.commit signals
-//    the mbarriers (S ready, O ready, K/V slot free).  S runs up to one tile ahead of
-//    P V, so the next scores are ready when the softmax of a tile ends.
+//    accumulators and row t of the Q tile in shared memory.  They stage Q, read each
+//    S tile from TMEM (tcgen05.ld), mask, keep the running max and sum (the sum in fp32
+//    from the unrounded weights; packed f32x2 arithmetic), write the bf16 weights P over
+//    the tile's S columns in TMEM (tcgen05.st; or to shared memory), rescale O in TMEM
+//    when the running max grows by more than 8 in the log2 domain (the sum and O always
+//    share one reference, so a stale reference only needs to keep the weights below
+//    2^8), and finally normalise O.
+//  * warp 4 ("S", one elected lane): S_j = Q K_j^T (M 128, N 64, K 128) into one of two
+//    TMEM S buffers by tcgen05.mma from shared-memory descriptors, once K_j has landed
+//    and the buffer is free; tcgen05.commit signals S ready and the K slot free.
+//  * warp 7 ("P V", one elected lane): O += P_j V_j (M 128, N 128, K 64) into the TMEM
+//    O accumulator once P_j and V_j are ready; commits O ready, the V slot free and
+//    (P in TMEM) the S buffer free.  A tcgen05.mma takes about 70 cycles to issue from
+//    one thread (an S product's eight take longer than they take to run), so the two
+//    kinds of product are issued by different warps and neither waits behind the other.
 //  * warps 5 and 6 ("tma"): lanes 0-3 load the four K (warp 5) or V (warp 6) blocks of
 //    each 64-key tile into their own two-slot ring (TMA tiled copies as in the mma.sync
 //    variant), reading the block ids one tile ahead.
@@ -369,7 +373,7 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 // TMEM: S buffers at columns 0 and 64, O at columns 128..255 (256 allocated).
 
 constexpr int kTcRows = 128;
-constexpr int kTcWarps = 7;
+constexpr int kTcWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 
 // Shared memory is requested 1024-byte aligned and sized exactly, so that two CTAs fit
@@ -733,89 +737,71 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     }
     tc_fence_before();
   } else if (warp == 4) {
-    // ---------------- mma warp: lane 0 issues ----------------
-    // A polling loop issues whichever product is ready, P V first (the softmax of the
-    // next tile waits for it), and lets S run at most one tile ahead of P V (two S
-    // buffers).  Lane 0 tests the barriers without blocking and broadcasts the result.
+    // ---------------- S warp: lane 0 issues the score products ----------------
+    // S_j goes into TMEM buffer j & 1 once K_j has landed and that buffer is free (tile
+    // j - 2's scores were read and, with P in tensor memory, its P V product -- which
+    // reads P from that buffer -- is done).  The P V products are issued by warp 7, so
+    // neither kind of product waits behind the other's issue.
     named_bar_sync(1, 160);
     tc_fence_after();
     constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
-    constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
-    int js = 0, jp = 0;
-    long long idle_since = -1;
-    while (jp < nkt) {
-      bool progressed = false;
-      if (jp < js) {
-        int ready = 0;
-        if (lane == 0)
-          ready = mbar_test_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u) &&
-                  mbar_test_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u);
-        if (__shfl_sync(kAll, ready, 0)) {
-          tc_fence_after();
-          const uint32_t vst = sV + (jp & 1) * Lay::kSlot;
-          if (lane == 0) {
+    int js = 0;
+    for (; js < nkt; ++js) {
+      const int sb = js & 1;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u, abort_flag, a.err) &&
+             (js < 2 || mbar_wait((PT ? pv_done : s_free) + 8 * sb,
+                                  (uint32_t)((js - 2) >> 1) & 1u, abort_flag, a.err));
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t kst = sK + sb * Lay::kSlot;
+      if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k) {
-              if (PT)
-                tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k, sw128_desc(vst + 2048 * k, 8192, 1024),
-                          idO, (jp > 0 || k > 0) ? 1u : 0u);
-              else
-                tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
-                       sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
-            }
-            tc_commit(o_done);
-            tc_commit(v_empty + 8 * (jp & 1));
-            if (PT) tc_commit(pv_done + 8 * (jp & 1));
-          }
-          __syncwarp();
-          ++jp;
-          progressed = true;
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(s_full + 8 * sb);
+        tc_commit(k_empty + 8 * sb);
       }
-      if (js < nkt && js <= jp + 1) {
-        const int sb = js & 1;
-        int ready = 0;
-        if (lane == 0)
-          // S buffer sb is free once tile js - 2's scores were read (and, with P in
-          // tensor memory, its P V product -- which reads P from that buffer -- is done).
-          ready = mbar_test_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u) &&
-                  (js < 2 || mbar_test_wait((PT ? pv_done : s_free) + 8 * sb,
-                                            (uint32_t)((js - 2) >> 1) & 1u));
-        if (__shfl_sync(kAll, ready, 0)) {
-          tc_fence_after();
-          const uint32_t kst = sK + sb * Lay::kSlot;
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                     sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(s_full + 8 * sb);
-            tc_commit(k_empty + 8 * sb);
-          }
-          __syncwarp();
-          ++js;
-          progressed = true;
-        }
-      }
-      if (progressed) {
-        idle_since = -1;
-      } else {
-        if (*abort_flag) break;
-        __nanosleep(32);  // poll less often: the softmax warps need the issue slots
-        const long long now = clock64();
-        if (idle_since < 0) {
-          idle_since = now;
-        } else if (now - idle_since > kWaitCycles) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            flag_error(a.err, PKV_DEV_TIMEOUT);
-          }
-          break;
-        }
-      }
+      __syncwarp();
     }
-    // Every MMA this thread issued has completed once `fin` fires (they complete in order).
+    // The score products this thread issued have completed once the last one's commit
+    // fires (a commit tracks every earlier product of its thread).
+    if (lane == 0 && js > 0) mbar_drain(s_full + 8 * ((js - 1) & 1), (uint32_t)((js - 1) >> 1) & 1u);
+    __syncwarp();
+    tc_fence_before();
+  } else if (warp == 7) {
+    // ---------------- P V warp: lane 0 issues O += P_j V_j ----------------
+    tc_fence_after();
+    constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
+    for (int jp = 0; jp < nkt; ++jp) {
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err) &&
+             mbar_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err);
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t vst = sV + (jp & 1) * Lay::kSlot;
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k) {
+          if (PT)
+            tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k, sw128_desc(vst + 2048 * k, 8192, 1024),
+                      idO, (jp > 0 || k > 0) ? 1u : 0u);
+          else
+            tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
+                   sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(v_empty + 8 * (jp & 1));
+        if (PT) tc_commit(pv_done + 8 * (jp & 1));
+      }
+      __syncwarp();
+    }
+    // Every P V product has completed once `fin` fires; the score products before them
+    // had to (each P V reads the softmax of its scores).
     if (lane == 0) tc_commit(fin);
     __syncwarp();
     mbar_drain(fin, 0);
