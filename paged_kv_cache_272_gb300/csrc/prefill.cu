@@ -750,9 +750,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       const int sb = js & 1;
       int ok = 1;
       if (lane == 0)
-        ok = mbar_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u, abort_flag, a.err) &&
-             (js < 2 || mbar_wait((PT ? pv_done : s_free) + 8 * sb,
-                                  (uint32_t)((js - 2) >> 1) & 1u, abort_flag, a.err));
+        ok = mbar_spin_wait(k_full + 8 * sb, (uint32_t)(js >> 1) & 1u, abort_flag, a.err) &&
+             (js < 2 || mbar_spin_wait((PT ? pv_done : s_free) + 8 * sb,
+                                       (uint32_t)((js - 2) >> 1) & 1u, abort_flag, a.err));
       if (!__shfl_sync(kAll, ok, 0)) break;
       tc_fence_after();
       const uint32_t kst = sK + sb * Lay::kSlot;
@@ -779,8 +779,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     for (int jp = 0; jp < nkt; ++jp) {
       int ok = 1;
       if (lane == 0)
-        ok = mbar_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err) &&
-             mbar_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err);
+        ok = mbar_spin_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err) &&
+             mbar_spin_wait(v_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag, a.err);
       if (!__shfl_sync(kAll, ok, 0)) break;
       tc_fence_after();
       const uint32_t vst = sV + (jp & 1) * Lay::kSlot;

@@ -71,6 +71,26 @@ __device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *ab
   }
 }
 
+// Bounded wait by polling (mbarrier.test_wait, no suspension): for a thread that has
+// nothing else to do and must react at once (it wakes within tens of cycles, where a
+// suspended try_wait took a few hundred).  Same give-up rules as mbar_wait.
+__device__ inline bool mbar_spin_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                      int32_t *err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *abort = 1;
+        flag_error(err, PKV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag (used to drain copies in flight).
 __device__ inline void mbar_drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
