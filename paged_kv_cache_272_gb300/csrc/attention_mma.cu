@@ -284,7 +284,7 @@ __global__ void __launch_bounds__((NW + 1) * 32,
           if (lane < NW && r + BPS * lane < n) {
             const int slot = pslot;
             const uint32_t fb = full0 + 8 * (lane * NS + slot);
-            ok = mbar_wait(empty0 + 8 * (lane * NS + slot), pphase ^ 1, abort_flag, a.err);
+            ok = mbar_spin_wait(empty0 + 8 * (lane * NS + slot), pphase ^ 1, abort_flag, a.err);
             if (ok) {
               // bit j: block j of the stage exists and its id is inside the pool
               int vbits = 0;
