@@ -820,7 +820,7 @@ template <bool KV8>
 int launch_mma_ring(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                     cudaStream_t st) {
   // Defaults measured on GB300: bf16 (one 8 KB block per stage) 3 consumer warps x 2
-  // stages, 3 CTAs per SM; E4M3 (two blocks, 8 KB, per stage) 2 x 2, 5 CTAs per SM.
+  // stages, 4 CTAs per SM; E4M3 (two blocks, 8 KB, per stage) 2 x 2, 5 CTAs per SM.
   int c = ring_choice();
   if (c < 0) c = KV8 ? 4 : 0;
   switch (c) {

@@ -710,10 +710,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       tc_fence_before();
       __syncwarp();
       // Two P barriers (by tile parity): without the P-tile wait above (P in tensor
-      // memory) the softmax may finish tile j + 1 before the MMA warp has seen tile j.
+      // memory) the softmax may finish tile j + 1 before the P V warp has seen tile j.
       if (lane == 0) mbar_arrive(p_full + 8 * sb);
     }
-    // Every product has completed once the MMA warp's final commit fires.
+    // Every product has completed once the P V warp's final commit fires.
     if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
     if (ok && !*abort_flag) {
       tc_fence_after();
