@@ -404,6 +404,21 @@ int pkv_sched_step(pkv_sched *sched, pkv_step_plan *plan);
 int pkv_sched_done(const pkv_sched *sched);  /* 1 when no request is waiting or running */
 int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
 
+/*
+ * pkv_selftest_bounded_wait -- exercises the kernels' failure path without a fault.
+ * Every wait inside the library's kernels is bounded (about one second); when one gives
+ * up, the kernel ORs PKV_DEV_TIMEOUT into the caller's error word and returns, and the
+ * context stays usable.  This call launches one thread that waits, with the same wait
+ * helpers (use_spin != 0: the polling variant) and a limit of limit_cycles clock cycles
+ * (0 < limit_cycles <= about one second), on an mbarrier phase that nothing completes.
+ * err_flag: int32 device word, ORed with PKV_DEV_TIMEOUT when the wait gives up.
+ * result: int64 device array of 3: [0] 1 if the wait succeeded (never), [1] cycles
+ * spent, [2] the CTA abort flag after the wait.  Returns PKV_ERR_NULL for a null pointer,
+ * PKV_ERR_SHAPE for a limit out of range, PKV_ERR_CUDA if the launch failed, else PKV_OK.
+ */
+int pkv_selftest_bounded_wait(int32_t *err_flag, long long *result, long long limit_cycles,
+                              int use_spin, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

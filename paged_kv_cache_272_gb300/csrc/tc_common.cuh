@@ -54,16 +54,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on one phase.  Gives up (returning false) after about a second, or at
-// once when another warp of the CTA has already given up; the first to give up raises
-// the CTA's abort flag and the device error bit.
-__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err) {
+// Bounded wait on one phase.  Gives up (returning false) after `limit` cycles (about a
+// second by default), or at once when another warp of the CTA has already given up;
+// the first to give up raises the CTA's abort flag and the device error bit.
+__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
+                                 long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       flag_error(err, PKV_DEV_TIMEOUT);
       return false;
@@ -75,14 +76,14 @@ __device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *ab
 // nothing else to do and must react at once (it wakes within tens of cycles, where a
 // suspended try_wait took a few hundred).  Same give-up rules as mbar_wait.
 __device__ inline bool mbar_spin_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                      int32_t *err) {
+                                      int32_t *err, long long limit = kWaitCycles) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > limit) {
         *abort = 1;
         flag_error(err, PKV_DEV_TIMEOUT);
         return false;

@@ -71,6 +71,7 @@ SIGNATURES = {
     "pkv_sched_step": (_I, [_P, _P]),
     "pkv_sched_done": (_I, [_P]),
     "pkv_sched_get_stats": (_I, [_P, _P]),
+    "pkv_selftest_bounded_wait": (_I, [_P, _P, ctypes.c_longlong, _I, _P]),
 }
 
 
@@ -281,3 +282,16 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_l
         float(k_scale), float(v_scale), int(partition_size), int(max_context_len),
         _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream)),
         "paged_attention_decode_fp8")
+
+
+def selftest_bounded_wait(err_flag, result, limit_cycles, use_spin=False, stream=None):
+    """Launch the bounded-wait self-test: one thread waits `limit_cycles` clock cycles on
+    an mbarrier phase that nothing completes, then gives up as the library's kernels do
+    (PKV_DEV_TIMEOUT ORed into err_flag).  result: int64 CUDA tensor of 3 (wait
+    succeeded, cycles spent, abort flag)."""
+    _i32("err_flag", err_flag)
+    if result.dtype != torch.int64 or not result.is_cuda or result.numel() < 3:
+        raise TypeError("result must be an int64 CUDA tensor of at least 3 elements")
+    check(lib.pkv_selftest_bounded_wait(_ptr(err_flag), _ptr(result), int(limit_cycles),
+                                        1 if use_spin else 0, _stream(stream)),
+          "pkv_selftest_bounded_wait")

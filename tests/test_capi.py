@@ -105,3 +105,15 @@ def test_slot_mapping_check():
         ops.paged_kv_check_slots(np.array([3, 9, 3]), 4)       # two tokens, one slot
     with pytest.raises(ops.PagedKVError):
         ops.paged_kv_check_slots(np.array([64]), 4)             # past the pool
+
+
+def test_selftest_bounded_wait_validates_on_host():
+    """The bounded-wait self-test rejects null pointers (PKV_ERR_NULL) and out-of-range
+    limits (PKV_ERR_SHAPE) before launching anything, so this runs without a GPU."""
+    from paged_kv_cache_272_gb300 import ops
+    ERR_NULL, ERR_SHAPE = -1, -2
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    assert ops.lib.pkv_selftest_bounded_wait(None, fake, 1000, 0, None) == ERR_NULL
+    assert ops.lib.pkv_selftest_bounded_wait(fake, None, 1000, 0, None) == ERR_NULL
+    assert ops.lib.pkv_selftest_bounded_wait(fake, fake, 0, 0, None) == ERR_SHAPE
+    assert ops.lib.pkv_selftest_bounded_wait(fake, fake, 1 << 40, 1, None) == ERR_SHAPE
