@@ -429,8 +429,8 @@ int blocks_per_sm(K kernel, int threads) {
 
 template <int D, int GM>
 int launch_fma_t(const AttnArgs &a, cudaStream_t st) {
-  static int occ = 0;
-  if (!occ) occ = blocks_per_sm(attn_fma_kernel<D, GM>, 128);
+  static std::atomic<int> occ_slots[kMaxDevices];
+  const int occ = per_device_setup(occ_slots, [] { return blocks_per_sm(attn_fma_kernel<D, GM>, 128); });
   const int64_t upper = (int64_t)a.num_seqs * a.max_parts * a.num_kv_heads * a.sub_groups;
   int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
@@ -439,12 +439,11 @@ int launch_fma_t(const AttnArgs &a, cudaStream_t st) {
 }
 
 int launch_merge(const AttnArgs &a, int head_dim, int64_t max_units, cudaStream_t st) {
-  static int occ[2] = {0, 0};
-  const int k = head_dim == 128 ? 1 : 0;
-  if (!occ[k])
-    occ[k] = head_dim == 128 ? blocks_per_sm(attn_merge_kernel<128>, 256)
-                             : blocks_per_sm(attn_merge_kernel<64>, 256);
-  int64_t grid = (int64_t)device_sm_count() * occ[k];
+  static std::atomic<int> occ128[kMaxDevices], occ64[kMaxDevices];
+  const int occ = head_dim == 128
+                      ? per_device_setup(occ128, [] { return blocks_per_sm(attn_merge_kernel<128>, 256); })
+                      : per_device_setup(occ64, [] { return blocks_per_sm(attn_merge_kernel<64>, 256); });
+  int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
   return (int)(head_dim == 128

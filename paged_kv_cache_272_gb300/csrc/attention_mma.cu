@@ -779,20 +779,20 @@ template <int D, int NW, int NS, bool KV8 = false>
 int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                  cudaStream_t st) {
   using L = MmaLayout<D, NW, NS, KV8>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // CTAs per SM (after opting the kernel into its shared memory on this device)
+  static std::atomic<int> occ_slots[kMaxDevices];
+  const int occ = per_device_setup(occ_slots, [] {
     const cudaError_t e = cudaFuncSetAttribute(
         attn_mma_kernel<D, NW, NS, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
-  static int occ = 0;
-  if (!occ) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_mma_kernel<D, NW, NS, KV8>,
+    if (e != cudaSuccess) return -(int)e;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_mma_kernel<D, NW, NS, KV8>,
                                                       (NW + 1) * 32, L::kSmem) != cudaSuccess ||
-        occ < 1)
-      occ = 1;
-  }
+        n < 1)
+      n = 1;
+    return n;
+  });
+  if (occ <= 0) return -occ;
   const int64_t upper = (int64_t)a.num_seqs * a.max_parts * a.num_kv_heads * a.sub_groups;
   int64_t grid = (int64_t)device_sm_count() * occ;
   if (grid > upper) grid = upper;
@@ -804,15 +804,15 @@ int launch_mma_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv
 // Ring shape (consumer warps x stages per warp), overridable for tuning through the
 // PKV_MMA_RING environment variable; -1 = the path's default.
 int ring_choice() {
-  static int choice = -2;
-  if (choice == -2) {
+  static const int choice = [] {  // read once (thread-safe static initialisation)
     static const char *names[] = {"3x2", "8x2", "4x4", "4x3", "2x2", "2x3", "4x2", "2x4", "3x3",
                                   "1x4", "1x6"};
     const char *v = std::getenv("PKV_MMA_RING");
-    choice = -1;
+    int c = -1;
     for (int i = 0; v && i < (int)(sizeof(names) / sizeof(names[0])); ++i)
-      if (std::strcmp(v, names[i]) == 0) choice = i;
-  }
+      if (std::strcmp(v, names[i]) == 0) c = i;
+    return c;
+  }();
   return choice;
 }
 

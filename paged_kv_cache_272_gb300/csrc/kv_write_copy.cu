@@ -121,15 +121,14 @@ int grid_for(int64_t total, int threads) {
 }  // namespace
 
 int device_sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
+  static std::atomic<int> slots[kMaxDevices];
+  return per_device_setup(slots, [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    return n;
+  });
 }
 
 }  // namespace pkv

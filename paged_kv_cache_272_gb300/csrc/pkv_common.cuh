@@ -1,6 +1,8 @@
 // Shared device helpers of libpagedkv.so (CUDA, sm_103a).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -89,5 +91,24 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int device_sm_count();  // cached per device
+
+// Per-device launch set-up (a kernel attribute, an occupancy figure), computed on the
+// first call that runs with a device current and kept for that device: `compute`
+// returns a positive value to keep, or a non-positive one (an error) that is returned
+// and not kept.  Safe under concurrent first calls from several host threads (each may
+// compute; every access is atomic); devices beyond the table are not cached.
+constexpr int kMaxDevices = 64;
+template <typename F>
+int per_device_setup(std::atomic<int> (&slots)[kMaxDevices], F compute) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = slots[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+  }
+  const int v = compute();
+  if (v > 0 && dev >= 0 && dev < kMaxDevices) slots[dev].store(v, std::memory_order_release);
+  return v;
+}
 
 }  // namespace pkv

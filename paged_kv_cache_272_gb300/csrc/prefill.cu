@@ -329,13 +329,13 @@ template <int D, int NST>
 int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                      cudaStream_t st) {
   using Lay = PrefillLayout<D, NST>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<int> ready[kMaxDevices];  // the kernel's shared-memory opt-in, per device
+  const int r = per_device_setup(ready, [] {
     const cudaError_t e = cudaFuncSetAttribute(
         prefill_kernel<D, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+    return e == cudaSuccess ? 1 : -(int)e;
+  });
+  if (r <= 0) return -r;
   return (int)launch_pdl(prefill_kernel<D, NST>,
                          dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
                               (unsigned)a.num_seqs),
@@ -860,17 +860,17 @@ template <bool PT>
 int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                         cudaStream_t st) {
   using Lay = TcLayout;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<int> ready[kMaxDevices];  // shared-memory opt-in and carve-out, per device
+  const int r = per_device_setup(ready, [] {
     cudaError_t e = cudaFuncSetAttribute(
         prefill_tc_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(prefill_tc_kernel<PT>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+    return e == cudaSuccess ? 1 : -(int)e;
+  });
+  if (r <= 0) return -r;
   return (int)launch_pdl(prefill_tc_kernel<PT>,
                          dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
                               (unsigned)a.num_seqs),
@@ -882,11 +882,10 @@ int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUten
 // stages P in shared memory.
 int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                       cudaStream_t st) {
-  static int p_in_tmem = -1;
-  if (p_in_tmem < 0) {
+  static const bool p_in_tmem = [] {  // read once (thread-safe static initialisation)
     const char *v = std::getenv("PKV_PREFILL_P");
-    p_in_tmem = (v && std::strcmp(v, "smem") == 0) ? 0 : 1;
-  }
+    return !(v && std::strcmp(v, "smem") == 0);
+  }();
   return p_in_tmem ? launch_prefill_tc_t<true>(a, tk, tv, st)
                    : launch_prefill_tc_t<false>(a, tk, tv, st);
 }
