@@ -25,6 +25,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 _lock = threading.Lock()
+ABI_VERSION = 2
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
@@ -54,6 +55,9 @@ def _declare(lib):
     P = ctypes.c_void_p
     I = ctypes.c_int
     lib.oracle_abi_version.restype = I
+    if lib.oracle_abi_version() != ABI_VERSION:
+        raise OracleError(f"stale oracle library (ABI {lib.oracle_abi_version()}, "
+                          f"expected {ABI_VERSION}): rebuild it with build(force=True)")
     lib.oracle_kv_write.argtypes = [P, P, P, P, P, I, I, I, I, I]
     lib.oracle_kv_write.restype = I
     lib.oracle_block_copy.argtypes = [P, P, P, I, I, I, I, I]
@@ -67,12 +71,12 @@ def _declare(lib):
     lib.oracle_e4m3_decode.restype = ctypes.c_double
     lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
-    lib.oracle_kv_write_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, ctypes.c_float]
+    lib.oracle_kv_write_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
     lib.oracle_kv_write_fp8.restype = I
     lib.oracle_block_copy_fp8.argtypes = [P, P, P, I, I, I, I, I]
     lib.oracle_block_copy_fp8.restype = I
     lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
-                                         ctypes.c_double, ctypes.c_double, P, I, I]
+                                         P, P, P, I, I]
     lib.oracle_attention_fp8.restype = I
     lib.oracle_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
                                              ctypes.c_double, P, I, I]
@@ -170,18 +174,28 @@ def e4m3_encode(x: float, lib=None) -> int:
     return int((lib or load()).oracle_e4m3_encode(float(x)))
 
 
+def _per_head(scale, num_kv_heads: int, dtype) -> np.ndarray:
+    """A scale per KV head: a scalar (one scale for the whole cache) or num_kv_heads
+    values."""
+    a = np.asarray(scale, dtype=dtype)
+    assert a.ndim == 0 or a.shape == (num_kv_heads,), a.shape
+    return np.ascontiguousarray(np.broadcast_to(a, (num_kv_heads,)))
+
+
 def kv_write_fp8(k_cache: np.ndarray, v_cache: np.ndarray, k_new, v_new, slot_mapping,
-                 k_scale: float, v_scale: float, lib=None) -> None:
-    """In place on uint8 caches: code = E4M3(bf16 / scale) at each slot."""
+                 k_scale, v_scale, lib=None) -> None:
+    """In place on uint8 caches: code = E4M3(bf16 / scale) at each slot (scale in fp32,
+    one value for the cache or one per KV head)."""
     lib = lib or load()
     assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
     NB, Hkv, bs, D = k_cache.shape
     k_new, v_new = _u16(k_new), _u16(v_new)
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     T = slots.shape[0]
+    ks, vs = _per_head(k_scale, Hkv, np.float32), _per_head(v_scale, Hkv, np.float32)
     _check(lib.oracle_kv_write_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-                                   _ptr(slots), T, NB, Hkv, D, bs, float(k_scale),
-                                   float(v_scale)), "oracle_kv_write_fp8")
+                                   _ptr(slots), T, NB, Hkv, D, bs, _ptr(ks), _ptr(vs)),
+           "oracle_kv_write_fp8")
 
 
 def block_copy_fp8(k_cache: np.ndarray, v_cache: np.ndarray, pairs, lib=None) -> None:
@@ -193,9 +207,10 @@ def block_copy_fp8(k_cache: np.ndarray, v_cache: np.ndarray, pairs, lib=None) ->
 
 
 def attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                  k_scale: float, v_scale: float, sel=None, nthreads: int = 1,
+                  k_scale, v_scale, sel=None, nthreads: int = 1,
                   lib=None) -> np.ndarray:
-    """fp64 decode attention over an E4M3 cache (element = decode(code) * scale)."""
+    """fp64 decode attention over an E4M3 cache (element = decode(code) * scale; the
+    scales are one value for the cache or one per KV head)."""
     lib = lib or load()
     q = _u16(q)
     k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
@@ -213,9 +228,10 @@ def attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
         sel_a = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
         out = np.empty((sel_a.shape[0], D), dtype=np.float64)
         sel_p, nsel = _ptr(sel_a), sel_a.shape[0]
+    ks, vs = _per_head(k_scale, Hkv, np.float64), _per_head(v_scale, Hkv, np.float64)
     _check(lib.oracle_attention_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
                                     _ptr(ctx), S, MB, Hq, Hkv, D, bs, NB, float(scale),
-                                    float(k_scale), float(v_scale), sel_p, nsel, int(nthreads)),
+                                    _ptr(ks), _ptr(vs), sel_p, nsel, int(nthreads)),
            "oracle_attention_fp8")
     return out
 

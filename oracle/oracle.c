@@ -55,7 +55,7 @@ static double bf16_to_f64(uint16_t bits) {
     return (double)f;
 }
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }  /* 2: E4M3 scales per KV head */
 
 int oracle_kv_write(uint16_t *k_cache, uint16_t *v_cache,
                     const uint16_t *k_new, const uint16_t *v_new,
@@ -215,7 +215,9 @@ int64_t oracle_kv_bytes_per_token(int layers, int kv_heads, int head_dim, int by
  * value 448.  Rounding is to nearest, ties to even; a finite value beyond 448 saturates
  * to +-448 (the "satfinite" convention).  A cache element holds
  * code = E4M3(bf16_value / scale), the division taken in fp32, and stands for
- * decode(code) * scale.
+ * decode(code) * scale.  A scale belongs to one KV head of one cache (k_scales[h],
+ * v_scales[h]): the per-tensor scheme is the case of equal entries.  The pages leave
+ * the scale's granularity open; per-KV-head scales follow each head's own range.
  * Layouts: K codes [NB][Hkv][block_size][D] like the bf16 cache; V codes transposed
  * within each block, [NB][Hkv][D][block_size] (an interface choice of the E4M3 cache).
  * ------------------------------------------------------------------------------------ */
@@ -252,8 +254,9 @@ uint8_t oracle_e4m3_encode(float x) {
 int oracle_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
                         const uint16_t *v_new, const int64_t *slot_mapping, int num_tokens,
                         int num_blocks, int num_kv_heads, int head_dim, int block_size,
-                        float k_scale, float v_scale) {
-    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+                        const float *k_scales, const float *v_scales) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        !k_scales || !v_scales)
         return -1;
     const int64_t num_slots = (int64_t)num_blocks * block_size;
     for (int t = 0; t < num_tokens; ++t)
@@ -273,8 +276,8 @@ int oracle_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_ne
             for (int d = 0; d < head_dim; ++d) {
                 float kx = (float)bf16_to_f64(k_new[src + d]);
                 float vx = (float)bf16_to_f64(v_new[src + d]);
-                k_cache[dst + d] = oracle_e4m3_encode(kx / k_scale);
-                v_cache[vbase + (size_t)d * block_size] = oracle_e4m3_encode(vx / v_scale);
+                k_cache[dst + d] = oracle_e4m3_encode(kx / k_scales[h]);
+                v_cache[vbase + (size_t)d * block_size] = oracle_e4m3_encode(vx / v_scales[h]);
             }
         }
     }
@@ -295,16 +298,18 @@ int oracle_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pai
     return 0;
 }
 
-/* Decode attention over an E4M3 cache: every element is decode(code) * scale in fp64;
- * the rest is the same textbook softmax as oracle_attention. */
+/* Decode attention over an E4M3 cache: every element of KV head g is
+ * decode(code) * k_scales[g] (K) or decode(code) * v_scales[g] (V) in fp64; the rest is
+ * the same textbook softmax as oracle_attention. */
 int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                          const uint8_t *v_cache, const int32_t *block_tables,
                          const int32_t *context_lens, int num_seqs, int max_blocks,
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                         int num_blocks, double scale, double k_scale, double v_scale,
-                         const int32_t *sel, int nsel, int nthreads) {
+                         int num_blocks, double scale, const double *k_scales,
+                         const double *v_scales, const int32_t *sel, int nsel, int nthreads) {
     if (num_seqs < 0 || max_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0)
+        head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
+        !k_scales || !v_scales)
         return -1;
     const int npairs = sel ? nsel : num_seqs * num_q_heads;
     const int group = num_q_heads / num_kv_heads;
@@ -336,6 +341,7 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
             const int32_t *table = block_tables + (size_t)s * max_blocks;
             double *o = out + (size_t)i * head_dim;
             const uint16_t *qh = q + ((size_t)s * num_q_heads + h) * head_dim;
+            const double k_scale = k_scales[kv_head], v_scale = v_scales[kv_head];
             if (ctx > max_blocks * block_size) { local = -2; continue; }
             int bad = 0;
             for (int t = 0; t < ctx && !bad; ++t) {

@@ -469,8 +469,17 @@ def _fp8_workload(seed, ctx, Hq=8, Hkv=2, D=128, **kw):
 def pin_fp8_write(lib):
     """The written byte is E4M3(bf16 / scale) (division in fp32), slots skipped when
     negative, everything else untouched; the stored value is within half a grid step.
-    K codes sit at [block][head][offset][d], V codes at [block][head][d][offset]."""
-    NB, Hkv, D = 6, 2, 128
+    K codes sit at [block][head][offset][d], V codes at [block][head][d][offset].  Run
+    with one scale for the cache and with a different scale for each KV head (head h
+    divides by its own entry)."""
+    for ks, vs in ((0.37, 0.0021), ([0.37, 1.5, 0.011], [0.0021, 0.25, 3.0])):
+        _fp8_write_case(lib, ks, vs)
+
+
+def _fp8_write_case(lib, ks, vs):
+    NB, Hkv, D = 6, 3, 128
+    ksh = np.broadcast_to(np.asarray(ks, np.float32), (Hkv,))
+    vsh = np.broadcast_to(np.asarray(vs, np.float32), (Hkv,))
     rng = np.random.default_rng(29)
     k = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
     v = rng.integers(0, 256, size=(NB, Hkv, BS, D), dtype=np.uint8)
@@ -478,7 +487,6 @@ def pin_fp8_write(lib):
     gen = torch.Generator().manual_seed(31)
     newk = (torch.randn(3, Hkv, D, generator=gen) * 40).to(torch.bfloat16)
     newv = (torch.randn(3, Hkv, D, generator=gen) * 0.01).to(torch.bfloat16)
-    ks, vs = 0.37, 0.0021
     slots = [4 * BS + 9, -1, 1 * BS + 0]
     oracle.kv_write_fp8(k, v, newk, newv, slots, ks, vs, lib=lib)
     for t, slot in enumerate(slots):
@@ -487,8 +495,8 @@ def pin_fp8_write(lib):
         b, o = slot // BS, slot % BS
         for h in range(Hkv):
             for d in range(D):
-                xk = float(np.float32(float(newk[t, h, d])) / np.float32(ks))
-                xv = float(np.float32(float(newv[t, h, d])) / np.float32(vs))
+                xk = float(np.float32(float(newk[t, h, d])) / ksh[h])
+                xv = float(np.float32(float(newv[t, h, d])) / vsh[h])
                 k0[b, h, o, d] = oracle.e4m3_encode(xk, lib=lib)
                 v0.reshape(NB, Hkv, D, BS)[b, h, d, o] = oracle.e4m3_encode(xv, lib=lib)
                 dk = oracle.e4m3_decode(int(k0[b, h, o, d]), lib=lib)
@@ -499,25 +507,29 @@ def pin_fp8_write(lib):
 
 def pin_fp8_attention_equals_bf16(lib):
     """With power-of-two scales every decoded element is a bf16 value, so attention over
-    the E4M3 cache equals the pinned bf16 oracle over those values, bit for bit."""
-    w = _fp8_workload(37, [1, 5, 16, 33, 70], poison=False)
+    the E4M3 cache equals the pinned bf16 oracle over those values, bit for bit.  Run
+    with one scale pair for the cache and with a different pair for each KV head (a
+    query head takes the scales of the KV head it reads)."""
+    w = _fp8_workload(37, [1, 5, 16, 33, 70], Hq=12, Hkv=3, poison=False)
     out16, k16, v16 = run_step(w, lib)
-    kq = np.zeros(k16.shape, np.uint8)
-    vq = np.zeros(v16.shape, np.uint8)
-    ks, vs = 0.25, 2.0
-    oracle.kv_write_fp8(kq, vq, _all_rows(k16), _all_rows(v16), np.arange(k16.shape[0] * BS),
-                        ks, vs, lib=lib)
+    NB, Hkv, bs, D = k16.shape
     dec = np.vectorize(lambda c: oracle.e4m3_decode(int(c), lib=lib))
-    NB, Hkv, bs, D = kq.shape
-    kd = torch.from_numpy(dec(kq) * ks).to(torch.bfloat16)
-    # V codes are stored [block][head][d][offset]
-    vt = np.ascontiguousarray(vq.reshape(NB, Hkv, D, bs).transpose(0, 1, 3, 2))
-    vd = torch.from_numpy(dec(vt) * vs).to(torch.bfloat16)
-    assert torch.equal(kd.double(), torch.from_numpy(dec(kq) * ks))  # exact in bf16
-    ref = oracle.attention(w.q, kd, vd, w.block_tables, w.context_lens, w.scale, lib=lib)
-    got = oracle.attention_fp8(w.q, kq, vq, w.block_tables, w.context_lens, w.scale, ks, vs,
-                               lib=lib)
-    assert np.array_equal(ref, got)
+    for ks, vs in ((0.25, 2.0), ([0.25, 4.0, 0.0625], [2.0, 0.5, 8.0])):
+        kq = np.zeros(k16.shape, np.uint8)
+        vq = np.zeros(v16.shape, np.uint8)
+        oracle.kv_write_fp8(kq, vq, _all_rows(k16), _all_rows(v16), np.arange(NB * BS),
+                            ks, vs, lib=lib)
+        ksh = np.broadcast_to(np.asarray(ks, np.float64), (Hkv,))[None, :, None, None]
+        vsh = np.broadcast_to(np.asarray(vs, np.float64), (Hkv,))[None, :, None, None]
+        kd = torch.from_numpy(dec(kq) * ksh).to(torch.bfloat16)
+        # V codes are stored [block][head][d][offset]
+        vt = np.ascontiguousarray(vq.reshape(NB, Hkv, D, bs).transpose(0, 1, 3, 2))
+        vd = torch.from_numpy(dec(vt) * vsh).to(torch.bfloat16)
+        assert torch.equal(kd.double(), torch.from_numpy(dec(kq) * ksh))  # exact in bf16
+        ref = oracle.attention(w.q, kd, vd, w.block_tables, w.context_lens, w.scale, lib=lib)
+        got = oracle.attention_fp8(w.q, kq, vq, w.block_tables, w.context_lens, w.scale, ks,
+                                   vs, lib=lib)
+        assert np.array_equal(ref, got), (ks, vs)
 
 
 def _all_rows(cache_u16):

@@ -44,10 +44,15 @@ MUTANTS = [
     ("e4m3-truncate", "const double r = rint(a / spacing);",
      "const double r = floor(a / spacing);"),
     ("e4m3-no-saturate", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
-    ("fp8-write-no-scale", "k_cache[dst + d] = oracle_e4m3_encode(kx / k_scale);",
+    ("fp8-write-no-scale", "k_cache[dst + d] = oracle_e4m3_encode(kx / k_scales[h]);",
      "k_cache[dst + d] = oracle_e4m3_encode(kx);"),
+    ("fp8-write-first-head-scale", "oracle_e4m3_encode(vx / v_scales[h]);",
+     "oracle_e4m3_encode(vx / v_scales[0]);"),
     ("fp8-attn-v-scale", "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size]) * v_scale;",
      "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size]) * k_scale;"),
+    ("fp8-attn-scale-by-query-head",
+     "const double k_scale = k_scales[kv_head], v_scale = v_scales[kv_head];",
+     "const double k_scale = k_scales[h % num_kv_heads], v_scale = v_scales[h % num_kv_heads];"),
     ("fp8-v-untransposed", "oracle_e4m3_decode(v_cache[vcol + (size_t)d * block_size])",
      "oracle_e4m3_decode(v_cache[row + d])"),
     ("fp8-write-v-untransposed", "v_cache[vbase + (size_t)d * block_size] =",
