@@ -173,21 +173,33 @@ def job_throughput(bytes_per_rank_step: int, steps: int, rank_ms: float, world: 
 FP8_K_SCALE, FP8_V_SCALE = 0.02, 0.015  # N(0,1) data stays well inside E4M3's +-448
 
 
-def oracle_sample_step(w, n_seqs: int, nthreads: int, k_host, v_host):
+def per_head_fp8_scales(w):
+    """Per-KV-head E4M3 scales calibrated on the pre-step cache: the largest finite |value|
+    of each head divided by 448 (E4M3's largest value).  float32 tensors [Hkv] on the
+    cache's device."""
+    def amax(c):
+        x = c.float().abs()
+        x = torch.where(torch.isfinite(x), x, torch.zeros_like(x))
+        return (x.amax(dim=(0, 2, 3)) / 448.0).clamp_min(1e-12).contiguous()
+    return amax(w.k_cache), amax(w.v_cache)
+
+
+def oracle_sample_step(w, n_seqs: int, nthreads: int, k_host, v_host, ks=FP8_K_SCALE,
+                       vs=FP8_V_SCALE):
     import oracle
     sub_bt = np.ascontiguousarray(w.block_tables[:n_seqs])
     sub_ctx = np.ascontiguousarray(w.context_lens[:n_seqs])
     q = w.q[:n_seqs].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
     if k_host.dtype == np.uint8:
-        oracle.attention_fp8(q, k_host, v_host, sub_bt, sub_ctx, w.scale, FP8_K_SCALE,
-                             FP8_V_SCALE, nthreads=nthreads)
+        oracle.attention_fp8(q, k_host, v_host, sub_bt, sub_ctx, w.scale, ks, vs,
+                             nthreads=nthreads)
     else:
         oracle.attention(q, k_host, v_host, sub_bt, sub_ctx, w.scale, nthreads=nthreads)
     return time.perf_counter() - t0, int(sub_ctx.astype(np.int64).sum())
 
 
-def host_caches(w, fp8: bool):
+def host_caches(w, fp8: bool, ks=FP8_K_SCALE, vs=FP8_V_SCALE):
     """The oracle's copy of the pre-step cache (E4M3 codes quantised by the oracle)."""
     import oracle
     k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -198,35 +210,36 @@ def host_caches(w, fp8: bool):
     rows = lambda c: np.ascontiguousarray(c.transpose(0, 2, 1, 3).reshape(NB * bs, Hkv, D))
     kq = np.zeros((NB, Hkv, bs, D), np.uint8)
     vq = np.zeros_like(kq)
-    oracle.kv_write_fp8(kq, vq, rows(k_host), rows(v_host), np.arange(NB * bs), FP8_K_SCALE,
-                        FP8_V_SCALE)
+    oracle.kv_write_fp8(kq, vq, rows(k_host), rows(v_host), np.arange(NB * bs), ks, vs)
     return kq, vq
 
 
-def cpu_baseline(w, budget_s: float = 12.0, fp8: bool = False):
+def cpu_baseline(w, budget_s: float = 12.0, fp8: bool = False, ks=FP8_K_SCALE,
+                 vs=FP8_V_SCALE):
     """Time the oracle, as it stands, on all host cores over the first sequences of the
-    workload, growing the sample until it takes about budget_s / 3, then once more."""
+    workload, growing the sample until it takes about budget_s / 3, then once more.
+    ks/vs: the E4M3 scales (one each, or one per KV head)."""
     nthreads = os.cpu_count() or 1
-    k_host, v_host = host_caches(w, fp8)
+    k_host, v_host = host_caches(w, fp8, ks, vs)
     n = min(w.num_seqs, 2)
     while True:
-        dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host)
+        dt, tok = oracle_sample_step(w, n, nthreads, k_host, v_host, ks, vs)
         if dt > budget_s / 3 or n >= w.num_seqs:
             break
         n = min(w.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 3) / max(dt, 1e-3)))))
     reps, dt, tok = 0, 0.0, 0
     while reps == 0 or dt < budget_s / 3:  # repeat short samples for a stable time
-        d, t = oracle_sample_step(w, n, nthreads, k_host, v_host)
+        d, t = oracle_sample_step(w, n, nthreads, k_host, v_host, ks, vs)
         reps, dt, tok = reps + 1, dt + d, tok + t
     kv_bytes = tok * 2 * w.num_kv_heads * w.head_dim * (1 if fp8 else 2)
     # The same oracle on one thread, over a smaller sample (about budget_s / 4).
     n1 = 1
     while True:
-        d1, t1 = oracle_sample_step(w, n1, 1, k_host, v_host)
+        d1, t1 = oracle_sample_step(w, n1, 1, k_host, v_host, ks, vs)
         if d1 > budget_s / 8 or n1 >= n:
             break
         n1 = min(n, max(n1 + 1, int(n1 * min(8.0, (budget_s / 8) / max(d1, 1e-3)))))
-    d1, t1 = oracle_sample_step(w, n1, 1, k_host, v_host)
+    d1, t1 = oracle_sample_step(w, n1, 1, k_host, v_host, ks, vs)
     kv1 = t1 * 2 * w.num_kv_heads * w.head_dim * (1 if fp8 else 2)
     return {"value": kv_bytes / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"first {n} of {w.num_seqs} sequences, all {w.num_q_heads} query heads, "
@@ -292,15 +305,24 @@ def run_ours(args):
     w = workloads.make_config(args.config, device="cuda")
     S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     fp8 = args.kv_dtype == "fp8"
+    per_head = fp8 and args.fp8_scales == "head"
+    KS, VS = FP8_K_SCALE, FP8_V_SCALE
+    if per_head:
+        ks_dev, vs_dev = per_head_fp8_scales(w)
+        KS, VS = ks_dev.cpu().numpy(), vs_dev.cpu().numpy()
     if fp8:
         # Quantise the whole pre-step cache once (untimed) with the library's own write.
         NB = w.num_blocks
         k = torch.empty(NB, Hkv, 16, D, dtype=torch.uint8, device=dev)
         v = torch.empty_like(k)
         rows = lambda c: c.permute(0, 2, 1, 3).reshape(NB * 16, Hkv, D).contiguous()
-        ops.paged_kv_write_fp8(rows(w.k_cache), rows(w.v_cache),
-                               torch.arange(NB * 16, dtype=torch.int64, device=dev), k, v,
-                               FP8_K_SCALE, FP8_V_SCALE)
+        all_slots = torch.arange(NB * 16, dtype=torch.int64, device=dev)
+        if per_head:
+            ops.paged_kv_write_fp8_per_head(rows(w.k_cache), rows(w.v_cache), all_slots, k, v,
+                                            ks_dev, vs_dev)
+        else:
+            ops.paged_kv_write_fp8(rows(w.k_cache), rows(w.v_cache), all_slots, k, v,
+                                   FP8_K_SCALE, FP8_V_SCALE)
         torch.cuda.synchronize()
     else:
         k = w.k_cache.to(dev).contiguous()
@@ -329,14 +351,21 @@ def run_ours(args):
                                                                      stream=stream)
 
     def do_write(kn, vn, sl):
-        if fp8:
+        if per_head:
+            ops.paged_kv_write_fp8_per_head(kn, vn, sl, k, v, ks_dev, vs_dev, err_flag=err,
+                                            stream=stream)
+        elif fp8:
             ops.paged_kv_write_fp8(kn, vn, sl, k, v, FP8_K_SCALE, FP8_V_SCALE, err_flag=err,
                                    stream=stream)
         else:
             ops.paged_kv_write(kn, vn, sl, k, v, err_flag=err, stream=stream)
 
     def do_attn(qq, btt, cx):
-        if fp8:
+        if per_head:
+            ops.paged_attention_decode_fp8_per_head(out, qq, k, v, btt, cx, w.scale, ks_dev,
+                                                    vs_dev, mcl, ws, P, err_flag=err,
+                                                    stream=stream)
+        elif fp8:
             ops.paged_attention_decode_fp8(out, qq, k, v, btt, cx, w.scale, FP8_K_SCALE,
                                            FP8_V_SCALE, mcl, ws, P, err_flag=err, stream=stream)
         else:
@@ -452,7 +481,10 @@ def run_ours(args):
         "dtype": "e4m3 KV / f16 tiles" if fp8 else "bf16",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "kv_dtype": args.kv_dtype, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "workload": w.name, "kv_dtype": args.kv_dtype,
+            **({"fp8_scales": "one per KV head (amax / 448)" if per_head else "one per cache"}
+               if fp8 else {}),
+            "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
             "head_dim": D, "block_size": w.block_size, "partition_size": P,
             "num_blocks": w.num_blocks, "mean_context": float(w.context_lens.mean()),
             "max_context": mcl, "kv_bytes_per_step": kv_bytes,
@@ -478,7 +510,7 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, fp8=fp8)
+        line["cpu_baseline"] = cpu_baseline(w, fp8=fp8, ks=KS, vs=VS)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -987,6 +1019,8 @@ def main():
                     help="split-K partition size in tokens (default: the workload's, 512)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
+    ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
+                    help="with --kv-dtype fp8: one E4M3 scale per cache, or one per KV head")
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc"],
                     help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc "
                          "for head_dim 128")

@@ -65,6 +65,7 @@ extern "C" {
 #define PKV_DEV_BAD_CONTEXT 4    /* context_len < 0 or beyond table / max_context_len */
 #define PKV_DEV_TIMEOUT 8        /* a bounded wait inside a kernel gave up            */
 #define PKV_DEV_LAYOUT 16        /* shared-memory window misaligned (kernel skipped)  */
+#define PKV_DEV_BAD_SCALE 32     /* a per-KV-head E4M3 scale is not > 0               */
 
 /* Library ABI version (incremented on any signature change). */
 int paged_kv_version(void);
@@ -146,7 +147,8 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
  * largest finite 448).  A cache element is one byte, code = E4M3(x / scale) with the
  * division rounded to nearest in fp32 and the conversion rounded to nearest even with
  * finite saturation; it stands for decode(code) * scale.  One scale per cache (k_scale,
- * v_scale, > 0).  Layouts: k_cache [num_blocks][num_kv_heads][16][head_dim] like the
+ * v_scale, > 0), or one per KV head (the _per_head entry points; the pages leave the
+ * granularity open).  Layouts: k_cache [num_blocks][num_kv_heads][16][head_dim] like the
  * bf16 cache; v_cache transposed within each block, [num_blocks][num_kv_heads][head_dim][16]
  * (so the P.V tile reads consecutive tokens).  Both 16-byte aligned.
  * ------------------------------------------------------------------------------------ */
@@ -157,6 +159,18 @@ int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64
                        int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
                        int num_kv_heads, int head_dim, int block_size, float k_scale,
                        float v_scale, int32_t *err_flag, void *stream);
+
+/* paged_kv_write_fp8 with one scale per KV head: head h's K values are divided by
+ * k_scales[h] and its V values by v_scales[h].  k_scales, v_scales: device arrays of
+ * num_kv_heads fp32 values, each > 0, read by the kernel (so they may be written by
+ * earlier work on the stream); NULL returns PKV_ERR_NULL.  A row whose head has a
+ * scale that is not > 0 (zero, negative, NaN) is not written and sets
+ * PKV_DEV_BAD_SCALE.  The per-cache scheme is the case of equal entries. */
+int paged_kv_write_fp8_per_head(const uint16_t *k_new, const uint16_t *v_new,
+                                const int64_t *slot_mapping, int num_tokens, uint8_t *k_cache,
+                                uint8_t *v_cache, int num_blocks, int num_kv_heads,
+                                int head_dim, int block_size, const float *k_scales,
+                                const float *v_scales, int32_t *err_flag, void *stream);
 
 /* Copy-on-write of whole blocks of E4M3 caches (as paged_block_copy, bit-exact). */
 int paged_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *block_pairs,
@@ -177,6 +191,23 @@ int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *
                                float k_scale, float v_scale, int partition_size,
                                int max_context_len, void *workspace, size_t workspace_bytes,
                                int32_t *err_flag, void *stream);
+
+/* paged_attention_decode_fp8 over caches written with paged_kv_write_fp8_per_head:
+ * every K element of KV head g is decode(code) * k_scales[g] and every V element
+ * decode(code) * v_scales[g], so query head h uses the scales of KV head
+ * h / (num_q_heads / num_kv_heads).  k_scales, v_scales: device arrays of num_kv_heads
+ * fp32 values, each > 0, read by the kernel; NULL returns PKV_ERR_NULL.  A scale that
+ * is not > 0 sets PKV_DEV_BAD_SCALE and the rows of the query heads reading that KV
+ * head are then unspecified (nothing is read or written out of bounds). */
+int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const uint8_t *k_cache,
+                                        const uint8_t *v_cache, const int32_t *block_tables,
+                                        const int32_t *context_lens, int num_seqs,
+                                        int max_blocks_per_seq, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, float scale, const float *k_scales,
+                                        const float *v_scales, int partition_size,
+                                        int max_context_len, void *workspace,
+                                        size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that cannot

@@ -524,7 +524,8 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                        int num_blocks, float scale, int partition_size, int max_context_len,
                        void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
-                       bool kv8, float k_scale, float v_scale) {
+                       bool kv8, float k_scale, float v_scale, const float *k_scales = nullptr,
+                       const float *v_scales = nullptr) {
   if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_context_len < 0 || num_q_heads % num_kv_heads != 0 ||
@@ -562,6 +563,8 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
   a.scale_log2 = (float)((double)scale * (kv8 ? (double)k_scale : 1.0) * 1.4426950408889634);
   a.v_scale = kv8 ? v_scale : 1.0f;
   a.kv8 = kv8 ? 1 : 0;
+  a.k_scales = kv8 ? k_scales : nullptr;
+  a.v_scales = kv8 ? v_scales : nullptr;
   a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
   a.work_next = reinterpret_cast<int32_t *>(wb + ws.work_next_off);
@@ -645,6 +648,24 @@ int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *
                      max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, partition_size, max_context_len, workspace,
                      workspace_bytes, err_flag, stream, true, k_scale, v_scale);
+}
+
+int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const uint8_t *k_cache,
+                                        const uint8_t *v_cache, const int32_t *block_tables,
+                                        const int32_t *context_lens, int num_seqs,
+                                        int max_blocks_per_seq, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, float scale, const float *k_scales,
+                                        const float *v_scales, int partition_size,
+                                        int max_context_len, void *workspace,
+                                        size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (num_seqs > 0 && (!k_scales || !v_scales)) return PKV_ERR_NULL;
+  // scale_log2 = scale * log2(e) here; the kernel multiplies in each KV head's k_scale.
+  return decode_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, partition_size, max_context_len, workspace,
+                     workspace_bytes, err_flag, stream, true, 1.f, 1.f, k_scales, v_scales);
 }
 
 }  // extern "C"

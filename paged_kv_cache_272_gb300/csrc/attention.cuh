@@ -31,6 +31,8 @@ struct AttnArgs {
   float scale_log2;              // scale * log2(e) (* k_scale for an E4M3 cache)
   float v_scale;                 // multiplies every output (1 for a bf16 cache)
   int kv8;                       // the caches hold E4M3 codes instead of bf16
+  const float *k_scales;         // [Hkv] per-KV-head E4M3 scales, or null (per cache:
+  const float *v_scales;         //   scale_log2 and v_scale already hold them)
   // workspace
   int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]

@@ -395,6 +395,15 @@ __global__ void __launch_bounds__((NW + 1) * 32,
     const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
     const int h0 = g * a.group + sub * 8;
     const int gcnt = min(8, a.group - sub * 8);
+    float sl2 = a.scale_log2, vsc = a.v_scale;  // per-cache values (1 for v_scale of bf16)
+    if constexpr (KV8) {
+      if (a.k_scales != nullptr) {  // E4M3 scales of this KV head
+        const float ks = __ldg(a.k_scales + g), vs = __ldg(a.v_scales + g);
+        if (lane == 0 && (!(ks > 0.f) || !(vs > 0.f))) flag_error(a.err, PKV_DEV_BAD_SCALE);
+        sl2 *= ks;
+        vsc = vs;
+      }
+    }
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc[KSTEPS][4];
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__((NW + 1) * 32,
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[j][i] = sc[j][i] * a.scale_log2;
+            for (int i = 0; i < 4; ++i) x[j][i] = sc[j][i] * sl2;
             if (tokA8 >= nv[j]) x[j][0] = x[j][1] = -INFINITY;
             if (tokB8 >= nv[j]) x[j][2] = x[j][3] = -INFINITY;
           }
@@ -645,7 +654,7 @@ __global__ void __launch_bounds__((NW + 1) * 32,
         L0 = fmaf(wl0[w], wm0[w], L0);
         L1 = fmaf(wl1[w], wm1[w], L1);
       }
-      const float f0 = a.v_scale / L0, f1 = a.v_scale / L1;  // v_scale is 1 for bf16
+      const float f0 = vsc / L0, f1 = vsc / L1;
       const bool single = rec.w == 1;
       const int p = t0 / a.part_tokens;
       const int hA = 2 * tig, hB = 2 * tig + 1;  // heads of this lane, within the item

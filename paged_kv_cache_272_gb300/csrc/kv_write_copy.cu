@@ -60,7 +60,8 @@ __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
                                     const int64_t *__restrict__ slots, int64_t total, int row_vecs,
                                     int heads, int64_t num_slots, uint2 *__restrict__ k_cache,
                                     uint8_t *__restrict__ v_cache, float k_scale, float v_scale,
-                                    int32_t *err) {
+                                    const float *__restrict__ k_scales,
+                                    const float *__restrict__ v_scales, int32_t *err) {
   pdl_trigger();
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -75,10 +76,19 @@ __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
       flag_error(err, PKV_DEV_BAD_SLOT);
       continue;
     }
+    float ks = k_scale, vs = v_scale;
+    if (k_scales != nullptr) {  // one scale per KV head
+      ks = __ldg(k_scales + h);
+      vs = __ldg(v_scales + h);
+      if (!(ks > 0.f) || !(vs > 0.f)) {
+        flag_error(err, PKV_DEV_BAD_SCALE);
+        continue;
+      }
+    }
     const int64_t dst = (((slot >> 4) * heads + h) * kBlockSize + (slot & 15)) * row_vecs + e;
     const uint4 kv = k_new[i], vv = v_new[i];
-    k_cache[dst] = make_uint2(quant4(kv.x, kv.y, k_scale), quant4(kv.z, kv.w, k_scale));
-    const uint32_t v0 = quant4(vv.x, vv.y, v_scale), v1 = quant4(vv.z, vv.w, v_scale);
+    k_cache[dst] = make_uint2(quant4(kv.x, kv.y, ks), quant4(kv.z, kv.w, ks));
+    const uint32_t v0 = quant4(vv.x, vv.y, vs), v1 = quant4(vv.z, vv.w, vs);
     const int D = row_vecs * 8;
     uint8_t *vcol = v_cache + (((slot >> 4) * heads + h) * D + e * 8) * kBlockSize + (slot & 15);
 #pragma unroll
@@ -202,12 +212,12 @@ int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_
 
 }  // extern "C"
 
-extern "C" {
-
-int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
-                       int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
-                       int num_kv_heads, int head_dim, int block_size, float k_scale,
-                       float v_scale, int32_t *err_flag, void *stream) {
+// Shared by the per-cache and per-KV-head entry points (k_scales null: per cache).
+static int write_fp8_impl(const uint16_t *k_new, const uint16_t *v_new,
+                          const int64_t *slot_mapping, int num_tokens, uint8_t *k_cache,
+                          uint8_t *v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                          int block_size, float k_scale, float v_scale, const float *k_scales,
+                          const float *v_scales, int32_t *err_flag, void *stream) {
   if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
   if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       head_dim % 16 != 0 || !(k_scale > 0.f) || !(v_scale > 0.f))
@@ -223,8 +233,31 @@ int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64
       kv_write_fp8_kernel, dim3(grid_for(total, threads)), dim3(threads), 0, (cudaStream_t)stream,
       reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
       slot_mapping, total, row_vecs, num_kv_heads, (int64_t)num_blocks * kBlockSize,
-      reinterpret_cast<uint2 *>(k_cache), v_cache, k_scale, v_scale, err_flag);
+      reinterpret_cast<uint2 *>(k_cache), v_cache, k_scale, v_scale, k_scales, v_scales,
+      err_flag);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" {
+
+int paged_kv_write_fp8(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slot_mapping,
+                       int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
+                       int num_kv_heads, int head_dim, int block_size, float k_scale,
+                       float v_scale, int32_t *err_flag, void *stream) {
+  return write_fp8_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                        num_kv_heads, head_dim, block_size, k_scale, v_scale, nullptr, nullptr,
+                        err_flag, stream);
+}
+
+int paged_kv_write_fp8_per_head(const uint16_t *k_new, const uint16_t *v_new,
+                                const int64_t *slot_mapping, int num_tokens, uint8_t *k_cache,
+                                uint8_t *v_cache, int num_blocks, int num_kv_heads,
+                                int head_dim, int block_size, const float *k_scales,
+                                const float *v_scales, int32_t *err_flag, void *stream) {
+  if (num_tokens > 0 && (!k_scales || !v_scales)) return PKV_ERR_NULL;
+  return write_fp8_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                        num_kv_heads, head_dim, block_size, 1.f, 1.f, k_scales, v_scales,
+                        err_flag, stream);
 }
 
 int paged_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *block_pairs,

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
 PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_SCALE = 32
 DEFAULT_PARTITION = 512
 
 # Every entry point the header declares: name -> (restype, argtypes).
@@ -37,9 +38,13 @@ SIGNATURES = {
     "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                             _F, _I, _I, _P, _P]),
     "paged_kv_write_fp8": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
+    "paged_kv_write_fp8_per_head": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P,
+                                         _P]),
     "paged_block_copy_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _F, _I, _I, _P, _SZ, _P, _P]),
+    "paged_attention_decode_fp8_per_head": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                 _I, _F, _P, _P, _I, _I, _P, _SZ, _P, _P]),
     "paged_attention_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      _F, _I, _P, _P]),
     "pkv_pool_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
@@ -253,6 +258,32 @@ def paged_kv_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_
           "paged_kv_write_fp8")
 
 
+def _scales_cuda(name, t, num_kv_heads):
+    if (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()
+            or tuple(t.shape) != (num_kv_heads,)):
+        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor of num_kv_heads")
+
+
+def paged_kv_write_fp8_per_head(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales,
+                                v_scales, err_flag=None, stream=None):
+    """paged_kv_write_fp8 with one scale per KV head (k_scales, v_scales: float32 CUDA
+    tensors [num_kv_heads])."""
+    _bf16_cuda("k_new", k_new)
+    _bf16_cuda("v_new", v_new)
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    NB, Hkv, bs, D = k_cache.shape
+    _scales_cuda("k_scales", k_scales, Hkv)
+    _scales_cuda("v_scales", v_scales, Hkv)
+    T = slot_mapping.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, D) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    check(lib.paged_kv_write_fp8_per_head(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping.contiguous()), T, _ptr(k_cache),
+        _ptr(v_cache), NB, Hkv, D, bs, _ptr(k_scales), _ptr(v_scales), _ptr(err_flag),
+        _stream(stream)), "paged_kv_write_fp8_per_head")
+
+
 def paged_block_copy_fp8(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
     _u8_cuda("k_cache", k_cache)
     _u8_cuda("v_cache", v_cache)
@@ -282,6 +313,32 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_l
         float(k_scale), float(v_scale), int(partition_size), int(max_context_len),
         _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream)),
         "paged_attention_decode_fp8")
+
+
+def paged_attention_decode_fp8_per_head(out, q, k_cache, v_cache, block_tables, context_lens,
+                                        scale, k_scales, v_scales, max_context_len, workspace,
+                                        partition_size=DEFAULT_PARTITION, err_flag=None,
+                                        stream=None):
+    """paged_attention_decode_fp8 with one scale per KV head (k_scales, v_scales: float32
+    CUDA tensors [num_kv_heads])."""
+    _bf16_cuda("out", out)
+    _bf16_cuda("q", q)
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    _scales_cuda("k_scales", k_scales, Hkv)
+    _scales_cuda("v_scales", v_scales, Hkv)
+    if D2 != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    check(lib.paged_attention_decode_fp8_per_head(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
+        _ptr(k_scales), _ptr(v_scales), int(partition_size), int(max_context_len),
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream)),
+        "paged_attention_decode_fp8_per_head")
 
 
 def selftest_bounded_wait(err_flag, result, limit_cycles, use_spin=False, stream=None):

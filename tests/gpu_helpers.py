@@ -113,28 +113,40 @@ def rows_of(cache: torch.Tensor) -> torch.Tensor:
 
 def fp8_step(w, ks=K_SCALE, vs=V_SCALE, partition_size=None, block_tables=None):
     """Quantise the pre-step cache, then COW copy + new-token write + attention, on the
-    GPU and in the oracle.  Returns (gpu_out, gpu k/v codes, oracle k/v codes, err)."""
+    GPU and in the oracle.  Returns (gpu_out, gpu k/v codes, oracle k/v codes, err).
+    ks/vs: one scale each, or one per KV head (sequences of num_kv_heads)."""
     o = ops()
     dev = "cuda"
     NB, Hkv, bs, D = w.k_cache.shape
     kq = torch.zeros(NB, Hkv, bs, D, dtype=torch.uint8, device=dev)
     vq = torch.zeros_like(kq)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if np.ndim(ks) or np.ndim(vs):  # one scale per KV head: the _per_head entry points
+        kst = torch.as_tensor(np.broadcast_to(np.asarray(ks, np.float32), (Hkv,)).copy(),
+                              device=dev)
+        vst = torch.as_tensor(np.broadcast_to(np.asarray(vs, np.float32), (Hkv,)).copy(),
+                              device=dev)
+        write = lambda kn, vn, sl: o.paged_kv_write_fp8_per_head(kn, vn, sl, kq, vq, kst, vst,
+                                                                 err_flag=err)
+        attend = lambda out, q, bt, ctx, ws, P: o.paged_attention_decode_fp8_per_head(
+            out, q, kq, vq, bt, ctx, w.scale, kst, vst, w.max_context_len, ws, P, err_flag=err)
+    else:
+        write = lambda kn, vn, sl: o.paged_kv_write_fp8(kn, vn, sl, kq, vq, ks, vs, err_flag=err)
+        attend = lambda out, q, bt, ctx, ws, P: o.paged_attention_decode_fp8(
+            out, q, kq, vq, bt, ctx, w.scale, ks, vs, w.max_context_len, ws, P, err_flag=err)
     slots_all = torch.arange(NB * bs, dtype=torch.int64, device=dev)
-    o.paged_kv_write_fp8(rows_of(w.k_cache.to(dev)), rows_of(w.v_cache.to(dev)), slots_all, kq, vq,
-                         ks, vs, err_flag=err)
+    write(rows_of(w.k_cache.to(dev)), rows_of(w.v_cache.to(dev)), slots_all)
     d = to_cuda(w)
     if d["pairs"].numel():
         o.paged_block_copy_fp8(kq, vq, d["pairs"], err_flag=err)
     if d["slots"].numel():
-        o.paged_kv_write_fp8(d["k_new"], d["v_new"], d["slots"], kq, vq, ks, vs, err_flag=err)
+        write(d["k_new"], d["v_new"], d["slots"])
     S, Hq, _ = d["q"].shape
     P = partition_size or w.partition_size
     out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = o.alloc_workspace(S, Hq, D, w.max_context_len, P)
     bt = d["bt"] if block_tables is None else block_tables
-    o.paged_attention_decode_fp8(out, d["q"], kq, vq, bt, d["ctx"], w.scale, ks, vs,
-                                 w.max_context_len, ws, P, err_flag=err)
+    attend(out, d["q"], bt, d["ctx"], ws, P)
     torch.cuda.synchronize()
     # oracle
     ko = np.zeros((NB, Hkv, bs, D), np.uint8)
@@ -151,3 +163,29 @@ def fp8_step(w, ks=K_SCALE, vs=V_SCALE, partition_size=None, block_tables=None):
 def fp8_ref(w, ko, vo, ks=K_SCALE, vs=V_SCALE, sel=None):
     return oracle.attention_fp8(u16(w.q), ko, vo, w.block_tables, w.context_lens, w.scale, ks,
                                 vs, sel=sel, nthreads=NTHREADS)
+
+
+def spread_heads(w, factors):
+    """Scale KV head h of the workload's caches and new rows by factors[h] (powers of two,
+    exact in bf16), so that the heads span different ranges."""
+    for h, f in enumerate(factors):
+        for t in (w.k_cache, w.v_cache):
+            t[:, h].mul_(f)
+        for t in (w.k_new, w.v_new):
+            if t.numel():
+                t[:, h].mul_(f)
+
+
+def per_head_scales(w, margin=1.0):
+    """Per-KV-head calibration: the largest |value| of head h over the cache and the new
+    rows (finite values only), divided by 448 (the largest E4M3 value), times margin."""
+    def fin(x):  # poisoned free blocks hold NaN; they take no part in the range
+        x = x.float().abs()
+        return torch.where(torch.isfinite(x), x, torch.zeros_like(x))
+
+    def amax(c, n):
+        a = fin(c).amax(dim=(0, 2, 3))
+        if n.numel():
+            a = torch.maximum(a, fin(n).amax(dim=(0, 2)))
+        return (a.cpu().numpy().astype(np.float64) / 448.0 * margin).astype(np.float32)
+    return amax(w.k_cache, w.k_new), amax(w.v_cache, w.v_new)

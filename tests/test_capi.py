@@ -77,6 +77,31 @@ def test_host_side_validation():
     assert lib.paged_attention_prefill(*pre(T=0)) == 0
 
 
+def test_fp8_per_head_host_validation():
+    """The per-KV-head E4M3 entry points reject missing scale arrays and bad shapes on the
+    host; with nothing to do they touch nothing."""
+    from paged_kv_cache_272_gb300.ops import lib
+    fake = 1 << 20
+    w = lambda **kw: [fake, fake, fake, kw.get("T", 4), fake, fake, 8, 2, kw.get("D", 128),
+                      kw.get("bs", 16), kw.get("ks", fake), kw.get("vs", fake), None, None]
+    assert lib.paged_kv_write_fp8_per_head(*w(ks=None)) == -1
+    assert lib.paged_kv_write_fp8_per_head(*w(vs=None)) == -1
+    assert lib.paged_kv_write_fp8_per_head(*w(bs=8)) == -3
+    assert lib.paged_kv_write_fp8_per_head(*w(D=72)) == -2
+    assert lib.paged_kv_write_fp8_per_head(*w(T=0, ks=None, vs=None)) == 0
+    ws = lib.paged_attention_workspace_size(4, 8, 128, 1000, 512)
+    a = lambda **kw: [fake, fake, fake, fake, fake, fake, kw.get("S", 4), 8, 8, 2,
+                      kw.get("D", 128), kw.get("bs", 16), 16, ctypes.c_float(0.1),
+                      kw.get("ks", fake), kw.get("vs", fake), 512, 1000, fake,
+                      kw.get("ws", ws), None, None]
+    assert lib.paged_attention_decode_fp8_per_head(*a(ks=None)) == -1
+    assert lib.paged_attention_decode_fp8_per_head(*a(vs=None)) == -1
+    assert lib.paged_attention_decode_fp8_per_head(*a(D=64)) == -2
+    assert lib.paged_attention_decode_fp8_per_head(*a(bs=32)) == -3
+    assert lib.paged_attention_decode_fp8_per_head(*a(ws=ws - 1)) == -5
+    assert lib.paged_attention_decode_fp8_per_head(*a(S=0, ks=None, vs=None)) == 0
+
+
 def test_strerror():
     from paged_kv_cache_272_gb300.ops import lib
     for code in (0, -1, -2, -3, -4, -5, -6, -10, -11, -12, -13, -14, -99):

@@ -123,3 +123,91 @@ def test_fp8_rejects_other_head_dims():
                                      torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
                                      torch.ones(1, dtype=torch.int32, device="cuda"), 0.125, 1.0,
                                      1.0, 16, ws)
+
+
+# ---- one scale per KV head ------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_fp8_per_head_config_parity(cfg):
+    """KV heads spread over 2^-3 .. 2^3 in range, each quantised with its own calibrated
+    scale: the write/copy bytes match the oracle and the output is within tolerance."""
+    w = workloads.make_config(cfg, device="cuda")
+    Hkv = w.num_kv_heads
+    H.spread_heads(w, [2.0 ** ((h % 7) - 3) for h in range(Hkv)])
+    ks, vs = H.per_head_scales(w)
+    assert len(set(ks.tolist())) > 1
+    out, kq, vq, ko, vo, err = fp8_step(w, ks, vs)
+    assert err == 0
+    assert same_codes(kq, ko) and same_codes(vq, vo), "per-head E4M3 write/copy not bit-exact"
+    if cfg == 2:
+        H.assert_attention_close(out, fp8_ref(w, ko, vo, ks, vs), f"fp8 per-head config {cfg}")
+    else:
+        sel = H.sample_pairs(w, n_short=256)
+        got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+                  torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+        H.assert_attention_close(got, fp8_ref(w, ko, vo, ks, vs, sel=sel),
+                                 f"fp8 per-head config {cfg} sample")
+
+
+@pytest.mark.parametrize("G", [1, 3, 8, 16])
+def test_fp8_per_head_groups(G):
+    """Every query head of a group takes its KV head's scales (three KV heads with
+    different scales; groups below, at and above the kernel's 8-row tile)."""
+    ctx = [1, 16, 17, 513, 1500]
+    w = workloads.build("fp8-ph", ctx, 3 * G, 3, 128, seed=120 + G, device="cuda")
+    H.spread_heads(w, [0.25, 1.0, 8.0])
+    ks = np.array([0.0005, 0.004, 0.03], np.float32)
+    vs = np.array([0.03, 0.0007, 0.005], np.float32)
+    for P in (64, 512):
+        out, kq, vq, ko, vo, err = fp8_step(w, ks, vs, partition_size=P)
+        assert err == 0
+        assert same_codes(kq, ko) and same_codes(vq, vo)
+        H.assert_attention_close(out, fp8_ref(w, ko, vo, ks, vs), f"fp8 per-head G={G} P={P}")
+
+
+def test_fp8_per_head_equal_entries_match_per_cache():
+    """Equal per-head entries write the same bytes as the one-scale write."""
+    w = workloads.build("fp8-eq", [30, 300], 8, 2, 128, seed=131, device="cuda")
+    _, kq1, vq1, _, _, err1 = fp8_step(w)
+    _, kq2, vq2, _, _, err2 = fp8_step(w, [K_SCALE] * 2, [V_SCALE] * 2)
+    assert err1 == err2 == 0
+    assert np.array_equal(kq1, kq2) and np.array_equal(vq1, vq2)
+
+
+def test_fp8_per_head_bad_scale_is_flagged():
+    """A scale that is not > 0 is reported: the write skips that head's rows, attention
+    flags it; the other KV head's rows are written and attended as usual."""
+    o = H.ops()
+    w = workloads.build("fp8-badscale", [20, 70], 8, 2, 128, seed=133, device="cuda",
+                        poison=False)
+    d = H.to_cuda(w)
+    NB, Hkv, bs, D = w.k_cache.shape
+    for bad in (0.0, -0.5, float("nan")):
+        kq = torch.zeros(NB, Hkv, bs, D, dtype=torch.uint8, device="cuda")
+        vq = torch.zeros_like(kq)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kst = torch.tensor([K_SCALE, K_SCALE], dtype=torch.float32, device="cuda")
+        vst = torch.tensor([V_SCALE, bad], dtype=torch.float32, device="cuda")
+        o.paged_kv_write_fp8_per_head(H.rows_of(w.k_cache.cuda()), H.rows_of(w.v_cache.cuda()),
+                                      torch.arange(NB * bs, device="cuda"), kq, vq, kst, vst,
+                                      err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == o.DEV_BAD_SCALE, bad
+        assert not kq[:, 1].any() and not vq[:, 1].any()  # head 1 untouched
+        ko = np.zeros((NB, Hkv, bs, D), np.uint8)
+        vo = np.zeros_like(ko)
+        oracle.kv_write_fp8(ko, vo, H.u16(H.rows_of(w.k_cache.cpu())),
+                            H.u16(H.rows_of(w.v_cache.cpu())), np.arange(NB * bs), K_SCALE,
+                            V_SCALE)
+        assert same_codes(kq.cpu().numpy()[:, 0], ko[:, 0])
+        assert same_codes(vq.cpu().numpy()[:, 0], vo[:, 0])
+        if bad != bad:  # NaN: the write check only
+            continue
+        err.zero_()
+        out = torch.zeros(w.num_seqs, 8, D, dtype=torch.bfloat16, device="cuda")
+        ws = o.alloc_workspace(w.num_seqs, 8, D, w.max_context_len, 64)
+        o.paged_attention_decode_fp8_per_head(out, d["q"], kq, vq, d["bt"], d["ctx"], w.scale,
+                                              kst, vst, w.max_context_len, ws, 64, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == o.DEV_BAD_SCALE, bad
+        ref = fp8_ref(w, ko, vo)
+        H.assert_attention_close(out[:, :4], ref[:, :4], "heads of the good KV head")
