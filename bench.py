@@ -177,10 +177,12 @@ def per_head_fp8_scales(w):
     """Per-KV-head E4M3 scales calibrated on the pre-step cache: the largest finite |value|
     of each head divided by 448 (E4M3's largest value).  float32 tensors [Hkv] on the
     cache's device."""
-    def amax(c):
-        x = c.float().abs()
-        x = torch.where(torch.isfinite(x), x, torch.zeros_like(x))
-        return (x.amax(dim=(0, 2, 3)) / 448.0).clamp_min(1e-12).contiguous()
+    def amax(c):  # one KV head at a time (bounded temporaries on large caches)
+        out = []
+        for h in range(c.shape[1]):
+            x = c[:, h].float().abs()
+            out.append(torch.where(torch.isfinite(x), x, torch.zeros_like(x)).amax())
+        return (torch.stack(out) / 448.0).clamp_min(1e-12).contiguous()
     return amax(w.k_cache), amax(w.v_cache)
 
 
@@ -423,28 +425,32 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
 
     # ---- end to end through the public API, host buffers ------------------------------
-    h = {name: t.cpu().pin_memory() for name, t in
-         (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("pairs", pairs),
-          ("bt", bt), ("ctx", ctx))}
+    # The step's inputs sit in one pinned host buffer, each at a 256-byte aligned offset,
+    # and cross in one copy; the output comes back in one copy.
+    srcs = (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots), ("pairs", pairs),
+            ("bt", bt), ("ctx", ctx))
+    offs, off = {}, 0
+    for name, t in srcs:
+        nb = t.numel() * t.element_size()
+        offs[name] = (off, nb)
+        off += (nb + 255) & ~255
+    h_in = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(h_in.numel(), dtype=torch.uint8, device=dev)
+    dv = {}
+    for name, t in srcs:
+        o, nb = offs[name]
+        h_in[o:o + nb].copy_(t.contiguous().reshape(-1).view(torch.uint8).cpu())
+        dv[name] = d_in[o:o + nb].view(t.dtype).view(t.shape)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dkn, dvn = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    dsl, dpr = torch.empty_like(slots), torch.empty_like(pairs)
-    dbt, dctx = torch.empty_like(bt), torch.empty_like(ctx)
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    h2d = h_in.numel()
     d2h = out.numel() * out.element_size()
 
     def e2e_step():
-        dq.copy_(h["q"], non_blocking=True)
-        dkn.copy_(h["k_new"], non_blocking=True)
-        dvn.copy_(h["v_new"], non_blocking=True)
-        dsl.copy_(h["slots"], non_blocking=True)
-        dbt.copy_(h["bt"], non_blocking=True)
-        dctx.copy_(h["ctx"], non_blocking=True)
-        if dpr.numel():
-            dpr.copy_(h["pairs"], non_blocking=True)
-            do_copy(dpr)
-        do_write(dkn, dvn, dsl)
-        do_attn(dq, dbt, dctx)
+        d_in.copy_(h_in, non_blocking=True)
+        if dv["pairs"].numel():
+            do_copy(dv["pairs"])
+        do_write(dv["k_new"], dv["v_new"], dv["slots"])
+        do_attn(dv["q"], dv["bt"], dv["ctx"])
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):

@@ -179,13 +179,12 @@ def spread_heads(w, factors):
 def per_head_scales(w, margin=1.0):
     """Per-KV-head calibration: the largest |value| of head h over the cache and the new
     rows (finite values only), divided by 448 (the largest E4M3 value), times margin."""
-    def fin(x):  # poisoned free blocks hold NaN; they take no part in the range
+    def fin_amax(x):  # poisoned free blocks hold NaN; they take no part in the range
         x = x.float().abs()
-        return torch.where(torch.isfinite(x), x, torch.zeros_like(x))
+        return float(torch.where(torch.isfinite(x), x, torch.zeros_like(x)).max())
 
-    def amax(c, n):
-        a = fin(c).amax(dim=(0, 2, 3))
-        if n.numel():
-            a = torch.maximum(a, fin(n).amax(dim=(0, 2)))
-        return (a.cpu().numpy().astype(np.float64) / 448.0 * margin).astype(np.float32)
+    def amax(c, n):  # one KV head at a time (bounded temporaries on large caches)
+        a = np.array([max(fin_amax(c[:, h]), fin_amax(n[:, h]) if n.numel() else 0.0)
+                      for h in range(c.shape[1])])
+        return (a / 448.0 * margin).astype(np.float32)
     return amax(w.k_cache, w.k_new), amax(w.v_cache, w.v_new)
