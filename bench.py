@@ -814,14 +814,17 @@ def serve_run(drv, stream, decode_bytes_per_token):
             tot["dec_ms"] += dev_pair[0].elapsed_time(dev_pair[1])
             tot["dec_bytes"] += int(p.context_lens[:nd].astype(np.int64).sum()) * decode_bytes_per_token
 
+    # timing events, reused: a set is free again once its step has retired
+    ev_sets = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(3)]
     t0 = time.perf_counter()
-    slot, pending = 0, []
+    slot, pending, k = 0, [], 0
     while not drv.done():
         x, staged = drv.plan_step(slot)  # the step that used this slot has retired
         if staged is None:  # nothing to compute this step
             continue
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        cur["dec"] = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        a, b, d0, d1 = ev_sets[k % 3]
+        k += 1
+        cur["dec"] = (d0, d1)
         drv.on_start = lambda: a.record(stream)
         nvtx.range_push(f"serving step {tot['steps'] + len(pending)}")
         dec, pre = drv.launch_step(x, staged)

@@ -19,6 +19,7 @@ position).
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 
 import numpy as np
@@ -155,7 +156,7 @@ class ServingDriver:
 
     def _dev(self, name, shape, dtype):
         """A device buffer, grown on demand; returns a view of the requested shape."""
-        n = int(np.prod(shape)) if len(shape) else 1
+        n = math.prod(shape)
         buf = self._dbufs.get(name)
         if buf is None or buf.numel() < n:
             buf = torch.empty(max(n, 1) * 2, dtype=dtype, device=self.dev)

@@ -34,9 +34,11 @@ class SchedStats(ctypes.Structure):
 
 
 def _arr(ptr, n, dtype):
-    if n <= 0:
-        return np.zeros(0, dtype)
-    return np.ctypeslib.as_array(ptr, shape=(n,)).copy()
+    """A numpy copy of n elements at a C array (one memmove)."""
+    a = np.empty(max(n, 0), dtype)
+    if n > 0:
+        ctypes.memmove(a.ctypes.data, ptr, a.nbytes)
+    return a
 
 
 @dataclass
