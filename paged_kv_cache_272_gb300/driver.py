@@ -31,19 +31,22 @@ from .serving import Plan, Scheduler
 BS = 16
 
 
+def _i64(a: np.ndarray) -> np.ndarray:
+    return np.asarray(a, dtype=np.int64)  # no copy when already int64
+
+
 def kv_row(token_ids: np.ndarray, positions: np.ndarray, rows: int) -> np.ndarray:
     """Row of the K/V tables for (token id, position)."""
-    return (token_ids.astype(np.int64) * 1000003 + positions.astype(np.int64) * 7919) % rows
+    return (_i64(token_ids) * 1000003 + _i64(positions) * 7919) % rows
 
 
 def q_row(rids: np.ndarray, positions: np.ndarray, rows: int) -> np.ndarray:
-    return (rids.astype(np.int64) * 2654435761 + positions.astype(np.int64) * 40503) % rows
+    return (_i64(rids) * 2654435761 + _i64(positions) * 40503) % rows
 
 
 def output_token(rids: np.ndarray, positions: np.ndarray) -> np.ndarray:
     """Synthetic id of the output token at a position (>= prompt length)."""
-    return ((rids.astype(np.int64) * 7777 + positions.astype(np.int64) * 131) % 32000).astype(
-        np.int32)
+    return ((_i64(rids) * 7777 + _i64(positions) * 131) % 32000).astype(np.int32)
 
 
 @dataclass
@@ -60,25 +63,33 @@ class StepInputs:
     prefill_max_query: int
 
 
-def prepare(plan: Plan, prompts: dict, kv_rows_n: int, q_rows_n: int) -> StepInputs:
+def prepare(plan: Plan, prompts: dict, kv_rows_n: int, q_rows_n: int,
+            prompt_lens: np.ndarray | None = None) -> StepInputs:
     """Token ids, positions and table rows of a step's new tokens (host only).  Entry i
     covers positions context_lens[i] - query_lens[i] .. context_lens[i] - 1; a position
-    inside the request's prompt takes the prompt's token, any later one a generated id."""
-    seq = plan.seq_ids.astype(np.int64)
+    inside the request's prompt takes the prompt's token, any later one a generated id.
+    prompt_lens: optional array of prompt lengths indexed by request id (a faster lookup
+    than the prompts dict when the ids are small integers)."""
+    seq = _i64(plan.seq_ids)
     L = plan.query_lens.astype(np.int64)
     c = plan.context_lens.astype(np.int64)
     T = int(L.sum())
+    first = c - L  # each entry's first new position
     starts = np.cumsum(L) - L
     rid_of = np.repeat(seq, L)
-    pos = np.repeat(c - L, L) + (np.arange(T, dtype=np.int64) - np.repeat(starts, L))
+    pos = np.repeat(first - starts, L) + np.arange(T, dtype=np.int64)
     ids = output_token(rid_of, pos)
-    plen = np.fromiter((len(prompts[r]) for r in seq.tolist()), dtype=np.int64, count=len(seq))
-    for i in np.flatnonzero(c - L < plen).tolist():  # entries that reach into their prompt
-        lo, hi = int(c[i] - L[i]), int(min(c[i], plen[i]))
+    if prompt_lens is not None:
+        plen = prompt_lens[seq]
+    else:
+        plen = np.fromiter((len(prompts[r]) for r in seq.tolist()), dtype=np.int64,
+                           count=len(seq))
+    for i in np.flatnonzero(first < plen).tolist():  # entries that reach into their prompt
+        lo, hi = int(first[i]), int(min(c[i], plen[i]))
         ids[starts[i]:starts[i] + hi - lo] = prompts[int(seq[i])][lo:hi]
     nd = plan.num_decode
     pq = plan.query_start[nd:] - plan.query_start[nd]
-    return StepInputs(plan=plan, token_ids=ids.astype(np.int32), positions=pos.astype(np.int32),
+    return StepInputs(plan=plan, token_ids=ids, positions=pos.astype(np.int32),
                       kv_rows=kv_row(ids, pos, kv_rows_n), q_rows=q_row(rid_of, pos, q_rows_n),
                       num_decode=nd,
                       decode_ctx_max=int(plan.context_lens[:nd].max()) if nd else 0,
@@ -107,6 +118,7 @@ class ServingDriver:
                                    device=self.dev)
         self.v_cache = torch.zeros_like(self.k_cache)
         self.prompts: dict[int, np.ndarray] = {}
+        self._plen: np.ndarray | None = np.zeros(1024, np.int64)
         self.max_context = max_context
         self.P = partition_size
         self.ws = ops.alloc_workspace(sched.max_num_seqs, num_q_heads, head_dim, max_context,
@@ -116,6 +128,7 @@ class ServingDriver:
         self.launches = 0
         self._bufs = {}
         self._dbufs = {}
+        self._views = {}
         self._host = {}
         self.h2d_bytes = 0
         self.d2h_bytes = 0
@@ -124,6 +137,15 @@ class ServingDriver:
 
     def add_request(self, rid: int, prompt, output_len: int) -> None:
         self.prompts[rid] = np.ascontiguousarray(prompt, dtype=np.int32)
+        if self._plen is not None:  # prompt lengths by id while the ids are small
+            if 0 <= rid < (1 << 20):
+                if rid >= self._plen.shape[0]:
+                    self._plen = np.concatenate(
+                        [self._plen, np.zeros(max(rid + 1, 2 * self._plen.shape[0]) -
+                                              self._plen.shape[0], np.int64)])
+                self._plen[rid] = self.prompts[rid].shape[0]
+            else:
+                self._plen = None
         self.sched.add_request(rid, self.prompts[rid], output_len)
 
     def done(self) -> bool:
@@ -155,13 +177,22 @@ class ServingDriver:
         return h[:total], d[:total], layout
 
     def _dev(self, name, shape, dtype):
-        """A device buffer, grown on demand; returns a view of the requested shape."""
+        """A device buffer, grown on demand; returns a view of the requested shape (views
+        are kept per shape until the buffer grows)."""
+        v = self._views.get((name, shape))
+        if v is not None:
+            return v
         n = math.prod(shape)
         buf = self._dbufs.get(name)
         if buf is None or buf.numel() < n:
             buf = torch.empty(max(n, 1) * 2, dtype=dtype, device=self.dev)
             self._dbufs[name] = buf
-        return buf[:n].view(shape)
+            self._views = {k: t for k, t in self._views.items() if k[0] != name}
+        if len(self._views) > 4096:
+            self._views.clear()
+        v = buf[:n].view(shape)
+        self._views[(name, shape)] = v
+        return v
 
     def fetch(self, *outs, slot=0):
         """Copy a step's outputs to pinned host memory (what a sampler would read), into
@@ -190,7 +221,7 @@ class ServingDriver:
         another slot than a step whose copies may still be pending).  Returns the staged
         step, or its inputs alone when the plan has no new token."""
         plan = self.sched.step()
-        x = prepare(plan, self.prompts, self.rows, self.rows)
+        x = prepare(plan, self.prompts, self.rows, self.rows, self._plen)
         if x.token_ids.shape[0] == 0:
             return x, None
         arrays = [("kvr", x.kv_rows, torch.int64), ("qr", x.q_rows, torch.int64),
@@ -217,8 +248,12 @@ class ServingDriver:
         hbuf, dbuf, layout = staged
         dbuf.copy_(hbuf, non_blocking=True)
         self.h2d_bytes += hbuf.numel()
-        dv = {name: dbuf[o:o + nb].view(dt).view(shape)
-              for name, (o, shape, dt, nb) in layout.items()}
+        typed = {torch.int64: (dbuf.view(torch.int64), 8), torch.int32: (dbuf.view(torch.int32), 4)}
+        dv = {}
+        for name, (o, shape, dt, nb) in layout.items():
+            t, es = typed[dt]
+            v = t[o // es:(o + nb) // es]
+            dv[name] = v if len(shape) == 1 else v.view(shape)
         k_new = self._dev("k", (T, self.Hkv, self.D), torch.bfloat16)
         v_new = self._dev("v", (T, self.Hkv, self.D), torch.bfloat16)
         q = self._dev("q", (T, self.Hq, self.D), torch.bfloat16)
