@@ -253,6 +253,53 @@ def cpu_baseline(w, budget_s: float = 12.0, fp8: bool = False, ks=FP8_K_SCALE,
                            "seconds": d1, "seq_steps_per_s_per_layer": n1 / d1}}
 
 
+def sample_parity(w, out, fp8: bool = False, ks=FP8_K_SCALE, vs=FP8_V_SCALE, n_pairs: int = 96,
+                  nthreads: int | None = None) -> dict:
+    """The bench's own output against the oracle on sampled (sequence, head) rows: one head
+    per KV head of the longest sequence plus random rows.  The oracle's caches are the
+    pre-step cache with the step applied (copy-on-write, then the new tokens' write) --
+    applying it to a cache that already holds it changes nothing.  Tolerance per element
+    1e-2 + 1e-2 |ref|, mean |err| <= 2e-3."""
+    import oracle
+    nthreads = nthreads or os.cpu_count() or 1
+    k_host, v_host = host_caches(w, fp8, ks, vs)
+    k_host, v_host = np.array(k_host), np.array(v_host)  # private, writable copies
+    u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    if w.cow_pairs.size:
+        (oracle.block_copy_fp8 if fp8 else oracle.block_copy)(k_host, v_host, w.cow_pairs)
+    if w.slot_mapping.size:
+        if fp8:
+            oracle.kv_write_fp8(k_host, v_host, u16(w.k_new), u16(w.v_new), w.slot_mapping, ks,
+                                vs)
+        else:
+            oracle.kv_write(k_host, v_host, u16(w.k_new), u16(w.v_new), w.slot_mapping)
+    rng = np.random.default_rng(7)
+    G = w.num_q_heads // w.num_kv_heads
+    s_long = int(np.argmax(w.context_lens))
+    pairs = [(s_long, g * G + int(rng.integers(G))) for g in range(w.num_kv_heads)]
+    while len(pairs) < n_pairs:
+        pairs.append((int(rng.integers(w.num_seqs)), int(rng.integers(w.num_q_heads))))
+    sel = np.array(pairs, dtype=np.int32)
+    q = u16(w.q)
+    if fp8:
+        ref = oracle.attention_fp8(q, k_host, v_host, w.block_tables, w.context_lens, w.scale,
+                                   ks, vs, sel=sel, nthreads=nthreads)
+    else:
+        ref = oracle.attention(q, k_host, v_host, w.block_tables, w.context_lens, w.scale,
+                               sel=sel, nthreads=nthreads)
+    idx_s = torch.as_tensor(sel[:, 0].astype(np.int64), device=out.device)
+    idx_h = torch.as_tensor(sel[:, 1].astype(np.int64), device=out.device)
+    got = out[idx_s, idx_h].float().cpu().double().numpy()
+    err = np.abs(got - ref)
+    bad = int(np.count_nonzero(~(err <= 1e-2 + 1e-2 * np.abs(ref))))
+    return {"rows": int(sel.shape[0]), "max_abs_err": float(err.max()),
+            "mean_abs_err": float(err.mean()), "elements_out_of_tolerance": bad,
+            "within_tolerance": bool(bad == 0 and err.mean() <= 2e-3),
+            "tolerance": "|err| <= 1e-2 + 1e-2 |ref| per element, mean |err| <= 2e-3",
+            "reference": "fp64 oracle on (sequence, head) rows: one head per KV head of the "
+                         "longest sequence plus random rows"}
+
+
 # -------------------------------------------------------------------------------------
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -517,6 +564,10 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, fp8=fp8, ks=KS, vs=VS)
+        try:  # the output of the last timed step against the oracle
+            line["parity"] = sample_parity(w, out, fp8, KS, VS)
+        except Exception as e:  # reported, never fatal to the measurement line
+            line["parity"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
