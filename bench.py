@@ -628,6 +628,34 @@ def prefill_cpu_baseline(w, budget_s: float = 12.0):
             "seconds": tot_t}
 
 
+def prefill_sample_parity(w, out, n_rows: int = 128, nthreads: int | None = None) -> dict:
+    """The bench's own prefill output against the oracle on sampled (token, head) rows: the
+    last token of every chunk plus random rows (cache = the pre-step cache with the
+    step's write applied; re-applying it to a cache that holds it changes nothing)."""
+    import oracle
+    nthreads = nthreads or os.cpu_count() or 1
+    k_host, v_host = prefill_host_caches(w)
+    rng = np.random.default_rng(11)
+    rows = [(int(w.query_start[s + 1]) - 1, int(rng.integers(w.num_q_heads)))
+            for s in range(w.num_seqs) if w.query_start[s + 1] > w.query_start[s]]
+    while len(rows) < n_rows:
+        rows.append((int(rng.integers(w.num_tokens)), int(rng.integers(w.num_q_heads))))
+    sel = np.array(rows, dtype=np.int32)
+    ref = oracle.attention_prefill(w.q.cpu(), k_host, v_host, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale, sel=sel, nthreads=nthreads)
+    idx_t = torch.as_tensor(sel[:, 0].astype(np.int64), device=out.device)
+    idx_h = torch.as_tensor(sel[:, 1].astype(np.int64), device=out.device)
+    got = out[idx_t, idx_h].float().cpu().double().numpy()
+    err = np.abs(got - ref)
+    bad = int(np.count_nonzero(~(err <= 1e-2 + 1e-2 * np.abs(ref))))
+    return {"rows": int(sel.shape[0]), "max_abs_err": float(err.max()),
+            "mean_abs_err": float(err.mean()), "elements_out_of_tolerance": bad,
+            "within_tolerance": bool(bad == 0 and err.mean() <= 2e-3),
+            "tolerance": "|err| <= 1e-2 + 1e-2 |ref| per element, mean |err| <= 2e-3",
+            "reference": "fp64 oracle on (token, head) rows: the last token of every chunk "
+                         "plus random rows"}
+
+
 def run_prefill_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -806,6 +834,10 @@ def run_prefill(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = prefill_cpu_baseline(w)
+        try:  # the output of the last timed step against the oracle
+            line["parity"] = prefill_sample_parity(w, out)
+        except Exception as e:  # reported, never fatal to the measurement line
+            line["parity"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
