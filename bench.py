@@ -307,7 +307,7 @@ def run_reference(args):
     if rank != 0:
         return
     w = workloads.make_config(args.config, device="cpu" if args.config == 1 else "cuda"
-                              if torch.cuda.is_available() else "cpu")
+                              if torch.cuda.is_available() else "cpu", seed=args.seed)
     nthreads = os.cpu_count() or 1
     k_host = w.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     v_host = w.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -351,7 +351,7 @@ def run_ours(args):
                "mma": ops.PKV_ATTN_MMA}[args.variant]
     ops.set_attention_variant(variant)
 
-    w = workloads.make_config(args.config, device="cuda")
+    w = workloads.make_config(args.config, device="cuda", seed=args.seed)
     S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     fp8 = args.kv_dtype == "fp8"
     per_head = fp8 and args.fp8_scales == "head"
@@ -535,6 +535,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": w.name, "kv_dtype": args.kv_dtype,
+            **({"seed": args.seed} if args.seed is not None else {}),
             **({"fp8_scales": "one per KV head (amax / 448)" if per_head else "one per cache"}
                if fp8 else {}),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
@@ -556,7 +557,8 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.name, vname),
+                     # captured on the default draw of each workload only
+                     "traffic": recorded_traffic(w.name, vname) if args.seed is None else None,
                      "kernel": "paged_attention_decode: plan + partition (%s) + merge kernels"
                                % vname,
                      "peak_source": f"{peak_kind} hbm_gbs"},
@@ -660,7 +662,7 @@ def run_prefill_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workloads.make_prefill_config(args.config, device="cpu")
+    w = workloads.make_prefill_config(args.config, device="cpu", seed=args.seed)
     nthreads = os.cpu_count() or 1
     k_host, v_host = prefill_host_caches(w)
     sel, _, _ = prefill_sample_rows(w, 0.7, nthreads, k_host, v_host)
@@ -694,7 +696,7 @@ def run_prefill(args):
     pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
           "tc": ops.PKV_PREFILL_TC}[args.prefill_kernel]
     ops.set_prefill_variant(pk)
-    w = workloads.make_prefill_config(args.config, device="cuda")
+    w = workloads.make_prefill_config(args.config, device="cuda", seed=args.seed)
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
     k = w.k_cache.to(dev).contiguous()
     v = w.v_cache.to(dev).contiguous()
@@ -808,7 +810,8 @@ def run_prefill(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": w.name, "num_seqs": w.num_seqs, "new_tokens_per_step": T,
+            "workload": w.name, **({"seed": args.seed} if args.seed is not None else {}),
+            "num_seqs": w.num_seqs, "new_tokens_per_step": T,
             "max_query_len": w.max_query_len, "num_q_heads": Hq, "num_kv_heads": Hkv,
             "head_dim": D, "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(w.context_lens.mean()), "max_context": w.max_context_len,
@@ -825,7 +828,8 @@ def run_prefill(args):
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.name, kname, PREFILL_SOURCES),
+                     "traffic": (recorded_traffic(w.name, kname, PREFILL_SOURCES)
+                                 if args.seed is None else None),
                      "kernel": ("paged_attention_prefill: prefill_tc_kernel (tcgen05.mma, "
                                 "TMEM accumulators)" if tc else
                                 "paged_attention_prefill: prefill_kernel (mma.sync)"),
@@ -1109,6 +1113,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition", type=int, default=0,
                     help="split-K partition size in tokens (default: the workload's, 512)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="draw the decode or prefill workload with this seed instead of its "
+                         "default (1000 + config, 2000 + config); the recorded DRAM traffic "
+                         "is then not reported")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
