@@ -327,6 +327,20 @@ int pkv_pool_step(pkv_pool *pool, const int64_t *seqs, int n, int64_t *slot_mapp
 int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_blocks,
                     int32_t pad, int32_t *block_tables, int32_t *context_lens);
 
+/* Checkpoint / resume of the host allocator (the pages have none; it lets a serving
+ * process save its block bookkeeping beside the KV caches and rebuild it).
+ * pkv_pool_save: the snapshot's size in bytes; with buf non-NULL and buf_bytes at least
+ * that size it also writes the snapshot there (caller-owned memory).  The snapshot holds
+ * the free order, every refcount (retains by a prefix cache included) and every
+ * sequence's table and length, as little-endian int64 words.  PKV_ERR_NULL for a NULL
+ * pool, PKV_ERR_ARG for a buffer too small.
+ * pkv_pool_load: a new pool (release it with pkv_pool_destroy) in the saved state; the
+ * next calls on it behave exactly as on the saved pool.  PKV_ERR_ARG, and *out = NULL,
+ * for bytes that are not a consistent snapshot (wrong size or magic, ids out of range,
+ * a repeated free block, a free block in a table, a refcount below its table uses). */
+int64_t pkv_pool_save(const pkv_pool *pool, void *buf, int64_t buf_bytes);
+int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out);
+
 /* ------------------------------------------------------------------------------------
  * Block pool: sharing primitives used by the prefix cache.
  * ------------------------------------------------------------------------------------ */

@@ -42,6 +42,34 @@ class BlockPool:
         self.num_blocks = num_blocks
         self.block_size = block_size
 
+    def retain(self, block: int) -> None:
+        """One more holder of an allocated block (as a prefix cache takes)."""
+        _chk(lib.pkv_block_retain(self._h, block), "pkv_block_retain")
+
+    def release(self, block: int) -> None:
+        """One holder fewer; the block returns to the pool with its last holder."""
+        _chk(lib.pkv_block_release(self._h, block), "pkv_block_release")
+
+    def save(self) -> bytes:
+        """A snapshot of the pool's state (free order, refcounts, tables, lengths)."""
+        n = lib.pkv_pool_save(self._h, None, 0)
+        _chk(min(int(n), 0), "pkv_pool_save")
+        buf = ctypes.create_string_buffer(int(n))
+        _chk(min(int(lib.pkv_pool_save(self._h, buf, n)), 0), "pkv_pool_save")
+        return buf.raw
+
+    @classmethod
+    def load(cls, data: bytes) -> "BlockPool":
+        """A new pool in the state a snapshot from save() recorded."""
+        h = ctypes.c_void_p()
+        buf = ctypes.create_string_buffer(bytes(data), len(data))
+        _chk(lib.pkv_pool_load(buf, len(data), ctypes.byref(h)), "pkv_pool_load")
+        self = cls.__new__(cls)
+        self._h = h
+        self.num_blocks = int.from_bytes(data[8:16], "little")
+        self.block_size = int.from_bytes(data[16:24], "little")
+        return self
+
     def close(self):
         if self._h:
             lib.pkv_pool_destroy(self._h)

@@ -12,6 +12,7 @@
 // failing call leaves the pool unchanged: the block demand of a call is counted before
 // anything is modified.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -237,6 +238,115 @@ int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_bl
     for (int j = (int)nb; j < max_blocks; ++j) row[j] = pad;
     context_lens[i] = (int32_t)sq.num_tokens;
   }
+  return PKV_OK;
+}
+
+// Snapshot of the pool (checkpoint / resume of the host allocator): little-endian int64
+// words -- magic, num_blocks, block_size, the free stack (bottom to top), every block's
+// refcount, then each sequence (ascending id) as id, num_tokens, table length, table.
+static const int64_t kPoolMagic = 0x314C4F4F5056504BLL;  // "PKVPOOL1"
+
+int64_t pkv_pool_save(const pkv_pool *pool, void *buf, int64_t buf_bytes) {
+  if (!pool) return PKV_ERR_NULL;
+  std::vector<int64_t> ids;
+  ids.reserve(pool->seqs.size());
+  int64_t words = 4 + (int64_t)pool->free_stack.size() + pool->num_blocks + 1;
+  for (const auto &kv : pool->seqs) {
+    ids.push_back(kv.first);
+    words += 3 + (int64_t)kv.second.table.size();
+  }
+  const int64_t bytes = words * 8;
+  if (!buf) return bytes;
+  if (buf_bytes < bytes) return PKV_ERR_ARG;
+  std::sort(ids.begin(), ids.end());
+  std::vector<int64_t> w;
+  w.reserve(words);
+  w.push_back(kPoolMagic);
+  w.push_back(pool->num_blocks);
+  w.push_back(pool->block_size);
+  w.push_back((int64_t)pool->free_stack.size());
+  for (int32_t b : pool->free_stack) w.push_back(b);
+  for (int32_t r : pool->refcount) w.push_back(r);
+  w.push_back((int64_t)ids.size());
+  for (int64_t id : ids) {
+    const pkv_pool::Seq &sq = pool->seqs.at(id);
+    w.push_back(id);
+    w.push_back(sq.num_tokens);
+    w.push_back((int64_t)sq.table.size());
+    for (int32_t b : sq.table) w.push_back(b);
+  }
+  std::memcpy(buf, w.data(), (size_t)bytes);
+  return bytes;
+}
+
+// Rebuild a pool from pkv_pool_save's bytes.  The snapshot is checked before anything
+// is built: sizes and ids in range, the free stack without repeats, free blocks (and only
+// they) at refcount 0, every table of length ceil(num_tokens / block_size) naming blocks
+// in use, and no block referenced by more tables than its refcount.
+int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out) {
+  if (!out) return PKV_ERR_NULL;
+  *out = nullptr;
+  if (!buf) return PKV_ERR_NULL;
+  if (buf_bytes < 40 || buf_bytes % 8 != 0) return PKV_ERR_ARG;
+  const int64_t n = buf_bytes / 8;
+  std::vector<int64_t> w((size_t)n);
+  std::memcpy(w.data(), buf, (size_t)buf_bytes);
+  int64_t at = 0;
+  auto next = [&](int64_t &v) -> bool {
+    if (at >= n) return false;
+    v = w[(size_t)at++];
+    return true;
+  };
+  int64_t magic, nb, bs, nfree;
+  if (!next(magic) || magic != kPoolMagic || !next(nb) || !next(bs) || !next(nfree))
+    return PKV_ERR_ARG;
+  if (nb <= 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX || nfree < 0 || nfree > nb)
+    return PKV_ERR_ARG;
+  pkv_pool *p = new (std::nothrow) pkv_pool();
+  if (!p) return PKV_ERR_OOM;
+  auto fail = [&](int code) {
+    delete p;
+    return code;
+  };
+  p->num_blocks = (int)nb;
+  p->block_size = (int)bs;
+  std::vector<char> is_free((size_t)nb, 0);
+  p->free_stack.reserve((size_t)nfree);
+  for (int64_t i = 0; i < nfree; ++i) {
+    int64_t b;
+    if (!next(b) || b < 0 || b >= nb || is_free[(size_t)b]) return fail(PKV_ERR_ARG);
+    is_free[(size_t)b] = 1;
+    p->free_stack.push_back((int32_t)b);
+  }
+  p->refcount.resize((size_t)nb);
+  for (int64_t b = 0; b < nb; ++b) {
+    int64_t r;
+    if (!next(r) || r < 0 || r > INT32_MAX || (r == 0) != (is_free[(size_t)b] != 0))
+      return fail(PKV_ERR_ARG);
+    p->refcount[(size_t)b] = (int32_t)r;
+  }
+  int64_t nseq;
+  if (!next(nseq) || nseq < 0) return fail(PKV_ERR_ARG);
+  std::vector<int64_t> uses((size_t)nb, 0);
+  for (int64_t i = 0; i < nseq; ++i) {
+    int64_t id, ntok, len;
+    if (!next(id) || !next(ntok) || !next(len) || ntok < 0 || len != (ntok + bs - 1) / bs ||
+        len > n - at || p->seqs.count(id))
+      return fail(PKV_ERR_ARG);
+    pkv_pool::Seq sq;
+    sq.num_tokens = ntok;
+    sq.table.reserve((size_t)len);
+    for (int64_t j = 0; j < len; ++j) {
+      int64_t b;
+      if (!next(b) || b < 0 || b >= nb || is_free[(size_t)b] ||
+          ++uses[(size_t)b] > p->refcount[(size_t)b])
+        return fail(PKV_ERR_ARG);
+      sq.table.push_back((int32_t)b);
+    }
+    p->seqs.emplace(id, std::move(sq));
+  }
+  if (at != n) return fail(PKV_ERR_ARG);
+  *out = p;
   return PKV_OK;
 }
 

@@ -60,6 +60,8 @@ SIGNATURES = {
     "pkv_seq_append_tokens": (_I, [_P, _I64, _I, _P, _P, _P]),
     "pkv_pool_step": (_I, [_P, _P, _I, _P, _P, _P]),
     "pkv_pool_export": (_I, [_P, _P, _I, _I, ctypes.c_int32, _P, _P]),
+    "pkv_pool_save": (_I64, [_P, _P, _I64]),
+    "pkv_pool_load": (_I, [_P, _I64, ctypes.POINTER(_P)]),
     "pkv_seq_add_shared": (_I, [_P, _I64, _P, _I]),
     "pkv_block_retain": (_I, [_P, _I]),
     "pkv_block_release": (_I, [_P, _I]),

@@ -136,3 +136,104 @@ def test_step_oom_is_atomic():
     with pytest.raises(OutOfBlocks):
         pool.step([0, 1])
     same_state(ref, pool, [0, 1])
+
+
+# -------------------------------------------------------------------------------------
+# Snapshot (checkpoint / resume) of the native pool
+# -------------------------------------------------------------------------------------
+def _random_op(rng, pool, live, nid):
+    """One random operation; returns (what happened, next id).  Out-of-blocks is an
+    outcome like any other."""
+    op = rng.random()
+    try:
+        if op < 0.12 or not live:
+            pool.add_seq(nid)
+            live.append(nid)
+            return ("add", nid), nid + 1
+        if op < 0.45:
+            s, c = rng.choice(live), rng.randint(0, 40)
+            slots, pairs = pool.append_tokens(s, c)
+            return ("append", slots.tolist(), pairs.tolist()), nid
+        if op < 0.70:
+            slots, pairs = pool.step([rng.choice(live) for _ in range(rng.randint(1, 6))])
+            return ("step", slots.tolist(), pairs.tolist()), nid
+        if op < 0.80:
+            return ("slot", pool.append_slot(rng.choice(live))), nid
+        if op < 0.88:
+            pool.fork(rng.choice(live), nid)
+            live.append(nid)
+            return ("fork", nid), nid + 1
+        if op < 0.93:  # an extra holder, as a prefix cache takes
+            s = rng.choice(live)
+            t = pool.block_table(s)
+            if t:
+                pool.retain(t[0])
+            return ("retain", t[:1]), nid
+        s = rng.choice(live)
+        pool.free_seq(s)
+        live.remove(s)
+        return ("free", s), nid
+    except OutOfBlocks:
+        return ("oom",), nid
+
+
+def _state(pool, live):
+    return (pool.num_free(), [pool.refcount(b) for b in range(pool.num_blocks)],
+            {s: (pool.block_table(s), pool.num_tokens(s)) for s in live})
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_snapshot_resumes_identically(seed):
+    """A pool rebuilt from a snapshot at random points answers every later operation
+    exactly as the original does, and snapshots itself to the same bytes."""
+    rng = random.Random(100 + seed)
+    nb = rng.choice([12, 60, 300])
+    pool = BlockPool(nb, BS, free_order=rng.sample(range(nb), nb))
+    live, nid = [], 0
+    for round_ in range(6):
+        for _ in range(rng.randint(50, 250)):
+            _, nid = _random_op(rng, pool, live, nid)
+        snap = pool.save()
+        copy = BlockPool.load(snap)
+        assert copy.save() == snap
+        assert (copy.num_blocks, copy.block_size) == (nb, BS)
+        assert _state(copy, live) == _state(pool, live)
+        r1, r2 = random.Random(seed * 7 + round_), random.Random(seed * 7 + round_)
+        live1, live2, n1, n2 = list(live), list(live), nid, nid
+        for _ in range(200):
+            a, n1 = _random_op(r1, pool, live1, n1)
+            b, n2 = _random_op(r2, copy, live2, n2)
+            assert a == b
+        assert live1 == live2 and _state(copy, live2) == _state(pool, live1)
+        live, nid = live1, n1
+        copy.close()
+
+
+def test_snapshot_rejects_inconsistent_bytes():
+    pool = BlockPool(10, BS)
+    pool.add_seq(1)
+    pool.append_tokens(1, 20)  # two blocks
+    pool.fork(1, 2)
+    snap = bytearray(pool.save())
+    w = np.frombuffer(bytes(snap), dtype="<i8").copy()
+    nfree = int(w[3])
+    ref_at = 4 + nfree  # the refcounts
+    seq_at = ref_at + 10 + 1  # first sequence record
+    table0 = int(w[seq_at + 3])
+
+    def bad(words):
+        with pytest.raises(PagedKVError):
+            BlockPool.load(np.asarray(words, dtype="<i8").tobytes())
+
+    bad(w[:-1])                                   # truncated
+    bad(np.concatenate([w, [0]]))                 # trailing word
+    x = w.copy(); x[0] ^= 1; bad(x)               # magic
+    x = w.copy(); x[1] = 0; bad(x)                # no blocks
+    x = w.copy(); x[4] = x[5]; bad(x)             # a block twice on the free stack
+    x = w.copy(); x[ref_at + table0] = 1; bad(x)  # refcount below the two tables' uses
+    x = w.copy(); x[ref_at + int(w[4])] = 1; bad(x)  # a free block with a holder
+    x = w.copy(); x[seq_at + 3] = 99; bad(x)      # table entry out of range
+    x = w.copy(); x[seq_at + 3] = w[4]; bad(x)    # a free block in a table
+    x = w.copy(); x[seq_at + 1] = 40; bad(x)      # length does not match the table
+    with pytest.raises(PagedKVError):
+        BlockPool.load(bytes(snap[:20]))          # shorter than the header
