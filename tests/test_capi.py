@@ -33,6 +33,58 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) <= set(ops.SIGNATURES)
 
 
+def _declarations():
+    """(return type, name, [parameter declarations]) of every function the header
+    declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    out = []
+    for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b([a-z_0-9]+)\s*\(([^;{]*?)\)\s*;",
+                                        text, flags=re.S):
+        ps = " ".join(params.split())
+        out.append((" ".join(ret.split()), name,
+                    [] if ps in ("", "void") else [p.strip() for p in ps.split(",")]))
+    return out
+
+
+def _ctype_of(decl: str):
+    """The ctypes type a C parameter (or return) declaration needs."""
+    if "*" in decl:
+        return "pointer"
+    words = decl.replace("const ", "").split()
+    base = " ".join(words[:-1]) if len(words) > 1 else words[0]
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64,
+            "long long": ctypes.c_longlong, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float, "double": ctypes.c_double, "void": None}[base]
+
+
+def _same(want, got):
+    if want == "pointer":
+        return got is ctypes.c_void_p or got is ctypes.c_char_p or (
+            isinstance(got, type) and issubclass(got, ctypes._Pointer))
+    if want is None:
+        return got is None
+    return ctypes.sizeof(want) == ctypes.sizeof(got) and (
+        issubclass(want, (ctypes.c_float, ctypes.c_double)) ==
+        issubclass(got, (ctypes.c_float, ctypes.c_double)))
+
+
+def test_binding_matches_header_parameter_by_parameter():
+    """Every declared function's ctypes signature has the header's parameter count and,
+    position by position, a pointer where the header has a pointer and an integer or
+    float of the header's width elsewhere (a mismatch would hand the library a wrong
+    value or pointer)."""
+    from paged_kv_cache_272_gb300 import ops
+    decls = _declarations()
+    assert len(decls) >= len(declared_functions())
+    for ret, name, params in decls:
+        restype, argtypes = ops.SIGNATURES[name]
+        assert len(argtypes) == len(params), (name, params, argtypes)
+        for i, (p, a) in enumerate(zip(params, argtypes)):
+            assert _same(_ctype_of(p), a), (name, i, p, a)
+        assert _same(_ctype_of(ret + " r"), restype), (name, ret, restype)
+
+
 def test_host_side_validation():
     from paged_kv_cache_272_gb300.ops import lib
     fake = 1 << 20  # never dereferenced: every call below fails validation first
