@@ -283,9 +283,15 @@ def test_driver_step_inputs_follow_the_plan(num_blocks):
     for r in reqs:
         prompts[r.rid] = r.prompt
         s.add_request(r.rid, r.prompt, r.output_len)
+    plen = np.zeros(max(prompts) + 1, np.int64)  # the driver's lookup by request id
+    for rid, pr in prompts.items():
+        plen[rid] = len(pr)
     while not s.done():
         plan = s.step()
         x = driver.prepare(plan, prompts, 4096, 4096)
+        y = driver.prepare(plan, prompts, 4096, 4096, plen)
+        for f in ("token_ids", "positions", "kv_rows", "q_rows", "prefill_query_start"):
+            assert np.array_equal(getattr(x, f), getattr(y, f)), f
         assert x.token_ids.shape[0] == plan.slot_mapping.shape[0]
         for i, rid in enumerate(plan.seq_ids.tolist()):
             a, b = int(plan.query_start[i]), int(plan.query_start[i + 1])
