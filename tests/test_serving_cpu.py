@@ -393,3 +393,23 @@ def test_scheduler_plans_pass_the_slot_check():
     nat, pool, cache, plans = native_run(reqs, 300, 8, 256, cache_entries=40)
     for p in plans:
         ops.paged_kv_check_slots(p.slot_mapping, 300)
+
+
+def test_driver_prompt_length_table_grows_and_falls_back():
+    """The driver's prompt-length table (request id -> length) grows past its first
+    size, and ids it cannot index (negative, huge) switch it off in favour of the
+    prompts dict (logic only: a stand-in object, no device)."""
+    from types import SimpleNamespace
+    from paged_kv_cache_272_gb300 import driver
+    added = []
+    fake = SimpleNamespace(prompts={}, _plen=np.zeros(4, np.int64),
+                           sched=SimpleNamespace(add_request=lambda *a: added.append(a[0])))
+    for rid, n in ((0, 5), (3, 7), (9, 2), (40, 11)):
+        driver.ServingDriver.add_request(fake, rid, np.arange(n), 3)
+    assert fake._plen.shape[0] >= 41
+    assert [int(fake._plen[r]) for r in (0, 3, 9, 40)] == [5, 7, 2, 11]
+    assert int(fake._plen[1]) == 0 and added == [0, 3, 9, 40]
+    driver.ServingDriver.add_request(fake, 1 << 40, np.arange(3), 3)
+    assert fake._plen is None and len(fake.prompts[1 << 40]) == 3
+    driver.ServingDriver.add_request(fake, 5, np.arange(6), 3)  # stays off
+    assert fake._plen is None
