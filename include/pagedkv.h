@@ -67,7 +67,10 @@ extern "C" {
 #define PKV_DEV_LAYOUT 16        /* shared-memory window misaligned (kernel skipped)  */
 #define PKV_DEV_BAD_SCALE 32     /* a per-KV-head E4M3 scale is not > 0               */
 
-/* Library ABI version (incremented on any signature change). */
+/* Library ABI version: PKV_ABI_VERSION of the build (incremented when an entry point is
+ * added or a signature changes).  2 added paged_kv_write_fp8_per_head,
+ * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load. */
+#define PKV_ABI_VERSION 2
 int paged_kv_version(void);
 
 /* Human-readable text of a PKV_ERR_* code. Never NULL; static storage. */

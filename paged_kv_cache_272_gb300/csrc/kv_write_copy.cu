@@ -147,7 +147,7 @@ using namespace pkv;
 
 extern "C" {
 
-int paged_kv_version(void) { return 1; }
+int paged_kv_version(void) { return PKV_ABI_VERSION; }
 
 const char *paged_kv_strerror(int code) {
   switch (code) {

@@ -24,6 +24,7 @@ DEFAULT_PARTITION = 512
 # Every entry point the header declares: name -> (restype, argtypes).
 _P, _I, _F, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
                          ctypes.c_int64)
+ABI_VERSION = 2  # PKV_ABI_VERSION of include/pagedkv.h
 SIGNATURES = {
     "paged_kv_version": (_I, []),
     "paged_kv_strerror": (ctypes.c_char_p, [_I]),
@@ -92,6 +93,9 @@ def _load():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    if lib.paged_kv_version() != ABI_VERSION:
+        raise ImportError(f"{LIB_PATH} has ABI version {lib.paged_kv_version()}, this binding "
+                          f"expects {ABI_VERSION}: rebuild the library")
     return lib
 
 

@@ -154,6 +154,12 @@ def test_fp8_per_head_host_validation():
     assert lib.paged_attention_decode_fp8_per_head(*a(S=0, ks=None, vs=None)) == 0
 
 
+def test_abi_version_matches_header():
+    from paged_kv_cache_272_gb300 import ops
+    m = re.search(r"#define PKV_ABI_VERSION (\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == ops.ABI_VERSION == ops.lib.paged_kv_version()
+
+
 def test_strerror():
     from paged_kv_cache_272_gb300.ops import lib
     for code in (0, -1, -2, -3, -4, -5, -6, -10, -11, -12, -13, -14, -99):
