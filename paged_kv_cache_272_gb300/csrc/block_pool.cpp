@@ -15,6 +15,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -279,42 +280,29 @@ int64_t pkv_pool_save(const pkv_pool *pool, void *buf, int64_t buf_bytes) {
   return bytes;
 }
 
-// Rebuild a pool from pkv_pool_save's bytes.  The snapshot is checked before anything
-// is built: sizes and ids in range, the free stack without repeats, free blocks (and only
-// they) at refcount 0, every table of length ceil(num_tokens / block_size) naming blocks
-// in use, and no block referenced by more tables than its refcount.
-int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out) {
-  if (!out) return PKV_ERR_NULL;
-  *out = nullptr;
-  if (!buf) return PKV_ERR_NULL;
-  if (buf_bytes < 40 || buf_bytes % 8 != 0) return PKV_ERR_ARG;
-  const int64_t n = buf_bytes / 8;
-  std::vector<int64_t> w((size_t)n);
-  std::memcpy(w.data(), buf, (size_t)buf_bytes);
-  int64_t at = 0;
+}  // extern "C"
+
+namespace {
+
+// The body of pkv_pool_load once the header words have been read and the buffer is known
+// to hold the free stack, the refcounts and the sequence count.  May throw
+// std::bad_alloc (caught by the caller); the partly built pool is then freed.
+int pool_load_checked(const std::vector<int64_t> &w, int64_t at, int64_t nb, int64_t bs,
+                      int64_t nfree, pkv_pool **out) {
+  const int64_t n = (int64_t)w.size();
   auto next = [&](int64_t &v) -> bool {
     if (at >= n) return false;
     v = w[(size_t)at++];
     return true;
   };
-  int64_t magic, nb, bs, nfree;
-  if (!next(magic) || magic != kPoolMagic || !next(nb) || !next(bs) || !next(nfree))
-    return PKV_ERR_ARG;
-  if (nb <= 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX || nfree < 0 || nfree > nb)
-    return PKV_ERR_ARG;
-  pkv_pool *p = new (std::nothrow) pkv_pool();
-  if (!p) return PKV_ERR_OOM;
-  auto fail = [&](int code) {
-    delete p;
-    return code;
-  };
+  std::unique_ptr<pkv_pool> p(new pkv_pool());
   p->num_blocks = (int)nb;
   p->block_size = (int)bs;
   std::vector<char> is_free((size_t)nb, 0);
   p->free_stack.reserve((size_t)nfree);
   for (int64_t i = 0; i < nfree; ++i) {
     int64_t b;
-    if (!next(b) || b < 0 || b >= nb || is_free[(size_t)b]) return fail(PKV_ERR_ARG);
+    if (!next(b) || b < 0 || b >= nb || is_free[(size_t)b]) return PKV_ERR_ARG;
     is_free[(size_t)b] = 1;
     p->free_stack.push_back((int32_t)b);
   }
@@ -322,17 +310,19 @@ int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out) {
   for (int64_t b = 0; b < nb; ++b) {
     int64_t r;
     if (!next(r) || r < 0 || r > INT32_MAX || (r == 0) != (is_free[(size_t)b] != 0))
-      return fail(PKV_ERR_ARG);
+      return PKV_ERR_ARG;
     p->refcount[(size_t)b] = (int32_t)r;
   }
   int64_t nseq;
-  if (!next(nseq) || nseq < 0) return fail(PKV_ERR_ARG);
+  if (!next(nseq) || nseq < 0) return PKV_ERR_ARG;
   std::vector<int64_t> uses((size_t)nb, 0);
   for (int64_t i = 0; i < nseq; ++i) {
     int64_t id, ntok, len;
-    if (!next(id) || !next(ntok) || !next(len) || ntok < 0 || len != (ntok + bs - 1) / bs ||
-        len > n - at || p->seqs.count(id))
-      return fail(PKV_ERR_ARG);
+    // No table covers more tokens than the pool holds (this also keeps the length
+    // arithmetic from overflowing).
+    if (!next(id) || !next(ntok) || !next(len) || ntok < 0 || ntok > nb * bs ||
+        len != ntok / bs + (ntok % bs != 0) || len > n - at || p->seqs.count(id))
+      return PKV_ERR_ARG;
     pkv_pool::Seq sq;
     sq.num_tokens = ntok;
     sq.table.reserve((size_t)len);
@@ -340,14 +330,46 @@ int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out) {
       int64_t b;
       if (!next(b) || b < 0 || b >= nb || is_free[(size_t)b] ||
           ++uses[(size_t)b] > p->refcount[(size_t)b])
-        return fail(PKV_ERR_ARG);
+        return PKV_ERR_ARG;
       sq.table.push_back((int32_t)b);
     }
     p->seqs.emplace(id, std::move(sq));
   }
-  if (at != n) return fail(PKV_ERR_ARG);
-  *out = p;
+  if (at != n) return PKV_ERR_ARG;
+  *out = p.release();
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Rebuild a pool from pkv_pool_save's bytes.  The snapshot is checked before anything
+// is built: sizes and ids in range, the buffer long enough for the counts it declares,
+// the free stack without repeats, free blocks (and only they) at refcount 0, every
+// table of length ceil(num_tokens / block_size) naming blocks in use, and no block
+// referenced by more tables than its refcount.  Running out of host memory while
+// building returns PKV_ERR_OOM (no exception crosses the C boundary).
+int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out) {
+  if (!out) return PKV_ERR_NULL;
+  *out = nullptr;
+  if (!buf) return PKV_ERR_NULL;
+  if (buf_bytes < 40 || buf_bytes % 8 != 0) return PKV_ERR_ARG;
+  try {
+    const int64_t n = buf_bytes / 8;
+    std::vector<int64_t> w((size_t)n);
+    std::memcpy(w.data(), buf, (size_t)buf_bytes);
+    const int64_t magic = w[0], nb = w[1], bs = w[2], nfree = w[3];
+    if (magic != kPoolMagic) return PKV_ERR_ARG;
+    if (nb <= 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX || nfree < 0 || nfree > nb)
+      return PKV_ERR_ARG;
+    // The free stack, one refcount per block and the sequence count must all be in the
+    // buffer: checked before any allocation sized by the snapshot's own numbers.
+    if (nfree + nb + 1 > n - 4) return PKV_ERR_ARG;
+    return pool_load_checked(w, 4, nb, bs, nfree, out);
+  } catch (const std::bad_alloc &) {
+    return PKV_ERR_OOM;
+  }
 }
 
 int paged_kv_check_slots(const int64_t *slot_mapping, int num_tokens, int num_blocks,

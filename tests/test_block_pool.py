@@ -237,3 +237,10 @@ def test_snapshot_rejects_inconsistent_bytes():
     x = w.copy(); x[seq_at + 1] = 40; bad(x)      # length does not match the table
     with pytest.raises(PagedKVError):
         BlockPool.load(bytes(snap[:20]))          # shorter than the header
+    # counts the buffer cannot hold are refused before anything is allocated for them
+    bad([w[0], 2**31 - 1, BS, 0, 0])              # INT32_MAX blocks in a 40-byte buffer
+    bad([w[0], 2**31 - 1, BS, 2**31 - 1, 0])      # ... and as many free blocks
+    x = w.copy(); x[3] = 10; bad(x)               # a free stack that runs past the buffer
+    # a token count near INT64_MAX (its block count would overflow) is refused
+    x = w.copy(); x[seq_at + 1] = 2**63 - 1; bad(x)
+    x = w.copy(); x[seq_at + 1] = 10 * BS + 1; bad(x)  # more tokens than the pool holds
