@@ -187,35 +187,32 @@ def pin_ctx_zero(lib):
 # -------------------------------------------------------------------------------------
 # Library routine and brute force
 # -------------------------------------------------------------------------------------
-class ContiguousKVCache:
-    """The contiguous cache of "Inference optimization", Step 1: per layer and head a
-    [max_seq][D] array; update() appends new rows along the sequence axis."""
+class AppendOnlyKV:
+    """A sequence's KV held contiguously, as "Inference optimization" ("KV cache") describes
+    it: each step computes only its new tokens' K/V and appends them along the sequence
+    axis.  Kept here as a list of the appended pieces, each [heads][new tokens][D];
+    `rows()` joins them into the [heads][tokens so far][D] view attention reads."""
 
-    def __init__(self, num_layers, num_heads, head_dim, max_seq_len):
-        self.k = np.zeros((num_layers, num_heads, max_seq_len, head_dim), np.float64)
-        self.v = np.zeros_like(self.k)
-        self.seq_len = 0
+    def __init__(self):
+        self._k, self._v = [], []
 
-    def update(self, layer, new_k, new_v):
-        n = new_k.shape[1]
-        end = self.seq_len + n
-        self.k[layer, :, self.seq_len:end] = new_k
-        self.v[layer, :, self.seq_len:end] = new_v
-        self.seq_len = end
-        return self.k[layer, :, :end], self.v[layer, :, :end]
+    def append(self, new_k, new_v):
+        self._k.append(np.asarray(new_k, np.float64))
+        self._v.append(np.asarray(new_v, np.float64))
+
+    def rows(self):
+        return np.concatenate(self._k, axis=1), np.concatenate(self._v, axis=1)
 
 
 def contiguous_from_paged(k, v, table, ctx, Hkv, D, chunk=7):
     """Feed a sequence's tokens, in logical order and in chunks, through the
     contiguous cache."""
-    cache = ContiguousKVCache(1, Hkv, D, ctx)
-    kk = vv = None
+    cache = AppendOnlyKV()
     for t0 in range(0, ctx, chunk):
         t1 = min(ctx, t0 + chunk)
-        nk = np.stack([gather(k, table, t1, g)[t0:t1] for g in range(Hkv)])
-        nv = np.stack([gather(v, table, t1, g)[t0:t1] for g in range(Hkv)])
-        kk, vv = cache.update(0, nk, nv)
-    return kk, vv
+        cache.append(np.stack([gather(k, table, t1, g)[t0:t1] for g in range(Hkv)]),
+                     np.stack([gather(v, table, t1, g)[t0:t1] for g in range(Hkv)]))
+    return cache.rows()
 
 
 def pin_sdpa_contiguous(lib, cfg=1, ctx_override=None, Hq=None, Hkv=None, seed=16):
@@ -329,8 +326,8 @@ def pin_shared_prefix_equals_private(lib):
 
 
 def pin_write_matches_kvcache_update(lib):
-    """Appending tokens one by one through slots reproduces the contiguous cache's
-    update() sequence when read back through the block table."""
+    """Appending tokens one by one through slots, read back through the block table,
+    gives the same rows as appending them to a contiguous per-sequence KV."""
     Hkv, D, n = 2, 64, 37
     bm = BlockManager(12, BS, free_order=np.random.default_rng(3).permutation(12))
     bm.add_seq(0)
@@ -339,13 +336,14 @@ def pin_write_matches_kvcache_update(lib):
     gen = torch.Generator().manual_seed(4)
     newk = torch.randn(n, Hkv, D, generator=gen).to(torch.bfloat16)
     newv = torch.randn(n, Hkv, D, generator=gen).to(torch.bfloat16)
-    cache = ContiguousKVCache(1, Hkv, D, n)
+    cache = AppendOnlyKV()
     for t in range(n):
         slot, cow = bm.append_slot(0)
         assert cow is None
         oracle.kv_write(k, v, newk[t:t + 1], newv[t:t + 1], [slot], lib=lib)
-        kk, vv = cache.update(0, to_f64(newk[t:t + 1]).transpose(1, 0, 2),
-                              to_f64(newv[t:t + 1]).transpose(1, 0, 2))
+        cache.append(to_f64(newk[t:t + 1]).transpose(1, 0, 2),
+                     to_f64(newv[t:t + 1]).transpose(1, 0, 2))
+    kk, vv = cache.rows()
     table = bm.block_table(0)
     for g in range(Hkv):
         assert np.array_equal(gather(k, table, n, g), kk[g])
