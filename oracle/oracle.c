@@ -136,11 +136,14 @@ static int attend_one(double *out, const uint16_t *q, const uint16_t *k_cache,
         x[t] = exp(x[t] - m);
         denom += x[t];
     }
-    for (int d = 0; d < head_dim; ++d) {
-        double acc = 0.0;
-        for (int t = 0; t < ctx; ++t) acc += x[t] * vc[(size_t)t * head_dim + d];
-        out[d] = acc / denom;
+    /* o[d] = sum_t w_t V[t][d] / sum_t w_t: for every d the terms are added in
+     * increasing t; t is the outer loop so that V is read one row at a time. */
+    for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+    for (int t = 0; t < ctx; ++t) {
+        const double *vt = vc + (size_t)t * head_dim;
+        for (int d = 0; d < head_dim; ++d) out[d] += x[t] * vt[d];
     }
+    for (int d = 0; d < head_dim; ++d) out[d] /= denom;
     return 0;
 }
 
@@ -374,11 +377,13 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                 x[t] = exp(x[t] - m);
                 denom += x[t];
             }
-            for (int d = 0; d < head_dim; ++d) {
-                double acc = 0.0;
-                for (int t = 0; t < ctx; ++t) acc += x[t] * vc[(size_t)t * head_dim + d];
-                o[d] = acc / denom;
+            /* as in attend_one: per d, terms added in increasing t, V read by rows */
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            for (int t = 0; t < ctx; ++t) {
+                const double *vt = vc + (size_t)t * head_dim;
+                for (int d = 0; d < head_dim; ++d) o[d] += x[t] * vt[d];
             }
+            for (int d = 0; d < head_dim; ++d) o[d] /= denom;
         }
 #ifdef _OPENMP
 #pragma omp critical

@@ -23,11 +23,11 @@ MUTANTS = [
      "size_t row = (((size_t)block * block_size + offset) * num_kv_heads + kv_head) * head_dim;"),
     ("v-from-k", "vc[(size_t)t * head_dim + d] = bf16_to_f64(v_cache[row + d]);",
      "vc[(size_t)t * head_dim + d] = bf16_to_f64(k_cache[row + d]);"),
-    ("not-normalised", "out[d] = acc / denom;", "out[d] = acc;"),
+    ("not-normalised", "for (int d = 0; d < head_dim; ++d) out[d] /= denom;", ""),
     ("sign-flipped", "x[t] = exp(x[t] - m);", "x[t] = exp(m - x[t]);"),
     ("base-two", "x[t] = exp(x[t] - m);", "x[t] = exp2(x[t] - m);"),
-    ("last-token-dropped", "for (int t = 0; t < ctx; ++t) acc += x[t]",
-     "for (int t = 0; t + 1 < ctx; ++t) acc += x[t]"),
+    ("last-token-dropped", "const double *vt = vc + (size_t)t * head_dim;",
+     "if (t + 1 == ctx) break;\n const double *vt = vc + (size_t)t * head_dim;"),
     ("q-transposed", "q + ((size_t)s * num_q_heads + h) * head_dim",
      "q + ((size_t)h * num_seqs + s) * head_dim"),
     ("write-layout",
