@@ -2,7 +2,9 @@
 
 One step = copy-on-write block copy (when the workload has pairs) + paged KV write of
 the step's new tokens + paged decode attention (plan, split-K partitions, LSE merge),
-all through the C ABI of libpagedkv.so on one stream.
+all through the C ABI of libpagedkv.so on one stream: by default one paged_decode_step
+call (the copies, the write and the plan share one launch), with --step-api separate
+the three calls paged_block_copy, paged_kv_write and paged_attention_decode.
 
 Prints ONE JSON line.  ``value`` is KV-read GB/s of the whole step (algorithmic bytes:
 every context token's K and V row of every KV head, read once) with inputs resident in
@@ -37,12 +39,33 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_cache_272_gb300 import workloads  # noqa: E402
 
-DEFAULT_CONFIG = 2
+# decode: the long-context mixed batch (the largest single-GPU workload); prefill and
+# serving runs: their workload 2
+DEFAULT_CONFIG = {"decode": 5, "prefill": 2, "serve": 2}
 METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); seq-steps/sec/layer"
 L2_BYTES = 129 * 1024 * 1024
+
+
+class L2Flush:
+    """Empties L2 of the step's data between timed steps: writes a buffer of twice the L2
+    size, then reads a second one of that size, so that L2 holds only clean lines of
+    unrelated data when the step starts (the write alone would leave it full of dirty
+    lines whose write-back would land inside the timed step)."""
+
+    def __init__(self, device):
+        self.w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
 ATTN_SOURCES = ["paged_kv_cache_272_gb300/csrc/attention.cu",
                 "paged_kv_cache_272_gb300/csrc/attention_mma.cu",
                 "paged_kv_cache_272_gb300/csrc/attention.cuh",
+                "paged_kv_cache_272_gb300/csrc/plan.cuh",
+                "paged_kv_cache_272_gb300/csrc/decode_step.cu",
+                "paged_kv_cache_272_gb300/csrc/kv_rows.cuh",
                 "paged_kv_cache_272_gb300/csrc/tc_common.cuh",
                 "paged_kv_cache_272_gb300/csrc/pkv_common.cuh"]
 PREFILL_SOURCES = ["paged_kv_cache_272_gb300/csrc/prefill.cu",
@@ -390,10 +413,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     kv_bytes = workloads.kv_read_bytes(w) // (2 if fp8 else 1)
     max_parts = (mcl + P - 1) // P
-    launches_per_step = (1 if pairs.numel() else 0) + 1 + 2 + (1 if max_parts > 1 else 0)
+    if args.step_api == "fused":  # prologue (copies + write + plan), partition, merge
+        launches_per_step = (1 if pairs.shape[0] > 1024 else 0) + 2 + (1 if max_parts > 1 else 0)
+    else:
+        launches_per_step = (1 if pairs.numel() else 0) + 1 + 2 + (1 if max_parts > 1 else 0)
     working_set = kv_bytes + q.numel() * 2 * 2
     flush = working_set < 2 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    scratch = L2Flush(dev) if flush else None
 
     def do_copy(pr):
         (ops.paged_block_copy_fp8 if fp8 else ops.paged_block_copy)(k, v, pr, err_flag=err,
@@ -421,7 +447,25 @@ def run_ours(args):
             ops.paged_attention_decode(out, qq, k, v, btt, cx, w.scale, mcl, ws, P, err_flag=err,
                                        stream=stream)
 
+    fused = args.step_api == "fused"
+
+    def do_step(qq, btt, cx, kn, vn, sl, pr):
+        """The whole step in one call of the fused entry point."""
+        if fp8:
+            ops.paged_decode_step_fp8(out, qq, k, v, btt, cx, w.scale,
+                                      ks_dev if per_head else FP8_K_SCALE,
+                                      vs_dev if per_head else FP8_V_SCALE, mcl, ws, k_new=kn,
+                                      v_new=vn, slot_mapping=sl, block_pairs=pr,
+                                      partition_size=P, err_flag=err, stream=stream)
+        else:
+            ops.paged_decode_step(out, qq, k, v, btt, cx, w.scale, mcl, ws, k_new=kn, v_new=vn,
+                                  slot_mapping=sl, block_pairs=pr, partition_size=P,
+                                  err_flag=err, stream=stream)
+
     def step():
+        if fused:
+            do_step(q, bt, ctx, k_new, v_new, slots, pairs)
+            return
         if pairs.numel():
             do_copy(pairs)
         do_write(k_new, v_new, slots)
@@ -445,17 +489,24 @@ def run_ours(args):
         nvtx.range_push("timed decode steps")
         for i in range(args.steps):
             if flush:
-                scratch.zero_()
+                scratch()
             e0, e1, e2 = ev[i]
             nvtx.range_push(f"step {i}")
             e0.record(stream)
-            if pairs.numel():
-                do_copy(pairs)
-            do_write(k_new, v_new, slots)
-            e1.record(stream)
-            nvtx.range_push("paged_attention_decode")
-            do_attn(q, bt, ctx)
-            nvtx.range_pop()
+            if fused:
+                # one call: e1 = e0, the "attention" time is the whole step's
+                e1.record(stream)
+                nvtx.range_push("paged_decode_step")
+                do_step(q, bt, ctx, k_new, v_new, slots, pairs)
+                nvtx.range_pop()
+            else:
+                if pairs.numel():
+                    do_copy(pairs)
+                do_write(k_new, v_new, slots)
+                e1.record(stream)
+                nvtx.range_push("paged_attention_decode")
+                do_attn(q, bt, ctx)
+                nvtx.range_pop()
             e2.record(stream)
             nvtx.range_pop()
         nvtx.range_pop()
@@ -494,10 +545,14 @@ def run_ours(args):
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
-        if dv["pairs"].numel():
-            do_copy(dv["pairs"])
-        do_write(dv["k_new"], dv["v_new"], dv["slots"])
-        do_attn(dv["q"], dv["bt"], dv["ctx"])
+        if fused:
+            do_step(dv["q"], dv["bt"], dv["ctx"], dv["k_new"], dv["v_new"], dv["slots"],
+                    dv["pairs"])
+        else:
+            if dv["pairs"].numel():
+                do_copy(dv["pairs"])
+            do_write(dv["k_new"], dv["v_new"], dv["slots"])
+            do_attn(dv["q"], dv["bt"], dv["ctx"])
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -506,7 +561,7 @@ def run_ours(args):
     e2e_ms = 0.0
     for _ in range(args.steps):
         if flush:
-            scratch.zero_()
+            scratch()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
@@ -545,9 +600,12 @@ def run_ours(args):
             "unique_kv_bytes_per_step": workloads.unique_kv_read_bytes(w) // (2 if fp8 else 1),
             "cow_pairs_per_step": int(w.cow_pairs.shape[0]),
             "new_tokens_per_step": int(w.slot_mapping.shape[0]),
-            "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
+            "l2": ("L2 flushed (256 MB write, then 256 MB read) before every timed step"
+                   if flush else
                    "inputs larger than L2 (KV read per step >> 129 MB)"),
             "attention_variant": args.variant, "attention_kernel": vname,
+            "step_api": ("paged_decode_step (one call)" if fused else
+                         "paged_block_copy + paged_kv_write + paged_attention_decode"),
             "parallelism": "replicas" if world > 1 else "single"},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "seq_steps_per_s_per_layer": world * S / (ms_per_step / 1e3),
@@ -558,8 +616,12 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      # captured on the default draw of each workload only
-                     "traffic": recorded_traffic(w.name, vname) if args.seed is None else None,
-                     "kernel": "paged_attention_decode: plan + partition (%s) + merge kernels"
+                     "traffic": (recorded_traffic(w.name, vname + ("-step" if fused else ""))
+                                 if args.seed is None else None),
+                     "kernel": ("paged_decode_step: prologue (copies + write + plan) + "
+                                "partition (%s) + merge kernels, timed over the whole step"
+                                if fused else
+                                "paged_attention_decode: plan + partition (%s) + merge kernels")
                                % vname,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clk.summary(),
@@ -694,7 +756,7 @@ def run_prefill(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
-          "tc": ops.PKV_PREFILL_TC}[args.prefill_kernel]
+          "tc": ops.PKV_PREFILL_TC, "tc128": ops.PKV_PREFILL_TC128}[args.prefill_kernel]
     ops.set_prefill_variant(pk)
     w = workloads.make_prefill_config(args.config, device="cuda", seed=args.seed)
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -713,7 +775,7 @@ def run_prefill(args):
     kv_bytes = int(w.context_lens.astype(np.int64).sum()) * 2 * Hkv * D * 2
     working_set = kv_bytes + 2 * q.numel() * 2
     flush = working_set < 2 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    scratch = L2Flush(dev) if flush else None
 
     def do_write(kn, vn, sl):
         ops.paged_kv_write(kn, vn, sl, k, v, err_flag=err, stream=stream)
@@ -743,7 +805,7 @@ def run_prefill(args):
         nvtx.range_push("timed prefill steps")
         for i in range(args.steps):
             if flush:
-                scratch.zero_()
+                scratch()
             e0, e1, e2 = ev[i]
             nvtx.range_push(f"step {i}")
             e0.record(stream)
@@ -786,7 +848,7 @@ def run_prefill(args):
     e2e_ms = 0.0
     for _ in range(args.steps):
         if flush:
-            scratch.zero_()
+            scratch()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
@@ -803,7 +865,8 @@ def run_prefill(args):
     achieved = flops / (attn_ms / 1e3) / 1e12
     # AUTO runs the tcgen05 kernel for head_dim 128 and the mma.sync kernel for 64
     tc = pk == ops.PKV_PREFILL_TC or (pk == ops.PKV_PREFILL_AUTO and D == 128)
-    kname = "prefill-tc" if tc else "prefill-mma"
+    kname = ("prefill-tc128" if pk == ops.PKV_PREFILL_TC128 and D == 128 else
+             "prefill-tc" if tc else "prefill-mma")
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
@@ -817,7 +880,8 @@ def run_prefill(args):
             "mean_context": float(w.context_lens.mean()), "max_context": w.max_context_len,
             "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
             "prefill_kernel": kname,
-            "l2": ("L2 flushed (256 MB write) before every timed step" if flush else
+            "l2": ("L2 flushed (256 MB write, then 256 MB read) before every timed step"
+                   if flush else
                    "working set (KV + q + out) larger than twice L2"),
             "parallelism": "replicas" if world > 1 else "single"},
         "pct_of_bf16_peak": 100.0 * value / peak,
@@ -1108,7 +1172,8 @@ def main():
                     help="decode step (default), chunked-prefill step, or a whole "
                          "continuous-batching serving run")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
-                    help="workload number (decode 1..5, default 2; prefill 1..3, default 2)")
+                    help="workload number (decode 1..5, default 5; prefill 1..3, default 2; "
+                         "serve 1..2, default 2)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition", type=int, default=0,
@@ -1121,13 +1186,16 @@ def main():
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
                     help="with --kv-dtype fp8: one E4M3 scale per cache, or one per KV head")
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc"],
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc", "tc128"],
                     help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc "
                          "for head_dim 128")
+    ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
+                    help="decode step through paged_decode_step (one call, default) or the "
+                         "three separate calls (copy, write, attention)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.config is None:
-        args.config = DEFAULT_CONFIG
+        args.config = DEFAULT_CONFIG[args.path]
     if args.path == "serve":
         if args.config not in SERVE_CONFIGS:
             ap.error("--path serve takes --config 1..2")

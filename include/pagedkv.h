@@ -69,8 +69,9 @@ extern "C" {
 
 /* Library ABI version: PKV_ABI_VERSION of the build (incremented when an entry point is
  * added or a signature changes).  2 added paged_kv_write_fp8_per_head,
- * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load. */
-#define PKV_ABI_VERSION 2
+ * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load; 3 added
+ * paged_decode_step and paged_decode_step_fp8. */
+#define PKV_ABI_VERSION 3
 int paged_kv_version(void);
 
 /* Human-readable text of a PKV_ERR_* code. Never NULL; static storage. */
@@ -142,6 +143,32 @@ int paged_attention_decode(uint16_t *out, const uint16_t *q, const uint16_t *k_c
                            void *workspace, size_t workspace_bytes, int32_t *err_flag,
                            void *stream);
 
+/*
+ * paged_decode_step -- one whole decode step of one layer: copy-on-write, the paged write
+ * of the step's new tokens, then decode attention.  The result is exactly that of
+ *   paged_block_copy(k_cache, v_cache, block_pairs, num_pairs, ...);
+ *   paged_kv_write(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, ...);
+ *   paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, ...);
+ * (every copy before every write, every write before attention), in three launches
+ * instead of five: the copies, the writes and the attention plan share the first.
+ * Arguments, layouts, ownership and errors are those of the three calls; num_tokens or
+ * num_pairs may be 0 (their pointers may then be NULL).  The pair rules of
+ * paged_block_copy apply (distinct dsts, no dst that is also a src); a new token may
+ * write into a pair's src or dst block (it lands after the copy).  With num_seqs == 0
+ * only the copies and the write run.
+ * Source: as the three calls ("Continuous batching and PagedAttention", section 3;
+ * "Inference optimization", section "KV cache"; "System-level optimization", sections
+ * 3.1 and 3.3).
+ */
+int paged_decode_step(uint16_t *out, const uint16_t *q, uint16_t *k_cache, uint16_t *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                      int max_blocks_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, float scale, int partition_size,
+                      int max_context_len, const uint16_t *k_new, const uint16_t *v_new,
+                      const int64_t *slot_mapping, int num_tokens, const int32_t *block_pairs,
+                      int num_pairs, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                      void *stream);
+
 /* ------------------------------------------------------------------------------------
  * E4M3 (FP8) KV cache.  "Continuous batching and PagedAttention", section 4: the
  * kv_cache_dtype="fp8" option doubles the batch a GPU holds; "Inference optimization",
@@ -212,6 +239,23 @@ int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const 
                                         int max_context_len, void *workspace,
                                         size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/* paged_decode_step over E4M3 caches: paged_block_copy_fp8, then the quantising write,
+ * then E4M3 decode attention, as one call (see paged_decode_step).  Scales: k_scales and
+ * v_scales both non-NULL selects one scale per KV head (the _per_head calls' semantics;
+ * k_scale and v_scale are then ignored), both NULL one scale per cache (k_scale, v_scale
+ * > 0, else PKV_ERR_SHAPE); one NULL and one not returns PKV_ERR_NULL.  head_dim must be
+ * 128. */
+int paged_decode_step_fp8(uint16_t *out, const uint16_t *q, uint8_t *k_cache, uint8_t *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                          int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, float scale,
+                          float k_scale, float v_scale, const float *k_scales,
+                          const float *v_scales, int partition_size, int max_context_len,
+                          const uint16_t *k_new, const uint16_t *v_new,
+                          const int64_t *slot_mapping, int num_tokens,
+                          const int32_t *block_pairs, int num_pairs, void *workspace,
+                          size_t workspace_bytes, int32_t *err_flag, void *stream);
+
 /*
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that cannot
  * allocate device memory (no cudaMalloc on their thread, memory owned by another
@@ -224,9 +268,11 @@ int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const 
  * enqueue nothing.  The call allocates nothing (no cudaMalloc/cudaFree or allocating
  * library routine).  Its first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call before any
- * stream capture.  All calls on one device share the array: calls whose kernels
- * overlap on the GPU (other streams, other threads) race, so order them on one
- * stream.  The array keeps the last call's contents; nothing in it needs clearing.
+ * stream capture.  The stream must belong to the current device (the array is chosen
+ * by the current device): a stream of another device returns PKV_ERR_ARG.  All calls on
+ * one device share the array: calls whose kernels overlap on the GPU (other streams,
+ * other threads) race, so order them on one stream.  The array keeps the last call's
+ * contents; nothing in it needs clearing.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 int paged_attention_decode_noalloc(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
@@ -276,6 +322,7 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 #define PKV_PREFILL_AUTO 0
 #define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
 #define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
+#define PKV_PREFILL_TC128 3 /* tcgen05, 128-key tiles, Q in TMEM, one CTA per SM       */
 int paged_attention_prefill_set_variant(int variant);
 
 /*
@@ -340,7 +387,13 @@ int pkv_pool_export(const pkv_pool *pool, const int64_t *seqs, int n, int max_bl
  * pkv_pool_load: a new pool (release it with pkv_pool_destroy) in the saved state; the
  * next calls on it behave exactly as on the saved pool.  PKV_ERR_ARG, and *out = NULL,
  * for bytes that are not a consistent snapshot (wrong size or magic, ids out of range,
- * a repeated free block, a free block in a table, a refcount below its table uses). */
+ * counts the buffer is too short to hold, a repeated free block, a free block in a
+ * table, a table longer than the pool or not matching its token count, a refcount below
+ * its table uses); PKV_ERR_OOM if host memory runs out while building.
+ * References held outside sequence tables (pkv_block_retain, the prefix cache) are
+ * saved as counts only: the snapshot does not record who holds them, so after a load
+ * each such holder must be re-registered (a prefix cache rebuilt over the loaded pool)
+ * or its references released with pkv_block_release, else those blocks stay allocated. */
 int64_t pkv_pool_save(const pkv_pool *pool, void *buf, int64_t buf_bytes);
 int pkv_pool_load(const void *buf, int64_t buf_bytes, pkv_pool **out);
 

@@ -21,6 +21,8 @@
 #include <atomic>
 
 #include "attention.cuh"
+#include "merge.cuh"
+#include "plan.cuh"
 
 namespace pkv {
 namespace {
@@ -28,87 +30,12 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------------------------------
-// Plan (one CTA): validate context lengths, count partitions, zero the output of
-// sequences with no tokens (a bad length is flagged and treated as empty), and list
-//  * the partitions as records ordered by block count, largest first (a counting sort
-//    over 1..32 blocks; order within one size is arbitrary and does not affect
-//    results), and
-//  * the merge units of sequences with several partitions: (sequence, group of 8
-//    query heads, chunk of kChunk partitions), units of multi-chunk sequences first.
+// Plan (one CTA of 1024 threads): see attn_plan_cta.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) attn_plan_kernel(const AttnArgs a, int head_dim) {
-  constexpr int kBins = 33;
-  __shared__ int hist[kBins];
-  __shared__ int cursor[kBins];
-  __shared__ int ucount[2], ucursor[2];  // merge units: [0] multi-chunk, [1] one chunk
   pdl_trigger();
   pdl_wait();
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x < 2) ucount[threadIdx.x] = 0;
-  __syncthreads();
-  const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
-  const int P = a.part_tokens;
-  const int G8 = (a.num_q_heads + 7) / 8;
-  int first_c = 0;  // this thread's first sequence's (validated) length, kept for pass 2
-  for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
-    int c = a.context_lens[s];
-    if (c < 0 || c > cap) {
-      flag_error(a.err, PKV_DEV_BAD_CONTEXT);
-      c = 0;
-    }
-    if (s == threadIdx.x) first_c = c;
-    const int n = (c + P - 1) / P;
-    a.nparts[s] = n;
-    if (n == 0) {  // no partition will write this sequence's output
-      uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * head_dim);
-      for (int i = 0; i < a.num_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-    }
-    if (n > 1) {
-      const int nch = (n + kChunk - 1) / kChunk;
-      atomicAdd(&ucount[nch > 1 ? 0 : 1], nch * G8);
-      if (nch > 1)  // arrival counters of the second merge level, one per head
-        for (int h = 0; h < a.num_q_heads; ++h) a.cnt_seq[(size_t)s * a.num_q_heads + h] = 0;
-    }
-    // n - 1 (or n) partitions of P tokens and at most one shorter tail.
-    const int nfull = c / P, tail = c - nfull * P;
-    if (nfull) atomicAdd(&hist[min(P / kBlockSize, 32)], nfull);
-    if (tail) atomicAdd(&hist[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int b = 32; b >= 1; --b) {
-      cursor[b] = run;
-      run += hist[b];
-    }
-    *a.num_items = run;
-    *a.work_next = 0;
-    ucursor[0] = 0;
-    ucursor[1] = ucount[0];
-    *a.num_units = ucount[0] + ucount[1];
-  }
-  __syncthreads();
-  for (int s = threadIdx.x; s < a.num_seqs; s += blockDim.x) {
-    // validated in pass 1 (a length is re-read only past the first 1024 sequences)
-    const int c = s == threadIdx.x ? first_c : (a.nparts[s] ? a.context_lens[s] : 0);
-    const int n = (c + P - 1) / P;
-    if (n == 0) continue;
-    const int nfull = c / P, tail = c - nfull * P;
-    if (nfull) {
-      int pos = atomicAdd(&cursor[min(P / kBlockSize, 32)], nfull);
-      for (int p = 0; p < nfull; ++p) a.items[pos++] = make_int4(s, p * P, (p + 1) * P, n);
-    }
-    if (tail) {
-      const int pos = atomicAdd(&cursor[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
-      a.items[pos] = make_int4(s, nfull * P, c, n);
-    }
-    if (n > 1) {
-      const int nch = (n + kChunk - 1) / kChunk;
-      int pos = atomicAdd(&ucursor[nch > 1 ? 0 : 1], nch * G8);
-      for (int ch = 0; ch < nch; ++ch)
-        for (int g = 0; g < G8; ++g) a.units[pos++] = make_int4(s, g, ch, n);
-    }
-  }
+  attn_plan_cta(a, head_dim);
 }
 
 // ------------------------------------------------------------------------------------
@@ -138,6 +65,7 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
   const int total = *a.num_items * per_pair;
   // K/V rows are read once: evict them first, so partials and queries stay in L2
   const uint64_t pol = l2_evict_first_policy();
+  const uint64_t keep = l2_evict_last_policy();
 
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const int pair = w / per_pair;
@@ -292,10 +220,10 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
       const int h = h0 + j;
       if (single) {
         a.out[((size_t)s * a.num_q_heads + h) * D + d] = f32_to_bf16(O / L);
-      } else {
+      } else {  // partials stay in L2 for the merge kernel (evict-last)
         const size_t idx = ((size_t)s * a.max_parts + p) * a.num_q_heads + h;
-        a.part_o[idx * D + d] = O / L;
-        if (d == 0) a.part_lse[idx] = M + log2f(L);
+        st_f32_hint(a.part_o + idx * D + d, O / L, keep);
+        if (d == 0) st_f32_hint(a.part_lse + idx, M + log2f(L), keep);
       }
     }
     __syncthreads();
@@ -303,120 +231,18 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
 }
 
 // ------------------------------------------------------------------------------------
-// Merge of the partitions (log-sum-exp weights):
-//   M = max_k lse_k,  o = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M).
-// A warp merges n entries of one query head: their lse values are read 32 at a time
-// (one per lane), their outputs eight at a time with all loads issued before use, and
-// the running sum is rescaled when the maximum grows.  Reads bypass L1 (the second
-// level reads results other CTAs of the same launch wrote).
+// Merge kernel: persistent and warp-granular, a work item is (merge unit, one of its 8
+// query heads), so the warps of a CTA never wait for one another (see merge_item).
 // ------------------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void warp_merge(const float *lse, const float *o, size_t stride, int n,
-                                           int lane, float &m, float &L, float (&acc)[D / 32]) {
-  constexpr int PER = D / 32;
-  m = -INFINITY;
-  L = 0.f;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  // Eight outputs at a time, every load of a batch issued before any use.
-  auto load8 = [&](int first, int cnt, float (&v)[8][PER]) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (first + u < cnt) {
-        const float *src = o + (size_t)(first + u) * stride * D + lane * PER;
-        if constexpr (PER == 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-          v[u][0] = t.x, v[u][1] = t.y, v[u][2] = t.z, v[u][3] = t.w;
-        } else {
-          const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-          v[u][0] = t.x, v[u][1] = t.y;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
-      }
-    }
-  };
-  for (int k0 = 0; k0 < n; k0 += 32) {
-    const int cnt = min(32, n - k0);
-    const float x = lane < cnt ? __ldcg(lse + (size_t)(k0 + lane) * stride) : -INFINITY;
-    // The first eight outputs do not depend on the weights: load them together with the
-    // lse values (one round trip for sequences with at most eight partitions).
-    float v[8][PER];
-    load8(k0, k0 + cnt, v);
-    float mb = x;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
-    const float mn = fmaxf(m, mb);
-    const float sc = exp2f(m - mn);
-    m = mn;
-    const float w = exp2f(x - mn);  // this lane's entry weight (0 past the end)
-    float ws = w;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(kFull, ws, off);
-    L = fmaf(L, sc, ws);
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] *= sc;
-    for (int k = 0; k < cnt; k += 8) {
-      if (k > 0) load8(k0 + k, k0 + cnt, v);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float c = k + u < cnt ? __shfl_sync(kFull, w, (k + u) & 31) : 0.f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = fmaf(c, v[u][e], acc[e]);
-      }
-    }
-  }
-}
-
-// Persistent and warp-granular: a work item is (merge unit, one of its 8 query heads), so
-// the warps of a CTA never wait for one another.  A sequence with one chunk is finished
-// by its items; one with several leaves a result per chunk and head, and the warp that
-// completes the last chunk of a head (an arrival counter per sequence and head) merges
-// that head's chunk results.
-template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
-  constexpr int PER = D / 32;
   const int lane = threadIdx.x & 31;
   const int warps = (int)(gridDim.x * (blockDim.x >> 5));
   pdl_trigger();
   pdl_wait();
   const int nitems = *a.num_units * 8;
-  for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nitems; it += warps) {
-    const int4 un = a.units[it >> 3];
-    const int s = un.x, g8 = un.y, ch = un.z, np = un.w;
-    const int h = g8 * 8 + (it & 7);
-    if (h >= a.num_q_heads) continue;
-    const int nch = (np + kChunk - 1) / kChunk;
-    const int p0 = ch * kChunk, n = min(kChunk, np - p0);
-    float m, L, acc[PER];
-    const size_t row = ((size_t)s * a.max_parts + p0) * a.num_q_heads + h;
-    warp_merge<D>(a.part_lse + row, a.part_o + row * D, a.num_q_heads, n, lane, m, L, acc);
-    float inv = 1.f / L;
-    if (nch == 1) {
-      uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
-      continue;
-    }
-    const size_t crow = ((size_t)s * a.max_chunks + ch) * a.num_q_heads + h;
-    float *co = a.chunk_o + crow * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) co[e] = acc[e] * inv;
-    if (lane == 0) a.chunk_lse[crow] = m + log2f(L);
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&a.cnt_seq[(size_t)s * a.num_q_heads + h], 1) == nch - 1;
-    if (!__shfl_sync(kFull, last, 0)) continue;
-    __threadfence();
-    const size_t row2 = (size_t)s * a.max_chunks * a.num_q_heads + h;
-    warp_merge<D>(a.chunk_lse + row2, a.chunk_o + row2 * D, a.num_q_heads, nch, lane, m, L, acc);
-    inv = 1.f / L;
-    uint16_t *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] = f32_to_bf16(acc[e] * inv);
-  }
+  for (int it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nitems; it += warps)
+    merge_item<D>(a, it, lane);
 }
 
 template <typename K>
@@ -461,8 +287,6 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
   AttnWorkspace w;
   size_t off = 0;
   const size_t S = (size_t)num_seqs, P = (size_t)max_parts, H = (size_t)num_q_heads;
-  w.nparts_off = off;
-  off = align256(off + S * sizeof(int32_t));
   w.num_items_off = off;
   off = align256(off + sizeof(int32_t));
   w.work_next_off = off;
@@ -518,14 +342,16 @@ int max_parts_for(int max_context_len, int part) {
 }
 }  // namespace
 
-static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
-                       const void *v_cache, const int32_t *block_tables,
-                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
-                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                       int num_blocks, float scale, int partition_size, int max_context_len,
-                       void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
-                       bool kv8, float k_scale, float v_scale, const float *k_scales = nullptr,
-                       const float *v_scales = nullptr) {
+namespace pkv {
+
+int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *k_cache,
+                   const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                   int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int num_blocks, float scale, int partition_size,
+                   int max_context_len, void *workspace, size_t workspace_bytes,
+                   int32_t *err_flag, bool kv8, float k_scale, float v_scale,
+                   const float *k_scales, const float *v_scales) {
+  d->empty = true;
   if (block_size != kBlockSize) return PKV_ERR_BLOCK_SIZE;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_context_len < 0 || num_q_heads % num_kv_heads != 0 ||
@@ -545,7 +371,7 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_ALIGN;
 
   char *wb = static_cast<char *>(workspace);
-  AttnArgs a;
+  AttnArgs &a = d->a;
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -565,7 +391,6 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
   a.kv8 = kv8 ? 1 : 0;
   a.k_scales = kv8 ? k_scales : nullptr;
   a.v_scales = kv8 ? v_scales : nullptr;
-  a.nparts = reinterpret_cast<int32_t *>(wb + ws.nparts_off);
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
   a.work_next = reinterpret_cast<int32_t *>(wb + ws.work_next_off);
   a.items = reinterpret_cast<int4 *>(wb + ws.items_off);
@@ -579,7 +404,6 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
   a.chunk_o = reinterpret_cast<float *>(wb + ws.chunk_o_off);
   a.err = err_flag;
 
-  cudaStream_t st = (cudaStream_t)stream;
   const int variant = g_variant.load();
   // AUTO: the tensor-core variant once a KV head serves 4 or more query heads (the
   // CUDA-core dot products then cost more issue slots than the bytes they consume);
@@ -591,16 +415,46 @@ static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
   if (kv8 && !tma_ok) return PKV_ERR_SHAPE;
   const int width = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
   a.sub_groups = use_mma ? (a.group + 7) / 8 : (a.group + width - 1) / width;
+  d->head_dim = head_dim;
+  d->use_mma = use_mma;
+  d->width = width;
+  d->empty = false;
+  return PKV_OK;
+}
 
-  if (launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, a, head_dim) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  const int rc = use_mma ? launch_attn_mma(a, head_dim, st) : launch_attn_fma(a, head_dim, width, st);
+int decode_launch_after_plan(const DecodeCall &d, cudaStream_t st) {
+  const AttnArgs &a = d.a;
+  const int rc = d.use_mma ? launch_attn_mma(a, d.head_dim, st)
+                           : launch_attn_fma(a, d.head_dim, d.width, st);
   if (rc != 0) return PKV_ERR_CUDA;
-  if (max_parts > 1) {
-    const int64_t units = (int64_t)num_seqs * ((num_q_heads + 7) / 8) * a.max_chunks;
-    if (launch_merge(a, head_dim, units, st) != 0) return PKV_ERR_CUDA;
+  if (a.max_parts > 1) {
+    const int64_t units = (int64_t)a.num_seqs * ((a.num_q_heads + 7) / 8) * a.max_chunks;
+    if (launch_merge(a, d.head_dim, units, st) != 0) return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+}  // namespace pkv
+
+static int decode_impl(uint16_t *out, const uint16_t *q, const void *k_cache,
+                       const void *v_cache, const int32_t *block_tables,
+                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, float scale, int partition_size, int max_context_len,
+                       void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
+                       bool kv8, float k_scale, float v_scale, const float *k_scales = nullptr,
+                       const float *v_scales = nullptr) {
+  DecodeCall d;
+  const int rc = decode_prepare(&d, out, q, k_cache, v_cache, block_tables, context_lens,
+                                num_seqs, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                                block_size, num_blocks, scale, partition_size, max_context_len,
+                                workspace, workspace_bytes, err_flag, kv8, k_scale, v_scale,
+                                k_scales, v_scales);
+  if (rc != PKV_OK || d.empty) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, d.a, head_dim) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return decode_launch_after_plan(d, st);
 }
 
 extern "C" {
@@ -642,7 +496,7 @@ int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *
                                float k_scale, float v_scale, int partition_size,
                                int max_context_len, void *workspace, size_t workspace_bytes,
                                int32_t *err_flag, void *stream) {
-  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (head_dim != 128 && head_dim != 64) return PKV_ERR_SHAPE;
   if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PKV_ERR_SHAPE;
   return decode_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                      max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -659,7 +513,7 @@ int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const 
                                         const float *v_scales, int partition_size,
                                         int max_context_len, void *workspace,
                                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
-  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (head_dim != 128 && head_dim != 64) return PKV_ERR_SHAPE;
   if (num_seqs > 0 && (!k_scales || !v_scales)) return PKV_ERR_NULL;
   // scale_log2 = scale * log2(e) here; the kernel multiplies in each KV head's k_scale.
   return decode_impl(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
@@ -716,6 +570,13 @@ extern "C" int paged_attention_decode_noalloc(
   const size_t need = paged_attention_workspace_size(num_seqs, num_q_heads, head_dim,
                                                      max_context_len, partition_size);
   if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  // The array is chosen by the current device; a stream of another device would get
+  // that device's kernels pointed at this device's array.
+  int cur = -1, sdev = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess ||
+      cudaStreamGetDevice((cudaStream_t)stream, &sdev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (sdev != cur) return PKV_ERR_ARG;
   void *scratch = nullptr;
   const int rc = noalloc_scratch(&scratch);
   if (rc != PKV_OK) return rc;

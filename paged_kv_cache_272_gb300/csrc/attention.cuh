@@ -34,7 +34,6 @@ struct AttnArgs {
   const float *k_scales;         // [Hkv] per-KV-head E4M3 scales, or null (per cache:
   const float *v_scales;         //   scale_log2 and v_scale already hold them)
   // workspace
-  int32_t *nparts;               // [S] partitions per sequence (0: empty or invalid)
   int32_t *num_items;            // [1]
   int32_t *work_next;            // [1] next record to claim (tensor-core kernel)
   int4 *items;                   // [S * max_parts] records {s, t0, t1, np}
@@ -50,7 +49,7 @@ struct AttnArgs {
 
 // Workspace carving (256-byte aligned sections).
 struct AttnWorkspace {
-  size_t nparts_off, num_items_off, work_next_off, items_off, lse_off, o_off, units_off, num_units_off,
+  size_t num_items_off, work_next_off, items_off, lse_off, o_off, units_off, num_units_off,
       cnt_seq_off, chunk_lse_off, chunk_o_off, total;
 };
 AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
@@ -58,5 +57,28 @@ AttnWorkspace attn_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
 // Launchers (return a cudaError_t value).
 int launch_attn_fma(const AttnArgs &a, int head_dim, int width, cudaStream_t st);
 int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st);
+
+// One decode-attention call, validated and laid out over its workspace.
+struct DecodeCall {
+  AttnArgs a;
+  int head_dim;
+  bool use_mma;  // tensor-core partition kernel (else the CUDA-core one)
+  int width;     // query rows per item of the CUDA-core kernel
+  bool empty;    // nothing to launch (no sequences)
+};
+
+// Checks the arguments of a decode-attention call and fills *d.  Returns PKV_OK or the
+// PKV_ERR_* code the entry points return; nothing is enqueued.
+int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *k_cache,
+                   const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                   int num_seqs, int max_blocks_per_seq, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int num_blocks, float scale, int partition_size,
+                   int max_context_len, void *workspace, size_t workspace_bytes,
+                   int32_t *err_flag, bool kv8, float k_scale, float v_scale,
+                   const float *k_scales, const float *v_scales);
+
+// Enqueues the partition kernel and the merge of a prepared call; the call's plan
+// (attn_plan_cta) must already be enqueued on `st`.  Returns PKV_OK or PKV_ERR_CUDA.
+int decode_launch_after_plan(const DecodeCall &d, cudaStream_t st);
 
 }  // namespace pkv

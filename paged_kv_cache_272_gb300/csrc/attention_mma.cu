@@ -368,12 +368,19 @@ __global__ void __launch_bounds__((NW + 1) * 32,
     }
   };
   const int gid = lane >> 2, tig = lane & 3;
+  const uint64_t keep = l2_evict_last_policy();  // for the split-K partials
   int cslot = 0, cphase = 0;  // ring slot and phase of this warp's next block
   // Per-thread shared-memory offsets inside a stage (the swizzle folded in once; a k-step
   // then only flips the 16-byte chunk bits 4..6, which a stage base never sets).
   const int tokA8 = 4 * (gid >> 1) + (gid & 1), tokB8 = tokA8 + 2;  // E4M3 token order
-  const uint32_t koffA = KV8 ? (uint32_t)(tokA8 * 128 + ((tokA8 & 7) << 4) + 4 * tig) : 0u;
-  const uint32_t koffB = KV8 ? (uint32_t)(tokB8 * 128 + ((tokB8 & 7) << 4) + 4 * tig) : 0u;
+  // E4M3 K rows are D bytes: head_dim 128 with the 128-byte swizzle (16-byte chunk ^= row
+  // & 7), head_dim 64 with the 64-byte swizzle (chunk ^= (row >> 1) & 3).
+  auto koff8 = [&](int tok) -> uint32_t {
+    return D == 128 ? (uint32_t)(tok * 128 + ((tok & 7) << 4) + 4 * tig)
+                    : (uint32_t)(tok * 64 + (((tok >> 1) & 3) << 4) + 4 * tig);
+  };
+  const uint32_t koffA = KV8 ? koff8(tokA8) : 0u;
+  const uint32_t koffB = KV8 ? koff8(tokB8) : 0u;
   const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row (bf16 K tile)
   const uint32_t koff16 = (uint32_t)(lrow * 128 + ((((lane >> 4) & 1) ^ (lrow & 7)) << 4));
   if (threadIdx.x == 0) fetch(0);
@@ -685,20 +692,21 @@ __global__ void __launch_bounds__((NW + 1) * 32,
             oa[D + 8] = f32_to_bf16(o[3] * f1);
           }
         } else {
+          // partials stay in L2 for the merge kernel (evict-last)
           float *oa = a.part_o + rowA * D + d0;
           if (hA < gcnt) {
-            oa[0] = o[0] * f0;
-            oa[8] = o[2] * f0;
+            st_f32_hint(oa, o[0] * f0, keep);
+            st_f32_hint(oa + 8, o[2] * f0, keep);
           }
           if (hB < gcnt) {
-            oa[D] = o[1] * f1;
-            oa[D + 8] = o[3] * f1;
+            st_f32_hint(oa + D, o[1] * f1, keep);
+            st_f32_hint(oa + D + 8, o[3] * f1, keep);
           }
         }
       }
       if (!single && warp == 0 && gid == 0) {
-        if (hA < gcnt) a.part_lse[rowA] = M0 + log2f(L0);
-        if (hB < gcnt) a.part_lse[rowA + 1] = M1 + log2f(L1);
+        if (hA < gcnt) st_f32_hint(a.part_lse + rowA, M0 + log2f(L0), keep);
+        if (hB < gcnt) st_f32_hint(a.part_lse + rowA + 1, M1 + log2f(L1), keep);
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
@@ -736,18 +744,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The cache viewed as a 2-D tensor [num_blocks * Hkv * 16 rows][head_dim], boxes of
-// 16 rows x 64 columns (128 bytes) with the 128-byte swizzle.
-// elem = 2 (bf16) or 1 (E4M3 codes): boxes of 16 rows x 128 bytes either way.
+// 16 rows x 128 bytes (64 bf16 columns or 128 E4M3 codes) with the 128-byte swizzle;
+// rows of only 64 bytes (E4M3, head_dim 64) are one box of 16 x 64 bytes with the
+// 64-byte swizzle.  elem = 2 (bf16) or 1 (E4M3 codes).
 bool encode_kv_map(CUtensorMap *m, const void *base, uint64_t rows, int D, int elem) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const bool narrow = D * elem < 128;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * elem};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)kBlockSize};
+  cuuint32_t box[2] = {(cuuint32_t)(narrow ? D : 128 / elem), (cuuint32_t)kBlockSize};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-            const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -862,6 +872,7 @@ int launch_attn_mma(const AttnArgs &a, int head_dim, cudaStream_t st) {
       !kv_tensor_map(&tv, a.v_cache, rows, head_dim, elem))
     return (int)cudaErrorInvalidValue;
   if (a.kv8) {
+    if (head_dim == 64) return launch_mma_t<64, 4, 4, true>(a, tk, tv, st);
     if (head_dim != 128) return (int)cudaErrorInvalidValue;
     return launch_mma_ring<true>(a, tk, tv, st);
   }

@@ -4,10 +4,9 @@
 // bit-exact by construction.  Sources: "Inference optimization", section "KV cache"
 // (append only the new token's K/V) and "Continuous batching and PagedAttention",
 // section 3 (copy-on-write of a shared block when a request diverges).
-#include <cuda_fp8.h>
-
 #include <cstring>
 
+#include "kv_rows.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -35,26 +34,12 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__
       flag_error(err, PKV_DEV_BAD_SLOT);
       continue;
     }
-    const int64_t block = slot >> 4, offset = slot & 15;
-    const int64_t dst = ((block * heads + h) * kBlockSize + offset) * row_vecs + e;
-    k_cache[dst] = k_new[i];
-    v_cache[dst] = v_new[i];
+    put_row_vec_bf16(k_new, v_new, i, slot, h, e, heads, row_vecs, k_cache, v_cache);
   }
 }
 
-// E4M3 write: thread i handles 8 consecutive elements of one (token, KV head) row:
-// code = E4M3(x / scale) with the division rounded to nearest in fp32, then the
-// hardware conversion (round to nearest even, finite saturation).
-__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float scale) {
-  const float2 lo = make_float2(__fdiv_rn(bf16_lo(w0), scale), __fdiv_rn(bf16_hi(w0), scale));
-  const float2 hi = make_float2(__fdiv_rn(bf16_lo(w1), scale), __fdiv_rn(bf16_hi(w1), scale));
-  const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-  return (a & 0xffffu) | (b << 16);
-}
-
-// V codes are stored transposed within a block, [block][head][d][offset], so each of the
-// row's 8 V codes is a separate byte store.
+// E4M3 write: thread i handles 8 consecutive elements of one (token, KV head) row (see
+// put_row_vec_e4m3).
 __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
                                     const uint4 *__restrict__ v_new,
                                     const int64_t *__restrict__ slots, int64_t total, int row_vecs,
@@ -76,26 +61,8 @@ __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
       flag_error(err, PKV_DEV_BAD_SLOT);
       continue;
     }
-    float ks = k_scale, vs = v_scale;
-    if (k_scales != nullptr) {  // one scale per KV head
-      ks = __ldg(k_scales + h);
-      vs = __ldg(v_scales + h);
-      if (!(ks > 0.f) || !(vs > 0.f)) {
-        flag_error(err, PKV_DEV_BAD_SCALE);
-        continue;
-      }
-    }
-    const int64_t dst = (((slot >> 4) * heads + h) * kBlockSize + (slot & 15)) * row_vecs + e;
-    const uint4 kv = k_new[i], vv = v_new[i];
-    k_cache[dst] = make_uint2(quant4(kv.x, kv.y, ks), quant4(kv.z, kv.w, ks));
-    const uint32_t v0 = quant4(vv.x, vv.y, vs), v1 = quant4(vv.z, vv.w, vs);
-    const int D = row_vecs * 8;
-    uint8_t *vcol = v_cache + (((slot >> 4) * heads + h) * D + e * 8) * kBlockSize + (slot & 15);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      vcol[j * kBlockSize] = (uint8_t)(v0 >> (8 * j));
-      vcol[(4 + j) * kBlockSize] = (uint8_t)(v1 >> (8 * j));
-    }
+    put_row_vec_e4m3(k_new, v_new, i, slot, h, e, heads, row_vecs, k_cache, v_cache, k_scale,
+                     v_scale, k_scales, v_scales, err);
   }
 }
 

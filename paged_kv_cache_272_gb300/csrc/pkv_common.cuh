@@ -28,6 +28,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// L2 policy for data written now and read back soon by another kernel (split-K partial
+// results): its lines are replaced last, so the streamed KV tiles do not push them to DRAM.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// fp32 store with an L2 cache policy.
+__device__ __forceinline__ void st_f32_hint(float *p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

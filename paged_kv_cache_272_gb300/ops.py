@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
-PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
+PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC, PKV_PREFILL_TC128 = 0, 1, 2, 3
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
 DEV_BAD_SCALE = 32
 DEFAULT_PARTITION = 512
@@ -24,7 +24,7 @@ DEFAULT_PARTITION = 512
 # Every entry point the header declares: name -> (restype, argtypes).
 _P, _I, _F, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
                          ctypes.c_int64)
-ABI_VERSION = 2  # PKV_ABI_VERSION of include/pagedkv.h
+ABI_VERSION = 3  # PKV_ABI_VERSION of include/pagedkv.h
 SIGNATURES = {
     "paged_kv_version": (_I, []),
     "paged_kv_strerror": (ctypes.c_char_p, [_I]),
@@ -34,6 +34,11 @@ SIGNATURES = {
     "paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _I, _P, _SZ, _P, _P]),
+    "paged_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                               _P, _P, _P, _I, _P, _I, _P, _SZ, _P, _P]),
+    "paged_decode_step_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
+                                   _F, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _SZ, _P,
+                                   _P]),
     "paged_attention_set_variant": (_I, [_I]),
     "paged_attention_prefill_set_variant": (_I, [_I]),
     "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -202,6 +207,49 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _ptr(err_flag), _stream(stream)), "paged_attention_decode")
 
 
+def _step_io(k_new, v_new, slot_mapping, pairs, Hkv, D):
+    """Checks of the write and copy arguments of a decode step; returns (T, P)."""
+    T = 0 if slot_mapping is None else slot_mapping.shape[0]
+    if T:
+        _bf16_cuda("k_new", k_new)
+        _bf16_cuda("v_new", v_new)
+        if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda \
+                or not slot_mapping.is_contiguous():
+            raise TypeError("slot_mapping must be a contiguous int64 CUDA tensor")
+        if tuple(k_new.shape) != (T, Hkv, D) or k_new.shape != v_new.shape:
+            raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    P = 0 if pairs is None else pairs.numel() // 2
+    if P:
+        _i32("block_pairs", pairs)
+    return T, P
+
+
+def paged_decode_step(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                      max_context_len, workspace, k_new=None, v_new=None, slot_mapping=None,
+                      block_pairs=None, partition_size=DEFAULT_PARTITION, err_flag=None,
+                      stream=None):
+    """One decode step: copy-on-write of block_pairs [P][2], the write of k_new/v_new
+    [T][Hkv][D] at slot_mapping, then paged decode attention into out [S][Hq][D]."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16_cuda(n, t)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S][max_blocks] and context_lens [S]")
+    T, P = _step_io(k_new, v_new, slot_mapping, block_pairs, Hkv, D)
+    check(lib.paged_decode_step(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
+        int(partition_size), int(max_context_len), _ptr(k_new) if T else None,
+        _ptr(v_new) if T else None, _ptr(slot_mapping) if T else None, T,
+        _ptr(block_pairs) if P else None, P, _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)), "paged_decode_step")
+
+
 def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
                             scale, max_query_len, err_flag=None, stream=None):
     """Chunked prefill: rows query_start[s] .. query_start[s+1]-1 of q [T][Hq][D] are the
@@ -226,7 +274,7 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
 
 
 def set_prefill_variant(variant: int) -> int:
-    """Select the chunked-prefill kernel (PKV_PREFILL_AUTO / _MMA / _TC); returns the
+    """Select the chunked-prefill kernel (PKV_PREFILL_AUTO / _MMA / _TC / _TC128); returns the
     previous selection."""
     prev = lib.paged_attention_prefill_set_variant(int(variant))
     if prev < 0:
@@ -358,3 +406,36 @@ def selftest_bounded_wait(err_flag, result, limit_cycles, use_spin=False, stream
     check(lib.pkv_selftest_bounded_wait(_ptr(err_flag), _ptr(result), int(limit_cycles),
                                         1 if use_spin else 0, _stream(stream)),
           "pkv_selftest_bounded_wait")
+
+
+def paged_decode_step_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                          v_scale, max_context_len, workspace, k_new=None, v_new=None,
+                          slot_mapping=None, block_pairs=None, partition_size=DEFAULT_PARTITION,
+                          err_flag=None, stream=None):
+    """paged_decode_step over E4M3 caches.  k_scale/v_scale: floats (one scale per cache)
+    or float32 CUDA tensors [num_kv_heads] (one scale per KV head)."""
+    _bf16_cuda("out", out)
+    _bf16_cuda("q", q)
+    _u8_cuda("k_cache", k_cache)
+    _u8_cuda("v_cache", v_cache)
+    _i32("block_tables", block_tables)
+    _i32("context_lens", context_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if D2 != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    T, P = _step_io(k_new, v_new, slot_mapping, block_pairs, Hkv, D)
+    per_head = torch.is_tensor(k_scale)
+    if per_head:
+        for n, t in (("k_scales", k_scale), ("v_scales", v_scale)):
+            if t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != (Hkv,):
+                raise TypeError(f"{n} must be a float32 CUDA tensor [num_kv_heads]")
+    check(lib.paged_decode_step_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, D, bs, NB, float(scale),
+        1.0 if per_head else float(k_scale), 1.0 if per_head else float(v_scale),
+        _ptr(k_scale) if per_head else None, _ptr(v_scale) if per_head else None,
+        int(partition_size), int(max_context_len), _ptr(k_new) if T else None,
+        _ptr(v_new) if T else None, _ptr(slot_mapping) if T else None, T,
+        _ptr(block_pairs) if P else None, P, _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)), "paged_decode_step_fp8")

@@ -105,6 +105,21 @@ def sample_pairs(w, n_short=64, seed=0):
     return np.array(pairs, dtype=np.int32)
 
 
+def wide_pairs(w, n_short=256, seed=0):
+    """(sequence, head) pairs: every query head of every sequence of the longest context
+    (each of their split-K merges in full), plus n_short distinct random rows of the
+    other sequences."""
+    rng = np.random.default_rng(seed)
+    longest = np.flatnonzero(w.context_lens == w.context_lens.max())
+    pairs = [(int(s), h) for s in longest for h in range(w.num_q_heads)]
+    others = np.setdiff1d(np.arange(w.num_seqs), longest)
+    cand = np.stack(np.meshgrid(others, np.arange(w.num_q_heads), indexing="ij"), -1)
+    cand = cand.reshape(-1, 2)
+    pick = rng.choice(len(cand), size=min(n_short, len(cand)), replace=False)
+    pairs += [tuple(int(x) for x in cand[i]) for i in pick]
+    return np.array(pairs, dtype=np.int32)
+
+
 def rows_of(cache: torch.Tensor) -> torch.Tensor:
     """[NB][Hkv][16][D] -> [NB*16][Hkv][D] in slot order (to quantise a whole cache)."""
     NB, Hkv, bs, D = cache.shape

@@ -148,7 +148,7 @@ def test_fp8_per_head_host_validation():
                       kw.get("ws", ws), None, None]
     assert lib.paged_attention_decode_fp8_per_head(*a(ks=None)) == -1
     assert lib.paged_attention_decode_fp8_per_head(*a(vs=None)) == -1
-    assert lib.paged_attention_decode_fp8_per_head(*a(D=64)) == -2
+    assert lib.paged_attention_decode_fp8_per_head(*a(D=96)) == -2
     assert lib.paged_attention_decode_fp8_per_head(*a(bs=32)) == -3
     assert lib.paged_attention_decode_fp8_per_head(*a(ws=ws - 1)) == -5
     assert lib.paged_attention_decode_fp8_per_head(*a(S=0, ks=None, vs=None)) == 0
@@ -200,3 +200,34 @@ def test_selftest_bounded_wait_validates_on_host():
     assert ops.lib.pkv_selftest_bounded_wait(fake, None, 1000, 0, None) == ERR_NULL
     assert ops.lib.pkv_selftest_bounded_wait(fake, fake, 0, 0, None) == ERR_SHAPE
     assert ops.lib.pkv_selftest_bounded_wait(fake, fake, 1 << 40, 1, None) == ERR_SHAPE
+
+
+def test_decode_step_host_validation():
+    """The fused decode-step entry points check the write and copy arguments on the host
+    before anything is enqueued."""
+    from paged_kv_cache_272_gb300.ops import lib
+    fake = 1 << 20
+    ws = lib.paged_attention_workspace_size(4, 8, 128, 1000, 512)
+
+    def st(**kw):
+        return [fake, fake, fake, fake, fake, fake, kw.get("S", 4), 8, 8, 2, kw.get("D", 128),
+                16, 16, ctypes.c_float(0.1), 512, 1000, kw.get("kn", fake), kw.get("vn", fake),
+                kw.get("sl", fake), kw.get("T", 4), kw.get("pr", fake), kw.get("P", 2), fake,
+                kw.get("ws", ws), None, None]
+    assert lib.paged_decode_step(*st(kn=None)) == -1          # k_new missing
+    assert lib.paged_decode_step(*st(sl=None)) == -1          # slot_mapping missing
+    assert lib.paged_decode_step(*st(pr=None)) == -1          # pairs missing
+    assert lib.paged_decode_step(*st(kn=fake + 8)) == -4      # k_new misaligned
+    assert lib.paged_decode_step(*st(T=-1)) == -2
+    assert lib.paged_decode_step(*st(P=-1)) == -2
+    assert lib.paged_decode_step(*st(D=96)) == -2
+    assert lib.paged_decode_step(*st(ws=ws - 1)) == -5
+
+    def st8(**kw):
+        return [fake, fake, fake, fake, fake, fake, 4, 8, 8, 2, kw.get("D", 128), 16, 16,
+                ctypes.c_float(0.1), ctypes.c_float(kw.get("k", 0.02)), ctypes.c_float(0.015),
+                kw.get("ks", None), kw.get("vs", None), 512, 1000, fake, fake, fake, 4, None, 0,
+                fake, ws, None, None]
+    assert lib.paged_decode_step_fp8(*st8(k=0.0)) == -2       # per-cache scale not > 0
+    assert lib.paged_decode_step_fp8(*st8(ks=fake)) == -1     # one per-head array only
+    assert lib.paged_decode_step_fp8(*st8(D=96)) == -2

@@ -58,9 +58,6 @@ def test_write_fp8_all_bf16_patterns():
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_fp8_config_parity(cfg):
     w = workloads.make_config(cfg, device="cpu" if cfg == 1 else "cuda")
-    if w.head_dim != 128:  # the E4M3 attention kernel takes head_dim 128
-        w = workloads.build("tiny-d128", w.context_lens, w.num_q_heads, w.num_kv_heads, 128,
-                            seed=1001, device="cpu", num_blocks=16)
     out, kq, vq, ko, vo, err = fp8_step(w)
     assert err == 0
     assert same_codes(kq, ko) and same_codes(vq, vo), "E4M3 write/copy not bit-exact"
@@ -72,7 +69,8 @@ def test_fp8_long_context_sampled():
     out, kq, vq, ko, vo, err = fp8_step(w)
     assert err == 0
     assert same_codes(kq, ko) and same_codes(vq, vo)
-    sel = H.sample_pairs(w, n_short=32)
+    sel = H.wide_pairs(w, n_short=256)  # all 512 long rows + 256 short ones
+    assert len(sel) >= 768
     ref = fp8_ref(w, ko, vo, sel=sel)
     got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
               torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
@@ -113,11 +111,29 @@ def test_fp8_bad_block_id_is_flagged_not_read():
         H.assert_attention_close(out[keep], ref[keep], f"untouched sequences (block {pos})")
 
 
+@pytest.mark.parametrize("G", [1, 2, 8])
+@pytest.mark.parametrize("P", [64, 512])
+def test_fp8_head_dim_64(G, P):
+    """head_dim 64 (64-byte E4M3 rows, the 64-byte swizzle): boundary contexts, groups and
+    partitions, one scale per cache and one per KV head."""
+    ctx = [1, 2, 15, 16, 17, 33, 511, 512, 513, 1500, 2999]
+    w = workloads.build("fp8-d64", ctx, 2 * G, 2, 64, seed=90 + G, device="cuda")
+    out, kq, vq, ko, vo, err = fp8_step(w, partition_size=P)
+    assert err == 0
+    assert same_codes(kq, ko) and same_codes(vq, vo)
+    H.assert_attention_close(out, fp8_ref(w, ko, vo), f"fp8 d64 G={G} P={P}")
+    ks, vs = np.array([0.02, 0.05], np.float32), np.array([0.015, 0.03], np.float32)
+    out, kq, vq, ko, vo, err = fp8_step(w, ks, vs, partition_size=P)
+    assert err == 0
+    assert same_codes(kq, ko) and same_codes(vq, vo)
+    H.assert_attention_close(out, fp8_ref(w, ko, vo, ks, vs), f"fp8 d64 per head G={G} P={P}")
+
+
 def test_fp8_rejects_other_head_dims():
     o = H.ops()
-    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(4, 1, 16, 64, dtype=torch.uint8, device="cuda")
-    ws = o.alloc_workspace(1, 2, 64, 16)
+    q = torch.zeros(1, 2, 96, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 1, 16, 96, dtype=torch.uint8, device="cuda")
+    ws = o.alloc_workspace(1, 2, 96, 16)
     with pytest.raises(o.PagedKVError):
         o.paged_attention_decode_fp8(q.clone(), q, kc, kc.clone(),
                                      torch.zeros(1, 1, dtype=torch.int32, device="cuda"),

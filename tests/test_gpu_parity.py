@@ -41,15 +41,17 @@ def test_config_parity_full(cfg, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_config5_long_context_sampled(variant):
-    """8 x 131072 + 120 short contexts at full size; the oracle computes a sample of
-    (sequence, head) outputs one by one.  Write and copy are checked in full."""
+    """8 x 131072 + 120 short contexts at full size; the oracle computes every query head
+    of the eight long sequences (512 rows, each a 256-partition split-K merge) and 256
+    rows of the short ones, one by one.  Write and copy are checked in full."""
     w = _make(5)
     out, k, v, err = H.gpu_step(w, variant)
     assert err == 0
     ko, vo = H.oracle_caches(w)
     assert np.array_equal(H.u16(k), ko)
     assert np.array_equal(H.u16(v), vo)
-    sel = H.sample_pairs(w, n_short=48)
+    sel = H.wide_pairs(w, n_short=256)
+    assert len(sel) >= 768
     ref = H.oracle_out(w, ko, vo, sel=sel)
     got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
               torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]

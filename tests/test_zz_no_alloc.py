@@ -1,4 +1,4 @@
-"""The allocation-free attention entry point against the regular one.
+"""The allocation-free attention entry point against the fp64 oracle and the regular one.
 
 paged_attention_decode_noalloc serves callers that cannot allocate device memory (no
 cudaMalloc on their thread, memory owned by another runtime, a stream someone else is
@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_272_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -61,6 +62,26 @@ def _close(a, b, what):
     assert e.mean() <= MEAN_TOL, f"{what}: mean err {e.mean()}"
 
 
+def _u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle(w):
+    """fp64 oracle output of the step: the new token written into host copies of the
+    caches, then attention over every sequence and head."""
+    k, v = _u16(w.k_cache).copy(), _u16(w.v_cache).copy()
+    oracle.kv_write(k, v, _u16(w.k_new), _u16(w.v_new), w.slot_mapping)
+    return oracle.attention(_u16(w.q), k, v, w.block_tables, w.context_lens, w.scale,
+                            nthreads=8)
+
+
+def _close_ref(a, ref, what):
+    a = a.float().cpu().double().numpy().reshape(ref.shape)
+    e = np.abs(a - ref)
+    assert np.all(e <= ATOL + RTOL * np.abs(ref)), f"{what}: max err {e.max()}"
+    assert e.mean() <= MEAN_TOL, f"{what}: mean err {e.mean()}"
+
+
 def test_noalloc_matches_regular_entry_point_twice():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -81,6 +102,7 @@ def test_noalloc_matches_regular_entry_point_twice():
         torch.cuda.synchronize()
         assert err.item() == 0
         _close(out, ref, f"call {i + 1}")
+        _close_ref(out, _oracle(w), f"call {i + 1} against the oracle")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
