@@ -316,13 +316,12 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 
 /*
  * Chunked-prefill kernel selection, process-wide (for measurement; default AUTO = the
- * tcgen05 kernel for head_dim 128, the mma.sync kernel for head_dim 64).  Returns the
+ * tcgen05 kernel, for head_dim 64 and 128).  Returns the
  * previous value, or PKV_ERR_ARG for an unknown value.
  */
 #define PKV_PREFILL_AUTO 0
 #define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
 #define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
-#define PKV_PREFILL_TC128 3 /* tcgen05, 128-key tiles, Q in TMEM, one CTA per SM       */
 int paged_attention_prefill_set_variant(int variant);
 
 /*

@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
-PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC, PKV_PREFILL_TC128 = 0, 1, 2, 3
+PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
 DEV_BAD_SCALE = 32
 DEFAULT_PARTITION = 512
@@ -274,7 +274,7 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
 
 
 def set_prefill_variant(variant: int) -> int:
-    """Select the chunked-prefill kernel (PKV_PREFILL_AUTO / _MMA / _TC / _TC128); returns the
+    """Select the chunked-prefill kernel (PKV_PREFILL_AUTO / _MMA / _TC); returns the
     previous selection."""
     prev = lib.paged_attention_prefill_set_variant(int(variant))
     if prev < 0:
