@@ -756,7 +756,7 @@ def run_prefill(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
-          "tc": ops.PKV_PREFILL_TC, "tc128": ops.PKV_PREFILL_TC128}[args.prefill_kernel]
+          "tc": ops.PKV_PREFILL_TC}[args.prefill_kernel]
     ops.set_prefill_variant(pk)
     w = workloads.make_prefill_config(args.config, device="cuda", seed=args.seed)
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -863,10 +863,9 @@ def run_prefill(args):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (attn_ms / 1e3) / 1e12
-    # AUTO runs the tcgen05 kernel for head_dim 128 and the mma.sync kernel for 64
-    tc = pk == ops.PKV_PREFILL_TC or (pk == ops.PKV_PREFILL_AUTO and D == 128)
-    kname = ("prefill-tc128" if pk == ops.PKV_PREFILL_TC128 and D == 128 else
-             "prefill-tc" if tc else "prefill-mma")
+    # AUTO runs the tcgen05 kernel (head_dim 64 and 128)
+    tc = pk in (ops.PKV_PREFILL_TC, ops.PKV_PREFILL_AUTO)
+    kname = "prefill-tc" if tc else "prefill-mma"
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
@@ -1186,9 +1185,8 @@ def main():
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
                     help="with --kv-dtype fp8: one E4M3 scale per cache, or one per KV head")
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc", "tc128"],
-                    help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc "
-                         "for head_dim 128")
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc"],
+                    help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc")
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="decode step through paged_decode_step (one call, default) or the "
                          "three separate calls (copy, write, attention)")

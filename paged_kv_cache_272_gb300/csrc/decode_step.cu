@@ -27,7 +27,7 @@ namespace {
 constexpr int kStepThreads = 512;
 constexpr int kStepMaxPairs = 1024;  // pairs the prologue takes (more: a copy launch first)
 constexpr int kStepMaxWindow = 64;   // most tokens a write CTA takes at a time
-constexpr int kCopyBatch = 4;        // 16-byte vectors a thread loads before it stores
+constexpr int kCopyBatch = 8;        // 16-byte vectors a thread loads before it stores
 
 // Tokens a write CTA takes at a time: about one 16-byte vector per thread.
 __host__ __device__ constexpr int step_window(int per_tok) {

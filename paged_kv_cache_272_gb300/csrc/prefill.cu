@@ -344,7 +344,7 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 
 
 // ------------------------------------------------------------------------------------
-// tcgen05 variant (head_dim 128): the same arithmetic on the 5th-generation tensor
+// tcgen05 variant (head_dim 64 and 128): the same arithmetic on the 5th-generation tensor
 // cores.  One CTA = 128 (token, head) rows of one (sequence, KV head), eight warps:
 //  * warps 0-3 ("softmax"): thread t owns row t -- TMEM lane t of the S and O
 //    accumulators and row t of the Q tile in shared memory.  They stage Q, read each
@@ -365,33 +365,44 @@ int launch_prefill_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensor
 //  * warps 5 and 6 ("tma"): lanes 0-3 load the four K (warp 5) or V (warp 6) blocks of
 //    each 64-key tile into their own two-slot ring (TMA tiled copies as in the mma.sync
 //    variant), reading the block ids one tile ahead.
-// Shared-memory tiles use the 128-byte swizzle that TMA writes: Q [2 halves of
-// head_dim][128 rows][128 B], P [128 rows][64 keys x 2 B], K and V tiles
-// [2 halves][64 keys][128 B] per ring slot.  Q, K (both K-major) and P (K-major) enter as
-// canonical SW128 operands (8-row groups 1024 B apart); V enters as the MN-major
-// operand of O += P V (64-column chunks 8192 B apart, 8-key groups 1024 B apart).
-// TMEM: S buffers at columns 0 and 64, O at columns 128..255 (256 allocated).
+// Shared-memory tiles use the 128-byte swizzle that TMA writes: Q [head_dim / 64 halves]
+// [128 rows][128 B], P [128 rows][64 keys x 2 B], K and V tiles [head_dim / 64 halves]
+// [64 keys][128 B] per ring slot.  Q, K (both K-major) and P (K-major) enter as canonical
+// SW128 operands (8-row groups 1024 B apart); V enters as the MN-major operand of
+// O += P V (64-column chunks 8192 B apart, 8-key groups 1024 B apart).  TMEM: S buffers
+// at columns 0 and 64, O at columns 128 .. 128 + head_dim - 1 (256 allocated).  At
+// head_dim 64 a score product is M 128 x N 64 x K 64 and O has 64 columns; the rest is
+// the same.
 
 constexpr int kTcRows = 128;
 constexpr int kTcWarps = 8;
 constexpr uint32_t kTmemCols = 256;
 
-// Shared memory is requested 1024-byte aligned and sized exactly, so that two CTAs fit
-// on one SM (2 x 112 KB); a CTA whose window is not aligned reports an error and exits
+// Shared memory is requested 1024-byte aligned, so that two CTAs fit on one SM (2 x 112
+// KB at head_dim 128; 2 x 78 KB at head_dim 64, where the tiles need 64 KB, so that a
+// third CTA does not wait for TMEM); a CTA whose window is not aligned reports an error
+// and exits
 // without touching it.  K and V tiles live in separate two-slot rings: a K slot is
 // released as soon as its scores are computed, a V slot once its P V product is done,
 // so the next K tiles load while the current softmax runs.
+template <int D>
 struct TcLayout {
-  static constexpr int kQ = 0;                       // 32 KB
-  static constexpr int kP = 32768;                   // 16 KB
-  static constexpr int kK = 49152;                   // 2 x 16 KB
-  static constexpr int kV = 81920;                   // 2 x 16 KB
-  static constexpr int kSlot = 16384;
-  static constexpr int kBars = 114688;
+  static constexpr int kHalves = D / 64;             // 64-column halves of head_dim
+  static constexpr int kQHalf = kTcRows * 128;       // 16 KB: 128 rows x 64 dims
+  static constexpr int kKHalf = kKeys * 128;         // 8 KB: 64 keys x 64 dims
+  static constexpr int kQ = 0;                       // D 128: 32 KB, D 64: 16 KB
+  static constexpr int kP = kHalves * kQHalf;        // 16 KB
+  static constexpr int kSlot = kHalves * kKHalf;     // one K or V tile
+  static constexpr int kK = kP + 16384;              // 2 slots
+  static constexpr int kV = kK + 2 * kSlot;          // 2 slots
+  static constexpr int kBars = kV + 2 * kSlot;
   static constexpr int kNumBars = 18;                // K full/empty x2, V full/empty x2,
                                                      // S full/free x2, P full x2, O done,
                                                      // final, P V done x2
   static constexpr int kSmem = kBars + kNumBars * 8 + 16;
+  // Requested per CTA: at least 78 KB, so that no more than two CTAs share an SM (each
+  // holds 256 TMEM columns; a third would wait in its allocation).
+  static constexpr int kSmemLaunch = kSmem > 78 * 1024 ? kSmem : 78 * 1024;
 };
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -483,12 +494,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                : "memory");
 }
 
-template <bool PT>
+template <int D, bool PT>
 __global__ void __launch_bounds__(kTcWarps * 32, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
-  constexpr int D = 128;
-  using Lay = TcLayout;
+  using Lay = TcLayout<D>;
+  constexpr int H = Lay::kHalves;
   extern __shared__ __align__(1024) unsigned char smem_tc[];
   const uint32_t base = smem_u32(smem_tc);
   if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
@@ -556,7 +567,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS = tmem, tO = tmem + 128;  // S buffers at columns 0 and 64, O after
 
   if (warp < 4) {
     // ---------------- softmax warps: thread t owns row t ----------------
@@ -571,10 +582,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       const uint4 *qrow = reinterpret_cast<const uint4 *>(
           a.q + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8 * H; ++c) {
         const uint4 v = valid ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
-        st_shared_v4(sQ + (c >> 3) * 16384 + t * 128 + (((c & 7) ^ (t & 7)) << 4), v.x, v.y, v.z,
-                     v.w);
+        st_shared_v4(sQ + (c >> 3) * Lay::kQHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4), v.x,
+                     v.y, v.z, v.w);
       }
     }
     fence_proxy_async();
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
           m = mn;
           l *= corr;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
             tmem_ld32(tO + 32 * cc + lane_base, o);
             tmem_wait_ld();
@@ -689,9 +700,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         }
         const uint32_t vst = sV + (j & 1) * Lay::kSlot;
         const int z0 = kv_end - t0;
-        for (int i = t; i < (kKeys - z0) * 16; i += 128) {
-          const int row = z0 + (i >> 4), rem = i & 15;
-          st_shared_v4(vst + (rem >> 3) * 8192 + row * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
+        for (int i = t; i < (kKeys - z0) * 8 * H; i += 128) {
+          const int row = z0 + i / (8 * H), rem = i % (8 * H);
+          st_shared_v4(vst + (rem >> 3) * Lay::kKHalf + row * 128 + (rem & 7) * 16, 0u, 0u, 0u,
+                       0u);
         }
       }
       if (PT) {
@@ -719,7 +731,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       tc_fence_after();
       const float inv = 1.f / l;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * cc + lane_base, o);
         tmem_wait_ld();
@@ -759,8 +771,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma(tS + 64 * sb, sw128_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idS,
+          tc_mma(tS + 64 * sb,
+                 sw128_desc(sQ + (kk >> 2) * Lay::kQHalf + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(kst + (kk >> 2) * Lay::kKHalf + (kk & 3) * 32, 16, 1024), idS,
                  kk > 0 ? 1u : 0u);
         tc_commit(s_full + 8 * sb);
         tc_commit(k_empty + 8 * sb);
@@ -788,11 +801,13 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
 #pragma unroll
         for (int k = 0; k < kKeys / 16; ++k) {
           if (PT)
-            tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k, sw128_desc(vst + 2048 * k, 8192, 1024),
-                      idO, (jp > 0 || k > 0) ? 1u : 0u);
+            tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k,
+                      sw128_desc(vst + 2048 * k, Lay::kKHalf, 1024), idO,
+                      (jp > 0 || k > 0) ? 1u : 0u);
           else
             tc_mma(tO, sw128_desc(sP + 32 * k, 16, 1024),
-                   sw128_desc(vst + 2048 * k, 8192, 1024), idO, (jp > 0 || k > 0) ? 1u : 0u);
+                   sw128_desc(vst + 2048 * k, Lay::kKHalf, 1024), idO,
+                   (jp > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(o_done);
         tc_commit(v_empty + 8 * (jp & 1));
@@ -830,12 +845,13 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
           blk = INT_MIN;
         }
         const uint32_t bar = full + 8 * slot;
-        mbar_arrive_expect_tx(bar, blk != INT_MIN ? 4096u : 0u);  // one head tile, two halves
+        // one head tile: H boxes of 16 rows x 64 columns
+        mbar_arrive_expect_tx(bar, blk != INT_MIN ? 2048u * H : 0u);
         if (blk != INT_MIN) {
           const int row = (blk * a.num_kv_heads + g) * kBlockSize;
           const uint32_t dst = ring + slot * Lay::kSlot + lane * 2048;
-          tma_load_2d(dst, map, 0, row, bar);
-          tma_load_2d(dst + 8192, map, 64, row, bar);
+#pragma unroll
+          for (int h = 0; h < H; ++h) tma_load_2d(dst + h * Lay::kKHalf, map, 64 * h, row, bar);
         }
         issued = j + 1;
       }
@@ -856,38 +872,41 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   }
 }
 
-template <bool PT>
+template <int D, bool PT>
 int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                         cudaStream_t st) {
-  using Lay = TcLayout;
+  using Lay = TcLayout<D>;
   static std::atomic<int> ready[kMaxDevices];  // shared-memory opt-in and carve-out, per device
   const int r = per_device_setup(ready, [] {
     cudaError_t e = cudaFuncSetAttribute(
-        prefill_tc_kernel<PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+        prefill_tc_kernel<D, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemLaunch);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_tc_kernel<PT>,
+      e = cudaFuncSetAttribute(prefill_tc_kernel<D, PT>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
     return e == cudaSuccess ? 1 : -(int)e;
   });
   if (r <= 0) return -r;
-  return (int)launch_pdl(prefill_tc_kernel<PT>,
+  return (int)launch_pdl(prefill_tc_kernel<D, PT>,
                          dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
                               (unsigned)a.num_seqs),
-                         dim3(kTcWarps * 32), (size_t)Lay::kSmem, st, a, tk, tv);
+                         dim3(kTcWarps * 32), (size_t)Lay::kSmemLaunch, st, a, tk, tv);
 }
 
 // P kept in tensor memory by default (the A operand of P V read from TMEM: no shared-
 // memory traffic for P, 6% faster on GB300); PKV_PREFILL_P=smem selects the variant that
 // stages P in shared memory.
 int launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                      cudaStream_t st) {
+                      int head_dim, cudaStream_t st) {
   static const bool p_in_tmem = [] {  // read once (thread-safe static initialisation)
     const char *v = std::getenv("PKV_PREFILL_P");
     return !(v && std::strcmp(v, "smem") == 0);
   }();
-  return p_in_tmem ? launch_prefill_tc_t<true>(a, tk, tv, st)
-                   : launch_prefill_tc_t<false>(a, tk, tv, st);
+  if (head_dim == 64)
+    return p_in_tmem ? launch_prefill_tc_t<64, true>(a, tk, tv, st)
+                     : launch_prefill_tc_t<64, false>(a, tk, tv, st);
+  return p_in_tmem ? launch_prefill_tc_t<128, true>(a, tk, tv, st)
+                   : launch_prefill_tc_t<128, false>(a, tk, tv, st);
 }
 
 std::atomic<int> g_prefill_variant{PKV_PREFILL_AUTO};
@@ -916,7 +935,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
     return PKV_ERR_ALIGN;
   const int group = num_q_heads / num_kv_heads;
   const int variant = g_prefill_variant.load();
-  const bool tc = head_dim == 128 && variant != PKV_PREFILL_MMA;
+  const bool tc = variant != PKV_PREFILL_MMA;
   const int rows_per_cta = tc ? kTcRows : kRows;
   const int64_t tiles = ((int64_t)max_query_len * group + rows_per_cta - 1) / rows_per_cta;
   const uint64_t cache_rows = (uint64_t)num_blocks * num_kv_heads * kBlockSize;
@@ -946,7 +965,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = tc ? launch_prefill_tc(a, tk, tv, st)
+  const int rc = tc ? launch_prefill_tc(a, tk, tv, head_dim, st)
                     : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
                                       : launch_prefill_t<64, 4>(a, tk, tv, st);
   return rc == 0 ? PKV_OK : PKV_ERR_CUDA;

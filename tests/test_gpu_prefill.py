@@ -20,8 +20,8 @@ def _need_gpu():
 
 @pytest.fixture(params=["tc", "mma"])
 def variant(request):
-    """Run a test with the tcgen05 kernel and with the mma.sync kernel (head_dim 64 always
-    takes the mma.sync kernel)."""
+    """Run a test with the tcgen05 kernel and with the mma.sync kernel (both take head_dim
+    64 and 128)."""
     o = H.ops()
     prev = o.set_prefill_variant(o.PKV_PREFILL_TC if request.param == "tc" else o.PKV_PREFILL_MMA)
     yield request.param
