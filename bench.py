@@ -942,48 +942,47 @@ def serve_setup(cfg, static=False, n=None, device="cuda"):
 
 
 def serve_run(drv, stream, decode_bytes_per_token):
-    """Run the stream to completion.  Every step's outputs are read back to the host
-    (what a sampler would read); the host keeps two steps in flight -- it plans and
-    queues step k + 1 (staging and output buffers of the other slot) before it waits
-    for step k's outputs, since the scheduler's decisions do not depend on the sampled
-    values.  Returns timing and counts."""
+    """Run the stream to completion on the driver's packed path (the native scheduler
+    packs each step's plan into pinned staging; one fused decode-step call and one
+    prefill call per step).  Every step's outputs are read back to the host (what a
+    sampler would read: every decode row, the last row of every prefill chunk); the host
+    keeps two steps in flight -- it plans and queues step k + 1 (staging and output
+    buffers of the other slot) before it waits for step k's outputs, since the
+    scheduler's decisions do not depend on the sampled values.  Returns timing and
+    counts."""
     tot = dict(dev_ms=0.0, dec_ms=0.0, dec_bytes=0, steps=0, outs=0)
     cur = {}
     drv.on_decode = lambda k: cur["dec"][k].record(stream)
 
     def retire(item):
-        x, a, b, dev_pair = item
+        pk, slot, a, b, dev_pair = item
         b.synchronize()  # this step's outputs are on the host
         tot["steps"] += 1
-        nd = x.num_decode
-        p = x.plan
-        tot["outs"] += nd + int(sum(1 for i in range(nd, p.seq_ids.shape[0])
-                                    if p.context_lens[i] == len(drv.prompts[int(p.seq_ids[i])])))
+        tot["outs"] += pk.outputs
         tot["dev_ms"] += a.elapsed_time(b)
+        nd = pk.num_decode
         if nd:
             tot["dec_ms"] += dev_pair[0].elapsed_time(dev_pair[1])
-            tot["dec_bytes"] += int(p.context_lens[:nd].astype(np.int64).sum()) * decode_bytes_per_token
+            ctx = drv.f_np[slot]["ctx"][:nd]
+            tot["dec_bytes"] += int(ctx.sum(dtype=np.int64)) * decode_bytes_per_token
 
     # timing events, reused: a set is free again once its step has retired
     ev_sets = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(3)]
     t0 = time.perf_counter()
     slot, pending, k = 0, [], 0
     while not drv.done():
-        x, staged = drv.plan_step(slot)  # the step that used this slot has retired
-        if staged is None:  # nothing to compute this step
+        pk = drv.plan_packed(slot)  # the step that used this slot has retired
+        if pk.num_tokens == 0:  # nothing to compute this step
             continue
         a, b, d0, d1 = ev_sets[k % 3]
         k += 1
         cur["dec"] = (d0, d1)
         drv.on_start = lambda: a.record(stream)
         nvtx.range_push(f"serving step {tot['steps'] + len(pending)}")
-        dec, pre = drv.launch_step(x, staged)
-        # what a sampler reads: every decode row, the last row of each prefill chunk
-        last = [pre[int(e) - 1] for e in x.prefill_query_start[1:]] if pre is not None else []
-        drv.fetch(dec, *last, slot=slot)
+        drv.launch_packed(pk, slot)
         b.record(stream)
         nvtx.range_pop()
-        pending.append((x, a, b, cur["dec"]))
+        pending.append((pk, slot, a, b, cur["dec"]))
         slot ^= 1
         if len(pending) == 2:
             retire(pending.pop(0))

@@ -70,7 +70,7 @@ extern "C" {
 /* Library ABI version: PKV_ABI_VERSION of the build (incremented when an entry point is
  * added or a signature changes).  2 added paged_kv_write_fp8_per_head,
  * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load; 3 added
- * paged_decode_step and paged_decode_step_fp8. */
+ * paged_decode_step, paged_decode_step_fp8 and pkv_sched_pack. */
 #define PKV_ABI_VERSION 3
 int paged_kv_version(void);
 
@@ -501,6 +501,46 @@ int pkv_sched_add_request(pkv_sched *sched, int64_t id, int prompt_len,
  * nothing is left to do), or PKV_ERR_OOM when requests remain but none can progress
  * (the pool is too small for the request at the head of the queue). */
 int pkv_sched_step(pkv_sched *sched, pkv_step_plan *plan);
+/* The last step's plan packed for one host-to-device copy.  Every array sits at a fixed
+ * 256-byte aligned offset that depends only on the capacities (max_tokens new tokens,
+ * max_seqs sequences, block-table rows of table_stride entries, -1 past the sequence's
+ * blocks), so device views of a staging buffer can be made once.  Besides the plan's
+ * arrays it holds, per new token, the request id, the position and the prompt token at
+ * that position (-1 past the prompt: a generated token, which the caller knows), and per
+ * prefill chunk its offset and the row of its last token within the prefill rows. */
+typedef struct {
+  int64_t slot_mapping;    /* int64 [num_tokens]                                       */
+  int64_t token_seq;       /* int64 [num_tokens] request id of each new token          */
+  int64_t last_rows;       /* int64 [chunks] last row of each prefill chunk            */
+  int64_t block_tables;    /* int32 [num_seqs][table_stride]                           */
+  int64_t context_lens;    /* int32 [num_seqs]                                         */
+  int64_t cow_pairs;       /* int32 [num_cow][2]                                       */
+  int64_t prefill_start;   /* int32 [chunks + 1] chunk offsets within the prefill rows */
+  int64_t token_ids;       /* int32 [num_tokens] prompt token, or -1                   */
+  int64_t positions;       /* int32 [num_tokens]                                       */
+  int64_t kv_rows;         /* int64 [num_tokens] left for pkv_step_synthetic_rows      */
+  int64_t q_rows;          /* int64 [num_tokens] left for pkv_step_synthetic_rows      */
+  int64_t total;           /* bytes the layout spans                                   */
+  int num_seqs, num_decode, num_tokens, num_cow;
+  int decode_max_context;  /* largest context among the decode entries                 */
+  int prefill_max_query;   /* longest prefill chunk                                    */
+  int outputs;             /* output tokens the step yields (decode entries + chunks
+                              that complete their prompt)                              */
+} pkv_step_pack;
+
+/* Writes the last pkv_sched_step's plan into buf (host memory, e.g. pinned staging)
+ * in the pkv_step_pack layout and fills *pack.  PKV_ERR_ARG if a count exceeds its
+ * capacity or buf_bytes < pack->total (the offsets and pack->total are filled even
+ * then); buf == NULL returns PKV_ERR_NULL after filling the layout. */
+int pkv_sched_pack(const pkv_sched *sched, void *buf, int64_t buf_bytes, int max_tokens,
+                   int max_seqs, int table_stride, pkv_step_pack *pack);
+/* The synthetic model of the serving benchmark and tests (it stands in for the layers
+ * that would produce each new token's q/K/V on the device): over a packed step in buf,
+ * every token id of -1 becomes the seeded generated id (rid * 7777 + pos * 131) mod
+ * 32000, and each new token gets the rows of its K/V in a table of table_rows rows,
+ * (token * 1000003 + pos * 7919) mod table_rows, and of its query,
+ * (rid * 2654435761 + pos * 40503) mod table_rows.  Not part of the method. */
+int pkv_step_synthetic_rows(void *buf, const pkv_step_pack *pack, int64_t table_rows);
 int pkv_sched_done(const pkv_sched *sched);  /* 1 when no request is waiting or running */
 int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
 

@@ -499,6 +499,109 @@ int pkv_sched_step(pkv_sched *s, pkv_step_plan *plan) {
   return rc;
 }
 
+int pkv_sched_pack(const pkv_sched *s, void *buf, int64_t buf_bytes, int max_tokens,
+                   int max_seqs, int table_stride, pkv_step_pack *pack) {
+  if (!s || !pack) return PKV_ERR_NULL;
+  if (max_tokens < 1 || max_seqs < 1 || table_stride < 1) return PKV_ERR_ARG;
+  // Fixed offsets (from the capacities alone), each 256-byte aligned.
+  auto al = [](int64_t x) { return (x + 255) & ~(int64_t)255; };
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = al(off + bytes);
+    return o;
+  };
+  const int64_t T = max_tokens, S = max_seqs;
+  pack->slot_mapping = take(8 * T);
+  pack->token_seq = take(8 * T);
+  pack->last_rows = take(8 * S);
+  pack->block_tables = take(4 * S * table_stride);
+  pack->context_lens = take(4 * S);
+  pack->cow_pairs = take(4 * 2 * S);
+  pack->prefill_start = take(4 * (S + 1));
+  pack->token_ids = take(4 * T);
+  pack->positions = take(4 * T);
+  pack->kv_rows = take(8 * T);
+  pack->q_rows = take(8 * T);
+  pack->total = off;
+  const int n = (int)s->p_seqs.size(), nd = s->p_num_decode;
+  const int ntok = (int)s->p_slots.size(), ncow = (int)(s->p_cow.size() / 2);
+  pack->num_seqs = n;
+  pack->num_decode = nd;
+  pack->num_tokens = ntok;
+  pack->num_cow = ncow;
+  if (ntok > max_tokens || n > max_seqs || ncow > max_seqs || s->p_max_blocks > table_stride)
+    return PKV_ERR_ARG;
+  if (!buf) return PKV_ERR_NULL;
+  if (buf_bytes < off) return PKV_ERR_ARG;
+  char *b = static_cast<char *>(buf);
+  int64_t *slots = reinterpret_cast<int64_t *>(b + pack->slot_mapping);
+  int64_t *tseq = reinterpret_cast<int64_t *>(b + pack->token_seq);
+  int64_t *last = reinterpret_cast<int64_t *>(b + pack->last_rows);
+  int32_t *tables = reinterpret_cast<int32_t *>(b + pack->block_tables);
+  int32_t *ctx = reinterpret_cast<int32_t *>(b + pack->context_lens);
+  int32_t *cow = reinterpret_cast<int32_t *>(b + pack->cow_pairs);
+  int32_t *pstart = reinterpret_cast<int32_t *>(b + pack->prefill_start);
+  int32_t *tok = reinterpret_cast<int32_t *>(b + pack->token_ids);
+  int32_t *pos = reinterpret_cast<int32_t *>(b + pack->positions);
+  if (ntok) std::memcpy(slots, s->p_slots.data(), sizeof(int64_t) * (size_t)ntok);
+  if (ncow) std::memcpy(cow, s->p_cow.data(), sizeof(int32_t) * 2 * (size_t)ncow);
+  if (n) std::memcpy(ctx, s->p_ctx.data(), sizeof(int32_t) * (size_t)n);
+  const int mb = s->p_max_blocks;
+  for (int i = 0; i < n; ++i) {
+    int32_t *row = tables + (size_t)i * table_stride;
+    std::memcpy(row, s->p_tables.data() + (size_t)i * mb, sizeof(int32_t) * (size_t)mb);
+    for (int c = mb; c < table_stride; ++c) row[c] = -1;
+  }
+  int dmax = 0, qmax = 0, outs = nd;
+  const int base = n > nd ? s->p_qstart[nd] : 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t rid = s->p_seqs[i];
+    const int L = s->p_qlens[i], c = s->p_ctx[i];
+    const int q0 = s->p_qstart[i];
+    const auto &rq = s->reqs.at(rid);
+    const int P = rq.P;
+    const bool toks = !rq.prompt.empty();
+    for (int k = 0; k < L; ++k) {
+      const int p = c - L + k;
+      tseq[q0 + k] = rid;
+      pos[q0 + k] = p;
+      tok[q0 + k] = (toks && p < P) ? rq.prompt[(size_t)p] : -1;
+    }
+    if (i < nd) {
+      dmax = std::max(dmax, c);
+    } else {
+      pstart[i - nd] = q0 - base;
+      last[i - nd] = (int64_t)(s->p_qstart[i + 1] - 1 - base);
+      qmax = std::max(qmax, L);
+      if (c == P) ++outs;  // the chunk completes the prompt: its first output token
+    }
+  }
+  if (n > nd) pstart[n - nd] = s->p_qstart[n] - base;
+  pack->decode_max_context = dmax;
+  pack->prefill_max_query = qmax;
+  pack->outputs = outs;
+  return PKV_OK;
+}
+
+int pkv_step_synthetic_rows(void *buf, const pkv_step_pack *pack, int64_t table_rows) {
+  if (!buf || !pack) return PKV_ERR_NULL;
+  if (table_rows <= 0) return PKV_ERR_ARG;
+  char *b = static_cast<char *>(buf);
+  int32_t *tok = reinterpret_cast<int32_t *>(b + pack->token_ids);
+  const int32_t *pos = reinterpret_cast<const int32_t *>(b + pack->positions);
+  const int64_t *rid = reinterpret_cast<const int64_t *>(b + pack->token_seq);
+  int64_t *kvr = reinterpret_cast<int64_t *>(b + pack->kv_rows);
+  int64_t *qr = reinterpret_cast<int64_t *>(b + pack->q_rows);
+  for (int t = 0; t < pack->num_tokens; ++t) {
+    const int64_t p = pos[t], r = rid[t];
+    if (tok[t] < 0) tok[t] = (int32_t)((r * 7777 + p * 131) % 32000);
+    kvr[t] = ((int64_t)tok[t] * 1000003 + p * 7919) % table_rows;
+    qr[t] = (r * 2654435761LL + p * 40503) % table_rows;
+  }
+  return PKV_OK;
+}
+
 int pkv_sched_done(const pkv_sched *s) {
   if (!s) return PKV_ERR_NULL;
   return s->waiting.empty() && s->running.empty() ? 1 : 0;

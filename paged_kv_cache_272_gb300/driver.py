@@ -19,6 +19,7 @@ position).
 """
 from __future__ import annotations
 
+import ctypes
 import math
 from dataclasses import dataclass
 
@@ -295,3 +296,125 @@ class ServingDriver:
         x, staged = self.plan_step()
         dec, pre = self.launch_step(x, staged)
         return x, dec, pre
+
+    # ---- the packed path: the plan written straight into pinned staging by the native
+    # scheduler (pkv_sched_pack), fixed offsets, device views and call arguments made
+    # once; the library is called directly with them (the buffers are the driver's own,
+    # sized for the capacities, so the wrappers' per-call checks are not needed) --------
+    def _fast_setup(self):
+        from .serving import StepPack
+        self.f_tokens = self.sched.max_batched_tokens + self.sched.max_num_seqs
+        self.f_seqs = self.sched.max_num_seqs
+        self.f_stride = (self.max_context + BS - 1) // BS
+        lay = StepPack()
+        try:  # layout only (a NULL buffer is refused after the layout is filled)
+            self.sched.pack(None, 0, self.f_tokens, self.f_seqs, self.f_stride, lay)
+        except ops.PagedKVError:
+            pass
+        self.f_lay = lay
+        self.f_bytes = lay.total
+        self.f_host = [torch.empty(self.f_bytes, dtype=torch.uint8).pin_memory()
+                       for _ in range(2)]
+        self.f_dev = torch.empty(self.f_bytes, dtype=torch.uint8, device=self.dev)
+        self.f_packs = [StepPack(), StepPack()]
+        T, S = self.f_tokens, self.f_seqs
+
+        def v(buf, off, n, dt):
+            return buf[off:off + n * torch.empty(0, dtype=dt).element_size()].view(dt)
+        self.f_np = [dict(ctx=v(h, lay.context_lens, S, torch.int32).numpy()) for h in self.f_host]
+        d = self.f_dev
+        self.f_dv = dict(kvr=v(d, lay.kv_rows, T, torch.int64), qr=v(d, lay.q_rows, T, torch.int64),
+                         last=v(d, lay.last_rows, S, torch.int64))
+        base = d.data_ptr()
+        self.f_ptr = {k: base + getattr(lay, k) for k in
+                      ("slot_mapping", "block_tables", "context_lens", "cow_pairs",
+                       "prefill_start")}
+        self.f_knew = torch.empty(T, self.Hkv, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_vnew = torch.empty_like(self.f_knew)
+        self.f_q = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_dec = torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_pre = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_last = torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_out_h = [[torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16).pin_memory()
+                         for _ in range(2)] for _ in range(2)]
+        self.f_row = self.Hq * self.D * 2  # bytes of one q / output row
+        self.f_krow = self.Hkv * self.D * 2
+        NB = self.k_cache.shape[0]
+        self.f_const = (self.k_cache.data_ptr(), self.v_cache.data_ptr(), NB, self.Hq, self.Hkv,
+                        self.D, BS, ctypes.c_float(self.scale))
+
+    def plan_packed(self, slot=0):
+        """Host part of one step on the packed path: the native scheduler steps, packs its
+        plan into pinned staging buffer `slot` (fixed offsets) and fills in the synthetic
+        model's generated token ids and table rows.  Returns the StepPack (counts and
+        layout)."""
+        if not hasattr(self, "f_host"):
+            self._fast_setup()
+        self.sched.step_only()
+        pk = self.f_packs[slot]
+        ptr = self.f_host[slot].data_ptr()
+        self.sched.pack(ptr, self.f_bytes, self.f_tokens, self.f_seqs, self.f_stride, pk)
+        if pk.num_tokens:
+            ops.check(ops.lib.pkv_step_synthetic_rows(ptr, ctypes.byref(pk), self.rows),
+                      "pkv_step_synthetic_rows")
+        return pk
+
+    def launch_packed(self, pk, slot=0):
+        """Device part of a packed step, queued on the stream: one host-to-device copy,
+        the row gathers, paged_decode_step (copies, write, decode attention) and the
+        prefill call, then the copies of what a sampler reads (every decode row, the
+        last row of every prefill chunk) into pinned buffers of `slot`.  Returns
+        (decode rows, prefill last rows) as host tensors, valid once the stream reaches
+        this point."""
+        T = pk.num_tokens
+        if T == 0:
+            return None, None
+        if self.on_start is not None:
+            self.on_start()
+        self.f_dev.copy_(self.f_host[slot], non_blocking=True)
+        self.h2d_bytes += self.f_bytes
+        dv = self.f_dv
+        k_new, v_new, q = self.f_knew[:T], self.f_vnew[:T], self.f_q[:T]
+        torch.index_select(self.k_tab_d, 0, dv["kvr"][:T], out=k_new)
+        torch.index_select(self.v_tab_d, 0, dv["kvr"][:T], out=v_new)
+        torch.index_select(self.q_tab_d, 0, dv["qr"][:T], out=q)
+        n, nd = pk.num_seqs, pk.num_decode
+        kc, vc, NB, Hq, Hkv, D, bs, scale = self.f_const
+        ptr, st = self.f_ptr, self.stream.cuda_stream
+        if self.on_decode is not None:
+            self.on_decode(0)
+        qp, dec_p = q.data_ptr(), self.f_dec.data_ptr()
+        ops.check(ops.lib.paged_decode_step(
+            dec_p, qp, kc, vc, ptr["block_tables"], ptr["context_lens"], nd, self.f_stride, Hq,
+            Hkv, D, bs, NB, scale, self.P, pk.decode_max_context, k_new.data_ptr(),
+            v_new.data_ptr(), ptr["slot_mapping"], T, ptr["cow_pairs"] if pk.num_cow else None,
+            pk.num_cow, self.ws.data_ptr(), self.ws.numel(), self.err.data_ptr(), st),
+            "paged_decode_step")
+        if self.on_decode is not None:
+            self.on_decode(1)
+        if nd:  # prologue (copies, write, plan), partition kernel, merge if split
+            self.launches += 2 + (1 if pk.decode_max_context > self.P else 0) + (
+                1 if pk.num_cow > 1024 else 0)
+        else:  # no decode entry: the copies and the write alone
+            self.launches += (1 if pk.num_cow else 0) + 1
+        outs = self.f_out_h[slot]
+        dec_h = last_h = None
+        if nd:
+            dec_h = outs[0][:nd]
+            dec_h.copy_(self.f_dec[:nd], non_blocking=True)
+            self.d2h_bytes += nd * self.f_row
+        if n > nd:
+            ch = n - nd
+            pre = self.f_pre[:T - nd]
+            ops.check(ops.lib.paged_attention_prefill(
+                pre.data_ptr(), qp + nd * self.f_row, kc, vc,
+                ptr["block_tables"] + nd * self.f_stride * 4, ptr["context_lens"] + nd * 4,
+                ptr["prefill_start"], ch, T - nd, self.f_stride, Hq, Hkv, D, bs, NB, scale,
+                pk.prefill_max_query, self.err.data_ptr(), st), "paged_attention_prefill")
+            self.launches += 1
+            last = self.f_last[:ch]
+            torch.index_select(pre, 0, dv["last"][:ch], out=last)
+            last_h = outs[1][:ch]
+            last_h.copy_(last, non_blocking=True)
+            self.d2h_bytes += ch * self.f_row
+        return dec_h, last_h

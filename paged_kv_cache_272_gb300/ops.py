@@ -83,6 +83,8 @@ SIGNATURES = {
     "pkv_sched_add_request": (_I, [_P, _I64, _I, _P, _I]),
     "pkv_sched_step": (_I, [_P, _P]),
     "pkv_sched_done": (_I, [_P]),
+    "pkv_sched_pack": (_I, [_P, _P, _I64, _I, _I, _I, _P]),
+    "pkv_step_synthetic_rows": (_I, [_P, _P, _I64]),
     "pkv_sched_get_stats": (_I, [_P, _P]),
     "pkv_selftest_bounded_wait": (_I, [_P, _P, ctypes.c_longlong, _I, _P]),
 }

@@ -25,6 +25,21 @@ class StepPlan(ctypes.Structure):
                 ("block_tables", _i32p), ("cow_pairs", _i32p)]
 
 
+class StepPack(ctypes.Structure):
+    """Layout and counts of a packed step (pkv_step_pack): byte offsets of the arrays in
+    the staging buffer, and the step's sizes."""
+    _fields_ = [("slot_mapping", ctypes.c_int64), ("token_seq", ctypes.c_int64),
+                ("last_rows", ctypes.c_int64), ("block_tables", ctypes.c_int64),
+                ("context_lens", ctypes.c_int64), ("cow_pairs", ctypes.c_int64),
+                ("prefill_start", ctypes.c_int64), ("token_ids", ctypes.c_int64),
+                ("positions", ctypes.c_int64), ("kv_rows", ctypes.c_int64),
+                ("q_rows", ctypes.c_int64), ("total", ctypes.c_int64),
+                ("num_seqs", ctypes.c_int), ("num_decode", ctypes.c_int),
+                ("num_tokens", ctypes.c_int), ("num_cow", ctypes.c_int),
+                ("decode_max_context", ctypes.c_int), ("prefill_max_query", ctypes.c_int),
+                ("outputs", ctypes.c_int)]
+
+
 class SchedStats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("finished", ctypes.c_int64),
                 ("preemptions", ctypes.c_int64), ("decode_tokens", ctypes.c_int64),
@@ -115,6 +130,8 @@ class Scheduler:
                                   ctypes.byref(h)), "pkv_sched_create")
         self._h, self.pool, self.cache = h, pool, cache
         self.max_num_seqs = max_num_seqs
+        self.max_batched_tokens = max_batched_tokens
+        self._pl = StepPlan()
 
     def close(self):
         if self._h:
@@ -149,6 +166,21 @@ class Scheduler:
                     cow_pairs=_arr(pl.cow_pairs, 2 * pl.num_cow, np.int32).reshape(-1, 2),
                     finished=pl.finished, preempted=pl.preempted, running=pl.running,
                     waiting=pl.waiting)
+
+    def step_only(self) -> int:
+        """Run one step without copying its plan out (see pack); returns the number of
+        scheduled sequences."""
+        n = lib.pkv_sched_step(self._h, ctypes.byref(self._pl))
+        _chk(min(n, 0), "pkv_sched_step")
+        return n
+
+    def pack(self, buf_ptr: int, buf_bytes: int, max_tokens: int, max_seqs: int,
+             table_stride: int, out: StepPack | None = None) -> StepPack:
+        """Write the last step's plan into host memory at buf_ptr (pkv_sched_pack)."""
+        pk = out if out is not None else StepPack()
+        _chk(lib.pkv_sched_pack(self._h, buf_ptr, buf_bytes, max_tokens, max_seqs,
+                                table_stride, ctypes.byref(pk)), "pkv_sched_pack")
+        return pk
 
     def stats(self) -> dict:
         s = SchedStats()

@@ -99,3 +99,63 @@ def test_driver_steps_match_oracle(cache_entries, blocks, overlap):
     assert np.array_equal(u16(drv.k_cache.cpu()), kh) and np.array_equal(u16(drv.v_cache.cpu()), vh)
     if cache is not None:
         assert cache.stats()["hits"] > 0
+
+
+@pytest.mark.parametrize("cache_entries,blocks", [(None, 400), (30, 60)])
+def test_packed_path_equals_the_checked_path(cache_entries, blocks):
+    """The packed serving path (native pack into pinned staging, fused decode step, two
+    steps in flight) gives, step by step, the same bits as the path checked against the
+    oracle above: every decode row, the last row of every prefill chunk, and the caches."""
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.driver import ServingDriver
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler
+    Hq, Hkv, D = 8, 2, 128
+    reqs = workloads.make_requests("shared-prefix", seed=22, n=24)
+    for r in reqs:
+        r.output_len = min(r.output_len, 40)
+    max_ctx = max(len(r.prompt) + r.output_len for r in reqs)
+
+    def make():
+        pool = BlockPool(blocks)
+        cache = PrefixCache(pool, cache_entries) if cache_entries else None
+        drv = ServingDriver(Scheduler(pool, 6, 96, cache=cache), blocks, Hq, Hkv, D, max_ctx,
+                            seed=3)
+        for r in reqs:
+            drv.add_request(r.rid, r.prompt, r.output_len)
+        return drv
+
+    ref = []
+    a = make()
+    for x, dec, pre in _steps(a, overlap=False):
+        if x.token_ids.shape[0] == 0:
+            continue
+        last = (pre[torch.as_tensor(x.prefill_query_start[1:].astype(np.int64) - 1,
+                                    device=pre.device)].cpu() if pre is not None else None)
+        ref.append((dec.cpu() if dec is not None else None, last))
+    b = make()
+    got, slot, pending = [], 0, []
+    while not b.done():
+        pk = b.plan_packed(slot)
+        if pk.num_tokens == 0:
+            continue
+        hd, hl = b.launch_packed(pk, slot)
+        ev = torch.cuda.Event()
+        ev.record()
+        pending.append((hd, hl, ev))
+        slot ^= 1
+        if len(pending) == 2:
+            hd0, hl0, ev0 = pending.pop(0)
+            ev0.synchronize()
+            got.append((None if hd0 is None else hd0.clone(), None if hl0 is None else hl0.clone()))
+    for hd0, hl0, ev0 in pending:
+        ev0.synchronize()
+        got.append((None if hd0 is None else hd0.clone(), None if hl0 is None else hl0.clone()))
+    assert len(got) == len(ref)
+    for k, ((rd, rl), (gd, gl)) in enumerate(zip(ref, got)):
+        for r_, g_, what in ((rd, gd, "decode"), (rl, gl, "prefill last rows")):
+            assert (r_ is None) == (g_ is None), (k, what)
+            if r_ is not None:
+                assert torch.equal(r_.view(torch.int16), g_.view(torch.int16)), (k, what)
+    assert int(a.err.item()) == 0 and int(b.err.item()) == 0
+    assert torch.equal(a.k_cache.view(torch.int16), b.k_cache.view(torch.int16))
+    assert torch.equal(a.v_cache.view(torch.int16), b.v_cache.view(torch.int16))

@@ -313,6 +313,88 @@ def test_driver_step_inputs_follow_the_plan(num_blocks):
         assert s.stats()["preemptions"] > 0
 
 
+@pytest.mark.parametrize("kind,num_blocks", [("pareto", 2000), ("pareto", 40),
+                                             ("shared-prefix", 3000)])
+def test_native_pack_equals_the_host_preparation(kind, num_blocks):
+    """pkv_sched_pack writes, at fixed offsets, exactly what the driver's numpy
+    preparation derives from a plan: slots, tables (padded with -1), context lengths,
+    copy pairs, chunk offsets and last rows, and per new token the request id, the
+    position and the prompt token (-1 past the prompt, where the synthetic sampler's id
+    goes); plus the step's maxima and its output-token count."""
+    import ctypes
+    from paged_kv_cache_272_gb300 import driver
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import PrefixCache, Scheduler, StepPack
+    reqs = workloads.make_requests(kind, seed=21, n=40)
+    pool = BlockPool(num_blocks)
+    cache = PrefixCache(pool, 256) if kind == "shared-prefix" else None
+    s = Scheduler(pool, 8, 96, cache=cache)
+    prompts = {}
+    for r in reqs:
+        prompts[r.rid] = np.ascontiguousarray(r.prompt, dtype=np.int32)
+        s.add_request(r.rid, prompts[r.rid], r.output_len)
+    maxT, maxS, stride = 96 + 8, 8, 200
+    pk = StepPack()
+    buf = (ctypes.c_uint8 * (1 << 20))()
+    base = ctypes.addressof(buf)
+    raw = np.frombuffer(buf, dtype=np.uint8)
+    view = lambda off, n, dt: raw[off:off + n * np.dtype(dt).itemsize].view(dt)
+    steps = outputs = 0
+    while not s.done():
+        plan = s.step()
+        s.pack(base, len(buf), maxT, maxS, stride, pk)
+        x = driver.prepare(plan, prompts, 4096, 4096)
+        T, n, nd = pk.num_tokens, pk.num_seqs, pk.num_decode
+        assert (T, n, nd, pk.num_cow) == (plan.slot_mapping.shape[0], plan.seq_ids.shape[0],
+                                          plan.num_decode, plan.cow_pairs.shape[0])
+        assert np.array_equal(view(pk.slot_mapping, T, np.int64), plan.slot_mapping)
+        tb = view(pk.block_tables, n * stride, np.int32).reshape(n, stride)
+        mb = plan.block_tables.shape[1]
+        assert np.array_equal(tb[:, :mb], plan.block_tables) and (tb[:, mb:] == -1).all()
+        assert np.array_equal(view(pk.context_lens, n, np.int32), plan.context_lens)
+        assert np.array_equal(view(pk.cow_pairs, 2 * pk.num_cow, np.int32).reshape(-1, 2),
+                              plan.cow_pairs)
+        assert np.array_equal(view(pk.positions, T, np.int32), x.positions)
+        rid = view(pk.token_seq, T, np.int64)
+        assert np.array_equal(rid, np.repeat(plan.seq_ids, plan.query_lens))
+        tok = view(pk.token_ids, T, np.int32).copy()
+        gen = tok < 0
+        tok[gen] = driver.output_token(rid[gen], x.positions[gen])
+        assert np.array_equal(tok, x.token_ids)
+        # the synthetic model's ids and table rows, natively, equal the driver's numpy ones
+        from paged_kv_cache_272_gb300 import ops
+        ops.check(ops.lib.pkv_step_synthetic_rows(base, ctypes.byref(pk), 4096), "rows")
+        assert np.array_equal(view(pk.token_ids, T, np.int32), x.token_ids)
+        assert np.array_equal(view(pk.kv_rows, T, np.int64), x.kv_rows)
+        assert np.array_equal(view(pk.q_rows, T, np.int64), x.q_rows)
+        ch = n - nd
+        if ch:
+            assert np.array_equal(view(pk.prefill_start, ch + 1, np.int32),
+                                  x.prefill_query_start)
+            assert np.array_equal(view(pk.last_rows, ch, np.int64),
+                                  x.prefill_query_start[1:].astype(np.int64) - 1)
+        assert pk.prefill_max_query == x.prefill_max_query
+        assert pk.decode_max_context == x.decode_ctx_max
+        want = nd + sum(1 for i in range(nd, n)
+                        if plan.context_lens[i] == len(prompts[int(plan.seq_ids[i])]))
+        assert pk.outputs == want
+        steps += 1
+        outputs += pk.outputs
+    assert steps > 10
+    if s.stats()["preemptions"] == 0:  # (a recomputed request's outputs count again)
+        assert outputs == sum(r.output_len for r in reqs)
+    # a capacity below the step's needs is refused
+    pool2 = BlockPool(2000)
+    s2 = Scheduler(pool2, 8, 96)
+    for r in reqs[:8]:
+        s2.add_request(r.rid, prompts[r.rid], r.output_len)
+    s2.step()
+    with pytest.raises(Exception):
+        s2.pack(base, len(buf), 4, maxS, stride)
+    with pytest.raises(Exception):
+        s2.pack(base, 16, maxT, maxS, stride)
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_native_scheduler_fuzz(seed):
     """Random pools, slot counts, budgets, cache sizes and request mixes (including pools
