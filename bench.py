@@ -952,36 +952,41 @@ def serve_run(drv, stream, decode_bytes_per_token):
     counts."""
     tot = dict(dev_ms=0.0, dec_ms=0.0, dec_bytes=0, steps=0, outs=0)
     cur = {}
-    drv.on_decode = lambda k: cur["dec"][k].record(stream)
+    # The decode attention is timed on every 4th step (its events cost host time every
+    # step they are recorded); the roofline uses the bytes and times of those steps.
+    drv.on_decode = lambda k: cur["dec"] is not None and cur["dec"][k].record(stream)
 
     def retire(item):
-        pk, slot, a, b, dev_pair = item
+        pk, slot, b_prev, b, dev_pair = item
         b.synchronize()  # this step's outputs are on the host
         tot["steps"] += 1
         tot["outs"] += pk.outputs
-        tot["dev_ms"] += a.elapsed_time(b)
+        tot["dev_ms"] += b_prev.elapsed_time(b)
         nd = pk.num_decode
-        if nd:
+        if nd and dev_pair is not None:
             tot["dec_ms"] += dev_pair[0].elapsed_time(dev_pair[1])
             ctx = drv.f_np[slot]["ctx"][:nd]
             tot["dec_bytes"] += int(ctx.sum(dtype=np.int64)) * decode_bytes_per_token
 
-    # timing events, reused: a set is free again once its step has retired
-    ev_sets = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(3)]
+    # Timing events, reused: a set is free again once its step has retired.  A step's
+    # device time runs from its first copy to its last (GPU idle time between steps is
+    # not counted).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(4)]
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(4)]
     t0 = time.perf_counter()
     slot, pending, k = 0, [], 0
     while not drv.done():
         pk = drv.plan_packed(slot)  # the step that used this slot has retired
         if pk.num_tokens == 0:  # nothing to compute this step
             continue
-        a, b, d0, d1 = ev_sets[k % 3]
+        a, b = ev[k % 4]
+        cur["dec"] = ev_dec[k % 4] if k % 4 == 0 else None
         k += 1
-        cur["dec"] = (d0, d1)
-        drv.on_start = lambda: a.record(stream)
-        nvtx.range_push(f"serving step {tot['steps'] + len(pending)}")
+        drv.start_event = a
         drv.launch_packed(pk, slot)
         b.record(stream)
-        nvtx.range_pop()
         pending.append((pk, slot, a, b, cur["dec"]))
         slot ^= 1
         if len(pending) == 2:
@@ -990,7 +995,7 @@ def serve_run(drv, stream, decode_bytes_per_token):
         retire(pending.pop(0))
     wall = time.perf_counter() - t0
     drv.on_decode = None
-    drv.on_start = None
+    drv.start_event = None
     return dict(wall_s=wall, device_ms=tot["dev_ms"], decode_ms=tot["dec_ms"],
                 decode_bytes=tot["dec_bytes"], steps=tot["steps"], output_tokens=tot["outs"])
 

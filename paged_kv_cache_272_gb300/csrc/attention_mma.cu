@@ -66,12 +66,6 @@ __device__ __forceinline__ void mma16816_f16(float (&c)[4], uint32_t a0, uint32_
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
                "f"(d)
@@ -373,14 +367,18 @@ __global__ void __launch_bounds__((NW + 1) * 32,
   // Per-thread shared-memory offsets inside a stage (the swizzle folded in once; a k-step
   // then only flips the 16-byte chunk bits 4..6, which a stage base never sets).
   const int tokA8 = 4 * (gid >> 1) + (gid & 1), tokB8 = tokA8 + 2;  // E4M3 token order
-  // E4M3 K rows are D bytes: head_dim 128 with the 128-byte swizzle (16-byte chunk ^= row
-  // & 7), head_dim 64 with the 64-byte swizzle (chunk ^= (row >> 1) & 3).
-  auto koff8 = [&](int tok) -> uint32_t {
-    return D == 128 ? (uint32_t)(tok * 128 + ((tok & 7) << 4) + 4 * tig)
-                    : (uint32_t)(tok * 64 + (((tok >> 1) & 3) << 4) + 4 * tig);
-  };
-  const uint32_t koffA = KV8 ? koff8(tokA8) : 0u;
-  const uint32_t koffB = KV8 ? koff8(tokB8) : 0u;
+  // E4M3 K rows are D bytes: head_dim 128 with the 128-byte swizzle (16-byte chunk ^=
+  // row & 7), head_dim 64 with the 64-byte swizzle (chunk ^= (row >> 1) & 3).
+  // E4M3 fragments come from ldmatrix.x4 (b16 view of the codes: a thread receives 4
+  // bytes of one 16-byte row segment, the 4 codes its f16 fragment needs).  K: lane l
+  // addresses row token (l >> 3) & 1 ? tokB : tokA of row-group l & 7, k-step + (l >> 4);
+  // V (transposed, [d][16] without swizzle): row d = 16 (l >> 4) + 8 ((l >> 3) & 1) + (l & 7).
+  const int lm = lane >> 3, lr = lane & 7;
+  const int ltok = 4 * (lr >> 1) + (lr & 1) + ((lm & 1) ? 2 : 0);
+  const uint32_t krow8 = (uint32_t)(ltok * D);  // D bytes per E4M3 K row
+  const uint32_t kkey8 = D == 128 ? (uint32_t)(ltok & 7) : (uint32_t)((ltok >> 1) & 3);
+  const uint32_t kstep8 = (uint32_t)(lm >> 1);
+  const uint32_t vrow8 = (uint32_t)((16 * (lm >> 1) + 8 * (lm & 1) + lr) * 16);
   const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row (bf16 K tile)
   const uint32_t koff16 = (uint32_t)(lrow * 128 + ((((lane >> 4) & 1) ^ (lrow & 7)) << 4));
   if (threadIdx.x == 0) fetch(0);
@@ -452,13 +450,17 @@ __global__ void __launch_bounds__((NW + 1) * 32,
             if (nv[j] == 0) continue;
             const uint32_t kj = kst + (uint32_t)(j * 2 * L::kTile);
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-              const uint32_t w0 = lds32(kj + (koffA ^ (uint32_t)(kk << 4)));
-              const uint32_t w1 = lds32(kj + (koffB ^ (uint32_t)(kk << 4)));
-              uint32_t a0, a1, a2, a3;
-              e4m3x4_to_f16x2x2(w0, a0, a2);
-              e4m3x4_to_f16x2x2(w1, a1, a3);
-              mma16816_f16(sc[j], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            for (int kk = 0; kk < KSTEPS; kk += 2) {
+              uint32_t w[4];  // (tokA, kk), (tokB, kk), (tokA, kk + 1), (tokB, kk + 1)
+              ldsm_x4(kj + krow8 + ((((uint32_t)kk + kstep8) ^ kkey8) << 4), w[0], w[1], w[2],
+                      w[3]);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(w[2 * h], a0, a2);
+                e4m3x4_to_f16x2x2(w[2 * h + 1], a1, a3);
+                mma16816_f16(sc[j], a0, a1, a2, a3, qb[kk + h][0], qb[kk + h][1]);
+              }
             }
           }
           float x[2][4];
@@ -504,13 +506,16 @@ __global__ void __launch_bounds__((NW + 1) * 32,
           // past the end of the context are masked to +0.
           auto pv8 = [&](uint32_t vst, uint32_t b0, uint32_t b1, uint32_t vmask) {
 #pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) {
-              const uint32_t w0 = lds32(vst + (16 * mt + gid) * 16 + 4 * tig) & vmask;
-              const uint32_t w1 = lds32(vst + (16 * mt + gid + 8) * 16 + 4 * tig) & vmask;
-              uint32_t a0, a1, a2, a3;
-              e4m3x4_to_f16x2x2(w0, a0, a2);
-              e4m3x4_to_f16x2x2(w1, a1, a3);
-              mma16816_f16(acc[mt], a0, a1, a2, a3, b0, b1);
+            for (int mt = 0; mt < KSTEPS; mt += 2) {
+              uint32_t w[4];  // d rows (16 mt + gid, + 8) of m-tiles mt and mt + 1
+              ldsm_x4(vst + (uint32_t)(mt * 256) + vrow8, w[0], w[1], w[2], w[3]);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(w[2 * h] & vmask, a0, a2);
+                e4m3x4_to_f16x2x2(w[2 * h + 1] & vmask, a1, a3);
+                mma16816_f16(acc[mt + h], a0, a1, a2, a3, b0, b1);
+              }
             }
           };
 #pragma unroll

@@ -135,6 +135,7 @@ class ServingDriver:
         self.d2h_bytes = 0
         self.on_decode = None  # optional hook(0 before / 1 after) around decode attention
         self.on_start = None   # optional hook called before the step's first copy
+        self.start_event = None  # packed path: optional event recorded before the first copy
 
     def add_request(self, rid: int, prompt, output_len: int) -> None:
         self.prompts[rid] = np.ascontiguousarray(prompt, dtype=np.int32)
@@ -369,8 +370,8 @@ class ServingDriver:
         T = pk.num_tokens
         if T == 0:
             return None, None
-        if self.on_start is not None:
-            self.on_start()
+        if self.start_event is not None:  # a timing event recorded before the step's copy
+            self.start_event.record(self.stream)
         self.f_dev.copy_(self.f_host[slot], non_blocking=True)
         self.h2d_bytes += self.f_bytes
         dv = self.f_dv
