@@ -333,11 +333,14 @@ class ServingDriver:
         self.f_knew = torch.empty(T, self.Hkv, self.D, dtype=torch.bfloat16, device=self.dev)
         self.f_vnew = torch.empty_like(self.f_knew)
         self.f_q = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
-        self.f_dec = torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        # what a sampler reads, in one device buffer: the decode rows, then the last row
+        # of each prefill chunk (copied to the host in one copy)
+        self.f_out = torch.empty(2 * S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_dec = self.f_out[:S]
         self.f_pre = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
-        self.f_last = torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
-        self.f_out_h = [[torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16).pin_memory()
-                         for _ in range(2)] for _ in range(2)]
+        self.f_out_h = [torch.empty(2 * S, self.Hq, self.D, dtype=torch.bfloat16).pin_memory()
+                        for _ in range(2)]
+        self.f_views = {}  # per token count: the step tensors' views
         self.f_row = self.Hq * self.D * 2  # bytes of one q / output row
         self.f_krow = self.Hkv * self.D * 2
         NB = self.k_cache.shape[0]
@@ -375,10 +378,14 @@ class ServingDriver:
         self.f_dev.copy_(self.f_host[slot], non_blocking=True)
         self.h2d_bytes += self.f_bytes
         dv = self.f_dv
-        k_new, v_new, q = self.f_knew[:T], self.f_vnew[:T], self.f_q[:T]
-        torch.index_select(self.k_tab_d, 0, dv["kvr"][:T], out=k_new)
-        torch.index_select(self.v_tab_d, 0, dv["kvr"][:T], out=v_new)
-        torch.index_select(self.q_tab_d, 0, dv["qr"][:T], out=q)
+        views = self.f_views.get(T)
+        if views is None:  # slicing costs host time: the views are kept per token count
+            views = (self.f_knew[:T], self.f_vnew[:T], self.f_q[:T], dv["kvr"][:T], dv["qr"][:T])
+            self.f_views[T] = views
+        k_new, v_new, q, kvr, qr = views
+        torch.index_select(self.k_tab_d, 0, kvr, out=k_new)
+        torch.index_select(self.v_tab_d, 0, kvr, out=v_new)
+        torch.index_select(self.q_tab_d, 0, qr, out=q)
         n, nd = pk.num_seqs, pk.num_decode
         kc, vc, NB, Hq, Hkv, D, bs, scale = self.f_const
         ptr, st = self.f_ptr, self.stream.cuda_stream
@@ -398,14 +405,8 @@ class ServingDriver:
                 1 if pk.num_cow > 1024 else 0)
         else:  # no decode entry: the copies and the write alone
             self.launches += (1 if pk.num_cow else 0) + 1
-        outs = self.f_out_h[slot]
-        dec_h = last_h = None
-        if nd:
-            dec_h = outs[0][:nd]
-            dec_h.copy_(self.f_dec[:nd], non_blocking=True)
-            self.d2h_bytes += nd * self.f_row
-        if n > nd:
-            ch = n - nd
+        ch = n - nd
+        if ch:
             pre = self.f_pre[:T - nd]
             ops.check(ops.lib.paged_attention_prefill(
                 pre.data_ptr(), qp + nd * self.f_row, kc, vc,
@@ -413,9 +414,9 @@ class ServingDriver:
                 ptr["prefill_start"], ch, T - nd, self.f_stride, Hq, Hkv, D, bs, NB, scale,
                 pk.prefill_max_query, self.err.data_ptr(), st), "paged_attention_prefill")
             self.launches += 1
-            last = self.f_last[:ch]
-            torch.index_select(pre, 0, dv["last"][:ch], out=last)
-            last_h = outs[1][:ch]
-            last_h.copy_(last, non_blocking=True)
-            self.d2h_bytes += ch * self.f_row
-        return dec_h, last_h
+            torch.index_select(pre, 0, dv["last"][:ch], out=self.f_out[nd:nd + ch])
+        # one copy of the decode rows and the chunks' last rows
+        out_h = self.f_out_h[slot][:n]
+        out_h.copy_(self.f_out[:n], non_blocking=True)
+        self.d2h_bytes += n * self.f_row
+        return (out_h[:nd] if nd else None), (out_h[nd:] if ch else None)
