@@ -22,6 +22,7 @@ whole step (algorithmic flops: 4 head_dim per visible (query row, key) pair).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -951,10 +952,6 @@ def serve_run(drv, stream, decode_bytes_per_token):
     scheduler's decisions do not depend on the sampled values.  Returns timing and
     counts."""
     tot = dict(dev_ms=0.0, dec_ms=0.0, dec_bytes=0, steps=0, outs=0)
-    cur = {}
-    # The decode attention is timed on every 4th step (its events cost host time every
-    # step they are recorded); the roofline uses the bytes and times of those steps.
-    drv.on_decode = lambda k: cur["dec"] is not None and cur["dec"][k].record(stream)
 
     def retire(item):
         pk, slot, b_prev, b, dev_pair = item
@@ -965,16 +962,24 @@ def serve_run(drv, stream, decode_bytes_per_token):
         nd = pk.num_decode
         if nd and dev_pair is not None:
             tot["dec_ms"] += dev_pair[0].elapsed_time(dev_pair[1])
-            ctx = drv.f_np[slot]["ctx"][:nd]
+            ctx = drv.f_np[slot][:nd]
             tot["dec_bytes"] += int(ctx.sum(dtype=np.int64)) * decode_bytes_per_token
 
     # Timing events, reused: a set is free again once its step has retired.  A step's
     # device time runs from its first copy to its last (GPU idle time between steps is
-    # not counted).
+    # not counted).  The decode attention is timed on every 4th step (events cost host
+    # time on every step they are recorded); the roofline uses those steps' bytes and
+    # times.  The native step call records them (handles passed as a ctypes array).
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(4)]
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(4)]
+    ev_dec = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for e in [x for pair in ev for x in pair] + list(ev_dec):
+        e.record(stream)  # creates the event, so that its handle exists
+    stream.synchronize()
+    handles = [(ctypes.c_void_p * 3)(ev[k][0].cuda_event,
+                                      ev_dec[0].cuda_event if k == 0 else None,
+                                      ev_dec[1].cuda_event if k == 0 else None)
+               for k in range(4)]
     t0 = time.perf_counter()
     slot, pending, k = 0, [], 0
     while not drv.done():
@@ -982,20 +987,16 @@ def serve_run(drv, stream, decode_bytes_per_token):
         if pk.num_tokens == 0:  # nothing to compute this step
             continue
         a, b = ev[k % 4]
-        cur["dec"] = ev_dec[k % 4] if k % 4 == 0 else None
-        k += 1
-        drv.start_event = a
-        drv.launch_packed(pk, slot)
+        drv.launch_packed(pk, slot, handles[k % 4])
         b.record(stream)
-        pending.append((pk, slot, a, b, cur["dec"]))
+        pending.append((pk, slot, a, b, ev_dec if k % 4 == 0 else None))
+        k += 1
         slot ^= 1
         if len(pending) == 2:
             retire(pending.pop(0))
     while pending:
         retire(pending.pop(0))
     wall = time.perf_counter() - t0
-    drv.on_decode = None
-    drv.start_event = None
     return dict(wall_s=wall, device_ms=tot["dev_ms"], decode_ms=tot["dec_ms"],
                 decode_bytes=tot["dec_bytes"], steps=tot["steps"], output_tokens=tot["outs"])
 

@@ -66,12 +66,14 @@ extern "C" {
 #define PKV_DEV_TIMEOUT 8        /* a bounded wait inside a kernel gave up            */
 #define PKV_DEV_LAYOUT 16        /* shared-memory window misaligned (kernel skipped)  */
 #define PKV_DEV_BAD_SCALE 32     /* a per-KV-head E4M3 scale is not > 0               */
+#define PKV_DEV_BAD_ROW 64       /* a gathered row index outside its table            */
 
 /* Library ABI version: PKV_ABI_VERSION of the build (incremented when an entry point is
  * added or a signature changes).  2 added paged_kv_write_fp8_per_head,
  * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load; 3 added
- * paged_decode_step, paged_decode_step_fp8 and pkv_sched_pack. */
-#define PKV_ABI_VERSION 3
+ * paged_decode_step, paged_decode_step_fp8 and pkv_sched_pack; 4 added
+ * paged_gather_rows and pkv_step_launch. */
+#define PKV_ABI_VERSION 4
 int paged_kv_version(void);
 
 /* Human-readable text of a PKV_ERR_* code. Never NULL; static storage. */
@@ -211,8 +213,8 @@ int paged_block_copy_fp8(uint8_t *k_cache, uint8_t *v_cache, const int32_t *bloc
  * decode(code) * k_scale and every V element decode(code) * v_scale.  The scores are
  * formed on tensor cores in f16 (E4M3 codes convert to f16 exactly; q is rounded
  * bf16 -> f16, exact for 2^-14 <= |q| <= 65504) with fp32 accumulation; the softmax
- * weights enter the P.V tile as f16.  head_dim must be 128.  The workspace is the one
- * paged_attention_workspace_size gives. */
+ * weights enter the P.V tile as f16.  head_dim 64 or 128 (else PKV_ERR_SHAPE).  The
+ * workspace is the one paged_attention_workspace_size gives. */
 int paged_attention_decode_fp8(uint16_t *out, const uint16_t *q, const uint8_t *k_cache,
                                const uint8_t *v_cache, const int32_t *block_tables,
                                const int32_t *context_lens, int num_seqs,
@@ -243,7 +245,7 @@ int paged_attention_decode_fp8_per_head(uint16_t *out, const uint16_t *q, const 
  * then E4M3 decode attention, as one call (see paged_decode_step).  Scales: k_scales and
  * v_scales both non-NULL selects one scale per KV head (the _per_head calls' semantics;
  * k_scale and v_scale are then ignored), both NULL one scale per cache (k_scale, v_scale
- * > 0, else PKV_ERR_SHAPE); one NULL and one not returns PKV_ERR_NULL.  head_dim must be
+ * > 0, else PKV_ERR_SHAPE); one NULL and one not returns PKV_ERR_NULL.  head_dim 64 or
  * 128. */
 int paged_decode_step_fp8(uint16_t *out, const uint16_t *q, uint8_t *k_cache, uint8_t *v_cache,
                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
@@ -541,6 +543,68 @@ int pkv_sched_pack(const pkv_sched *sched, void *buf, int64_t buf_bytes, int max
  * (token * 1000003 + pos * 7919) mod table_rows, and of its query,
  * (rid * 2654435761 + pos * 40503) mod table_rows.  Not part of the method. */
 int pkv_step_synthetic_rows(void *buf, const pkv_step_pack *pack, int64_t table_rows);
+
+/*
+ * paged_gather_rows -- dst row i = src row idx[i] for i < n, rows of row_bytes bytes (a
+ * multiple of 16; dst and src 16-byte aligned, device memory; idx int64 [n], device).
+ * An index outside [0, src_rows) sets PKV_DEV_BAD_ROW and leaves that destination row
+ * unwritten.  n == 0 does nothing.  PKV_ERR_SHAPE when n * row_bytes / 16 >= 2^31.
+ * The serving step uses it to pick each chunk's last prefill row and the synthetic
+ * model's q/K/V rows.
+ */
+int paged_gather_rows(void *dst, const void *src, const int64_t *idx, int n, int64_t src_rows,
+                      int row_bytes, int32_t *err_flag, void *stream);
+
+/*
+ * pkv_step_launch -- the device half of one packed serving step, queued on `stream` by
+ * one call (the loop of "Continuous batching and PagedAttention", section 2: every step
+ * runs the decode entries and the prefill chunks the scheduler picked):
+ *   1. one copy of the packed step (pack->total bytes, pkv_sched_pack) from
+ *      io->host_stage[slot] to io->dev_stage;
+ *   2. if io->k_table != NULL (the synthetic model): one launch gathering, per new token
+ *      t, k_new[t] = k_table[kv_rows[t]], v_new[t] = v_table[kv_rows[t]] and
+ *      q[t] = q_table[q_rows[t]] (pkv_step_synthetic_rows); with k_table NULL the
+ *      caller has filled k_new, v_new and q (rows in the pack's token order);
+ *   3. paged_decode_step: the step's copy-on-write pairs, the paged write of every new
+ *      token, decode attention of the num_decode decode entries into out rows
+ *      0 .. num_decode - 1;
+ *   4. with prefill chunks: paged_attention_prefill of the chunk rows (new tokens
+ *      num_decode .. num_tokens - 1) into prefill_out, then the last row of chunk c
+ *      gathered into out row num_decode + c;
+ *   5. one copy of out rows 0 .. num_seqs - 1 to io->out_host[slot].
+ * events: NULL, or three cudaEvent_t (each may be NULL) recorded on the stream before
+ * step 1, before step 3 and after step 3.  All buffers are the caller's and stay
+ * untouched by the host; host_stage[slot] and out_host[slot] must be pinned and must
+ * not be reused before the stream has passed this step.  A pack with more tokens or
+ * sequences than io's capacities, or a total above stage_bytes, returns PKV_ERR_SHAPE
+ * and queues nothing; otherwise the first failing call's code is returned and nothing
+ * after it is queued.  Device-side errors are ORed into io->err_flag as by the calls.
+ */
+typedef struct {
+  void *host_stage[2];        /* pinned staging buffers, one per in-flight step        */
+  void *dev_stage;            /* device copy of a staging buffer (stage_bytes)         */
+  int64_t stage_bytes;
+  const uint16_t *k_table;    /* bf16 [table_rows][num_kv_heads][head_dim], or NULL    */
+  const uint16_t *v_table;    /* bf16 [table_rows][num_kv_heads][head_dim]             */
+  const uint16_t *q_table;    /* bf16 [table_rows][num_q_heads][head_dim]              */
+  int64_t table_rows;
+  uint16_t *k_new, *v_new;    /* bf16 [max_tokens][num_kv_heads][head_dim]             */
+  uint16_t *q;                /* bf16 [max_tokens][num_q_heads][head_dim]              */
+  uint16_t *prefill_out;      /* bf16 [max_tokens][num_q_heads][head_dim]              */
+  uint16_t *out;              /* bf16 [max_seqs][num_q_heads][head_dim], device        */
+  uint16_t *out_host[2];      /* the same shape, pinned host, one per in-flight step   */
+  uint16_t *k_cache, *v_cache;/* bf16 [num_blocks][num_kv_heads][16][head_dim]         */
+  int max_tokens, max_seqs;   /* capacities (the pkv_sched_pack capacities)            */
+  int num_blocks, num_q_heads, num_kv_heads, head_dim, block_size;
+  int table_stride;           /* entries per block-table row in the pack               */
+  int partition_size;
+  float scale;
+  void *workspace;            /* decode workspace for max_seqs sequences               */
+  size_t workspace_bytes;
+  int32_t *err_flag;          /* device word (may be NULL)                             */
+} pkv_step_io;
+int pkv_step_launch(const pkv_step_io *io, const pkv_step_pack *pack, int slot,
+                    void *const *events, void *stream);
 int pkv_sched_done(const pkv_sched *sched);  /* 1 when no request is waiting or running */
 int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
 

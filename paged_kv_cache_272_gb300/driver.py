@@ -135,7 +135,6 @@ class ServingDriver:
         self.d2h_bytes = 0
         self.on_decode = None  # optional hook(0 before / 1 after) around decode attention
         self.on_start = None   # optional hook called before the step's first copy
-        self.start_event = None  # packed path: optional event recorded before the first copy
 
     def add_request(self, rid: int, prompt, output_len: int) -> None:
         self.prompts[rid] = np.ascontiguousarray(prompt, dtype=np.int32)
@@ -299,11 +298,11 @@ class ServingDriver:
         return x, dec, pre
 
     # ---- the packed path: the plan written straight into pinned staging by the native
-    # scheduler (pkv_sched_pack), fixed offsets, device views and call arguments made
-    # once; the library is called directly with them (the buffers are the driver's own,
-    # sized for the capacities, so the wrappers' per-call checks are not needed) --------
+    # scheduler (pkv_sched_pack) at fixed offsets, and the device half of each step
+    # queued by one native call (pkv_step_launch) over buffers made once, sized for the
+    # capacities --------------------------------------------------------------------
     def _fast_setup(self):
-        from .serving import StepPack
+        from .serving import StepIO, StepPack
         self.f_tokens = self.sched.max_batched_tokens + self.sched.max_num_seqs
         self.f_seqs = self.sched.max_num_seqs
         self.f_stride = (self.max_context + BS - 1) // BS
@@ -312,40 +311,44 @@ class ServingDriver:
             self.sched.pack(None, 0, self.f_tokens, self.f_seqs, self.f_stride, lay)
         except ops.PagedKVError:
             pass
-        self.f_lay = lay
         self.f_bytes = lay.total
         self.f_host = [torch.empty(self.f_bytes, dtype=torch.uint8).pin_memory()
                        for _ in range(2)]
         self.f_dev = torch.empty(self.f_bytes, dtype=torch.uint8, device=self.dev)
         self.f_packs = [StepPack(), StepPack()]
         T, S = self.f_tokens, self.f_seqs
-
-        def v(buf, off, n, dt):
-            return buf[off:off + n * torch.empty(0, dtype=dt).element_size()].view(dt)
-        self.f_np = [dict(ctx=v(h, lay.context_lens, S, torch.int32).numpy()) for h in self.f_host]
-        d = self.f_dev
-        self.f_dv = dict(kvr=v(d, lay.kv_rows, T, torch.int64), qr=v(d, lay.q_rows, T, torch.int64),
-                         last=v(d, lay.last_rows, S, torch.int64))
-        base = d.data_ptr()
-        self.f_ptr = {k: base + getattr(lay, k) for k in
-                      ("slot_mapping", "block_tables", "context_lens", "cow_pairs",
-                       "prefill_start")}
+        # the staging's context lengths, per slot (read by callers that count bytes)
+        self.f_np = [h[lay.context_lens:lay.context_lens + 4 * S].view(torch.int32).numpy()
+                     for h in self.f_host]
         self.f_knew = torch.empty(T, self.Hkv, self.D, dtype=torch.bfloat16, device=self.dev)
         self.f_vnew = torch.empty_like(self.f_knew)
         self.f_q = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_pre = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
         # what a sampler reads, in one device buffer: the decode rows, then the last row
         # of each prefill chunk (copied to the host in one copy)
-        self.f_out = torch.empty(2 * S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
-        self.f_dec = self.f_out[:S]
-        self.f_pre = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
-        self.f_out_h = [torch.empty(2 * S, self.Hq, self.D, dtype=torch.bfloat16).pin_memory()
+        self.f_out = torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16, device=self.dev)
+        self.f_out_h = [torch.empty(S, self.Hq, self.D, dtype=torch.bfloat16).pin_memory()
                         for _ in range(2)]
-        self.f_views = {}  # per token count: the step tensors' views
         self.f_row = self.Hq * self.D * 2  # bytes of one q / output row
-        self.f_krow = self.Hkv * self.D * 2
         NB = self.k_cache.shape[0]
-        self.f_const = (self.k_cache.data_ptr(), self.v_cache.data_ptr(), NB, self.Hq, self.Hkv,
-                        self.D, BS, ctypes.c_float(self.scale))
+        io = StepIO()
+        io.host_stage[0], io.host_stage[1] = (h.data_ptr() for h in self.f_host)
+        io.dev_stage, io.stage_bytes = self.f_dev.data_ptr(), self.f_bytes
+        io.k_table, io.v_table = self.k_tab_d.data_ptr(), self.v_tab_d.data_ptr()
+        io.q_table, io.table_rows = self.q_tab_d.data_ptr(), self.rows
+        io.k_new, io.v_new, io.q = (t.data_ptr() for t in (self.f_knew, self.f_vnew, self.f_q))
+        io.prefill_out, io.out = self.f_pre.data_ptr(), self.f_out.data_ptr()
+        io.out_host[0], io.out_host[1] = (h.data_ptr() for h in self.f_out_h)
+        io.k_cache, io.v_cache = self.k_cache.data_ptr(), self.v_cache.data_ptr()
+        io.max_tokens, io.max_seqs, io.num_blocks = T, S, NB
+        io.num_q_heads, io.num_kv_heads, io.head_dim = self.Hq, self.Hkv, self.D
+        io.block_size, io.table_stride, io.partition_size = BS, self.f_stride, self.P
+        io.scale = self.scale
+        io.workspace, io.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
+        io.err_flag = self.err.data_ptr()
+        self.f_io = io
+        self.f_io_ref = ctypes.byref(io)
+        self.f_stream = ctypes.c_void_p(self.stream.cuda_stream)
 
     def plan_packed(self, slot=0):
         """Host part of one step on the packed path: the native scheduler steps, packs its
@@ -363,60 +366,31 @@ class ServingDriver:
                       "pkv_step_synthetic_rows")
         return pk
 
-    def launch_packed(self, pk, slot=0):
-        """Device part of a packed step, queued on the stream: one host-to-device copy,
-        the row gathers, paged_decode_step (copies, write, decode attention) and the
-        prefill call, then the copies of what a sampler reads (every decode row, the
-        last row of every prefill chunk) into pinned buffers of `slot`.  Returns
+    def launch_packed(self, pk, slot=0, events=None):
+        """Device part of a packed step, queued on the stream by one native call
+        (pkv_step_launch): the copy of the packed plan, the synthetic model's row gathers,
+        paged_decode_step (copies, write, decode attention), the prefill call, the
+        gather of each chunk's last row and one copy of what a sampler reads (every
+        decode row, the last row of every prefill chunk) into pinned buffers of `slot`.
+        events: None or a ctypes array of three cudaEvent_t handles (each may be None)
+        recorded before the first copy, before and after the decode step.  Returns
         (decode rows, prefill last rows) as host tensors, valid once the stream reaches
         this point."""
         T = pk.num_tokens
         if T == 0:
             return None, None
-        if self.start_event is not None:  # a timing event recorded before the step's copy
-            self.start_event.record(self.stream)
-        self.f_dev.copy_(self.f_host[slot], non_blocking=True)
-        self.h2d_bytes += self.f_bytes
-        dv = self.f_dv
-        views = self.f_views.get(T)
-        if views is None:  # slicing costs host time: the views are kept per token count
-            views = (self.f_knew[:T], self.f_vnew[:T], self.f_q[:T], dv["kvr"][:T], dv["qr"][:T])
-            self.f_views[T] = views
-        k_new, v_new, q, kvr, qr = views
-        torch.index_select(self.k_tab_d, 0, kvr, out=k_new)
-        torch.index_select(self.v_tab_d, 0, kvr, out=v_new)
-        torch.index_select(self.q_tab_d, 0, qr, out=q)
+        ops.check(ops.lib.pkv_step_launch(self.f_io_ref, ctypes.byref(pk), slot, events,
+                                          self.f_stream), "pkv_step_launch")
         n, nd = pk.num_seqs, pk.num_decode
-        kc, vc, NB, Hq, Hkv, D, bs, scale = self.f_const
-        ptr, st = self.f_ptr, self.stream.cuda_stream
-        if self.on_decode is not None:
-            self.on_decode(0)
-        qp, dec_p = q.data_ptr(), self.f_dec.data_ptr()
-        ops.check(ops.lib.paged_decode_step(
-            dec_p, qp, kc, vc, ptr["block_tables"], ptr["context_lens"], nd, self.f_stride, Hq,
-            Hkv, D, bs, NB, scale, self.P, pk.decode_max_context, k_new.data_ptr(),
-            v_new.data_ptr(), ptr["slot_mapping"], T, ptr["cow_pairs"] if pk.num_cow else None,
-            pk.num_cow, self.ws.data_ptr(), self.ws.numel(), self.err.data_ptr(), st),
-            "paged_decode_step")
-        if self.on_decode is not None:
-            self.on_decode(1)
-        if nd:  # prologue (copies, write, plan), partition kernel, merge if split
-            self.launches += 2 + (1 if pk.decode_max_context > self.P else 0) + (
-                1 if pk.num_cow > 1024 else 0)
-        else:  # no decode entry: the copies and the write alone
-            self.launches += (1 if pk.num_cow else 0) + 1
-        ch = n - nd
-        if ch:
-            pre = self.f_pre[:T - nd]
-            ops.check(ops.lib.paged_attention_prefill(
-                pre.data_ptr(), qp + nd * self.f_row, kc, vc,
-                ptr["block_tables"] + nd * self.f_stride * 4, ptr["context_lens"] + nd * 4,
-                ptr["prefill_start"], ch, T - nd, self.f_stride, Hq, Hkv, D, bs, NB, scale,
-                pk.prefill_max_query, self.err.data_ptr(), st), "paged_attention_prefill")
-            self.launches += 1
-            torch.index_select(pre, 0, dv["last"][:ch], out=self.f_out[nd:nd + ch])
-        # one copy of the decode rows and the chunks' last rows
-        out_h = self.f_out_h[slot][:n]
-        out_h.copy_(self.f_out[:n], non_blocking=True)
+        self.h2d_bytes += pk.total
         self.d2h_bytes += n * self.f_row
-        return (out_h[:nd] if nd else None), (out_h[nd:] if ch else None)
+        launches = 1  # the row gathers
+        if nd:  # prologue (copies, write, plan), partition, merge if split, extra copies
+            launches += 2 + (pk.decode_max_context > self.P) + (pk.num_cow > 1024)
+        else:  # no decode entry: the copies (if any) and the write alone
+            launches += 1 + (pk.num_cow > 0)
+        if n > nd:  # the prefill and its last-row gather
+            launches += 2
+        self.launches += launches
+        out_h = self.f_out_h[slot]
+        return (out_h[:nd] if nd else None), (out_h[nd:n] if n > nd else None)

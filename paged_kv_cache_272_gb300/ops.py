@@ -18,13 +18,13 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
 PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
-DEV_BAD_SCALE = 32
+DEV_BAD_SCALE, DEV_BAD_ROW = 32, 64
 DEFAULT_PARTITION = 512
 
 # Every entry point the header declares: name -> (restype, argtypes).
 _P, _I, _F, _SZ, _I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
                          ctypes.c_int64)
-ABI_VERSION = 3  # PKV_ABI_VERSION of include/pagedkv.h
+ABI_VERSION = 4  # PKV_ABI_VERSION of include/pagedkv.h
 SIGNATURES = {
     "paged_kv_version": (_I, []),
     "paged_kv_strerror": (ctypes.c_char_p, [_I]),
@@ -85,6 +85,8 @@ SIGNATURES = {
     "pkv_sched_done": (_I, [_P]),
     "pkv_sched_pack": (_I, [_P, _P, _I64, _I, _I, _I, _P]),
     "pkv_step_synthetic_rows": (_I, [_P, _P, _I64]),
+    "paged_gather_rows": (_I, [_P, _P, _P, _I, _I64, _I, _P, _P]),
+    "pkv_step_launch": (_I, [_P, _P, _I, _P, _P]),
     "pkv_sched_get_stats": (_I, [_P, _P]),
     "pkv_selftest_bounded_wait": (_I, [_P, _P, ctypes.c_longlong, _I, _P]),
 }
@@ -173,6 +175,20 @@ def paged_block_copy(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
     P = block_pairs.numel() // 2
     check(lib.paged_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), P, NB, Hkv, D,
                                bs, _ptr(err_flag), _stream(stream)), "paged_block_copy")
+
+
+def paged_gather_rows(dst, src, idx, err_flag=None, stream=None):
+    """dst[i] = src[idx[i]] for i < len(idx): whole rows (the leading dimension) of
+    contiguous CUDA tensors of one dtype; idx int64."""
+    if not (dst.is_cuda and src.is_cuda and idx.is_cuda) or dst.dtype != src.dtype:
+        raise ValueError("dst, src and idx must be CUDA tensors; dst and src of one dtype")
+    if idx.dtype != torch.int64 or not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("idx must be int64; dst and src contiguous")
+    row = src[0].numel() * src.element_size() if src.shape[0] else 0
+    if dst.shape[1:] != src.shape[1:] or dst.shape[0] < idx.numel():
+        raise ValueError("dst rows must match src rows and hold len(idx) rows")
+    check(lib.paged_gather_rows(_ptr(dst), _ptr(src), _ptr(idx), idx.numel(), src.shape[0], row,
+                                _ptr(err_flag), _stream(stream)), "paged_gather_rows")
 
 
 def paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,

@@ -40,6 +40,21 @@ class StepPack(ctypes.Structure):
                 ("outputs", ctypes.c_int)]
 
 
+class StepIO(ctypes.Structure):
+    """Buffers and constants of the device half of a packed step (pkv_step_io)."""
+    _P = ctypes.c_void_p
+    _fields_ = [("host_stage", _P * 2), ("dev_stage", _P), ("stage_bytes", ctypes.c_int64),
+                ("k_table", _P), ("v_table", _P), ("q_table", _P),
+                ("table_rows", ctypes.c_int64), ("k_new", _P), ("v_new", _P), ("q", _P),
+                ("prefill_out", _P), ("out", _P), ("out_host", _P * 2), ("k_cache", _P),
+                ("v_cache", _P), ("max_tokens", ctypes.c_int), ("max_seqs", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("table_stride", ctypes.c_int),
+                ("partition_size", ctypes.c_int), ("scale", ctypes.c_float),
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("err_flag", _P)]
+
+
 class SchedStats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("finished", ctypes.c_int64),
                 ("preemptions", ctypes.c_int64), ("decode_tokens", ctypes.c_int64),

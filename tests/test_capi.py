@@ -231,3 +231,68 @@ def test_decode_step_host_validation():
     assert lib.paged_decode_step_fp8(*st8(k=0.0)) == -2       # per-cache scale not > 0
     assert lib.paged_decode_step_fp8(*st8(ks=fake)) == -1     # one per-head array only
     assert lib.paged_decode_step_fp8(*st8(D=96)) == -2
+
+
+def _c_layout(struct: str, fields):
+    """(sizeof, {field: offsetof}) of a header struct, from a C program compiled with gcc."""
+    import subprocess
+    import tempfile
+    body = "".join(f'  printf(" %zu", offsetof({struct}, {f}));\n' for f in fields)
+    src = ("#include <stddef.h>\n#include <stdio.h>\n#include \"pagedkv.h\"\n"
+           f"int main(void) {{\n  printf(\"%zu\", sizeof({struct}));\n{body}"
+           "  printf(\"\\n\");\n  return 0;\n}\n")
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(c, "w") as f:
+            f.write(src)
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), c, "-o", exe],
+                       check=True)
+        vals = [int(x) for x in subprocess.run([exe], check=True, capture_output=True,
+                                               text=True).stdout.split()]
+    return vals[0], dict(zip(fields, vals[1:]))
+
+
+@pytest.mark.parametrize("struct,pyname", [("pkv_step_io", "StepIO"),
+                                           ("pkv_step_pack", "StepPack"),
+                                           ("pkv_sched_stats", "SchedStats")])
+def test_struct_layouts_match_the_header(struct, pyname):
+    """The ctypes mirrors of the header's structs have the C compiler's size and field
+    offsets (a mismatch would hand the library shifted pointers)."""
+    from paged_kv_cache_272_gb300 import serving
+    py = getattr(serving, pyname)
+    names = [f[0] for f in py._fields_]
+    size, offs = _c_layout(struct, names)
+    assert ctypes.sizeof(py) == size
+    for n in names:
+        assert getattr(py, n).offset == offs[n], (struct, n)
+
+
+def test_step_launch_and_gather_host_validation():
+    """pkv_step_launch and paged_gather_rows reject bad arguments on the host, before
+    anything is queued (so this runs without a GPU)."""
+    from paged_kv_cache_272_gb300 import ops
+    from paged_kv_cache_272_gb300.serving import StepIO, StepPack
+    lib = ops.lib
+    fake = 1 << 20
+    # gather: row size not a multiple of 16, null, misaligned, too many vectors, n == 0
+    assert lib.paged_gather_rows(fake, fake, fake, 4, 10, 24, None, None) == -2
+    assert lib.paged_gather_rows(None, fake, fake, 4, 10, 32, None, None) == -1
+    assert lib.paged_gather_rows(fake + 8, fake, fake, 4, 10, 32, None, None) == -4
+    assert lib.paged_gather_rows(fake, fake, fake, 1 << 21, 10, 1 << 14, None, None) == -2
+    assert lib.paged_gather_rows(fake, fake, fake, 4, 0, 32, None, None) == -2
+    assert lib.paged_gather_rows(None, None, None, 0, 10, 32, None, None) == 0
+    io, pk = StepIO(), StepPack()
+    io.max_tokens, io.max_seqs, io.stage_bytes = 64, 8, 4096
+    pk.total, pk.num_tokens, pk.num_seqs, pk.num_decode = 1024, 16, 4, 2
+    assert lib.pkv_step_launch(None, ctypes.byref(pk), 0, None, None) == -1
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 2, None, None) == -14
+    pk.num_tokens = 65  # above the capacity
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -2
+    pk.num_tokens, pk.num_decode = 16, 5  # more decode entries than sequences
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -2
+    pk.num_decode, pk.total = 2, 8192  # pack larger than the staging buffer
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -2
+    pk.total = 1024  # buffers missing
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -1
+    pk.num_tokens = 0  # nothing to do
+    assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == 0

@@ -159,3 +159,30 @@ def test_packed_path_equals_the_checked_path(cache_entries, blocks):
     assert int(a.err.item()) == 0 and int(b.err.item()) == 0
     assert torch.equal(a.k_cache.view(torch.int16), b.k_cache.view(torch.int16))
     assert torch.equal(a.v_cache.view(torch.int16), b.v_cache.view(torch.int16))
+
+
+def test_gather_rows_bit_exact_and_flags_bad_rows():
+    """paged_gather_rows moves whole rows bit for bit; a row index outside the table sets
+    PKV_DEV_BAD_ROW and leaves that destination row as it was."""
+    from paged_kv_cache_272_gb300 import ops
+    g = torch.Generator().manual_seed(9)
+    src = torch.randint(-32768, 32767, (300, 8, 128), generator=g, dtype=torch.int16)
+    idx = torch.randint(0, 300, (517,), generator=g)
+    idx[5], idx[9] = 300, -1
+    dst = torch.zeros(517, 8, 128, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.paged_gather_rows(dst, src.cuda().view(torch.bfloat16), idx.cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == ops.DEV_BAD_ROW
+    ok = torch.ones(517, dtype=torch.bool)
+    ok[5] = ok[9] = False
+    got = dst.cpu().view(torch.int16)
+    assert torch.equal(got[ok], src[idx[ok]])
+    assert (got[~ok] == 0).all()
+    # a one-row table, 16-byte rows, and nothing to gather
+    one = torch.arange(8, dtype=torch.int16).reshape(1, 8)
+    d1 = torch.zeros(3, 8, dtype=torch.int16, device="cuda")
+    ops.paged_gather_rows(d1, one.cuda(), torch.zeros(3, dtype=torch.int64, device="cuda"))
+    ops.paged_gather_rows(d1, one.cuda(), torch.zeros(0, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(d1.cpu(), one.expand(3, 8))
