@@ -141,8 +141,7 @@ int pkv_seq_append_slot(pkv_pool *pool, int64_t seq, int64_t *slot, int32_t *cow
   if (!pool || !slot || !cow_src || !cow_dst) return PKV_ERR_NULL;
   auto it = pool->seqs.find(seq);
   if (it == pool->seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
-  std::unordered_map<int32_t, int> delta;
-  if (pool->demand(it->second, it->second.num_tokens, delta) > (int)pool->free_stack.size())
+  if (pool->demand1(it->second, it->second.num_tokens) > (int)pool->free_stack.size())
     return PKV_ERR_OOM;
   *slot = pool->append(it->second, cow_src, cow_dst);
   return PKV_OK;
@@ -157,13 +156,12 @@ int pkv_seq_append_tokens(pkv_pool *pool, int64_t seq, int count, int64_t *slots
   auto &sq = it->second;
   // Demand: a copy only for the first token (afterwards the block is private), plus
   // one block per block boundary crossed.
-  std::unordered_map<int32_t, int> delta;
   int64_t need = 0;
   if (count > 0) {
     const int64_t n = sq.num_tokens, bs = pool->block_size;
     const int64_t have = (n + bs - 1) / bs, want = (n + count + bs - 1) / bs;
     need = want - have;
-    if (n % bs != 0) need += pool->demand(sq, n, delta);
+    if (n % bs != 0) need += pool->demand1(sq, n);
   }
   if (need > (int64_t)pool->free_stack.size()) return PKV_ERR_OOM;
   int ncow = 0;

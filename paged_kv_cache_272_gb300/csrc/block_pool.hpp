@@ -30,6 +30,13 @@ struct pkv_pool {
     return b;
   }
 
+  // Blocks one append at token position n of one sequence needs (a fresh block at a
+  // block boundary, a copy when the last block is shared, else none).
+  int demand1(const Seq &sq, int64_t n) const {
+    if (n % block_size == 0) return 1;
+    return refcount[sq.table[n / block_size]] > 1 ? 1 : 0;
+  }
+
   // Blocks one append at token position n needs, given pending refcount changes.
   int demand(const Seq &sq, int64_t n, std::unordered_map<int32_t, int> &delta) const {
     if (n % block_size == 0) return 1;

@@ -12,7 +12,8 @@
 // (P - 1) / 16 blocks, so the last prompt token is always computed.  Stamps from one
 // counter order the entries by last use; only leaves are evicted, least recently used
 // first; after an insertion the cache evicts down to max_entries; to free a pool block
-// it evicts a leaf whose block no request holds.
+// it evicts a leaf whose block no request holds.  The leaves are kept ordered by stamp,
+// so an eviction visits leaves oldest first instead of scanning every entry.
 //
 // Scheduler ("Continuous batching and PagedAttention", section 2: iteration-level
 // scheduling -- finished requests leave and waiting requests join at every step --
@@ -27,6 +28,7 @@
 #include <cstring>
 #include <deque>
 #include <new>
+#include <set>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -48,6 +50,8 @@ struct pkv_prefix_cache {
   std::vector<Node> nodes;  // nodes[0] is the root (no block)
   std::vector<int> free_ids;
   std::unordered_map<std::string, int> edges;
+  std::set<std::pair<uint64_t, int>> leaves;  // (stamp, id) of every live leaf
+  mutable std::string probe;  // lookup key buffer (no allocation per lookup)
   uint64_t clock = 0;
   int64_t entries = 0, lookups = 0, hits = 0, query_tokens = 0, matched_tokens = 0,
           evictions = 0;
@@ -60,7 +64,10 @@ struct pkv_prefix_cache {
   }
 
   int child(int parent, const int32_t *toks) const {
-    auto it = edges.find(edge(parent, toks));
+    probe.resize(sizeof(int) + sizeof(int32_t) * bs);
+    std::memcpy(&probe[0], &parent, sizeof(int));
+    std::memcpy(&probe[sizeof(int)], toks, sizeof(int32_t) * bs);
+    auto it = edges.find(probe);
     return it == edges.end() ? -1 : it->second;
   }
 
@@ -78,7 +85,13 @@ struct pkv_prefix_cache {
     return (int)path.size();
   }
 
-  void touch(int id) { nodes[id].stamp = ++clock; }
+  void touch(int id) {
+    Node &nd = nodes[id];
+    const bool leaf = id != 0 && nd.alive && nd.nchild == 0;
+    if (leaf) leaves.erase({nd.stamp, id});
+    nd.stamp = ++clock;
+    if (leaf) leaves.insert({nd.stamp, id});
+  }
 
   void use(const int32_t *toks, int n, int nmatched) {
     std::vector<int> path;
@@ -107,9 +120,12 @@ struct pkv_prefix_cache {
         nd.parent = at;
         nd.nchild = 0;
         nd.alive = true;
+        nd.stamp = 0;
         nd.key = edge(at, toks + (size_t)i * bs);
         edges.emplace(nd.key, c);
+        if (at != 0 && nodes[at].nchild == 0) leaves.erase({nodes[at].stamp, at});
         nodes[at].nchild += 1;
+        leaves.insert({0, c});
         pool->refcount[table[i]] += 1;  // the cache's own reference
         entries += 1;
       }
@@ -124,16 +140,18 @@ struct pkv_prefix_cache {
   // require_free).  Returns false if there is none.
   bool evict(bool require_free) {
     int best = -1;
-    for (int id = 1; id < (int)nodes.size(); ++id) {
-      const Node &nd = nodes[id];
-      if (!nd.alive || nd.nchild != 0) continue;
-      if (require_free && pool->refcount[nd.block] != 1) continue;
-      if (best < 0 || nd.stamp < nodes[best].stamp) best = id;
-    }
+    for (const auto &e : leaves)  // oldest first
+      if (!require_free || pool->refcount[nodes[e.second].block] == 1) {
+        best = e.second;
+        break;
+      }
     if (best < 0) return false;
     Node &nd = nodes[best];
+    leaves.erase({nd.stamp, best});
     edges.erase(nd.key);
-    nodes[nd.parent].nchild -= 1;
+    Node &up = nodes[nd.parent];
+    up.nchild -= 1;
+    if (nd.parent != 0 && up.nchild == 0) leaves.insert({up.stamp, nd.parent});
     pool->release(nd.block);
     nd.alive = false;
     nd.key.clear();
@@ -150,6 +168,7 @@ struct pkv_prefix_cache {
     nodes[0].alive = true;
     free_ids.clear();
     edges.clear();
+    leaves.clear();
     entries = 0;
   }
 };
@@ -159,10 +178,11 @@ struct pkv_sched {
     int64_t id = 0;
     std::vector<int32_t> prompt;  // empty: the request does not use the prefix cache
     int P = 0, O = 0, computed = 0, generated = 0;
+    bool active = false;  // in `running`
   };
   struct Entry {
     int64_t rid;
-    std::vector<int64_t> slots;
+    int off, n;  // its new tokens' slots: step_slots[off .. off + n)
   };
   enum Room { kOk, kSelf, kStuck };
 
@@ -177,15 +197,21 @@ struct pkv_sched {
   std::vector<int32_t> p_qlens, p_ctx, p_qstart, p_tables, p_cow;
   int p_num_decode = 0, p_max_blocks = 1, p_finished = 0, p_preempted = 0;
   pkv_sched_stats st = {};
+  // per-step scratch, kept between steps (no allocation once warm)
+  std::vector<Entry> dec, pre;
+  std::vector<int64_t> step_slots, order;
+  std::vector<int32_t> step_pairs;
 
   bool is_running(int64_t rid) const {
-    return std::find(running.begin(), running.end(), rid) != running.end();
+    auto it = reqs.find(rid);
+    return it != reqs.end() && it->second.active;
   }
 
   void preempt(int64_t rid) {
     pkv_seq_free(pool, rid);
     Req &r = reqs.at(rid);
     r.computed = r.generated = 0;
+    r.active = false;
     running.erase(std::find(running.begin(), running.end(), rid));
     waiting.push_front(rid);
     p_preempted += 1;
@@ -230,9 +256,11 @@ struct pkv_sched {
     }
     int budget = budget_per_step;
     const bool was_empty = running.empty();
-    std::vector<Entry> dec, pre;
+    dec.clear();
+    pre.clear();
+    step_slots.clear();
     // (2) one decode token per request whose prompt is complete
-    std::vector<int64_t> order = running;
+    order = running;
     for (int64_t rid : order) {
       if (!is_running(rid)) continue;
       Req &r = reqs.at(rid);
@@ -251,7 +279,8 @@ struct pkv_sched {
       }
       if (!ok) continue;
       r.computed += 1;
-      dec.push_back({rid, {slot}});
+      step_slots.push_back(slot);
+      dec.push_back({rid, (int)step_slots.size() - 1, 1});
       if (src >= 0) {
         p_cow.push_back(src);
         p_cow.push_back(dst);
@@ -265,13 +294,14 @@ struct pkv_sched {
       Req &r = reqs.at(rid);
       if (r.computed >= r.P || budget <= 0) continue;
       const int chunk = std::min(r.P - r.computed, budget);
-      std::vector<int64_t> slots(chunk);
-      std::vector<int32_t> pairs(2 * (size_t)chunk);
+      const size_t off = step_slots.size();
+      step_slots.resize(off + chunk);
+      step_pairs.resize(2 * (size_t)chunk);
       int ncow = 0;
       bool ok = false;
       while (true) {
-        const int rc =
-            pkv_seq_append_tokens(pool, rid, chunk, slots.data(), pairs.data(), &ncow);
+        const int rc = pkv_seq_append_tokens(pool, rid, chunk, step_slots.data() + off,
+                                             step_pairs.data(), &ncow);
         if (rc == PKV_OK) {
           ok = true;
           break;
@@ -279,10 +309,13 @@ struct pkv_sched {
         if (rc != PKV_ERR_OOM) return rc;
         if (make_room(rid, dec, &pre) != kOk) break;
       }
-      if (!ok) continue;
+      if (!ok) {
+        step_slots.resize(off);
+        continue;
+      }
       r.computed += chunk;
-      pre.push_back({rid, slots});
-      p_cow.insert(p_cow.end(), pairs.begin(), pairs.begin() + 2 * ncow);
+      pre.push_back({rid, (int)off, chunk});
+      p_cow.insert(p_cow.end(), step_pairs.begin(), step_pairs.begin() + 2 * ncow);
       budget -= chunk;
     }
     // (4) admission, first come first served
@@ -309,16 +342,19 @@ struct pkv_sched {
         break;
       }
       if (cached) cache->use(r.prompt.data(), r.P, nm);
-      std::vector<int64_t> slots(chunk);
-      std::vector<int32_t> pairs(2 * (size_t)chunk);
+      const size_t off = step_slots.size();
+      step_slots.resize(off + chunk);
+      step_pairs.resize(2 * (size_t)chunk);
       int ncow = 0;
-      rc = pkv_seq_append_tokens(pool, rid, chunk, slots.data(), pairs.data(), &ncow);
+      rc = pkv_seq_append_tokens(pool, rid, chunk, step_slots.data() + off, step_pairs.data(),
+                                 &ncow);
       if (rc != PKV_OK) return rc;
       r.computed = start + chunk;
       waiting.pop_front();
       running.push_back(rid);
-      pre.push_back({rid, slots});
-      p_cow.insert(p_cow.end(), pairs.begin(), pairs.begin() + 2 * ncow);
+      r.active = true;
+      pre.push_back({rid, (int)off, chunk});
+      p_cow.insert(p_cow.end(), step_pairs.begin(), step_pairs.begin() + 2 * ncow);
       budget -= chunk;
     }
     // (5) sampling: decode entries produce a token; a completed prompt produces its first
@@ -337,9 +373,10 @@ struct pkv_sched {
     for (const std::vector<Entry> *list : {&dec, &pre})
       for (const Entry &e : *list) {
         p_seqs.push_back(e.rid);
-        p_qlens.push_back((int32_t)e.slots.size());
+        p_qlens.push_back((int32_t)e.n);
         p_ctx.push_back(reqs.at(e.rid).computed);
-        p_slots.insert(p_slots.end(), e.slots.begin(), e.slots.end());
+        p_slots.insert(p_slots.end(), step_slots.begin() + e.off,
+                       step_slots.begin() + e.off + e.n);
         p_qstart.push_back((int32_t)p_slots.size());
         p_max_blocks = std::max(p_max_blocks, (int)pool->seqs.at(e.rid).table.size());
       }
@@ -364,7 +401,7 @@ struct pkv_sched {
       st.slots_unused += held - sq.num_tokens;
     }
     st.decode_tokens += (int64_t)dec.size();
-    for (const Entry &e : pre) st.prefill_tokens += (int64_t)e.slots.size();
+    for (const Entry &e : pre) st.prefill_tokens += (int64_t)e.n;
     return (int)p_seqs.size();
   }
 };
