@@ -943,9 +943,9 @@ def serve_setup(cfg, static=False, n=None, device="cuda"):
 
 
 def serve_run(drv, stream, decode_bytes_per_token):
-    """Run the stream to completion on the driver's packed path (the native scheduler
-    packs each step's plan into pinned staging; one fused decode-step call and one
-    prefill call per step).  Every step's outputs are read back to the host (what a
+    """Run the stream to completion, one native call per step (pkv_engine_step: the
+    scheduler step, its plan packed into pinned staging, the copy in, the fused decode
+    step, the prefill and the copy out).  Every step's outputs are read back to the host (what a
     sampler would read: every decode row, the last row of every prefill chunk); the host
     keeps two steps in flight -- it plans and queues step k + 1 (staging and output
     buffers of the other slot) before it waits for step k's outputs, since the
@@ -983,11 +983,11 @@ def serve_run(drv, stream, decode_bytes_per_token):
     t0 = time.perf_counter()
     slot, pending, k = 0, [], 0
     while not drv.done():
-        pk = drv.plan_packed(slot)  # the step that used this slot has retired
-        if pk.num_tokens == 0:  # nothing to compute this step
+        # the step that used this slot has retired
+        pk, _, _ = drv.engine_step(slot, handles[k % 4])
+        if pk.num_tokens == 0:  # nothing computed this step
             continue
         a, b = ev[k % 4]
-        drv.launch_packed(pk, slot, handles[k % 4])
         b.record(stream)
         pending.append((pk, slot, a, b, ev_dec if k % 4 == 0 else None))
         k += 1

@@ -72,7 +72,7 @@ extern "C" {
  * added or a signature changes).  2 added paged_kv_write_fp8_per_head,
  * paged_attention_decode_fp8_per_head, pkv_pool_save and pkv_pool_load; 3 added
  * paged_decode_step, paged_decode_step_fp8 and pkv_sched_pack; 4 added
- * paged_gather_rows and pkv_step_launch. */
+ * paged_gather_rows, pkv_step_launch and pkv_engine_step. */
 #define PKV_ABI_VERSION 4
 int paged_kv_version(void);
 
@@ -604,6 +604,19 @@ typedef struct {
   int32_t *err_flag;          /* device word (may be NULL)                             */
 } pkv_step_io;
 int pkv_step_launch(const pkv_step_io *io, const pkv_step_pack *pack, int slot,
+                    void *const *events, void *stream);
+
+/*
+ * pkv_engine_step -- one whole iteration of the serving loop from the host: pkv_sched_step
+ * on `sched`, pkv_sched_pack of its plan into io->host_stage[slot] (capacities
+ * io->max_tokens, io->max_seqs, io->table_stride, io->stage_bytes), then, if
+ * io->k_table != NULL, pkv_step_synthetic_rows over it (io->table_rows), then
+ * pkv_step_launch(io, pack, slot, events, stream).  Fills *pack.  Returns the number of
+ * scheduled sequences (pkv_sched_step's value; the step launches nothing when
+ * pack->num_tokens == 0, and no event is then recorded), or the first failing call's
+ * code.  host_stage[slot] must not be in use by an earlier step still on the stream.
+ */
+int pkv_engine_step(pkv_sched *sched, const pkv_step_io *io, pkv_step_pack *pack, int slot,
                     void *const *events, void *stream);
 int pkv_sched_done(const pkv_sched *sched);  /* 1 when no request is waiting or running */
 int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);

@@ -173,4 +173,21 @@ int pkv_step_launch(const pkv_step_io *io, const pkv_step_pack *pk, int slot,
   return PKV_OK;
 }
 
+int pkv_engine_step(pkv_sched *sched, const pkv_step_io *io, pkv_step_pack *pk, int slot,
+                    void *const *events, void *stream) {
+  if (!sched || !io || !pk) return PKV_ERR_NULL;
+  if (slot != 0 && slot != 1) return PKV_ERR_ARG;
+  pkv_step_plan plan;
+  const int n = pkv_sched_step(sched, &plan);
+  if (n < 0) return n;
+  int rc = pkv_sched_pack(sched, io->host_stage[slot], io->stage_bytes, io->max_tokens,
+                          io->max_seqs, io->table_stride, pk);
+  if (rc != PKV_OK) return rc;
+  if (pk->num_tokens == 0) return n;
+  if (io->k_table && (rc = pkv_step_synthetic_rows(io->host_stage[slot], pk, io->table_rows)))
+    return rc;
+  rc = pkv_step_launch(io, pk, slot, events, stream);
+  return rc != PKV_OK ? rc : n;
+}
+
 }  // extern "C"

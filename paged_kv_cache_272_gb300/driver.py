@@ -381,6 +381,26 @@ class ServingDriver:
             return None, None
         ops.check(ops.lib.pkv_step_launch(self.f_io_ref, ctypes.byref(pk), slot, events,
                                           self.f_stream), "pkv_step_launch")
+        return self._launched(pk, slot)
+
+    def engine_step(self, slot=0, events=None):
+        """One whole serving iteration in one native call (pkv_engine_step): the scheduler
+        step, its pack into pinned staging `slot`, the synthetic model's rows and the
+        device half of the step (see launch_packed).  Returns (pack, decode rows, prefill
+        last rows); the rows are host tensors valid once the stream reaches this point,
+        None when the step launched nothing (pack.num_tokens == 0)."""
+        if not hasattr(self, "f_host"):
+            self._fast_setup()
+        pk = self.f_packs[slot]
+        n = ops.lib.pkv_engine_step(self.sched._h, self.f_io_ref, ctypes.byref(pk), slot, events,
+                                    self.f_stream)
+        ops.check(min(n, 0), "pkv_engine_step")
+        if pk.num_tokens == 0:
+            return pk, None, None
+        return (pk, *self._launched(pk, slot))
+
+    def _launched(self, pk, slot):
+        """Counts of a launched packed step; its host output views."""
         n, nd = pk.num_seqs, pk.num_decode
         self.h2d_bytes += pk.total
         self.d2h_bytes += n * self.f_row

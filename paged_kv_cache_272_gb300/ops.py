@@ -87,6 +87,7 @@ SIGNATURES = {
     "pkv_step_synthetic_rows": (_I, [_P, _P, _I64]),
     "paged_gather_rows": (_I, [_P, _P, _P, _I, _I64, _I, _P, _P]),
     "pkv_step_launch": (_I, [_P, _P, _I, _P, _P]),
+    "pkv_engine_step": (_I, [_P, _P, _P, _I, _P, _P]),
     "pkv_sched_get_stats": (_I, [_P, _P]),
     "pkv_selftest_bounded_wait": (_I, [_P, _P, ctypes.c_longlong, _I, _P]),
 }

@@ -296,3 +296,23 @@ def test_step_launch_and_gather_host_validation():
     assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -1
     pk.num_tokens = 0  # nothing to do
     assert lib.pkv_step_launch(ctypes.byref(io), ctypes.byref(pk), 0, None, None) == 0
+
+
+def test_engine_step_host_validation():
+    """pkv_engine_step checks its arguments first, and a step with nothing to schedule
+    packs an empty plan and launches nothing (so this runs without a GPU)."""
+    from paged_kv_cache_272_gb300 import ops
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.serving import Scheduler, StepIO, StepPack
+    lib = ops.lib
+    pool = BlockPool(64)
+    sched = Scheduler(pool, 4, 64)
+    io, pk = StepIO(), StepPack()
+    buf = (ctypes.c_uint8 * 65536)()
+    io.host_stage[0] = io.host_stage[1] = ctypes.addressof(buf)
+    io.stage_bytes, io.max_tokens, io.max_seqs, io.table_stride = 65536, 68, 4, 8
+    assert lib.pkv_engine_step(None, ctypes.byref(io), ctypes.byref(pk), 0, None, None) == -1
+    assert lib.pkv_engine_step(sched._h, None, ctypes.byref(pk), 0, None, None) == -1
+    assert lib.pkv_engine_step(sched._h, ctypes.byref(io), ctypes.byref(pk), 3, None, None) == -14
+    assert lib.pkv_engine_step(sched._h, ctypes.byref(io), ctypes.byref(pk), 1, None, None) == 0
+    assert pk.num_tokens == 0 and pk.num_seqs == 0 and pk.total > 0

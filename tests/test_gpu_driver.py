@@ -101,10 +101,12 @@ def test_driver_steps_match_oracle(cache_entries, blocks, overlap):
         assert cache.stats()["hits"] > 0
 
 
+@pytest.mark.parametrize("engine", [False, True])
 @pytest.mark.parametrize("cache_entries,blocks", [(None, 400), (30, 60)])
-def test_packed_path_equals_the_checked_path(cache_entries, blocks):
+def test_packed_path_equals_the_checked_path(cache_entries, blocks, engine):
     """The packed serving path (native pack into pinned staging, fused decode step, two
-    steps in flight) gives, step by step, the same bits as the path checked against the
+    steps in flight; its device half in one native call, or the whole iteration in one,
+    pkv_engine_step) gives, step by step, the same bits as the path checked against the
     oracle above: every decode row, the last row of every prefill chunk, and the caches."""
     from paged_kv_cache_272_gb300.block_pool import BlockPool
     from paged_kv_cache_272_gb300.driver import ServingDriver
@@ -135,10 +137,15 @@ def test_packed_path_equals_the_checked_path(cache_entries, blocks):
     b = make()
     got, slot, pending = [], 0, []
     while not b.done():
-        pk = b.plan_packed(slot)
-        if pk.num_tokens == 0:
-            continue
-        hd, hl = b.launch_packed(pk, slot)
+        if engine:  # one native call per step
+            pk, hd, hl = b.engine_step(slot)
+            if pk.num_tokens == 0:
+                continue
+        else:
+            pk = b.plan_packed(slot)
+            if pk.num_tokens == 0:
+                continue
+            hd, hl = b.launch_packed(pk, slot)
         ev = torch.cuda.Event()
         ev.record()
         pending.append((hd, hl, ev))
