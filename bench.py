@@ -407,18 +407,22 @@ def run_ours(args):
     bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev)
     ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev)
     out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device=dev)
-    P = args.partition or w.partition_size
+    # 0: the automatic split (each call's plan picks 512 / 1024 / 2048 tokens)
+    P = 0 if args.partition is None else args.partition
     mcl = w.max_context_len
     ws = ops.alloc_workspace(S, Hq, D, mcl, P, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     kv_bytes = workloads.kv_read_bytes(w) // (2 if fp8 else 1)
-    max_parts = (mcl + P - 1) // P
+    max_parts = (mcl + (P or 512) - 1) // (P or 512)  # the workspace's partitions
     if args.step_api == "fused":  # prologue (copies + write + plan), partition, merge
         launches_per_step = (1 if pairs.shape[0] > 1024 else 0) + 2 + (1 if max_parts > 1 else 0)
     else:
         launches_per_step = (1 if pairs.numel() else 0) + 1 + 2 + (1 if max_parts > 1 else 0)
-    working_set = kv_bytes + q.numel() * 2 * 2
+    # distinct bytes a step touches: a shared prefix block counts once (it stays in L2
+    # from one step to the next unless flushed)
+    unique_kv = workloads.unique_kv_read_bytes(w) // (2 if fp8 else 1)
+    working_set = unique_kv + q.numel() * 2 * 2
     flush = working_set < 2 * L2_BYTES
     scratch = L2Flush(dev) if flush else None
 
@@ -595,10 +599,12 @@ def run_ours(args):
             **({"fp8_scales": "one per KV head (amax / 448)" if per_head else "one per cache"}
                if fp8 else {}),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
-            "head_dim": D, "block_size": w.block_size, "partition_size": P,
+            "head_dim": D, "block_size": w.block_size,
+            "partition_size": P if P else "auto (512-2048 tokens, chosen per call on the device)",
+            **({"partition_chosen": int(ws[4:8].view(torch.int32).item())} if not P else {}),
             "num_blocks": w.num_blocks, "mean_context": float(w.context_lens.mean()),
             "max_context": mcl, "kv_bytes_per_step": kv_bytes,
-            "unique_kv_bytes_per_step": workloads.unique_kv_read_bytes(w) // (2 if fp8 else 1),
+            "unique_kv_bytes_per_step": unique_kv,
             "cow_pairs_per_step": int(w.cow_pairs.shape[0]),
             "new_tokens_per_step": int(w.slot_mapping.shape[0]),
             "l2": ("L2 flushed (256 MB write, then 256 MB read) before every timed step"
@@ -757,7 +763,7 @@ def run_prefill(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
-          "tc": ops.PKV_PREFILL_TC}[args.prefill_kernel]
+          "tc": ops.PKV_PREFILL_TC, "tc_pair": ops.PKV_PREFILL_TC_PAIR}[args.prefill_kernel]
     ops.set_prefill_variant(pk)
     w = workloads.make_prefill_config(args.config, device="cuda", seed=args.seed)
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -864,9 +870,9 @@ def run_prefill(args):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (attn_ms / 1e3) / 1e12
-    # AUTO runs the tcgen05 kernel (head_dim 64 and 128)
-    tc = pk in (ops.PKV_PREFILL_TC, ops.PKV_PREFILL_AUTO)
-    kname = "prefill-tc" if tc else "prefill-mma"
+    # AUTO runs the one-tile tcgen05 kernel (head_dim 64 and 128)
+    kname = {ops.PKV_PREFILL_TC_PAIR: "prefill-tc-pair", ops.PKV_PREFILL_MMA: "prefill-mma"}.get(
+        pk, "prefill-tc")
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
@@ -894,9 +900,13 @@ def run_prefill(args):
                      "frac": achieved / peak,
                      "traffic": (recorded_traffic(w.name, kname, PREFILL_SOURCES)
                                  if args.seed is None else None),
-                     "kernel": ("paged_attention_prefill: prefill_tc_kernel (tcgen05.mma, "
-                                "TMEM accumulators)" if tc else
-                                "paged_attention_prefill: prefill_kernel (mma.sync)"),
+                     "kernel": {"prefill-tc": "paged_attention_prefill: prefill_tc_kernel "
+                                              "(tcgen05.mma, TMEM accumulators)",
+                                "prefill-tc-pair": "paged_attention_prefill: "
+                                                   "prefill_tc_pair_kernel (tcgen05.mma, two "
+                                                   "query tiles per CTA sharing K/V tiles)",
+                                "prefill-mma": "paged_attention_prefill: prefill_kernel "
+                                               "(mma.sync)"}[kname],
                      "peak_source": f"{peak_kind} bf16_tflops (burst)"},
         "clocks": clk.summary(),
     }
@@ -1180,8 +1190,9 @@ def main():
                          "serve 1..2, default 2)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--partition", type=int, default=0,
-                    help="split-K partition size in tokens (default: the workload's, 512)")
+    ap.add_argument("--partition", type=int, default=None,
+                    help="split-K partition size in tokens (default: automatic, chosen per "
+                         "call from the context lengths)")
     ap.add_argument("--seed", type=int, default=None,
                     help="draw the decode or prefill workload with this seed instead of its "
                          "default (1000 + config, 2000 + config); the recorded DRAM traffic "
@@ -1190,7 +1201,7 @@ def main():
                     help="KV cache element type: bf16, or fp8 (E4M3 codes with one scale each)")
     ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
                     help="with --kv-dtype fp8: one E4M3 scale per cache, or one per KV head")
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc"],
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc", "tc_pair"],
                     help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc")
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="decode step through paged_decode_step (one call, default) or the "

@@ -116,7 +116,7 @@ int paged_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_
 
 /*
  * Bytes of device workspace paged_attention_decode needs for these sizes.
- * partition_size <= 0 selects the default (512 tokens).
+ * partition_size <= 0 (the automatic size) needs the workspace of 512-token partitions.
  */
 size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_dim,
                                       int max_context_len, int partition_size);
@@ -127,8 +127,13 @@ size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_di
  *   x_t = scale * q[s][h] . K_s[t][g],   t < n, where K_s[t] is read through block_tables
  *   out[s][h] = sum_t exp(x_t - max x) V_s[t][g] / sum_t exp(x_t - max x)
  * computed in fp32 from bf16 inputs and rounded to bf16.  n == 0 gives zeros.
- * Long contexts are split into partitions of partition_size tokens (a multiple of 16;
- * <= 0 selects 512) whose partial results are merged with a log-sum-exp reduction.
+ * Long contexts are split into partitions of partition_size tokens (a multiple of 16)
+ * whose partial results are merged with a log-sum-exp reduction.  partition_size <= 0
+ * lets each call choose on the device, from context_lens: 512, 1024 or 2048 tokens, the
+ * largest not above (sum of context_lens x KV heads x query sub-groups) / (16 x SMs),
+ * i.e. about four partitions' worth of work per resident CTA of the partition kernel
+ * (large batches get fewer partitions: fewer items and partial results to merge).  The
+ * result depends on the split only through fp32 rounding.
  * max_context_len is a host-side upper bound of context_lens (it sizes the workspace);
  * a context above it sets PKV_DEV_BAD_CONTEXT and that sequence's output is zeros.
  * workspace (device, >= paged_attention_workspace_size bytes, 256-byte aligned) is
@@ -324,6 +329,7 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 #define PKV_PREFILL_AUTO 0
 #define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
 #define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
+#define PKV_PREFILL_TC_PAIR 3 /* tcgen05, two 128-row tiles per CTA sharing K/V tiles */
 int paged_attention_prefill_set_variant(int variant);
 
 /*

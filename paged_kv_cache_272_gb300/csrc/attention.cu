@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
   pdl_wait();
   const int per_pair = a.num_kv_heads * a.sub_groups;
   const int total = *a.num_items * per_pair;
+  const int part = *a.part_eff;
   // K/V rows are read once: evict them first, so partials and queries stay in L2
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep = l2_evict_last_policy();
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(128) attn_fma_kernel(const AttnArgs a) {
     const int4 rec = a.items[pair];
     const int s = rec.x, t0 = rec.y, t1 = rec.z;
     const bool single = rec.w == 1;
-    const int p = t0 / a.part_tokens;
+    const int p = t0 / part;
     const int nblk = (t1 - t0 + kBlockSize - 1) / kBlockSize;
     const int h0 = g * a.group + sub * GM;
     const int gcnt = min(GM, a.group - sub * GM);
@@ -334,7 +335,10 @@ int launch_attn_fma(const AttnArgs &a, int head_dim, int width, cudaStream_t st)
 using namespace pkv;
 
 namespace {
+// partition_size <= 0: the workspace holds 512-token partitions and each call's plan
+// picks 512, 1024 or 2048 tokens (see attn_plan_cta).
 constexpr int kDefaultPartition = 512;
+constexpr int kAutoPartitionMax = 4 * kDefaultPartition;
 
 int max_parts_for(int max_context_len, int part) {
   const int mp = (max_context_len + part - 1) / part;
@@ -357,7 +361,8 @@ int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *
       num_blocks <= 0 || max_context_len < 0 || num_q_heads % num_kv_heads != 0 ||
       (head_dim != 64 && head_dim != 128))
     return PKV_ERR_SHAPE;
-  const int part = partition_size > 0 ? partition_size : kDefaultPartition;
+  const bool auto_part = partition_size <= 0;
+  const int part = auto_part ? kDefaultPartition : partition_size;
   if (part % kBlockSize != 0) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
@@ -385,6 +390,8 @@ int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *
   a.group = num_q_heads / num_kv_heads;
   a.num_blocks = num_blocks;
   a.part_tokens = part;
+  a.part_max = auto_part ? kAutoPartitionMax : part;
+  a.slots = device_sm_count() * 4;
   a.max_parts = max_parts;
   a.scale_log2 = (float)((double)scale * (kv8 ? (double)k_scale : 1.0) * 1.4426950408889634);
   a.v_scale = kv8 ? v_scale : 1.0f;
@@ -392,6 +399,7 @@ int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *
   a.k_scales = kv8 ? k_scales : nullptr;
   a.v_scales = kv8 ? v_scales : nullptr;
   a.num_items = reinterpret_cast<int32_t *>(wb + ws.num_items_off);
+  a.part_eff = a.num_items + 1;  // same 256-byte section
   a.work_next = reinterpret_cast<int32_t *>(wb + ws.work_next_off);
   a.items = reinterpret_cast<int4 *>(wb + ws.items_off);
   a.part_lse = reinterpret_cast<float *>(wb + ws.lse_off);

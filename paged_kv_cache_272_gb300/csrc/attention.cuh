@@ -10,7 +10,9 @@ constexpr int kChunk = 32;  // partitions one merge unit combines
 // One work item is (sequence s, partition p) x (KV head g, query sub-group).  The plan
 // kernel lists every non-empty partition as an int4 record {s, t0, t1, np} (tokens
 // [t0, t1) of sequence s, which has np partitions), ordered by block count, largest
-// first, so that round-robin dealing of records to CTAs balances load.
+// first, so that round-robin dealing of records to CTAs balances load.  Partitions
+// hold part_tokens tokens, or, when part_max > part_tokens, a power-of-two multiple of
+// it chosen by the plan from the call's total context (written to *part_eff).
 //
 // The merge kernel works on units (sequence, group of 8 query heads, chunk of up to
 // kChunk partitions), also listed by the plan; a sequence with several chunks leaves
@@ -24,8 +26,11 @@ struct AttnArgs {
   const int32_t *block_tables;   // [S][MB]
   const int32_t *context_lens;   // [S]
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, group, num_blocks;
-  int part_tokens;               // partition size in tokens (multiple of 16)
-  int max_parts;                 // partitions per sequence the workspace holds
+  int part_tokens;               // smallest partition size in tokens (multiple of 16)
+  int part_max;                  // largest the plan may choose (part_tokens: exact size)
+  int slots;                     // about the partition kernel's resident CTAs
+  int max_parts;                 // partitions per sequence the workspace holds (of
+                                 //   part_tokens tokens)
   int sub_groups;                // query sub-groups per KV head (group > kernel width)
   int max_chunks;                // ceil(max_parts / kChunk)
   float scale_log2;              // scale * log2(e) (* k_scale for an E4M3 cache)
@@ -35,6 +40,7 @@ struct AttnArgs {
   const float *v_scales;         //   scale_log2 and v_scale already hold them)
   // workspace
   int32_t *num_items;            // [1]
+  int32_t *part_eff;             // [1] partition size the plan chose (read by the kernels)
   int32_t *work_next;            // [1] next record to claim (tensor-core kernel)
   int4 *items;                   // [S * max_parts] records {s, t0, t1, np}
   float *part_lse;               // [S][max_parts][Hq]   log2-sum-exp2 of the partition

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__((NW + 1) * 32,
 
   const int per_pair = a.num_kv_heads * a.sub_groups;
   const int total = *a.num_items * per_pair;
+  const int part = *a.part_eff;  // the plan's partition size
 
   if (warp == NW) {
     // ------------------------------- producer -------------------------------------
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__((NW + 1) * 32,
       }
       const float f0 = vsc / L0, f1 = vsc / L1;
       const bool single = rec.w == 1;
-      const int p = t0 / a.part_tokens;
+      const int p = t0 / part;
       const int hA = 2 * tig, hB = 2 * tig + 1;  // heads of this lane, within the item
       const size_t rowA = single ? ((size_t)s * a.num_q_heads + h0 + hA)
                                  : (((size_t)s * a.max_parts + p) * a.num_q_heads + h0 + hA);

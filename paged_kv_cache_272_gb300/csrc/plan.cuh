@@ -6,9 +6,16 @@
 //  * validates every length (a negative one, or one beyond the block table or the
 //    workspace, sets PKV_DEV_BAD_CONTEXT and counts as empty) and writes zeros to the
 //    output of every empty sequence (no partition will write it);
-//  * lists the partitions as records {s, t0, t1, np} ordered by block count, largest
-//    first (a counting sort over 1..32 blocks: every partition but a sequence's last has
-//    part_tokens tokens), so that claiming records in order balances load;
+//  * chooses the partition size P: part_tokens, or, when part_max > part_tokens, the
+//    largest part_tokens * 2^k <= part_max not above (total context tokens x work items
+//    per partition) / (4 x the partition kernel's resident CTAs) -- each CTA then meets
+//    four partitions' worth of work or more, so claiming still balances, while a large
+//    batch gets fewer, longer partitions (fewer items, fewer partial results to merge);
+//    P goes to *part_eff for the partition kernel;
+//  * lists the partitions as records {s, t0, t1, np} ordered by size, largest first (a
+//    counting sort over 32 bins of P / 32 tokens, rounded up to whole blocks: every
+//    partition but a sequence's last has P tokens), so that claiming records in order
+//    balances load;
 //  * lists the merge units (sequence, group of 8 query heads, chunk of kChunk
 //    partitions) of sequences with several partitions, multi-chunk sequences first (the
 //    longest merges start first), and zeroes their second-level arrival counters;
@@ -69,9 +76,28 @@ __device__ __forceinline__ void attn_plan_cta(const AttnArgs &a, int head_dim) {
   if (tid == 0) nbig = 0;
   __syncthreads();
   const int cap = min(a.max_blocks * kBlockSize, a.max_parts * a.part_tokens);
-  const int P = a.part_tokens;
+  // Pass 0 (automatic size only): the call's total context, then P.
+  int P = a.part_tokens;
+  if (a.part_max > P) {
+    __shared__ unsigned long long total;
+    if (tid == 0) total = 0;
+    __syncthreads();
+    unsigned long long mine = 0;
+    for (int s = tid; s < a.num_seqs; s += nthr) mine += (unsigned)plan_len(a, s, cap, false);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kPlanFull, mine, off);
+    if (lane == 0 && mine) atomicAdd(&total, mine);
+    __syncthreads();
+    const unsigned long long budget =
+        total * (unsigned)(a.num_kv_heads * a.sub_groups) / (4ull * (unsigned)a.slots);
+    while (2 * P <= a.part_max && (unsigned long long)(2 * P) <= budget) P *= 2;
+  }
+  if (tid == 0) *a.part_eff = P;
   const int G8 = (a.num_q_heads + 7) / 8;
-  const int full_bin = min(P / kBlockSize, 32);
+  // Bins of P / 32 tokens (whole blocks when P <= 512): bin(blocks) in 1..32.
+  const int nbP = P / kBlockSize;
+  auto bin_of = [&](int blocks) { return nbP <= 32 ? blocks : (blocks * 32 + nbP - 1) / nbP; };
+  const int full_bin = bin_of(nbP);
   const int row_vecs = a.num_q_heads * head_dim / 8;  // 16-byte vectors of one output row
   // Every warp runs the same number of rounds, so the warp-wide steps see all lanes.
   const int rounds = (a.num_seqs + nthr - 1) / nthr;
@@ -87,7 +113,7 @@ __device__ __forceinline__ void attn_plan_cta(const AttnArgs &a, int head_dim) {
     if (n > 1) atomicAdd(&ucount[nch > 1 ? 0 : 1], nch * G8);
     const int nfull = c / P, tail = c - nfull * P;
     if (nfull) atomicAdd(&hist[full_bin], nfull);
-    if (tail) atomicAdd(&hist[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
+    if (tail) atomicAdd(&hist[bin_of((tail + kBlockSize - 1) / kBlockSize)], 1);
     const int4 me = make_int4(s, 0, 0, 0);
     warp_spread(live && n == 0 ? row_vecs : 0, me, lane, [&](int4 v, int i) {
       reinterpret_cast<uint4 *>(a.out + (size_t)v.x * a.num_q_heads * head_dim)[i] =
@@ -127,7 +153,7 @@ __device__ __forceinline__ void attn_plan_cta(const AttnArgs &a, int head_dim) {
     const int nfull = c / P, tail = c - nfull * P;
     const int pos = nfull ? atomicAdd(&cursor[full_bin], nfull) : 0;
     if (tail) {
-      const int at = atomicAdd(&cursor[min((tail + kBlockSize - 1) / kBlockSize, 32)], 1);
+      const int at = atomicAdd(&cursor[bin_of((tail + kBlockSize - 1) / kBlockSize)], 1);
       a.items[at] = make_int4(s, nfull * P, c, n);
     }
     // the full partitions of sequence s occupy records pos .. pos + nfull - 1; a long

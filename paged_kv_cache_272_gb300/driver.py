@@ -101,7 +101,7 @@ def prepare(plan: Plan, prompts: dict, kv_rows_n: int, q_rows_n: int,
 class ServingDriver:
     def __init__(self, sched: Scheduler, num_blocks: int, num_q_heads: int, num_kv_heads: int,
                  head_dim: int, max_context: int, seed: int = 0, table_rows: int = 4096,
-                 device="cuda", partition_size: int = 512):
+                 device="cuda", partition_size: int = 0):
         self.sched = sched
         self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
         self.dev = torch.device(device)
@@ -121,7 +121,8 @@ class ServingDriver:
         self.prompts: dict[int, np.ndarray] = {}
         self._plen: np.ndarray | None = np.zeros(1024, np.int64)
         self.max_context = max_context
-        self.P = partition_size
+        self.P = partition_size  # 0: each decode call picks its split on the device
+        self.P_ws = partition_size if partition_size > 0 else 512  # the workspace's partitions
         self.ws = ops.alloc_workspace(sched.max_num_seqs, num_q_heads, head_dim, max_context,
                                       partition_size, device=self.dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.dev)
@@ -280,7 +281,7 @@ class ServingDriver:
                                        err_flag=self.err, stream=self.stream)
             if self.on_decode is not None:
                 self.on_decode(1)
-            self.launches += 3 if x.decode_ctx_max > self.P else 2
+            self.launches += 3 if x.decode_ctx_max > self.P_ws else 2
         if plan.seq_ids.shape[0] > nd:
             pre_out = self._dev("pre_out", (T - nd, self.Hq, self.D), torch.bfloat16)
             ops.paged_attention_prefill(pre_out, q[nd:], self.k_cache, self.v_cache, tables[nd:],
@@ -406,7 +407,7 @@ class ServingDriver:
         self.d2h_bytes += n * self.f_row
         launches = 1  # the row gathers
         if nd:  # prologue (copies, write, plan), partition, merge if split, extra copies
-            launches += 2 + (pk.decode_max_context > self.P) + (pk.num_cow > 1024)
+            launches += 2 + (pk.decode_max_context > self.P_ws) + (pk.num_cow > 1024)
         else:  # no decode entry: the copies (if any) and the write alone
             launches += 1 + (pk.num_cow > 0)
         if n > nd:  # the prefill and its last-row gather

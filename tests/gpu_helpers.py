@@ -40,7 +40,7 @@ def gpu_step(w: workloads.Workload, variant=None, partition_size=None, max_conte
     d = d or to_cuda(w)
     if variant is not None:
         o.set_attention_variant(variant)
-    P = partition_size or w.partition_size
+    P = w.partition_size if partition_size is None else partition_size  # 0: automatic
     mcl = w.max_context_len if max_context_len is None else max_context_len
     bt = d["bt"] if block_tables is None else block_tables
     ctx = d["ctx"] if context_lens is None else context_lens
@@ -157,7 +157,7 @@ def fp8_step(w, ks=K_SCALE, vs=V_SCALE, partition_size=None, block_tables=None):
     if d["slots"].numel():
         write(d["k_new"], d["v_new"], d["slots"])
     S, Hq, _ = d["q"].shape
-    P = partition_size or w.partition_size
+    P = w.partition_size if partition_size is None else partition_size  # 0: automatic
     out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = o.alloc_workspace(S, Hq, D, w.max_context_len, P)
     bt = d["bt"] if block_tables is None else block_tables

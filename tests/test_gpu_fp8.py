@@ -77,6 +77,20 @@ def test_fp8_long_context_sampled():
     H.assert_attention_close(got, ref, "fp8 config 5 sample")
 
 
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_fp8_auto_partition(cfg):
+    """partition_size 0 (the plan picks 1024 / 2048-token partitions for these batches):
+    config 3 in full, config 5 on every long row plus 256 short ones."""
+    w = workloads.make_config(cfg, device="cuda")
+    out, kq, vq, ko, vo, err = fp8_step(w, partition_size=0)
+    assert err == 0
+    sel = H.wide_pairs(w, n_short=256) if cfg == 5 else None
+    ref = fp8_ref(w, ko, vo, sel=sel)
+    got = out if sel is None else out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+                                      torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+    H.assert_attention_close(got, ref, f"fp8 config {cfg}, automatic split")
+
+
 @pytest.mark.parametrize("G", [1, 2, 3, 8, 16])
 @pytest.mark.parametrize("P", [64, 512, 8192])
 def test_fp8_groups_and_partitions(G, P):

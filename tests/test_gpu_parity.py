@@ -101,6 +101,64 @@ def test_partition_size_invariance(variant):
         assert (o - outs[0]).abs().max().item() <= 2e-2
 
 
+def _chosen_partition(ws):
+    """The partition size the call's plan chose: an int32 at byte 4 of the workspace (the
+    library's internal layout, beside the record count)."""
+    return int(ws[4:8].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_auto_partition_full(cfg, variant):
+    """partition_size 0: each call picks its partition size on the device; every output
+    matches the oracle, and stays within rounding of the 512-token split."""
+    w = _make(cfg)
+    out, k, v, err = H.gpu_step(w, variant, partition_size=0)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    H.assert_attention_close(out, H.oracle_out(w, ko, vo), f"config {cfg}, automatic split")
+    out512, _, _, err = H.gpu_step(w, variant, partition_size=512)
+    assert err == 0 and (out.float() - out512.float()).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_auto_partition_config5_sampled(variant):
+    """The long-context batch under the automatic split (2048-token partitions, 64 per
+    long sequence): every query head of the long sequences and 256 short rows."""
+    w = _make(5)
+    out, k, v, err = H.gpu_step(w, variant, partition_size=0)
+    assert err == 0
+    ko, vo = H.oracle_caches(w)
+    sel = H.wide_pairs(w, n_short=256)
+    ref = H.oracle_out(w, ko, vo, sel=sel)
+    got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+              torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+    H.assert_attention_close(got, ref, "config 5 sample, automatic split")
+
+
+@pytest.mark.parametrize("cfg,want", [(1, 512), (3, 1024), (4, 512), (5, 2048)])
+def test_auto_partition_choice(cfg, want):
+    """The plan's choice: the largest of 512 / 1024 / 2048 tokens not above (total context
+    x KV heads) / (16 x SMs); the 512-token workspace serves every choice."""
+    o = H.ops()
+    w = _make(cfg)
+    d = H.to_cuda(w)
+    S, Hq, D = d["q"].shape
+    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, 0)
+    out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device="cuda")
+    o.paged_attention_decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale,
+                             w.max_context_len, ws, 0)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    total = int(w.context_lens.astype(np.int64).sum()) * w.num_kv_heads
+    expect = 512
+    while 2 * expect <= 2048 and 2 * expect <= total // (16 * sms):
+        expect *= 2
+    assert _chosen_partition(ws) == expect
+    if sms == 152:  # the sizes these workloads were tuned on
+        assert expect == want
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_large_magnitude_scores(variant):
     w = workloads.build("big", [40, 600, 1500], 16, 2, 128, seed=95, device="cuda")

@@ -20,8 +20,9 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def fused_step(w, d=None, pairs=None, slots=None, k_new=None, v_new=None):
+def fused_step(w, d=None, pairs=None, slots=None, k_new=None, v_new=None, partition_size=None):
     """paged_decode_step on device copies of the workload; returns (out, k, v, err)."""
+    P = w.partition_size if partition_size is None else partition_size  # 0: automatic
     o = H.ops()
     d = d or H.to_cuda(w)
     pairs = d["pairs"] if pairs is None else pairs
@@ -30,12 +31,12 @@ def fused_step(w, d=None, pairs=None, slots=None, k_new=None, v_new=None):
     v_new = d["v_new"] if v_new is None else v_new
     S, Hq, D = d["q"].shape
     out = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, w.partition_size)
+    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, P)
     ws.fill_(0xFF)  # stale workspace content must not matter
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o.paged_decode_step(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale,
                         w.max_context_len, ws, k_new=k_new, v_new=v_new, slot_mapping=slots,
-                        block_pairs=pairs, partition_size=w.partition_size, err_flag=err)
+                        block_pairs=pairs, partition_size=P, err_flag=err)
     torch.cuda.synchronize()
     return out, d["k"], d["v"], int(err.item())
 
@@ -51,13 +52,15 @@ def _check(w, out, k, v, err, sel=None):
     H.assert_attention_close(got, ref, w.name)
 
 
+@pytest.mark.parametrize("P", [None, 0])
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
-def test_step_configs(cfg):
+def test_step_configs(cfg, P):
+    """The workload's 512-token split, and the automatic one (P = 0)."""
     w = workloads.make_config(cfg, device="cpu" if cfg == 1 else "cuda")
-    out, k, v, err = fused_step(w)
+    out, k, v, err = fused_step(w, partition_size=P)
     _check(w, out, k, v, err)
     # the three separate calls give the same bits
-    out3, k3, v3, err3 = H.gpu_step(w)
+    out3, k3, v3, err3 = H.gpu_step(w, partition_size=P)
     assert err3 == 0
     assert torch.equal(out.view(torch.int16), out3.view(torch.int16))
     assert torch.equal(k.view(torch.int16), k3.view(torch.int16))
