@@ -893,6 +893,466 @@ int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUten
                          dim3(kTcWarps * 32), (size_t)Lay::kSmemLaunch, st, a, tk, tv);
 }
 
+// ------------------------------------------------------------------------------------
+// Two-tile variant (PKV_PREFILL_TC_PAIR).  The tensor core reads its shared-memory
+// operands at about 128 bytes per cycle per SM (probes: an M 128 x N 64 x K 16 product
+// with both operands in shared memory, 6 KB, takes 48 cycles; N 128, 8 KB, 64), and the
+// TMA writes of the K/V tiles share that bandwidth.  In the kernel above two CTAs per SM
+// each stage their own copy of every K and V tile: per 64-key tile and CTA the score
+// products read 48 KB (Q 32 KB + K 16 KB), the P V products 16 KB (V) and the copies
+// write 32 KB, i.e. about 1500 cycles of shared-memory traffic per 1024 cycles of tensor
+// work on the SM.  Here one CTA per SM holds two consecutive 128-row query tiles of one
+// (sequence, KV head) as two independent chains -- each with its own Q tile, two S
+// buffers and O accumulator in TMEM (columns 256 c .. 256 c + 255, all 512 allocated)
+// and its own softmax, score and P V warps -- that share every K and V tile: the copies
+// write half as much per query row (≈ 1250 cycles per 1024).
+//  * warps 0-3 / 4-7: softmax of chain 0 / 1 (thread t owns row t of its tile);
+//  * warps 8 / 9: score products of chain 0 / 1; warps 10 / 11: P V products;
+//  * warps 12 / 13: K / V copies into NS-slot rings (lane b: block b of the tile).
+// A K (V) slot is free once both chains' score (P V) products on it are done (two
+// arrivals).  Chain 1 may need a tile more than chain 0 (its rows see later keys);
+// a chain that does not use a staged tile waits for it to land and then only adds its
+// arrival, so neither chain can run ahead of the copies.  P sits over its S columns in
+// TMEM (as in the kernel above).
+constexpr int kPairWarps = 14;
+
+template <int D, int NS>
+struct PairLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQHalf = kTcRows * 128;         // 16 KB: 128 rows x 64 dims
+  static constexpr int kKHalf = kKeys * 128;           // 8 KB: 64 keys x 64 dims
+  static constexpr int kQChain = kHalves * kQHalf;     // one chain's Q tile
+  static constexpr int kSlot = kHalves * kKHalf;       // one K or V tile
+  static constexpr int kK = 2 * kQChain;
+  static constexpr int kV = kK + NS * kSlot;
+  static constexpr int kBars = kV + NS * kSlot;
+  // k_full, k_empty, v_full, v_empty [NS]; per chain: s_full[2], p_full[2], pv_done[2],
+  // o_done, fin
+  static constexpr int kNumBars = 4 * NS + 2 * 8;
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16;
+  // more than half an SM's shared memory: one CTA per SM (it holds all 512 TMEM columns)
+  static constexpr int kSmemLaunch = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(kPairWarps * 32, 1)
+    prefill_tc_pair_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
+                           const __grid_constant__ CUtensorMap tv) {
+  using Lay = PairLayout<D, NS>;
+  constexpr int H = Lay::kHalves;
+  extern __shared__ __align__(1024) unsigned char smem_tc[];
+  const uint32_t base = smem_u32(smem_tc);
+  if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
+    if (threadIdx.x == 0) flag_error(a.err, PKV_DEV_LAYOUT);
+    return;
+  }
+  const uint32_t sK = base + Lay::kK, sV = base + Lay::kV;
+  const uint32_t bars = base + Lay::kBars;
+  const uint32_t k_full = bars, k_empty = bars + 8 * NS, v_full = bars + 16 * NS,
+                 v_empty = bars + 24 * NS;
+  auto chain_bar = [&](int c, int k) { return bars + 32 * NS + 64 * c + 8 * k; };
+  // per chain c: s_full = chain_bar(c, 0..1), p_full (2..3), pv_done (4..5), o_done (6),
+  // fin (7)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_tc + Lay::kBars + Lay::kNumBars * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int pair = (a.row_tiles + 1) / 2 - 1 - (int)blockIdx.x;  // latest rows first
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(k_full + 8 * i, kTileBlocks);
+      mbar_init(k_empty + 8 * i, 2);
+      mbar_init(v_full + 8 * i, kTileBlocks);
+      mbar_init(v_empty + 8 * i, 2);
+    }
+    for (int c = 0; c < 2; ++c) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(chain_bar(c, i), 1);
+        mbar_init(chain_bar(c, 2 + i), 4);
+        mbar_init(chain_bar(c, 4 + i), 1);
+      }
+      mbar_init(chain_bar(c, 6), 1);
+      mbar_init(chain_bar(c, 7), 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+  const int ctx = a.context_lens[s];
+  const int L = q1 - q0;
+  if (q0 < 0 || L < 0 || q1 > a.num_tokens || L > a.max_query_len || L > ctx ||
+      ctx > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+    return;
+  }
+  const int G = a.group;
+  const int rows = L * G;
+  const int first_pos = ctx - L;
+  // Chain c's rows start at r0 + 128 c; its keys end at kv_end_c (tiles: nkt_c).
+  const int r0 = 2 * pair * kTcRows;
+  if (r0 >= rows) return;  // no row of this pair exists
+  auto keys_end = [&](int rs) { return first_pos + (min(rs + kTcRows, rows) - 1) / G + 1; };
+  const int kv_end0 = keys_end(r0);
+  const bool has1 = r0 + kTcRows < rows;
+  const int kv_end = has1 ? keys_end(r0 + kTcRows) : kv_end0;  // the CTA's last key + 1
+  const int nkt0 = (kv_end0 + kKeys - 1) / kKeys;
+  const int nkt = (kv_end + kKeys - 1) / kKeys;
+  auto chain_tiles = [&](int c) { return c == 0 ? nkt0 : (has1 ? nkt : 0); };
+
+  if (warp == 8) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    // ---------------- softmax warps: chain c, thread t owns row t of its tile ----------
+    const int c = warp >> 2, t = threadIdx.x & 127, wq = warp & 3;
+    const int nk = chain_tiles(c);
+    const uint32_t tS = tmem + 256 * c, tO = tS + 128;
+    const uint32_t sQ = base + c * Lay::kQChain;
+    const uint32_t s_full = chain_bar(c, 0), p_full = chain_bar(c, 2), o_done = chain_bar(c, 6),
+                   fin = chain_bar(c, 7);
+    if (nk > 0) {
+      const int rc0 = r0 + c * kTcRows;
+      const int r = rc0 + t;
+      const bool valid = r < rows;
+      const int r_last = min(rc0 + kTcRows, rows) - 1;
+      const int pos = first_pos + (valid ? r : r_last) / G;
+      const int warp_pos_lo = first_pos + min(rc0 + wq * 32, r_last) / G;
+      const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+      uint16_t *orow = a.out + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D;
+      {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(
+            a.q + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D);
+#pragma unroll
+        for (int cc = 0; cc < 8 * H; ++cc) {
+          const uint4 v = valid ? qrow[cc] : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(sQ + (cc >> 3) * Lay::kQHalf + t * 128 + (((cc & 7) ^ (t & 7)) << 4),
+                       v.x, v.y, v.z, v.w);
+        }
+      }
+      fence_proxy_async();
+      named_bar_sync(1 + c, 160);
+
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nk; ++j) {
+        const int sb = j & 1;
+        const int t0 = j * kKeys;
+        if (!mbar_wait(s_full + 8 * sb, (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t x[64];
+        {
+          uint32_t (&x0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[0]);
+          uint32_t (&x1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[32]);
+          tmem_ld32(tS + 64 * sb + lane_base, x0);
+          tmem_ld32(tS + 64 * sb + 32 + lane_base, x1);
+          tmem_wait_ld();
+        }
+        // Raw scores; keys past the row's position become -inf (diagonal tiles only).
+        const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
+        if (need_mask) {
+#pragma unroll
+          for (int cc = 0; cc < 64; ++cc)
+            if (t0 + cc > pos) x[cc] = __float_as_uint(-INFINITY);
+        }
+        float mxv[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) mxv[cc] = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 2)
+          mxv[(cc >> 1) & 7] =
+              max3f(mxv[(cc >> 1) & 7], __uint_as_float(x[cc]), __uint_as_float(x[cc + 1]));
+        float mx = max3f(max3f(mxv[0], mxv[1], mxv[2]), max3f(mxv[3], mxv[4], mxv[5]),
+                         fmaxf(mxv[6], mxv[7]));
+        mx *= a.scale_log2;
+        if (j == 0) {
+          m = mx;  // key 0 is visible to every row
+        } else {
+          const bool need = mx > m + 8.f;
+          if (__any_sync(kAll, need)) {
+            if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float mn = need ? mx : m;
+            const float corr = fast_exp2(m - mn);
+            m = mn;
+            l *= corr;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * cc + lane_base, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+              tmem_st32(tO + 32 * cc + lane_base, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        uint32_t pk[32];
+        uint64_t ps2[4];
+        const uint64_t sl2 = f32x2(a.scale_log2, a.scale_log2), nm2 = f32x2(-m, -m);
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) {
+          float e0, e1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[2 * cc]), __uint_as_float(x[2 * cc + 1])),
+                                sl2, nm2),
+                      e0, e1);
+          const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+          const uint64_t pp = f32x2(p0, p1);
+          ps2[cc & 3] = cc < 4 ? pp : add_f32x2(ps2[cc & 3], pp);
+          pk[cc] = pack_bf16(p0, p1);
+        }
+        {
+          float s0, s1;
+          f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+          l += s0 + s1;
+        }
+        if (t0 + kKeys > kv_end) {
+          // The CTA's last tile: V rows at or past kv_end (tail of the last block, blocks
+          // not staged) are set to zero so that their zero weights add exactly nothing.
+          // Both chains may zero them (the same values) before their own P V product.
+          const int slot = j % NS;
+          if (!mbar_wait(v_full + 8 * slot, (uint32_t)(j / NS) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vst = sV + slot * Lay::kSlot;
+          const int z0 = kv_end - t0;
+          for (int i = t; i < (kKeys - z0) * 8 * H; i += 128) {
+            const int row = z0 + i / (8 * H), rem = i % (8 * H);
+            st_shared_v4(vst + (rem >> 3) * Lay::kKHalf + row * 128 + (rem & 7) * 16, 0u, 0u,
+                         0u, 0u);
+          }
+          fence_proxy_async();
+        }
+        // P overwrites the first 32 columns of this tile's S buffer (already read).
+        tmem_st32(tS + 64 * sb + lane_base, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + 8 * sb);
+      }
+      // Every product of this chain has completed once its P V warp's final commit fires.
+      if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
+      if (ok && !*abort_flag) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * cc + lane_base, o);
+          tmem_wait_ld();
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(
+                  pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * e + 2]) * inv,
+                            __uint_as_float(o[8 * e + 3]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * e + 4]) * inv,
+                            __uint_as_float(o[8 * e + 5]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * e + 6]) * inv,
+                            __uint_as_float(o[8 * e + 7]) * inv));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (warp < 10) {
+    // ---------------- score warps: lane 0 issues S_j = Q_c K_j^T ----------------
+    const int c = warp - 8;
+    const int nk = chain_tiles(c);
+    const uint32_t tS = tmem + 256 * c, sQ = base + c * Lay::kQChain;
+    const uint32_t s_full = chain_bar(c, 0), pv_done = chain_bar(c, 4);
+    if (nk > 0) named_bar_sync(1 + c, 160);
+    tc_fence_after();
+    constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
+    int js = 0;
+    for (; js < nkt; ++js) {
+      const int sb = js & 1, slot = js % NS;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_spin_wait(k_full + 8 * slot, (uint32_t)(js / NS) & 1u, abort_flag, a.err) &&
+             (js >= nk || js < 2 ||
+              mbar_spin_wait(pv_done + 8 * sb, (uint32_t)((js - 2) >> 1) & 1u, abort_flag,
+                             a.err));
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t kst = sK + slot * Lay::kSlot;
+      if (lane == 0) {
+        if (js < nk) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma(tS + 64 * sb,
+                   sw128_desc(sQ + (kk >> 2) * Lay::kQHalf + (kk & 3) * 32, 16, 1024),
+                   sw128_desc(kst + (kk >> 2) * Lay::kKHalf + (kk & 3) * 32, 16, 1024), idS,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(s_full + 8 * sb);
+          tc_commit(k_empty + 8 * slot);
+        } else {
+          mbar_arrive(k_empty + 8 * slot);  // a tile only the other chain reads
+        }
+      }
+      __syncwarp();
+    }
+    // The score products this thread issued have completed once the last one's commit
+    // fires (a commit tracks every earlier product of its thread).
+    const int last = min(js, nk) - 1;
+    if (lane == 0 && last >= 0) mbar_drain(s_full + 8 * (last & 1), (uint32_t)(last >> 1) & 1u);
+    __syncwarp();
+    tc_fence_before();
+  } else if (warp < 12) {
+    // ---------------- P V warps: lane 0 issues O_c += P_j V_j ----------------
+    const int c = warp - 10;
+    const int nk = chain_tiles(c);
+    const uint32_t tS = tmem + 256 * c, tO = tS + 128;
+    const uint32_t p_full = chain_bar(c, 2), pv_done = chain_bar(c, 4), o_done = chain_bar(c, 6),
+                   fin = chain_bar(c, 7);
+    tc_fence_after();
+    constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
+    for (int jp = 0; jp < nkt; ++jp) {
+      const int slot = jp % NS;
+      int ok = 1;
+      if (lane == 0)
+        ok = (jp >= nk || mbar_spin_wait(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u,
+                                          abort_flag, a.err)) &&
+             mbar_spin_wait(v_full + 8 * slot, (uint32_t)(jp / NS) & 1u, abort_flag, a.err);
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t vst = sV + slot * Lay::kSlot;
+      if (lane == 0) {
+        if (jp < nk) {
+#pragma unroll
+          for (int k = 0; k < kKeys / 16; ++k)
+            tc_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k,
+                      sw128_desc(vst + 2048 * k, Lay::kKHalf, 1024), idO,
+                      (jp > 0 || k > 0) ? 1u : 0u);
+          tc_commit(o_done);
+          tc_commit(v_empty + 8 * slot);
+          tc_commit(pv_done + 8 * (jp & 1));
+        } else {
+          mbar_arrive(v_empty + 8 * slot);  // a tile only the other chain reads
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) tc_commit(fin);
+    __syncwarp();
+    mbar_drain(fin, 0);
+    tc_fence_before();
+  } else {
+    // ---------------- copy warps: warp 12 stages K, warp 13 V; lane b block b ------------
+    const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
+    const bool is_v = warp == 13;
+    const uint32_t full = is_v ? v_full : k_full, empty = is_v ? v_empty : k_empty;
+    const uint32_t ring = is_v ? sV : sK;
+    const CUtensorMap *map = is_v ? &tv : &tk;
+    int issued = 0;
+    if (lane < kTileBlocks) {
+      // block ids are read one tile ahead, so their latency overlaps the slot waits
+      int next = lane * kBlockSize < kv_end ? table[lane] : INT_MIN;
+      for (int j = 0; j < nkt; ++j) {
+        const int slot = j % NS;
+        int blk = next;
+        const int tok_n = (j + 1) * kKeys + lane * kBlockSize;
+        next = (j + 1 < nkt && tok_n < kv_end) ? table[tok_n / kBlockSize] : INT_MIN;
+        if (j >= NS &&
+            !mbar_wait(empty + 8 * slot, (uint32_t)((j - NS) / NS) & 1u, abort_flag, a.err))
+          break;
+        if (blk != INT_MIN && (blk < 0 || blk >= a.num_blocks)) {
+          flag_error(a.err, PKV_DEV_BAD_BLOCK);
+          blk = INT_MIN;
+        }
+        const uint32_t bar = full + 8 * slot;
+        mbar_arrive_expect_tx(bar, blk != INT_MIN ? 2048u * H : 0u);
+        if (blk != INT_MIN) {
+          const int row = (blk * a.num_kv_heads + g) * kBlockSize;
+          const uint32_t dst = ring + slot * Lay::kSlot + lane * 2048;
+#pragma unroll
+          for (int h = 0; h < H; ++h) tma_load_2d(dst + h * Lay::kKHalf, map, 64 * h, row, bar);
+        }
+        issued = j + 1;
+      }
+    }
+    __syncwarp();
+    // If a wait gave up, let the copies still in flight land before the CTA exits.
+    if (lane == 0 && *abort_flag)
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        mbar_drain(full + 8 * (j % NS), (uint32_t)(j / NS) & 1u);
+  }
+
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
+}
+
+template <int D, int NS>
+int launch_prefill_pair_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                          cudaStream_t st) {
+  using Lay = PairLayout<D, NS>;
+  static std::atomic<int> ready[kMaxDevices];  // shared-memory opt-in, per device
+  const int r = per_device_setup(ready, [] {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_pair_kernel<D, NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay::kSmemLaunch);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_tc_pair_kernel<D, NS>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    return e == cudaSuccess ? 1 : -(int)e;
+  });
+  if (r <= 0) return -r;
+  return (int)launch_pdl(prefill_tc_pair_kernel<D, NS>,
+                         dim3((unsigned)((a.row_tiles + 1) / 2), (unsigned)a.num_kv_heads,
+                              (unsigned)a.num_seqs),
+                         dim3(kPairWarps * 32), (size_t)Lay::kSmemLaunch, st, a, tk, tv);
+}
+
+// K/V ring depth, overridable for tuning through PKV_PREFILL_PAIR_STAGES (2, 3 or 4).
+int pair_stages() {
+  static const int n = [] {  // read once (thread-safe static initialisation)
+    const char *v = std::getenv("PKV_PREFILL_PAIR_STAGES");
+    const int k = v ? std::atoi(v) : 2;
+    return k >= 2 && k <= 4 ? k : 2;
+  }();
+  return n;
+}
+
+int launch_prefill_pair(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                        int head_dim, cudaStream_t st) {
+  switch (pair_stages()) {
+    case 3: return head_dim == 64 ? launch_prefill_pair_t<64, 3>(a, tk, tv, st)
+                                  : launch_prefill_pair_t<128, 3>(a, tk, tv, st);
+    case 4: return head_dim == 64 ? launch_prefill_pair_t<64, 4>(a, tk, tv, st)
+                                  : launch_prefill_pair_t<128, 4>(a, tk, tv, st);
+    default: return head_dim == 64 ? launch_prefill_pair_t<64, 2>(a, tk, tv, st)
+                                   : launch_prefill_pair_t<128, 2>(a, tk, tv, st);
+  }
+}
+
 // P kept in tensor memory by default (the A operand of P V read from TMEM: no shared-
 // memory traffic for P, 6% faster on GB300); PKV_PREFILL_P=smem selects the variant that
 // stages P in shared memory.
@@ -936,6 +1396,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
   const int group = num_q_heads / num_kv_heads;
   const int variant = g_prefill_variant.load();
   const bool tc = variant != PKV_PREFILL_MMA;
+  const bool pair = variant == PKV_PREFILL_TC_PAIR;
   const int rows_per_cta = tc ? kTcRows : kRows;
   const int64_t tiles = ((int64_t)max_query_len * group + rows_per_cta - 1) / rows_per_cta;
   const uint64_t cache_rows = (uint64_t)num_blocks * num_kv_heads * kBlockSize;
@@ -965,14 +1426,16 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = tc ? launch_prefill_tc(a, tk, tv, head_dim, st)
-                    : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
-                                      : launch_prefill_t<64, 4>(a, tk, tv, st);
+  const int rc = pair ? launch_prefill_pair(a, tk, tv, head_dim, st)
+                 : tc   ? launch_prefill_tc(a, tk, tv, head_dim, st)
+                 : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
+                                   : launch_prefill_t<64, 4>(a, tk, tv, st);
   return rc == 0 ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" int paged_attention_prefill_set_variant(int variant) {
-  if (variant != PKV_PREFILL_AUTO && variant != PKV_PREFILL_MMA && variant != PKV_PREFILL_TC)
+  if (variant != PKV_PREFILL_AUTO && variant != PKV_PREFILL_MMA && variant != PKV_PREFILL_TC &&
+      variant != PKV_PREFILL_TC_PAIR)
     return PKV_ERR_ARG;
   return g_prefill_variant.exchange(variant);
 }

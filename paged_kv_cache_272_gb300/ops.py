@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
-PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC = 0, 1, 2
+PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC, PKV_PREFILL_TC_PAIR = 0, 1, 2, 3
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
 DEV_BAD_SCALE, DEV_BAD_ROW = 32, 64
 DEFAULT_PARTITION = 512
