@@ -330,6 +330,7 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 #define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
 #define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
 #define PKV_PREFILL_TC_PAIR 3 /* tcgen05, two 128-row tiles per CTA sharing K/V tiles */
+#define PKV_PREFILL_TC_2SM 4  /* tcgen05 on SM pairs (M = 256), head_dim 128; else TC  */
 int paged_attention_prefill_set_variant(int variant);
 
 /*

@@ -1353,6 +1353,522 @@ int launch_prefill_pair(const PrefillArgs &a, const CUtensorMap &tk, const CUten
   }
 }
 
+// ------------------------------------------------------------------------------------
+// SM-pair variant (PKV_PREFILL_TC_2SM, head_dim 128): a cluster of two CTAs on two SMs
+// runs one chain over 256 query rows -- CTA rank r holds rows 128 r .. 128 r + 127 of the
+// pair: its own Q tile, softmax warps, S buffers and O accumulator in its TMEM -- and
+// rank 0 issues every product as tcgen05.mma.cta_group::2 (M = 256): one instruction
+// drives both SMs' tensor pipes, each reading its own A rows (Q, or P from its TMEM) and
+// its half of B from its own shared memory at the same offsets.  So each SM stages half
+// of every tile: the 32 keys 32 r .. 32 r + 31 of a K tile (score products, N = 64) and
+// the head-dim columns 64 r .. 64 r + 63 of a V tile (P V products, N = 128).  Per SM and
+// 64-key tile that halves the copies and the B operand reads, and halves the product
+// instructions an SM issues.  Two clusters share each pair of SMs (256 TMEM columns per
+// CTA).
+//  * warps 0-3 (both ranks): softmax of the CTA's 128 rows, as in the one-tile kernel;
+//    rank 1 signals its Q and each P to rank 0's barriers (remote mbarrier arrivals).
+//  * warp 4: rank 0 issues the score products; rank 1 forwards its K copies' completion
+//    to rank 0.  warp 7: rank 0 issues the P V products; rank 1 forwards its V copies'.
+//  * warps 5 / 6: this CTA's halves of the K / V tiles (TMA), into NS-slot rings.
+// Completion of the products (tcgen05.commit ... multicast) arrives at both CTAs'
+// barriers (S ready, K / V slot free, O updated, P V done, final).  Every wait is bounded;
+// both CTAs leave through one cluster barrier before the pair releases its tensor memory.
+constexpr int kPairCtaWarps = 8;
+
+template <int NS>
+struct Sm2Layout {
+  static constexpr int kQHalf = kTcRows * 128;  // 16 KB: 128 rows x 64 dims
+  static constexpr int kKPart = 32 * 128;       // 4 KB: 32 keys x 64 dims
+  static constexpr int kKSlot = 2 * kKPart;     // this CTA's 32 keys, both dim halves
+  static constexpr int kVSlot = kKeys * 128;    // 8 KB: 64 keys x this CTA's 64 dims
+  static constexpr int kQ = 0;
+  static constexpr int kK = 2 * kQHalf;
+  static constexpr int kV = kK + NS * kKSlot;
+  static constexpr int kBars = kV + NS * kVSlot;
+  // k_full, k_empty, kp_full, v_full, v_empty, vp_full [NS]; s_full[2], p_full[2],
+  // pv_done[2], o_done, fin, q_full
+  static constexpr int kNumBars = 6 * NS + 9;
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16;
+  // at least 78 KB, so that no more than two CTAs share an SM (256 TMEM columns each)
+  static constexpr int kSmemLaunch = kSmem > 78 * 1024 ? kSmem : 78 * 1024;
+};
+
+__device__ __forceinline__ bool mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_spin_wait for a barrier that the peer CTA also arrives on (acquire at cluster
+// scope, pairing with the peer's release): same give-up rules.
+__device__ inline bool mbar_spin_wait_cl(uint32_t bar, uint32_t parity, volatile int *abort,
+                                         int32_t *err, long long limit = kWaitCycles) {
+  if (mbar_test_wait_cl(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait_cl(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        flag_error(err, PKV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// One arrival on the barrier at the same shared-memory offset in CTA `rank` of the
+// cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc2_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc2_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Completion of this thread's earlier products arrives at the barrier at offset `bar`
+// in both CTAs of the pair.
+__device__ __forceinline__ void tc2_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kPairCtaWarps * 32, 2)
+    prefill_tc2sm_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv) {
+  constexpr int D = 128;
+  using Lay = Sm2Layout<NS>;
+  extern __shared__ __align__(1024) unsigned char smem_tc[];
+  const uint32_t base = smem_u32(smem_tc);
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  // The swizzled tiles need a 1024-byte aligned window; both CTAs run the same code, so
+  // a misaligned window is misaligned in both and both leave here.
+  if (base & 1023u) {
+    if (threadIdx.x == 0) flag_error(a.err, PKV_DEV_LAYOUT);
+    return;
+  }
+  const uint32_t sQ = base + Lay::kQ, sK = base + Lay::kK, sV = base + Lay::kV;
+  const uint32_t bars = base + Lay::kBars;
+  const uint32_t k_full = bars, k_empty = bars + 8 * NS, kp_full = bars + 16 * NS,
+                 v_full = bars + 24 * NS, v_empty = bars + 32 * NS, vp_full = bars + 40 * NS;
+  const uint32_t s_full = bars + 48 * NS, p_full = s_full + 16, pv_done = p_full + 16,
+                 o_done = pv_done + 16, fin = o_done + 8, q_full = fin + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_tc + Lay::kBars + Lay::kNumBars * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int pair = (a.row_tiles + 1) / 2 - 1 - (int)(blockIdx.x >> 1);  // latest rows first
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(k_full + 8 * i, 2);        // two producer lanes: this CTA's two K blocks
+      mbar_init(k_empty + 8 * i, 1);
+      mbar_init(kp_full + 8 * i, 1);       // rank 1's forwarded K completion (rank 0 only)
+      mbar_init(v_full + 8 * i, kTileBlocks);
+      mbar_init(v_empty + 8 * i, 1);
+      mbar_init(vp_full + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(p_full + 8 * i, 8);        // four softmax warps of each CTA (rank 0's copy)
+      mbar_init(pv_done + 8 * i, 1);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(fin, 1);
+    mbar_init(q_full, 8);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  // Both CTAs of a pair read the same sequence and rows, so they leave (or stay) together.
+  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+  const int ctx = a.context_lens[s];
+  const int L = q1 - q0;
+  if (q0 < 0 || L < 0 || q1 > a.num_tokens || L > a.max_query_len || L > ctx ||
+      ctx > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+    return;
+  }
+  const int G = a.group;
+  const int rows = L * G;
+  const int rp = pair * 2 * kTcRows;  // the pair's first row
+  if (rp >= rows) return;
+  const int first_pos = ctx - L;
+  const int kv_end = first_pos + (min(rp + 2 * kTcRows, rows) - 1) / G + 1;  // pair's last key + 1
+  const int nkt = (kv_end + kKeys - 1) / kKeys;
+
+  // Every barrier of both CTAs is initialised before either CTA arrives on the other's.
+  cluster_sync_all();
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;  // S buffers at columns 0 and 64, O after
+
+  if (warp < 4) {
+    // ---------------- softmax warps: thread t owns row t of this CTA ----------------
+    const int t = threadIdx.x;
+    const int r0 = rp + (int)rank * kTcRows;
+    const int r = r0 + t;
+    const bool valid = r < rows;
+    const int r_clamp = min(r, rows - 1);
+    const int pos = first_pos + r_clamp / G;
+    const int warp_pos_lo = first_pos + min(r0 + warp * 32, rows - 1) / G;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint16_t *orow = a.out + ((size_t)(q0 + r_clamp / G) * a.num_q_heads + g * G + r_clamp % G) * D;
+    {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          a.q + ((size_t)(q0 + r_clamp / G) * a.num_q_heads + g * G + r_clamp % G) * D);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = valid ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(sQ + (c >> 3) * Lay::kQHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4), v.x,
+                     v.y, v.z, v.w);
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cta(q_full, 0);  // this CTA's Q is staged
+
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int sb = j & 1;
+      const int t0 = j * kKeys;
+      if (!mbar_wait(s_full + 8 * sb, (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[64];
+      {
+        uint32_t (&x0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[0]);
+        uint32_t (&x1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[32]);
+        tmem_ld32(tS + 64 * sb + lane_base, x0);
+        tmem_ld32(tS + 64 * sb + 32 + lane_base, x1);
+        tmem_wait_ld();
+      }
+      // Keys past the row's position become -inf (diagonal tiles only; rows past the
+      // chunk take the last row's position, their outputs are not stored).
+      const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (t0 + c > pos) x[c] = __float_as_uint(-INFINITY);
+      }
+      float mxv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mxv[c] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2)
+        mxv[(c >> 1) & 7] =
+            max3f(mxv[(c >> 1) & 7], __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
+      float mx = max3f(max3f(mxv[0], mxv[1], mxv[2]), max3f(mxv[3], mxv[4], mxv[5]),
+                       fmaxf(mxv[6], mxv[7]));
+      mx *= a.scale_log2;
+      if (j == 0) {
+        m = mx;  // key 0 is visible to every row
+      } else {
+        const bool need = mx > m + 8.f;
+        if (__any_sync(kAll, need)) {
+          if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float mn = need ? mx : m;
+          const float corr = fast_exp2(m - mn);
+          m = mn;
+          l *= corr;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * cc + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(tO + 32 * cc + lane_base, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      uint32_t pk[32];
+      uint64_t ps2[4];
+      const uint64_t sl2 = f32x2(a.scale_log2, a.scale_log2), nm2 = f32x2(-m, -m);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float e0, e1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])),
+                              sl2, nm2),
+                    e0, e1);
+        const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+        const uint64_t pp = f32x2(p0, p1);
+        ps2[c & 3] = c < 4 ? pp : add_f32x2(ps2[c & 3], pp);
+        pk[c] = pack_bf16(p0, p1);
+      }
+      {
+        float s0, s1;
+        f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+        l += s0 + s1;
+      }
+      if (t0 + kKeys > kv_end) {
+        // Last tile: this CTA's V columns in rows at or past kv_end (tail of the last
+        // block, blocks not staged) are set to zero, so that zero weights add nothing.
+        const int slot = j % NS;
+        if (!mbar_wait(v_full + 8 * slot, (uint32_t)(j / NS) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vst = sV + slot * Lay::kVSlot;
+        const int z0 = kv_end - t0;
+        for (int i = t; i < (kKeys - z0) * 8; i += 128) {
+          const int row = z0 + i / 8, rem = i % 8;
+          st_shared_v4(vst + row * 128 + rem * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();
+      }
+      // P overwrites the first 32 columns of this tile's S buffer (already read).
+      tmem_st32(tS + 64 * sb + lane_base, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(p_full + 8 * sb, 0);
+    }
+    // Every product has completed once rank 0's final commit fires.
+    if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
+    if (ok && !*abort_flag) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc + lane_base, o);
+        tmem_wait_ld();
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(
+                pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (warp == 4 || warp == 7) {
+    const bool is_pv = warp == 7;
+    if (rank == 1) {
+      // ---------------- rank 1: forward this CTA's K (warp 4) / V (warp 7) copies ------
+      const uint32_t full = is_pv ? v_full : k_full, fwd = is_pv ? vp_full : kp_full;
+      if (lane == 0)
+        for (int j = 0; j < nkt; ++j) {
+          if (!mbar_wait(full + 8 * (j % NS), (uint32_t)(j / NS) & 1u, abort_flag, a.err)) break;
+          mbar_arrive_cta(fwd + 8 * (j % NS), 0);
+        }
+      __syncwarp();
+    } else if (!is_pv) {
+      // ---------------- rank 0, warp 4: S_j = Q K_j^T for both CTAs' rows ----------------
+      tc_fence_after();
+      constexpr uint32_t idS = bf16_idesc(2 * kTcRows, kKeys, false);
+      int ok = 1;
+      if (lane == 0) ok = mbar_spin_wait_cl(q_full, 0u, abort_flag, a.err);
+      int js = 0;
+      if (__shfl_sync(kAll, ok, 0))
+        for (; js < nkt; ++js) {
+          const int sb = js & 1, slot = js % NS;
+          if (lane == 0)
+            ok = mbar_spin_wait(k_full + 8 * slot, (uint32_t)(js / NS) & 1u, abort_flag, a.err) &&
+                 mbar_spin_wait_cl(kp_full + 8 * slot, (uint32_t)(js / NS) & 1u, abort_flag,
+                                   a.err) &&
+                 (js < 2 || mbar_spin_wait(pv_done + 8 * sb, (uint32_t)((js - 2) >> 1) & 1u,
+                                           abort_flag, a.err));
+          if (!__shfl_sync(kAll, ok, 0)) break;
+          tc_fence_after();
+          const uint32_t kst = sK + slot * Lay::kKSlot;
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc2_mma(tS + 64 * sb,
+                      sw128_desc(sQ + (kk >> 2) * Lay::kQHalf + (kk & 3) * 32, 16, 1024),
+                      sw128_desc(kst + (kk >> 2) * Lay::kKPart + (kk & 3) * 32, 16, 1024), idS,
+                      kk > 0 ? 1u : 0u);
+            tc2_commit(s_full + 8 * sb);
+            tc2_commit(k_empty + 8 * slot);
+          }
+          __syncwarp();
+        }
+      // the products this thread issued have completed once its last commit fires
+      if (lane == 0 && js > 0) mbar_drain(s_full + 8 * ((js - 1) & 1), (uint32_t)((js - 1) >> 1) & 1u);
+      __syncwarp();
+      tc_fence_before();
+    } else {
+      // ---------------- rank 0, warp 7: O += P_j V_j for both CTAs' rows ----------------
+      tc_fence_after();
+      constexpr uint32_t idO = bf16_idesc(2 * kTcRows, D, true);
+      for (int jp = 0; jp < nkt; ++jp) {
+        const int slot = jp % NS;
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_spin_wait_cl(p_full + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag,
+                                 a.err) &&
+               mbar_spin_wait(v_full + 8 * slot, (uint32_t)(jp / NS) & 1u, abort_flag, a.err) &&
+               mbar_spin_wait_cl(vp_full + 8 * slot, (uint32_t)(jp / NS) & 1u, abort_flag, a.err);
+        if (!__shfl_sync(kAll, ok, 0)) break;
+        tc_fence_after();
+        const uint32_t vst = sV + slot * Lay::kVSlot;
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < kKeys / 16; ++k)
+            tc2_mma_ts(tO, tS + 64 * (jp & 1) + 8 * k, sw128_desc(vst + 2048 * k, 8192, 1024),
+                       idO, (jp > 0 || k > 0) ? 1u : 0u);
+          tc2_commit(o_done);
+          tc2_commit(v_empty + 8 * slot);
+          tc2_commit(pv_done + 8 * (jp & 1));
+        }
+        __syncwarp();
+      }
+      if (lane == 0) tc2_commit(fin);
+      __syncwarp();
+      mbar_drain(fin, 0);
+      tc_fence_before();
+    }
+  } else {
+    // ---------------- copy warps: warp 5 K (this CTA's 32 keys), warp 6 V (its 64 dims) --
+    const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
+    const bool is_v = warp == 6;
+    const uint32_t full = is_v ? v_full : k_full, empty = is_v ? v_empty : k_empty;
+    const int nlanes = is_v ? kTileBlocks : 2;
+    // K: lane b copies block 2 rank + b of the tile (both dim halves); V: lane b copies
+    // block b (the CTA's dim half)
+    const int blk_in_tile = is_v ? lane : 2 * (int)rank + lane;
+    const CUtensorMap *map = is_v ? &tv : &tk;
+    int issued = 0;
+    if (lane < nlanes) {
+      int next = blk_in_tile * kBlockSize < kv_end ? table[blk_in_tile] : INT_MIN;
+      for (int j = 0; j < nkt; ++j) {
+        const int slot = j % NS;
+        int blk = next;
+        const int tok_n = (j + 1) * kKeys + blk_in_tile * kBlockSize;
+        next = (j + 1 < nkt && tok_n < kv_end) ? table[tok_n / kBlockSize] : INT_MIN;
+        if (j >= NS &&
+            !mbar_wait(empty + 8 * slot, (uint32_t)((j - NS) / NS) & 1u, abort_flag, a.err))
+          break;
+        if (blk != INT_MIN && (blk < 0 || blk >= a.num_blocks)) {
+          flag_error(a.err, PKV_DEV_BAD_BLOCK);
+          blk = INT_MIN;
+        }
+        const uint32_t bar = full + 8 * slot;
+        mbar_arrive_expect_tx(bar, blk != INT_MIN ? (is_v ? 2048u : 4096u) : 0u);
+        if (blk != INT_MIN) {
+          const int row = (blk * a.num_kv_heads + g) * kBlockSize;
+          if (is_v) {
+            tma_load_2d(sV + slot * Lay::kVSlot + lane * 2048, map, 64 * (int)rank, row, bar);
+          } else {
+            const uint32_t dst = sK + slot * Lay::kKSlot + lane * 2048;
+            tma_load_2d(dst, map, 0, row, bar);
+            tma_load_2d(dst + Lay::kKPart, map, 64, row, bar);
+          }
+        }
+        issued = j + 1;
+      }
+    }
+    __syncwarp();
+    // If a wait gave up, let the copies still in flight land before the CTA exits.
+    if (lane == 0 && *abort_flag)
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        mbar_drain(full + 8 * (j % NS), (uint32_t)(j / NS) & 1u);
+  }
+
+  __syncthreads();
+  // Neither CTA releases the pair's tensor memory, or exits, while the other may still
+  // read it or arrive on its barriers.
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+template <int NS>
+int launch_prefill_2sm_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                         cudaStream_t st) {
+  using Lay = Sm2Layout<NS>;
+  static std::atomic<int> ready[kMaxDevices];  // shared-memory opt-in, per device
+  const int r = per_device_setup(ready, [] {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc2sm_kernel<NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay::kSmemLaunch);
+    return e == cudaSuccess ? 1 : -(int)e;
+  });
+  if (r <= 0) return -r;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * ((a.row_tiles + 1) / 2)), (unsigned)a.num_kv_heads,
+                     (unsigned)a.num_seqs);
+  cfg.blockDim = dim3(kPairCtaWarps * 32);
+  cfg.dynamicSmemBytes = (size_t)Lay::kSmemLaunch;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return (int)cudaLaunchKernelEx(&cfg, prefill_tc2sm_kernel<NS>, a, tk, tv);
+}
+
 // P kept in tensor memory by default (the A operand of P V read from TMEM: no shared-
 // memory traffic for P, 6% faster on GB300); PKV_PREFILL_P=smem selects the variant that
 // stages P in shared memory.
@@ -1397,6 +1913,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
   const int variant = g_prefill_variant.load();
   const bool tc = variant != PKV_PREFILL_MMA;
   const bool pair = variant == PKV_PREFILL_TC_PAIR;
+  const bool sm2 = variant == PKV_PREFILL_TC_2SM && head_dim == 128;
   const int rows_per_cta = tc ? kTcRows : kRows;
   const int64_t tiles = ((int64_t)max_query_len * group + rows_per_cta - 1) / rows_per_cta;
   const uint64_t cache_rows = (uint64_t)num_blocks * num_kv_heads * kBlockSize;
@@ -1426,7 +1943,8 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = pair ? launch_prefill_pair(a, tk, tv, head_dim, st)
+  const int rc = sm2    ? launch_prefill_2sm_t<3>(a, tk, tv, st)
+                 : pair ? launch_prefill_pair(a, tk, tv, head_dim, st)
                  : tc   ? launch_prefill_tc(a, tk, tv, head_dim, st)
                  : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
                                    : launch_prefill_t<64, 4>(a, tk, tv, st);
@@ -1435,7 +1953,7 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
 
 extern "C" int paged_attention_prefill_set_variant(int variant) {
   if (variant != PKV_PREFILL_AUTO && variant != PKV_PREFILL_MMA && variant != PKV_PREFILL_TC &&
-      variant != PKV_PREFILL_TC_PAIR)
+      variant != PKV_PREFILL_TC_PAIR && variant != PKV_PREFILL_TC_2SM)
     return PKV_ERR_ARG;
   return g_prefill_variant.exchange(variant);
 }
