@@ -193,3 +193,38 @@ def test_gather_rows_bit_exact_and_flags_bad_rows():
     ops.paged_gather_rows(d1, one.cuda(), torch.zeros(0, dtype=torch.int64, device="cuda"))
     torch.cuda.synchronize()
     assert torch.equal(d1.cpu(), one.expand(3, 8))
+
+
+def test_engine_step_records_its_events():
+    """pkv_engine_step records the caller's events (before the staging copy, around the
+    decode step) on the stream, in order, and records none for a step with no tokens."""
+    import ctypes
+    from paged_kv_cache_272_gb300.block_pool import BlockPool
+    from paged_kv_cache_272_gb300.driver import ServingDriver
+    from paged_kv_cache_272_gb300.serving import Scheduler
+    reqs = workloads.make_requests("pareto", seed=23, n=6)
+    pool = BlockPool(200)
+    drv = ServingDriver(Scheduler(pool, 4, 64), 200, 8, 2, 128,
+                        max(len(r.prompt) + min(r.output_len, 12) for r in reqs), seed=4)
+    for r in reqs:
+        drv.add_request(r.rid, r.prompt, min(r.output_len, 12))
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev:
+        e.record(stream)  # creates the events
+    stream.synchronize()
+    handles = (ctypes.c_void_p * 3)(ev[0].cuda_event, ev[1].cuda_event, ev[2].cuda_event)
+    timed = 0
+    slot = 0
+    while not drv.done():
+        pk, hd, hl = drv.engine_step(slot, handles)
+        if pk.num_tokens == 0:
+            continue
+        ev[3].record(stream)
+        ev[3].synchronize()
+        t_all = ev[0].elapsed_time(ev[3])
+        t_dec = ev[1].elapsed_time(ev[2])
+        assert 0.0 < t_dec <= t_all and ev[0].elapsed_time(ev[1]) >= 0.0
+        timed += 1
+        slot ^= 1
+    assert timed > 3 and int(drv.err.item()) == 0
