@@ -323,8 +323,9 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 
 /*
  * Chunked-prefill kernel selection, process-wide (for measurement; default AUTO = the
- * tcgen05 kernel, for head_dim 64 and 128).  Returns the
- * previous value, or PKV_ERR_ARG for an unknown value.
+ * one-tile tcgen05 kernel, for head_dim 64 and 128, the fastest measured on GB300; the
+ * two-tile and SM-pair variants compute the same result and are kept for comparison).
+ * Returns the previous value, or PKV_ERR_ARG for an unknown value.
  */
 #define PKV_PREFILL_AUTO 0
 #define PKV_PREFILL_MMA 1  /* mma.sync tiles, 64 rows per CTA                         */
