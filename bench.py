@@ -764,7 +764,7 @@ def run_prefill(args):
     torch.cuda.set_device(dev)
     pk = {"auto": ops.PKV_PREFILL_AUTO, "mma": ops.PKV_PREFILL_MMA,
           "tc": ops.PKV_PREFILL_TC, "tc_pair": ops.PKV_PREFILL_TC_PAIR,
-          "tc_2sm": ops.PKV_PREFILL_TC_2SM}[args.prefill_kernel]
+          "tc_2sm": ops.PKV_PREFILL_TC_2SM, "tc_sep": ops.PKV_PREFILL_TC_SEP}[args.prefill_kernel]
     ops.set_prefill_variant(pk)
     w = workloads.make_prefill_config(args.config, device="cuda", seed=args.seed)
     T, Hq, Hkv, D = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -871,9 +871,10 @@ def run_prefill(args):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (attn_ms / 1e3) / 1e12
-    # AUTO runs the one-tile tcgen05 kernel (head_dim 64 and 128)
+    # AUTO runs the separate-P tcgen05 kernel (head_dim 64 and 128)
     kname = {ops.PKV_PREFILL_TC_PAIR: "prefill-tc-pair", ops.PKV_PREFILL_MMA: "prefill-mma",
-             ops.PKV_PREFILL_TC_2SM: "prefill-tc-2sm"}.get(pk, "prefill-tc")
+             ops.PKV_PREFILL_TC_2SM: "prefill-tc-2sm", ops.PKV_PREFILL_TC: "prefill-tc",
+             ops.PKV_PREFILL_TC_SEP: "prefill-tc-sep"}.get(pk, "prefill-tc-sep")
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
@@ -906,6 +907,9 @@ def run_prefill(args):
                                 "prefill-tc-pair": "paged_attention_prefill: "
                                                    "prefill_tc_pair_kernel (tcgen05.mma, two "
                                                    "query tiles per CTA sharing K/V tiles)",
+                                "prefill-tc-sep": "paged_attention_prefill: "
+                                                  "prefill_tcs_kernel (tcgen05.mma, one S "
+                                                  "buffer, P and half of Q in TMEM)",
                                 "prefill-tc-2sm": "paged_attention_prefill: "
                                                   "prefill_tc2sm_kernel (tcgen05.mma "
                                                   "cta_group::2, SM pairs)",
@@ -1206,8 +1210,9 @@ def main():
     ap.add_argument("--fp8-scales", default="cache", choices=["cache", "head"],
                     help="with --kv-dtype fp8: one E4M3 scale per cache, or one per KV head")
     ap.add_argument("--prefill-kernel", default="auto",
-                    choices=["auto", "mma", "tc", "tc_pair", "tc_2sm"],
-                    help="chunked-prefill kernel: tcgen05 (tc) or mma.sync (mma); auto = tc")
+                    choices=["auto", "mma", "tc", "tc_sep", "tc_pair", "tc_2sm"],
+                    help="chunked-prefill kernel: tcgen05 variants (tc_sep, tc, tc_pair, "
+                         "tc_2sm) or mma.sync (mma); auto = tc_sep")
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="decode step through paged_decode_step (one call, default) or the "
                          "three separate calls (copy, write, attention)")

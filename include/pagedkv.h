@@ -323,8 +323,8 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 
 /*
  * Chunked-prefill kernel selection, process-wide (for measurement; default AUTO = the
- * one-tile tcgen05 kernel, for head_dim 64 and 128, the fastest measured on GB300; the
- * two-tile and SM-pair variants compute the same result and are kept for comparison).
+ * separate-P tcgen05 kernel, for head_dim 64 and 128, the fastest measured on GB300; the
+ * others compute the same result and are kept for comparison).
  * Returns the previous value, or PKV_ERR_ARG for an unknown value.
  */
 #define PKV_PREFILL_AUTO 0
@@ -332,6 +332,7 @@ int paged_attention_prefill(uint16_t *out, const uint16_t *q, const uint16_t *k_
 #define PKV_PREFILL_TC 2   /* tcgen05 tiles with TMEM accumulators, 128 rows per CTA  */
 #define PKV_PREFILL_TC_PAIR 3 /* tcgen05, two 128-row tiles per CTA sharing K/V tiles */
 #define PKV_PREFILL_TC_2SM 4  /* tcgen05 on SM pairs (M = 256), head_dim 128; else TC  */
+#define PKV_PREFILL_TC_SEP 5  /* tcgen05, one S buffer, P and half of Q in own TMEM    */
 int paged_attention_prefill_set_variant(int variant);
 
 /*

@@ -872,6 +872,423 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
   }
 }
 
+// ------------------------------------------------------------------------------------
+// Separate-P variant (PKV_PREFILL_TC_SEP): the same CTA, warps and rings as the kernel
+// above, with another TMEM layout (256 columns): one S buffer at columns 0..63, P (bf16
+// pairs) at 64..95, the first 64 head-dim columns of Q at 96..127 and O at 128.  S is
+// free again as soon as the softmax has read it into registers, so the next score
+// product is issued while the softmax of this tile runs (it no longer waits for the
+// P V product that read P out of S's columns), and P's one buffer is free once the
+// previous P V product has completed -- well before the softmax needs it again.  The
+// score products take their A operand for head-dim columns 0..63 from TMEM (only the K
+// tile is read from shared memory there) and for 64..127 from shared memory.
+// Shared memory: Q's head-dim columns 64..127 (D 128 only), then NS-slot K and V rings.
+template <int D, int NS>
+struct SepLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQHalf = kTcRows * 128;           // 16 KB: 128 rows x 64 dims
+  static constexpr int kKHalf = kKeys * 128;             // 8 KB: 64 keys x 64 dims
+  static constexpr int kSlot = kHalves * kKHalf;         // one K or V tile
+  static constexpr int kQ = 0;
+  static constexpr int kK = (kHalves - 1) * kQHalf;
+  static constexpr int kV = kK + NS * kSlot;
+  static constexpr int kBars = kV + NS * kSlot;
+  static constexpr int kNumBars = 4 * NS + 5;  // K/V full and empty [NS]; S full, S free,
+                                               // P full, O done, final
+  static constexpr int kSmem = kBars + kNumBars * 8 + 16;
+  // at least 78 KB, so that no more than two CTAs share an SM (256 TMEM columns each)
+  static constexpr int kSmemLaunch = kSmem > 78 * 1024 ? kSmem : 78 * 1024;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(kTcWarps * 32, 2)
+    prefill_tcs_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv) {
+  using Lay = SepLayout<D, NS>;
+  constexpr int H = Lay::kHalves;
+  extern __shared__ __align__(1024) unsigned char smem_tc[];
+  const uint32_t base = smem_u32(smem_tc);
+  if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
+    if (threadIdx.x == 0) flag_error(a.err, PKV_DEV_LAYOUT);
+    return;
+  }
+  const uint32_t sQ = base + Lay::kQ;
+  const uint32_t sK = base + Lay::kK, sV = base + Lay::kV;
+  const uint32_t k_full = base + Lay::kBars, k_empty = k_full + 8 * NS;
+  const uint32_t v_full = k_empty + 8 * NS, v_empty = v_full + 8 * NS;
+  const uint32_t s_full = v_empty + 8 * NS, s_free = s_full + 8, p_full = s_free + 8;
+  const uint32_t o_done = p_full + 8, fin = o_done + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_tc + Lay::kBars + Lay::kNumBars * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int tile = a.row_tiles - 1 - (int)blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(k_full + 8 * i, kTileBlocks);
+      mbar_init(k_empty + 8 * i, 1);
+      mbar_init(v_full + 8 * i, kTileBlocks);
+      mbar_init(v_empty + 8 * i, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+  const int ctx = a.context_lens[s];
+  const int L = q1 - q0;
+  if (q0 < 0 || L < 0 || q1 > a.num_tokens || L > a.max_query_len || L > ctx ||
+      ctx > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, PKV_DEV_BAD_CONTEXT);
+    return;
+  }
+  const int G = a.group;
+  const int rows = L * G;
+  const int r0 = tile * kTcRows;
+  if (r0 >= rows) return;
+  const int first_pos = ctx - L;
+  const int r_last = min(r0 + kTcRows, rows) - 1;
+  const int kv_end = first_pos + r_last / G + 1;
+  const int nkt = (kv_end + kKeys - 1) / kKeys;
+
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tP = tmem + 64, tQ = tmem + 96, tO = tmem + 128;
+
+  if (warp < 4) {
+    // ---------------- softmax warps: thread t owns row t ----------------
+    const int t = threadIdx.x;
+    const int r = r0 + t;
+    const bool valid = r < rows;
+    const int pos = first_pos + (valid ? r : r_last) / G;
+    const int warp_pos_lo = first_pos + min(r0 + warp * 32, r_last) / G;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint16_t *orow = a.out + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D;
+    {
+      // Q: head-dim columns 0..63 into TMEM (row t = lane t of this warp's quarter, two
+      // bf16 per column, the lower column in the low half), 64..127 into shared memory.
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          a.q + ((size_t)(q0 + r / G) * a.num_q_heads + g * G + r % G) * D);
+      uint32_t qt[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = valid ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+        qt[4 * c] = v.x, qt[4 * c + 1] = v.y, qt[4 * c + 2] = v.z, qt[4 * c + 3] = v.w;
+      }
+      tmem_st32(tQ + lane_base, qt);
+#pragma unroll
+      for (int c = 8; c < 8 * H; ++c) {
+        const uint4 v = valid ? qrow[c] : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(sQ + t * 128 + (((c & 7) ^ (t & 7)) << 4),
+                     v.x, v.y, v.z, v.w);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    named_bar_sync(1, 160);
+
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int t0 = j * kKeys;
+      if (!mbar_wait(s_full, (uint32_t)j & 1u, abort_flag, a.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[64];
+      {
+        uint32_t (&x0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[0]);
+        uint32_t (&x1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&x[32]);
+        tmem_ld32(tS + lane_base, x0);
+        tmem_ld32(tS + 32 + lane_base, x1);
+        tmem_wait_ld();
+      }
+      // S has been read: the next score product may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+
+      // Raw scores; keys past the row's position become -inf (diagonal tiles only).
+      const bool need_mask = t0 + kKeys - 1 > warp_pos_lo;
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (t0 + c > pos) x[c] = __float_as_uint(-INFINITY);
+      }
+      float mxv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mxv[c] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2)
+        mxv[(c >> 1) & 7] =
+            max3f(mxv[(c >> 1) & 7], __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
+      float mx = max3f(max3f(mxv[0], mxv[1], mxv[2]), max3f(mxv[3], mxv[4], mxv[5]),
+                       fmaxf(mxv[6], mxv[7]));
+      mx *= a.scale_log2;
+      bool p_free = j == 0;  // P's buffer: free once P V j - 1 has completed
+      if (j == 0) {
+        m = mx;  // key 0 is visible to every row
+      } else {
+        const bool need = mx > m + 8.f;
+        if (__any_sync(kAll, need)) {
+          if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          p_free = true;
+          tc_fence_after();
+          const float mn = need ? mx : m;
+          const float corr = fast_exp2(m - mn);
+          m = mn;
+          l *= corr;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * cc + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(tO + 32 * cc + lane_base, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      uint32_t pk[32];
+      uint64_t ps2[4];
+      const uint64_t sl2 = f32x2(a.scale_log2, a.scale_log2), nm2 = f32x2(-m, -m);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float e0, e1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])),
+                              sl2, nm2),
+                    e0, e1);
+        const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+        const uint64_t pp = f32x2(p0, p1);
+        ps2[c & 3] = c < 4 ? pp : add_f32x2(ps2[c & 3], pp);
+        pk[c] = pack_bf16(p0, p1);
+      }
+      {
+        float s0, s1;
+        f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+        l += s0 + s1;
+      }
+      if (t0 + kKeys > kv_end) {
+        // Last tile: V rows at or past kv_end (tail of the last block, blocks not staged)
+        // are set to zero so that their zero weights contribute exactly nothing.
+        if (!mbar_wait(v_full + 8 * (j % NS), (uint32_t)(j / NS) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vst = sV + (j % NS) * Lay::kSlot;
+        const int z0 = kv_end - t0;
+        for (int i = t; i < (kKeys - z0) * 8 * H; i += 128) {
+          const int row = z0 + i / (8 * H), rem = i % (8 * H);
+          st_shared_v4(vst + (rem >> 3) * Lay::kKHalf + row * 128 + (rem & 7) * 16, 0u, 0u, 0u,
+                       0u);
+        }
+        fence_proxy_async();
+      }
+      if (!p_free) {
+        if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tP + lane_base, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // Every product has completed once the P V warp's final commit fires.
+    if (ok && !mbar_wait(fin, 0u, abort_flag, a.err)) ok = false;
+    if (ok && !*abort_flag) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc + lane_base, o);
+        tmem_wait_ld();
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(
+                pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (warp == 4) {
+    // ---------------- S warp: lane 0 issues S_j = Q K_j^T ----------------
+    named_bar_sync(1, 160);
+    tc_fence_after();
+    constexpr uint32_t idS = bf16_idesc(kTcRows, kKeys, false);
+    int js = 0;
+    for (; js < nkt; ++js) {
+      const int sb = js % NS;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_spin_wait(k_full + 8 * sb, (uint32_t)(js / NS) & 1u, abort_flag, a.err) &&
+             (js < 1 || mbar_spin_wait(s_free, (uint32_t)(js - 1) & 1u, abort_flag, a.err));
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t kst = sK + sb * Lay::kSlot;
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bdesc = sw128_desc(kst + (kk >> 2) * Lay::kKHalf + (kk & 3) * 32, 16, 1024);
+          if (kk < 4)  // head-dim columns 0..63: Q from TMEM
+            tc_mma_ts(tS, tQ + 8 * kk, bdesc, idS, kk > 0 ? 1u : 0u);
+          else
+            tc_mma(tS, sw128_desc(sQ + (kk & 3) * 32, 16, 1024),
+                   bdesc, idS, 1u);
+        }
+        tc_commit(s_full);
+        tc_commit(k_empty + 8 * sb);
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && js > 0) mbar_drain(s_full, (uint32_t)(js - 1) & 1u);
+    __syncwarp();
+    tc_fence_before();
+  } else if (warp == 7) {
+    // ---------------- P V warp: lane 0 issues O += P_j V_j ----------------
+    tc_fence_after();
+    constexpr uint32_t idO = bf16_idesc(kTcRows, D, true);
+    for (int jp = 0; jp < nkt; ++jp) {
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_spin_wait(p_full, (uint32_t)jp & 1u, abort_flag, a.err) &&
+             mbar_spin_wait(v_full + 8 * (jp % NS), (uint32_t)(jp / NS) & 1u, abort_flag, a.err);
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      tc_fence_after();
+      const uint32_t vst = sV + (jp % NS) * Lay::kSlot;
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k)
+          tc_mma_ts(tO, tP + 8 * k, sw128_desc(vst + 2048 * k, Lay::kKHalf, 1024), idO,
+                    (jp > 0 || k > 0) ? 1u : 0u);
+        tc_commit(o_done);
+        tc_commit(v_empty + 8 * (jp % NS));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) tc_commit(fin);
+    __syncwarp();
+    mbar_drain(fin, 0);
+    tc_fence_before();
+  } else {
+    // ---------------- producer warps: warp 5 stages K, warp 6 V; lane b block b ----------------
+    const int32_t *table = a.block_tables + (size_t)s * a.max_blocks;
+    const bool is_v = warp == 6;
+    const uint32_t full = is_v ? v_full : k_full, empty = is_v ? v_empty : k_empty;
+    const uint32_t ring = is_v ? sV : sK;
+    const CUtensorMap *map = is_v ? &tv : &tk;
+    int issued = 0;
+    if (lane < kTileBlocks) {
+      int next = lane * kBlockSize < kv_end ? table[lane] : INT_MIN;
+      for (int j = 0; j < nkt; ++j) {
+        const int slot = j % NS;
+        int blk = next;
+        const int tok_n = (j + 1) * kKeys + lane * kBlockSize;
+        next = (j + 1 < nkt && tok_n < kv_end) ? table[tok_n / kBlockSize] : INT_MIN;
+        if (j >= NS &&
+            !mbar_wait(empty + 8 * slot, (uint32_t)((j - NS) / NS) & 1u, abort_flag, a.err))
+          break;
+        if (blk != INT_MIN && (blk < 0 || blk >= a.num_blocks)) {
+          flag_error(a.err, PKV_DEV_BAD_BLOCK);
+          blk = INT_MIN;
+        }
+        const uint32_t bar = full + 8 * slot;
+        mbar_arrive_expect_tx(bar, blk != INT_MIN ? 2048u * H : 0u);
+        if (blk != INT_MIN) {
+          const int row = (blk * a.num_kv_heads + g) * kBlockSize;
+          const uint32_t dst = ring + slot * Lay::kSlot + lane * 2048;
+#pragma unroll
+          for (int h = 0; h < H; ++h) tma_load_2d(dst + h * Lay::kKHalf, map, 64 * h, row, bar);
+        }
+        issued = j + 1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && *abort_flag)
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        mbar_drain(full + 8 * (j % NS), (uint32_t)(j / NS) & 1u);
+  }
+
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+template <int D, int NS>
+int launch_prefill_tcs_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                         cudaStream_t st) {
+  using Lay = SepLayout<D, NS>;
+  static std::atomic<int> ready[kMaxDevices];  // shared-memory opt-in and carve-out, per device
+  const int r = per_device_setup(ready, [] {
+    cudaError_t e = cudaFuncSetAttribute(
+        prefill_tcs_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemLaunch);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_tcs_kernel<D, NS>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    return e == cudaSuccess ? 1 : -(int)e;
+  });
+  if (r <= 0) return -r;
+  return (int)launch_pdl(prefill_tcs_kernel<D, NS>,
+                         dim3((unsigned)a.row_tiles, (unsigned)a.num_kv_heads,
+                              (unsigned)a.num_seqs),
+                         dim3(kTcWarps * 32), (size_t)Lay::kSmemLaunch, st, a, tk, tv);
+}
+
+// K/V ring depth of the separate-P kernel: 3 slots each (the shared memory the P tile
+// and Q's first half used in the kernel above), overridable for tuning through
+// PKV_PREFILL_SEP_STAGES (2 or 3).  Measured on chunked-prefill config 2 / 3: 2 slots
+// 1212-1237 / 1044 TFLOP/s, 3 slots 1219-1220 / 1123.
+int launch_prefill_sep(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                       int head_dim, cudaStream_t st) {
+  static const int stages = [] {  // read once (thread-safe static initialisation)
+    const char *v = std::getenv("PKV_PREFILL_SEP_STAGES");
+    return v && std::atoi(v) == 2 ? 2 : 3;
+  }();
+  if (head_dim == 64)
+    return stages == 3 ? launch_prefill_tcs_t<64, 3>(a, tk, tv, st)
+                       : launch_prefill_tcs_t<64, 2>(a, tk, tv, st);
+  return stages == 3 ? launch_prefill_tcs_t<128, 3>(a, tk, tv, st)
+                     : launch_prefill_tcs_t<128, 2>(a, tk, tv, st);
+}
+
 template <int D, bool PT>
 int launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                         cudaStream_t st) {
@@ -1914,6 +2331,8 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
   const bool tc = variant != PKV_PREFILL_MMA;
   const bool pair = variant == PKV_PREFILL_TC_PAIR;
   const bool sm2 = variant == PKV_PREFILL_TC_2SM && head_dim == 128;
+  // AUTO: the separate-P tcgen05 kernel (the fastest measured, head_dim 64 and 128)
+  const bool sep = variant == PKV_PREFILL_TC_SEP || variant == PKV_PREFILL_AUTO;
   const int rows_per_cta = tc ? kTcRows : kRows;
   const int64_t tiles = ((int64_t)max_query_len * group + rows_per_cta - 1) / rows_per_cta;
   const uint64_t cache_rows = (uint64_t)num_blocks * num_kv_heads * kBlockSize;
@@ -1943,7 +2362,8 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
       !kv_tensor_map(&tv, v_cache, cache_rows, head_dim, 2))
     return PKV_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = sm2    ? launch_prefill_2sm_t<3>(a, tk, tv, st)
+  const int rc = sep    ? launch_prefill_sep(a, tk, tv, head_dim, st)
+                 : sm2  ? launch_prefill_2sm_t<3>(a, tk, tv, st)
                  : pair ? launch_prefill_pair(a, tk, tv, head_dim, st)
                  : tc   ? launch_prefill_tc(a, tk, tv, head_dim, st)
                  : head_dim == 128 ? launch_prefill_t<128, 3>(a, tk, tv, st)
@@ -1953,7 +2373,8 @@ extern "C" int paged_attention_prefill(uint16_t *out, const uint16_t *q, const u
 
 extern "C" int paged_attention_prefill_set_variant(int variant) {
   if (variant != PKV_PREFILL_AUTO && variant != PKV_PREFILL_MMA && variant != PKV_PREFILL_TC &&
-      variant != PKV_PREFILL_TC_PAIR && variant != PKV_PREFILL_TC_2SM)
+      variant != PKV_PREFILL_TC_PAIR && variant != PKV_PREFILL_TC_2SM &&
+      variant != PKV_PREFILL_TC_SEP)
     return PKV_ERR_ARG;
   return g_prefill_variant.exchange(variant);
 }

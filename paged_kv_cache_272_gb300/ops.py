@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_ATTN_AUTO, PKV_ATTN_FMA, PKV_ATTN_MMA = 0, 1, 2
 PKV_PREFILL_AUTO, PKV_PREFILL_MMA, PKV_PREFILL_TC, PKV_PREFILL_TC_PAIR = 0, 1, 2, 3
-PKV_PREFILL_TC_2SM = 4
+PKV_PREFILL_TC_2SM, PKV_PREFILL_TC_SEP = 4, 5
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CONTEXT, DEV_TIMEOUT = 1, 2, 4, 8
 DEV_BAD_SCALE, DEV_BAD_ROW = 32, 64
 DEFAULT_PARTITION = 512

@@ -18,14 +18,14 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-@pytest.fixture(params=["tc", "tc_pair", "tc_2sm", "mma"])
+@pytest.fixture(params=["tc", "tc_sep", "tc_pair", "tc_2sm", "mma"])
 def variant(request):
     """Run a test with each prefill kernel: tcgen05 with one 128-row tile per CTA, tcgen05
     with two tiles per CTA sharing the K/V tiles, tcgen05 on SM pairs (head_dim 128; 64
     runs the one-tile kernel), and mma.sync (all take head_dim 64 and 128)."""
     o = H.ops()
     prev = o.set_prefill_variant({"tc": o.PKV_PREFILL_TC, "tc_pair": o.PKV_PREFILL_TC_PAIR,
-                                  "tc_2sm": o.PKV_PREFILL_TC_2SM,
+                                  "tc_2sm": o.PKV_PREFILL_TC_2SM, "tc_sep": o.PKV_PREFILL_TC_SEP,
                                   "mma": o.PKV_PREFILL_MMA}[request.param])
     yield request.param
     o.set_prefill_variant(prev)
@@ -191,7 +191,8 @@ def test_prefill_long_context_rows():
     ctx, L = [9000, 3000, 700], [40, 300, 129]
     w = workloads.build_prefill("prefill-long", ctx, L, 16, 2, 128, seed=99, device="cuda")
     w.q.mul_(4)  # sharper softmax: the running maximum moves more
-    for v in (o.PKV_PREFILL_TC, o.PKV_PREFILL_TC_PAIR, o.PKV_PREFILL_TC_2SM, o.PKV_PREFILL_MMA):
+    for v in (o.PKV_PREFILL_TC, o.PKV_PREFILL_TC_SEP, o.PKV_PREFILL_TC_PAIR, o.PKV_PREFILL_TC_2SM,
+              o.PKV_PREFILL_MMA):
         prev = o.set_prefill_variant(v)
         try:
             out, err = gpu_prefill(w)
