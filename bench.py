@@ -65,6 +65,7 @@ ATTN_SOURCES = ["paged_kv_cache_272_gb300/csrc/attention.cu",
                 "paged_kv_cache_272_gb300/csrc/attention_mma.cu",
                 "paged_kv_cache_272_gb300/csrc/attention.cuh",
                 "paged_kv_cache_272_gb300/csrc/plan.cuh",
+                "paged_kv_cache_272_gb300/csrc/merge.cuh",
                 "paged_kv_cache_272_gb300/csrc/decode_step.cu",
                 "paged_kv_cache_272_gb300/csrc/kv_rows.cuh",
                 "paged_kv_cache_272_gb300/csrc/tc_common.cuh",

@@ -50,6 +50,7 @@ struct StepIO {
   float k_scale, v_scale;
   const float *k_scales, *v_scales;
   int pair_ctas, write_ctas;
+  int win;          // tokens a write CTA takes at a time
   int table_slots;  // entries of the block -> owner hash table (a power of two)
   int32_t *err;
 };
@@ -89,7 +90,7 @@ __device__ __forceinline__ void put_vec(const StepIO &io, int64_t i, int64_t slo
 }
 
 // Block 0: the attention plan.  Blocks 1 .. pair_ctas: copy pairs, then the writes into
-// their blocks.  The rest: every other new token, step_window tokens at a time.
+// their blocks.  The rest: every other new token, io.win tokens at a time.
 __global__ void __launch_bounds__(kStepThreads) step_prologue_kernel(const AttnArgs a,
                                                                      int head_dim,
                                                                      const StepIO io) {
@@ -192,9 +193,8 @@ __global__ void __launch_bounds__(kStepThreads) step_prologue_kernel(const AttnA
     }
     return;
   }
-  // Write CTAs: windows of about one vector per thread; tokens owned by a pair CTA are
-  // skipped.
-  const int win = step_window(per_tok);
+  // Write CTAs: windows of io.win tokens; tokens owned by a pair CTA are skipped.
+  const int win = io.win;
   for (int t0 = (b - C) * win; t0 < io.num_tokens; t0 += io.write_ctas * win) {
     if (tid < win) {
       const int t = t0 + tid;
@@ -310,8 +310,15 @@ static int step_impl(uint16_t *out, const uint16_t *q, void *k_cache, void *v_ca
   io.err = err_flag;
   const int sms = device_sm_count();
   io.pair_ctas = num_pairs > 0 ? std::min(num_pairs, sms) : 0;
-  const int win = step_window(num_kv_heads * (head_dim / 8));
-  io.write_ctas = num_tokens > 0 ? std::min((num_tokens + win - 1) / win, 4 * sms) : 0;
+  // Tokens per write CTA: about one 16-byte vector per thread; for an E4M3 cache, whose
+  // V stores take four times the sectors, as few as lets every CTA of the prologue start
+  // at once (one per SM: the copy path needs more than 64 registers a thread).
+  io.win = step_window(num_kv_heads * (head_dim / 8));
+  if (kv8 && num_tokens > 0) {
+    const int room = std::max(1, sms - 1 - io.pair_ctas);
+    io.win = std::min(io.win, std::max(1, (num_tokens + room - 1) / room));
+  }
+  io.write_ctas = num_tokens > 0 ? std::min((num_tokens + io.win - 1) / io.win, 4 * sms) : 0;
   int slots = 64;
   while (slots < 4 * num_pairs) slots *= 2;
   io.table_slots = slots;

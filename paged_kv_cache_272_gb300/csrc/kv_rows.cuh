@@ -33,9 +33,16 @@ __device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float scale
 }
 
 // E4M3 cache: K codes [NB][Hkv][16][D], V codes transposed within a block,
-// [NB][Hkv][D][16], so each of the vector's 8 V codes is a separate byte store.  Scales:
+// [NB][Hkv][D][16], so each V code is a byte of its own head-dim row.  Scales:
 // k_scales / v_scales per KV head when non-null (a scale that is not > 0 sets
 // PKV_DEV_BAD_SCALE and the vector is skipped), else k_scale / v_scale.
+// When row_vecs is a power of two up to 32 (head_dim 64, 128, ...), the row_vecs vectors
+// of one (token, KV head) row must be handled by row_vecs consecutive lanes of one warp
+// (lane & (row_vecs - 1) == e), all calling together: they trade V codes through
+// shuffles so that in each of eight rounds lane e stores the code of head-dim row
+// row_vecs * round + e -- the group's stores of a round cover row_vecs consecutive rows,
+// two per 32-byte sector, half the sectors of storing each lane's own eight codes.
+// Other head dims store each lane's own eight codes.
 __device__ __forceinline__ void put_row_vec_e4m3(const uint4 *__restrict__ k_new,
                                                  const uint4 *__restrict__ v_new, int64_t i,
                                                  int64_t slot, int h, int e, int heads,
@@ -55,13 +62,26 @@ __device__ __forceinline__ void put_row_vec_e4m3(const uint4 *__restrict__ k_new
   const int64_t dst = (((slot >> 4) * heads + h) * kBlockSize + (slot & 15)) * row_vecs + e;
   const uint4 kv = k_new[i], vv = v_new[i];
   k_cache[dst] = make_uint2(quant4(kv.x, kv.y, ks), quant4(kv.z, kv.w, ks));
+  // codes of head-dim rows 8e .. 8e + 3 (v0) and 8e + 4 .. 8e + 7 (v1), lowest byte first
   const uint32_t v0 = quant4(vv.x, vv.y, vs), v1 = quant4(vv.z, vv.w, vs);
   const int D = row_vecs * 8;
-  uint8_t *vcol = v_cache + (((slot >> 4) * heads + h) * D + e * 8) * kBlockSize + (slot & 15);
+  uint8_t *vblk = v_cache + ((slot >> 4) * heads + h) * (int64_t)D * kBlockSize + (slot & 15);
+  if ((row_vecs & (row_vecs - 1)) == 0 && row_vecs <= 32) {
+    const int gbase = (int)(threadIdx.x & 31) & ~(row_vecs - 1);
+    const unsigned gmask = (row_vecs == 32 ? 0xffffffffu : ((1u << row_vecs) - 1u)) << gbase;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    vcol[j * kBlockSize] = (uint8_t)(v0 >> (8 * j));
-    vcol[(4 + j) * kBlockSize] = (uint8_t)(v1 >> (8 * j));
+    for (int k = 0; k < 8; ++k) {
+      const int d = row_vecs * k + e;  // the row this lane stores in round k
+      const uint32_t w0 = __shfl_sync(gmask, v0, gbase + (d >> 3));
+      const uint32_t w1 = __shfl_sync(gmask, v1, gbase + (d >> 3));
+      vblk[(int64_t)d * kBlockSize] = (uint8_t)(((d & 4) ? w1 : w0) >> (8 * (d & 3)));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      vblk[(int64_t)(8 * e + j) * kBlockSize] = (uint8_t)(v0 >> (8 * j));
+      vblk[(int64_t)(8 * e + 4 + j) * kBlockSize] = (uint8_t)(v1 >> (8 * j));
+    }
   }
 }
 

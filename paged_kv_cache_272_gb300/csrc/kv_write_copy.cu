@@ -39,7 +39,8 @@ __global__ void kv_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__
 }
 
 // E4M3 write: thread i handles 8 consecutive elements of one (token, KV head) row (see
-// put_row_vec_e4m3).
+// put_row_vec_e4m3: the block size and the grid stride are multiples of row_vecs, so a
+// row's vectors fall on consecutive lanes, and a row's lanes skip or stay together).
 __global__ void kv_write_fp8_kernel(const uint4 *__restrict__ k_new,
                                     const uint4 *__restrict__ v_new,
                                     const int64_t *__restrict__ slots, int64_t total, int row_vecs,
