@@ -55,6 +55,44 @@ def test_write_fp8_all_bf16_patterns():
         vq.zero_()
 
 
+
+@pytest.mark.parametrize("D,Hkv", [(48, 1), (64, 3), (96, 2), (128, 5), (256, 3), (512, 1)])
+def test_write_fp8_head_dims(D, Hkv):
+    """The quantising write at head dims whose row of 16-byte vectors is a power of two up
+    to 32 (64, 128, 256: the lanes of a row trade V codes so each store round covers
+    consecutive head-dim rows) and at the others (48, 96, 512: each lane stores its own
+    codes), with one scale per cache and one per KV head: codes equal the oracle's byte
+    for byte, slots out of order, some skipped (-1)."""
+    o = H.ops()
+    g = torch.Generator().manual_seed(D * 7 + Hkv)
+    NB, T = 9, 40
+    kn = (torch.randn(T, Hkv, D, generator=g) * 3).to(torch.bfloat16)
+    vn = (torch.randn(T, Hkv, D, generator=g) * 2).to(torch.bfloat16)
+    slots = torch.randperm(NB * BS, generator=g)[:T].to(torch.int64)
+    slots[::7] = -1
+    ks_h = (torch.rand(Hkv, generator=g) * 0.05 + 0.005).to(torch.float32)
+    vs_h = (torch.rand(Hkv, generator=g) * 0.05 + 0.005).to(torch.float32)
+    kn16, vn16 = kn.view(torch.int16).numpy().view(np.uint16), vn.view(torch.int16).numpy().view(np.uint16)
+    for per_head in (False, True):
+        kq = torch.zeros(NB, Hkv, BS, D, dtype=torch.uint8, device="cuda")
+        vq = torch.zeros_like(kq)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if per_head:
+            o.paged_kv_write_fp8_per_head(kn.cuda(), vn.cuda(), slots.cuda(), kq, vq, ks_h.cuda(),
+                                          vs_h.cuda(), err_flag=err)
+            ks, vs = ks_h.numpy(), vs_h.numpy()
+        else:
+            o.paged_kv_write_fp8(kn.cuda(), vn.cuda(), slots.cuda(), kq, vq, K_SCALE, V_SCALE,
+                                 err_flag=err)
+            ks, vs = K_SCALE, V_SCALE
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ko = np.zeros((NB, Hkv, BS, D), np.uint8)
+        vo = np.zeros_like(ko)
+        oracle.kv_write_fp8(ko, vo, kn16, vn16, slots.numpy(), ks, vs)
+        assert same_codes(kq.cpu().numpy(), ko), (D, Hkv, per_head, "K")
+        assert same_codes(vq.cpu().numpy(), vo), (D, Hkv, per_head, "V")
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_fp8_config_parity(cfg):
     w = workloads.make_config(cfg, device="cpu" if cfg == 1 else "cuda")
