@@ -408,7 +408,7 @@ def run_ours(args):
     bt = torch.as_tensor(w.block_tables, dtype=torch.int32, device=dev)
     ctx = torch.as_tensor(w.context_lens, dtype=torch.int32, device=dev)
     out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device=dev)
-    # 0: the automatic split (each call's plan picks 512 / 1024 / 2048 tokens)
+    # 0: the automatic split (each call's plan picks 512 ... 4096 tokens)
     P = 0 if args.partition is None else args.partition
     mcl = w.max_context_len
     ws = ops.alloc_workspace(S, Hq, D, mcl, P, device=dev)

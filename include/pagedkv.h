@@ -129,10 +129,12 @@ size_t paged_attention_workspace_size(int num_seqs, int num_q_heads, int head_di
  * computed in fp32 from bf16 inputs and rounded to bf16.  n == 0 gives zeros.
  * Long contexts are split into partitions of partition_size tokens (a multiple of 16)
  * whose partial results are merged with a log-sum-exp reduction.  partition_size <= 0
- * lets each call choose on the device, from context_lens: 512, 1024 or 2048 tokens, the
- * largest not above (sum of context_lens x KV heads x query sub-groups) / (16 x SMs),
- * i.e. about four partitions' worth of work per resident CTA of the partition kernel
- * (large batches get fewer partitions: fewer items and partial results to merge).  The
+ * lets each call choose on the device, from context_lens, the largest candidate size not
+ * above (sum of context_lens x KV heads x query sub-groups) / (d x 4 x SMs), i.e. about
+ * d partitions' worth of work per resident CTA of the partition kernel (large batches
+ * get fewer partitions: fewer items and partial results to merge): on the tensor-core
+ * path with 4 or more query heads per KV head d = 3 and the candidates are 512, 768,
+ * 1024, 1536, 2048, 3072 and 4096 tokens; otherwise d = 4 and 512, 1024 or 2048.  The
  * result depends on the split only through fp32 rounding.
  * max_context_len is a host-side upper bound of context_lens (it sizes the workspace);
  * a context above it sets PKV_DEV_BAD_CONTEXT and that sequence's output is zeros.

@@ -339,6 +339,7 @@ namespace {
 // picks 512, 1024 or 2048 tokens (see attn_plan_cta).
 constexpr int kDefaultPartition = 512;
 constexpr int kAutoPartitionMax = 4 * kDefaultPartition;
+constexpr int kAutoPartitionMaxGqa = 8 * kDefaultPartition;
 
 int max_parts_for(int max_context_len, int part) {
   const int mp = (max_context_len + part - 1) / part;
@@ -390,7 +391,6 @@ int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *
   a.group = num_q_heads / num_kv_heads;
   a.num_blocks = num_blocks;
   a.part_tokens = part;
-  a.part_max = auto_part ? kAutoPartitionMax : part;
   a.slots = device_sm_count() * 4;
   a.max_parts = max_parts;
   a.scale_log2 = (float)((double)scale * (kv8 ? (double)k_scale : 1.0) * 1.4426950408889634);
@@ -423,6 +423,14 @@ int decode_prepare(DecodeCall *d, uint16_t *out, const uint16_t *q, const void *
   if (kv8 && !tma_ok) return PKV_ERR_SHAPE;
   const int width = a.group >= 8 ? 8 : (a.group >= 4 ? 4 : (a.group >= 2 ? 2 : 1));
   a.sub_groups = use_mma ? (a.group + 7) / 8 : (a.group + width - 1) / width;
+  // Automatic size: the grouped (G >= 4) tensor-core path runs best with about three
+  // partitions' worth of records per resident CTA, sizes 512 x {1, 1.5, 2, 3, 4, 6, 8}
+  // (measured on GB300: GQA-8 B=256 1536 tokens, the long-context batch 4096); MHA and
+  // small groups with four, in powers of two up to 2048 (MHA B=64: 1024).
+  const bool gqa_mma = auto_part && use_mma && a.group >= 4;
+  a.part_max = auto_part ? (gqa_mma ? kAutoPartitionMaxGqa : kAutoPartitionMax) : part;
+  a.part_fine = gqa_mma ? 1 : 0;
+  a.part_div = gqa_mma ? 3 : 4;
   d->head_dim = head_dim;
   d->use_mma = use_mma;
   d->width = width;

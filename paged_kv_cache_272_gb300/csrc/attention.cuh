@@ -28,6 +28,8 @@ struct AttnArgs {
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, group, num_blocks;
   int part_tokens;               // smallest partition size in tokens (multiple of 16)
   int part_max;                  // largest the plan may choose (part_tokens: exact size)
+  int part_fine;                 // automatic size in steps of 1.5x / 1.33x (else 2x)
+  int part_div;                  // automatic size: records per resident CTA aimed at
   int slots;                     // about the partition kernel's resident CTAs
   int max_parts;                 // partitions per sequence the workspace holds (of
                                  //   part_tokens tokens)

@@ -7,11 +7,12 @@
 //    workspace, sets PKV_DEV_BAD_CONTEXT and counts as empty) and writes zeros to the
 //    output of every empty sequence (no partition will write it);
 //  * chooses the partition size P: part_tokens, or, when part_max > part_tokens, the
-//    largest part_tokens * 2^k <= part_max not above (total context tokens x work items
-//    per partition) / (4 x the partition kernel's resident CTAs) -- each CTA then meets
-//    four partitions' worth of work or more, so claiming still balances, while a large
-//    batch gets fewer, longer partitions (fewer items, fewer partial results to merge);
-//    P goes to *part_eff for the partition kernel;
+//    largest candidate <= part_max (part_tokens x 2^k, or with part_fine part_tokens x
+//    1, 1.5, 2, 3, 4, 6, 8) not above (total context tokens x work items per partition)
+//    / (part_div x the partition kernel's resident CTAs) -- each CTA then meets part_div
+//    partitions' worth of work or more, so claiming still balances, while a large batch
+//    gets fewer, longer partitions (fewer items, fewer partial results to merge); P goes
+//    to *part_eff for the partition kernel;
 //  * lists the partitions as records {s, t0, t1, np} ordered by size, largest first (a
 //    counting sort over 32 bins of P / 32 tokens, rounded up to whole blocks: every
 //    partition but a sequence's last has P tokens), so that claiming records in order
@@ -88,9 +89,15 @@ __device__ __forceinline__ void attn_plan_cta(const AttnArgs &a, int head_dim) {
     for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kPlanFull, mine, off);
     if (lane == 0 && mine) atomicAdd(&total, mine);
     __syncthreads();
-    const unsigned long long budget =
-        total * (unsigned)(a.num_kv_heads * a.sub_groups) / (4ull * (unsigned)a.slots);
-    while (2 * P <= a.part_max && (unsigned long long)(2 * P) <= budget) P *= 2;
+    const unsigned long long budget = total * (unsigned)(a.num_kv_heads * a.sub_groups) /
+                                      ((unsigned long long)a.part_div * (unsigned)a.slots);
+    // candidates part_tokens x m / 2, m = 2, 3, 4, 6, 8, 12, 16 (fine) or 2, 4, 8, ...
+    for (int k = 1;; ++k) {
+      const int next = a.part_fine ? a.part_tokens / 2 * ((k & 1) ? 3 << (k >> 1) : 2 << (k >> 1))
+                                   : a.part_tokens << k;
+      if (next > a.part_max || (unsigned long long)next > budget) break;
+      P = next;
+    }
   }
   if (tid == 0) *a.part_eff = P;
   const int G8 = (a.num_q_heads + 7) / 8;

@@ -117,7 +117,7 @@ def test_fp8_long_context_sampled():
 
 @pytest.mark.parametrize("cfg", [3, 5])
 def test_fp8_auto_partition(cfg):
-    """partition_size 0 (the plan picks 1024 / 2048-token partitions for these batches):
+    """partition_size 0 (the plan picks 1536 / 4096-token partitions for these batches):
     config 3 in full, config 5 on every long row plus 256 short ones."""
     w = workloads.make_config(cfg, device="cuda")
     out, kq, vq, ko, vo, err = fp8_step(w, partition_size=0)

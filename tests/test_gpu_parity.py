@@ -123,7 +123,7 @@ def test_auto_partition_full(cfg, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_auto_partition_config5_sampled(variant):
-    """The long-context batch under the automatic split (2048-token partitions, 64 per
+    """The long-context batch under the automatic split (4096-token partitions, 32 per
     long sequence): every query head of the long sequences and 256 short rows."""
     w = _make(5)
     out, k, v, err = H.gpu_step(w, variant, partition_size=0)
@@ -136,10 +136,12 @@ def test_auto_partition_config5_sampled(variant):
     H.assert_attention_close(got, ref, "config 5 sample, automatic split")
 
 
-@pytest.mark.parametrize("cfg,want", [(1, 512), (3, 1024), (4, 512), (5, 2048)])
+@pytest.mark.parametrize("cfg,want", [(1, 512), (3, 1536), (4, 512), (5, 4096)])
 def test_auto_partition_choice(cfg, want):
-    """The plan's choice: the largest of 512 / 1024 / 2048 tokens not above (total context
-    x KV heads) / (16 x SMs); the 512-token workspace serves every choice."""
+    """The plan's choice: the largest candidate not above (total context x KV heads x
+    query sub-groups) / (d x 4 x SMs) -- on the tensor-core path with G >= 4 (configs 3 to
+    5) d = 3 and candidates 512 x {1, 1.5, 2, 3, 4, 6, 8}, else (config 1) d = 4 and
+    512 / 1024 / 2048; the 512-token workspace serves every choice."""
     o = H.ops()
     w = _make(cfg)
     d = H.to_cuda(w)
@@ -150,10 +152,14 @@ def test_auto_partition_choice(cfg, want):
                              w.max_context_len, ws, 0)
     torch.cuda.synchronize()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    total = int(w.context_lens.astype(np.int64).sum()) * w.num_kv_heads
-    expect = 512
-    while 2 * expect <= 2048 and 2 * expect <= total // (16 * sms):
-        expect *= 2
+    group = w.num_q_heads // w.num_kv_heads
+    subs = (group + 7) // 8 if group >= 4 else 1
+    total = int(w.context_lens.astype(np.int64).sum()) * w.num_kv_heads * subs
+    if group >= 4:
+        cands, d = [512 * m // 2 for m in (2, 3, 4, 6, 8, 12, 16)], 3
+    else:
+        cands, d = [512, 1024, 2048], 4
+    expect = max([c for c in cands if c <= total // (d * 4 * sms)] or [512])
     assert _chosen_partition(ws) == expect
     if sms == 152:  # the sizes these workloads were tuned on
         assert expect == want
