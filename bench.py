@@ -601,7 +601,7 @@ def run_ours(args):
                if fp8 else {}),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
             "head_dim": D, "block_size": w.block_size,
-            "partition_size": P if P else "auto (512-2048 tokens, chosen per call on the device)",
+            "partition_size": P if P else "auto (512-4096 tokens, chosen per call on the device)",
             **({"partition_chosen": int(ws[4:8].view(torch.int32).item())} if not P else {}),
             "num_blocks": w.num_blocks, "mean_context": float(w.context_lens.mean()),
             "max_context": mcl, "kv_bytes_per_step": kv_bytes,
