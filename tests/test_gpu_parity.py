@@ -85,14 +85,14 @@ def test_group_sizes(G, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_partition_size_invariance(variant):
-    """Split-K merge: partitions of 16, 64, 512 and 8192 tokens all match the oracle and
-    each other."""
+    """Split-K merge: partitions of 16, 48, 64, 512, 768, 1536, 3072 and 8192 tokens (powers
+    of two and not) all match the oracle and each other."""
     ctx = np.random.default_rng(3).integers(1, 3000, size=24)
     w = workloads.build("parts", ctx, 16, 2, 128, seed=90, device="cuda")
     ko, vo = H.oracle_caches(w)
     ref = H.oracle_out(w, ko, vo)
     outs = []
-    for P in (16, 64, 512, 8192):
+    for P in (16, 48, 64, 512, 768, 1536, 3072, 8192):
         out, k, v, err = H.gpu_step(w, variant, partition_size=P)
         assert err == 0
         H.assert_attention_close(out, ref, f"partition {P}")
@@ -164,6 +164,42 @@ def test_auto_partition_choice(cfg, want):
     if sms == 152:  # the sizes these workloads were tuned on
         assert expect == want
 
+
+
+@pytest.mark.parametrize("hq,hkv,nseq,ctx_mean,want", [(64, 16, 40, 2500, 768),
+                                                       (128, 32, 80, 2600, 3072)])
+def test_auto_partition_fine_sizes(hq, hkv, nseq, ctx_mean, want):
+    """Grouped batches whose automatic split lands on the 1.5x-step sizes (768 and 3072
+    tokens on 152 SMs): the plan's choice follows the rule on any SM count, and sampled
+    rows -- every head of the longest sequence and 256 others -- match the oracle."""
+    o = H.ops()
+    rng = np.random.default_rng(hq + nseq)
+    ctx = rng.integers(ctx_mean - 400, ctx_mean + 400, size=nseq, endpoint=True)
+    w = workloads.build(f"fine-{want}", ctx, hq, hkv, 128, seed=hkv + 7, device="cuda")
+    d = H.to_cuda(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if d["slots"].numel():
+        o.paged_kv_write(d["k_new"], d["v_new"], d["slots"], d["k"], d["v"], err_flag=err)
+    S, Hq, D = d["q"].shape
+    ws = o.alloc_workspace(S, Hq, D, w.max_context_len, 0)
+    out = torch.empty(S, Hq, D, dtype=torch.bfloat16, device="cuda")
+    o.paged_attention_decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale,
+                             w.max_context_len, ws, 0, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    total = int(w.context_lens.astype(np.int64).sum()) * hkv
+    cands = [512 * m // 2 for m in (2, 3, 4, 6, 8, 12, 16)]
+    expect = max([c for c in cands if c <= total // (3 * 4 * sms)] or [512])
+    assert _chosen_partition(ws) == expect
+    if sms == 152:
+        assert expect == want
+    ko, vo = H.oracle_caches(w)
+    sel = H.wide_pairs(w, n_short=256)
+    ref = H.oracle_out(w, ko, vo, sel=sel)
+    got = out[torch.as_tensor(sel[:, 0].astype(np.int64), device="cuda"),
+              torch.as_tensor(sel[:, 1].astype(np.int64), device="cuda")]
+    H.assert_attention_close(got, ref, f"automatic split {expect}")
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_large_magnitude_scores(variant):
