@@ -130,7 +130,7 @@ def test_fp8_auto_partition(cfg):
 
 
 @pytest.mark.parametrize("G", [1, 2, 3, 8, 16])
-@pytest.mark.parametrize("P", [64, 512, 8192])
+@pytest.mark.parametrize("P", [48, 64, 512, 768, 8192])
 def test_fp8_groups_and_partitions(G, P):
     ctx = [1, 2, 15, 16, 17, 33, 511, 512, 513, 1500, 2999]
     w = workloads.build("fp8-edges", ctx, 2 * G, 2, 128, seed=60 + G, device="cuda")
