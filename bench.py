@@ -13,7 +13,7 @@ and the output copied back inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
                     [--variant auto|fma|mma] [--impl ours|reference]
-    python bench.py --path prefill [--config 1..3]
+    python bench.py --path prefill [--config 1..4]
 
 With ``--path prefill`` one step = paged KV write of every sequence's new chunk +
 chunked-prefill attention (causal, tensor cores); ``value`` is attention TFLOP/s of the
@@ -1195,7 +1195,7 @@ def main():
                     help="decode step (default), chunked-prefill step, or a whole "
                          "continuous-batching serving run")
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
-                    help="workload number (decode 1..5, default 5; prefill 1..3, default 2; "
+                    help="workload number (decode 1..5, default 5; prefill 1..4, default 2; "
                          "serve 1..2, default 2)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -1227,7 +1227,7 @@ def main():
         (run_serve_reference if args.impl == "reference" else run_serve)(args)
     elif args.path == "prefill":
         if args.config not in workloads.PREFILL_CONFIG_NAMES:
-            ap.error("--path prefill takes --config 1..3")
+            ap.error("--path prefill takes --config 1..4")
         (run_prefill_reference if args.impl == "reference" else run_prefill)(args)
     elif args.impl == "reference":
         run_reference(args)

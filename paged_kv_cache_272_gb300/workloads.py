@@ -345,6 +345,7 @@ PREFILL_CONFIG_NAMES = {
     1: "prefill-tiny-gqa2-d64",
     2: "chunked-prefill-llama3-70b-gqa8",
     3: "chunked-prefill-llama2-7b-mha",
+    4: "chunked-prefill-gqa4-d64",
 }
 
 
@@ -358,6 +359,8 @@ def make_prefill_config(n: int, device="cpu", seed: int | None = None, **kw) -> 
        U{0..3584} tokens (a scheduler's per-step token budget of 8192).
     3: Llama-2-7B shapes (32 heads, MHA, head_dim 128): 8 sequences, 512-token chunks
        after U{0..3584} cached tokens.
+    4: head_dim 64 at scale (32 query heads, 8 KV heads): 16 sequences, 512-token
+       chunks after U{0..3584} cached tokens.
     """
     seed = 2000 + n if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
@@ -365,12 +368,12 @@ def make_prefill_config(n: int, device="cpu", seed: int | None = None, **kw) -> 
     if n == 1:
         ctx, L = [1, 5, 40, 70, 100], [1, 5, 17, 2, 64]
         return build_prefill(name, ctx, L, 4, 2, 64, seed, device, **kw)
-    if n in (2, 3):
-        S = 16 if n == 2 else 8
+    if n in (2, 3, 4):
+        S = 8 if n == 3 else 16
         prior = rng.integers(0, 3584, size=S, endpoint=True)
         L = np.full(S, 512)
-        Hq, Hkv = (64, 8) if n == 2 else (32, 32)
-        return build_prefill(name, prior + L, L, Hq, Hkv, 128, seed, device, **kw)
+        Hq, Hkv, D = {2: (64, 8, 128), 3: (32, 32, 128), 4: (32, 8, 64)}[n]
+        return build_prefill(name, prior + L, L, Hq, Hkv, D, seed, device, **kw)
     raise ValueError(n)
 
 

@@ -92,7 +92,7 @@ def test_prefill_tiny_config():
     H.assert_attention_close(out, oracle_prefill(w), "prefill config 1")
 
 
-@pytest.mark.parametrize("cfg", [2, 3])
+@pytest.mark.parametrize("cfg", [2, 3, 4])
 def test_prefill_full_size_sampled(cfg, variant):
     w = workloads.make_prefill_config(cfg, device="cuda")
     out, err = gpu_prefill(w)
